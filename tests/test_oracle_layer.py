@@ -1,0 +1,256 @@
+"""Pins of the layer oracle: brute force on tiny inputs, finite differences, invariants
+and special cases (no GPU)."""
+import math
+
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+from oracle import moe
+from oracle.numerics import silu
+
+
+def small_problem(rng, T=12, H=16, I=8, E=5, k=2, shared=False, bias=False):
+    x = rng.normal(0, 1, (T, H))
+    Wr = rng.normal(0, 0.3, (H, E))
+    b = rng.normal(0, 0.5, E) if bias else None
+    Wu = rng.normal(0, 0.3, (E, H, I))
+    Wg = rng.normal(0, 0.3, (E, H, I))
+    Wd = rng.normal(0, 0.3, (E, I, H))
+    sh = None
+    if shared:
+        sh = (rng.normal(0, 0.3, (H, 6)), rng.normal(0, 0.3, (H, 6)), rng.normal(0, 0.3, (6, H)))
+    dY = rng.normal(0, 1, (T, H))
+    return x, Wr, b, Wu, Wg, Wd, sh, dY
+
+
+# ----------------------------------------------------------------------------- routing
+def test_route_matches_python_brute_force(rng):
+    x, Wr, b, *_ = small_problem(rng, T=20, E=7, k=3, bias=True)
+    r = moe.route(x, Wr, 3, b)
+    for t in range(20):
+        logits = [math.fsum(x[t, h] * Wr[h, e] for h in range(x.shape[1])) + b[e]
+                  for e in range(7)]
+        m = max(logits)
+        p = [math.exp(l - m) for l in logits]
+        z = math.fsum(p)
+        p = [v / z for v in p]
+        chosen = sorted(range(7), key=lambda e: (-logits[e], e))[:3]
+        assert list(r.idx[t]) == chosen
+        zS = math.fsum(p[e] for e in chosen)
+        assert np.allclose(r.gates[t], [p[e] / zS for e in chosen], rtol=1e-13, atol=0)
+
+
+def test_route_ties_go_to_lower_expert():
+    x = np.ones((1, 2))
+    Wr = np.array([[1.0, 2.0, 2.0, 0.5, 2.0], [0.0, 0.0, 0.0, 0.0, 0.0]])
+    r = moe.route(x, Wr, 3)
+    assert list(r.idx[0]) == [1, 2, 4]
+    assert np.allclose(r.gates[0], 1 / 3)
+
+
+def test_route_invariants(rng):
+    cfg = mi.CONFIGS["tiny"]
+    inp = mi.make_inputs(cfg)
+    r = moe.route(mi.to_f64(inp["x"]), mi.to_f64(inp["Wr"]), cfg.k)
+    assert np.allclose(r.gates.sum(1), 1.0, atol=1e-14)
+    assert np.all(np.diff(r.gates, axis=1) <= 0)          # slot order: descending gate
+    assert np.all(r.gates > 0)
+    assert np.all([len(set(row)) == cfg.k for row in r.idx])
+
+
+# ----------------------------------------------------------------------------- schedule
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (7, 3, 2), (64, 8, 2), (33, 40, 6)])
+def test_plan_matches_loops_and_invariants(rng, T, E, k):
+    idx = np.stack([rng.choice(E, k, replace=k > E) for _ in range(T)])
+    p = moe.plan(idx, E)
+    q = moe.plan_loops(idx, E)
+    for f in ("counts", "offsets", "table", "inv"):
+        assert np.array_equal(getattr(p, f), getattr(q, f)), f
+    R = T * k
+    assert p.counts.sum() == R and p.offsets[-1] == R
+    assert np.all(np.diff(p.offsets) >= 0)
+    # every (t, j) appears exactly once; each token exactly k times
+    pairs = {tuple(v) for v in p.table}
+    assert len(pairs) == R
+    assert np.all(np.bincount(p.table[:, 0], minlength=T) == k)
+    # inverse of the table
+    assert np.array_equal(p.inv[p.table[:, 0], p.table[:, 1]], np.arange(R))
+    # rows of one expert hold that expert, in ascending (t, j)
+    for e in range(E):
+        seg = p.table[p.offsets[e]:p.offsets[e + 1]]
+        assert np.all(idx[seg[:, 0], seg[:, 1]] == e)
+        key = seg[:, 0] * k + seg[:, 1]
+        assert np.all(np.diff(key) > 0)
+
+
+def test_plan_duplicate_expert_in_one_token():
+    idx = np.array([[2, 2, 0], [0, 2, 2]])
+    p = moe.plan(idx, 3)
+    assert list(p.counts) == [2, 0, 4]
+    assert p.table.tolist() == [[0, 2], [1, 0], [0, 0], [0, 1], [1, 1], [1, 2]]
+
+
+def test_zipf_counts_of_the_ep64_slice():
+    c = mi.zipf_counts(16384, 6, 1.2)
+    assert sum(c) == 16384
+    w = np.arange(1, 7) ** -1.2
+    assert np.all(np.abs(np.array(c) - 16384 * w / w.sum()) < 1.0)
+
+
+# ----------------------------------------------------------------------------- forward
+def test_forward_matches_per_token_brute_force(rng):
+    x, Wr, b, Wu, Wg, Wd, _, _ = small_problem(rng, T=16, E=6, k=3)
+    r = moe.route(x, Wr, 3)
+    y, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd)
+    for t in range(16):
+        yt = moe.token_forward_bruteforce(x[t], r.idx[t], r.gates[t], Wu, Wg, Wd)
+        assert np.allclose(y[t], yt, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_identity_experts_return_input(rng):
+    """combine(dispatch(x)) = sum_j g_tj x_t = x_t when every expert is the identity."""
+    x, Wr, _, Wu, Wg, Wd, _, _ = small_problem(rng, T=30, E=5, k=3)
+    r = moe.route(x, Wr, 3)
+    y, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, expert_fn=lambda e, X: X)
+    assert np.allclose(y, x, rtol=0, atol=1e-14)
+
+
+def test_forward_single_expert_is_dense_swiglu(rng):
+    x, _, _, Wu, Wg, Wd, _, _ = small_problem(rng, T=9, E=1, k=1)
+    idx = np.zeros((9, 1), np.int64)
+    g = np.ones((9, 1))
+    y, _ = moe.forward(x, idx, g, Wu, Wg, Wd)
+    u = np.einsum("th,hi->ti", x, Wu[0])
+    v = np.einsum("th,hi->ti", x, Wg[0])
+    dense = np.einsum("ti,ih->th", v / (1 + np.exp(-v)) * u, Wd[0])
+    assert np.allclose(y, dense, rtol=1e-12, atol=1e-13)
+
+
+def test_forward_is_linear_in_gates(rng):
+    x, Wr, _, Wu, Wg, Wd, _, _ = small_problem(rng, T=10, E=4, k=2)
+    r = moe.route(x, Wr, 2)
+    y1, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd)
+    y2, _ = moe.forward(x, r.idx, 2 * r.gates, Wu, Wg, Wd)
+    assert np.allclose(y2, 2 * y1, rtol=1e-13, atol=1e-14)
+
+
+def test_shared_expert_adds_dense_ffn(rng):
+    x, Wr, _, Wu, Wg, Wd, sh, _ = small_problem(rng, T=8, E=3, k=1, shared=True)
+    r = moe.route(x, Wr, 1)
+    y0, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd)
+    y1, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh)
+    for t in range(8):
+        u, v = x[t] @ sh[0], x[t] @ sh[1]
+        assert np.allclose(y1[t] - y0[t], (silu(v) * u) @ sh[2], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("mode,tol", [("bf16", 1e-2), ("mxfp8", 1.5e-1)])
+def test_rounded_modes_stay_near_fp64(mode, tol):
+    """The rounding model only perturbs: rms(rounded - fp64) / rms(fp64) stays near the
+    formats' unit roundoff (2^-9 for bf16, about 2^-4 per MXFP8 element)."""
+    cfg = mi.CONFIGS["tiny"]
+    inp = mi.make_inputs(cfg)
+    x, Wr = mi.to_f64(inp["x"]), mi.to_f64(inp["Wr"])
+    W = [mi.to_f64(inp[n]) for n in ("W_up", "W_gate", "W_down")]
+    r = moe.route(x, Wr, cfg.k)
+    y0, s0 = moe.forward(x, r.idx, r.gates, *W)
+    y1, s1 = moe.forward(x, r.idx, r.gates, *W, precision=mode)
+    def rel(a, b):
+        return np.sqrt(((a - b) ** 2).mean()) / np.sqrt((a ** 2).mean())
+
+    assert rel(y0, y1) < tol
+    dY = mi.to_f64(inp["dY"])
+    g0 = moe.backward(x, r.idx, r.gates, *W, s0, dY, Wr=Wr)
+    g1 = moe.backward(x, r.idx, r.gates, *W, s1, dY, precision=mode, Wr=Wr)
+    for f in ("dX", "dW_up", "dW_gate", "dW_down", "dgates", "dWr"):
+        assert rel(getattr(g0, f), getattr(g1, f)) < tol, f
+
+
+# ----------------------------------------------------------------------------- backward
+def _fd_check(f, arr, grad, rng, n=12, eps=1e-6, rtol=1e-6):
+    flat = arr.reshape(-1)
+    gflat = grad.reshape(-1)
+    picks = rng.choice(flat.size, size=min(n, flat.size), replace=False)
+    scale = max(np.abs(gflat).max(), 1e-30)
+    for i in picks:
+        old = flat[i]
+        flat[i] = old + eps
+        lp = f()
+        flat[i] = old - eps
+        lm = f()
+        flat[i] = old
+        fd = (lp - lm) / (2 * eps)
+        assert abs(fd - gflat[i]) <= rtol * scale + 1e-9 * abs(fd), (i, fd, gflat[i])
+
+
+@pytest.mark.parametrize("shared,bias", [(False, False), (True, True)])
+def test_backward_matches_finite_differences(rng, shared, bias):
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=10, H=12, I=6, E=4, k=2,
+                                                 shared=shared, bias=bias)
+    r = moe.route(x, Wr, 2, b)
+    S = r.idx.copy()
+    y, saved = moe.forward(x, S, r.gates, Wu, Wg, Wd, shared=sh)
+    g = moe.backward(x, S, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, Wr=Wr)
+
+    def L():
+        return moe.layer_loss(x, Wr, b, S, Wu, Wg, Wd, dY, shared=sh)
+
+    _fd_check(L, x, g.dX, rng)
+    _fd_check(L, Wu, g.dW_up, rng)
+    _fd_check(L, Wg, g.dW_gate, rng)
+    _fd_check(L, Wd, g.dW_down, rng)
+    _fd_check(L, Wr, g.dWr, rng)
+    if shared:
+        for arr, gr in zip(sh, (g.dWs_up, g.dWs_gate, g.dWs_down)):
+            _fd_check(L, arr, gr, rng)
+
+
+def test_dgates_match_finite_differences(rng):
+    x, Wr, _, Wu, Wg, Wd, _, dY = small_problem(rng, T=8, E=4, k=3)
+    r = moe.route(x, Wr, 3)
+    gates = r.gates.copy()
+    y, saved = moe.forward(x, r.idx, gates, Wu, Wg, Wd)
+    g = moe.backward(x, r.idx, gates, Wu, Wg, Wd, saved, dY)
+
+    def L():
+        yy, _ = moe.forward(x, r.idx, gates, Wu, Wg, Wd)
+        return float((yy * dY).sum())
+
+    _fd_check(L, gates, g.dgates, rng, n=24)
+
+
+def test_router_backward_invariants(rng):
+    x, Wr, _, Wu, Wg, Wd, _, dY = small_problem(rng, T=15, E=6, k=3)
+    r = moe.route(x, Wr, 3)
+    dg = rng.normal(0, 1, r.gates.shape)
+    dl, dWr, dx = moe.router_backward(x, Wr, r.idx, r.gates, dg)
+    # softmax over S is shift invariant: the logit gradient sums to zero per token
+    assert np.allclose(dl.sum(1), 0, atol=1e-14)
+    # zero outside the selected set
+    mask = np.zeros_like(dl, bool)
+    np.put_along_axis(mask, r.idx, True, axis=1)
+    assert np.all(dl[~mask] == 0)
+    # dg equal on every slot of a token is a pure shift: no logit gradient
+    dl2, _, _ = moe.router_backward(x, Wr, r.idx, r.gates, np.ones_like(dg) * 3.0)
+    assert np.allclose(dl2, 0, atol=1e-14)
+
+
+def test_backward_linear_in_dY(rng):
+    x, Wr, _, Wu, Wg, Wd, _, dY = small_problem(rng, T=10, E=4, k=2)
+    r = moe.route(x, Wr, 2)
+    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd)
+    g1 = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, Wr=Wr)
+    g2 = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, 2 * dY, Wr=Wr)
+    for f in ("dX", "dW_up", "dW_gate", "dW_down", "dgates", "dWr"):
+        assert np.allclose(getattr(g2, f), 2 * getattr(g1, f), rtol=1e-12, atol=1e-14)
+
+
+def test_empty_experts_get_zero_gradients(rng):
+    x, _, _, Wu, Wg, Wd, _, dY = small_problem(rng, T=6, E=5, k=1)
+    idx = np.zeros((6, 1), np.int64)           # only expert 0 is used
+    gates = np.ones((6, 1))
+    _, saved = moe.forward(x, idx, gates, Wu, Wg, Wd)
+    g = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY)
+    assert np.all(g.dW_up[1:] == 0) and np.all(g.dW_down[1:] == 0)
+    assert np.abs(g.dW_up[0]).max() > 0
