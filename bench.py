@@ -1,0 +1,421 @@
+"""Benchmark: MoE SwiGLU layer forward + backward tokens/s on GB300 (one step = plan,
+forward and backward of one batch), as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Default workload: the Kimi-2.5-shaped layer (T=8192, H=7168, I=2048, E=384, top-8, one
+BF16 shared expert with I=2048), BF16. Inputs are seeded synthetic tensors resident in HBM;
+the expert weights alone are 34 GB, far larger than the 129 MB L2, so no flush is needed
+between steps. Under torchrun each rank runs an independent replica on its own batch
+(weak scaling, no collective on the data path).
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload on
+the host cores (router for every token, a few experts and a slice of the shared expert,
+extrapolated to the whole layer).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/sec fwd & bwd (BF16, MXFP8) on 1 GB300; grouped-GEMM % of TC peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="kimi_8192")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-experts", type=int, default=4)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+def workload_config(name):
+    import moe_inputs as mi
+    return mi.CONFIGS[name]
+
+
+def algorithmic(cfg):
+    """Algorithmic FLOPs and bytes of one step (plan + forward + backward).
+
+    FLOPs: per routed row 6*H*I forward (up, gate, down), 12*H*I backward (dX, dW);
+    shared expert the same per token; router 2*H*E per token forward, backward dWr and
+    dX router path 4*H*k per token. Bytes: compulsory HBM traffic (inputs, weights read
+    once per pass, outputs, weight gradients written once)."""
+    T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
+    R = T * k
+    f_fwd = 6.0 * H * I * R + 6.0 * H * Is * T + 2.0 * H * E * T
+    f_bwd = 12.0 * H * I * R + 12.0 * H * Is * T + 4.0 * H * k * T
+    w_bytes = 2.0 * 3 * H * I * E + 2.0 * 3 * H * Is
+    b_fwd = w_bytes + 2.0 * T * H * 2 + 4.0 * H * E
+    b_bwd = 2 * w_bytes + 2.0 * T * H * 3 + 4.0 * H * E * 2
+    return f_fwd, f_bwd, b_fwd, b_bwd
+
+
+# per-kernel algorithmic work, for the roofline of the dominant kernel
+def kernel_work(cfg, name, counts=None):
+    T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
+    R = T * k
+    rows = R
+    tbl = {
+        "gemm_fwd_upgate_swiglu": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + rows * H + 3 * rows * I)),
+        "gemm_fwd_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I + rows * H)),
+        "gemm_bwd_dh_swiglu": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * H + 5 * rows * I)),
+        "gemm_bwd_dx": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + 2 * rows * I + rows * H)),
+        "gemm_bwd_dw_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I + rows * H)),
+        "gemm_bwd_dw_upgate": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + rows * H + 2 * rows * I)),
+    }
+    return tbl.get(name)
+
+
+def kernels_per_step(cfg):
+    n_plan = 4 if cfg.router else 3
+    n_fwd = 4 + (2 if cfg.shared_I else 0)
+    n_bwd = 9 + (4 if cfg.shared_I else 0) + (2 if cfg.router else 0)
+    return n_plan + n_fwd + n_bwd
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import moe_inputs as mi
+    from grouped_gemm_built_gb300 import mok
+    from grouped_gemm_built_gb300.layer import MoELayer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = workload_config(args.workload)
+    inp = mi.make_inputs(cfg, seed=1000 + rank, device="cuda", with_dy=True)
+    L = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, shared_I=cfg.shared_I, router=cfg.router,
+                 macrobatches=cfg.macrobatches, ring_bytes=cfg.ring_bytes,
+                 precision=cfg.precision)
+    w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
+                  inp["Ws_down"])
+    grads = L.alloc_grads()
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    Wr = inp["Wr"]
+
+    def step():
+        if cfg.router:
+            L.plan(x=inp["x"], Wr=Wr, bias=inp["bias"])
+        else:
+            L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
+        L.forward(inp["x"], w, y)
+        L.backward(inp["x"], Wr if cfg.router else None, w, inp["dY"], grads)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    barrier()
+    if L.status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    stream = torch.cuda.current_stream()
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    mok.mok_profile_enable(L.ctx, True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    prof, launches = mok.mok_profile_report(L.ctx)
+    mok.mok_profile_enable(L.ctx, False)
+    clocks = clk.stop()
+    if L.status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * cfg.T * args.steps / (ms / 1e3)
+
+    # ------------------------------------------------------------ e2e (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.empty_like(inp["x"], device="cpu").pin_memory()
+        hdy = torch.empty_like(inp["dY"], device="cpu").pin_memory()
+        hx.copy_(inp["x"])
+        hdy.copy_(inp["dY"])
+        hy = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+        hdx = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+        dx_dev = torch.empty_like(inp["x"])
+        dy_dev = torch.empty_like(inp["dY"])
+
+        def e2e_step():
+            dx_dev.copy_(hx, non_blocking=True)
+            dy_dev.copy_(hdy, non_blocking=True)
+            if cfg.router:
+                L.plan(x=dx_dev, Wr=Wr, bias=inp["bias"])
+            else:
+                L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
+            L.forward(dx_dev, w, y)
+            L.backward(dx_dev, Wr if cfg.router else None, w, dy_dev, grads)
+            hy.copy_(y, non_blocking=True)
+            hdx.copy_(grads["dX"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        k_e2e = max(2, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ms_e2e = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": world * cfg.T * k_e2e / (ms_e2e / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": hx.numel() * 2 + hdy.numel() * 2,
+               "d2h_bytes_per_step": hy.numel() * 2 + hdx.numel() * 2,
+               "steps": k_e2e}
+
+    # ------------------------------------------------------------ roofline
+    pk = peaks()
+    gemm = {n: v for n, v in prof.items() if n.startswith("gemm_")}
+    top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
+    roofline = None
+    per_kernel = {n: {"launches": c, "ms_per_launch": t / c, "share": None}
+                  for n, (c, t) in prof.items()}
+    tot = sum(t for _, t in prof.values()) or 1.0
+    for n, (c, t) in prof.items():
+        per_kernel[n]["share"] = round(t / tot, 4)
+    if top is not None:
+        name, (cnt, tms) = top
+        flops, byts = kernel_work(cfg, name)
+        dur = tms / cnt / 1e3
+        ai = flops / byts
+        ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+        if ai < ridge:
+            achieved = byts / dur / 1e9
+            roofline = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
+                        "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                        "peak_source": pk["source"] + " (copy bandwidth)"}
+        else:
+            achieved = flops / dur / 1e12
+            roofline = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1),
+                        "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                        "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
+                        "traffic": None, "peak_source": pk["source"] + " (sustained bf16)"}
+    f_fwd, f_bwd, b_fwd, b_bwd = algorithmic(cfg)
+    t_roof = max((f_fwd + f_bwd) / (pk["bf16_tflops_sustained"] * 1e12),
+                 (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
+    layer_roofline = {"ms_per_step_bound": round(t_roof * 1e3, 3),
+                      "frac": round(t_roof * 1e3 / ms_step, 4),
+                      "bound": "hbm" if (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9) >
+                      (f_fwd + f_bwd) / (pk["bf16_tflops_sustained"] * 1e12) else "tensor"}
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(cfg, args.cpu_sample_experts)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if cfg.precision == "bf16" else "mxfp8", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} "
+                                   f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} fwd+bwd",
+                       "step": "plan + forward + backward", "T": cfg.T, "H": cfg.H, "I": cfg.I,
+                       "E": cfg.E, "k": cfg.k, "shared_I": cfg.shared_I,
+                       "precision": cfg.precision,
+                       "l2": "inputs larger than L2 (expert weights 34 GB), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "clocks": clocks, "gpu_launches": launches,
+            "roofline": roofline, "layer_roofline": layer_roofline,
+            "kernels": per_kernel, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def cpu_baseline(cfg, n_experts=4, seed=0):
+    """Time the fp64 oracle on a bounded sample of the workload and extrapolate to the
+    whole layer: router over all T tokens, n_experts routed experts (fwd + bwd over the
+    rows the router sends them), the shared expert over T/64 tokens."""
+    import numpy as np
+
+    from oracle import moe
+
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
+    cores = os.cpu_count()
+    x = rng.standard_normal((T, H)).astype(np.float32).astype(np.float64)
+    t0 = time.perf_counter()
+    if cfg.router:
+        Wr = rng.normal(0, cfg.wr_std, (H, E))
+        r = moe.route(x, Wr, k)
+        idx, gates = r.idx, r.gates
+    else:
+        idx = rng.integers(0, E, (T, k))
+        gates = np.full((T, k), 1.0 / k)
+    pl = moe.plan(idx, E)
+    t_route = time.perf_counter() - t0
+    t_exp = 0.0
+    rows_done = 0
+    for e in range(min(n_experts, E)):
+        r0, r1 = pl.offsets[e], pl.offsets[e + 1]
+        n = r1 - r0
+        if n == 0:
+            continue
+        sel = pl.table[r0:r1]
+        Wu = rng.normal(0, cfg.w_std, (1, H, I))
+        Wg = rng.normal(0, cfg.w_std, (1, H, I))
+        Wd = rng.normal(0, cfg.w_std, (1, I, H))
+        xs = x[sel[:, 0]]
+        sub_idx = np.zeros((n, 1), np.int64)
+        sub_g = gates[sel[:, 0], sel[:, 1]][:, None]
+        dY = rng.standard_normal((n, H))
+        t1 = time.perf_counter()
+        y, saved = moe.forward(xs, sub_idx, sub_g, Wu, Wg, Wd, precision="bf16")
+        moe.backward(xs, sub_idx, sub_g, Wu, Wg, Wd, saved, dY, precision="bf16")
+        t_exp += time.perf_counter() - t1
+        rows_done += n
+    t_shared = 0.0
+    Ts = max(1, T // 64)
+    if Is:
+        sh = (rng.normal(0, cfg.w_std, (H, Is)), rng.normal(0, cfg.w_std, (H, Is)),
+              rng.normal(0, cfg.w_std, (Is, H)))
+        xs = x[:Ts]
+        dY = rng.standard_normal((Ts, H))
+        t1 = time.perf_counter()
+        O, ss = moe.shared_forward(xs, *sh, "bf16")
+        moe.shared_backward(xs, *sh, ss, dY, "bf16")
+        t_shared = time.perf_counter() - t1
+    total = t_route + (t_exp / max(rows_done, 1)) * T * k + t_shared * (T / Ts)
+    return {"value": round(T / total, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"router+schedule over all {T} tokens; {min(n_experts, E)} of {E} routed "
+                      f"experts fwd+bwd ({rows_done} rows) scaled to {T * k} rows; shared "
+                      f"expert over {Ts} tokens scaled to {T}; fp64 NumPy, bf16 rounding model",
+            "seconds_measured": round(t_route + t_exp + t_shared, 2),
+            "seconds_extrapolated": round(total, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = workload_config(args.workload)
+    cpu = cpu_baseline(cfg, args.cpu_sample_experts)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * cfg.T / cpu["value"], 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} "
+                               f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} fwd+bwd",
+                   "step": "plan + forward + backward (CPU oracle, bounded sample)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": cpu["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,583 @@
+// Host side of the C ABI declared in include/mok.h: argument checks, buffer layouts and
+// the launch sequences of mok_plan, mok_moe_fwd and mok_moe_bwd.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/mok_profile.h"
+
+#include "mok_internal.h"
+
+#define MOK_CHECK_CUDA(expr)                    \
+  do {                                          \
+    cudaError_t _e = (expr);                    \
+    if (_e != cudaSuccess) return MOK_ERR_CUDA; \
+  } while (0)
+
+struct mok_ctx_s {
+  mok_dims dims;
+  mok::Dims d;
+  mok_precision precision;
+  int device;
+  int num_sms;
+  // optional per-launch timing (mok_profile.h)
+  bool profile = false;
+  struct Rec {
+    const char* name;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t pool_used = 0;
+  cudaEvent_t ev() {
+    if (pool_used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[pool_used++];
+  }
+  ~mok_ctx_s() {
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+namespace {
+// Run a launcher; when profiling, bracket it with two events on the launch stream.
+template <class F>
+cudaError_t prof_launch(mok_ctx_s* c, const char* name, cudaStream_t s, F&& f) {
+  if (!c->profile) return f();
+  cudaEvent_t a = c->ev(), b = c->ev();
+  if (a) cudaEventRecord(a, s);
+  cudaError_t e = f();
+  if (b) cudaEventRecord(b, s);
+  if (a && b) c->recs.push_back({name, a, b});
+  return e;
+}
+}  // namespace
+#define MOK_LAUNCH(name, expr) MOK_CHECK_CUDA(prof_launch(ctx, name, s, [&]() { return (expr); }))
+
+namespace mok {
+
+Dims make_dims(const mok_dims& x) {
+  Dims d;
+  d.T = x.T;
+  d.H = x.H;
+  d.I = x.I;
+  d.E = x.E;
+  d.k = x.k;
+  d.Is = x.shared_I;
+  d.router = x.router;
+  d.R = x.T * x.k;
+  d.P_max = (int)align_up((size_t)d.R + (size_t)d.E * (kRowPad - 1), kRowPad);
+  d.mt_max = d.P_max / kRowPad;
+  d.nblk = (x.T + kTokBlock - 1) / kTokBlock;
+  return d;
+}
+
+namespace {
+struct Bump {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  }
+};
+}  // namespace
+
+AuxLayout aux_layout(const Dims& d) {
+  Bump b;
+  AuxLayout L;
+  L.status = b.take(sizeof(uint32_t));
+  L.poff = b.take(sizeof(int32_t) * (d.E + 1));
+  L.tile_expert = b.take(sizeof(int32_t) * d.mt_max);
+  L.num_mtiles = b.take(sizeof(int32_t));
+  L.total = b.off;
+  return L;
+}
+
+PlanWs plan_ws(const Dims& d) {
+  Bump b;
+  PlanWs L;
+  L.logits = b.take(sizeof(float) * (size_t)d.T * d.E);
+  L.hist = b.take(sizeof(int32_t) * (size_t)d.nblk * d.E);
+  L.lrank = b.take(sizeof(int32_t) * (size_t)d.R);
+  L.total = b.off;
+  return L;
+}
+
+FwdWs fwd_ws(const Dims& d) {
+  Bump b;
+  FwdWs L;
+  const size_t P = d.P_max;
+  L.xg = b.take(2 * P * d.H);
+  L.h = b.take(2 * P * d.I);
+  L.o = b.take(2 * P * d.H);
+  L.hs = b.take(2 * (size_t)d.T * d.Is);
+  L.os = b.take(2 * (size_t)d.T * d.H);
+  L.total = b.off;
+  return L;
+}
+
+BwdWs bwd_ws(const Dims& d) {
+  Bump b;
+  BwdWs L;
+  const size_t P = d.P_max;
+  L.dyg = b.take(2 * P * d.H);
+  L.xg = b.take(2 * P * d.H);
+  L.du = b.take(2 * P * d.I);
+  L.dv = b.take(2 * P * d.I);
+  L.hg = b.take(2 * P * d.I);
+  L.dxg = b.take(2 * P * d.H);
+  L.dgp = b.take(sizeof(float) * P * gemm_dh_parts(d.I));
+  L.dl = b.take(sizeof(float) * (size_t)d.R);
+  L.dus = b.take(2 * (size_t)d.T * d.Is);
+  L.dvs = b.take(2 * (size_t)d.T * d.Is);
+  L.hsg = b.take(2 * (size_t)d.T * d.Is);
+  L.dxs = b.take(2 * (size_t)d.T * d.H + sizeof(float) * (size_t)d.E * d.H);  // + Wr^T
+  L.total = b.off;
+  return L;
+}
+
+SavedLayout saved_layout(const Dims& d) {
+  Bump b;
+  SavedLayout L;
+  const size_t P = d.P_max;
+  L.u = b.take(2 * P * d.I);
+  L.v = b.take(2 * P * d.I);
+  L.us = b.take(2 * (size_t)d.T * d.Is);
+  L.vs = b.take(2 * (size_t)d.T * d.Is);
+  L.total = b.off;
+  return L;
+}
+
+}  // namespace mok
+
+using namespace mok;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mok_status check_sched(const Dims& d, const mok_sched* s) {
+  if (!s || !s->topk_idx || !s->gates || !s->counts || !s->offsets || !s->table || !s->inv)
+    return MOK_ERR_INVALID_ARG;
+  if (!s->aux || !aligned(s->aux, 256)) return MOK_ERR_WORKSPACE;
+  (void)d;
+  return MOK_OK;
+}
+
+char* at(void* base, size_t off) { return static_cast<char*>(base) + off; }
+
+const char* gemm_name(const GemmCall& c) {
+  static const char* routed[] = {"gemm_fwd_upgate_swiglu", "gemm_fwd_down", "gemm_bwd_dh_swiglu",
+                                 "gemm_bwd_dx", "gemm_bwd_dw_down", "gemm_bwd_dw_upgate"};
+  static const char* dense[] = {"shared_fwd_upgate_swiglu", "shared_fwd_down",
+                                "shared_bwd_dh_swiglu", "shared_bwd_dx", "shared_bwd_dw_down",
+                                "shared_bwd_dw_upgate"};
+  return c.dense ? dense[c.mode] : routed[c.mode];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mok_status_string(mok_status s) {
+  switch (s) {
+    case MOK_OK: return "ok";
+    case MOK_ERR_INVALID_ARG: return "invalid argument";
+    case MOK_ERR_UNSUPPORTED: return "unsupported";
+    case MOK_ERR_WORKSPACE: return "workspace missing or misaligned";
+    case MOK_ERR_CUDA: return "CUDA error";
+    case MOK_ERR_TIMEOUT: return "device wait timed out";
+    case MOK_ERR_DEVICE: return "device flagged bad data";
+  }
+  return "unknown status";
+}
+
+int mok_minibatch_tokens(int H, int I, int k, int num_sms) {
+  // Two full waves: every SM takes one 64-row slice of a grouped-GEMM tile per wave, so a
+  // minibatch must route at least 2 * num_sms * 64 rows, i.e. ceil(that / k) tokens.
+  if (H <= 0 || I <= 0 || k <= 0 || num_sms <= 0) return -1;
+  const long rows = 2L * num_sms * 64;
+  return (int)((rows + k - 1) / k);
+}
+
+mok_status mok_create(const mok_dims* dims, mok_ctx_t* out) {
+  if (!dims || !out) return MOK_ERR_INVALID_ARG;
+  *out = nullptr;
+  const mok_dims& x = *dims;
+  if (x.T < 1 || x.H < 128 || x.I < 128 || x.E < 1 || x.k < 1) return MOK_ERR_INVALID_ARG;
+  if (x.H % 128 || x.I % 128) return MOK_ERR_INVALID_ARG;
+  if (x.E > kMaxE || x.k > kMaxK) return MOK_ERR_INVALID_ARG;
+  if (x.router && x.k > x.E) return MOK_ERR_INVALID_ARG;
+  if (x.shared_I < 0 || (x.shared_I % 128) != 0) return MOK_ERR_INVALID_ARG;
+  if (x.router != 0 && x.router != 1) return MOK_ERR_INVALID_ARG;
+  if (x.macrobatches < 0) return MOK_ERR_INVALID_ARG;
+  if ((long long)x.T * x.k + (long long)x.E * 127 > (1LL << 30)) return MOK_ERR_INVALID_ARG;
+  if ((long long)x.E * x.H > (1LL << 31) || (long long)x.E * x.I > (1LL << 31))
+    return MOK_ERR_INVALID_ARG;
+  mok_ctx_s* c = new (std::nothrow) mok_ctx_s;
+  if (!c) return MOK_ERR_INVALID_ARG;
+  c->dims = x;
+  c->d = make_dims(x);
+  c->precision = MOK_BF16;
+  // Without a usable device the context still answers the host-only queries
+  // (mok_get_sizes); every call that launches work then returns MOK_ERR_CUDA.
+  c->device = -1;
+  c->num_sms = 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+    c->device = dev;
+    c->num_sms = sms;
+  } else {
+    cudaGetLastError();
+  }
+  *out = c;
+  return MOK_OK;
+}
+
+void mok_destroy(mok_ctx_t ctx) { delete ctx; }
+
+mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  if (p != MOK_BF16 && p != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+  if (p == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  ctx->precision = p;
+  return MOK_OK;
+}
+
+mok_status mok_get_sizes(mok_ctx_t ctx, mok_sizes* out) {
+  if (!ctx || !out) return MOK_ERR_INVALID_ARG;
+  const Dims& d = ctx->d;
+  out->aux_bytes = aux_layout(d).total;
+  size_t ws = plan_ws(d).total;
+  size_t f = fwd_ws(d).total, b = bwd_ws(d).total;
+  if (f > ws) ws = f;
+  if (b > ws) ws = b;
+  out->workspace_bytes = ws;
+  out->saved_bytes = saved_layout(d).total;
+  out->mx_weight_bytes = 0;
+  out->padded_rows_max = d.P_max;
+  out->macrobatches = 1;
+  return MOK_OK;
+}
+
+mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* logit_bias,
+                    mok_sched* sched, void* workspace, void* stream) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  const Dims& d = ctx->d;
+  mok_status st = check_sched(d, sched);
+  if (st != MOK_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return MOK_ERR_WORKSPACE;
+  if (d.router) {
+    if (!x || !Wr || !aligned(x, 16)) return MOK_ERR_INVALID_ARG;
+  } else if (x || Wr || logit_bias) {
+    return MOK_ERR_INVALID_ARG;
+  }
+  if (ctx->num_sms <= 0) return MOK_ERR_CUDA;  // no usable device
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AuxPtrs a = aux_ptrs(d, sched->aux);
+  PlanWs L = plan_ws(d);
+  float* logits = reinterpret_cast<float*>(at(workspace, L.logits));
+  int32_t* hist = reinterpret_cast<int32_t*>(at(workspace, L.hist));
+  int32_t* lrank = reinterpret_cast<int32_t*>(at(workspace, L.lrank));
+  MOK_CHECK_CUDA(cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s));
+  if (d.router) MOK_LAUNCH("router_logits", launch_router_logits(d, x, Wr, logit_bias, logits, s));
+  MOK_LAUNCH("topk_rank", launch_topk_rank(d, d.router ? logits : nullptr, sched->topk_idx,
+                                            sched->gates, hist, lrank, a.status, s));
+  MOK_LAUNCH("plan_scan", launch_plan_scan(d, hist, sched->counts, sched->offsets, a, s));
+  MOK_LAUNCH("plan_scatter", launch_plan_scatter(d, sched->topk_idx, hist, lrank,
+                                                  sched->offsets, sched->table, sched->inv, s));
+  return MOK_OK;
+}
+
+static mok_status check_weights(const Dims& d, const mok_weights* w) {
+  if (!w || !w->W_up || !w->W_gate || !w->W_down) return MOK_ERR_INVALID_ARG;
+  if (!aligned(w->W_up, 16) || !aligned(w->W_gate, 16) || !aligned(w->W_down, 16))
+    return MOK_ERR_INVALID_ARG;
+  if (d.Is) {
+    if (!w->Ws_up || !w->Ws_gate || !w->Ws_down) return MOK_ERR_INVALID_ARG;
+    if (!aligned(w->Ws_up, 16) || !aligned(w->Ws_gate, 16) || !aligned(w->Ws_down, 16))
+      return MOK_ERR_INVALID_ARG;
+  }
+  return MOK_OK;
+}
+
+static GemmCall routed_call(const Dims& d, const mok_sched* sc, const AuxPtrs& a, GemmMode m) {
+  GemmCall c;
+  memset(&c, 0, sizeof(c));
+  c.mode = m;
+  c.M_rows = d.P_max;
+  c.dense = false;
+  c.H = d.H;
+  c.I = d.I;
+  c.groups = d.E;
+  c.poff = a.poff;
+  c.counts = sc->counts;
+  c.offsets = sc->offsets;
+  c.tile_expert = a.tile_expert;
+  c.num_mtiles = a.num_mtiles;
+  c.table = sc->table;
+  c.gates = sc->gates;
+  c.k = d.k;
+  c.status = a.status;
+  return c;
+}
+
+static GemmCall dense_call(const Dims& d, const AuxPtrs& a, GemmMode m) {
+  GemmCall c;
+  memset(&c, 0, sizeof(c));
+  c.mode = m;
+  c.M_rows = d.T;
+  c.dense = true;
+  c.H = d.H;
+  c.I = d.Is;
+  c.groups = 1;
+  c.k = d.k;
+  c.status = a.status;
+  return c;
+}
+
+mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
+                       const mok_weights* w, void* y, void* saved, void* workspace,
+                       void* stream) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  const Dims& d = ctx->d;
+  mok_status st = check_sched(d, sched);
+  if (st != MOK_OK) return st;
+  if ((st = check_weights(d, w)) != MOK_OK) return st;
+  if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return MOK_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || !saved || !aligned(saved, 256))
+    return MOK_ERR_WORKSPACE;
+  if (ctx->num_sms <= 0) return MOK_ERR_CUDA;  // no usable device
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AuxPtrs a = aux_ptrs(d, sched->aux);
+  FwdWs L = fwd_ws(d);
+  SavedLayout S = saved_layout(d);
+  void* xg = at(workspace, L.xg);
+  void* h = at(workspace, L.h);
+  void* o = at(workspace, L.o);
+
+  // dispatch: pull token rows into expert order through the table
+  MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
+  // grouped up|gate GEMM + SwiGLU
+  GemmCall c = routed_call(d, sched, a, kFwdUpGate);
+  c.a0 = xg;
+  c.b0 = w->W_up;
+  c.b1 = w->W_gate;
+  c.out0 = h;
+  c.out1 = at(saved, S.u);
+  c.out2 = at(saved, S.v);
+  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  // grouped down GEMM
+  c = routed_call(d, sched, a, kFwdDown);
+  c.a0 = h;
+  c.b0 = w->W_down;
+  c.out0 = o;
+  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  const void* shared_out = nullptr;
+  if (d.Is) {
+    GemmCall cs = dense_call(d, a, kFwdUpGate);
+    cs.a0 = x;
+    cs.b0 = w->Ws_up;
+    cs.b1 = w->Ws_gate;
+    cs.out0 = at(workspace, L.hs);
+    cs.out1 = at(saved, S.us);
+    cs.out2 = at(saved, S.vs);
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    cs = dense_call(d, a, kFwdDown);
+    cs.a0 = at(workspace, L.hs);
+    cs.b0 = w->Ws_down;
+    cs.out0 = at(workspace, L.os);
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    shared_out = at(workspace, L.os);
+  }
+  // weighted combine in slot order
+  MOK_LAUNCH("combine", launch_combine(d, o, *sched, a, shared_out, true, y, s));
+  return MOK_OK;
+}
+
+mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, const float* Wr,
+                       const mok_weights* w, const void* saved, const void* dY, void* dX,
+                       mok_grads* g, void* workspace, void* stream) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  const Dims& d = ctx->d;
+  mok_status st = check_sched(d, sched);
+  if (st != MOK_OK) return st;
+  if ((st = check_weights(d, w)) != MOK_OK) return st;
+  if (!x || !dY || !dX || !aligned(x, 16) || !aligned(dY, 16) || !aligned(dX, 16))
+    return MOK_ERR_INVALID_ARG;
+  if (!g || !g->dW_up || !g->dW_gate || !g->dW_down || !g->dgates) return MOK_ERR_INVALID_ARG;
+  if (d.router && (!Wr || !g->dWr)) return MOK_ERR_INVALID_ARG;
+  if (!d.router && (Wr || g->dWr)) return MOK_ERR_INVALID_ARG;
+  if (d.Is && (!g->dWs_up || !g->dWs_gate || !g->dWs_down)) return MOK_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || !saved || !aligned(saved, 256))
+    return MOK_ERR_WORKSPACE;
+  if (ctx->num_sms <= 0) return MOK_ERR_CUDA;  // no usable device
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AuxPtrs a = aux_ptrs(d, sched->aux);
+  BwdWs L = bwd_ws(d);
+  SavedLayout S = saved_layout(d);
+  void* dyg = at(workspace, L.dyg);
+  void* xg = at(workspace, L.xg);
+  void* du = at(workspace, L.du);
+  void* dv = at(workspace, L.dv);
+  void* hg = at(workspace, L.hg);
+  void* dxg = at(workspace, L.dxg);
+  float* dgp = reinterpret_cast<float*>(at(workspace, L.dgp));
+  float* dl = reinterpret_cast<float*>(at(workspace, L.dl));
+
+  // reverse dispatch of dY and replay of the forward gather, both through the table
+  MOK_LAUNCH("reverse_dispatch_gather", launch_gather_rows(d, dY, *sched, a, dyg, ctx->num_sms, s));
+  MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
+  // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
+  GemmCall c = routed_call(d, sched, a, kBwdDH);
+  c.a0 = dyg;
+  c.b0 = w->W_down;
+  c.aux0 = at(const_cast<void*>(saved), S.u);
+  c.aux1 = at(const_cast<void*>(saved), S.v);
+  c.out0 = du;
+  c.out1 = dv;
+  c.out2 = hg;
+  c.dgp = dgp;
+  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  // dXg = du W_up^T + dv W_gate^T
+  c = routed_call(d, sched, a, kBwdDX);
+  c.a0 = du;
+  c.a1 = dv;
+  c.b0 = w->W_up;
+  c.b1 = w->W_gate;
+  c.out0 = dxg;
+  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  // router-weight gradient and the renormalised-softmax backward
+  MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I), *sched, a,
+                                                g->dgates, d.router ? dl : nullptr, s));
+  const void* dxs = nullptr;
+  if (d.Is) {
+    GemmCall cs = dense_call(d, a, kBwdDH);
+    cs.a0 = dY;
+    cs.b0 = w->Ws_down;
+    cs.aux0 = at(const_cast<void*>(saved), S.us);
+    cs.aux1 = at(const_cast<void*>(saved), S.vs);
+    cs.out0 = at(workspace, L.dus);
+    cs.out1 = at(workspace, L.dvs);
+    cs.out2 = at(workspace, L.hsg);
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    cs = dense_call(d, a, kBwdDX);
+    cs.a0 = at(workspace, L.dus);
+    cs.a1 = at(workspace, L.dvs);
+    cs.b0 = w->Ws_up;
+    cs.b1 = w->Ws_gate;
+    cs.out0 = at(workspace, L.dxs);
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    dxs = at(workspace, L.dxs);
+  }
+  // dX: reverse combine in slot order (+ shared expert, + router path)
+  float* wrt = reinterpret_cast<float*>(at(workspace, L.dxs + 2 * (size_t)d.T * d.H));
+  if (d.router) MOK_LAUNCH("transpose_wr", launch_transpose_wr(d, Wr, wrt, s));
+  MOK_LAUNCH("reverse_combine", launch_reverse_combine(d, dxg, *sched, a, dxs,
+                                                       d.router ? dl : nullptr, wrt, dX, s));
+  // weight gradients, each a fixed-order sum over the expert's rows
+  c = routed_call(d, sched, a, kBwdDWUpGate);
+  c.a0 = xg;
+  c.b0 = du;
+  c.b1 = dv;
+  c.out0 = g->dW_up;
+  c.out1 = g->dW_gate;
+  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  c = routed_call(d, sched, a, kBwdDWDown);
+  c.a0 = hg;
+  c.b0 = dyg;
+  c.out0 = g->dW_down;
+  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  if (d.Is) {
+    GemmCall cs = dense_call(d, a, kBwdDWUpGate);
+    cs.a0 = x;
+    cs.b0 = at(workspace, L.dus);
+    cs.b1 = at(workspace, L.dvs);
+    cs.out0 = g->dWs_up;
+    cs.out1 = g->dWs_gate;
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    cs = dense_call(d, a, kBwdDWDown);
+    cs.a0 = at(workspace, L.hsg);
+    cs.b0 = dY;
+    cs.out0 = g->dWs_down;
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+  }
+  if (d.router) MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, dl, g->dWr, s));
+  return MOK_OK;
+}
+
+mok_status mok_quantize_weights_mxfp8(mok_ctx_t ctx, const mok_weights* w, void* mx_out,
+                                      void* stream) {
+  (void)w;
+  (void)mx_out;
+  (void)stream;
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  return MOK_ERR_UNSUPPORTED;
+}
+
+mok_status mok_get_status(mok_ctx_t ctx, const mok_sched* sched, void* stream) {
+  if (!ctx || !sched || !sched->aux) return MOK_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AuxPtrs a = aux_ptrs(ctx->d, sched->aux);
+  uint32_t v = 0;
+  MOK_CHECK_CUDA(cudaMemcpyAsync(&v, a.status, sizeof(v), cudaMemcpyDeviceToHost, s));
+  MOK_CHECK_CUDA(cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s));
+  MOK_CHECK_CUDA(cudaStreamSynchronize(s));
+  if (v & kErrTimeout) return MOK_ERR_TIMEOUT;
+  if (v & kErrBadExpert) return MOK_ERR_DEVICE;
+  return MOK_OK;
+}
+
+mok_status mok_profile_enable(mok_ctx_t ctx, int enable) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  ctx->profile = enable != 0;
+  ctx->recs.clear();
+  ctx->pool_used = 0;
+  return MOK_OK;
+}
+
+mok_status mok_profile_report(mok_ctx_t ctx, char* buf, size_t len, int* total_launches) {
+  if (!ctx || !buf || len == 0) return MOK_ERR_INVALID_ARG;
+  std::vector<std::string> names;
+  std::vector<int> cnt;
+  std::vector<double> ms;
+  for (auto& r : ctx->recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return MOK_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return MOK_ERR_CUDA;
+    size_t i = 0;
+    while (i < names.size() && names[i] != r.name) ++i;
+    if (i == names.size()) {
+      names.push_back(r.name);
+      cnt.push_back(0);
+      ms.push_back(0.0);
+    }
+    cnt[i] += 1;
+    ms[i] += t;
+  }
+  std::string out;
+  for (size_t i = 0; i < names.size(); ++i) {
+    char line[256];
+    snprintf(line, sizeof(line), "%s %d %.6f\n", names[i].c_str(), cnt[i], ms[i]);
+    out += line;
+  }
+  size_t n = out.size() < len - 1 ? out.size() : len - 1;
+  memcpy(buf, out.data(), n);
+  buf[n] = 0;
+  if (total_launches) *total_launches = (int)ctx->recs.size();
+  ctx->recs.clear();
+  ctx->pool_used = 0;
+  return MOK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,314 @@
+// Routing and the no-sort schedule table.
+//
+// "Das Scheduling" (sebask.de MoK article): a pull schedule is a list of source indices
+// whose order follows from the routing itself, built entirely on the GPU without a sort;
+// "Escolha da direcao de comunicacao" (stamatios.com): the table is built once and reused
+// by forward dispatch/combine and backward reverse-dispatch/reverse-combine.
+//
+// Construction (deterministic, no sort, no atomics):
+//   1. router logits, softmax top-k and renormalised gates per token;
+//   2. per block of 32 tokens, one warp walks the block's slots in ascending (t, j) and
+//      gives each slot its rank among the block's slots of the same expert
+//      (__match_any_sync + popc), producing a per-block expert histogram;
+//   3. one CTA scans the histograms over blocks (per expert) and over experts (warp-scan)
+//      into counts, offsets and 128-row padded offsets, and maps each 128-row tile of the
+//      padded row space to its expert;
+//   4. every slot lands at offsets[e] + (rows of e in earlier blocks) + its block rank.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mok_internal.h"
+
+namespace mok {
+
+// ---------------------------------------------------------------- 1a. logits (fp32 FMA)
+// CTA: 64 tokens x 128 experts; thread tile 8 tokens x 4 experts; H walked in chunks of
+// 32 in ascending order, so every logit is one fixed-order fp32 sum.
+constexpr int kLgTok = 64, kLgExp = 128, kLgK = 32;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(int T, int H, int E,
+                                                            const __nv_bfloat16* __restrict__ x,
+                                                            const float* __restrict__ Wr,
+                                                            const float* __restrict__ bias,
+                                                            float* __restrict__ logits) {
+  __shared__ float xs[kLgK][kLgTok + 4];
+  __shared__ float ws[kLgK][kLgExp];
+  const int tid = threadIdx.x;
+  const int tx = tid & 31, ty = tid >> 5;
+  const int t0 = blockIdx.x * kLgTok, e0 = blockIdx.y * kLgExp;
+  float acc[8][4];
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+
+  for (int h0 = 0; h0 < H; h0 += kLgK) {
+    // x tile: 64 tokens x 32 h, stored transposed
+    for (int i = tid; i < kLgTok * kLgK; i += 256) {
+      int tt = i / kLgK, hh = i % kLgK;
+      int t = t0 + tt;
+      xs[hh][tt] = (t < T) ? __bfloat162float(x[(size_t)t * H + h0 + hh]) : 0.f;
+    }
+    for (int i = tid; i < kLgK * kLgExp; i += 256) {
+      int hh = i / kLgExp, ee = i % kLgExp;
+      int e = e0 + ee;
+      ws[hh][ee] = (e < E) ? Wr[(size_t)(h0 + hh) * E + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < kLgK; ++kk) {
+      float a[8], b[4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = xs[kk][ty * 8 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx + 32 * j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int t = t0 + ty * 8 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int e = e0 + tx + 32 * j;
+      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const Dims& d, const void* x, const float* Wr, const float* bias,
+                                 float* logits, cudaStream_t s) {
+  dim3 grid((d.T + kLgTok - 1) / kLgTok, (d.E + kLgExp - 1) / kLgExp);
+  router_logits_kernel<<<grid, 256, 0, s>>>(d.T, d.H, d.E,
+                                            static_cast<const __nv_bfloat16*>(x), Wr, bias,
+                                            logits);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 1b+2. top-k and ranks
+// One CTA per block of 32 tokens (8 warps, 4 tokens each). logits == nullptr: topk_idx is
+// an input (expert ids are range-checked; a bad id is flagged and replaced by 0 so that
+// every later index stays in bounds).
+__global__ void __launch_bounds__(256) topk_rank_kernel(int T, int E, int k,
+                                                        const float* __restrict__ logits,
+                                                        int32_t* __restrict__ topk_idx,
+                                                        float* __restrict__ gates,
+                                                        int32_t* __restrict__ hist,
+                                                        int32_t* __restrict__ lrank,
+                                                        uint32_t* __restrict__ status) {
+  __shared__ int32_t s_idx[kTokBlock * kMaxK];
+  __shared__ int32_t s_hist[kMaxE];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int blk = blockIdx.x;
+  const int t0 = blk * kTokBlock;
+  const int ntok = min(kTokBlock, T - t0);
+  for (int e = tid; e < E; e += 256) s_hist[e] = 0;
+
+  if (logits != nullptr) {
+    for (int tt = warp; tt < ntok; tt += 8) {
+      const int t = t0 + tt;
+      float v[kMaxE / 32];
+      const float* lg = logits + (size_t)t * E;
+#pragma unroll
+      for (int i = 0; i < kMaxE / 32; ++i) {
+        int e = lane + 32 * i;
+        v[i] = (e < E) ? lg[e] : -INFINITY;
+      }
+      uint32_t taken = 0;
+      float top_l[kMaxK];
+      int top_e[kMaxK];
+      for (int j = 0; j < k; ++j) {
+        // lane-local best: larger value, ties to the lower expert id
+        float bv = -INFINITY;
+        int be = 0x7fffffff;  // sentinel: no candidate yet
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) {
+          int e = lane + 32 * i;
+          bool ok = (e < E) && !((taken >> i) & 1u);
+          if (ok && (be == 0x7fffffff || v[i] > bv || (v[i] == bv && e < be))) {
+            bv = v[i];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if (be == 0x7fffffff) {  // only NaN logits left: flag, keep indices in range
+          if (lane == 0) atomicOr(status, kErrBadExpert);
+          be = 0;
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        top_l[j] = bv;
+        top_e[j] = be;
+      }
+      if (lane == 0) {
+        // gates = softmax over the chosen logits (= renormalised softmax probabilities)
+        float z = 0.f, p[kMaxK];
+        for (int j = 0; j < k; ++j) {
+          p[j] = expf(top_l[j] - top_l[0]);
+          z += p[j];
+        }
+        for (int j = 0; j < k; ++j) {
+          topk_idx[(size_t)t * k + j] = top_e[j];
+          gates[(size_t)t * k + j] = p[j] / z;
+          s_idx[tt * k + j] = top_e[j];
+        }
+      }
+    }
+  } else {
+    for (int i = tid; i < ntok * k; i += 256) {
+      int e = topk_idx[(size_t)t0 * k + i];
+      if (e < 0 || e >= E) {
+        atomicOr(status, kErrBadExpert);
+        e = 0;
+      }
+      s_idx[i] = e;
+    }
+  }
+  __syncthreads();
+
+  // ranks inside the block, walking slots in ascending (t, j)
+  if (warp == 0) {
+    const int nslots = ntok * k;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int c = 0; c < nslots; c += 32) {
+      int sl = c + lane;
+      int e = (sl < nslots) ? s_idx[sl] : -1 - lane;  // idle lanes match nobody
+      unsigned peers = __match_any_sync(0xffffffffu, e);
+      int r = 0;
+      if (sl < nslots) r = s_hist[e] + __popc(peers & lt_mask);
+      __syncwarp();
+      if (sl < nslots) {
+        lrank[(size_t)t0 * k + sl] = r;
+        if ((__ffs(peers) - 1) == lane) s_hist[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) hist[(size_t)blk * E + e] = s_hist[e];
+}
+
+cudaError_t launch_topk_rank(const Dims& d, const float* logits, int32_t* topk_idx, float* gates,
+                             int32_t* hist, int32_t* lrank, uint32_t* status, cudaStream_t s) {
+  topk_rank_kernel<<<d.nblk, 256, 0, s>>>(d.T, d.E, d.k, logits, topk_idx, gates, hist, lrank,
+                                          status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 3. scans (one CTA)
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int u = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += u;
+  }
+  return v;
+}
+
+// Exclusive scan of one value per thread over the CTA (blockDim.x multiple of 32).
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = warp_inclusive_scan(v);
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < nw) ? s_warp[lane] : 0;
+    int wi = warp_inclusive_scan(w);
+    if (lane < nw) s_warp[lane] = wi - w;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  int r = s_warp[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32_t* hist,
+                                                          int32_t* counts, int32_t* offsets,
+                                                          int32_t* poff, int32_t* tile_expert,
+                                                          int32_t* num_mtiles) {
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    // rows of e in earlier blocks (exclusive, in place); loads batched for latency
+    for (int b0 = 0; b0 < nblk; b0 += 32) {
+      int v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = (b0 + i < nblk) ? hist[(size_t)(b0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (b0 + i < nblk) hist[(size_t)(b0 + i) * E + e] = run;
+        run += v[i];
+      }
+    }
+  }
+  const int cnt = (e < E) ? run : 0;
+  const int pcnt = (cnt + kRowPad - 1) / kRowPad * kRowPad;
+  int off = block_exclusive_scan(cnt, s_warp, &s_total);
+  const int R = s_total;
+  int poff_e = block_exclusive_scan(pcnt, s_warp, &s_total);
+  const int P = s_total;
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    poff[e] = poff_e;
+    for (int m = poff_e / kRowPad; m < (poff_e + pcnt) / kRowPad; ++m) tile_expert[m] = e;
+  }
+  if (e == 0) {
+    offsets[E] = R;
+    poff[E] = P;
+    *num_mtiles = P / kRowPad;
+  }
+}
+
+cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int32_t* offsets,
+                             const AuxPtrs& a, cudaStream_t s) {
+  int threads = (d.E + 31) / 32 * 32;
+  plan_scan_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, hist, counts, offsets, a.poff,
+                                         a.tile_expert, a.num_mtiles);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 4. scatter into the table
+__global__ void plan_scatter_kernel(int R, int k, int E, const int32_t* __restrict__ topk_idx,
+                                    const int32_t* __restrict__ hist,
+                                    const int32_t* __restrict__ lrank,
+                                    const int32_t* __restrict__ offsets,
+                                    int32_t* __restrict__ table, int32_t* __restrict__ inv) {
+  int sl = blockIdx.x * blockDim.x + threadIdx.x;
+  if (sl >= R) return;
+  int t = sl / k, j = sl - t * k;
+  int e = topk_idx[sl];
+  if (e < 0 || e >= E) e = 0;  // already flagged by the rank kernel
+  int row = offsets[e] + hist[(size_t)(t / kTokBlock) * E + e] + lrank[sl];
+  table[2 * (size_t)row] = t;
+  table[2 * (size_t)row + 1] = j;
+  inv[sl] = row;
+}
+
+cudaError_t launch_plan_scatter(const Dims& d, const int32_t* topk_idx, const int32_t* hist,
+                                const int32_t* lrank, const int32_t* offsets, int32_t* table,
+                                int32_t* inv, cudaStream_t s) {
+  int threads = 256;
+  int blocks = (d.R + threads - 1) / threads;
+  plan_scatter_kernel<<<blocks, threads, 0, s>>>(d.R, d.k, d.E, topk_idx, hist, lrank, offsets,
+                                                 table, inv);
+  return cudaGetLastError();
+}
+
+}  // namespace mok

@@ -1,0 +1,195 @@
+/*
+ * mok.h - C ABI of the GB300 (sm_103a) MoE SwiGLU layer library.
+ *
+ * The library runs the data-parallel hot path of a Mixture-of-Experts layer as the
+ * Mixture-of-Kittens articles describe it, on one GPU:
+ *   top-k routing -> schedule table built on the GPU with no sort -> gather of token rows
+ *   into expert order -> grouped up/gate GEMM with SwiGLU -> grouped down GEMM ->
+ *   weighted combine; and the backward pass (SwiGLU derivative fused with the
+ *   router-weight gradient, then dX, dW_up, dW_gate, dW_down in a fixed order).
+ *
+ * Sources for what is computed (page title, then section):
+ *   [S] "Mixture-of-Kittens: Cursors Open-Source-Ansatz fuer effizientes MoE-Training auf
+ *       NVL72" (sebask.de): intro (router, experts with up/gate/down projection);
+ *       "Push oder Pull?" (pull dispatch, push combine, one plan for the four exchange
+ *       steps); "Das Scheduling" (table of source indices, order follows from routing,
+ *       no sort, built on the GPU); "Determinismus und MXFP8-Unterstuetzung".
+ *   [C] "Cursor abre codigo de megakernel MoE para GPUs NVL72" (stamatios.com):
+ *       "Escolha da direcao de comunicacao" (table built once, reused by the four ops);
+ *       "Granularidade do overlap" (minibatch of at least two full SM waves);
+ *       "Ring token buffers (macrobatch)"; "Outras caracteristicas" (determinism,
+ *       MXFP8 with BF16 shared expert, router-weight gradient fused into SwiGLU bwd).
+ *
+ * Conventions (every entry point):
+ *   - All tensors are row-major and dense. "bf16" buffers hold IEEE bfloat16 bits.
+ *   - Every data pointer is a DEVICE pointer owned by the caller. The library never
+ *     allocates device memory inside these calls; scratch space is the caller's
+ *     `workspace`, whose size mok_get_sizes reports.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls only enqueue work
+ *     on it; none synchronises with the host except mok_get_status.
+ *   - Argument errors are detected on the host and returned before anything is launched.
+ *     Errors found on the device (bounded waits that time out, out-of-range expert ids)
+ *     set bits in a device status word kept in the schedule's aux buffer; mok_get_status
+ *     reads and clears it.
+ *   - Results are bitwise reproducible from run to run: every reduction has a fixed
+ *     order that depends only on the schedule table.
+ */
+#ifndef MOK_H_
+#define MOK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = -1, /* bad pointer, size or combination of arguments        */
+  MOK_ERR_UNSUPPORTED = -2, /* valid request this build does not support            */
+  MOK_ERR_WORKSPACE = -3,   /* workspace/aux/saved buffer missing or misaligned     */
+  MOK_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed                    */
+  MOK_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired                   */
+  MOK_ERR_DEVICE = -6       /* the device flagged bad data (e.g. expert id >= E)    */
+} mok_status;
+
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
+
+typedef struct mok_ctx_s* mok_ctx_t;
+
+/* Layer dimensions. T tokens, H hidden, I expert intermediate size, E routed experts,
+ * k experts per token. H and I must be multiples of 128; 1 <= k <= 8 <= ... E <= 512;
+ * shared_I (0 = no shared expert) a multiple of 128. router = 1: mok_plan routes from
+ * x and Wr; router = 0: the caller supplies topk_idx and gates (an expert slice fed by
+ * an external dispatcher). macrobatches (0 = auto) splits the token range into
+ * consecutive chunks that pass through the ring token buffer one after another;
+ * ring_bytes (0 = auto) bounds that buffer ([C] "Ring token buffers"). */
+typedef struct {
+  int T, H, I, E, k;
+  int shared_I;
+  int router;
+  int macrobatches;
+  size_t ring_bytes;
+} mok_dims;
+
+/* Schedule produced by mok_plan and passed unchanged to mok_moe_fwd and mok_moe_bwd
+ * ([S] "Push oder Pull?": the dispatch plan is reused by the other exchange steps).
+ * All device pointers, caller-owned:
+ *   topk_idx [T][k] int32  expert of slot (t, j); slot order = descending gate
+ *   gates    [T][k] fp32   renormalised routing weights
+ *   counts   [E]    int32  rows routed to each expert
+ *   offsets  [E+1]  int32  exclusive prefix sum of counts
+ *   table    [T*k][2] int32 for expert row r: (source token t, slot j), rows of expert e
+ *                          at offsets[e] .. offsets[e+1]-1 in ascending (t, j)
+ *   inv      [T][k] int32  row of (t, j) in the table
+ *   aux      mok_sizes.aux_bytes, 256-byte aligned: library-private schedule data
+ *            (padded offsets, tile maps, per-block histograms, device status word). */
+typedef struct {
+  int32_t* topk_idx;
+  float* gates;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* table;
+  int32_t* inv;
+  void* aux;
+} mok_sched;
+
+/* Weights (device, bf16 unless noted):
+ *   W_up, W_gate [E][H][I]; W_down [E][I][H]
+ *   Ws_up, Ws_gate [H][shared_I]; Ws_down [shared_I][H]  (NULL when shared_I == 0)
+ *   mx: MXFP8 copies of W_up, W_gate, W_down written by mok_quantize_weights_mxfp8
+ *       (mok_sizes.mx_weight_bytes, library-private layout); required in MXFP8 mode. */
+typedef struct {
+  const void* W_up;
+  const void* W_gate;
+  const void* W_down;
+  const void* Ws_up;
+  const void* Ws_gate;
+  const void* Ws_down;
+  const void* mx;
+} mok_weights;
+
+/* Gradients written by mok_moe_bwd (device). dW_* bf16 with the weights' shapes;
+ * dgates [T][k] fp32 (dL/dgate, the router-weight gradient); dWr [H][E] fp32 (NULL
+ * when there is no router); dWs_* bf16 (NULL when there is no shared expert). */
+typedef struct {
+  void* dW_up;
+  void* dW_gate;
+  void* dW_down;
+  float* dgates;
+  float* dWr;
+  void* dWs_up;
+  void* dWs_gate;
+  void* dWs_down;
+} mok_grads;
+
+typedef struct {
+  size_t aux_bytes;        /* mok_sched.aux                                   */
+  size_t workspace_bytes;  /* scratch for mok_plan / mok_moe_fwd / mok_moe_bwd  */
+  size_t saved_bytes;      /* forward activations kept for the backward        */
+  size_t mx_weight_bytes;  /* mok_weights.mx                                    */
+  int padded_rows_max;     /* upper bound of expert rows after 128-row padding  */
+  int macrobatches;        /* resolved macrobatch count                         */
+} mok_sizes;
+
+/* ---- helpers (host only; nothing is launched) ---------------------------------- */
+
+/* Validate dims and create a context for the current CUDA device. *out owns no device
+ * memory. Returns MOK_ERR_INVALID_ARG for unsupported shapes. */
+mok_status mok_create(const mok_dims* dims, mok_ctx_t* out);
+void mok_destroy(mok_ctx_t ctx);
+/* Buffer sizes for the context's dims and precision. */
+mok_status mok_get_sizes(mok_ctx_t ctx, mok_sizes* out);
+/* Smallest token count whose routed rows fill at least two full waves of `num_sms` SMs
+ * when every SM takes 64 rows of a grouped-GEMM tile per wave ([C] "Granularidade do
+ * overlap": two waves; the page gives T >= 2368 for H=7168, I=2048, k=8, 148 SMs).
+ * Returns -1 on bad arguments. */
+int mok_minibatch_tokens(int H, int I, int k, int num_sms);
+const char* mok_status_string(mok_status s);
+
+/* ---- the layer ----------------------------------------------------------------- */
+
+/* Select the arithmetic of later mok_moe_fwd / mok_moe_bwd calls: MOK_BF16 (bf16
+ * operands) or MOK_MXFP8 (E4M3 elements with one UE8M0 scale per 32 along each GEMM's
+ * contraction axis; the shared expert stays BF16) ([S] "Determinismus und
+ * MXFP8-Unterstuetzung"; [C] "Outras caracteristicas"). Host-only state change. */
+mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
+
+/* Routing and schedule on the device ([S] "Das Scheduling"; [C] "Escolha da direcao").
+ *   x [T][H] bf16; Wr [H][E] fp32; logit_bias [E] fp32 or NULL.
+ * With dims.router = 1, writes topk_idx and gates (softmax of x Wr + bias, top-k, gates
+ * renormalised over the k chosen experts; ties go to the lower expert id). With
+ * dims.router = 0, x/Wr/logit_bias must be NULL and sched->topk_idx, sched->gates are
+ * inputs. Then, with no sort, writes counts, offsets, table, inv and the aux data.
+ * Deterministic: depends only on topk_idx. */
+mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* logit_bias,
+                    mok_sched* sched, void* workspace, void* stream);
+
+/* Forward: y [T][H] bf16 = sum_j gates[t][j] * FFN_{topk_idx[t][j]}(x[t]) (+ shared
+ * expert), FFN_e(v) = (silu(v W_gate[e]) * (v W_up[e])) W_down[e]; the k terms are added
+ * in slot order in fp32. `saved` (mok_sizes.saved_bytes) receives what mok_moe_bwd
+ * needs; it must stay untouched until then. */
+mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
+                       const mok_weights* w, void* y, void* saved, void* workspace,
+                       void* stream);
+
+/* Backward for upstream gradient dY [T][H] bf16. Writes dX [T][H] bf16 (routed experts,
+ * shared expert and, when routing ran on the device, the router path) and `grads`.
+ * Wr must be the router weight given to mok_plan (NULL when dims.router = 0). */
+mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, const float* Wr,
+                       const mok_weights* w, const void* saved, const void* dY, void* dX,
+                       mok_grads* grads, void* workspace, void* stream);
+
+/* MXFP8 copies of the routed expert weights in every layout the forward and backward
+ * GEMMs read (blocks of 32 along H and along I), into w->mx. */
+mok_status mok_quantize_weights_mxfp8(mok_ctx_t ctx, const mok_weights* w, void* mx_out,
+                                      void* stream);
+
+/* Synchronise `stream`, read and clear the device status word of `sched`. */
+mok_status mok_get_status(mok_ctx_t ctx, const mok_sched* sched, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOK_H_ */

@@ -1,0 +1,116 @@
+"""Single-output evaluators of the layer for full-size workloads (fp64, NumPy).
+
+TEST INFRASTRUCTURE ONLY (see oracle/__init__.py). The dense oracle in ``moe`` holds every
+routed row of every expert; at the Kimi/DeepSeek sizes that is too much, so these
+functions compute one token's y or dX row, or one element of a weight gradient, straight
+from the definition (with the same bf16 rounding model as ``moe``, precision "bf16"):
+
+* y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(bf16(silu(x W_gate) * (x W_up)) W_down);
+* dX_t = sum_j bf16(du W_up^T + dv W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j], with
+  D = dY_t W_down^T, du = bf16(g D silu(V)), dv = bf16(g D U silu'(V)) from the bf16 U, V;
+* dW_down[e][i][h] = sum over e's rows of bf16(g silu(V) U)[i] dY[t][h];
+* dW_up[e][h][i] = sum over e's rows of x[t][h] du[i] (dW_gate with dv).
+
+``W`` arguments are callables returning one expert's float64 matrices on demand, so the
+caller can stream them from wherever they live.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .numerics import bf16_round, dsilu, silu
+
+
+def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
+    u = x_t @ Wu
+    v = x_t @ Wg
+    U, V = bf16_round(u), bf16_round(v)
+    h = bf16_round(silu(v) * u)
+    O = bf16_round(h @ Wd)
+    out = {"O": O}
+    if dY_t is not None:
+        D = Wd @ dY_t                      # = dY_t W_down^T
+        hv = silu(V) * U
+        out["dg"] = float(D @ hv)
+        du = bf16_round(g * D * silu(V))
+        dv = bf16_round(g * D * U * dsilu(V))
+        out["dXg"] = bf16_round(Wu @ du + Wg @ dv)
+    return out
+
+
+def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
+    """y_t, and with dY: dX_t and dg_t (the k router-weight gradients) for token t.
+    weights(e) -> (W_up[e], W_gate[e], W_down[e]) float64; shared = (Ws_up, Ws_gate,
+    Ws_down) float64 or None; Wr [H][E] float64 or None (router path of dX)."""
+    x_t = np.asarray(x[t], np.float64)
+    dY_t = None if dY is None else np.asarray(dY[t], np.float64)
+    k = idx.shape[1]
+    y = np.zeros(x_t.shape[0])
+    dX = np.zeros(x_t.shape[0])
+    dg = np.zeros(k)
+    for j in range(k):
+        e = int(idx[t, j])
+        g = float(gates[t, j])
+        r = _row_terms(x_t, dY_t, g, *weights(e))
+        y += g * r["O"]
+        if dY_t is not None:
+            dg[j] = r["dg"]
+            dX += r["dXg"]
+    if shared is not None:
+        Ws_up, Ws_gate, Ws_down = shared
+        u = x_t @ Ws_up
+        v = x_t @ Ws_gate
+        y += bf16_round(bf16_round(silu(v) * u) @ Ws_down)
+        if dY_t is not None:
+            U, V = bf16_round(u), bf16_round(v)
+            D = Ws_down @ dY_t
+            du = bf16_round(D * silu(V))
+            dv = bf16_round(D * U * dsilu(V))
+            dX += bf16_round(Ws_up @ du + Ws_gate @ dv)
+    out = {"y": y}
+    if dY_t is not None:
+        if Wr is not None:
+            s = float((gates[t] * dg).sum())
+            dl = gates[t] * (dg - s)
+            for j in range(k):
+                dX += dl[j] * Wr[:, int(idx[t, j])]
+        out["dX"] = dX
+        out["dgates"] = dg
+    return out
+
+
+def expert_rows(plan, e):
+    """(token, slot) pairs of expert e in table order."""
+    return plan.table[plan.offsets[e]:plan.offsets[e + 1]]
+
+
+def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks):
+    """Elements of expert e's weight gradients. pairs: [n, 2] (t, j) rows of e;
+    picks: list of (name, a, b) with name in dW_up (a=h, b=i), dW_gate (a=h, b=i),
+    dW_down (a=i, b=h). Wu, Wg [H][I], Wd [I][H] float64."""
+    t = pairs[:, 0]
+    g = np.asarray(gates[t, pairs[:, 1]], np.float64)
+    X = np.asarray(x[t], np.float64)
+    dYe = np.asarray(dY[t], np.float64)
+    out = []
+    for name, a, b in picks:
+        if len(t) == 0:
+            out.append(0.0)
+            continue
+        if name == "dW_down":
+            i, h = a, b
+            U = bf16_round(X @ Wu[:, i])
+            V = bf16_round(X @ Wg[:, i])
+            hg = bf16_round(g * silu(V) * U)
+            out.append(float(hg @ dYe[:, h]))
+        else:
+            h, i = a, b
+            U = bf16_round(X @ Wu[:, i])
+            V = bf16_round(X @ Wg[:, i])
+            D = dYe @ Wd[i, :]
+            if name == "dW_up":
+                d = bf16_round(g * D * silu(V))
+            else:
+                d = bf16_round(g * D * U * dsilu(V))
+            out.append(float(X[:, h] @ d))
+    return np.array(out)

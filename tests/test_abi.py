@@ -1,0 +1,81 @@
+"""The C ABI without a GPU: the library loads, exports what include/*.h declares, and its
+host-only logic (argument checks, sizes, the minibatch planner) behaves."""
+import ctypes
+import os
+
+import pytest
+
+from grouped_gemm_built_gb300 import build, mok
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+    mok.lib()
+
+
+def test_exports_every_declared_symbol():
+    declared = mok.declared_symbols()
+    assert {"mok_plan", "mok_moe_fwd", "mok_moe_bwd", "mok_set_precision"} <= set(declared)
+    L = ctypes.CDLL(build.lib_path())
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_two_wave_minibatch_matches_the_page():
+    line = [l for l in open(os.path.join(GOLDEN, "two_wave_minibatch.txt"))
+            if not l.startswith("#") and l.strip()][0]
+    kv = dict(p.split("=") for p in line.split())
+    got = mok.mok_minibatch_tokens(int(kv["H"]), int(kv["I"]), int(kv["k"]), int(kv["sms"]))
+    assert got == int(kv["tokens"])
+    assert mok.mok_minibatch_tokens(7168, 2048, 8, 0) == -1
+
+
+def dims(**over):
+    base = dict(T=256, H=256, I=128, E=8, k=2, shared_I=0, router=1, macrobatches=0,
+                ring_bytes=0)
+    base.update(over)
+    return mok.MokDims(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(H=200), dict(I=96), dict(E=0), dict(E=513), dict(k=9),
+                                 dict(k=9, E=4, router=0), dict(k=5, E=4), dict(T=0),
+                                 dict(shared_I=100), dict(router=2)])
+def test_create_rejects_bad_dims(bad):
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_create(dims(**bad))
+    assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+
+
+def test_sizes_cover_the_padded_row_space():
+    ctx = mok.mok_create(dims(T=300, E=12, k=3, I=256, shared_I=128))
+    s = mok.mok_get_sizes(ctx)
+    R = 300 * 3
+    assert s.padded_rows_max >= R + 12 * 127 and s.padded_rows_max % 128 == 0
+    assert s.saved_bytes >= 2 * 2 * s.padded_rows_max * 256 + 2 * 2 * 300 * 128
+    assert s.workspace_bytes >= 2 * s.padded_rows_max * 256 * 4
+    assert s.aux_bytes >= 4 * (12 + 1)
+    mok.mok_destroy(ctx)
+
+
+def test_calls_check_arguments_before_touching_the_device():
+    ctx = mok.mok_create(dims())
+    sched = mok.MokSched()          # all null
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_plan(ctx, 16, 16, None, sched, 256, None)
+    assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+    full = mok.MokSched(*([256] * 6), 1000)  # aux not 256-byte aligned
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_plan(ctx, 16, 16, None, full, 256, None)
+    assert ei.value.status == mok.MOK_ERR_WORKSPACE
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_set_precision(ctx, 7)
+    assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+    mok.mok_destroy(ctx)
+
+
+def test_status_strings():
+    for st in (0, -1, -2, -3, -4, -5, -6):
+        assert mok.mok_status_string(st)

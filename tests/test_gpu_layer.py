@@ -1,0 +1,95 @@
+"""GPU parity of the whole layer through the C ABI against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny": mi.CONFIGS["tiny"],
+    # ragged token count, shared expert, several 128-row tiles per expert
+    "ragged_shared": mi.MoEConfig("ragged_shared", T=300, H=256, I=256, E=12, k=3,
+                                  shared_I=128),
+    # most experts empty (zero-row segments, zero dW)
+    "sparse": mi.MoEConfig("sparse", T=64, H=128, I=128, E=64, k=1),
+    "single_token": mi.MoEConfig("single_token", T=1, H=128, I=128, E=4, k=2),
+    # routing supplied by the caller, a token may pick one expert twice
+    "external_routing": mi.MoEConfig("external_routing", T=100, H=256, I=128, E=6, k=8,
+                                     router=False, zipf_s=1.2, macrobatches=0),
+    "mid": mi.CONFIGS["mid"],
+}
+
+
+def _check_route_and_plan(cfg, inp, res, orc_idx, orc_gates, logits):
+    if cfg.router:
+        amb = set(gu.ambiguous_tokens(cfg, inp, logits).tolist())
+        diff = np.where((res["topk_idx"] != orc_idx).any(axis=1))[0]
+        bad = [t for t in diff if t not in amb]
+        assert not bad, f"top-k differs outside near-ties: tokens {bad[:10]}"
+        assert len(diff) == 0, f"near-tie tokens routed differently: {diff[:10]}"
+        assert np.abs(res["gates"] - orc_gates).max() < 1e-5
+        assert np.allclose(res["gates"].sum(1), 1.0, atol=1e-5)
+    pl = gu.moe.plan(orc_idx, cfg.E)
+    assert np.array_equal(res["counts"], pl.counts)
+    assert np.array_equal(res["offsets"], pl.offsets)
+    assert np.array_equal(res["table"], pl.table)
+    assert np.array_equal(res["inv"], pl.inv)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_matches_oracle(name):
+    cfg = CASES[name]
+    inp = gu.gpu_inputs(cfg, seed=0)
+    idx, gates, logits = gu.oracle_route(cfg, inp)
+    res, _ = gu.run_gpu(cfg, inp, backward=True)
+    assert res["status"] == 0
+    _check_route_and_plan(cfg, inp, res, idx, gates, logits)
+    ref = gu.run_oracle(cfg, inp, idx, gates, backward=True)
+    tol = gu.TOL[cfg.precision]
+    fields = ["y", "dX", "dW_up", "dW_gate", "dW_down", "dgates"]
+    if cfg.router:
+        fields.append("dWr")
+    if cfg.shared_I:
+        fields += ["dWs_up", "dWs_gate", "dWs_down"]
+    errs = {f: gu.rel_err(res[f], ref[f]) for f in fields}
+    print(name, errs)
+    for f, e in errs.items():
+        assert e <= tol, (f, e)
+
+
+def test_plan_bit_exact_with_oracle_routing():
+    """The schedule built on the GPU from the oracle's expert ids equals the oracle's."""
+    cfg = mi.MoEConfig("plan_ext", T=999, H=128, I=128, E=37, k=5, router=False)
+    inp = gu.gpu_inputs(cfg, seed=3)
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.choice(37, 5, replace=False) for _ in range(999)])
+    idx[::7, 1] = idx[::7, 0]          # some tokens hit one expert twice
+    g = rng.uniform(0.1, 1, idx.shape)
+    g = g / g.sum(1, keepdims=True)
+    res, _ = gu.run_gpu(cfg, inp, backward=False, routing=(idx, g))
+    pl = gu.moe.plan(idx, cfg.E)
+    for f in ("counts", "offsets", "table", "inv"):
+        assert np.array_equal(res[f], getattr(pl, f)), f
+
+
+def test_bitwise_deterministic_over_10_runs():
+    cfg = CASES["ragged_shared"]
+    inp = gu.gpu_inputs(cfg, seed=1)
+    first, L = gu.run_gpu(cfg, inp)
+    for _ in range(9):
+        again, _ = gu.run_gpu(cfg, inp, layer=L)
+        for f in ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates", "dWr", "dWs_up"):
+            assert torch.equal(torch.as_tensor(first[f]), torch.as_tensor(again[f])), f
+
+
+def test_bad_expert_id_is_flagged():
+    cfg = mi.MoEConfig("bad_id", T=40, H=128, I=128, E=4, k=2, router=False)
+    inp = gu.gpu_inputs(cfg)
+    idx = np.zeros((40, 2), np.int64)
+    idx[3, 1] = 9                       # out of range
+    res, _ = gu.run_gpu(cfg, inp, backward=False, routing=(idx, np.full((40, 2), 0.5)))
+    from grouped_gemm_built_gb300 import mok
+    assert res["status"] == mok.MOK_ERR_DEVICE

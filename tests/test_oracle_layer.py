@@ -254,3 +254,27 @@ def test_empty_experts_get_zero_gradients(rng):
     g = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY)
     assert np.all(g.dW_up[1:] == 0) and np.all(g.dW_down[1:] == 0)
     assert np.abs(g.dW_up[0]).max() > 0
+
+
+def test_sampled_evaluators_match_the_dense_oracle(rng):
+    """Per-token and per-element evaluators (no table, no streaming) against the dense
+    per-expert oracle, bf16 rounding model, shared expert and router path included."""
+    from oracle import sampled
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=14, H=16, I=8, E=5, k=2, shared=True)
+    r = moe.route(x, Wr, 2)
+    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16")
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16",
+                     Wr=Wr)
+    W = lambda e: (Wu[e], Wg[e], Wd[e])
+    for t in range(14):
+        o = sampled.token_outputs(t, x, r.idx, r.gates, W, dY=dY, shared=sh, Wr=Wr)
+        assert np.allclose(o["y"], y[t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(o["dX"], g.dX[t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(o["dgates"], g.dgates[t], rtol=1e-12, atol=1e-12)
+    pl = saved["plan"]
+    for e in range(5):
+        pairs = sampled.expert_rows(pl, e)
+        picks = [("dW_up", 3, 5), ("dW_gate", 15, 0), ("dW_down", 7, 11), ("dW_down", 0, 0)]
+        got = sampled.dw_elements(e, pairs, x, dY, r.gates, Wu[e], Wg[e], Wd[e], picks)
+        ref = [g.dW_up[e, 3, 5], g.dW_gate[e, 15, 0], g.dW_down[e, 7, 11], g.dW_down[e, 0, 0]]
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
