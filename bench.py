@@ -121,9 +121,12 @@ def algorithmic(cfg):
     R = T * k
     f_fwd = 6.0 * H * I * R + 6.0 * H * Is * T + 2.0 * H * E * T
     f_bwd = 12.0 * H * I * R + 12.0 * H * Is * T + 4.0 * H * k * T
-    w_bytes = 2.0 * 3 * H * I * E + 2.0 * 3 * H * Is
-    b_fwd = w_bytes + 2.0 * T * H * 2 + 4.0 * H * E
-    b_bwd = 2 * w_bytes + 2.0 * T * H * 3 + 4.0 * H * E * 2
+    wb = 1.0 if cfg.precision == "mxfp8" else 2.0      # weight element bytes read
+    n_w = 3.0 * H * I * E + 3.0 * H * Is
+    # forward: weights, x (bf16) in, y (fp32) out, router weights
+    b_fwd = wb * n_w + 2.0 * T * H + 4.0 * T * H + 4.0 * H * E
+    # backward: weights in, fp32 weight gradients out, x and dY in, dX (fp32) out, Wr, dWr
+    b_bwd = wb * n_w + 4.0 * n_w + 2.0 * 2 * T * H + 4.0 * T * H + 4.0 * H * E * 2
     return f_fwd, f_bwd, b_fwd, b_bwd
 
 
@@ -132,13 +135,17 @@ def kernel_work(cfg, name, counts=None):
     T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
     R = T * k
     rows = R
+    # (FLOPs, bytes): bf16 operands (2 B), fp32 O / dXg rows and weight gradients (4 B)
     tbl = {
-        "gemm_fwd_upgate_swiglu": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + rows * H + 3 * rows * I)),
-        "gemm_fwd_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I + rows * H)),
-        "gemm_bwd_dh_swiglu": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * H + 5 * rows * I)),
-        "gemm_bwd_dx": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + 2 * rows * I + rows * H)),
-        "gemm_bwd_dw_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I + rows * H)),
-        "gemm_bwd_dw_upgate": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + rows * H + 2 * rows * I)),
+        "gemm_fwd_upgate_swiglu": (4.0 * H * I * rows,
+                                   2.0 * (2 * H * I * E + rows * H + 3 * rows * I)),
+        "gemm_fwd_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I) + 4.0 * rows * H),
+        "gemm_bwd_dh_swiglu": (2.0 * H * I * rows,
+                               2.0 * (H * I * E + rows * H + 5 * rows * I) + 4.0 * rows),
+        "gemm_bwd_dx": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + 2 * rows * I) + 4.0 * rows * H),
+        "gemm_bwd_dw_down": (2.0 * H * I * rows, 2.0 * (rows * I + rows * H) + 4.0 * H * I * E),
+        "gemm_bwd_dw_upgate": (4.0 * H * I * rows,
+                               2.0 * (rows * H + 2 * rows * I) + 4.0 * 2 * H * I * E),
     }
     return tbl.get(name)
 
@@ -173,7 +180,7 @@ def run_gpu(args):
     w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
                   inp["Ws_down"])
     grads = L.alloc_grads()
-    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device="cuda")
     Wr = inp["Wr"]
 
     def step():
@@ -228,8 +235,8 @@ def run_gpu(args):
         hdy = torch.empty_like(inp["dY"], device="cpu").pin_memory()
         hx.copy_(inp["x"])
         hdy.copy_(inp["dY"])
-        hy = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
-        hdx = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+        hy = torch.empty((cfg.T, cfg.H), dtype=torch.float32).pin_memory()
+        hdx = torch.empty((cfg.T, cfg.H), dtype=torch.float32).pin_memory()
         dx_dev = torch.empty_like(inp["x"])
         dy_dev = torch.empty_like(inp["dY"])
 
@@ -261,7 +268,7 @@ def run_gpu(args):
             ms_e2e = float(t.item())
         e2e = {"value": world * cfg.T * k_e2e / (ms_e2e / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": hx.numel() * 2 + hdy.numel() * 2,
-               "d2h_bytes_per_step": hy.numel() * 2 + hdx.numel() * 2,
+               "d2h_bytes_per_step": hy.numel() * 4 + hdx.numel() * 4,
                "steps": k_e2e}
 
     # ------------------------------------------------------------ roofline

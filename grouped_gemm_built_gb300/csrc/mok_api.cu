@@ -118,9 +118,33 @@ FwdWs fwd_ws(const Dims& d) {
   const size_t P = d.P_max;
   L.xg = b.take(2 * P * d.H);
   L.h = b.take(2 * P * d.I);
-  L.o = b.take(2 * P * d.H);
+  L.o = b.take(4 * P * d.H);
   L.hs = b.take(2 * (size_t)d.T * d.Is);
-  L.os = b.take(2 * (size_t)d.T * d.H);
+  L.os = b.take(4 * (size_t)d.T * d.H);
+  L.xq = b.take(P * d.H);
+  L.xsf = b.take(P * d.H / 32);
+  L.hq = b.take(P * d.I);
+  L.hsf = b.take(P * d.I / 32);
+  L.total = b.off;
+  return L;
+}
+
+MxWeights mx_weights_layout(const Dims& d) {
+  Bump b;
+  MxWeights L;
+  const size_t n = (size_t)d.E * d.H * d.I;
+  L.up_h = b.take(n);
+  L.up_h_sf = b.take(n / 32);
+  L.gate_h = b.take(n);
+  L.gate_h_sf = b.take(n / 32);
+  L.down_i = b.take(n);
+  L.down_i_sf = b.take(n / 32);
+  L.down_h = b.take(n);
+  L.down_h_sf = b.take(n / 32);
+  L.up_i = b.take(n);
+  L.up_i_sf = b.take(n / 32);
+  L.gate_i = b.take(n);
+  L.gate_i_sf = b.take(n / 32);
   L.total = b.off;
   return L;
 }
@@ -134,13 +158,29 @@ BwdWs bwd_ws(const Dims& d) {
   L.du = b.take(2 * P * d.I);
   L.dv = b.take(2 * P * d.I);
   L.hg = b.take(2 * P * d.I);
-  L.dxg = b.take(2 * P * d.H);
+  L.dxg = b.take(4 * P * d.H);
   L.dgp = b.take(sizeof(float) * P * gemm_dh_parts(d.I));
   L.dl = b.take(sizeof(float) * (size_t)d.R);
   L.dus = b.take(2 * (size_t)d.T * d.Is);
   L.dvs = b.take(2 * (size_t)d.T * d.Is);
   L.hsg = b.take(2 * (size_t)d.T * d.Is);
-  L.dxs = b.take(2 * (size_t)d.T * d.H + sizeof(float) * (size_t)d.E * d.H);  // + Wr^T
+  L.dxs = b.take(4 * (size_t)d.T * d.H + sizeof(float) * (size_t)d.E * d.H);  // + Wr^T
+  L.q_dy_h = b.take(P * d.H);
+  L.sf_dy_h = b.take(P * d.H / 32);
+  L.q_dy_r = b.take(P * d.H);
+  L.sf_dy_r = b.take(P * d.H / 32);
+  L.q_x_r = b.take(P * d.H);
+  L.sf_x_r = b.take(P * d.H / 32);
+  L.q_du_i = b.take(P * d.I);
+  L.sf_du_i = b.take(P * d.I / 32);
+  L.q_dv_i = b.take(P * d.I);
+  L.sf_dv_i = b.take(P * d.I / 32);
+  L.q_du_r = b.take(P * d.I);
+  L.sf_du_r = b.take(P * d.I / 32);
+  L.q_dv_r = b.take(P * d.I);
+  L.sf_dv_r = b.take(P * d.I / 32);
+  L.q_hg_r = b.take(P * d.I);
+  L.sf_hg_r = b.take(P * d.I / 32);
   L.total = b.off;
   return L;
 }
@@ -249,7 +289,6 @@ void mok_destroy(mok_ctx_t ctx) { delete ctx; }
 mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
   if (p != MOK_BF16 && p != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
-  if (p == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
   ctx->precision = p;
   return MOK_OK;
 }
@@ -264,7 +303,7 @@ mok_status mok_get_sizes(mok_ctx_t ctx, mok_sizes* out) {
   if (b > ws) ws = b;
   out->workspace_bytes = ws;
   out->saved_bytes = saved_layout(d).total;
-  out->mx_weight_bytes = 0;
+  out->mx_weight_bytes = mx_weights_layout(d).total;
   out->padded_rows_max = d.P_max;
   out->macrobatches = 1;
   return MOK_OK;
@@ -354,6 +393,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
   mok_status st = check_sched(d, sched);
   if (st != MOK_OK) return st;
   if ((st = check_weights(d, w)) != MOK_OK) return st;
+  if (ctx->precision == MOK_MXFP8 && (!w->mx || !aligned(w->mx, 256))) return MOK_ERR_INVALID_ARG;
   if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return MOK_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256) || !saved || !aligned(saved, 256))
     return MOK_ERR_WORKSPACE;
@@ -365,24 +405,55 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
   void* xg = at(workspace, L.xg);
   void* h = at(workspace, L.h);
   void* o = at(workspace, L.o);
+  const bool mx = ctx->precision == MOK_MXFP8;
 
-  // dispatch: pull token rows into expert order through the table
-  MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
-  // grouped up|gate GEMM + SwiGLU
-  GemmCall c = routed_call(d, sched, a, kFwdUpGate);
-  c.a0 = xg;
-  c.b0 = w->W_up;
-  c.b1 = w->W_gate;
-  c.out0 = h;
-  c.out1 = at(saved, S.u);
-  c.out2 = at(saved, S.v);
-  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
-  // grouped down GEMM
-  c = routed_call(d, sched, a, kFwdDown);
-  c.a0 = h;
-  c.b0 = w->W_down;
-  c.out0 = o;
-  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  if (!mx) {
+    // dispatch: pull token rows into expert order through the table
+    MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
+    // grouped up|gate GEMM + SwiGLU
+    GemmCall c = routed_call(d, sched, a, kFwdUpGate);
+    c.a0 = xg;
+    c.b0 = w->W_up;
+    c.b1 = w->W_gate;
+    c.out0 = h;
+    c.out1 = at(saved, S.u);
+    c.out2 = at(saved, S.v);
+    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+    // grouped down GEMM
+    c = routed_call(d, sched, a, kFwdDown);
+    c.a0 = h;
+    c.b0 = w->W_down;
+    c.out0 = o;
+    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  } else {
+    MxWeights M = mx_weights_layout(d);
+    char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
+    // dispatch with MXFP8 quantisation along H fused in
+    MOK_LAUNCH("dispatch_gather_mxfp8",
+               launch_gather_quant(d, x, *sched, a, at(workspace, L.xq), at(workspace, L.xsf),
+                                   ctx->num_sms, s));
+    GemmCall c = routed_call(d, sched, a, kFwdUpGate);
+    c.mx = true;
+    c.a0 = at(workspace, L.xq);
+    c.sfa = at(workspace, L.xsf);
+    c.b0 = mxw + M.up_h;
+    c.b1 = mxw + M.gate_h;
+    c.sfb0 = mxw + M.up_h_sf;
+    c.sfb1 = mxw + M.gate_h_sf;
+    c.out_q[0] = at(workspace, L.hq);
+    c.out_sf[0] = at(workspace, L.hsf);
+    c.out1 = at(saved, S.u);
+    c.out2 = at(saved, S.v);
+    MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(c, ctx->num_sms, s));
+    c = routed_call(d, sched, a, kFwdDown);
+    c.mx = true;
+    c.a0 = at(workspace, L.hq);
+    c.sfa = at(workspace, L.hsf);
+    c.b0 = mxw + M.down_i;
+    c.sfb0 = mxw + M.down_i_sf;
+    c.out0 = o;
+    MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(c, ctx->num_sms, s));
+  }
   const void* shared_out = nullptr;
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kFwdUpGate);
@@ -416,6 +487,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   if (!x || !dY || !dX || !aligned(x, 16) || !aligned(dY, 16) || !aligned(dX, 16))
     return MOK_ERR_INVALID_ARG;
   if (!g || !g->dW_up || !g->dW_gate || !g->dW_down || !g->dgates) return MOK_ERR_INVALID_ARG;
+  if (ctx->precision == MOK_MXFP8 && (!w->mx || !aligned(w->mx, 256))) return MOK_ERR_INVALID_ARG;
   if (d.router && (!Wr || !g->dWr)) return MOK_ERR_INVALID_ARG;
   if (!d.router && (Wr || g->dWr)) return MOK_ERR_INVALID_ARG;
   if (d.Is && (!g->dWs_up || !g->dWs_gate || !g->dWs_down)) return MOK_ERR_INVALID_ARG;
@@ -435,28 +507,77 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   float* dgp = reinterpret_cast<float*>(at(workspace, L.dgp));
   float* dl = reinterpret_cast<float*>(at(workspace, L.dl));
 
-  // reverse dispatch of dY and replay of the forward gather, both through the table
-  MOK_LAUNCH("reverse_dispatch_gather", launch_gather_rows(d, dY, *sched, a, dyg, ctx->num_sms, s));
-  MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
-  // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
-  GemmCall c = routed_call(d, sched, a, kBwdDH);
-  c.a0 = dyg;
-  c.b0 = w->W_down;
-  c.aux0 = at(const_cast<void*>(saved), S.u);
-  c.aux1 = at(const_cast<void*>(saved), S.v);
-  c.out0 = du;
-  c.out1 = dv;
-  c.out2 = hg;
-  c.dgp = dgp;
-  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
-  // dXg = du W_up^T + dv W_gate^T
-  c = routed_call(d, sched, a, kBwdDX);
-  c.a0 = du;
-  c.a1 = dv;
-  c.b0 = w->W_up;
-  c.b1 = w->W_gate;
-  c.out0 = dxg;
-  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  const bool mx = ctx->precision == MOK_MXFP8;
+  MxWeights M = mx_weights_layout(d);
+  char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
+  auto W = [&](size_t off) -> void* { return at(workspace, off); };
+  if (!mx) {
+    // reverse dispatch of dY and replay of the forward gather, both through the table
+    MOK_LAUNCH("reverse_dispatch_gather", launch_gather_rows(d, dY, *sched, a, dyg, ctx->num_sms, s));
+    MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
+    // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
+    GemmCall c = routed_call(d, sched, a, kBwdDH);
+    c.a0 = dyg;
+    c.b0 = w->W_down;
+    c.aux0 = at(const_cast<void*>(saved), S.u);
+    c.aux1 = at(const_cast<void*>(saved), S.v);
+    c.out0 = du;
+    c.out1 = dv;
+    c.out2 = hg;
+    c.dgp = dgp;
+    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+    // dXg = du W_up^T + dv W_gate^T
+    c = routed_call(d, sched, a, kBwdDX);
+    c.a0 = du;
+    c.a1 = dv;
+    c.b0 = w->W_up;
+    c.b1 = w->W_gate;
+    c.out0 = dxg;
+    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  } else {
+    // reverse dispatch of dY (blocks along H for the dH GEMM, 32-row blocks for dW_down)
+    // and replay of x (32-row blocks for dW_up / dW_gate), all through the table
+    MOK_LAUNCH("reverse_dispatch_gather_mxfp8",
+               launch_gather_quant(d, dY, *sched, a, W(L.q_dy_h), W(L.sf_dy_h), ctx->num_sms, s));
+    MOK_LAUNCH("reverse_dispatch_gather_rows_mxfp8",
+               launch_gather_quant_rows(d, dY, *sched, a, W(L.q_dy_r), W(L.sf_dy_r),
+                                        ctx->num_sms, s));
+    MOK_LAUNCH("replay_gather_rows_mxfp8",
+               launch_gather_quant_rows(d, x, *sched, a, W(L.q_x_r), W(L.sf_x_r), ctx->num_sms,
+                                        s));
+    GemmCall c = routed_call(d, sched, a, kBwdDH);
+    c.mx = true;
+    c.a0 = W(L.q_dy_h);
+    c.sfa = W(L.sf_dy_h);
+    c.b0 = mxw + M.down_h;
+    c.sfb0 = mxw + M.down_h_sf;
+    c.aux0 = at(const_cast<void*>(saved), S.u);
+    c.aux1 = at(const_cast<void*>(saved), S.v);
+    c.out_q[0] = W(L.q_du_i);
+    c.out_sf[0] = W(L.sf_du_i);
+    c.out_q[1] = W(L.q_dv_i);
+    c.out_sf[1] = W(L.sf_dv_i);
+    c.out_q[2] = W(L.q_du_r);
+    c.out_sf[2] = W(L.sf_du_r);
+    c.out_q[3] = W(L.q_dv_r);
+    c.out_sf[3] = W(L.sf_dv_r);
+    c.out_q[4] = W(L.q_hg_r);
+    c.out_sf[4] = W(L.sf_hg_r);
+    c.dgp = dgp;
+    MOK_LAUNCH("gemm_bwd_dh_swiglu_mxfp8", launch_gemm(c, ctx->num_sms, s));
+    c = routed_call(d, sched, a, kBwdDX);
+    c.mx = true;
+    c.a0 = W(L.q_du_i);
+    c.sfa = W(L.sf_du_i);
+    c.a1 = W(L.q_dv_i);
+    c.sfa1 = W(L.sf_dv_i);
+    c.b0 = mxw + M.up_i;
+    c.sfb0 = mxw + M.up_i_sf;
+    c.b1 = mxw + M.gate_i;
+    c.sfb1 = mxw + M.gate_i_sf;
+    c.out0 = dxg;
+    MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(c, ctx->num_sms, s));
+  }
   // router-weight gradient and the renormalised-softmax backward
   MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I), *sched, a,
                                                 g->dgates, d.router ? dl : nullptr, s));
@@ -481,23 +602,30 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     dxs = at(workspace, L.dxs);
   }
   // dX: reverse combine in slot order (+ shared expert, + router path)
-  float* wrt = reinterpret_cast<float*>(at(workspace, L.dxs + 2 * (size_t)d.T * d.H));
+  float* wrt = reinterpret_cast<float*>(at(workspace, L.dxs + 4 * (size_t)d.T * d.H));
   if (d.router) MOK_LAUNCH("transpose_wr", launch_transpose_wr(d, Wr, wrt, s));
   MOK_LAUNCH("reverse_combine", launch_reverse_combine(d, dxg, *sched, a, dxs,
                                                        d.router ? dl : nullptr, wrt, dX, s));
   // weight gradients, each a fixed-order sum over the expert's rows
-  c = routed_call(d, sched, a, kBwdDWUpGate);
-  c.a0 = xg;
-  c.b0 = du;
-  c.b1 = dv;
+  GemmCall c = routed_call(d, sched, a, kBwdDWUpGate);
+  c.mx = mx;
+  c.a0 = mx ? W(L.q_x_r) : xg;
+  c.b0 = mx ? W(L.q_du_r) : du;
+  c.b1 = mx ? W(L.q_dv_r) : dv;
+  c.sfa = W(L.sf_x_r);
+  c.sfb0 = W(L.sf_du_r);
+  c.sfb1 = W(L.sf_dv_r);
   c.out0 = g->dW_up;
   c.out1 = g->dW_gate;
-  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
   c = routed_call(d, sched, a, kBwdDWDown);
-  c.a0 = hg;
-  c.b0 = dyg;
+  c.mx = mx;
+  c.a0 = mx ? W(L.q_hg_r) : hg;
+  c.b0 = mx ? W(L.q_dy_r) : dyg;
+  c.sfa = W(L.sf_hg_r);
+  c.sfb0 = W(L.sf_dy_r);
   c.out0 = g->dW_down;
-  MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDWUpGate);
     cs.a0 = x;
@@ -518,11 +646,32 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
 
 mok_status mok_quantize_weights_mxfp8(mok_ctx_t ctx, const mok_weights* w, void* mx_out,
                                       void* stream) {
-  (void)w;
-  (void)mx_out;
-  (void)stream;
   if (!ctx) return MOK_ERR_INVALID_ARG;
-  return MOK_ERR_UNSUPPORTED;
+  const Dims& d = ctx->d;
+  mok_status st = check_weights(d, w);
+  if (st != MOK_OK) return st;
+  if (!mx_out || !aligned(mx_out, 256)) return MOK_ERR_INVALID_ARG;
+  if (ctx->num_sms <= 0) return MOK_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights M = mx_weights_layout(d);
+  char* o = static_cast<char*>(mx_out);
+  // W_up / W_gate [E][H][I]: blocks along H (the rows), atoms [e][H/128][I/128]
+  MOK_LAUNCH("quant_w_up", launch_mx_quant(w->W_up, d.H, d.I, d.E, false, o + M.up_h,
+                                           o + M.up_h_sf, d.I / 128, 1, s));
+  MOK_LAUNCH("quant_w_gate", launch_mx_quant(w->W_gate, d.H, d.I, d.E, false, o + M.gate_h,
+                                             o + M.gate_h_sf, d.I / 128, 1, s));
+  // W_down [E][I][H]: blocks along I (the rows), atoms [e][I/128][H/128]
+  MOK_LAUNCH("quant_w_down", launch_mx_quant(w->W_down, d.I, d.H, d.E, false, o + M.down_i,
+                                             o + M.down_i_sf, d.H / 128, 1, s));
+  // backward copies: W_down along H (dH GEMM, N = I), W_up / W_gate along I (dX GEMM,
+  // N = H); atoms [e][K/128][N/128]
+  MOK_LAUNCH("quant_w_down_h", launch_mx_quant(w->W_down, d.I, d.H, d.E, true, o + M.down_h,
+                                               o + M.down_h_sf, d.I / 128, 1, s));
+  MOK_LAUNCH("quant_w_up_i", launch_mx_quant(w->W_up, d.H, d.I, d.E, true, o + M.up_i,
+                                             o + M.up_i_sf, d.H / 128, 1, s));
+  MOK_LAUNCH("quant_w_gate_i", launch_mx_quant(w->W_gate, d.H, d.I, d.E, true, o + M.gate_i,
+                                               o + M.gate_i_sf, d.H / 128, 1, s));
+  return MOK_OK;
 }
 
 mok_status mok_get_status(mok_ctx_t ctx, const mok_sched* sched, void* stream) {

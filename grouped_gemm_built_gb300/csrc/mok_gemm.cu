@@ -2,15 +2,19 @@
 //
 // Expert FFN (sebask.de MoK article, intro: up, gate and down projection; stamatios.com,
 // "Outras caracteristicas": SwiGLU, router-weight gradient fused into the SwiGLU
-// backward). One persistent, warp-specialised kernel serves every GEMM of the layer:
+// backward, MXFP8 with a BF16 shared expert). One persistent, warp-specialised kernel
+// serves every GEMM of the layer:
 //
-//   warp 0      TMA producer: one elected lane streams A/B tiles into a 4-stage ring of
-//               shared-memory buffers (128-byte swizzle), mbarrier-tracked;
-//   warp 1      MMA issuer: allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and issues tcgen05.mma (M=128, N=256, K=16) from one lane;
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output row),
-//               apply the mode's fused math, store bf16 rows; the accumulator is handed
-//               back so the next tile's MMAs overlap this tile's epilogue.
+//   warp 0      TMA producer: one lane streams A/B tiles (and, in MXFP8, their scale
+//               atoms) into a 4-stage ring of shared-memory buffers (128-byte swizzle);
+//   warp 1      MMA issuer: allocates 512 TMEM columns and issues tcgen05.mma
+//               (M=128, N=256) from one lane; BF16: kind::f16, K=16 per instruction, two
+//               256-column accumulators; MXFP8: kind::mxf8f6f4.block_scale, K=32 per
+//               instruction, one accumulator plus per-stage scale columns filled by
+//               tcgen05.cp;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output row), run
+//               the mode's fused math, store rows; with two accumulators the next tile's
+//               MMAs overlap this tile's epilogue.
 //
 // Tiles of the routed row space are 128 rows of one expert (segments are padded to 128
 // rows by the schedule), so a tile never mixes experts. Each output element is one fp32
@@ -19,6 +23,7 @@
 // word, drains its outstanding copies and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -33,28 +38,39 @@ namespace mok {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;                      // bf16 elements per 128-byte swizzle row
 constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = 256 * BK * 2;       // 32 KB (N up to 256)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = 16384;              // 128 rows x 128 bytes
+constexpr int B_BYTES = 32768;              // 256 rows x 128 bytes
 constexpr int TMEM_COLS = 512;
-constexpr int ACC_COLS = 256;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+template <bool MX>
+struct Cfg {
+  static constexpr int BK = MX ? 128 : 64;           // K elements per stage (128 bytes/row)
+  static constexpr int MMA_K = MX ? 32 : 16;         // K elements per instruction
+  static constexpr int MN_CHUNK = MX ? 128 : 64;     // elements per 128-byte MN-major chunk
+  static constexpr int MN_LBO = BK * 128;            // bytes between MN chunks in smem
+  static constexpr int MN_KSTEP = MMA_K * 128;       // bytes per instruction along K, MN-major
+  static constexpr int SF_OFF = A_BYTES + B_BYTES;   // scale atoms: A 512 B, B 1024 B
+  static constexpr int STAGE_BYTES = MX ? 51200 : 49152;
+  static constexpr int NACC = MX ? 1 : 2;
+  static constexpr int ACC_COLS = 256;
+  static constexpr int SF_TMEM = 256;                // MX: scale columns start here
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+};
 
 struct Params {
   int mode;
   int dense;        // 1: one group over M_rows rows (shared expert)
-  int M_rows;       // dense rows (T)
+  int M_rows;       // rows of the row space (dense: T)
   int H, I;         // hidden, intermediate of this FFN
   int k;            // top-k (gate lookup)
   int BN;           // MMA N (256 or 128)
   int n_tiles;      // tiles along N
   int m_tiles_dw;   // dW modes: tiles along M of one expert's dW
   int groups;
-  int kiters;       // row-space modes: K / 64
+  int kiters;       // row-space modes: K / BK
   // schedule
   const int32_t* poff;
   const int32_t* counts;
@@ -69,15 +85,27 @@ struct Params {
   __nv_bfloat16* out2;
   const __nv_bfloat16* aux0;
   const __nv_bfloat16* aux1;
+  float* outf0;     // fp32 outputs: O / dXg rows, dW (dW_up, dW_gate)
+  float* outf1;
   float* dgp;
   uint32_t* status;
+  // MXFP8 scale atoms (512 B each): A side [row tile][kcs_a], B side [e][kcs_b][ncs_b]
+  const uint8_t* sfa;
+  const uint8_t* sfb0;
+  const uint8_t* sfb1;
+  int kcs_a, kcs_b, ncs_b;
+  const uint8_t* sfa1;  // second A operand's atoms (kBwdDX: dv)
+  // MX outputs. kFwdUpGate: q[0] = h along I. kBwdDH: q[0], q[1] = du, dv along I;
+  // q[2], q[3], q[4] = du, dv, g*h in 32-row blocks. E4M3 [rows][I], atoms [row tile][I/128].
+  uint8_t* out_q[5];
+  uint8_t* out_sf[5];
 };
 
 struct TileInfo {
   int e;        // expert (0 when dense)
   int row0;     // first row of the row space (row-space modes) / first dW row (dW modes)
   int n0;       // first output column
-  int kiters;   // K iterations of 64
+  int kiters;   // K iterations
   int krow0;    // dW modes: first row of the contraction range
 };
 
@@ -90,7 +118,9 @@ __device__ __forceinline__ int num_tiles_of(const Params& p) {
   return mt * p.n_tiles;
 }
 
+template <bool MX>
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
+  constexpr int BK = Cfg<MX>::BK;
   TileInfo ti;
   if (is_dw(p.mode)) {
     const int per_e = p.m_tiles_dw * p.n_tiles;
@@ -132,6 +162,11 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
     d[q] = w;
   }
 }
+__device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -148,17 +183,46 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v)
 }
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.f / (1.f + __expf(-v)); }
 
+// MXFP8 block of 32 (one thread's chunk): returns the scale byte, writes 32 E4M3 codes.
+__device__ __forceinline__ uint32_t quant32_e4m3(const float* v, uint4* q2) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  uint32_t sb = 127u;
+  if (amax != 0.f) {
+    const int b = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 8;
+    sb = (uint32_t)(b < 0 ? 0 : b);
+  }
+  const float inv = __uint_as_float((254u - sb) << 23);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    w[i] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  q2[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  q2[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return sb;
+}
+
 // ------------------------------------------------------------------ producer
+template <bool MX>
 __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorMap* tA1,
                         const CUtensorMap* tB0, const CUtensorMap* tB1, uint8_t* smem,
                         uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+  using C = Cfg<MX>;
+  constexpr int BK = C::BK;
+  constexpr int CH = C::MN_LBO;        // bytes of one MN-major chunk
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
-  const uint32_t b_bytes = (p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 256 * BK * 2
-                                                                              : p.BN * BK * 2;
+  uint32_t b_bytes = (p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 256 * 128 : p.BN * 128;
+  if (MX) b_bytes += 512 + ((p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 1024 : p.BN * 4);
   bool ok = true;
   for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-    const TileInfo ti = tile_info(p, tile);
+    const TileInfo ti = tile_info<MX>(p, tile);
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
       const uint32_t round = it / STAGES;
@@ -168,63 +232,98 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
         ok = false;
         break;
       }
-      uint8_t* sa = smem + stage * STAGE_BYTES;
+      uint8_t* sa = smem + stage * C::STAGE_BYTES;
       uint8_t* sb = sa + A_BYTES;
-      mbar_arrive_expect_tx(&full[stage], A_BYTES + b_bytes);
+      uint8_t* sf = sa + C::SF_OFF;
+      uint64_t* bar = &full[stage];
+      mbar_arrive_expect_tx(bar, A_BYTES + b_bytes);
       const int k0 = kb * BK;
       switch (p.mode) {
         case kFwdUpGate: {   // A: Xg rows (K-major); B: W_up|W_gate cols n0..n0+127 (MN-major)
-          tma_load_2d(sa, tA0, &full[stage], k0, ti.row0);
+          tma_load_2d(sa, tA0, bar, k0, ti.row0);
           const int brow = ti.e * p.H + k0;
-          tma_load_2d(sb + 0 * 8192, tB0, &full[stage], ti.n0, brow);
-          tma_load_2d(sb + 1 * 8192, tB0, &full[stage], ti.n0 + 64, brow);
-          tma_load_2d(sb + 2 * 8192, tB1, &full[stage], ti.n0, brow);
-          tma_load_2d(sb + 3 * 8192, tB1, &full[stage], ti.n0 + 64, brow);
+          for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
+            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, brow);
+            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, tB1, bar, ti.n0 + c * C::MN_CHUNK, brow);
+          }
+          if (MX) {
+            bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
+            const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
+            bulk_load(sf + 512, p.sfb0 + bi, 512, bar);
+            bulk_load(sf + 1024, p.sfb1 + bi, 512, bar);
+          }
           break;
         }
         case kFwdDown: {     // A: h rows (K-major); B: W_down cols (MN-major)
-          tma_load_2d(sa, tA0, &full[stage], k0, ti.row0);
+          tma_load_2d(sa, tA0, bar, k0, ti.row0);
           const int brow = ti.e * p.I + k0;
-          for (int c = 0; c < p.BN / 64; ++c)
-            tma_load_2d(sb + c * 8192, tB0, &full[stage], ti.n0 + 64 * c, brow);
+          for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
+            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, brow);
+          if (MX) {
+            bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
+            const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
+            bulk_load(sf + 512, p.sfb0 + bi, p.BN * 4, bar);
+          }
           break;
         }
         case kBwdDH: {       // A: dYg rows (K-major); B: W_down rows i (K-major over H)
-          tma_load_2d(sa, tA0, &full[stage], k0, ti.row0);
-          tma_load_2d(sb, tB0, &full[stage], k0, ti.e * p.I + ti.n0);
+          tma_load_2d(sa, tA0, bar, k0, ti.row0);
+          tma_load_2d(sb, tB0, bar, k0, ti.e * p.I + ti.n0);
+          if (MX) {
+            bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
+            const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
+            bulk_load(sf + 512, p.sfb0 + bi, p.BN * 4, bar);
+          }
           break;
         }
         case kBwdDX: {       // K = [I of du | I of dv]; B: W_up / W_gate rows h (K-major over I)
           const int half = p.I / BK;
           const bool second = kb >= half;
-          const int kk = (second ? kb - half : kb) * BK;
-          tma_load_2d(sa, second ? tA1 : tA0, &full[stage], kk, ti.row0);
-          tma_load_2d(sb, second ? tB1 : tB0, &full[stage], kk, ti.e * p.H + ti.n0);
+          const int kq = second ? kb - half : kb;
+          tma_load_2d(sa, second ? tA1 : tA0, bar, kq * BK, ti.row0);
+          tma_load_2d(sb, second ? tB1 : tB0, bar, kq * BK, ti.e * p.H + ti.n0);
+          if (MX) {
+            bulk_load(sf, (second ? p.sfa1 : p.sfa) + ((size_t)(ti.row0 / BM) * p.kcs_a + kq) * 512,
+                      512, bar);
+            const size_t bi = (((size_t)ti.e * p.kcs_b + kq) * p.ncs_b + ti.n0 / 128) * 512;
+            bulk_load(sf + 512, (second ? p.sfb1 : p.sfb0) + bi, p.BN * 4, bar);
+          }
           break;
         }
         case kBwdDWDown: {   // A: (g h)^T (MN-major, M = I); B: dYg (MN-major, N = H)
           const int kr = ti.krow0 + k0;
-          tma_load_2d(sa, tA0, &full[stage], ti.row0, kr);
-          tma_load_2d(sa + 8192, tA0, &full[stage], ti.row0 + 64, kr);
-          for (int c = 0; c < p.BN / 64; ++c)
-            tma_load_2d(sb + c * 8192, tB0, &full[stage], ti.n0 + 64 * c, kr);
+          for (int c = 0; c < BM / C::MN_CHUNK; ++c)
+            tma_load_2d(sa + c * CH, tA0, bar, ti.row0 + c * C::MN_CHUNK, kr);
+          for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
+            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, kr);
+          if (MX) {   // row-block atoms [row tile][M/128] and [row tile][N/128]
+            bulk_load(sf, p.sfa + ((size_t)(kr / BM) * (p.I / 128) + ti.row0 / 128) * 512, 512, bar);
+            bulk_load(sf + 512, p.sfb0 + ((size_t)(kr / BM) * (p.H / 128) + ti.n0 / 128) * 512,
+                      p.BN * 4, bar);
+          }
           break;
         }
         default: {           // kBwdDWUpGate: A: Xg^T (M = H); B: du | dv cols n0..n0+127
           const int kr = ti.krow0 + k0;
-          tma_load_2d(sa, tA0, &full[stage], ti.row0, kr);
-          tma_load_2d(sa + 8192, tA0, &full[stage], ti.row0 + 64, kr);
-          tma_load_2d(sb + 0 * 8192, tB0, &full[stage], ti.n0, kr);
-          tma_load_2d(sb + 1 * 8192, tB0, &full[stage], ti.n0 + 64, kr);
-          tma_load_2d(sb + 2 * 8192, tB1, &full[stage], ti.n0, kr);
-          tma_load_2d(sb + 3 * 8192, tB1, &full[stage], ti.n0 + 64, kr);
+          for (int c = 0; c < BM / C::MN_CHUNK; ++c)
+            tma_load_2d(sa + c * CH, tA0, bar, ti.row0 + c * C::MN_CHUNK, kr);
+          for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
+            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, kr);
+            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, tB1, bar, ti.n0 + c * C::MN_CHUNK, kr);
+          }
+          if (MX) {
+            bulk_load(sf, p.sfa + ((size_t)(kr / BM) * (p.H / 128) + ti.row0 / 128) * 512, 512, bar);
+            const size_t bi = ((size_t)(kr / BM) * (p.I / 128) + ti.n0 / 128) * 512;
+            bulk_load(sf + 512, p.sfb0 + bi, 512, bar);
+            bulk_load(sf + 1024, p.sfb1 + bi, 512, bar);
+          }
           break;
         }
       }
     }
   }
-  // Drain: make sure every issued copy has landed and every MMA commit has arrived
-  // before the CTA's shared memory goes away.
+  // Drain: every issued copy has landed and every MMA commit has arrived before the
+  // CTA's shared memory goes away.
   const uint32_t n_armed = it;
   for (uint32_t s = 0; s < STAGES && s < n_armed; ++s) {
     const uint32_t last = ((n_armed - 1 - s) / STAGES) * STAGES + s;  // last use of stage s
@@ -237,13 +336,14 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
 }
 
 // ------------------------------------------------------------------ MMA issuer
+template <bool MX>
 __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                           uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
                           volatile int* abort_flag) {
+  using C = Cfg<MX>;
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
-  // operand majorness and descriptor strides per mode
   bool a_mn = false, b_mn = false;
   int n_mma = p.BN;
   switch (p.mode) {
@@ -256,16 +356,16 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
   }
   const uint32_t idesc = idesc_bf16(BM, n_mma, a_mn, b_mn);
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-    const TileInfo ti = tile_info(p, tile);
-    const int acc = local & 1;
-    const uint32_t use = local >> 1;
+    const TileInfo ti = tile_info<MX>(p, tile);
+    const int acc = local % C::NACC;
+    const uint32_t use = local / C::NACC;
     if (use > 0 && !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + kTimeoutNs)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
       return;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+    const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
       const uint32_t round = it / STAGES;
@@ -275,18 +375,32 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
         return;
       }
       tc_fence_after();
-      const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+      const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
       const uint32_t sb = sa + A_BYTES;
+      uint32_t t_sfa = 0, t_sfb = 0;
+      if (MX) {
+        // scale atoms -> TMEM: A in 4 columns, B in 4 columns per 128 rows of N
+        const uint32_t col = C::SF_TMEM + stage * 16;
+        t_sfa = tmem_base + col;
+        t_sfb = tmem_base + col + 4;
+        tmem_cp_32x128b_x4(t_sfa, smem_desc_rows16(sa + C::SF_OFF));
+        for (int j = 0; j < n_mma / 128; ++j)
+          tmem_cp_32x128b_x4(t_sfb + 4 * j, smem_desc_rows16(sa + C::SF_OFF + 512 + 512 * j));
+      }
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk) {
-        // K-major: the k-th 16-element slice starts 32 bytes further along the row.
-        // MN-major: it starts 16 rows (2048 bytes) further; 64-element MN chunks are
-        // 8 KB apart (leading byte offset), 8-row groups 1 KB apart (stride offset).
-        const uint64_t ad = a_mn ? umma_desc_sw128(sa + kk * 2048, 8192, 1024)
+      for (int kk = 0; kk < 4; ++kk) {
+        // K-major: the kk-th K slice starts 32 bytes further along each 128-byte row.
+        // MN-major: it starts MMA_K rows further; 128-byte MN chunks are MN_LBO apart
+        // (leading byte offset), 8-row groups 1 KB apart (stride byte offset).
+        const uint64_t ad = a_mn ? umma_desc_sw128(sa + kk * C::MN_KSTEP, C::MN_LBO, 1024)
                                  : umma_desc_sw128(sa + kk * 32, 16, 1024);
-        const uint64_t bd = b_mn ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
+        const uint64_t bd = b_mn ? umma_desc_sw128(sb + kk * C::MN_KSTEP, C::MN_LBO, 1024)
                                  : umma_desc_sw128(sb + kk * 32, 16, 1024);
-        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+        if (MX)
+          umma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, n_mma, a_mn, b_mn, kk), t_sfa, t_sfb, accum);
+        else
+          umma_bf16(d_tmem, ad, bd, idesc, accum);
       }
       umma_commit(&empty[stage]);   // frees the stage once these MMAs have read it
     }
@@ -296,24 +410,26 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
 }
 
 // ------------------------------------------------------------------ epilogue
+template <bool MX>
 __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empty,
                          uint32_t tmem_base, volatile int* abort_flag) {
+  using C = Cfg<MX>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
   const int r = quarter * 32 + lane;        // row inside the tile
   const int ntiles = num_tiles_of(p);
   int local = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-    const TileInfo ti = tile_info(p, tile);
-    const int acc = local & 1;
-    const uint32_t use = local >> 1;
+    const TileInfo ti = tile_info<MX>(p, tile);
+    const int acc = local % C::NACC;
+    const uint32_t use = local / C::NACC;
     if (!mbar_wait(&acc_full[acc], use & 1, globaltimer_ns() + kTimeoutNs)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
       return;
     }
     tc_fence_after();
-    const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t t_row = tmem_base + acc * C::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
     const bool have = ti.kiters > 0;
     float a[32], b[32];
     // tcgen05.ld is warp-collective: every lane loads, rows outside the problem only
@@ -323,6 +439,7 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
     switch (p.mode) {
       case kFwdUpGate: {
         const size_t o = (size_t)row * p.I + ti.n0;
+        uint32_t sbytes = 0;
         for (int c = 0; c < 4; ++c) {
           tmem_ld32(t_row + c * 32, a);          // U
           tmem_ld32(t_row + 128 + c * 32, b);    // V
@@ -330,18 +447,31 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
-          store_bf16x32(p.out0 + o + c * 32, h);
+          if (MX) {   // h feeds the down GEMM as MXFP8 blocks of 32 along I
+            uint4 q[2];
+            sbytes |= quant32_e4m3(h, q) << (8 * c);
+            uint4* dq = reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32);
+            dq[0] = q[0];
+            dq[1] = q[1];
+          } else {
+            store_bf16x32(p.out0 + o + c * 32, h);
+          }
           store_bf16x32(p.out1 + o + c * 32, a);
           store_bf16x32(p.out2 + o + c * 32, b);
+        }
+        if (MX && valid) {
+          const size_t atom = (size_t)(row / BM) * (p.I / 128) + ti.n0 / 128;
+          *reinterpret_cast<uint32_t*>(p.out_sf[0] + atom * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
+              sbytes;
         }
         break;
       }
       case kFwdDown:
-      case kBwdDX: {
+      case kBwdDX: {   // expert outputs / routed dX rows, fp32
         const size_t o = (size_t)row * p.H + ti.n0;
         for (int c = 0; c < p.BN / 32; ++c) {
           tmem_ld32(t_row + c * 32, a);
-          if (valid) store_bf16x32(p.out0 + o + c * 32, a);
+          if (valid) store_f32x32(p.outf0 + o + c * 32, a);
         }
         break;
       }
@@ -375,26 +505,98 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
             dv[i] = dh * u[i] * (sg * (1.f + v[i] * (1.f - sg)));
             hg[i] = g * hv;
           }
-          store_bf16x32(p.out0 + o + c * 32, du);
-          store_bf16x32(p.out1 + o + c * 32, dv);
-          store_bf16x32(p.out2 + o + c * 32, hg);
+          if (!MX) {
+            store_bf16x32(p.out0 + o + c * 32, du);
+            store_bf16x32(p.out1 + o + c * 32, dv);
+            store_bf16x32(p.out2 + o + c * 32, hg);
+          } else {
+            // du, dv feed the dX GEMM (K = I): per-thread blocks of 32 along I
+            const int col = ti.n0 + c * 32;
+            const size_t atom_i = ((size_t)(row / BM) * (p.I / 128) + col / 128) * 512 +
+                                  16 * (r & 31) + 4 * (r >> 5) + ((col & 127) >> 5);
+            uint4 q[2];
+            p.out_sf[0][atom_i] = (uint8_t)quant32_e4m3(du, q);
+            reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32)[0] = q[0];
+            reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32)[1] = q[1];
+            p.out_sf[1][atom_i] = (uint8_t)quant32_e4m3(dv, q);
+            reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[0] = q[0];
+            reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[1] = q[1];
+          }
+        }
+        if (MX) {
+          // du, dv, g*h feed the dW GEMMs (K = rows): blocks of the warp's 32 rows. Every
+          // lane takes part (invalid rows are zero), so the warp reductions stay converged.
+          for (int c = 0; c < p.BN / 32; ++c) {
+            const int col = ti.n0 + c * 32;
+            const size_t o2 = (size_t)row * p.I + col;
+            float u[32], v[32];
+            tmem_ld32(t_row + c * 32, a);
+            if (valid) {
+              load_bf16x32(p.aux0 + o2, u);
+              load_bf16x32(p.aux1 + o2, v);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) u[i] = v[i] = 0.f;
+            }
+            const size_t atom_r = ((size_t)(row / BM) * (p.I / 128) + col / 128) * 512 +
+                                  16 * (lane & 31) + 4 * (((col & 127) + lane) >> 5) + quarter;
+            for (int out = 0; out < 3; ++out) {
+              float x[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float sg = sigmoidf_(v[i]);
+                const float sl = v[i] * sg;
+                const float dh = valid ? g * a[i] : 0.f;
+                x[i] = out == 0 ? dh * sl
+                     : out == 1 ? dh * u[i] * (sg * (1.f + v[i] * (1.f - sg)))
+                                : (valid ? g * sl * u[i] : 0.f);
+              }
+              uint32_t w[8];
+              uint32_t my_sb = 127u;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[i])));
+                uint32_t sb = 127u;
+                if (am != 0u) {
+                  const int bb = (int)((am >> 23) & 0xFF) - 8;
+                  sb = (uint32_t)(bb < 0 ? 0 : bb);
+                }
+                if (i == lane) my_sb = sb;
+                const float inv = __uint_as_float((254u - sb) << 23);
+                const uint32_t code =
+                    __nv_cvt_float2_to_fp8x2(make_float2(x[i] * inv, 0.f), __NV_SATFINITE, __NV_E4M3) &
+                    0xFFu;
+                if ((i & 3) == 0) w[i >> 2] = 0;
+                w[i >> 2] |= code << (8 * (i & 3));
+              }
+              if (valid) {
+                uint4* dq = reinterpret_cast<uint4*>(p.out_q[2 + out] + o2);
+                dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              } else if (!p.dense) {   // padding rows of the row space: zero codes
+                uint4* dq = reinterpret_cast<uint4*>(p.out_q[2 + out] + o2);
+                dq[0] = dq[1] = make_uint4(0, 0, 0, 0);
+              }
+              p.out_sf[2 + out][atom_r] = (uint8_t)my_sb;
+            }
+          }
         }
         if (valid && p.dgp) p.dgp[(size_t)row * p.n_tiles + ti.n0 / p.BN] = dg;
         break;
       }
-      case kBwdDWDown: {                         // row = i index of dW_down[e]
-        __nv_bfloat16* dst = p.out0 + ((size_t)ti.e * p.I + row) * p.H + ti.n0;
+      case kBwdDWDown: {                         // row = i index of dW_down[e], fp32
+        float* dst = p.outf0 + ((size_t)ti.e * p.I + row) * p.H + ti.n0;
         for (int c = 0; c < p.BN / 32; ++c) {
           if (have) tmem_ld32(t_row + c * 32, a);
           else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = 0.f;
           }
-          store_bf16x32(dst + c * 32, a);
+          store_f32x32(dst + c * 32, a);
         }
         break;
       }
-      default: {                                 // kBwdDWUpGate; row = h index
+      default: {                                 // kBwdDWUpGate; row = h index, fp32
         const size_t o = ((size_t)ti.e * p.H + row) * p.I + ti.n0;
         for (int c = 0; c < 4; ++c) {
           if (have) {
@@ -404,8 +606,8 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.f;
           }
-          store_bf16x32(p.out0 + o + c * 32, a);
-          store_bf16x32(p.out1 + o + c * 32, b);
+          store_f32x32(p.outf0 + o + c * 32, a);
+          store_f32x32(p.outf1 + o + c * 32, b);
         }
         break;
       }
@@ -415,13 +617,15 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
   }
 }
 
+template <bool MX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant__ CUtensorMap tA1,
                         const __grid_constant__ CUtensorMap tB0, const __grid_constant__ CUtensorMap tB1,
                         const Params p) {
+  using C = Cfg<MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -450,12 +654,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (threadIdx.x == 0) produce(p, &tA0, &tA1, &tB0, &tB1, smem, full, empty, abort_flag);
+    if (threadIdx.x == 0) produce<MX>(p, &tA0, &tA1, &tB0, &tB1, smem, full, empty, abort_flag);
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0)
-      mma_issue(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag);
+      mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag);
   } else {
-    epilogue(p, acc_full, acc_empty, tmem_base, abort_flag);
+    epilogue<MX>(p, acc_full, acc_empty, tmem_base, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -486,33 +690,35 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box (64 cols, box_rows rows),
-// 128-byte swizzle; reads outside the matrix return zeros.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, int box_rows) {
+// 2-D tensor map over a row-major [rows][cols] matrix of 1- or 2-byte elements, box
+// (128 bytes of columns, box_rows rows), 128-byte swizzle; reads outside return zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, int box_rows,
+              int elem_bytes) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc || base == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {cols * elem_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                   2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-int gemm_dh_parts(int I) { return (I % 256 == 0) ? I / 256 : I / 128; }
-
-cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s) {
+template <bool MX>
+cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
+  using C = Cfg<MX>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (MX && c.dense) return cudaErrorNotSupported;  // the shared expert stays BF16
   Params p;
   memset(&p, 0, sizeof(p));
   p.mode = c.mode;
@@ -534,10 +740,21 @@ cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.out2 = static_cast<__nv_bfloat16*>(c.out2);
   p.aux0 = static_cast<const __nv_bfloat16*>(c.aux0);
   p.aux1 = static_cast<const __nv_bfloat16*>(c.aux1);
+  p.outf0 = static_cast<float*>(c.out0);
+  p.outf1 = static_cast<float*>(c.out1);
   p.dgp = c.dgp;
   p.status = c.status;
+  p.sfa = static_cast<const uint8_t*>(c.sfa);
+  p.sfb0 = static_cast<const uint8_t*>(c.sfb0);
+  p.sfb1 = static_cast<const uint8_t*>(c.sfb1);
+  p.sfa1 = static_cast<const uint8_t*>(c.sfa1);
+  for (int i = 0; i < 5; ++i) {
+    p.out_q[i] = static_cast<uint8_t*>(c.out_q[i]);
+    p.out_sf[i] = static_cast<uint8_t*>(c.out_sf[i]);
+  }
 
-  const uint64_t rows = (uint64_t)c.M_rows;  // rows of the row-space buffers
+  const int eb = MX ? 1 : 2;                  // element bytes of the GEMM operands
+  const uint64_t rows = (uint64_t)c.M_rows;   // rows of the row-space buffers
   const uint64_t G = (uint64_t)p.groups;
   CUtensorMap tA0, tA1, tB0, tB1;
   memset(&tA1, 0, sizeof(tA1));
@@ -545,50 +762,64 @@ cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s) {
   bool ok = true;
   int max_tiles = 0;
   const int mt_rows = (int)((rows + BM - 1) / BM);
+  const int BK = C::BK;
   switch (c.mode) {
     case kFwdUpGate:
       p.BN = 256;
       p.n_tiles = c.I / 128;
       p.kiters = c.H / BK;
-      ok = make_map(&tA0, c.a0, c.H, rows, BM) && make_map(&tB0, c.b0, c.I, G * c.H, BK) &&
-           make_map(&tB1, c.b1, c.I, G * c.H, BK);
+      p.kcs_a = c.H / 128;
+      p.kcs_b = c.H / 128;
+      p.ncs_b = c.I / 128;
+      ok = make_map(&tA0, c.a0, c.H, rows, BM, eb) && make_map(&tB0, c.b0, c.I, G * c.H, BK, eb) &&
+           make_map(&tB1, c.b1, c.I, G * c.H, BK, eb);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kFwdDown:
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
       p.kiters = c.I / BK;
-      ok = make_map(&tA0, c.a0, c.I, rows, BM) && make_map(&tB0, c.b0, c.H, G * c.I, BK);
+      p.kcs_a = c.I / 128;
+      p.kcs_b = c.I / 128;
+      p.ncs_b = c.H / 128;
+      ok = make_map(&tA0, c.a0, c.I, rows, BM, eb) && make_map(&tB0, c.b0, c.H, G * c.I, BK, eb);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDH:
       p.BN = (c.I % 256 == 0) ? 256 : 128;
       p.n_tiles = c.I / p.BN;
       p.kiters = c.H / BK;
-      ok = make_map(&tA0, c.a0, c.H, rows, BM) && make_map(&tB0, c.b0, c.H, G * c.I, p.BN);
+      p.kcs_a = c.H / 128;
+      p.kcs_b = c.H / 128;
+      p.ncs_b = c.I / 128;
+      ok = make_map(&tA0, c.a0, c.H, rows, BM, eb) && make_map(&tB0, c.b0, c.H, G * c.I, p.BN, eb);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDX:
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
       p.kiters = 2 * (c.I / BK);
-      ok = make_map(&tA0, c.a0, c.I, rows, BM) && make_map(&tA1, c.a1, c.I, rows, BM) &&
-           make_map(&tB0, c.b0, c.I, G * c.H, p.BN) && make_map(&tB1, c.b1, c.I, G * c.H, p.BN);
+      p.kcs_a = c.I / 128;
+      p.kcs_b = c.I / 128;
+      p.ncs_b = c.H / 128;
+      ok = make_map(&tA0, c.a0, c.I, rows, BM, eb) && make_map(&tA1, c.a1, c.I, rows, BM, eb) &&
+           make_map(&tB0, c.b0, c.I, G * c.H, p.BN, eb) &&
+           make_map(&tB1, c.b1, c.I, G * c.H, p.BN, eb);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDWDown:
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
       p.m_tiles_dw = c.I / BM;
-      ok = make_map(&tA0, c.a0, c.I, rows, BK) && make_map(&tB0, c.b0, c.H, rows, BK);
+      ok = make_map(&tA0, c.a0, c.I, rows, BK, eb) && make_map(&tB0, c.b0, c.H, rows, BK, eb);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
     case kBwdDWUpGate:
       p.BN = 256;
       p.n_tiles = c.I / 128;
       p.m_tiles_dw = c.H / BM;
-      ok = make_map(&tA0, c.a0, c.H, rows, BK) && make_map(&tB0, c.b0, c.I, rows, BK) &&
-           make_map(&tB1, c.b1, c.I, rows, BK);
+      ok = make_map(&tA0, c.a0, c.H, rows, BK, eb) && make_map(&tB0, c.b0, c.I, rows, BK, eb) &&
+           make_map(&tB1, c.b1, c.I, rows, BK, eb);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
   }
@@ -597,8 +828,16 @@ cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s) {
   if (c.mode == kFwdDown || c.mode == kBwdDH || c.mode == kBwdDWDown) tB1 = tB0;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tA0, tA1, tB0, tB1, p);
+  grouped_gemm_kernel<MX><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(tA0, tA1, tB0, tB1, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_dh_parts(int I) { return (I % 256 == 0) ? I / 256 : I / 128; }
+
+cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s) {
+  return c.mx ? launch_impl<true>(c, num_sms, s) : launch_impl<false>(c, num_sms, s);
 }
 
 }  // namespace mok

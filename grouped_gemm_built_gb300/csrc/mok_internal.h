@@ -34,13 +34,24 @@ struct AuxLayout {
 struct PlanWs {
   size_t logits, hist, lrank, total;
 };
-// scratch for the forward
+// scratch for the forward (xq/xsf, hq/hsf: MXFP8 operands and their scale atoms)
 struct FwdWs {
-  size_t xg, h, o, hs, os, total;
+  size_t xg, h, o, hs, os, xq, xsf, hq, hsf, total;
 };
-// scratch for the backward
+// MXFP8 copies of the routed weights (mok_quantize_weights_mxfp8): data in the weights'
+// own layouts, atoms [e][K/128][N/128]. *_h: blocks along H; *_i: blocks along I.
+struct MxWeights {
+  size_t up_h, up_h_sf, gate_h, gate_h_sf, down_i, down_i_sf;  // forward GEMMs
+  size_t down_h, down_h_sf, up_i, up_i_sf, gate_i, gate_i_sf;  // backward dH / dX GEMMs
+  size_t total;
+};
+// scratch for the backward. MXFP8 operands (E4M3 + atoms): dY along H (dH GEMM), dY and
+// x in 32-row blocks (dW GEMMs), du/dv along I (dX GEMM), du/dv/g*h in 32-row blocks.
 struct BwdWs {
-  size_t dyg, xg, du, dv, hg, dxg, dgp, dl, dus, dvs, hsg, dxs, total;
+  size_t dyg, xg, du, dv, hg, dxg, dgp, dl, dus, dvs, hsg, dxs;
+  size_t q_dy_h, sf_dy_h, q_dy_r, sf_dy_r, q_x_r, sf_x_r;
+  size_t q_du_i, sf_du_i, q_dv_i, sf_dv_i, q_du_r, sf_du_r, q_dv_r, sf_dv_r, q_hg_r, sf_hg_r;
+  size_t total;
 };
 // saved activations (forward -> backward)
 struct SavedLayout {
@@ -53,6 +64,7 @@ PlanWs plan_ws(const Dims& d);
 FwdWs fwd_ws(const Dims& d);
 BwdWs bwd_ws(const Dims& d);
 SavedLayout saved_layout(const Dims& d);
+MxWeights mx_weights_layout(const Dims& d);
 
 // Pointers into the aux buffer.
 struct AuxPtrs {
@@ -84,12 +96,13 @@ cudaError_t launch_plan_scatter(const Dims& d, const int32_t* topk_idx, const in
 // Xg[p] = src[table token of padded row p] (zero rows for padding); optional per-row gate.
 cudaError_t launch_gather_rows(const Dims& d, const void* src, const mok_sched& sc,
                                const AuxPtrs& a, void* dst, int num_sms, cudaStream_t s);
-// y[t] = sum_j gates[t][j] * O[row(t,j)] (+ add[t]) in fp32, slot order, -> bf16.
+// y[t] = sum_j gates[t][j] * O[row(t,j)] (+ add[t]), all fp32, in slot order.
 cudaError_t launch_combine(const Dims& d, const void* O, const mok_sched& sc, const AuxPtrs& a,
                            const void* add, bool weighted, void* y, cudaStream_t s);
 // WrT [E][H] = Wr [H][E]^T (router rows made contiguous for the reverse combine)
 cudaError_t launch_transpose_wr(const Dims& d, const float* Wr, float* WrT, cudaStream_t s);
-// dX[t] = sum_j dXg[row(t,j)] + dXs[t] + sum_j dl[t][j] * WrT[e_j][:]  (dl may be null)
+// dX[t] = sum_j dXg[row(t,j)] + dXs[t] + sum_j dl[t][j] * WrT[e_j][:], all fp32
+// (dl may be null)
 cudaError_t launch_reverse_combine(const Dims& d, const void* dXg, const mok_sched& sc,
                                    const AuxPtrs& a, const void* dXs, const float* dl,
                                    const float* WrT, void* dX, cudaStream_t s);
@@ -120,7 +133,7 @@ struct GemmCall {
   // operands (device pointers)
   const void* a0; const void* a1;      // row-space operands (Xg / h / dYg / du, dv ...)
   const void* b0; const void* b1;      // weights
-  void* out0; void* out1; void* out2;  // outputs
+  void* out0; void* out1; void* out2;  // outputs (bf16; fp32 for O, dXg and dW)
   const void* aux0; const void* aux1;  // extra epilogue inputs (saved U, V)
   float* dgp;                          // kBwdDH: per-tile partial router-weight gradients
   // schedule (routed case)
@@ -128,8 +141,31 @@ struct GemmCall {
   const int32_t* tile_expert; const int32_t* num_mtiles;
   const int32_t* table; const float* gates; int k;
   uint32_t* status;
+  // MXFP8 (E4M3 operands with 512-byte scale atoms; see mok_quant.cu)
+  bool mx;
+  const void* sfa; const void* sfa1;                   // A scale atoms (second: kBwdDX dv)
+  const void* sfb0; const void* sfb1;                  // B scale atoms
+  void* out_q[5]; void* out_sf[5];                     // quantised epilogue outputs + atoms
 };
 cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- MXFP8 quantisers (mok_quant.cu)
+// src [batch][rows][cols] bf16 -> dst e4m3 (same layout) + 512-byte scale atoms; blocks of
+// 32 along the columns (k_along_cols) or along the rows. Atom (kc, mc) of batch z is at
+// atoms + z*(rows/128)*(cols/128)*512 + (kc*s_kc + mc*s_mc)*512, kc indexing K / 128 and
+// mc the other axis / 128.
+cudaError_t launch_mx_quant(const void* src, int rows, int cols, int batch, bool k_along_cols,
+                            void* dst, void* atoms, int s_kc, int s_mc, cudaStream_t s);
+// forward dispatch in MXFP8: pull x rows by the table and quantise along H
+// (atoms [P/128][H/128]).
+cudaError_t launch_gather_quant(const Dims& d, const void* src, const mok_sched& sc,
+                                const AuxPtrs& a, void* dst, void* atoms, int num_sms,
+                                cudaStream_t s);
+// the same pull, quantised in blocks of 32 padded rows (contraction axis of the dW GEMMs):
+// atoms [P/128][H/128] with m = column, b = 32-row block inside the 128-row tile.
+cudaError_t launch_gather_quant_rows(const Dims& d, const void* src, const mok_sched& sc,
+                                     const AuxPtrs& a, void* dst, void* atoms, int num_sms,
+                                     cudaStream_t s);
 int gemm_dh_parts(int I);  // number of partial dg columns kBwdDH writes per row
 
 }  // namespace mok

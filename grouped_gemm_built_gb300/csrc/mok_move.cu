@@ -25,23 +25,6 @@ __device__ __forceinline__ int padded_row(int sl, int E, const int32_t* topk_idx
   return inv[sl] - offsets[e] + poff[e];
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
-  uint4 v;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-  return v;
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------- dispatch (pull gather)
@@ -80,18 +63,19 @@ cudaError_t launch_gather_rows(const Dims& d, const void* src, const mok_sched& 
 }
 
 // ---------------------------------------------------------------- combine
-// One warp per token. weighted: y = sum_j g_tj O[row(t,j)] (+ add[t]); otherwise the
-// plain sum (the reverse combine of the backward without its router term).
+// One warp per token, fp32 rows. weighted: y = sum_j g_tj O[row(t,j)] (+ add[t]);
+// otherwise the plain sum (the reverse combine of the backward), plus the router path
+// sum_j dl_tj Wr[:, e_j] when dl is given.
 __global__ void __launch_bounds__(256) combine_kernel(
-    int T, int H, int E, int k, const uint4* __restrict__ O, const int32_t* __restrict__ topk_idx,
+    int T, int H, int E, int k, const float4* __restrict__ O, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ gates, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ poff,
-    const uint4* __restrict__ add, const float* __restrict__ dl, const float* __restrict__ WrT,
-    int weighted, uint4* __restrict__ y) {
+    const float4* __restrict__ add, const float* __restrict__ dl, const float* __restrict__ WrT,
+    int weighted, float4* __restrict__ y) {
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  const int nvec = H / 8;
+  const int nvec = H / 4;
   int my_row = 0, my_e = 0;
   float my_g = 0.f, my_dl = 0.f;
   if (lane < k) {
@@ -111,55 +95,54 @@ __global__ void __launch_bounds__(256) combine_kernel(
     dls[j] = __shfl_sync(0xffffffffu, my_dl, j);
   }
   for (int i = lane; i < nvec; i += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j < k) {
-        float f[8];
-        bf16x8_to_f32(__ldg(O + (size_t)rows[j] * nvec + i), f);
+        const float4 f = __ldg(O + (size_t)rows[j] * nvec + i);
         if (weighted) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = fmaf(g[j], f[q], acc[q]);
+          acc.x = fmaf(g[j], f.x, acc.x);
+          acc.y = fmaf(g[j], f.y, acc.y);
+          acc.z = fmaf(g[j], f.z, acc.z);
+          acc.w = fmaf(g[j], f.w, acc.w);
         } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+          acc.x += f.x;
+          acc.y += f.y;
+          acc.z += f.z;
+          acc.w += f.w;
         }
       }
     }
     if (add) {
-      float f[8];
-      bf16x8_to_f32(__ldg(add + (size_t)t * nvec + i), f);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      const float4 f = __ldg(add + (size_t)t * nvec + i);
+      acc.x += f.x;
+      acc.y += f.y;
+      acc.z += f.z;
+      acc.w += f.w;
     }
-    if (dl) {  // router path of dX: sum_j dl_tj * Wr[:, e_j]
+    if (dl) {
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
-          const float4* w = reinterpret_cast<const float4*>(WrT + (size_t)ex[j] * H) + 2 * i;
-          float4 w0 = __ldg(w), w1 = __ldg(w + 1);
-          acc[0] = fmaf(dls[j], w0.x, acc[0]);
-          acc[1] = fmaf(dls[j], w0.y, acc[1]);
-          acc[2] = fmaf(dls[j], w0.z, acc[2]);
-          acc[3] = fmaf(dls[j], w0.w, acc[3]);
-          acc[4] = fmaf(dls[j], w1.x, acc[4]);
-          acc[5] = fmaf(dls[j], w1.y, acc[5]);
-          acc[6] = fmaf(dls[j], w1.z, acc[6]);
-          acc[7] = fmaf(dls[j], w1.w, acc[7]);
+          const float4 w = __ldg(reinterpret_cast<const float4*>(WrT + (size_t)ex[j] * H) + i);
+          acc.x = fmaf(dls[j], w.x, acc.x);
+          acc.y = fmaf(dls[j], w.y, acc.y);
+          acc.z = fmaf(dls[j], w.z, acc.z);
+          acc.w = fmaf(dls[j], w.w, acc.w);
         }
       }
     }
-    y[(size_t)t * nvec + i] = f32_to_bf16x8(acc);
+    y[(size_t)t * nvec + i] = acc;
   }
 }
 
 cudaError_t launch_combine(const Dims& d, const void* O, const mok_sched& sc, const AuxPtrs& a,
                            const void* add, bool weighted, void* y, cudaStream_t s) {
   int blocks = (d.T * 32 + 255) / 256;
-  combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const uint4*>(O),
+  combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const float4*>(O),
                                         sc.topk_idx, sc.gates, sc.inv, sc.offsets, a.poff,
-                                        static_cast<const uint4*>(add), nullptr, nullptr,
-                                        weighted ? 1 : 0, static_cast<uint4*>(y));
+                                        static_cast<const float4*>(add), nullptr, nullptr,
+                                        weighted ? 1 : 0, static_cast<float4*>(y));
   return cudaGetLastError();
 }
 
@@ -187,10 +170,10 @@ cudaError_t launch_reverse_combine(const Dims& d, const void* dXg, const mok_sch
                                    const AuxPtrs& a, const void* dXs, const float* dl,
                                    const float* WrT, void* dX, cudaStream_t s) {
   int blocks = (d.T * 32 + 255) / 256;
-  combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const uint4*>(dXg),
+  combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const float4*>(dXg),
                                         sc.topk_idx, sc.gates, sc.inv, sc.offsets, a.poff,
-                                        static_cast<const uint4*>(dXs), dl, dl ? WrT : nullptr, 0,
-                                        static_cast<uint4*>(dX));
+                                        static_cast<const float4*>(dXs), dl, dl ? WrT : nullptr,
+                                        0, static_cast<float4*>(dX));
   return cudaGetLastError();
 }
 

@@ -123,6 +123,48 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
       : "memory");
 }
 
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: E4M3 A and B (format 0),
+// UE8M0 scales (bit 23), scale byte `sf_id` of the 32-bit TMEM scale word for A (bits
+// 29-30) and B (bits 4-5); fp32 accumulation is implied.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, bool a_mn, bool b_mn,
+                                                  uint32_t sf_id) {
+  return ((sf_id & 3u) << 4)                // B scale byte
+         | (0u << 7) | (0u << 10)           // A, B format: E4M3
+         | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | (1u << 23)  // scale format UE8M0
+         | ((uint32_t)(M >> 4) << 24) | ((sf_id & 3u) << 29);  // A scale byte
+}
+
+__device__ __forceinline__ void umma_mxf8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t tmem_sfa, uint32_t tmem_sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled block of rows of 16 bytes (row i at 16*i):
+// 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;  // swizzle mode 0 (none)
+}
+
+// Copy a 32-row x 128-bit block from shared memory into TMEM columns taddr..taddr+3,
+// replicated into all four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

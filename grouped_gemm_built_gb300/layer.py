@@ -66,6 +66,14 @@ class MoELayer:
                               Ws_up=_ptr(Ws_up), Ws_gate=_ptr(Ws_gate), Ws_down=_ptr(Ws_down),
                               mx=_ptr(mx))
 
+    def quantize_weights(self, W_up, W_gate, W_down):
+        """MXFP8 copies of the routed weights (library-private layout), as a uint8 tensor."""
+        mx = torch.empty(self.sizes.mx_weight_bytes, dtype=torch.uint8, device=self.device)
+        w = mok.MokWeights(W_up=W_up.data_ptr(), W_gate=W_gate.data_ptr(),
+                           W_down=W_down.data_ptr())
+        mok.mok_quantize_weights_mxfp8(self.ctx, w, mx.data_ptr(), self._stream())
+        return mx
+
     def plan(self, x=None, Wr=None, bias=None, topk_idx=None, gates=None):
         if not self.router:
             self.topk_idx.copy_(topk_idx)
@@ -75,14 +83,14 @@ class MoELayer:
 
     def forward(self, x, w: "mok.MokWeights", y=None):
         if y is None:
-            y = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
+            y = torch.empty((self.T, self.H), dtype=torch.float32, device=self.device)
         mok.mok_moe_fwd(self.ctx, self.sched, x.data_ptr(), w, y.data_ptr(),
                         self.saved.data_ptr(), self.workspace.data_ptr(), self._stream())
         return y
 
     def alloc_grads(self):
         dev = self.device
-        bf = dict(dtype=torch.bfloat16, device=dev)
+        bf = dict(dtype=torch.float32, device=dev)   # all gradients are fp32
         g = {
             "dX": torch.empty((self.T, self.H), **bf),
             "dW_up": torch.empty((self.E, self.H, self.I), **bf),

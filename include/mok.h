@@ -110,9 +110,10 @@ typedef struct {
   const void* mx;
 } mok_weights;
 
-/* Gradients written by mok_moe_bwd (device). dW_* bf16 with the weights' shapes;
- * dgates [T][k] fp32 (dL/dgate, the router-weight gradient); dWr [H][E] fp32 (NULL
- * when there is no router); dWs_* bf16 (NULL when there is no shared expert). */
+/* Gradients written by mok_moe_bwd (device, all fp32): dW_* with the weights' shapes
+ * (fp32 sums of bf16/MXFP8 products); dgates [T][k] (dL/dgate, the router-weight
+ * gradient); dWr [H][E] (NULL when there is no router); dWs_* (NULL when there is no
+ * shared expert). */
 typedef struct {
   void* dW_up;
   void* dW_gate;
@@ -166,15 +167,16 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
 mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* logit_bias,
                     mok_sched* sched, void* workspace, void* stream);
 
-/* Forward: y [T][H] bf16 = sum_j gates[t][j] * FFN_{topk_idx[t][j]}(x[t]) (+ shared
- * expert), FFN_e(v) = (silu(v W_gate[e]) * (v W_up[e])) W_down[e]; the k terms are added
- * in slot order in fp32. `saved` (mok_sizes.saved_bytes) receives what mok_moe_bwd
- * needs; it must stay untouched until then. */
+/* Forward: y [T][H] fp32 = sum_j gates[t][j] * FFN_{topk_idx[t][j]}(x[t]) (+ shared
+ * expert), FFN_e(v) = (silu(v W_gate[e]) * (v W_up[e])) W_down[e]; the GEMMs take bf16
+ * (or MXFP8) operands with fp32 accumulation, h is rounded to the operand format, and the
+ * k terms are added in slot order in fp32. `saved` (mok_sizes.saved_bytes) receives what
+ * mok_moe_bwd needs; it must stay untouched until then. */
 mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
                        const mok_weights* w, void* y, void* saved, void* workspace,
                        void* stream);
 
-/* Backward for upstream gradient dY [T][H] bf16. Writes dX [T][H] bf16 (routed experts,
+/* Backward for upstream gradient dY [T][H] bf16. Writes dX [T][H] fp32 (routed experts,
  * shared expert and, when routing ran on the device, the router path) and `grads`.
  * Wr must be the router weight given to mok_plan (NULL when dims.router = 0). */
 mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, const float* Wr,

@@ -30,10 +30,11 @@ Readings taken where the pages are silent (each is also listed in the design not
 * gradients at the top-k boundary are taken with the selected set S held fixed.
 
 Precision model (``precision``): "fp64" applies no rounding at all. "bf16" and "mxfp8"
-round exactly where the GPU path stores a value in bf16 (U, V saved for backward, expert
-outputs O, the routed dX rows, the shared expert's outputs) or feeds a GEMM with a
-quantised operand (bf16 h, du, dv, g*h; or MXFP8 blocks of 32 along that GEMM's
-contraction axis). Everything else is float64. The shared expert is always BF16.
+round exactly where the GPU path stores a value in bf16 (U, V saved for the backward) or
+feeds a GEMM with a quantised operand (bf16 h, du, dv, g*h; or MXFP8 blocks of 32 along
+that GEMM's contraction axis). Expert outputs, the routed dX rows and the layer's
+results are fp32 on the GPU and stay unrounded here. Everything else is float64. The
+shared expert is always BF16.
 """
 from __future__ import annotations
 
@@ -162,7 +163,7 @@ def shared_forward(x, Ws_up, Ws_gate, Ws_down, mode: str):
     U = x @ Ws_up
     V = x @ Ws_gate
     h = P.act(silu(V) * U, 1)
-    O = P.store(h @ Ws_down)
+    O = h @ Ws_down
     return O, {"Us": P.store(U), "Vs": P.store(V)}
 
 
@@ -194,7 +195,7 @@ def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
         U = A @ P.op(W_up[e], 0)
         V = A @ P.op(W_gate[e], 0)
         h = P.act(silu(V) * U, 1)
-        O_rows[r0:r1] = P.store(h @ P.op(W_down[e], 0))
+        O_rows[r0:r1] = h @ P.op(W_down[e], 0)
         U_s[r0:r1] = P.store(U)
         V_s[r0:r1] = P.store(V)
     y = np.zeros((T, H))
@@ -230,7 +231,7 @@ def shared_backward(x, Ws_up, Ws_gate, Ws_down, saved, dY, mode: str):
     hv = silu(Vs) * Us
     du = P.act(D * silu(Vs), 1)
     dv = P.act(D * Us * dsilu(Vs), 1)
-    dXs = P.store(du @ Ws_up.T + dv @ Ws_gate.T)
+    dXs = du @ Ws_up.T + dv @ Ws_gate.T
     dWs_down = P.act(hv, 0).T @ dY
     dWs_up = x.T @ du
     dWs_gate = x.T @ dv
@@ -283,8 +284,8 @@ def backward(x, idx, gates, W_up, W_gate, W_down, saved, dY, shared=None,
         dh = g * D
         du = dh * silu(Vs)
         dv = dh * Us * dsilu(Vs)
-        dXg[r0:r1] = P.store(P.act(du, 1) @ P.op(W_up[e], 1).T
-                             + P.act(dv, 1) @ P.op(W_gate[e], 1).T)
+        dXg[r0:r1] = (P.act(du, 1) @ P.op(W_up[e], 1).T
+                      + P.act(dv, 1) @ P.op(W_gate[e], 1).T)
         dW_down[e] = P.act_rows(g * hv).T @ P.op_rows(dYe)
         XR = P.op_rows(Xe)
         dW_up[e] = XR.T @ P.act_rows(du)

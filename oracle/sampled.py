@@ -5,8 +5,8 @@ routed row of every expert; at the Kimi/DeepSeek sizes that is too much, so thes
 functions compute one token's y or dX row, or one element of a weight gradient, straight
 from the definition (with the same bf16 rounding model as ``moe``, precision "bf16"):
 
-* y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(bf16(silu(x W_gate) * (x W_up)) W_down);
-* dX_t = sum_j bf16(du W_up^T + dv W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j], with
+* y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(silu(x W_gate) * (x W_up)) W_down;
+* dX_t = sum_j (du W_up^T + dv W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j], with
   D = dY_t W_down^T, du = bf16(g D silu(V)), dv = bf16(g D U silu'(V)) from the bf16 U, V;
 * dW_down[e][i][h] = sum over e's rows of bf16(g silu(V) U)[i] dY[t][h];
 * dW_up[e][h][i] = sum over e's rows of x[t][h] du[i] (dW_gate with dv).
@@ -26,7 +26,7 @@ def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
     v = x_t @ Wg
     U, V = bf16_round(u), bf16_round(v)
     h = bf16_round(silu(v) * u)
-    O = bf16_round(h @ Wd)
+    O = h @ Wd
     out = {"O": O}
     if dY_t is not None:
         D = Wd @ dY_t                      # = dY_t W_down^T
@@ -34,7 +34,7 @@ def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
         out["dg"] = float(D @ hv)
         du = bf16_round(g * D * silu(V))
         dv = bf16_round(g * D * U * dsilu(V))
-        out["dXg"] = bf16_round(Wu @ du + Wg @ dv)
+        out["dXg"] = Wu @ du + Wg @ dv
     return out
 
 
@@ -60,13 +60,13 @@ def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
         Ws_up, Ws_gate, Ws_down = shared
         u = x_t @ Ws_up
         v = x_t @ Ws_gate
-        y += bf16_round(bf16_round(silu(v) * u) @ Ws_down)
+        y += bf16_round(silu(v) * u) @ Ws_down
         if dY_t is not None:
             U, V = bf16_round(u), bf16_round(v)
             D = Ws_down @ dY_t
             du = bf16_round(D * silu(V))
             dv = bf16_round(D * U * dsilu(V))
-            dX += bf16_round(Ws_up @ du + Ws_gate @ dv)
+            dX += Ws_up @ du + Ws_gate @ dv
     out = {"y": y}
     if dY_t is not None:
         if Wr is not None:

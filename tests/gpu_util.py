@@ -54,7 +54,11 @@ def run_gpu(cfg, inp_cpu, backward=True, layer=None, routing=None):
         idx, g = routing if routing is not None else (d["topk_idx"], d["gates"])
         L.plan(topk_idx=torch.as_tensor(np.asarray(idx), dtype=torch.int32).cuda(),
                gates=torch.as_tensor(np.asarray(g), dtype=torch.float32).cuda())
-    w = L.weights(d["W_up"], d["W_gate"], d["W_down"], d["Ws_up"], d["Ws_gate"], d["Ws_down"])
+    mx = None
+    if cfg.precision == "mxfp8":
+        mx = L.quantize_weights(d["W_up"], d["W_gate"], d["W_down"])
+    w = L.weights(d["W_up"], d["W_gate"], d["W_down"], d["Ws_up"], d["Ws_gate"], d["Ws_down"],
+                  mx=mx)
     y = L.forward(d["x"], w)
     out = {"y": y}
     if backward:
@@ -121,3 +125,32 @@ def ambiguous_tokens(cfg, inp, logits):
     else:
         bsum = bv[:, :-1] + bv[:, 1:]
     return np.where((gaps <= bsum).any(axis=1))[0]
+
+
+def mx_weight_offsets(E, H, I):
+    """Byte offsets of the MXFP8 weight copies written by mok_quantize_weights_mxfp8
+    (the library's bump layout: 256-byte aligned, in this order)."""
+    def al(v):
+        return (v + 255) // 256 * 256
+    n = E * H * I
+    names = ["up_h", "up_h_sf", "gate_h", "gate_h_sf", "down_i", "down_i_sf"]
+    sizes = [n, n // 32, n, n // 32, n, n // 32]
+    off, out = 0, {}
+    for nm, sz in zip(names, sizes):
+        out[nm] = (off, sz)
+        off = al(off + sz)
+    return out
+
+
+def unpack_atoms(buf, E, K, N):
+    """Scale bytes [E][K/32][N] from 512-byte atoms laid out [e][K/128][N/128], byte
+    (m, b) of an atom at 16*(m%32) + 4*((m%128)//32) + b (m the N index, b the 32-block
+    inside the atom's 128 K elements)."""
+    a = np.asarray(buf).reshape(E, K // 128, N // 128, 512)
+    m = np.arange(128)
+    out = np.empty((E, K // 32, N), np.uint8)
+    for b in range(4):
+        pos = 16 * (m % 32) + 4 * (m // 32) + b
+        blk = a[:, :, :, pos]                      # [E, K/128, N/128, 128]
+        out[:, b::4, :] = blk.reshape(E, K // 128, N)
+    return out

@@ -93,3 +93,58 @@ def test_bad_expert_id_is_flagged():
     res, _ = gu.run_gpu(cfg, inp, backward=False, routing=(idx, np.full((40, 2), 0.5)))
     from grouped_gemm_built_gb300 import mok
     assert res["status"] == mok.MOK_ERR_DEVICE
+
+
+# ----------------------------------------------------------------------------- MXFP8
+MX_CASES = {
+    "tiny_mx": mi.MoEConfig("tiny_mx", T=256, H=256, I=256, E=8, k=2, precision="mxfp8"),
+    "biased_mx": mi.MoEConfig("biased_mx", T=512, H=512, I=256, E=16, k=4,
+                              bias_experts=(0, 1, 2, 3), bias_value=3.0, precision="mxfp8"),
+    "ep64_slice_small": mi.MoEConfig("ep64_slice_small", T=256, H=512, I=256, E=6, k=8,
+                                     router=False, zipf_s=1.2, precision="mxfp8",
+                                     backward=False),
+    "ragged_shared_mx": mi.MoEConfig("ragged_shared_mx", T=300, H=256, I=256, E=12, k=3,
+                                     shared_I=128, precision="mxfp8"),
+}
+
+
+def test_mxfp8_weight_quantizer_is_bit_exact():
+    from oracle import numerics as nu
+    cfg = MX_CASES["tiny_mx"]
+    inp = gu.gpu_inputs(cfg)
+    L = gu.make_layer(cfg)
+    d = gu.to_dev(inp)
+    mx = L.quantize_weights(d["W_up"], d["W_gate"], d["W_down"]).cpu().numpy()
+    E, H, I = cfg.E, cfg.H, cfg.I
+    off = gu.mx_weight_offsets(E, H, I)
+    for name, wname, K, N in (("up_h", "W_up", H, I), ("gate_h", "W_gate", H, I),
+                              ("down_i", "W_down", I, H)):
+        o, n = off[name]
+        codes = mx[o:o + n].reshape(E, K, N)
+        so, sn = off[name + "_sf"]
+        scales = gu.unpack_atoms(mx[so:so + sn], E, K, N)
+        rc, rs = nu.mx_quantize(gu.np64(inp[wname]), axis=1)
+        assert np.array_equal(codes, rc), name
+        assert np.array_equal(scales, rs), name + " scales"
+
+
+@pytest.mark.parametrize("name", list(MX_CASES))
+def test_mxfp8_layer_matches_oracle(name):
+    cfg = MX_CASES[name]
+    inp = gu.gpu_inputs(cfg, seed=0)
+    idx, gates, logits = gu.oracle_route(cfg, inp)
+    res, _ = gu.run_gpu(cfg, inp, backward=cfg.backward)
+    assert res["status"] == 0
+    _check_route_and_plan(cfg, inp, res, idx, gates, logits)
+    ref = gu.run_oracle(cfg, inp, idx, gates, backward=cfg.backward)
+    fields = ["y"]
+    if cfg.backward:
+        fields += ["dX", "dW_up", "dW_gate", "dW_down", "dgates"]
+        if cfg.router:
+            fields.append("dWr")
+        if cfg.shared_I:
+            fields += ["dWs_up", "dWs_gate", "dWs_down"]
+    errs = {f: gu.rel_err(res[f], ref[f]) for f in fields}
+    print(name, errs)
+    for f, e in errs.items():
+        assert e <= gu.TOL["mxfp8"], (f, e)
