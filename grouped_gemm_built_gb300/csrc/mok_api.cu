@@ -648,8 +648,9 @@ mok_status mok_quantize_weights_mxfp8(mok_ctx_t ctx, const mok_weights* w, void*
                                       void* stream) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
   const Dims& d = ctx->d;
-  mok_status st = check_weights(d, w);
-  if (st != MOK_OK) return st;
+  if (!w || !w->W_up || !w->W_gate || !w->W_down) return MOK_ERR_INVALID_ARG;
+  if (!aligned(w->W_up, 16) || !aligned(w->W_gate, 16) || !aligned(w->W_down, 16))
+    return MOK_ERR_INVALID_ARG;
   if (!mx_out || !aligned(mx_out, 256)) return MOK_ERR_INVALID_ARG;
   if (ctx->num_sms <= 0) return MOK_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

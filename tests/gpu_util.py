@@ -50,8 +50,10 @@ def run_gpu(cfg, inp_cpu, backward=True, layer=None, routing=None):
     L = layer or make_layer(cfg)
     if cfg.router and routing is None:
         L.plan(x=d["x"], Wr=d["Wr"], bias=d["bias"])
+    elif routing is None:
+        L.plan(topk_idx=d["topk_idx"], gates=d["gates"])
     else:
-        idx, g = routing if routing is not None else (d["topk_idx"], d["gates"])
+        idx, g = routing
         L.plan(topk_idx=torch.as_tensor(np.asarray(idx), dtype=torch.int32).cuda(),
                gates=torch.as_tensor(np.asarray(g), dtype=torch.float32).cuda())
     mx = None
