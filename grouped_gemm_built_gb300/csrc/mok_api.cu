@@ -199,6 +199,11 @@ SavedLayout saved_layout(const Dims& d) {
 
 }  // namespace mok
 
+namespace mok {
+const Dims* ctx_dims(mok_ctx_t ctx) { return ctx ? &ctx->d : nullptr; }
+int ctx_num_sms(mok_ctx_t ctx) { return ctx ? ctx->num_sms : 0; }
+}  // namespace mok
+
 using namespace mok;
 
 namespace {

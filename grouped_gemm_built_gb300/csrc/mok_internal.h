@@ -81,6 +81,10 @@ inline AuxPtrs aux_ptrs(const Dims& d, void* aux) {
                  reinterpret_cast<int32_t*>(b + L.num_mtiles)};
 }
 
+// Read-only views of a context (defined in mok_api.cu).
+const Dims* ctx_dims(mok_ctx_t ctx);
+int ctx_num_sms(mok_ctx_t ctx);
+
 // ---------------------------------------------------------------- launchers (mok_route.cu)
 cudaError_t launch_router_logits(const Dims& d, const void* x, const float* Wr, const float* bias,
                                  float* logits, cudaStream_t s);

@@ -80,6 +80,7 @@ def _declare(L):
                                 c_void_p]),
         "mok_quantize_weights_mxfp8": (c_int, [c_void_p, _P(MokWeights), c_void_p, c_void_p]),
         "mok_get_status": (c_int, [c_void_p, _P(MokSched), c_void_p]),
+        "mok_plan_noalloc": (c_int, [c_void_p, _P(MokSched), c_void_p]),
         "mok_profile_enable": (c_int, [c_void_p, c_int]),
         "mok_profile_report": (c_int, [c_void_p, c_char_p, c_size_t, _P(c_int)]),
     }
@@ -178,6 +179,11 @@ def mok_quantize_weights_mxfp8(ctx, weights: MokWeights, mx_out, stream) -> None
 def mok_get_status(ctx, sched: MokSched, stream) -> int:
     """Synchronises the stream; returns the device status (0 = ok) and clears it."""
     return lib().mok_get_status(ctx, ctypes.byref(sched), _v(stream))
+
+
+def mok_plan_noalloc(ctx, sched: MokSched, stream) -> None:
+    """Schedule from caller-supplied routing, with no workspace (see include/mok.h)."""
+    _check(lib().mok_plan_noalloc(ctx, ctypes.byref(sched), _v(stream)), "mok_plan_noalloc")
 
 
 def mok_profile_enable(ctx, enable: bool) -> None:

@@ -191,6 +191,27 @@ mok_status mok_quantize_weights_mxfp8(mok_ctx_t ctx, const mok_weights* w, void*
 /* Synchronise `stream`, read and clear the device status word of `sched`. */
 mok_status mok_get_status(mok_ctx_t ctx, const mok_sched* sched, void* stream);
 
+/* Schedule construction that allocates nothing and takes no workspace. The articles have
+ * no counterpart: this serves callers that cannot allocate device memory, e.g. code
+ * embedded in a host runtime that owns every device allocation, or code that runs where
+ * the allocator must not be called. They still pass inputs and outputs (sched, with
+ * topk_idx and gates filled in by the caller, and aux), but not a workspace.
+ *
+ * Computes exactly what mok_plan computes for a context created with router = 0 (counts,
+ * offsets, table, inv and the aux data, bitwise the same). Its scratch (per-block expert
+ * histograms and slot ranks, (ceil(T/32)*E + T*k) * 4 bytes, the first part rounded up
+ * to 256) lives in a fixed 4 MiB device array inside the library, which every GPU that
+ * loads the library holds until the process exits. Larger problems return
+ * MOK_ERR_UNSUPPORTED; contexts with router = 1 return MOK_ERR_INVALID_ARG.
+ *
+ * The first call on a device looks up that array's device address (with the device
+ * current) and caches it; make that first call before any stream capture. Every call
+ * shares the one array: calls whose work overlaps on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller. No state carries over from one
+ * call to the next: the scratch is fully rewritten before it is read. Does not call
+ * cudaMalloc, cudaFree or any allocating routine. */
+mok_status mok_plan_noalloc(mok_ctx_t ctx, mok_sched* sched, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
