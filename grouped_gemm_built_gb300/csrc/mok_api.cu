@@ -155,15 +155,21 @@ BwdWs bwd_ws(const Dims& d) {
   const size_t P = d.P_max;
   L.dyg = b.take(2 * P * d.H);
   L.xg = b.take(2 * P * d.H);
-  L.du = b.take(2 * P * d.I);
+  L.du = b.take(2 * P * d.I);   // du, dv, g*h: bf16 hi parts ...
   L.dv = b.take(2 * P * d.I);
   L.hg = b.take(2 * P * d.I);
+  L.du_lo = b.take(2 * P * d.I);  // ... and lo parts
+  L.dv_lo = b.take(2 * P * d.I);
+  L.hg_lo = b.take(2 * P * d.I);
   L.dxg = b.take(4 * P * d.H);
   L.dgp = b.take(sizeof(float) * P * gemm_dh_parts(d.I));
   L.dl = b.take(sizeof(float) * (size_t)d.R);
   L.dus = b.take(2 * (size_t)d.T * d.Is);
   L.dvs = b.take(2 * (size_t)d.T * d.Is);
   L.hsg = b.take(2 * (size_t)d.T * d.Is);
+  L.dus_lo = b.take(2 * (size_t)d.T * d.Is);
+  L.dvs_lo = b.take(2 * (size_t)d.T * d.Is);
+  L.hsg_lo = b.take(2 * (size_t)d.T * d.Is);
   L.dxs = b.take(4 * (size_t)d.T * d.H + sizeof(float) * (size_t)d.E * d.H);  // + Wr^T
   L.q_dy_h = b.take(P * d.H);
   L.sf_dy_h = b.take(P * d.H / 32);
@@ -189,10 +195,10 @@ SavedLayout saved_layout(const Dims& d) {
   Bump b;
   SavedLayout L;
   const size_t P = d.P_max;
-  L.u = b.take(2 * P * d.I);
-  L.v = b.take(2 * P * d.I);
-  L.us = b.take(2 * (size_t)d.T * d.Is);
-  L.vs = b.take(2 * (size_t)d.T * d.Is);
+  L.u = b.take(4 * P * d.I);
+  L.v = b.take(4 * P * d.I);
+  L.us = b.take(4 * (size_t)d.T * d.Is);
+  L.vs = b.take(4 * (size_t)d.T * d.Is);
   L.total = b.off;
   return L;
 }
@@ -407,74 +413,72 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
   AuxPtrs a = aux_ptrs(d, sched->aux);
   FwdWs L = fwd_ws(d);
   SavedLayout S = saved_layout(d);
-  void* xg = at(workspace, L.xg);
-  void* h = at(workspace, L.h);
-  void* o = at(workspace, L.o);
+  auto W = [&](size_t off) -> void* { return at(workspace, off); };
+  void* o = W(L.o);
   const bool mx = ctx->precision == MOK_MXFP8;
 
   if (!mx) {
     // dispatch: pull token rows into expert order through the table
-    MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
-    // grouped up|gate GEMM + SwiGLU
+    MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), ctx->num_sms, s));
+    // grouped up|gate GEMM + SwiGLU (h bf16; U, V saved in fp32)
     GemmCall c = routed_call(d, sched, a, kFwdUpGate);
-    c.a0 = xg;
-    c.b0 = w->W_up;
-    c.b1 = w->W_gate;
-    c.out0 = h;
-    c.out1 = at(saved, S.u);
-    c.out2 = at(saved, S.v);
+    c.a[0] = W(L.xg);
+    c.b[0] = w->W_up;
+    c.b[1] = w->W_gate;
+    c.out[0] = W(L.h);
+    c.out[1] = at(saved, S.u);
+    c.out[2] = at(saved, S.v);
     MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
     // grouped down GEMM
     c = routed_call(d, sched, a, kFwdDown);
-    c.a0 = h;
-    c.b0 = w->W_down;
-    c.out0 = o;
+    c.a[0] = W(L.h);
+    c.b[0] = w->W_down;
+    c.out[0] = o;
     MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
   } else {
     MxWeights M = mx_weights_layout(d);
     char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
     // dispatch with MXFP8 quantisation along H fused in
     MOK_LAUNCH("dispatch_gather_mxfp8",
-               launch_gather_quant(d, x, *sched, a, at(workspace, L.xq), at(workspace, L.xsf),
-                                   ctx->num_sms, s));
+               launch_gather_quant(d, x, *sched, a, W(L.xq), W(L.xsf), ctx->num_sms, s));
     GemmCall c = routed_call(d, sched, a, kFwdUpGate);
     c.mx = true;
-    c.a0 = at(workspace, L.xq);
-    c.sfa = at(workspace, L.xsf);
-    c.b0 = mxw + M.up_h;
-    c.b1 = mxw + M.gate_h;
+    c.a[0] = W(L.xq);
+    c.sfa = W(L.xsf);
+    c.b[0] = mxw + M.up_h;
+    c.b[1] = mxw + M.gate_h;
     c.sfb0 = mxw + M.up_h_sf;
     c.sfb1 = mxw + M.gate_h_sf;
-    c.out_q[0] = at(workspace, L.hq);
-    c.out_sf[0] = at(workspace, L.hsf);
-    c.out1 = at(saved, S.u);
-    c.out2 = at(saved, S.v);
+    c.out_q[0] = W(L.hq);
+    c.out_sf[0] = W(L.hsf);
+    c.out[1] = at(saved, S.u);
+    c.out[2] = at(saved, S.v);
     MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(c, ctx->num_sms, s));
     c = routed_call(d, sched, a, kFwdDown);
     c.mx = true;
-    c.a0 = at(workspace, L.hq);
-    c.sfa = at(workspace, L.hsf);
-    c.b0 = mxw + M.down_i;
+    c.a[0] = W(L.hq);
+    c.sfa = W(L.hsf);
+    c.b[0] = mxw + M.down_i;
     c.sfb0 = mxw + M.down_i_sf;
-    c.out0 = o;
+    c.out[0] = o;
     MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(c, ctx->num_sms, s));
   }
   const void* shared_out = nullptr;
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kFwdUpGate);
-    cs.a0 = x;
-    cs.b0 = w->Ws_up;
-    cs.b1 = w->Ws_gate;
-    cs.out0 = at(workspace, L.hs);
-    cs.out1 = at(saved, S.us);
-    cs.out2 = at(saved, S.vs);
+    cs.a[0] = x;
+    cs.b[0] = w->Ws_up;
+    cs.b[1] = w->Ws_gate;
+    cs.out[0] = W(L.hs);
+    cs.out[1] = at(saved, S.us);
+    cs.out[2] = at(saved, S.vs);
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
     cs = dense_call(d, a, kFwdDown);
-    cs.a0 = at(workspace, L.hs);
-    cs.b0 = w->Ws_down;
-    cs.out0 = at(workspace, L.os);
+    cs.a[0] = W(L.hs);
+    cs.b[0] = w->Ws_down;
+    cs.out[0] = W(L.os);
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
-    shared_out = at(workspace, L.os);
+    shared_out = W(L.os);
   }
   // weighted combine in slot order
   MOK_LAUNCH("combine", launch_combine(d, o, *sched, a, shared_out, true, y, s));
@@ -492,6 +496,8 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   if (!x || !dY || !dX || !aligned(x, 16) || !aligned(dY, 16) || !aligned(dX, 16))
     return MOK_ERR_INVALID_ARG;
   if (!g || !g->dW_up || !g->dW_gate || !g->dW_down || !g->dgates) return MOK_ERR_INVALID_ARG;
+  if (!aligned(g->dW_up, 16) || !aligned(g->dW_gate, 16) || !aligned(g->dW_down, 16))
+    return MOK_ERR_INVALID_ARG;
   if (ctx->precision == MOK_MXFP8 && (!w->mx || !aligned(w->mx, 256))) return MOK_ERR_INVALID_ARG;
   if (d.router && (!Wr || !g->dWr)) return MOK_ERR_INVALID_ARG;
   if (!d.router && (Wr || g->dWr)) return MOK_ERR_INVALID_ARG;
@@ -503,41 +509,44 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   AuxPtrs a = aux_ptrs(d, sched->aux);
   BwdWs L = bwd_ws(d);
   SavedLayout S = saved_layout(d);
-  void* dyg = at(workspace, L.dyg);
-  void* xg = at(workspace, L.xg);
-  void* du = at(workspace, L.du);
-  void* dv = at(workspace, L.dv);
-  void* hg = at(workspace, L.hg);
-  void* dxg = at(workspace, L.dxg);
-  float* dgp = reinterpret_cast<float*>(at(workspace, L.dgp));
-  float* dl = reinterpret_cast<float*>(at(workspace, L.dl));
-
+  auto W = [&](size_t off) -> void* { return at(workspace, off); };
+  const float* su = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.u));
+  const float* sv = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.v));
+  void* dxg = W(L.dxg);
+  float* dgp = reinterpret_cast<float*>(W(L.dgp));
+  float* dl = reinterpret_cast<float*>(W(L.dl));
   const bool mx = ctx->precision == MOK_MXFP8;
   MxWeights M = mx_weights_layout(d);
   char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
-  auto W = [&](size_t off) -> void* { return at(workspace, off); };
+
   if (!mx) {
     // reverse dispatch of dY and replay of the forward gather, both through the table
-    MOK_LAUNCH("reverse_dispatch_gather", launch_gather_rows(d, dY, *sched, a, dyg, ctx->num_sms, s));
-    MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, xg, ctx->num_sms, s));
+    MOK_LAUNCH("reverse_dispatch_gather",
+               launch_gather_rows(d, dY, *sched, a, W(L.dyg), ctx->num_sms, s));
+    MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), ctx->num_sms, s));
     // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
     GemmCall c = routed_call(d, sched, a, kBwdDH);
-    c.a0 = dyg;
-    c.b0 = w->W_down;
-    c.aux0 = at(const_cast<void*>(saved), S.u);
-    c.aux1 = at(const_cast<void*>(saved), S.v);
-    c.out0 = du;
-    c.out1 = dv;
-    c.out2 = hg;
+    c.a[0] = W(L.dyg);
+    c.b[0] = w->W_down;
+    c.u = su;
+    c.v = sv;
+    c.out[0] = W(L.du);
+    c.out[1] = W(L.du_lo);
+    c.out[2] = W(L.dv);
+    c.out[3] = W(L.dv_lo);
+    c.out[4] = W(L.hg);
+    c.out[5] = W(L.hg_lo);
     c.dgp = dgp;
     MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
     // dXg = du W_up^T + dv W_gate^T
     c = routed_call(d, sched, a, kBwdDX);
-    c.a0 = du;
-    c.a1 = dv;
-    c.b0 = w->W_up;
-    c.b1 = w->W_gate;
-    c.out0 = dxg;
+    c.a[0] = W(L.du);
+    c.a[1] = W(L.du_lo);
+    c.a[2] = W(L.dv);
+    c.a[3] = W(L.dv_lo);
+    c.b[0] = w->W_up;
+    c.b[1] = w->W_gate;
+    c.out[0] = dxg;
     MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
   } else {
     // reverse dispatch of dY (blocks along H for the dH GEMM, 32-row blocks for dW_down)
@@ -552,12 +561,12 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
                                         s));
     GemmCall c = routed_call(d, sched, a, kBwdDH);
     c.mx = true;
-    c.a0 = W(L.q_dy_h);
+    c.a[0] = W(L.q_dy_h);
     c.sfa = W(L.sf_dy_h);
-    c.b0 = mxw + M.down_h;
+    c.b[0] = mxw + M.down_h;
     c.sfb0 = mxw + M.down_h_sf;
-    c.aux0 = at(const_cast<void*>(saved), S.u);
-    c.aux1 = at(const_cast<void*>(saved), S.v);
+    c.u = su;
+    c.v = sv;
     c.out_q[0] = W(L.q_du_i);
     c.out_sf[0] = W(L.sf_du_i);
     c.out_q[1] = W(L.q_dv_i);
@@ -572,39 +581,44 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     MOK_LAUNCH("gemm_bwd_dh_swiglu_mxfp8", launch_gemm(c, ctx->num_sms, s));
     c = routed_call(d, sched, a, kBwdDX);
     c.mx = true;
-    c.a0 = W(L.q_du_i);
+    c.a[0] = W(L.q_du_i);
     c.sfa = W(L.sf_du_i);
-    c.a1 = W(L.q_dv_i);
+    c.a[1] = W(L.q_dv_i);
     c.sfa1 = W(L.sf_dv_i);
-    c.b0 = mxw + M.up_i;
+    c.b[0] = mxw + M.up_i;
     c.sfb0 = mxw + M.up_i_sf;
-    c.b1 = mxw + M.gate_i;
+    c.b[1] = mxw + M.gate_i;
     c.sfb1 = mxw + M.gate_i_sf;
-    c.out0 = dxg;
+    c.out[0] = dxg;
     MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(c, ctx->num_sms, s));
   }
   // router-weight gradient and the renormalised-softmax backward
   MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I), *sched, a,
-                                                g->dgates, d.router ? dl : nullptr, s));
+                                              g->dgates, d.router ? dl : nullptr, s));
   const void* dxs = nullptr;
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDH);
-    cs.a0 = dY;
-    cs.b0 = w->Ws_down;
-    cs.aux0 = at(const_cast<void*>(saved), S.us);
-    cs.aux1 = at(const_cast<void*>(saved), S.vs);
-    cs.out0 = at(workspace, L.dus);
-    cs.out1 = at(workspace, L.dvs);
-    cs.out2 = at(workspace, L.hsg);
+    cs.a[0] = dY;
+    cs.b[0] = w->Ws_down;
+    cs.u = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.us));
+    cs.v = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.vs));
+    cs.out[0] = W(L.dus);
+    cs.out[1] = W(L.dus_lo);
+    cs.out[2] = W(L.dvs);
+    cs.out[3] = W(L.dvs_lo);
+    cs.out[4] = W(L.hsg);
+    cs.out[5] = W(L.hsg_lo);
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDX);
-    cs.a0 = at(workspace, L.dus);
-    cs.a1 = at(workspace, L.dvs);
-    cs.b0 = w->Ws_up;
-    cs.b1 = w->Ws_gate;
-    cs.out0 = at(workspace, L.dxs);
+    cs.a[0] = W(L.dus);
+    cs.a[1] = W(L.dus_lo);
+    cs.a[2] = W(L.dvs);
+    cs.a[3] = W(L.dvs_lo);
+    cs.b[0] = w->Ws_up;
+    cs.b[1] = w->Ws_gate;
+    cs.out[0] = W(L.dxs);
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
-    dxs = at(workspace, L.dxs);
+    dxs = W(L.dxs);
   }
   // dX: reverse combine in slot order (+ shared expert, + router path)
   float* wrt = reinterpret_cast<float*>(at(workspace, L.dxs + 4 * (size_t)d.T * d.H));
@@ -614,35 +628,52 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   // weight gradients, each a fixed-order sum over the expert's rows
   GemmCall c = routed_call(d, sched, a, kBwdDWUpGate);
   c.mx = mx;
-  c.a0 = mx ? W(L.q_x_r) : xg;
-  c.b0 = mx ? W(L.q_du_r) : du;
-  c.b1 = mx ? W(L.q_dv_r) : dv;
-  c.sfa = W(L.sf_x_r);
-  c.sfb0 = W(L.sf_du_r);
-  c.sfb1 = W(L.sf_dv_r);
-  c.out0 = g->dW_up;
-  c.out1 = g->dW_gate;
+  if (mx) {
+    c.a[0] = W(L.q_x_r);
+    c.b[0] = W(L.q_du_r);
+    c.b[1] = W(L.q_dv_r);
+    c.sfa = W(L.sf_x_r);
+    c.sfb0 = W(L.sf_du_r);
+    c.sfb1 = W(L.sf_dv_r);
+  } else {
+    c.a[0] = W(L.xg);
+    c.b[0] = W(L.du);
+    c.b[1] = W(L.dv);
+    c.b[2] = W(L.du_lo);
+    c.b[3] = W(L.dv_lo);
+  }
+  c.out[0] = g->dW_up;
+  c.out[1] = g->dW_gate;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
   c = routed_call(d, sched, a, kBwdDWDown);
   c.mx = mx;
-  c.a0 = mx ? W(L.q_hg_r) : hg;
-  c.b0 = mx ? W(L.q_dy_r) : dyg;
-  c.sfa = W(L.sf_hg_r);
-  c.sfb0 = W(L.sf_dy_r);
-  c.out0 = g->dW_down;
+  if (mx) {
+    c.a[0] = W(L.q_hg_r);
+    c.b[0] = W(L.q_dy_r);
+    c.sfa = W(L.sf_hg_r);
+    c.sfb0 = W(L.sf_dy_r);
+  } else {
+    c.a[0] = W(L.hg);
+    c.a[1] = W(L.hg_lo);
+    c.b[0] = W(L.dyg);
+  }
+  c.out[0] = g->dW_down;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDWUpGate);
-    cs.a0 = x;
-    cs.b0 = at(workspace, L.dus);
-    cs.b1 = at(workspace, L.dvs);
-    cs.out0 = g->dWs_up;
-    cs.out1 = g->dWs_gate;
+    cs.a[0] = x;
+    cs.b[0] = W(L.dus);
+    cs.b[1] = W(L.dvs);
+    cs.b[2] = W(L.dus_lo);
+    cs.b[3] = W(L.dvs_lo);
+    cs.out[0] = g->dWs_up;
+    cs.out[1] = g->dWs_gate;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDWDown);
-    cs.a0 = at(workspace, L.hsg);
-    cs.b0 = dY;
-    cs.out0 = g->dWs_down;
+    cs.a[0] = W(L.hsg);
+    cs.a[1] = W(L.hsg_lo);
+    cs.b[0] = dY;
+    cs.out[0] = g->dWs_down;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
   }
   if (d.router) MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, dl, g->dWr, s));

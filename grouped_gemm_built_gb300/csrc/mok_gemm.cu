@@ -6,21 +6,27 @@
 // serves every GEMM of the layer:
 //
 //   warp 0      TMA producer: one lane streams A/B tiles (and, in MXFP8, their scale
-//               atoms) into a 4-stage ring of shared-memory buffers (128-byte swizzle);
+//               atoms) into a ring of shared-memory stages (128-byte swizzle);
 //   warp 1      MMA issuer: allocates 512 TMEM columns and issues tcgen05.mma
 //               (M=128, N=256) from one lane; BF16: kind::f16, K=16 per instruction, two
 //               256-column accumulators; MXFP8: kind::mxf8f6f4.block_scale, K=32 per
 //               instruction, one accumulator plus per-stage scale columns filled by
 //               tcgen05.cp;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output row), run
-//               the mode's fused math, store rows; with two accumulators the next tile's
-//               MMAs overlap this tile's epilogue.
+//               the mode's fused math, stage 32-row boxes in shared memory and store them
+//               with TMA; with two accumulators the next tile's MMAs overlap this epilogue.
 //
 // Tiles of the routed row space are 128 rows of one expert (segments are padded to 128
 // rows by the schedule), so a tile never mixes experts. Each output element is one fp32
-// sum in a fixed K order, so results are bitwise reproducible. Every mbarrier wait is
-// bounded by a deadline; on expiry the kernel records MOK_ERR_TIMEOUT in the status
-// word, drains its outstanding copies and returns.
+// sum in a fixed K order, so results are bitwise reproducible.
+//
+// Precision of the BF16 backward: the computed operands du, dv and g*h are kept as a pair
+// of bf16 values (hi = bf16(v), lo = bf16(v - hi)); the dX and dW GEMMs run both halves
+// of each K chunk back to back into the same fp32 accumulator, so these operands carry a
+// 16-bit significand while the tensor cores still take bf16.
+//
+// Every mbarrier wait is bounded by a deadline; on expiry the kernel records
+// MOK_ERR_TIMEOUT in the status word, drains its outstanding copies and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -38,15 +44,17 @@ namespace mok {
 namespace {
 
 constexpr int BM = 128;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = 16384;              // 128 rows x 128 bytes
 constexpr int B_BYTES = 32768;              // 256 rows x 128 bytes
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int STAGE_OUT_BYTES = 4096;               // one 32-row epilogue staging box
+constexpr int OUT_STAGING = 4 * 2 * STAGE_OUT_BYTES;  // 4 epilogue warps x 2 buffers
 
 template <bool MX>
 struct Cfg {
+  static constexpr int STAGES = MX ? 3 : 4;          // an MXFP8 stage holds twice the K
   static constexpr int BK = MX ? 128 : 64;           // K elements per stage (128 bytes/row)
   static constexpr int MMA_K = MX ? 32 : 16;         // K elements per instruction
   static constexpr int MN_CHUNK = MX ? 128 : 64;     // elements per 128-byte MN-major chunk
@@ -57,7 +65,14 @@ struct Cfg {
   static constexpr int NACC = MX ? 1 : 2;
   static constexpr int ACC_COLS = 256;
   static constexpr int SF_TMEM = 256;                // MX: scale columns start here
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING + 1024 + 256;
+};
+
+// Tensor maps of one launch: operands a[], b[] (loads) and outputs o[] (stores).
+struct Maps {
+  CUtensorMap a[4];
+  CUtensorMap b[4];
+  CUtensorMap o[6];
 };
 
 struct Params {
@@ -70,7 +85,8 @@ struct Params {
   int n_tiles;      // tiles along N
   int m_tiles_dw;   // dW modes: tiles along M of one expert's dW
   int groups;
-  int kiters;       // row-space modes: K / BK
+  int kiters;       // row-space modes: K iterations per tile
+  int split;        // 1: the dX / dW GEMMs run hi and lo halves of their computed operand
   // schedule
   const int32_t* poff;
   const int32_t* counts;
@@ -79,22 +95,17 @@ struct Params {
   const int32_t* num_mtiles;
   const int32_t* table;
   const float* gates;
-  // epilogue
-  __nv_bfloat16* out0;
-  __nv_bfloat16* out1;
-  __nv_bfloat16* out2;
-  const __nv_bfloat16* aux0;
-  const __nv_bfloat16* aux1;
-  float* outf0;     // fp32 outputs: O / dXg rows, dW (dW_up, dW_gate)
-  float* outf1;
+  // epilogue inputs
+  const float* u;   // kBwdDH: saved U, V [rows][I] fp32
+  const float* v;
   float* dgp;
   uint32_t* status;
   // MXFP8 scale atoms (512 B each): A side [row tile][kcs_a], B side [e][kcs_b][ncs_b]
   const uint8_t* sfa;
+  const uint8_t* sfa1;
   const uint8_t* sfb0;
   const uint8_t* sfb1;
   int kcs_a, kcs_b, ncs_b;
-  const uint8_t* sfa1;  // second A operand's atoms (kBwdDX: dv)
   // MX outputs. kFwdUpGate: q[0] = h along I. kBwdDH: q[0], q[1] = du, dv along I;
   // q[2], q[3], q[4] = du, dv, g*h in 32-row blocks. E4M3 [rows][I], atoms [row tile][I/128].
   uint8_t* out_q[5];
@@ -136,6 +147,7 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
       ti.krow0 = p.poff[ti.e];
       ti.kiters = (p.poff[ti.e + 1] - ti.krow0) / BK;
     }
+    ti.kiters <<= p.split;
   } else {
     const int mt = tile / p.n_tiles;
     ti.e = p.dense ? 0 : min(max(p.tile_expert[mt], 0), p.groups - 1);
@@ -151,37 +163,27 @@ __device__ __forceinline__ void set_error(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void load_f32x32(const float* src, float* v) {
+  const float4* s = reinterpret_cast<const float4*>(src);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-    d[q] = w;
-  }
-}
-__device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
-  float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w = __ldg(s + q);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 f = __bfloat1622float2(h[i]);
-      v[8 * q + 2 * i] = f.x;
-      v[8 * q + 2 * i + 1] = f.y;
-    }
+  for (int q = 0; q < 8; ++q) {
+    const float4 w = __ldg(s + q);
+    v[4 * q] = w.x;
+    v[4 * q + 1] = w.y;
+    v[4 * q + 2] = w.z;
+    v[4 * q + 3] = w.w;
   }
 }
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.f / (1.f + __expf(-v)); }
+
+// bf16 pair of an fp32 value: hi = bf16(v), lo = bf16(v - hi) (v - hi is exact in fp32).
+__device__ __forceinline__ void split_bf16(const float* v, float* hi, float* lo) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    hi[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+    lo[i] = v[i] - hi[i];
+  }
+}
 
 // MXFP8 block of 32 (one thread's chunk): returns the scale byte, writes 32 E4M3 codes.
 __device__ __forceinline__ uint32_t quant32_e4m3(const float* v, uint4* q2) {
@@ -208,15 +210,69 @@ __device__ __forceinline__ uint32_t quant32_e4m3(const float* v, uint4* q2) {
   return sb;
 }
 
+// Epilogue output path: a warp stages its 32 rows x 128 bytes in shared memory (swizzled
+// like the TMA box, so the 16-byte stores of 32 lanes spread over all banks) and one lane
+// stores the box with TMA. Two buffers per warp: a buffer is refilled only after the TMA
+// store issued two boxes earlier has finished reading it. Every lane calls these.
+struct Stager {
+  uint8_t* buf;   // this warp's 2 x 4 KB, 1024-byte aligned
+  uint32_t n;
+  int lane;
+  __device__ __forceinline__ uint8_t* next() {
+    uint8_t* b = buf + (n & 1) * STAGE_OUT_BYTES;
+    if (n >= 2 && lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    return b;
+  }
+  __device__ __forceinline__ void issue(const CUtensorMap* m, const uint8_t* b, int col, int row) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(m, b, col, row);
+      bulk_commit();
+    }
+    ++n;
+  }
+  // 32 fp32 of this lane's row -> box (32 cols, 32 rows), 128-byte swizzle
+  __device__ __forceinline__ void f32(const CUtensorMap* m, const float* v, int col, int row) {
+    uint8_t* b = next();
+    uint8_t* r = b + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(r + ((j ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    issue(m, b, col, row);
+  }
+  // 32 bf16 of this lane's row -> box (32 cols, 32 rows), 64-byte swizzle
+  __device__ __forceinline__ void bf16(const CUtensorMap* m, const float* v, int col, int row) {
+    uint8_t* b = next();
+    uint8_t* r = b + lane * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 w;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+      *reinterpret_cast<uint4*>(r + ((j ^ ((lane >> 1) & 3)) << 4)) = w;
+    }
+    issue(m, b, col, row);
+  }
+  __device__ __forceinline__ void drain() {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
 // ------------------------------------------------------------------ producer
 template <bool MX>
-__device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorMap* tA1,
-                        const CUtensorMap* tB0, const CUtensorMap* tB1, uint8_t* smem,
-                        uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+__device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
+                        uint64_t* empty, volatile int* abort_flag) {
   using C = Cfg<MX>;
   constexpr int BK = C::BK;
+  constexpr int STAGES = C::STAGES;
   constexpr int CH = C::MN_LBO;        // bytes of one MN-major chunk
   const int ntiles = num_tiles_of(p);
+  const int sp = p.split;
   uint32_t it = 0;
   uint32_t b_bytes = (p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 256 * 128 : p.BN * 128;
   if (MX) b_bytes += 512 + ((p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 1024 : p.BN * 4);
@@ -238,13 +294,16 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
       uint64_t* bar = &full[stage];
       mbar_arrive_expect_tx(bar, A_BYTES + b_bytes);
       const int k0 = kb * BK;
+      // with split operands, iteration kb covers K chunk kb >> 1, half kb & 1
+      const int chunk = kb >> sp, part = kb & sp;
       switch (p.mode) {
         case kFwdUpGate: {   // A: Xg rows (K-major); B: W_up|W_gate cols n0..n0+127 (MN-major)
-          tma_load_2d(sa, tA0, bar, k0, ti.row0);
+          tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
           const int brow = ti.e * p.H + k0;
           for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
-            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, brow);
-            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, tB1, bar, ti.n0 + c * C::MN_CHUNK, brow);
+            tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, brow);
+            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, &mp.b[1], bar, ti.n0 + c * C::MN_CHUNK,
+                        brow);
           }
           if (MX) {
             bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
@@ -255,10 +314,10 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
           break;
         }
         case kFwdDown: {     // A: h rows (K-major); B: W_down cols (MN-major)
-          tma_load_2d(sa, tA0, bar, k0, ti.row0);
+          tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
           const int brow = ti.e * p.I + k0;
           for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
-            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, brow);
+            tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, brow);
           if (MX) {
             bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
             const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
@@ -267,8 +326,8 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
           break;
         }
         case kBwdDH: {       // A: dYg rows (K-major); B: W_down rows i (K-major over H)
-          tma_load_2d(sa, tA0, bar, k0, ti.row0);
-          tma_load_2d(sb, tB0, bar, k0, ti.e * p.I + ti.n0);
+          tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
+          tma_load_2d(sb, &mp.b[0], bar, k0, ti.e * p.I + ti.n0);
           if (MX) {
             bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
             const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
@@ -277,11 +336,13 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
           break;
         }
         case kBwdDX: {       // K = [I of du | I of dv]; B: W_up / W_gate rows h (K-major over I)
-          const int half = p.I / BK;
-          const bool second = kb >= half;
-          const int kq = second ? kb - half : kb;
-          tma_load_2d(sa, second ? tA1 : tA0, bar, kq * BK, ti.row0);
-          tma_load_2d(sb, second ? tB1 : tB0, bar, kq * BK, ti.e * p.H + ti.n0);
+          const int per_half = (p.I / BK) << sp;
+          const int second = kb >= per_half ? 1 : 0;
+          const int r = kb - second * per_half;
+          const int kq = r >> sp;                  // K chunk inside the half
+          const int ai = MX ? second : 2 * second + (r & sp);
+          tma_load_2d(sa, &mp.a[ai], bar, kq * BK, ti.row0);
+          tma_load_2d(sb, &mp.b[second], bar, kq * BK, ti.e * p.H + ti.n0);
           if (MX) {
             bulk_load(sf, (second ? p.sfa1 : p.sfa) + ((size_t)(ti.row0 / BM) * p.kcs_a + kq) * 512,
                       512, bar);
@@ -290,12 +351,12 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
           }
           break;
         }
-        case kBwdDWDown: {   // A: (g h)^T (MN-major, M = I); B: dYg (MN-major, N = H)
-          const int kr = ti.krow0 + k0;
+        case kBwdDWDown: {   // A: (g h)^T (MN-major, M = I), hi/lo; B: dYg (MN-major, N = H)
+          const int kr = ti.krow0 + chunk * BK;
           for (int c = 0; c < BM / C::MN_CHUNK; ++c)
-            tma_load_2d(sa + c * CH, tA0, bar, ti.row0 + c * C::MN_CHUNK, kr);
+            tma_load_2d(sa + c * CH, &mp.a[part], bar, ti.row0 + c * C::MN_CHUNK, kr);
           for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
-            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, kr);
+            tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, kr);
           if (MX) {   // row-block atoms [row tile][M/128] and [row tile][N/128]
             bulk_load(sf, p.sfa + ((size_t)(kr / BM) * (p.I / 128) + ti.row0 / 128) * 512, 512, bar);
             bulk_load(sf + 512, p.sfb0 + ((size_t)(kr / BM) * (p.H / 128) + ti.n0 / 128) * 512,
@@ -303,13 +364,14 @@ __device__ void produce(const Params& p, const CUtensorMap* tA0, const CUtensorM
           }
           break;
         }
-        default: {           // kBwdDWUpGate: A: Xg^T (M = H); B: du | dv cols n0..n0+127
-          const int kr = ti.krow0 + k0;
+        default: {           // kBwdDWUpGate: A: Xg^T (M = H); B: du | dv cols n0..n0+127, hi/lo
+          const int kr = ti.krow0 + chunk * BK;
           for (int c = 0; c < BM / C::MN_CHUNK; ++c)
-            tma_load_2d(sa + c * CH, tA0, bar, ti.row0 + c * C::MN_CHUNK, kr);
+            tma_load_2d(sa + c * CH, &mp.a[0], bar, ti.row0 + c * C::MN_CHUNK, kr);
           for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
-            tma_load_2d(sb + c * CH, tB0, bar, ti.n0 + c * C::MN_CHUNK, kr);
-            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, tB1, bar, ti.n0 + c * C::MN_CHUNK, kr);
+            tma_load_2d(sb + c * CH, &mp.b[2 * part], bar, ti.n0 + c * C::MN_CHUNK, kr);
+            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, &mp.b[2 * part + 1], bar,
+                        ti.n0 + c * C::MN_CHUNK, kr);
           }
           if (MX) {
             bulk_load(sf, p.sfa + ((size_t)(kr / BM) * (p.H / 128) + ti.row0 / 128) * 512, 512, bar);
@@ -341,6 +403,7 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
                           uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
                           volatile int* abort_flag) {
   using C = Cfg<MX>;
+  constexpr int STAGES = C::STAGES;
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
@@ -411,13 +474,14 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
 
 // ------------------------------------------------------------------ epilogue
 template <bool MX>
-__device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empty,
-                         uint32_t tmem_base, volatile int* abort_flag) {
+__device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint64_t* acc_full,
+                         uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag) {
   using C = Cfg<MX>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
   const int r = quarter * 32 + lane;        // row inside the tile
   const int ntiles = num_tiles_of(p);
+  Stager st{staging + (warp - 2) * 2 * STAGE_OUT_BYTES, 0u, lane};
   int local = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
     const TileInfo ti = tile_info<MX>(p, tile);
@@ -426,15 +490,16 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
     if (!mbar_wait(&acc_full[acc], use & 1, globaltimer_ns() + kTimeoutNs)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
-      return;
+      break;
     }
     tc_fence_after();
     const uint32_t t_row = tmem_base + acc * C::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
     const bool have = ti.kiters > 0;
     float a[32], b[32];
-    // tcgen05.ld is warp-collective: every lane loads, rows outside the problem only
-    // skip their global loads and stores.
+    // tcgen05.ld and the staged stores are warp-collective: every lane takes part, rows
+    // outside the problem only skip their global loads (TMA drops their stores).
     const int row = ti.row0 + r;
+    const int wrow = ti.row0 + quarter * 32;  // first row of this warp's 32-row box
     const bool valid = !(p.dense && !is_dw(p.mode) && row >= p.M_rows);
     switch (p.mode) {
       case kFwdUpGate: {
@@ -443,21 +508,23 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
         for (int c = 0; c < 4; ++c) {
           tmem_ld32(t_row + c * 32, a);          // U
           tmem_ld32(t_row + 128 + c * 32, b);    // V
-          if (!valid) continue;
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
+          const int col = ti.n0 + c * 32;
           if (MX) {   // h feeds the down GEMM as MXFP8 blocks of 32 along I
             uint4 q[2];
             sbytes |= quant32_e4m3(h, q) << (8 * c);
-            uint4* dq = reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32);
-            dq[0] = q[0];
-            dq[1] = q[1];
+            if (valid) {
+              uint4* dq = reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32);
+              dq[0] = q[0];
+              dq[1] = q[1];
+            }
           } else {
-            store_bf16x32(p.out0 + o + c * 32, h);
+            st.bf16(&mp.o[0], h, col, wrow);     // h, bf16 operand of the down GEMM
           }
-          store_bf16x32(p.out1 + o + c * 32, a);
-          store_bf16x32(p.out2 + o + c * 32, b);
+          st.f32(&mp.o[1], a, col, wrow);        // saved U, fp32
+          st.f32(&mp.o[2], b, col, wrow);        // saved V, fp32
         }
         if (MX && valid) {
           const size_t atom = (size_t)(row / BM) * (p.I / 128) + ti.n0 / 128;
@@ -468,10 +535,9 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
       }
       case kFwdDown:
       case kBwdDX: {   // expert outputs / routed dX rows, fp32
-        const size_t o = (size_t)row * p.H + ti.n0;
         for (int c = 0; c < p.BN / 32; ++c) {
           tmem_ld32(t_row + c * 32, a);
-          if (valid) store_f32x32(p.outf0 + o + c * 32, a);
+          st.f32(&mp.o[0], a, ti.n0 + c * 32, wrow);
         }
         break;
       }
@@ -488,11 +554,16 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
         const size_t o = (size_t)row * p.I + ti.n0;
         float dg = 0.f;
         for (int c = 0; c < p.BN / 32; ++c) {
+          const int col = ti.n0 + c * 32;
           tmem_ld32(t_row + c * 32, a);          // D = dY W_down^T
-          if (!valid) continue;
           float u[32], v[32];
-          load_bf16x32(p.aux0 + o + c * 32, u);  // saved U
-          load_bf16x32(p.aux1 + o + c * 32, v);  // saved V
+          if (valid) {
+            load_f32x32(p.u + o + c * 32, u);    // saved U
+            load_f32x32(p.v + o + c * 32, v);    // saved V
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = v[i] = a[i] = 0.f;
+          }
           float du[32], dv[32], hg[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -505,22 +576,34 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
             dv[i] = dh * u[i] * (sg * (1.f + v[i] * (1.f - sg)));
             hg[i] = g * hv;
           }
-          if (!MX) {
-            store_bf16x32(p.out0 + o + c * 32, du);
-            store_bf16x32(p.out1 + o + c * 32, dv);
-            store_bf16x32(p.out2 + o + c * 32, hg);
+          if (!MX) {   // bf16 hi/lo pairs of du, dv, g*h
+            float hi[32], lo[32];
+            split_bf16(du, hi, lo);
+            st.bf16(&mp.o[0], hi, col, wrow);
+            st.bf16(&mp.o[1], lo, col, wrow);
+            split_bf16(dv, hi, lo);
+            st.bf16(&mp.o[2], hi, col, wrow);
+            st.bf16(&mp.o[3], lo, col, wrow);
+            split_bf16(hg, hi, lo);
+            st.bf16(&mp.o[4], hi, col, wrow);
+            st.bf16(&mp.o[5], lo, col, wrow);
           } else {
             // du, dv feed the dX GEMM (K = I): per-thread blocks of 32 along I
-            const int col = ti.n0 + c * 32;
             const size_t atom_i = ((size_t)(row / BM) * (p.I / 128) + col / 128) * 512 +
                                   16 * (r & 31) + 4 * (r >> 5) + ((col & 127) >> 5);
             uint4 q[2];
-            p.out_sf[0][atom_i] = (uint8_t)quant32_e4m3(du, q);
-            reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32)[0] = q[0];
-            reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32)[1] = q[1];
-            p.out_sf[1][atom_i] = (uint8_t)quant32_e4m3(dv, q);
-            reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[0] = q[0];
-            reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[1] = q[1];
+            const uint8_t sb_du = (uint8_t)quant32_e4m3(du, q);
+            if (valid) {
+              p.out_sf[0][atom_i] = sb_du;
+              reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32)[0] = q[0];
+              reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32)[1] = q[1];
+            }
+            const uint8_t sb_dv = (uint8_t)quant32_e4m3(dv, q);
+            if (valid) {
+              p.out_sf[1][atom_i] = sb_dv;
+              reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[0] = q[0];
+              reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[1] = q[1];
+            }
           }
         }
         if (MX) {
@@ -532,8 +615,8 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
             float u[32], v[32];
             tmem_ld32(t_row + c * 32, a);
             if (valid) {
-              load_bf16x32(p.aux0 + o2, u);
-              load_bf16x32(p.aux1 + o2, v);
+              load_f32x32(p.u + o2, u);
+              load_f32x32(p.v + o2, v);
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i) u[i] = v[i] = 0.f;
@@ -573,9 +656,6 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
                 uint4* dq = reinterpret_cast<uint4*>(p.out_q[2 + out] + o2);
                 dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
-              } else if (!p.dense) {   // padding rows of the row space: zero codes
-                uint4* dq = reinterpret_cast<uint4*>(p.out_q[2 + out] + o2);
-                dq[0] = dq[1] = make_uint4(0, 0, 0, 0);
               }
               p.out_sf[2 + out][atom_r] = (uint8_t)my_sb;
             }
@@ -584,20 +664,20 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
         if (valid && p.dgp) p.dgp[(size_t)row * p.n_tiles + ti.n0 / p.BN] = dg;
         break;
       }
-      case kBwdDWDown: {                         // row = i index of dW_down[e], fp32
-        float* dst = p.outf0 + ((size_t)ti.e * p.I + row) * p.H + ti.n0;
+      case kBwdDWDown: {                         // rows = i of dW_down[e], fp32
+        const int orow = ti.e * p.I + wrow;
         for (int c = 0; c < p.BN / 32; ++c) {
           if (have) tmem_ld32(t_row + c * 32, a);
           else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = 0.f;
           }
-          store_f32x32(dst + c * 32, a);
+          st.f32(&mp.o[0], a, ti.n0 + c * 32, orow);
         }
         break;
       }
-      default: {                                 // kBwdDWUpGate; row = h index, fp32
-        const size_t o = ((size_t)ti.e * p.H + row) * p.I + ti.n0;
+      default: {                                 // kBwdDWUpGate; rows = h, fp32
+        const int orow = ti.e * p.H + wrow;
         for (int c = 0; c < 4; ++c) {
           if (have) {
             tmem_ld32(t_row + c * 32, a);
@@ -606,8 +686,8 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.f;
           }
-          store_f32x32(p.outf0 + o + c * 32, a);
-          store_f32x32(p.outf1 + o + c * 32, b);
+          st.f32(&mp.o[0], a, ti.n0 + c * 32, orow);
+          st.f32(&mp.o[1], b, ti.n0 + c * 32, orow);
         }
         break;
       }
@@ -615,17 +695,18 @@ __device__ void epilogue(const Params& p, uint64_t* acc_full, uint64_t* acc_empt
     tc_fence_before();
     mbar_arrive(&acc_empty[acc]);
   }
+  st.drain();
 }
 
 template <bool MX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0, const __grid_constant__ CUtensorMap tA1,
-                        const __grid_constant__ CUtensorMap tB0, const __grid_constant__ CUtensorMap tB1,
-                        const Params p) {
+    grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p) {
   using C = Cfg<MX>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + OUT_STAGING);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -644,8 +725,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tA0);
-    tma_prefetch_desc(&tB0);
+    tma_prefetch_desc(&mp.a[0]);
+    tma_prefetch_desc(&mp.b[0]);
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -654,12 +735,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (threadIdx.x == 0) produce<MX>(p, &tA0, &tA1, &tB0, &tB1, smem, full, empty, abort_flag);
+    if (threadIdx.x == 0) produce<MX>(p, mp, smem, full, empty, abort_flag);
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0)
       mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag);
   } else {
-    epilogue<MX>(p, acc_full, acc_empty, tmem_base, abort_flag);
+    epilogue<MX>(p, mp, staging, acc_full, acc_empty, tmem_base, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -707,6 +788,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, in
   return r == CUDA_SUCCESS;
 }
 
+// Output map for the epilogue's 32 x 32 boxes: fp32 (128-byte rows, 128-byte swizzle) or
+// bf16 (64-byte rows, 64-byte swizzle); stores outside the matrix are dropped.
+bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int elem_bytes) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || base == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * elem_bytes};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   elem_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <bool MX>
 cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   using C = Cfg<MX>;
@@ -728,6 +825,7 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.I = c.I;
   p.k = c.k;
   p.groups = c.dense ? 1 : c.groups;
+  p.split = (!MX && (c.mode == kBwdDX || c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
   p.poff = c.poff;
   p.counts = c.counts;
   p.offsets = c.offsets;
@@ -735,19 +833,14 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.num_mtiles = c.num_mtiles;
   p.table = c.table;
   p.gates = c.gates;
-  p.out0 = static_cast<__nv_bfloat16*>(c.out0);
-  p.out1 = static_cast<__nv_bfloat16*>(c.out1);
-  p.out2 = static_cast<__nv_bfloat16*>(c.out2);
-  p.aux0 = static_cast<const __nv_bfloat16*>(c.aux0);
-  p.aux1 = static_cast<const __nv_bfloat16*>(c.aux1);
-  p.outf0 = static_cast<float*>(c.out0);
-  p.outf1 = static_cast<float*>(c.out1);
+  p.u = c.u;
+  p.v = c.v;
   p.dgp = c.dgp;
   p.status = c.status;
   p.sfa = static_cast<const uint8_t*>(c.sfa);
+  p.sfa1 = static_cast<const uint8_t*>(c.sfa1);
   p.sfb0 = static_cast<const uint8_t*>(c.sfb0);
   p.sfb1 = static_cast<const uint8_t*>(c.sfb1);
-  p.sfa1 = static_cast<const uint8_t*>(c.sfa1);
   for (int i = 0; i < 5; ++i) {
     p.out_q[i] = static_cast<uint8_t*>(c.out_q[i]);
     p.out_sf[i] = static_cast<uint8_t*>(c.out_sf[i]);
@@ -756,9 +849,8 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   const int eb = MX ? 1 : 2;                  // element bytes of the GEMM operands
   const uint64_t rows = (uint64_t)c.M_rows;   // rows of the row-space buffers
   const uint64_t G = (uint64_t)p.groups;
-  CUtensorMap tA0, tA1, tB0, tB1;
-  memset(&tA1, 0, sizeof(tA1));
-  memset(&tB1, 0, sizeof(tB1));
+  Maps mp;
+  memset(&mp, 0, sizeof(mp));
   bool ok = true;
   int max_tiles = 0;
   const int mt_rows = (int)((rows + BM - 1) / BM);
@@ -771,8 +863,12 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.kcs_a = c.H / 128;
       p.kcs_b = c.H / 128;
       p.ncs_b = c.I / 128;
-      ok = make_map(&tA0, c.a0, c.H, rows, BM, eb) && make_map(&tB0, c.b0, c.I, G * c.H, BK, eb) &&
-           make_map(&tB1, c.b1, c.I, G * c.H, BK, eb);
+      ok = make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
+           make_map(&mp.b[0], c.b[0], c.I, G * c.H, BK, eb) &&
+           make_map(&mp.b[1], c.b[1], c.I, G * c.H, BK, eb) &&
+           (MX || make_out_map(&mp.o[0], c.out[0], c.I, rows, 2)) &&
+           make_out_map(&mp.o[1], c.out[1], c.I, rows, 4) &&
+           make_out_map(&mp.o[2], c.out[2], c.I, rows, 4);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kFwdDown:
@@ -782,7 +878,9 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.kcs_a = c.I / 128;
       p.kcs_b = c.I / 128;
       p.ncs_b = c.H / 128;
-      ok = make_map(&tA0, c.a0, c.I, rows, BM, eb) && make_map(&tB0, c.b0, c.H, G * c.I, BK, eb);
+      ok = make_map(&mp.a[0], c.a[0], c.I, rows, BM, eb) &&
+           make_map(&mp.b[0], c.b[0], c.H, G * c.I, BK, eb) &&
+           make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDH:
@@ -792,43 +890,48 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.kcs_a = c.H / 128;
       p.kcs_b = c.H / 128;
       p.ncs_b = c.I / 128;
-      ok = make_map(&tA0, c.a0, c.H, rows, BM, eb) && make_map(&tB0, c.b0, c.H, G * c.I, p.BN, eb);
+      ok = make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
+           make_map(&mp.b[0], c.b[0], c.H, G * c.I, p.BN, eb);
+      for (int i = 0; i < 6 && ok && !MX; ++i) ok = make_out_map(&mp.o[i], c.out[i], c.I, rows, 2);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDX:
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
-      p.kiters = 2 * (c.I / BK);
+      p.kiters = (2 * (c.I / BK)) << p.split;
       p.kcs_a = c.I / 128;
       p.kcs_b = c.I / 128;
       p.ncs_b = c.H / 128;
-      ok = make_map(&tA0, c.a0, c.I, rows, BM, eb) && make_map(&tA1, c.a1, c.I, rows, BM, eb) &&
-           make_map(&tB0, c.b0, c.I, G * c.H, p.BN, eb) &&
-           make_map(&tB1, c.b1, c.I, G * c.H, p.BN, eb);
+      for (int i = 0; i < (MX ? 2 : 4) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BM, eb);
+      ok = ok && make_map(&mp.b[0], c.b[0], c.I, G * c.H, p.BN, eb) &&
+           make_map(&mp.b[1], c.b[1], c.I, G * c.H, p.BN, eb) &&
+           make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDWDown:
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
       p.m_tiles_dw = c.I / BM;
-      ok = make_map(&tA0, c.a0, c.I, rows, BK, eb) && make_map(&tB0, c.b0, c.H, rows, BK, eb);
+      for (int i = 0; i < (MX ? 1 : 2) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BK, eb);
+      ok = ok && make_map(&mp.b[0], c.b[0], c.H, rows, BK, eb) &&
+           make_out_map(&mp.o[0], c.out[0], c.H, G * c.I, 4);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
     case kBwdDWUpGate:
       p.BN = 256;
       p.n_tiles = c.I / 128;
       p.m_tiles_dw = c.H / BM;
-      ok = make_map(&tA0, c.a0, c.H, rows, BK, eb) && make_map(&tB0, c.b0, c.I, rows, BK, eb) &&
-           make_map(&tB1, c.b1, c.I, rows, BK, eb);
+      ok = make_map(&mp.a[0], c.a[0], c.H, rows, BK, eb);
+      for (int i = 0; i < (MX ? 2 : 4) && ok; ++i) ok = make_map(&mp.b[i], c.b[i], c.I, rows, BK, eb);
+      ok = ok && make_out_map(&mp.o[0], c.out[0], c.I, G * c.H, 4) &&
+           make_out_map(&mp.o[1], c.out[1], c.I, G * c.H, 4);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
-  if (c.mode != kBwdDX) tA1 = tA0;  // second maps only used by the modes that set them
-  if (c.mode == kFwdDown || c.mode == kBwdDH || c.mode == kBwdDWDown) tB1 = tB0;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MX><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(tA0, tA1, tB0, tB1, p);
+  grouped_gemm_kernel<MX><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(mp, p);
   return cudaGetLastError();
 }
 

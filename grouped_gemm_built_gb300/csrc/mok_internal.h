@@ -48,12 +48,13 @@ struct MxWeights {
 // scratch for the backward. MXFP8 operands (E4M3 + atoms): dY along H (dH GEMM), dY and
 // x in 32-row blocks (dW GEMMs), du/dv along I (dX GEMM), du/dv/g*h in 32-row blocks.
 struct BwdWs {
-  size_t dyg, xg, du, dv, hg, dxg, dgp, dl, dus, dvs, hsg, dxs;
+  size_t dyg, xg, du, dv, hg, du_lo, dv_lo, hg_lo, dxg, dgp, dl, dus, dvs, hsg, dus_lo,
+      dvs_lo, hsg_lo, dxs;
   size_t q_dy_h, sf_dy_h, q_dy_r, sf_dy_r, q_x_r, sf_x_r;
   size_t q_du_i, sf_du_i, q_dv_i, sf_dv_i, q_du_r, sf_du_r, q_dv_r, sf_dv_r, q_hg_r, sf_hg_r;
   size_t total;
 };
-// saved activations (forward -> backward)
+// saved activations (forward -> backward): U, V fp32
 struct SavedLayout {
   size_t u, v, us, vs, total;
 };
@@ -127,6 +128,17 @@ enum GemmMode : int {
   kBwdDWUpGate = 5, // dW_up = Xg^T du, dW_gate = Xg^T dv
 };
 
+// Operands per mode (BF16; MXFP8 in brackets):
+//   kFwdUpGate   a0 = Xg [x_q]; b0, b1 = W_up, W_gate; out0 = h bf16 [out_q0 + atoms],
+//                out1, out2 = U, V fp32 (saved)
+//   kFwdDown     a0 = h [h_q]; b0 = W_down; out0 = O fp32
+//   kBwdDH       a0 = dYg [dY_q]; b0 = W_down; u, v = saved U, V; out0..5 = du, dv, g*h as
+//                bf16 hi/lo pairs [out_q0..4 + atoms]; dgp
+//   kBwdDX       a0..3 = du_hi, du_lo, dv_hi, dv_lo [a0, a1 = du_q, dv_q]; b0, b1 = W_up,
+//                W_gate; out0 = dXg fp32
+//   kBwdDWDown   a0, a1 = g*h hi, lo [a0 = g*h_q]; b0 = dYg [dY_q]; out0 = dW_down fp32
+//   kBwdDWUpGate a0 = Xg [x_q]; b0, b1 = du_hi, dv_hi; b2, b3 = du_lo, dv_lo
+//                [b0, b1 = du_q, dv_q]; out0, out1 = dW_up, dW_gate fp32
 struct GemmCall {
   GemmMode mode;
   // problem
@@ -134,12 +146,12 @@ struct GemmCall {
   bool dense;           // one group over M_rows rows (shared expert); else routed groups
   int H, I;             // hidden size and this FFN's intermediate size
   int groups;           // experts (dense: 1)
-  // operands (device pointers)
-  const void* a0; const void* a1;      // row-space operands (Xg / h / dYg / du, dv ...)
-  const void* b0; const void* b1;      // weights
-  void* out0; void* out1; void* out2;  // outputs (bf16; fp32 for O, dXg and dW)
-  const void* aux0; const void* aux1;  // extra epilogue inputs (saved U, V)
-  float* dgp;                          // kBwdDH: per-tile partial router-weight gradients
+  const void* a[4];     // row-space operands
+  const void* b[4];     // weights / second row-space operand
+  void* out[6];         // outputs
+  const float* u;       // kBwdDH: saved U, V (fp32)
+  const float* v;
+  float* dgp;           // kBwdDH: per-tile partial router-weight gradients
   // schedule (routed case)
   const int32_t* poff; const int32_t* counts; const int32_t* offsets;
   const int32_t* tile_expert; const int32_t* num_mtiles;

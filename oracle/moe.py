@@ -29,12 +29,12 @@ Readings taken where the pages are silent (each is also listed in the design not
 * schedule order inside an expert: ascending token, then ascending slot;
 * gradients at the top-k boundary are taken with the selected set S held fixed.
 
-Precision model (``precision``): "fp64" applies no rounding at all. "bf16" and "mxfp8"
-round exactly where the GPU path stores a value in bf16 (U, V saved for the backward) or
-feeds a GEMM with a quantised operand (bf16 h, du, dv, g*h; or MXFP8 blocks of 32 along
-that GEMM's contraction axis). Expert outputs, the routed dX rows and the layer's
-results are fp32 on the GPU and stay unrounded here. Everything else is float64. The
-shared expert is always BF16.
+Precision model (``precision``): "fp64" applies no rounding at all. "bf16" rounds h, the
+operand of the down GEMM, to bf16; the GPU keeps U, V, expert outputs, routed dX rows and
+all results in fp32, and feeds du, dv and g*h to the backward GEMMs as bf16 hi/lo pairs
+(a 16-bit significand), so those stay unrounded here. "mxfp8" quantises every GEMM operand
+to MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, dv, g*h,
+dY). Everything else is float64. The shared expert is always BF16.
 """
 from __future__ import annotations
 
@@ -131,10 +131,6 @@ class Precision:
     def mx(self):
         return self.mode == "mxfp8"
 
-    def store(self, a):
-        """A tensor the GPU writes in bf16."""
-        return a if self.mode == "fp64" else bf16_round(a)
-
     def op(self, a, axis):
         """A GEMM operand that is already bf16-exact (inputs, weights): MXFP8 blocks of 32
         along the contraction axis ``axis`` in mxfp8 mode, unchanged otherwise."""
@@ -144,16 +140,19 @@ class Precision:
         """A GEMM operand whose contraction axis is the (ragged) expert-row axis 0."""
         return mx_qdq_rows_padded(a) if self.mx else a
 
-    def act(self, a, axis):
-        """A computed activation feeding a GEMM along ``axis``: bf16, or MXFP8 blocks."""
+    def fwd_act(self, a, axis):
+        """h, the forward down GEMM's operand: bf16, or MXFP8 blocks along ``axis``."""
         if self.mode == "fp64":
             return a
         return mx_qdq(a, axis) if self.mx else bf16_round(a)
 
-    def act_rows(self, a):
-        if self.mode == "fp64":
-            return a
-        return mx_qdq_rows_padded(a) if self.mx else bf16_round(a)
+    def bwd_act(self, a, axis):
+        """du, dv, g*h feeding a backward GEMM along ``axis``: MXFP8 blocks in mxfp8 mode;
+        in bf16 mode the GPU's hi/lo pair carries them at fp32-like precision."""
+        return mx_qdq(a, axis) if self.mx else a
+
+    def bwd_act_rows(self, a):
+        return mx_qdq_rows_padded(a) if self.mx else a
 
 
 # ----------------------------------------------------------------------------- forward
@@ -162,9 +161,9 @@ def shared_forward(x, Ws_up, Ws_gate, Ws_down, mode: str):
     P = Precision("fp64" if mode == "fp64" else "bf16")
     U = x @ Ws_up
     V = x @ Ws_gate
-    h = P.act(silu(V) * U, 1)
+    h = P.fwd_act(silu(V) * U, 1)
     O = h @ Ws_down
-    return O, {"Us": P.store(U), "Vs": P.store(V)}
+    return O, {"Us": U, "Vs": V}
 
 
 def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
@@ -194,10 +193,10 @@ def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
         A = P.op(Xe, 1)
         U = A @ P.op(W_up[e], 0)
         V = A @ P.op(W_gate[e], 0)
-        h = P.act(silu(V) * U, 1)
+        h = P.fwd_act(silu(V) * U, 1)
         O_rows[r0:r1] = h @ P.op(W_down[e], 0)
-        U_s[r0:r1] = P.store(U)
-        V_s[r0:r1] = P.store(V)
+        U_s[r0:r1] = U
+        V_s[r0:r1] = V
     y = np.zeros((T, H))
     for j in range(k):                                  # combine in slot order
         y += gates[:, j:j + 1] * O_rows[pl.inv[:, j]]
@@ -225,14 +224,13 @@ class Grads:
 
 
 def shared_backward(x, Ws_up, Ws_gate, Ws_down, saved, dY, mode: str):
-    P = Precision("fp64" if mode == "fp64" else "bf16")
     Us, Vs = saved["Us"], saved["Vs"]
     D = dY @ Ws_down.T
     hv = silu(Vs) * Us
-    du = P.act(D * silu(Vs), 1)
-    dv = P.act(D * Us * dsilu(Vs), 1)
+    du = D * silu(Vs)
+    dv = D * Us * dsilu(Vs)
     dXs = du @ Ws_up.T + dv @ Ws_gate.T
-    dWs_down = P.act(hv, 0).T @ dY
+    dWs_down = hv.T @ dY
     dWs_up = x.T @ du
     dWs_gate = x.T @ dv
     return dXs, dWs_up, dWs_gate, dWs_down
@@ -284,12 +282,12 @@ def backward(x, idx, gates, W_up, W_gate, W_down, saved, dY, shared=None,
         dh = g * D
         du = dh * silu(Vs)
         dv = dh * Us * dsilu(Vs)
-        dXg[r0:r1] = (P.act(du, 1) @ P.op(W_up[e], 1).T
-                      + P.act(dv, 1) @ P.op(W_gate[e], 1).T)
-        dW_down[e] = P.act_rows(g * hv).T @ P.op_rows(dYe)
+        dXg[r0:r1] = (P.bwd_act(du, 1) @ P.op(W_up[e], 1).T
+                      + P.bwd_act(dv, 1) @ P.op(W_gate[e], 1).T)
+        dW_down[e] = P.bwd_act_rows(g * hv).T @ P.op_rows(dYe)
         XR = P.op_rows(Xe)
-        dW_up[e] = XR.T @ P.act_rows(du)
-        dW_gate[e] = XR.T @ P.act_rows(dv)
+        dW_up[e] = XR.T @ P.bwd_act_rows(du)
+        dW_gate[e] = XR.T @ P.bwd_act_rows(dv)
     dX = np.zeros((T, H))
     for j in range(k):                                   # reverse combine in slot order
         dX += dXg[pl.inv[:, j]]

@@ -3,12 +3,13 @@
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py). The dense oracle in ``moe`` holds every
 routed row of every expert; at the Kimi/DeepSeek sizes that is too much, so these
 functions compute one token's y or dX row, or one element of a weight gradient, straight
-from the definition (with the same bf16 rounding model as ``moe``, precision "bf16"):
+from the definition (with the same rounding model as ``moe``, precision "bf16": only h,
+the down GEMM's operand, is rounded to bf16):
 
 * y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(silu(x W_gate) * (x W_up)) W_down;
 * dX_t = sum_j (du W_up^T + dv W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j], with
-  D = dY_t W_down^T, du = bf16(g D silu(V)), dv = bf16(g D U silu'(V)) from the bf16 U, V;
-* dW_down[e][i][h] = sum over e's rows of bf16(g silu(V) U)[i] dY[t][h];
+  D = dY_t W_down^T, du = g D silu(V), dv = g D U silu'(V);
+* dW_down[e][i][h] = sum over e's rows of (g silu(V) U)[i] dY[t][h];
 * dW_up[e][h][i] = sum over e's rows of x[t][h] du[i] (dW_gate with dv).
 
 ``W`` arguments are callables returning one expert's float64 matrices on demand, so the
@@ -22,18 +23,17 @@ from .numerics import bf16_round, dsilu, silu
 
 
 def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
-    u = x_t @ Wu
-    v = x_t @ Wg
-    U, V = bf16_round(u), bf16_round(v)
-    h = bf16_round(silu(v) * u)
+    U = x_t @ Wu
+    V = x_t @ Wg
+    h = bf16_round(silu(V) * U)
     O = h @ Wd
     out = {"O": O}
     if dY_t is not None:
         D = Wd @ dY_t                      # = dY_t W_down^T
         hv = silu(V) * U
         out["dg"] = float(D @ hv)
-        du = bf16_round(g * D * silu(V))
-        dv = bf16_round(g * D * U * dsilu(V))
+        du = g * D * silu(V)
+        dv = g * D * U * dsilu(V)
         out["dXg"] = Wu @ du + Wg @ dv
     return out
 
@@ -62,10 +62,9 @@ def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
         v = x_t @ Ws_gate
         y += bf16_round(silu(v) * u) @ Ws_down
         if dY_t is not None:
-            U, V = bf16_round(u), bf16_round(v)
             D = Ws_down @ dY_t
-            du = bf16_round(D * silu(V))
-            dv = bf16_round(D * U * dsilu(V))
+            du = D * silu(v)
+            dv = D * u * dsilu(v)
             dX += Ws_up @ du + Ws_gate @ dv
     out = {"y": y}
     if dY_t is not None:
@@ -99,18 +98,18 @@ def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks):
             continue
         if name == "dW_down":
             i, h = a, b
-            U = bf16_round(X @ Wu[:, i])
-            V = bf16_round(X @ Wg[:, i])
-            hg = bf16_round(g * silu(V) * U)
+            U = X @ Wu[:, i]
+            V = X @ Wg[:, i]
+            hg = g * silu(V) * U
             out.append(float(hg @ dYe[:, h]))
         else:
             h, i = a, b
-            U = bf16_round(X @ Wu[:, i])
-            V = bf16_round(X @ Wg[:, i])
+            U = X @ Wu[:, i]
+            V = X @ Wg[:, i]
             D = dYe @ Wd[i, :]
             if name == "dW_up":
-                d = bf16_round(g * D * silu(V))
+                d = g * D * silu(V)
             else:
-                d = bf16_round(g * D * U * dsilu(V))
+                d = g * D * U * dsilu(V)
             out.append(float(X[:, h] @ d))
     return np.array(out)
