@@ -65,6 +65,9 @@ class ClockSampler:
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
 
     def start(self):
+        """Start sampling and wait for the first sample: nvidia-smi's start-up (NVML
+        initialisation) can stall CUDA calls of this process for seconds, so it must be
+        over before anything is timed."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
@@ -74,6 +77,24 @@ class ClockSampler:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 20:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.1)
+        time.sleep(0.5)
+
+    def mark(self):
+        """Only samples taken after this point count (the timed region)."""
+        self.f.flush()
+        try:
+            self.skip = sum(1 for _ in open(self.path))
+        except OSError:
+            self.skip = 0
 
     def stop(self):
         if self.proc is None:
@@ -86,7 +107,9 @@ class ClockSampler:
         self.f.close()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for n_line, line in enumerate(open(self.path)):
+            if n_line < getattr(self, "skip", 0):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -196,6 +219,8 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    clk = ClockSampler(local)
+    clk.start()
     for _ in range(max(args.warmup, 0)):
         step()
     barrier()
@@ -203,9 +228,7 @@ def run_gpu(args):
         raise RuntimeError("device status error during warm-up")
 
     stream = torch.cuda.current_stream()
-    clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
+    clk.mark()
     mok.mok_profile_enable(L.ctx, True)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)

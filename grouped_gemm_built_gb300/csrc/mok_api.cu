@@ -538,12 +538,10 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.out[5] = W(L.hg_lo);
     c.dgp = dgp;
     MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
-    // dXg = du W_up^T + dv W_gate^T
+    // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
     c = routed_call(d, sched, a, kBwdDX);
     c.a[0] = W(L.du);
-    c.a[1] = W(L.du_lo);
-    c.a[2] = W(L.dv);
-    c.a[3] = W(L.dv_lo);
+    c.a[1] = W(L.dv);
     c.b[0] = w->W_up;
     c.b[1] = w->W_gate;
     c.out[0] = dxg;
@@ -611,9 +609,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDX);
     cs.a[0] = W(L.dus);
-    cs.a[1] = W(L.dus_lo);
-    cs.a[2] = W(L.dvs);
-    cs.a[3] = W(L.dvs_lo);
+    cs.a[1] = W(L.dvs);
     cs.b[0] = w->Ws_up;
     cs.b[1] = w->Ws_gate;
     cs.out[0] = W(L.dxs);

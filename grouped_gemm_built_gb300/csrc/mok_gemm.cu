@@ -20,10 +20,11 @@
 // rows by the schedule), so a tile never mixes experts. Each output element is one fp32
 // sum in a fixed K order, so results are bitwise reproducible.
 //
-// Precision of the BF16 backward: the computed operands du, dv and g*h are kept as a pair
-// of bf16 values (hi = bf16(v), lo = bf16(v - hi)); the dX and dW GEMMs run both halves
-// of each K chunk back to back into the same fp32 accumulator, so these operands carry a
-// 16-bit significand while the tensor cores still take bf16.
+// Precision of the BF16 backward: the computed operands du, dv and g*h are also kept as a
+// pair of bf16 values (hi = bf16(v), lo = bf16(v - hi)); the dW GEMMs run both halves of
+// each K chunk back to back into the same fp32 accumulator, so there these operands carry
+// a 16-bit significand while the tensor cores still take bf16. (The dX GEMM sums over I
+// and takes the bf16 hi parts only.)
 //
 // Every mbarrier wait is bounded by a deadline; on expiry the kernel records
 // MOK_ERR_TIMEOUT in the status word, drains its outstanding copies and returns.
@@ -54,7 +55,8 @@ constexpr int OUT_STAGING = 4 * 2 * STAGE_OUT_BYTES;  // 4 epilogue warps x 2 bu
 
 template <bool MX>
 struct Cfg {
-  static constexpr int STAGES = MX ? 3 : 4;          // an MXFP8 stage holds twice the K
+  static constexpr int STAGES = MX ? 3 : 4;          // most stages a launch uses (an MXFP8
+                                                     // stage holds twice the K)
   static constexpr int BK = MX ? 128 : 64;           // K elements per stage (128 bytes/row)
   static constexpr int MMA_K = MX ? 32 : 16;         // K elements per instruction
   static constexpr int MN_CHUNK = MX ? 128 : 64;     // elements per 128-byte MN-major chunk
@@ -65,7 +67,13 @@ struct Cfg {
   static constexpr int NACC = MX ? 1 : 2;
   static constexpr int ACC_COLS = 256;
   static constexpr int SF_TMEM = 256;                // MX: scale columns start here
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING + 1024 + 256;
+  // data area: the larger of (STAGES stages + 2 staging boxes per warp) and
+  // (STAGES - 1 stages + 4 staging boxes per warp), then barriers
+  static constexpr int DATA_BYTES =
+      (STAGES * STAGE_BYTES + OUT_STAGING > (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING)
+          ? STAGES * STAGE_BYTES + OUT_STAGING
+          : (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING;
+  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 256;
 };
 
 // Tensor maps of one launch: operands a[], b[] (loads) and outputs o[] (stores).
@@ -86,7 +94,9 @@ struct Params {
   int m_tiles_dw;   // dW modes: tiles along M of one expert's dW
   int groups;
   int kiters;       // row-space modes: K iterations per tile
-  int split;        // 1: the dX / dW GEMMs run hi and lo halves of their computed operand
+  int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
+  int stages;       // shared-memory stages of the operand ring
+  int nbuf;         // epilogue staging boxes per warp (2 or 4)
   // schedule
   const int32_t* poff;
   const int32_t* counts;
@@ -215,12 +225,16 @@ __device__ __forceinline__ uint32_t quant32_e4m3(const float* v, uint4* q2) {
 // stores the box with TMA. Two buffers per warp: a buffer is refilled only after the TMA
 // store issued two boxes earlier has finished reading it. Every lane calls these.
 struct Stager {
-  uint8_t* buf;   // this warp's 2 x 4 KB, 1024-byte aligned
+  uint8_t* buf;   // this warp's nbuf x 4 KB, 1024-byte aligned
   uint32_t n;
   int lane;
+  int nbuf;       // 2 or 4
   __device__ __forceinline__ uint8_t* next() {
-    uint8_t* b = buf + (n & 1) * STAGE_OUT_BYTES;
-    if (n >= 2 && lane == 0) bulk_wait_read<1>();
+    uint8_t* b = buf + (n & (nbuf - 1)) * STAGE_OUT_BYTES;
+    if (n >= (uint32_t)nbuf && lane == 0) {
+      if (nbuf == 4) bulk_wait_read<3>();
+      else bulk_wait_read<1>();
+    }
     __syncwarp();
     return b;
   }
@@ -269,7 +283,7 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
                         uint64_t* empty, volatile int* abort_flag) {
   using C = Cfg<MX>;
   constexpr int BK = C::BK;
-  constexpr int STAGES = C::STAGES;
+  const int STAGES = p.stages;
   constexpr int CH = C::MN_LBO;        // bytes of one MN-major chunk
   const int ntiles = num_tiles_of(p);
   const int sp = p.split;
@@ -340,7 +354,7 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
           const int second = kb >= per_half ? 1 : 0;
           const int r = kb - second * per_half;
           const int kq = r >> sp;                  // K chunk inside the half
-          const int ai = MX ? second : 2 * second + (r & sp);
+          const int ai = sp ? 2 * second + (r & 1) : second;
           tma_load_2d(sa, &mp.a[ai], bar, kq * BK, ti.row0);
           tma_load_2d(sb, &mp.b[second], bar, kq * BK, ti.e * p.H + ti.n0);
           if (MX) {
@@ -387,7 +401,7 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
   // Drain: every issued copy has landed and every MMA commit has arrived before the
   // CTA's shared memory goes away.
   const uint32_t n_armed = it;
-  for (uint32_t s = 0; s < STAGES && s < n_armed; ++s) {
+  for (uint32_t s = 0; s < (uint32_t)STAGES && s < n_armed; ++s) {
     const uint32_t last = ((n_armed - 1 - s) / STAGES) * STAGES + s;  // last use of stage s
     const uint32_t round = last / STAGES;
     if (!mbar_wait(&empty[s], round & 1, globaltimer_ns() + kTimeoutNs)) {
@@ -403,7 +417,7 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
                           uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
                           volatile int* abort_flag) {
   using C = Cfg<MX>;
-  constexpr int STAGES = C::STAGES;
+  const int STAGES = p.stages;
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
@@ -481,7 +495,7 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
   const int r = quarter * 32 + lane;        // row inside the tile
   const int ntiles = num_tiles_of(p);
-  Stager st{staging + (warp - 2) * 2 * STAGE_OUT_BYTES, 0u, lane};
+  Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
   int local = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
     const TileInfo ti = tile_info<MX>(p, tile);
@@ -702,11 +716,11 @@ template <bool MX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p) {
   using C = Cfg<MX>;
-  constexpr int STAGES = C::STAGES;
+  constexpr int STAGES = C::STAGES;   // barrier slots; the launch uses p.stages of them
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + OUT_STAGING);
+  uint8_t* staging = smem + p.stages * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -825,7 +839,11 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.I = c.I;
   p.k = c.k;
   p.groups = c.dense ? 1 : c.groups;
-  p.split = (!MX && (c.mode == kBwdDX || c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
+  p.split = (!MX && (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
+  // Every mode keeps the full operand ring: the dW modes are bound by refilling their
+  // operands from L2, and trading a stage for deeper output staging made them slower.
+  p.stages = C::STAGES;
+  p.nbuf = 2;
   p.poff = c.poff;
   p.counts = c.counts;
   p.offsets = c.offsets;
@@ -902,7 +920,7 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.kcs_a = c.I / 128;
       p.kcs_b = c.I / 128;
       p.ncs_b = c.H / 128;
-      for (int i = 0; i < (MX ? 2 : 4) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BM, eb);
+      for (int i = 0; i < (p.split ? 4 : 2) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BM, eb);
       ok = ok && make_map(&mp.b[0], c.b[0], c.I, G * c.H, p.BN, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, p.BN, eb) &&
            make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);

@@ -134,8 +134,7 @@ enum GemmMode : int {
 //   kFwdDown     a0 = h [h_q]; b0 = W_down; out0 = O fp32
 //   kBwdDH       a0 = dYg [dY_q]; b0 = W_down; u, v = saved U, V; out0..5 = du, dv, g*h as
 //                bf16 hi/lo pairs [out_q0..4 + atoms]; dgp
-//   kBwdDX       a0..3 = du_hi, du_lo, dv_hi, dv_lo [a0, a1 = du_q, dv_q]; b0, b1 = W_up,
-//                W_gate; out0 = dXg fp32
+//   kBwdDX       a0, a1 = du_hi, dv_hi [du_q, dv_q]; b0, b1 = W_up, W_gate; out0 = dXg fp32
 //   kBwdDWDown   a0, a1 = g*h hi, lo [a0 = g*h_q]; b0 = dYg [dY_q]; out0 = dW_down fp32
 //   kBwdDWUpGate a0 = Xg [x_q]; b0, b1 = du_hi, dv_hi; b2, b3 = du_lo, dv_lo
 //                [b0, b1 = du_q, dv_q]; out0, out1 = dW_up, dW_gate fp32

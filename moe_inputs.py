@@ -59,6 +59,9 @@ CONFIGS = {
     "dsv3_imbalanced": MoEConfig("dsv3_imbalanced", T=16384, H=7168, I=2048, E=256, k=8,
                                  bias_experts=(0, 1, 2, 3), bias_value=3.0,
                                  precision="mxfp8"),
+    # Kimi-2.5 expert shape with 24 experts and the same ~171 rows per expert as T=8192:
+    # a few GB on the device, for detailed kernel profiles.
+    "kimi_e24_profile": MoEConfig("kimi_e24_profile", T=512, H=7168, I=2048, E=24, k=8),
 }
 
 

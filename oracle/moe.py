@@ -30,9 +30,10 @@ Readings taken where the pages are silent (each is also listed in the design not
 * gradients at the top-k boundary are taken with the selected set S held fixed.
 
 Precision model (``precision``): "fp64" applies no rounding at all. "bf16" rounds h, the
-operand of the down GEMM, to bf16; the GPU keeps U, V, expert outputs, routed dX rows and
-all results in fp32, and feeds du, dv and g*h to the backward GEMMs as bf16 hi/lo pairs
-(a 16-bit significand), so those stay unrounded here. "mxfp8" quantises every GEMM operand
+operand of the down GEMM, and du, dv as operands of the dX GEMM to bf16; the GPU keeps
+U, V, expert outputs, routed dX rows and all results in fp32, and feeds du, dv and g*h to
+the weight-gradient GEMMs as bf16 hi/lo pairs (a 16-bit significand), so there they stay
+unrounded here. "mxfp8" quantises every GEMM operand
 to MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, dv, g*h,
 dY). Everything else is float64. The shared expert is always BF16.
 """
@@ -146,12 +147,14 @@ class Precision:
             return a
         return mx_qdq(a, axis) if self.mx else bf16_round(a)
 
-    def bwd_act(self, a, axis):
-        """du, dv, g*h feeding a backward GEMM along ``axis``: MXFP8 blocks in mxfp8 mode;
-        in bf16 mode the GPU's hi/lo pair carries them at fp32-like precision."""
-        return mx_qdq(a, axis) if self.mx else a
+    def dx_act(self, a, axis):
+        """du, dv feeding the dX GEMM along ``axis`` (I): bf16, or MXFP8 blocks."""
+        return self.fwd_act(a, axis)
 
     def bwd_act_rows(self, a):
+        """du, dv, g*h feeding a weight-gradient GEMM (K = expert rows): MXFP8 blocks of 32
+        rows in mxfp8 mode; in bf16 mode the GPU's hi/lo pair carries them at fp32-like
+        precision."""
         return mx_qdq_rows_padded(a) if self.mx else a
 
 
@@ -224,12 +227,13 @@ class Grads:
 
 
 def shared_backward(x, Ws_up, Ws_gate, Ws_down, saved, dY, mode: str):
+    P = Precision("fp64" if mode == "fp64" else "bf16")
     Us, Vs = saved["Us"], saved["Vs"]
     D = dY @ Ws_down.T
     hv = silu(Vs) * Us
     du = D * silu(Vs)
     dv = D * Us * dsilu(Vs)
-    dXs = du @ Ws_up.T + dv @ Ws_gate.T
+    dXs = P.dx_act(du, 1) @ Ws_up.T + P.dx_act(dv, 1) @ Ws_gate.T
     dWs_down = hv.T @ dY
     dWs_up = x.T @ du
     dWs_gate = x.T @ dv
@@ -282,8 +286,8 @@ def backward(x, idx, gates, W_up, W_gate, W_down, saved, dY, shared=None,
         dh = g * D
         du = dh * silu(Vs)
         dv = dh * Us * dsilu(Vs)
-        dXg[r0:r1] = (P.bwd_act(du, 1) @ P.op(W_up[e], 1).T
-                      + P.bwd_act(dv, 1) @ P.op(W_gate[e], 1).T)
+        dXg[r0:r1] = (P.dx_act(du, 1) @ P.op(W_up[e], 1).T
+                      + P.dx_act(dv, 1) @ P.op(W_gate[e], 1).T)
         dW_down[e] = P.bwd_act_rows(g * hv).T @ P.op_rows(dYe)
         XR = P.op_rows(Xe)
         dW_up[e] = XR.T @ P.bwd_act_rows(du)

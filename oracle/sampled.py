@@ -3,12 +3,12 @@
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py). The dense oracle in ``moe`` holds every
 routed row of every expert; at the Kimi/DeepSeek sizes that is too much, so these
 functions compute one token's y or dX row, or one element of a weight gradient, straight
-from the definition (with the same rounding model as ``moe``, precision "bf16": only h,
-the down GEMM's operand, is rounded to bf16):
+from the definition (with the same rounding model as ``moe``, precision "bf16": h, the
+down GEMM's operand, and du, dv as operands of the dX GEMM are rounded to bf16):
 
 * y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(silu(x W_gate) * (x W_up)) W_down;
-* dX_t = sum_j (du W_up^T + dv W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j], with
-  D = dY_t W_down^T, du = g D silu(V), dv = g D U silu'(V);
+* dX_t = sum_j (bf16(du) W_up^T + bf16(dv) W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j],
+  with D = dY_t W_down^T, du = g D silu(V), dv = g D U silu'(V);
 * dW_down[e][i][h] = sum over e's rows of (g silu(V) U)[i] dY[t][h];
 * dW_up[e][h][i] = sum over e's rows of x[t][h] du[i] (dW_gate with dv).
 
@@ -34,7 +34,7 @@ def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
         out["dg"] = float(D @ hv)
         du = g * D * silu(V)
         dv = g * D * U * dsilu(V)
-        out["dXg"] = Wu @ du + Wg @ dv
+        out["dXg"] = Wu @ bf16_round(du) + Wg @ bf16_round(dv)
     return out
 
 
@@ -65,7 +65,7 @@ def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
             D = Ws_down @ dY_t
             du = D * silu(v)
             dv = D * u * dsilu(v)
-            dX += Ws_up @ du + Ws_gate @ dv
+            dX += Ws_up @ bf16_round(du) + Ws_gate @ bf16_round(dv)
     out = {"y": y}
     if dY_t is not None:
         if Wr is not None:
