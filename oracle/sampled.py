@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .numerics import bf16_round, dsilu, silu
+from .numerics import bf16_round, dsilu, mx_qdq, mx_qdq_rows_padded, silu
 
 
 def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
@@ -113,3 +113,59 @@ def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks):
                 d = g * D * U * dsilu(V)
             out.append(float(X[:, h] @ d))
     return np.array(out)
+
+
+# ----------------------------------------------------------------------------- whole dW lines
+def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i):
+    """For one expert (its table rows ``pairs``) and one intermediate index i: the row
+    dW_down[e][i, :] (length H) and the columns dW_up[e][:, i], dW_gate[e][:, i]
+    (length H), BF16 rounding model (du, dv, g*h unrounded on the weight-gradient path)."""
+    t = pairs[:, 0]
+    g = np.asarray(gates[t, pairs[:, 1]], np.float64)
+    X = np.asarray(x[t], np.float64)
+    dYe = np.asarray(dY[t], np.float64)
+    U = X @ Wu[:, i]
+    V = X @ Wg[:, i]
+    D = dYe @ Wd[i, :]
+    hg = g * silu(V) * U
+    du = g * D * silu(V)
+    dv = g * D * U * dsilu(V)
+    return {"dW_down": hg @ dYe, "dW_up": X.T @ du, "dW_gate": X.T @ dv}
+
+
+# ----------------------------------------------------------------------------- MXFP8 forward
+def mx_expert_weights(Wu, Wg, Wd):
+    """The MXFP8 values the forward GEMMs see for one expert: W_up, W_gate quantised in
+    blocks of 32 along H, W_down in blocks of 32 along I."""
+    return mx_qdq(Wu, 0), mx_qdq(Wg, 0), mx_qdq(Wd, 0)
+
+
+def token_forward_mx(t, x, idx, gates, weights_q, shared=None):
+    """y_t in MXFP8 mode: x_t in blocks of 32 along H, h in blocks of 32 along I; the
+    shared expert BF16 (h rounded to bf16). weights_q(e) -> mx_expert_weights(...)."""
+    x_t = np.asarray(x[t], np.float64)
+    xq = mx_qdq(x_t[None, :], 1)[0]
+    y = np.zeros(x_t.shape[0])
+    for j in range(idx.shape[1]):
+        Wu, Wg, Wd = weights_q(int(idx[t, j]))
+        U = xq @ Wu
+        V = xq @ Wg
+        hq = mx_qdq((silu(V) * U)[None, :], 1)[0]
+        y += float(gates[t, j]) * (hq @ Wd)
+    if shared is not None:
+        Ws_up, Ws_gate, Ws_down = shared
+        u = x_t @ Ws_up
+        v = x_t @ Ws_gate
+        y += bf16_round(silu(v) * u) @ Ws_down
+    return y
+
+
+def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i):
+    """Shared expert (gate 1, every token): dWs_down[i, :], dWs_up[:, i], dWs_gate[:, i]."""
+    x = np.asarray(x, np.float64)
+    dY = np.asarray(dY, np.float64)
+    U = x @ Ws_up[:, i]
+    V = x @ Ws_gate[:, i]
+    D = dY @ Ws_down[i, :]
+    return {"dWs_down": (silu(V) * U) @ dY, "dWs_up": x.T @ (D * silu(V)),
+            "dWs_gate": x.T @ (D * U * dsilu(V))}

@@ -278,3 +278,46 @@ def test_sampled_evaluators_match_the_dense_oracle(rng):
         got = sampled.dw_elements(e, pairs, x, dY, r.gates, Wu[e], Wg[e], Wd[e], picks)
         ref = [g.dW_up[e, 3, 5], g.dW_gate[e, 15, 0], g.dW_down[e, 7, 11], g.dW_down[e, 0, 0]]
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng):
+    """The full-size evaluators (whole dW lines; MXFP8 per-token forward) against the
+    dense per-expert oracle."""
+    from oracle import sampled
+    from oracle.numerics import bf16_round
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=20, H=64, I=32, E=4, k=2, shared=True)
+    x = bf16_round(x)
+    r = moe.route(x, Wr, 2)
+    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16")
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16")
+    pl = saved["plan"]
+    for e in range(4):
+        for i in (0, 17, 31):
+            L = sampled.dw_lines(sampled.expert_rows(pl, e), x, dY, r.gates, Wu[e], Wg[e], Wd[e], i)
+            assert np.allclose(L["dW_down"], g.dW_down[e, i, :], rtol=1e-12, atol=1e-12)
+            assert np.allclose(L["dW_up"], g.dW_up[e, :, i], rtol=1e-12, atol=1e-12)
+            assert np.allclose(L["dW_gate"], g.dW_gate[e, :, i], rtol=1e-12, atol=1e-12)
+    ym, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="mxfp8")
+    cache = {}
+
+    def wq(e):
+        if e not in cache:
+            cache[e] = sampled.mx_expert_weights(Wu[e], Wg[e], Wd[e])
+        return cache[e]
+
+    for t in range(20):
+        yt = sampled.token_forward_mx(t, x, r.idx, r.gates, wq, shared=sh)
+        assert np.allclose(yt, ym[t], rtol=1e-12, atol=1e-12)
+
+
+def test_shared_dw_lines_match_the_dense_oracle(rng):
+    from oracle import sampled
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=12, H=16, I=8, E=3, k=1, shared=True)
+    r = moe.route(x, Wr, 1)
+    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16")
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16")
+    for i in range(6):
+        L = sampled.shared_dw_lines(x, dY, *sh, i)
+        assert np.allclose(L["dWs_down"], g.dWs_down[i], rtol=1e-12, atol=1e-12)
+        assert np.allclose(L["dWs_up"], g.dWs_up[:, i], rtol=1e-12, atol=1e-12)
+        assert np.allclose(L["dWs_gate"], g.dWs_gate[:, i], rtol=1e-12, atol=1e-12)
