@@ -164,7 +164,8 @@ def kernel_work(cfg, name, counts=None):
                                    2.0 * (2 * H * I * E + rows * H + 3 * rows * I)),
         "gemm_fwd_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I) + 4.0 * rows * H),
         "gemm_bwd_dh_swiglu": (2.0 * H * I * rows,
-                               2.0 * (H * I * E + rows * H + 5 * rows * I) + 4.0 * rows),
+                               2.0 * (H * I * E + rows * H + 3 * rows * I)
+                               + 4.0 * (2 * rows * I + rows)),
         "gemm_bwd_dx": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + 2 * rows * I) + 4.0 * rows * H),
         "gemm_bwd_dw_down": (2.0 * H * I * rows, 2.0 * (rows * I + rows * H) + 4.0 * H * I * E),
         "gemm_bwd_dw_upgate": (4.0 * H * I * rows,
@@ -338,7 +339,7 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if cfg.precision == "bf16" else "mxfp8", "data": "synthetic",
+            "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
             "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} "
                                    f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} fwd+bwd",
                        "step": "plan + forward + backward", "T": cfg.T, "H": cfg.H, "I": cfg.I,

@@ -299,7 +299,7 @@ void mok_destroy(mok_ctx_t ctx) { delete ctx; }
 
 mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
-  if (p != MOK_BF16 && p != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+  if (p != MOK_BF16 && p != MOK_MXFP8 && p != MOK_BF16_WGRAD_PLAIN) return MOK_ERR_INVALID_ARG;
   ctx->precision = p;
   return MOK_OK;
 }
@@ -516,6 +516,9 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   float* dgp = reinterpret_cast<float*>(W(L.dgp));
   float* dl = reinterpret_cast<float*>(W(L.dl));
   const bool mx = ctx->precision == MOK_MXFP8;
+  const bool hilo = ctx->precision == MOK_BF16;  // dW operands as bf16 hi + lo pairs
+  // the shared expert is BF16 in the MXFP8 mode too, with that mode's dW operands
+  const bool hilo_s = ctx->precision != MOK_BF16_WGRAD_PLAIN;
   MxWeights M = mx_weights_layout(d);
   char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
 
@@ -531,11 +534,13 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.u = su;
     c.v = sv;
     c.out[0] = W(L.du);
-    c.out[1] = W(L.du_lo);
     c.out[2] = W(L.dv);
-    c.out[3] = W(L.dv_lo);
     c.out[4] = W(L.hg);
-    c.out[5] = W(L.hg_lo);
+    if (hilo) {
+      c.out[1] = W(L.du_lo);
+      c.out[3] = W(L.dv_lo);
+      c.out[5] = W(L.hg_lo);
+    }
     c.dgp = dgp;
     MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
     // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
@@ -601,11 +606,13 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     cs.u = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.us));
     cs.v = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.vs));
     cs.out[0] = W(L.dus);
-    cs.out[1] = W(L.dus_lo);
     cs.out[2] = W(L.dvs);
-    cs.out[3] = W(L.dvs_lo);
     cs.out[4] = W(L.hsg);
-    cs.out[5] = W(L.hsg_lo);
+    if (hilo_s) {
+      cs.out[1] = W(L.dus_lo);
+      cs.out[3] = W(L.dvs_lo);
+      cs.out[5] = W(L.hsg_lo);
+    }
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDX);
     cs.a[0] = W(L.dus);
@@ -635,8 +642,11 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.a[0] = W(L.xg);
     c.b[0] = W(L.du);
     c.b[1] = W(L.dv);
-    c.b[2] = W(L.du_lo);
-    c.b[3] = W(L.dv_lo);
+    if (hilo) {
+      c.split = true;
+      c.b[2] = W(L.du_lo);
+      c.b[3] = W(L.dv_lo);
+    }
   }
   c.out[0] = g->dW_up;
   c.out[1] = g->dW_gate;
@@ -650,8 +660,11 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.sfb0 = W(L.sf_dy_r);
   } else {
     c.a[0] = W(L.hg);
-    c.a[1] = W(L.hg_lo);
     c.b[0] = W(L.dyg);
+    if (hilo) {
+      c.split = true;
+      c.a[1] = W(L.hg_lo);
+    }
   }
   c.out[0] = g->dW_down;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
@@ -660,15 +673,21 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     cs.a[0] = x;
     cs.b[0] = W(L.dus);
     cs.b[1] = W(L.dvs);
-    cs.b[2] = W(L.dus_lo);
-    cs.b[3] = W(L.dvs_lo);
+    if (hilo_s) {
+      cs.split = true;
+      cs.b[2] = W(L.dus_lo);
+      cs.b[3] = W(L.dvs_lo);
+    }
     cs.out[0] = g->dWs_up;
     cs.out[1] = g->dWs_gate;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDWDown);
     cs.a[0] = W(L.hsg);
-    cs.a[1] = W(L.hsg_lo);
     cs.b[0] = dY;
+    if (hilo_s) {
+      cs.split = true;
+      cs.a[1] = W(L.hsg_lo);
+    }
     cs.out[0] = g->dWs_down;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
   }

@@ -95,6 +95,7 @@ struct Params {
   int groups;
   int kiters;       // row-space modes: K iterations per tile
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
+  int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
   int stages;       // shared-memory stages of the operand ring
   int nbuf;         // epilogue staging boxes per warp (2 or 4)
   // schedule
@@ -154,8 +155,9 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
       ti.krow0 = 0;
       ti.kiters = (p.M_rows + BK - 1) / BK;
     } else {
+      // the expert's rows rounded up to the K step; the segment's padding rows are zero
       ti.krow0 = p.poff[ti.e];
-      ti.kiters = (p.poff[ti.e + 1] - ti.krow0) / BK;
+      ti.kiters = min((max(p.counts[ti.e], 0) + BK - 1) / BK, (p.poff[ti.e + 1] - ti.krow0) / BK);
     }
     ti.kiters <<= p.split;
   } else {
@@ -594,13 +596,13 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
             float hi[32], lo[32];
             split_bf16(du, hi, lo);
             st.bf16(&mp.o[0], hi, col, wrow);
-            st.bf16(&mp.o[1], lo, col, wrow);
+            if (p.lo_out) st.bf16(&mp.o[1], lo, col, wrow);
             split_bf16(dv, hi, lo);
             st.bf16(&mp.o[2], hi, col, wrow);
-            st.bf16(&mp.o[3], lo, col, wrow);
+            if (p.lo_out) st.bf16(&mp.o[3], lo, col, wrow);
             split_bf16(hg, hi, lo);
             st.bf16(&mp.o[4], hi, col, wrow);
-            st.bf16(&mp.o[5], lo, col, wrow);
+            if (p.lo_out) st.bf16(&mp.o[5], lo, col, wrow);
           } else {
             // du, dv feed the dX GEMM (K = I): per-thread blocks of 32 along I
             const size_t atom_i = ((size_t)(row / BM) * (p.I / 128) + col / 128) * 512 +
@@ -839,7 +841,8 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.I = c.I;
   p.k = c.k;
   p.groups = c.dense ? 1 : c.groups;
-  p.split = (!MX && (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
+  p.split = (!MX && c.split && (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
+  p.lo_out = (!MX && c.mode == kBwdDH && c.out[1] && c.out[3] && c.out[5]) ? 1 : 0;
   // Every mode keeps the full operand ring: the dW modes are bound by refilling their
   // operands from L2, and trading a stage for deeper output staging made them slower.
   p.stages = C::STAGES;
@@ -910,7 +913,8 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.ncs_b = c.I / 128;
       ok = make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
            make_map(&mp.b[0], c.b[0], c.H, G * c.I, p.BN, eb);
-      for (int i = 0; i < 6 && ok && !MX; ++i) ok = make_out_map(&mp.o[i], c.out[i], c.I, rows, 2);
+      for (int i = 0; i < 6 && ok && !MX; ++i)
+        if (i % 2 == 0 || p.lo_out) ok = make_out_map(&mp.o[i], c.out[i], c.I, rows, 2);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDX:
@@ -930,7 +934,7 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
       p.m_tiles_dw = c.I / BM;
-      for (int i = 0; i < (MX ? 1 : 2) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BK, eb);
+      for (int i = 0; i < (p.split ? 2 : 1) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BK, eb);
       ok = ok && make_map(&mp.b[0], c.b[0], c.H, rows, BK, eb) &&
            make_out_map(&mp.o[0], c.out[0], c.H, G * c.I, 4);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
@@ -940,7 +944,7 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.n_tiles = c.I / 128;
       p.m_tiles_dw = c.H / BM;
       ok = make_map(&mp.a[0], c.a[0], c.H, rows, BK, eb);
-      for (int i = 0; i < (MX ? 2 : 4) && ok; ++i) ok = make_map(&mp.b[i], c.b[i], c.I, rows, BK, eb);
+      for (int i = 0; i < (p.split ? 4 : 2) && ok; ++i) ok = make_map(&mp.b[i], c.b[i], c.I, rows, BK, eb);
       ok = ok && make_out_map(&mp.o[0], c.out[0], c.I, G * c.H, 4) &&
            make_out_map(&mp.o[1], c.out[1], c.I, G * c.H, 4);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;

@@ -147,7 +147,8 @@ struct GemmCall {
   int groups;           // experts (dense: 1)
   const void* a[4];     // row-space operands
   const void* b[4];     // weights / second row-space operand
-  void* out[6];         // outputs
+  void* out[6];         // outputs (kBwdDH: du, du lo, dv, dv lo, g*h, g*h lo; lo optional)
+  bool split;           // dW modes (bf16): operands a[1] / b[2..3] hold the lo halves
   const float* u;       // kBwdDH: saved U, V (fp32)
   const float* v;
   float* dgp;           // kBwdDH: per-tile partial router-weight gradients

@@ -54,7 +54,11 @@ class MoELayer:
 
     def set_precision(self, precision: str):
         self.precision = precision
-        mok.mok_set_precision(self.ctx, mok.MOK_MXFP8 if precision == "mxfp8" else mok.MOK_BF16)
+        codes = {"bf16": mok.MOK_BF16, "mxfp8": mok.MOK_MXFP8,
+                 "bf16_plain": mok.MOK_BF16_WGRAD_PLAIN}
+        if precision not in codes:
+            raise ValueError(f"precision must be one of {sorted(codes)}, got {precision!r}")
+        mok.mok_set_precision(self.ctx, codes[precision])
 
     @staticmethod
     def _stream():

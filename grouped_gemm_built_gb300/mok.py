@@ -24,6 +24,7 @@ MOK_ERR_TIMEOUT = -5
 MOK_ERR_DEVICE = -6
 MOK_BF16 = 0
 MOK_MXFP8 = 1
+MOK_BF16_WGRAD_PLAIN = 2
 
 
 class MokDims(ctypes.Structure):

@@ -54,7 +54,16 @@ typedef enum {
   MOK_ERR_DEVICE = -6       /* the device flagged bad data (e.g. expert id >= E)    */
 } mok_status;
 
-typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
+/* MOK_BF16: bf16 tensor-core operands with fp32 accumulation and fp32 outputs. Inputs,
+ *   weights, h and the dX GEMM's du, dv are bf16; the weight-gradient GEMMs take du, dv
+ *   and g*h as bf16 hi + lo pairs (two MMAs per K step), close to fp32 operands.
+ * MOK_MXFP8: E4M3 elements with one UE8M0 scale per 32 along each GEMM's contraction axis;
+ *   the shared expert stays BF16 (as in MOK_BF16).
+ * MOK_BF16_WGRAD_PLAIN: as MOK_BF16 with single bf16 du, dv, g*h in the weight-gradient
+ *   GEMMs: half their MMAs, at the cost of one bf16 rounding of each operand. The pages
+ *   name BF16 and MXFP8 only; how BF16 feeds the weight gradients is this library's
+ *   choice. */
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1, MOK_BF16_WGRAD_PLAIN = 2 } mok_precision;
 
 typedef struct mok_ctx_s* mok_ctx_t;
 
@@ -151,10 +160,9 @@ const char* mok_status_string(mok_status s);
 
 /* ---- the layer ----------------------------------------------------------------- */
 
-/* Select the arithmetic of later mok_moe_fwd / mok_moe_bwd calls: MOK_BF16 (bf16
- * operands) or MOK_MXFP8 (E4M3 elements with one UE8M0 scale per 32 along each GEMM's
- * contraction axis; the shared expert stays BF16) ([S] "Determinismus und
- * MXFP8-Unterstuetzung"; [C] "Outras caracteristicas"). Host-only state change. */
+/* Select the arithmetic of later mok_moe_fwd / mok_moe_bwd calls (mok_precision above;
+ * BF16 and MXFP8 from [S] "Determinismus und MXFP8-Unterstuetzung"; [C] "Outras
+ * caracteristicas"). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
 
 /* Routing and schedule on the device ([S] "Das Scheduling"; [C] "Escolha da direcao").

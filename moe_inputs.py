@@ -38,7 +38,7 @@ class MoEConfig:
     x_std: float = 1.0
     w_std: float = 0.02
     wr_std: float = 0.02
-    precision: str = "bf16"      # "bf16" or "mxfp8"
+    precision: str = "bf16"      # "bf16", "mxfp8" or "bf16_plain" (single bf16 dW operands)
     backward: bool = True
     macrobatches: int = 1
     ring_bytes: int = 0          # 0 = ring sized to hold every routed row
@@ -53,6 +53,8 @@ CONFIGS = {
     "mid": MoEConfig("mid", T=4096, H=2048, I=1024, E=64, k=6),
     "kimi_2368": MoEConfig("kimi_2368", T=2368, H=7168, I=2048, E=384, k=8, shared_I=2048),
     "kimi_8192": MoEConfig("kimi_8192", T=8192, H=7168, I=2048, E=384, k=8, shared_I=2048),
+    "kimi_8192_plain": MoEConfig("kimi_8192_plain", T=8192, H=7168, I=2048, E=384, k=8,
+                                 shared_I=2048, precision="bf16_plain"),
     "ep64_slice": MoEConfig("ep64_slice", T=2048, H=7168, I=2048, E=6, k=8, router=False,
                             zipf_s=1.2, precision="mxfp8", backward=False, macrobatches=4,
                             ring_bytes=256 << 20),

@@ -29,13 +29,16 @@ Readings taken where the pages are silent (each is also listed in the design not
 * schedule order inside an expert: ascending token, then ascending slot;
 * gradients at the top-k boundary are taken with the selected set S held fixed.
 
-Precision model (``precision``): "fp64" applies no rounding at all. "bf16" rounds h, the
-operand of the down GEMM, and du, dv as operands of the dX GEMM to bf16; the GPU keeps
-U, V, expert outputs, routed dX rows and all results in fp32, and feeds du, dv and g*h to
-the weight-gradient GEMMs as bf16 hi/lo pairs (a 16-bit significand), so there they stay
-unrounded here. "mxfp8" quantises every GEMM operand
-to MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, dv, g*h,
-dY). Everything else is float64. The shared expert is always BF16.
+Precision model (``precision``): "fp64" applies no rounding at all. "bf16" (the articles'
+BF16 mode: bf16 tensor-core operands, fp32 accumulation) rounds h, the down GEMM's
+operand, and du, dv as operands of the dX GEMM to bf16; the GPU feeds du, dv and g*h to
+the weight-gradient GEMMs as bf16 hi + lo pairs (a 16-bit significand), so there they
+stay unrounded here; U, V, expert outputs, routed dX rows and all results stay unrounded
+too (the GPU keeps them in fp32). "bf16_plain" is "bf16" with du, dv and g*h rounded to
+bf16 for the weight-gradient GEMMs as well. "mxfp8" quantises every GEMM operand to
+MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, dv, g*h,
+dY). Everything else is float64. The shared expert is always BF16: single bf16
+weight-gradient operands in "bf16_plain", hi/lo ones in "bf16" and "mxfp8".
 """
 from __future__ import annotations
 
@@ -124,7 +127,7 @@ class Precision:
     """Where the GPU path rounds. See the module docstring."""
 
     def __init__(self, mode: str):
-        if mode not in ("fp64", "bf16", "mxfp8"):
+        if mode not in ("fp64", "bf16", "bf16_plain", "mxfp8"):
             raise ValueError(mode)
         self.mode = mode
 
@@ -153,9 +156,14 @@ class Precision:
 
     def bwd_act_rows(self, a):
         """du, dv, g*h feeding a weight-gradient GEMM (K = expert rows): MXFP8 blocks of 32
-        rows in mxfp8 mode; in bf16 mode the GPU's hi/lo pair carries them at fp32-like
-        precision."""
-        return mx_qdq_rows_padded(a) if self.mx else a
+        rows in mxfp8 mode, bf16 in bf16_plain mode; bf16 mode carries them as a bf16
+        hi + lo pair, which this model takes as exact (the pair's error, 2^-16 relative,
+        is far below the comparison's tolerance)."""
+        if self.mx:
+            return mx_qdq_rows_padded(a)
+        if self.mode == "bf16_plain":
+            return bf16_round(a)
+        return a
 
 
 # ----------------------------------------------------------------------------- forward
@@ -227,16 +235,18 @@ class Grads:
 
 
 def shared_backward(x, Ws_up, Ws_gate, Ws_down, saved, dY, mode: str):
-    P = Precision("fp64" if mode == "fp64" else "bf16")
+    """Shared expert backward: BF16 (single bf16 weight-gradient operands in bf16_plain,
+    hi/lo ones in the bf16 and mxfp8 modes)."""
+    P = Precision(mode if mode in ("fp64", "bf16_plain") else "bf16")
     Us, Vs = saved["Us"], saved["Vs"]
     D = dY @ Ws_down.T
     hv = silu(Vs) * Us
     du = D * silu(Vs)
     dv = D * Us * dsilu(Vs)
     dXs = P.dx_act(du, 1) @ Ws_up.T + P.dx_act(dv, 1) @ Ws_gate.T
-    dWs_down = hv.T @ dY
-    dWs_up = x.T @ du
-    dWs_gate = x.T @ dv
+    dWs_down = P.bwd_act_rows(hv).T @ dY
+    dWs_up = x.T @ P.bwd_act_rows(du)
+    dWs_gate = x.T @ P.bwd_act_rows(dv)
     return dXs, dWs_up, dWs_gate, dWs_down
 
 

@@ -2,9 +2,10 @@
 
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py). The dense oracle in ``moe`` holds every
 routed row of every expert; at the Kimi/DeepSeek sizes that is too much, so these
-functions compute one token's y or dX row, or one element of a weight gradient, straight
-from the definition (with the same rounding model as ``moe``, precision "bf16": h, the
-down GEMM's operand, and du, dv as operands of the dX GEMM are rounded to bf16):
+functions compute one token's y or dX row, or one element or line of a weight gradient,
+straight from the definition (with the same rounding model as ``moe``, precision "bf16":
+h, the down GEMM's operand, and du, dv as operands of the dX GEMM are rounded to bf16;
+the weight-gradient functions take ``plain`` to choose "bf16_plain" over "bf16"):
 
 * y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(silu(x W_gate) * (x W_up)) W_down;
 * dX_t = sum_j (bf16(du) W_up^T + bf16(dv) W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j],
@@ -83,10 +84,11 @@ def expert_rows(plan, e):
     return plan.table[plan.offsets[e]:plan.offsets[e + 1]]
 
 
-def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks):
+def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks, plain=False):
     """Elements of expert e's weight gradients. pairs: [n, 2] (t, j) rows of e;
     picks: list of (name, a, b) with name in dW_up (a=h, b=i), dW_gate (a=h, b=i),
     dW_down (a=i, b=h). Wu, Wg [H][I], Wd [I][H] float64."""
+    rnd = bf16_round if plain else (lambda v: v)
     t = pairs[:, 0]
     g = np.asarray(gates[t, pairs[:, 1]], np.float64)
     X = np.asarray(x[t], np.float64)
@@ -100,7 +102,7 @@ def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks):
             i, h = a, b
             U = X @ Wu[:, i]
             V = X @ Wg[:, i]
-            hg = g * silu(V) * U
+            hg = rnd(g * silu(V) * U)
             out.append(float(hg @ dYe[:, h]))
         else:
             h, i = a, b
@@ -108,18 +110,19 @@ def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks):
             V = X @ Wg[:, i]
             D = dYe @ Wd[i, :]
             if name == "dW_up":
-                d = g * D * silu(V)
+                d = rnd(g * D * silu(V))
             else:
-                d = g * D * U * dsilu(V)
+                d = rnd(g * D * U * dsilu(V))
             out.append(float(X[:, h] @ d))
     return np.array(out)
 
 
 # ----------------------------------------------------------------------------- whole dW lines
-def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i):
+def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i, plain=False):
     """For one expert (its table rows ``pairs``) and one intermediate index i: the row
     dW_down[e][i, :] (length H) and the columns dW_up[e][:, i], dW_gate[e][:, i]
-    (length H), BF16 rounding model (du, dv, g*h unrounded on the weight-gradient path)."""
+    (length H); du, dv, g*h unrounded (rounded to bf16 with ``plain``)."""
+    rnd = bf16_round if plain else (lambda v: v)
     t = pairs[:, 0]
     g = np.asarray(gates[t, pairs[:, 1]], np.float64)
     X = np.asarray(x[t], np.float64)
@@ -127,9 +130,9 @@ def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i):
     U = X @ Wu[:, i]
     V = X @ Wg[:, i]
     D = dYe @ Wd[i, :]
-    hg = g * silu(V) * U
-    du = g * D * silu(V)
-    dv = g * D * U * dsilu(V)
+    hg = rnd(g * silu(V) * U)
+    du = rnd(g * D * silu(V))
+    dv = rnd(g * D * U * dsilu(V))
     return {"dW_down": hg @ dYe, "dW_up": X.T @ du, "dW_gate": X.T @ dv}
 
 
@@ -160,12 +163,13 @@ def token_forward_mx(t, x, idx, gates, weights_q, shared=None):
     return y
 
 
-def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i):
+def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i, plain=False):
     """Shared expert (gate 1, every token): dWs_down[i, :], dWs_up[:, i], dWs_gate[:, i]."""
+    rnd = bf16_round if plain else (lambda v: v)
     x = np.asarray(x, np.float64)
     dY = np.asarray(dY, np.float64)
     U = x @ Ws_up[:, i]
     V = x @ Ws_gate[:, i]
     D = dY @ Ws_down[i, :]
-    return {"dWs_down": (silu(V) * U) @ dY, "dWs_up": x.T @ (D * silu(V)),
-            "dWs_gate": x.T @ (D * U * dsilu(V))}
+    return {"dWs_down": rnd(silu(V) * U) @ dY, "dWs_up": x.T @ rnd(D * silu(V)),
+            "dWs_gate": x.T @ rnd(D * U * dsilu(V))}

@@ -20,6 +20,12 @@ CASES = {
     "external_routing": mi.MoEConfig("external_routing", T=100, H=256, I=128, E=6, k=8,
                                      router=False, zipf_s=1.2, macrobatches=0),
     "mid": mi.CONFIGS["mid"],
+    # weight-gradient GEMMs on single bf16 operands (compared with the flip allowance)
+    "ragged_shared_plain": mi.MoEConfig("ragged_shared_plain", T=300, H=256, I=256, E=12, k=3,
+                                        shared_I=128, precision="bf16_plain"),
+    "mid_plain": mi.scaled(mi.CONFIGS["mid"], name="mid_plain", precision="bf16_plain"),
+    "sparse_plain": mi.MoEConfig("sparse_plain", T=64, H=128, I=128, E=64, k=1,
+                                 precision="bf16_plain"),
 }
 
 
@@ -56,6 +62,15 @@ def test_layer_matches_oracle(name):
         fields += ["dWs_up", "dWs_gate", "dWs_down"]
     errs = {f: gu.rel_err(res[f], ref[f]) for f in fields}
     print(name, errs)
+    if cfg.precision == "bf16_plain":
+        # du, dv, g*h are rounded to bf16 before the weight-gradient GEMMs: operands whose
+        # exact value sits within the fp32 error bound of a rounding midpoint may round
+        # either way, and with few rows per expert one such flip is visible in dW
+        slack, frac = gu.bf16_flip_slack(cfg, inp, idx, gates)
+        for f in list(errs):
+            if f in slack:
+                errs[f] = gu.rel_err_slack(res[f], ref[f], slack[f])
+        print(name, f"with flip slack ({frac:.4f} of dW operands near a midpoint):", errs)
     for f, e in errs.items():
         assert e <= tol, (f, e)
 

@@ -145,7 +145,7 @@ def test_shared_expert_adds_dense_ffn(rng):
         assert np.allclose(y1[t] - y0[t], (silu(v) * u) @ sh[2], rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("mode,tol", [("bf16", 1e-2), ("mxfp8", 1.5e-1)])
+@pytest.mark.parametrize("mode,tol", [("bf16", 1e-2), ("bf16_plain", 1e-2), ("mxfp8", 1.5e-1)])
 def test_rounded_modes_stay_near_fp64(mode, tol):
     """The rounding model only perturbs: rms(rounded - fp64) / rms(fp64) stays near the
     formats' unit roundoff (2^-9 for bf16, about 2^-4 per MXFP8 element)."""
@@ -280,7 +280,8 @@ def test_sampled_evaluators_match_the_dense_oracle(rng):
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
-def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng):
+@pytest.mark.parametrize("mode", ["bf16", "bf16_plain"])
+def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng, mode):
     """The full-size evaluators (whole dW lines; MXFP8 per-token forward) against the
     dense per-expert oracle."""
     from oracle import sampled
@@ -288,12 +289,13 @@ def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng):
     x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=20, H=64, I=32, E=4, k=2, shared=True)
     x = bf16_round(x)
     r = moe.route(x, Wr, 2)
-    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16")
-    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16")
+    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision=mode)
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision=mode)
     pl = saved["plan"]
     for e in range(4):
         for i in (0, 17, 31):
-            L = sampled.dw_lines(sampled.expert_rows(pl, e), x, dY, r.gates, Wu[e], Wg[e], Wd[e], i)
+            L = sampled.dw_lines(sampled.expert_rows(pl, e), x, dY, r.gates, Wu[e], Wg[e], Wd[e], i,
+                                 plain=mode != "bf16")
             assert np.allclose(L["dW_down"], g.dW_down[e, i, :], rtol=1e-12, atol=1e-12)
             assert np.allclose(L["dW_up"], g.dW_up[e, :, i], rtol=1e-12, atol=1e-12)
             assert np.allclose(L["dW_gate"], g.dW_gate[e, :, i], rtol=1e-12, atol=1e-12)
@@ -310,14 +312,41 @@ def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng):
         assert np.allclose(yt, ym[t], rtol=1e-12, atol=1e-12)
 
 
-def test_shared_dw_lines_match_the_dense_oracle(rng):
+@pytest.mark.parametrize("mode", ["bf16", "bf16_plain", "mxfp8"])
+def test_shared_dw_lines_match_the_dense_oracle(rng, mode):
     from oracle import sampled
-    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=12, H=16, I=8, E=3, k=1, shared=True)
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=12, H=32, I=32, E=3, k=1, shared=True)
     r = moe.route(x, Wr, 1)
-    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16")
-    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16")
+    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision=mode)
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision=mode)
     for i in range(6):
-        L = sampled.shared_dw_lines(x, dY, *sh, i)
+        L = sampled.shared_dw_lines(x, dY, *sh, i, plain=mode == "bf16_plain")
         assert np.allclose(L["dWs_down"], g.dWs_down[i], rtol=1e-12, atol=1e-12)
         assert np.allclose(L["dWs_up"], g.dWs_up[:, i], rtol=1e-12, atol=1e-12)
         assert np.allclose(L["dWs_gate"], g.dWs_gate[:, i], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "bf16_plain"])
+def test_weight_gradient_operand_rounding_point(rng, mode):
+    """One token routed to one expert, x made of powers of two: dW_up[e][h][i] =
+    x[h] * du[i] exactly, so dW_up / x is du itself. In the bf16_plain mode every such du
+    is a bf16 value; with hi/lo operands (bf16) it is the unrounded du (a bf16 value only
+    by chance)."""
+    from oracle.numerics import bf16_round
+    H, I = 32, 64
+    x = np.ldexp(1.0, rng.integers(-3, 3, (1, H))) * rng.choice([-1.0, 1.0], (1, H))
+    Wu = bf16_round(rng.normal(0, 0.2, (1, H, I)))
+    Wg = bf16_round(rng.normal(0, 0.2, (1, H, I)))
+    Wd = bf16_round(rng.normal(0, 0.2, (1, I, H)))
+    dY = bf16_round(rng.normal(0, 1, (1, H)))
+    idx = np.zeros((1, 1), np.int64)
+    gates = np.ones((1, 1))
+    _, saved = moe.forward(x, idx, gates, Wu, Wg, Wd, precision=mode)
+    g = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY, precision=mode)
+    du = g.dW_up[0] / x[0][:, None]
+    assert np.allclose(du, du[0][None, :], rtol=0, atol=0)     # one du row, scaled by x[h]
+    n_bf16 = int((bf16_round(du[0]) == du[0]).sum())
+    if mode == "bf16_plain":
+        assert n_bf16 == I
+    else:
+        assert n_bf16 < I // 4
