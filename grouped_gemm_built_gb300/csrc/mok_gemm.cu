@@ -24,7 +24,9 @@
 // pair of bf16 values (hi = bf16(v), lo = bf16(v - hi)); the dW GEMMs run both halves of
 // each K chunk back to back into the same fp32 accumulator, so there these operands carry
 // a 16-bit significand while the tensor cores still take bf16. (The dX GEMM sums over I
-// and takes the bf16 hi parts only.)
+// and takes the bf16 hi parts only.) One pipeline stage then holds a K chunk of the other
+// operand once and both halves of the split one (SPLIT_STAGE_BYTES), so the shared
+// operand crosses shared memory once per chunk.
 //
 // Every mbarrier wait is bounded by a deadline; on expiry the kernel records
 // MOK_ERR_TIMEOUT in the status word, drains its outstanding copies and returns.
@@ -52,6 +54,9 @@ constexpr int NUM_THREADS = 192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int STAGE_OUT_BYTES = 4096;               // one 32-row epilogue staging box
 constexpr int OUT_STAGING = 4 * 2 * STAGE_OUT_BYTES;  // 4 epilogue warps x 2 buffers
+// split (hi/lo) dW stage: [A 16 KB][B 32 KB][second half: B lo 32 KB, or A lo 16 KB]
+constexpr int SPLIT_STAGE_BYTES = A_BYTES + 2 * B_BYTES;
+constexpr int SPLIT_EXTRA_OFF = A_BYTES + B_BYTES;
 
 template <bool MX>
 struct Cfg {
@@ -95,6 +100,7 @@ struct Params {
   int groups;
   int kiters;       // row-space modes: K iterations per tile
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
+  int stage_bytes;  // bytes of one pipeline stage (Cfg::STAGE_BYTES or SPLIT_STAGE_BYTES)
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
   int stages;       // shared-memory stages of the operand ring
   int nbuf;         // epilogue staging boxes per warp (2 or 4)
@@ -159,7 +165,6 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
       ti.krow0 = p.poff[ti.e];
       ti.kiters = min((max(p.counts[ti.e], 0) + BK - 1) / BK, (p.poff[ti.e + 1] - ti.krow0) / BK);
     }
-    ti.kiters <<= p.split;
   } else {
     const int mt = tile / p.n_tiles;
     ti.e = p.dense ? 0 : min(max(p.tile_expert[mt], 0), p.groups - 1);
@@ -304,14 +309,14 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
         ok = false;
         break;
       }
-      uint8_t* sa = smem + stage * C::STAGE_BYTES;
+      uint8_t* sa = smem + stage * p.stage_bytes;
       uint8_t* sb = sa + A_BYTES;
       uint8_t* sf = sa + C::SF_OFF;
       uint64_t* bar = &full[stage];
-      mbar_arrive_expect_tx(bar, A_BYTES + b_bytes);
+      uint32_t extra = 0;   // split dW stages also carry the lo half of the split operand
+      if (sp) extra = p.mode == kBwdDWUpGate ? 2 * 128 * 128 : BM * 128;
+      mbar_arrive_expect_tx(bar, A_BYTES + b_bytes + extra);
       const int k0 = kb * BK;
-      // with split operands, iteration kb covers K chunk kb >> 1, half kb & 1
-      const int chunk = kb >> sp, part = kb & sp;
       switch (p.mode) {
         case kFwdUpGate: {   // A: Xg rows (K-major); B: W_up|W_gate cols n0..n0+127 (MN-major)
           tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
@@ -352,12 +357,10 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
           break;
         }
         case kBwdDX: {       // K = [I of du | I of dv]; B: W_up / W_gate rows h (K-major over I)
-          const int per_half = (p.I / BK) << sp;
+          const int per_half = p.I / BK;
           const int second = kb >= per_half ? 1 : 0;
-          const int r = kb - second * per_half;
-          const int kq = r >> sp;                  // K chunk inside the half
-          const int ai = sp ? 2 * second + (r & 1) : second;
-          tma_load_2d(sa, &mp.a[ai], bar, kq * BK, ti.row0);
+          const int kq = kb - second * per_half;   // K chunk inside the half
+          tma_load_2d(sa, &mp.a[second], bar, kq * BK, ti.row0);
           tma_load_2d(sb, &mp.b[second], bar, kq * BK, ti.e * p.H + ti.n0);
           if (MX) {
             bulk_load(sf, (second ? p.sfa1 : p.sfa) + ((size_t)(ti.row0 / BM) * p.kcs_a + kq) * 512,
@@ -367,10 +370,13 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
           }
           break;
         }
-        case kBwdDWDown: {   // A: (g h)^T (MN-major, M = I), hi/lo; B: dYg (MN-major, N = H)
-          const int kr = ti.krow0 + chunk * BK;
-          for (int c = 0; c < BM / C::MN_CHUNK; ++c)
-            tma_load_2d(sa + c * CH, &mp.a[part], bar, ti.row0 + c * C::MN_CHUNK, kr);
+        case kBwdDWDown: {   // A: (g h)^T (MN-major, M = I), hi (+ lo); B: dYg (MN-major, N = H)
+          const int kr = ti.krow0 + kb * BK;
+          for (int c = 0; c < BM / C::MN_CHUNK; ++c) {
+            tma_load_2d(sa + c * CH, &mp.a[0], bar, ti.row0 + c * C::MN_CHUNK, kr);
+            if (sp)
+              tma_load_2d(sa + SPLIT_EXTRA_OFF + c * CH, &mp.a[1], bar, ti.row0 + c * C::MN_CHUNK, kr);
+          }
           for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
             tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, kr);
           if (MX) {   // row-block atoms [row tile][M/128] and [row tile][N/128]
@@ -380,14 +386,17 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
           }
           break;
         }
-        default: {           // kBwdDWUpGate: A: Xg^T (M = H); B: du | dv cols n0..n0+127, hi/lo
-          const int kr = ti.krow0 + chunk * BK;
+        default: {           // kBwdDWUpGate: A: Xg^T (M = H); B: du | dv cols n0..n0+127 (+ lo)
+          const int kr = ti.krow0 + kb * BK;
           for (int c = 0; c < BM / C::MN_CHUNK; ++c)
             tma_load_2d(sa + c * CH, &mp.a[0], bar, ti.row0 + c * C::MN_CHUNK, kr);
-          for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
-            tma_load_2d(sb + c * CH, &mp.b[2 * part], bar, ti.n0 + c * C::MN_CHUNK, kr);
-            tma_load_2d(sb + (128 / C::MN_CHUNK + c) * CH, &mp.b[2 * part + 1], bar,
-                        ti.n0 + c * C::MN_CHUNK, kr);
+          for (int part = 0; part <= sp; ++part) {
+            uint8_t* dst = part ? sa + SPLIT_EXTRA_OFF : sb;
+            for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
+              tma_load_2d(dst + c * CH, &mp.b[2 * part], bar, ti.n0 + c * C::MN_CHUNK, kr);
+              tma_load_2d(dst + (128 / C::MN_CHUNK + c) * CH, &mp.b[2 * part + 1], bar,
+                          ti.n0 + c * C::MN_CHUNK, kr);
+            }
           }
           if (MX) {
             bulk_load(sf, p.sfa + ((size_t)(kr / BM) * (p.H / 128) + ti.row0 / 128) * 512, 512, bar);
@@ -454,7 +463,7 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
         return;
       }
       tc_fence_after();
-      const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+      const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
       const uint32_t sb = sa + A_BYTES;
       uint32_t t_sfa = 0, t_sfb = 0;
       if (MX) {
@@ -480,6 +489,17 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
           umma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, n_mma, a_mn, b_mn, kk), t_sfa, t_sfb, accum);
         else
           umma_bf16(d_tmem, ad, bd, idesc, accum);
+      }
+      if (!MX && p.split) {
+        // the lo half of the K chunk, after the hi half, into the same accumulator:
+        // dW_up|gate pairs A with B lo, dW_down pairs A lo with B
+        const uint32_t sx = sa + SPLIT_EXTRA_OFF;
+        const uint32_t a2 = p.mode == kBwdDWDown ? sx : sa;
+        const uint32_t b2 = p.mode == kBwdDWDown ? sb : sx;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(d_tmem, umma_desc_sw128(a2 + kk * C::MN_KSTEP, C::MN_LBO, 1024),
+                    umma_desc_sw128(b2 + kk * C::MN_KSTEP, C::MN_LBO, 1024), idesc, 1u);
       }
       umma_commit(&empty[stage]);   // frees the stage once these MMAs have read it
     }
@@ -721,7 +741,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int STAGES = C::STAGES;   // barrier slots; the launch uses p.stages of them
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* staging = smem + p.stages * C::STAGE_BYTES;
+  uint8_t* staging = smem + p.stages * p.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
@@ -842,11 +862,19 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   p.k = c.k;
   p.groups = c.dense ? 1 : c.groups;
   p.split = (!MX && c.split && (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
+  static_assert(2 * SPLIT_STAGE_BYTES + 2 * OUT_STAGING <= Cfg<false>::DATA_BYTES,
+                "split stages and staging exceed the data area");
   p.lo_out = (!MX && c.mode == kBwdDH && c.out[1] && c.out[3] && c.out[5]) ? 1 : 0;
-  // Every mode keeps the full operand ring: the dW modes are bound by refilling their
-  // operands from L2, and trading a stage for deeper output staging made them slower.
+  // Modes without split keep the full operand ring (trading a stage for deeper output
+  // staging made the dW modes slower).
   p.stages = C::STAGES;
   p.nbuf = 2;
+  p.stage_bytes = C::STAGE_BYTES;
+  if (p.split) {   // two chunk-sized hi/lo stages leave room for 4 staging boxes per warp
+    p.stages = 2;
+    p.nbuf = 4;
+    p.stage_bytes = SPLIT_STAGE_BYTES;
+  }
   p.poff = c.poff;
   p.counts = c.counts;
   p.offsets = c.offsets;
@@ -920,11 +948,11 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
     case kBwdDX:
       p.BN = (c.H % 256 == 0) ? 256 : 128;
       p.n_tiles = c.H / p.BN;
-      p.kiters = (2 * (c.I / BK)) << p.split;
+      p.kiters = 2 * (c.I / BK);
       p.kcs_a = c.I / 128;
       p.kcs_b = c.I / 128;
       p.ncs_b = c.H / 128;
-      for (int i = 0; i < (p.split ? 4 : 2) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BM, eb);
+      for (int i = 0; i < 2 && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BM, eb);
       ok = ok && make_map(&mp.b[0], c.b[0], c.I, G * c.H, p.BN, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, p.BN, eb) &&
            make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);
