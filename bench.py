@@ -53,6 +53,37 @@ def peaks():
             "source": "fallback"}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a kernel, from
+# one ncu capture, scaled to the workload's launch as the named profile summary states.
+# A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
+NCU_TRAFFIC = {
+    ("kimi_8192", "gemm_bwd_dw_upgate"): {
+        "bytes": 46.43e9, "rev": "ec029a4e93f85a30",
+        "profile": "profiles/grouped_gemm_dw_kimi_e24.md"},
+}
+GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
+                "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
+                "grouped_gemm_built_gb300/csrc/mok_internal.h")
+
+
+def gemm_source_rev():
+    """First 16 hex digits of sha256 over the lines '<sha256>  <path>' of the GEMM sources
+    (what `sha256sum <files> | sha256sum` prints)."""
+    import hashlib
+    text = ""
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            text += f"{hashlib.sha256(f.read()).hexdigest()}  {rel}\n"
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    rec = NCU_TRAFFIC.get((workload, kernel))
+    if rec is None or rec["rev"] != gemm_source_rev():
+        return None
+    return rec["bytes"]
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -313,9 +344,13 @@ def run_gpu(args):
         ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
         if ai < ridge:
             achieved = byts / dur / 1e9
+            tr = ncu_traffic(args.workload, name)
             roofline = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
                         "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                        "frac": round(achieved / pk["hbm_gbs"], 4),
+                        "traffic": None if tr is None else round(tr / 1e9, 3),
+                        "traffic_unit": "GB per launch",
+                        "algorithmic": round(byts / 1e9, 3),
                         "peak_source": pk["source"] + " (copy bandwidth)"}
         else:
             achieved = flops / dur / 1e12
