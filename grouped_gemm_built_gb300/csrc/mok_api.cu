@@ -2,6 +2,7 @@
 // the launch sequences of mok_plan, mok_moe_fwd and mok_moe_bwd.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -23,6 +24,7 @@ struct mok_ctx_s {
   mok_dims dims;
   mok::Dims d;
   mok_precision precision;
+  mok_fwd_path fwd_path = MOK_FWD_MEGAKERNEL;
   int device;
   int num_sms;
   // optional per-launch timing (mok_profile.h)
@@ -77,6 +79,21 @@ Dims make_dims(const mok_dims& x) {
   d.P_max = (int)align_up((size_t)d.R + (size_t)d.E * (kRowPad - 1), kRowPad);
   d.mt_max = d.P_max / kRowPad;
   d.nblk = (x.T + kTokBlock - 1) / kTokBlock;
+  // macrobatches: Tm tokens each, a multiple of 128 (so a macrobatch is whole histogram
+  // blocks and whole 128-token tiles); 0 means one
+  const int want = x.macrobatches > 0 ? x.macrobatches : 1;
+  d.Tm = (int)align_up((size_t)((x.T + want - 1) / want), kRowPad);
+  d.M = (x.T + d.Tm - 1) / d.Tm;
+  const long long rows_m = (long long)std::min(d.Tm, x.T) * x.k;
+  d.mt_m_max = (int)((rows_m + (long long)std::min<long long>(x.E, rows_m) * (kRowPad - 1) +
+                      kRowPad - 1) / kRowPad);
+  d.P_slot = d.mt_m_max * kRowPad;
+  d.P_cat = (int)align_up((size_t)d.R + (size_t)d.E * (kRowPad - 1) * d.M, kRowPad);
+  if (d.M == 1) d.P_cat = std::max(d.P_cat, d.P_max);
+  // ring slots: as many as ring_bytes holds at bf16 (the larger row format), at most M
+  const size_t slot_bytes = (size_t)d.P_slot * d.H * 2;
+  d.S = d.M;
+  if (x.ring_bytes > 0) d.S = (int)std::min<size_t>((size_t)d.M, x.ring_bytes / slot_bytes);
   return d;
 }
 
@@ -98,6 +115,12 @@ AuxLayout aux_layout(const Dims& d) {
   L.poff = b.take(sizeof(int32_t) * (d.E + 1));
   L.tile_expert = b.take(sizeof(int32_t) * d.mt_max);
   L.num_mtiles = b.take(sizeof(int32_t));
+  L.mstart = b.take(sizeof(int32_t) * (size_t)d.M * d.E);
+  L.mcount = b.take(sizeof(int32_t) * (size_t)d.M * d.E);
+  L.mpoff = b.take(sizeof(int32_t) * (size_t)d.M * (d.E + 1));
+  L.mtile_expert = b.take(sizeof(int32_t) * (size_t)d.M * d.mt_m_max);
+  L.mtiles = b.take(sizeof(int32_t) * (size_t)d.M);
+  L.mrow0 = b.take(sizeof(int32_t) * (size_t)(d.M + 1));
   L.total = b.off;
   return L;
 }
@@ -115,7 +138,7 @@ PlanWs plan_ws(const Dims& d) {
 FwdWs fwd_ws(const Dims& d) {
   Bump b;
   FwdWs L;
-  const size_t P = d.P_max;
+  const size_t P = d.P_cat;
   L.xg = b.take(2 * P * d.H);
   L.h = b.take(2 * P * d.I);
   L.o = b.take(4 * P * d.H);
@@ -125,6 +148,9 @@ FwdWs fwd_ws(const Dims& d) {
   L.xsf = b.take(P * d.H / 32);
   L.hq = b.take(P * d.I);
   L.hsf = b.take(P * d.I / 32);
+  L.ring = b.take((size_t)d.S * d.P_slot * d.H * 2);
+  L.ring_sf = b.take((size_t)d.S * d.P_slot * d.H / 32);
+  L.cnt = b.take(sizeof(int) * (size_t)mega_cnt(d).total);
   L.total = b.off;
   return L;
 }
@@ -194,7 +220,7 @@ BwdWs bwd_ws(const Dims& d) {
 SavedLayout saved_layout(const Dims& d) {
   Bump b;
   SavedLayout L;
-  const size_t P = d.P_max;
+  const size_t P = d.P_cat;
   L.u = b.take(4 * P * d.I);
   L.v = b.take(4 * P * d.I);
   L.us = b.take(4 * (size_t)d.T * d.Is);
@@ -271,6 +297,7 @@ mok_status mok_create(const mok_dims* dims, mok_ctx_t* out) {
   if (x.shared_I < 0 || (x.shared_I % 128) != 0) return MOK_ERR_INVALID_ARG;
   if (x.router != 0 && x.router != 1) return MOK_ERR_INVALID_ARG;
   if (x.macrobatches < 0) return MOK_ERR_INVALID_ARG;
+  if (make_dims(x).S < 1) return MOK_ERR_INVALID_ARG;  // ring_bytes below one slot
   if ((long long)x.T * x.k + (long long)x.E * 127 > (1LL << 30)) return MOK_ERR_INVALID_ARG;
   if ((long long)x.E * x.H > (1LL << 31) || (long long)x.E * x.I > (1LL << 31))
     return MOK_ERR_INVALID_ARG;
@@ -304,6 +331,13 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
   return MOK_OK;
 }
 
+mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  if (path != MOK_FWD_MEGAKERNEL && path != MOK_FWD_LAUNCHES) return MOK_ERR_INVALID_ARG;
+  ctx->fwd_path = path;
+  return MOK_OK;
+}
+
 mok_status mok_get_sizes(mok_ctx_t ctx, mok_sizes* out) {
   if (!ctx || !out) return MOK_ERR_INVALID_ARG;
   const Dims& d = ctx->d;
@@ -316,7 +350,8 @@ mok_status mok_get_sizes(mok_ctx_t ctx, mok_sizes* out) {
   out->saved_bytes = saved_layout(d).total;
   out->mx_weight_bytes = mx_weights_layout(d).total;
   out->padded_rows_max = d.P_max;
-  out->macrobatches = 1;
+  out->macrobatches = d.M;
+  out->ring_slots = d.S;
   return MOK_OK;
 }
 
@@ -417,6 +452,83 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
   void* o = W(L.o);
   const bool mx = ctx->precision == MOK_MXFP8;
 
+  if (ctx->fwd_path == MOK_FWD_MEGAKERNEL) {
+    // shared expert first (BF16, dense launches); the megakernel's combine adds its output
+    const float* os = nullptr;
+    if (d.Is) {
+      GemmCall cs = dense_call(d, a, kFwdUpGate);
+      cs.a[0] = x;
+      cs.b[0] = w->Ws_up;
+      cs.b[1] = w->Ws_gate;
+      cs.out[0] = W(L.hs);
+      cs.out[1] = at(saved, S.us);
+      cs.out[2] = at(saved, S.vs);
+      MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+      cs = dense_call(d, a, kFwdDown);
+      cs.a[0] = W(L.hs);
+      cs.b[0] = w->Ws_down;
+      cs.out[0] = W(L.os);
+      MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+      os = reinterpret_cast<const float*>(W(L.os));
+    }
+    MegaCall mc;
+    memset(&mc, 0, sizeof(mc));
+    mc.up = routed_call(d, sched, a, kFwdUpGate);
+    mc.down = routed_call(d, sched, a, kFwdDown);
+    mc.up.M_rows = mc.down.M_rows = d.P_cat;
+    mc.up.a_rows = d.S * d.P_slot;
+    mc.up.mx = mc.down.mx = mx;
+    mc.up.a[0] = W(L.ring);
+    mc.up.out[1] = at(saved, S.u);
+    mc.up.out[2] = at(saved, S.v);
+    mc.down.out[0] = o;
+    if (!mx) {
+      mc.up.b[0] = w->W_up;
+      mc.up.b[1] = w->W_gate;
+      mc.up.out[0] = W(L.h);
+      mc.down.a[0] = W(L.h);
+      mc.down.b[0] = w->W_down;
+    } else {
+      MxWeights M = mx_weights_layout(d);
+      char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
+      mc.up.sfa = W(L.ring_sf);
+      mc.up.b[0] = mxw + M.up_h;
+      mc.up.b[1] = mxw + M.gate_h;
+      mc.up.sfb0 = mxw + M.up_h_sf;
+      mc.up.sfb1 = mxw + M.gate_h_sf;
+      mc.up.out_q[0] = W(L.hq);
+      mc.up.out_sf[0] = W(L.hsf);
+      mc.down.a[0] = W(L.hq);
+      mc.down.sfa = W(L.hsf);
+      mc.down.b[0] = mxw + M.down_i;
+      mc.down.sfb0 = mxw + M.down_i_sf;
+    }
+    mc.M = d.M;
+    mc.S = d.S;
+    mc.P_slot = d.P_slot;
+    mc.Tm = d.Tm;
+    mc.T = d.T;
+    mc.mt_m_max = d.mt_m_max;
+    mc.mstart = a.mstart;
+    mc.mcount = a.mcount;
+    mc.mpoff = a.mpoff;
+    mc.mtile_expert = a.mtile_expert;
+    mc.mtiles = a.mtiles;
+    mc.mrow0 = a.mrow0;
+    mc.topk_idx = sched->topk_idx;
+    mc.inv = sched->inv;
+    mc.x = x;
+    mc.ring = W(L.ring);
+    mc.ring_sf = W(L.ring_sf);
+    mc.O = reinterpret_cast<const float*>(o);
+    mc.Os = os;
+    mc.y = static_cast<float*>(y);
+    mc.cnt = reinterpret_cast<int*>(W(L.cnt));
+    MOK_CHECK_CUDA(cudaMemsetAsync(mc.cnt, 0, sizeof(int) * (size_t)mega_cnt(d).total, s));
+    MOK_LAUNCH(mx ? "fwd_megakernel_mxfp8" : "fwd_megakernel", launch_fwd_mega(mc, ctx->num_sms, s));
+    return MOK_OK;
+  }
+
   if (!mx) {
     // dispatch: pull token rows into expert order through the table
     MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), ctx->num_sms, s));
@@ -498,6 +610,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   if (!g || !g->dW_up || !g->dW_gate || !g->dW_down || !g->dgates) return MOK_ERR_INVALID_ARG;
   if (!aligned(g->dW_up, 16) || !aligned(g->dW_gate, 16) || !aligned(g->dW_down, 16))
     return MOK_ERR_INVALID_ARG;
+  if (d.M > 1) return MOK_ERR_UNSUPPORTED;   // saved U, V are per macrobatch then
   if (ctx->precision == MOK_MXFP8 && (!w->mx || !aligned(w->mx, 256))) return MOK_ERR_INVALID_ARG;
   if (d.router && (!Wr || !g->dWr)) return MOK_ERR_INVALID_ARG;
   if (!d.router && (Wr || g->dWr)) return MOK_ERR_INVALID_ARG;

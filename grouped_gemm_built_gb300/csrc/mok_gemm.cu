@@ -40,6 +40,7 @@
 #include <mutex>
 
 #include "mok_internal.h"
+#include "mok_mx.cuh"
 #include "mok_ptx.cuh"
 
 namespace mok {
@@ -132,6 +133,7 @@ struct Params {
 struct TileInfo {
   int e;        // expert (0 when dense)
   int row0;     // first row of the row space (row-space modes) / first dW row (dW modes)
+  int arow0;    // row-space modes: first row of the A operand (row0 unless A lives elsewhere)
   int n0;       // first output column
   int kiters;   // K iterations
   int krow0;    // dW modes: first row of the contraction range
@@ -173,6 +175,7 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
     ti.kiters = p.kiters;
     ti.krow0 = 0;
   }
+  ti.arow0 = ti.row0;
   return ti;
 }
 
@@ -285,29 +288,27 @@ struct Stager {
 };
 
 // ------------------------------------------------------------------ producer
+// One tile's K loop: fills stages it, it+1, ... (it counts stage uses over the CTA's
+// whole task sequence). Returns false after a timed-out wait.
 template <bool MX>
-__device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
-                        uint64_t* empty, volatile int* abort_flag) {
+__device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
+                             uint64_t* empty, volatile int* abort_flag, const TileInfo& ti,
+                             uint32_t& it) {
   using C = Cfg<MX>;
   constexpr int BK = C::BK;
   const int STAGES = p.stages;
   constexpr int CH = C::MN_LBO;        // bytes of one MN-major chunk
-  const int ntiles = num_tiles_of(p);
   const int sp = p.split;
-  uint32_t it = 0;
   uint32_t b_bytes = (p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 256 * 128 : p.BN * 128;
   if (MX) b_bytes += 512 + ((p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 1024 : p.BN * 4);
-  bool ok = true;
-  for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-    const TileInfo ti = tile_info<MX>(p, tile);
+  {
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
       const uint32_t round = it / STAGES;
       if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1, globaltimer_ns() + kTimeoutNs)) {
         set_error(p.status, kErrTimeout);
         *abort_flag = 1;
-        ok = false;
-        break;
+        return false;
       }
       uint8_t* sa = smem + stage * p.stage_bytes;
       uint8_t* sb = sa + A_BYTES;
@@ -319,7 +320,7 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
       const int k0 = kb * BK;
       switch (p.mode) {
         case kFwdUpGate: {   // A: Xg rows (K-major); B: W_up|W_gate cols n0..n0+127 (MN-major)
-          tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
+          tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
           const int brow = ti.e * p.H + k0;
           for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
             tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, brow);
@@ -327,7 +328,7 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
                         brow);
           }
           if (MX) {
-            bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
+            bulk_load(sf, p.sfa + ((size_t)(ti.arow0 / BM) * p.kcs_a + kb) * 512, 512, bar);
             const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
             bulk_load(sf + 512, p.sfb0 + bi, 512, bar);
             bulk_load(sf + 1024, p.sfb1 + bi, 512, bar);
@@ -335,22 +336,22 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
           break;
         }
         case kFwdDown: {     // A: h rows (K-major); B: W_down cols (MN-major)
-          tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
+          tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
           const int brow = ti.e * p.I + k0;
           for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
             tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, brow);
           if (MX) {
-            bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
+            bulk_load(sf, p.sfa + ((size_t)(ti.arow0 / BM) * p.kcs_a + kb) * 512, 512, bar);
             const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
             bulk_load(sf + 512, p.sfb0 + bi, p.BN * 4, bar);
           }
           break;
         }
         case kBwdDH: {       // A: dYg rows (K-major); B: W_down rows i (K-major over H)
-          tma_load_2d(sa, &mp.a[0], bar, k0, ti.row0);
+          tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
           tma_load_2d(sb, &mp.b[0], bar, k0, ti.e * p.I + ti.n0);
           if (MX) {
-            bulk_load(sf, p.sfa + ((size_t)(ti.row0 / BM) * p.kcs_a + kb) * 512, 512, bar);
+            bulk_load(sf, p.sfa + ((size_t)(ti.arow0 / BM) * p.kcs_a + kb) * 512, 512, bar);
             const size_t bi = (((size_t)ti.e * p.kcs_b + kb) * p.ncs_b + ti.n0 / 128) * 512;
             bulk_load(sf + 512, p.sfb0 + bi, p.BN * 4, bar);
           }
@@ -360,10 +361,10 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
           const int per_half = p.I / BK;
           const int second = kb >= per_half ? 1 : 0;
           const int kq = kb - second * per_half;   // K chunk inside the half
-          tma_load_2d(sa, &mp.a[second], bar, kq * BK, ti.row0);
+          tma_load_2d(sa, &mp.a[second], bar, kq * BK, ti.arow0);
           tma_load_2d(sb, &mp.b[second], bar, kq * BK, ti.e * p.H + ti.n0);
           if (MX) {
-            bulk_load(sf, (second ? p.sfa1 : p.sfa) + ((size_t)(ti.row0 / BM) * p.kcs_a + kq) * 512,
+            bulk_load(sf, (second ? p.sfa1 : p.sfa) + ((size_t)(ti.arow0 / BM) * p.kcs_a + kq) * 512,
                       512, bar);
             const size_t bi = (((size_t)ti.e * p.kcs_b + kq) * p.ncs_b + ti.n0 / 128) * 512;
             bulk_load(sf + 512, (second ? p.sfb1 : p.sfb0) + bi, p.BN * 4, bar);
@@ -409,9 +410,15 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
       }
     }
   }
-  // Drain: every issued copy has landed and every MMA commit has arrived before the
-  // CTA's shared memory goes away.
-  const uint32_t n_armed = it;
+  return true;
+}
+
+// Drain: every issued copy has landed and every MMA commit has arrived before the CTA's
+// shared memory goes away (n_armed = stage uses issued).
+template <bool MX>
+__device__ void produce_drain(const Params& p, uint64_t* full, uint64_t* empty,
+                              uint32_t n_armed) {
+  const int STAGES = p.stages;
   for (uint32_t s = 0; s < (uint32_t)STAGES && s < n_armed; ++s) {
     const uint32_t last = ((n_armed - 1 - s) / STAGES) * STAGES + s;  // last use of stage s
     const uint32_t round = last / STAGES;
@@ -422,16 +429,25 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
   }
 }
 
-// ------------------------------------------------------------------ MMA issuer
 template <bool MX>
-__device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                          uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
-                          volatile int* abort_flag) {
-  using C = Cfg<MX>;
-  const int STAGES = p.stages;
+__device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
+                        uint64_t* empty, volatile int* abort_flag) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
-  int local = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+    if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, tile_info<MX>(p, tile), it)) break;
+  produce_drain<MX>(p, full, empty, it);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+// One tile: waits for a free accumulator (local = the CTA's tile count so far), issues the
+// K loop's MMAs and commits the accumulator. Returns false after a timed-out wait.
+template <bool MX>
+__device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                         uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                         volatile int* abort_flag, const TileInfo& ti, uint32_t& it, int local) {
+  using C = Cfg<MX>;
+  const int STAGES = p.stages;
   bool a_mn = false, b_mn = false;
   int n_mma = p.BN;
   switch (p.mode) {
@@ -443,14 +459,13 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
     default: a_mn = true; b_mn = true; n_mma = 256; break;
   }
   const uint32_t idesc = idesc_bf16(BM, n_mma, a_mn, b_mn);
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-    const TileInfo ti = tile_info<MX>(p, tile);
+  {
     const int acc = local % C::NACC;
     const uint32_t use = local / C::NACC;
     if (use > 0 && !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + kTimeoutNs)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
-      return;
+      return false;
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
@@ -460,7 +475,7 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
       if (!mbar_wait(&full[stage], round & 1, globaltimer_ns() + kTimeoutNs)) {
         set_error(p.status, kErrTimeout);
         *abort_flag = 1;
-        return;
+        return false;
       }
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
@@ -506,27 +521,41 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
     if (ti.kiters > 0) umma_commit(&acc_full[acc]);
     else mbar_arrive(&acc_full[acc]);  // nothing to accumulate: epilogue writes zeros
   }
+  return true;
+}
+
+template <bool MX>
+__device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                          uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                          volatile int* abort_flag) {
+  const int ntiles = num_tiles_of(p);
+  uint32_t it = 0;
+  int local = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local)
+    if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag,
+                      tile_info<MX>(p, tile), it, local))
+      return;
 }
 
 // ------------------------------------------------------------------ epilogue
+// One tile (local = the CTA's tile count so far): waits for its accumulator, runs the
+// mode's epilogue and frees the accumulator. Warp-collective over the 4 epilogue warps.
+// Returns false after a timed-out wait.
 template <bool MX>
-__device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint64_t* acc_full,
-                         uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag) {
+__device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint64_t* acc_full,
+                              uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag,
+                              const TileInfo& ti, int local) {
   using C = Cfg<MX>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
   const int r = quarter * 32 + lane;        // row inside the tile
-  const int ntiles = num_tiles_of(p);
-  Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
-  int local = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-    const TileInfo ti = tile_info<MX>(p, tile);
+  {
     const int acc = local % C::NACC;
     const uint32_t use = local / C::NACC;
     if (!mbar_wait(&acc_full[acc], use & 1, globaltimer_ns() + kTimeoutNs)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
-      break;
+      return false;
     }
     tc_fence_after();
     const uint32_t t_row = tmem_base + acc * C::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
@@ -731,6 +760,20 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
     tc_fence_before();
     mbar_arrive(&acc_empty[acc]);
   }
+  return true;
+}
+
+template <bool MX>
+__device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint64_t* acc_full,
+                         uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = num_tiles_of(p);
+  Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
+  int local = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local)
+    if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag,
+                           tile_info<MX>(p, tile), local))
+      break;
   st.drain();
 }
 
@@ -787,6 +830,462 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ forward megakernel
+// One persistent launch for dispatch, the grouped up|gate and down GEMMs and the combine
+// of the routed experts ([C] "O que e o MoK", "Granularidade do overlap", "Ring token
+// buffers (macrobatch)"; [S] "Das Scheduling"). Its CTAs (one per SM, co-resident by a
+// cooperative launch) are split in software:
+//
+//   CTAs 0 .. n_comm-1   gather/combine SMs: move the dispatched rows of macrobatch m into
+//                        ring slot m % S with TMA bulk copies (MXFP8: quantised along H on
+//                        the way), 128-row tile by tile, and combine finished macrobatches;
+//   the other CTAs       GEMM SMs: the warp-specialised tcgen05 pipeline above, over a fixed
+//                        task order: for each macrobatch, its up|gate tiles, then its down
+//                        tiles; task i goes to GEMM CTA i mod G.
+//
+// The sides signal through device counters (release adds, acquire loads):
+//   gathered[m][r]  row tile r of m is in its slot           (up|gate tiles of r wait)
+//   hcnt[m][r]      up|gate tiles of row tile r done         (down tiles of r wait for all)
+//   upg_done[m]     up|gate tiles of m done: slot m % S is free again (gather m + S waits)
+//   down_done[m]    down tiles of m done                     (combine of m waits)
+// Every dependency points to an earlier task, and each CTA takes its tasks in order, so the
+// earliest unfinished task can always run. Every wait is bounded; on expiry the waiter
+// records MOK_ERR_TIMEOUT, raises the shared abort flag and returns.
+struct MegaParams {
+  Params up, down;
+  int M, S, P_slot, Tm, T, H, I, E, k, mt_m_max, n_comm, has_shared;
+  const int32_t* mstart;
+  const int32_t* mcount;
+  const int32_t* mpoff;
+  const int32_t* mtile_expert;
+  const int32_t* mtiles;
+  const int32_t* mrow0;
+  const int32_t* table;
+  const int32_t* topk_idx;
+  const int32_t* inv;
+  const float* gates;
+  const uint8_t* x;     // [T][H] bf16
+  uint8_t* ring;        // [S][P_slot][H] bf16 (MXFP8: e4m3)
+  uint8_t* ring_sf;     // MXFP8: atoms [S][P_slot/128][H/128]
+  const float* O;       // expert outputs [P_cat][H]
+  const float* Os;      // shared expert output [T][H] or null
+  float* y;             // [T][H]
+  int* cnt;             // counters (MegaCnt layout), zero at launch
+  uint32_t* status;
+};
+struct MegaMaps {
+  Maps up, down;
+};
+
+constexpr int kCommWarps = NUM_THREADS / 32;
+constexpr int kCopyChunk = 8192;                 // bytes per bulk copy
+constexpr int kCopyBufs = 3;                     // per warp
+
+// Bounded wait until *c >= need (acquire). False if the deadline passed or another CTA
+// raised the abort flag.
+__device__ bool wait_count(const int* c, int need, int* abort_g, uint32_t* status) {
+  const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
+  uint32_t spins = 0;
+  while (ld_acquire(c) < need) {
+    if ((++spins & 63u) == 0) {
+      if (ld_relaxed(abort_g)) return false;
+      if (globaltimer_ns() > deadline) {
+        set_error(status, kErrTimeout);
+        atomicExch(abort_g, 1);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+__device__ __forceinline__ int mega_mtiles(const MegaParams& q, int m) {
+  return min(max(q.mtiles[m], 0), q.mt_m_max);
+}
+
+__device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph, int t) {
+  const Params& p = ph ? q.down : q.up;
+  const int r = t / p.n_tiles, n = t - r * p.n_tiles;
+  TileInfo ti;
+  const int e = q.mtile_expert[(size_t)m * q.mt_m_max + r];
+  ti.e = (e < 0 || e >= q.E) ? 0 : e;
+  ti.row0 = q.mrow0[m] + r * BM;                                   // h, U, V, O rows
+  ti.arow0 = ph ? ti.row0 : (m % q.S) * q.P_slot + r * BM;        // ring slot rows
+  ti.n0 = n * (ph ? p.BN : 128);
+  ti.kiters = p.kiters;
+  ti.krow0 = 0;
+  return ti;
+}
+
+// Calls f(m, phase, t) for GEMM CTA g's tasks in order; stops when f returns false.
+template <class F>
+__device__ void mega_for_each(const MegaParams& q, int g, int G, F&& f) {
+  int base = 0;   // tasks before the current phase, mod G
+  for (int m = 0; m < q.M; ++m) {
+    const int mt = mega_mtiles(q, m);
+    for (int ph = 0; ph < 2; ++ph) {
+      const int n = mt * (ph ? q.down.n_tiles : q.up.n_tiles);
+      int t = (g - base) % G;
+      if (t < 0) t += G;
+      for (; t < n; t += G)
+        if (!f(m, ph, t)) return;
+      base = (base + n) % G;
+    }
+  }
+}
+
+// Gather row tile r of macrobatch m into its ring slot. Each warp moves rows warp, warp+6,
+// ...: lane 0 runs a 3-buffer pipeline of bulk copies global -> shared -> global (two
+// loads ahead); MXFP8 converts each chunk in shared memory (blocks of 32 along H) and
+// writes E4M3 codes and scale bytes with ordinary stores. Padding rows are zeros.
+template <bool MX>
+__device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* bufs, const uint8_t* zero,
+                                 uint64_t* bars, uint32_t& phase, int* abort_g) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e_raw = q.mtile_expert[(size_t)m * q.mt_m_max + r];
+  const int e = (e_raw < 0 || e_raw >= q.E) ? 0 : e_raw;
+  const int po = q.mpoff[(size_t)m * (q.E + 1) + e];
+  const int cnt = q.mcount[(size_t)m * q.E + e];
+  const int st = q.mstart[(size_t)m * q.E + e];
+  const int slot_row0 = (m % q.S) * q.P_slot + r * BM;   // ring row of the tile's row 0
+  const uint32_t rowbytes = (uint32_t)q.H * 2;          // bf16 source row
+  const int nch = (int)((rowbytes + kCopyChunk - 1) / kCopyChunk);
+  const int nrows = (BM - warp + kCommWarps - 1) / kCommWarps;
+  const int V = nrows * nch;
+  uint8_t* mybuf = bufs + (size_t)warp * kCopyBufs * kCopyChunk;
+  uint64_t* mybar = bars + warp * kCopyBufs;
+  // chunk v: row i = warp + (v / nch) * 6 of the tile, bytes [c * chunk, ...) of the row
+  auto src_of = [&](int v, uint32_t& off, uint32_t& bytes, int& i) -> const uint8_t* {
+    i = warp + (v / nch) * kCommWarps;
+    const int c = v - (v / nch) * nch;
+    off = (uint32_t)c * kCopyChunk;
+    bytes = min((uint32_t)kCopyChunk, rowbytes - off);
+    const int local = r * BM + i - po;                  // row of e inside macrobatch m
+    if (local < 0 || local >= cnt) return nullptr;
+    const int t = q.table[2 * (size_t)(st + local)];
+    return q.x + (size_t)t * rowbytes + off;
+  };
+  uint32_t pending = 0;   // buffers with a load in flight (every lane tracks the same)
+  auto issue_load = [&](int v) {   // lane 0 issues; every lane records it
+    uint32_t off, bytes;
+    int i;
+    const uint8_t* src = src_of(v, off, bytes, i);
+    if (src) {
+      if (lane == 0) {
+        uint64_t* bar = mybar + v % kCopyBufs;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(mybuf + (v % kCopyBufs) * kCopyChunk, src, bytes, bar);
+      }
+      pending |= 1u << (v % kCopyBufs);
+    }
+  };
+  bool ok = true;
+  for (int v = 0; v < min(2, V); ++v) issue_load(v);
+  for (int v = 0; v < V; ++v) {
+    uint32_t off, bytes;
+    int i;
+    const uint8_t* src = src_of(v, off, bytes, i);
+    const int b = v % kCopyBufs;
+    uint8_t* buf = mybuf + b * kCopyChunk;
+    const size_t ring_row = (size_t)slot_row0 + i;
+    if (src) {   // every lane waits for the load (the MXFP8 path reads it)
+      const bool got = mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + kTimeoutNs);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          set_error(q.status, kErrTimeout);
+          atomicExch(abort_g, 1);
+        }
+        ok = false;
+        break;
+      }
+      phase ^= 1u << b;
+      pending &= ~(1u << b);
+    }
+    if (!MX) {
+      if (lane == 0) {
+        bulk_store(q.ring + ring_row * rowbytes + off, src ? buf : zero, bytes);
+        bulk_commit();
+      }
+    } else {
+      // 32 lanes x (bytes / 64) blocks: block bk of this chunk covers bf16 elements
+      // [off/2 + 32 bk, +32); codes go to the E4M3 row, scales into the slot's atoms
+      const int nblk = (int)(bytes / 64);
+      const size_t hrow = ring_row * (size_t)q.H;          // e4m3 row start
+      for (int bk = lane; bk < nblk; bk += 32) {
+        float f[32];
+        float amax = 0.f;
+        if (src) {
+          const uint4* sp4 = reinterpret_cast<const uint4*>(buf + bk * 64);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 w = sp4[u];
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+              const float2 t2 = __bfloat1622float2(h2[z]);
+              f[8 * u + 2 * z] = t2.x;
+              f[8 * u + 2 * z + 1] = t2.y;
+              amax = fmaxf(amax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int z = 0; z < 32; ++z) f[z] = 0.f;
+        }
+        const uint32_t sb = mx_scale_byte(amax);
+        const float inv = mx_inv_scale(sb);
+        uint32_t wq[8];
+#pragma unroll
+        for (int z = 0; z < 8; ++z)
+          wq[z] = (uint32_t)f32x2_to_e4m3x2(f[4 * z] * inv, f[4 * z + 1] * inv) |
+                  ((uint32_t)f32x2_to_e4m3x2(f[4 * z + 2] * inv, f[4 * z + 3] * inv) << 16);
+        const int hk = (int)(off / 2) + bk * 32;            // first H index of the block
+        uint4* dq = reinterpret_cast<uint4*>(q.ring + hrow + hk);
+        dq[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        dq[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+        const size_t atom = (ring_row >> 7) * (size_t)(q.H / 128) + (size_t)(hk >> 7);
+        q.ring_sf[atom * 512 + atom_byte((int)(ring_row & 127), hk)] = (uint8_t)sb;
+      }
+      fence_proxy_async_smem();   // these reads come before the next bulk load into buf
+      __syncwarp();
+    }
+    if (v + 2 < V) {
+      if (!MX && lane == 0) bulk_wait_read<1>();   // the store from buffer (v+2) % 3 read it
+      issue_load(v + 2);
+    }
+    __syncwarp();
+  }
+  if (!ok) {   // let the loads still in flight land before the CTA can leave
+    for (int b = 0; b < kCopyBufs; ++b)
+      if (pending & (1u << b))
+        mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + kTimeoutNs);
+  }
+  if (lane == 0) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+  }
+  __threadfence();
+  return ok;
+}
+
+// y[t] = sum_j g_tj O[row(t, j)] (+ Os[t]) for the tokens of macrobatch m, one warp per
+// token, warps wi, wi + nw, ... (same arithmetic and order as the standalone combine).
+__device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
+  const int lane = threadIdx.x & 31;
+  const int t0 = m * q.Tm, t1 = min(q.T, t0 + q.Tm);
+  const int nvec = q.H / 4;
+  const float4* O = reinterpret_cast<const float4*>(q.O);
+  const float4* Os = reinterpret_cast<const float4*>(q.Os);
+  float4* y = reinterpret_cast<float4*>(q.y);
+  for (int t = t0 + wi; t < t1; t += nw) {
+    int my_row = 0;
+    float my_g = 0.f;
+    if (lane < q.k) {
+      const int sl = t * q.k + lane;
+      int e = q.topk_idx[sl];
+      e = (e < 0 || e >= q.E) ? 0 : e;
+      my_row = q.mrow0[m] + q.mpoff[(size_t)m * (q.E + 1) + e] +
+               (q.inv[sl] - q.mstart[(size_t)m * q.E + e]);
+      my_g = q.gates[sl];
+    }
+    int rows[kMaxK];
+    float g[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+      g[j] = __shfl_sync(0xffffffffu, my_g, j);
+    }
+    for (int i = lane; i < nvec; i += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < q.k) {
+          const float4 f = __ldcg(O + (size_t)rows[j] * nvec + i);
+          acc.x = fmaf(g[j], f.x, acc.x);
+          acc.y = fmaf(g[j], f.y, acc.y);
+          acc.z = fmaf(g[j], f.z, acc.z);
+          acc.w = fmaf(g[j], f.w, acc.w);
+        }
+      }
+      if (Os) {
+        const float4 f = __ldcg(Os + (size_t)t * nvec + i);
+        acc.x += f.x;
+        acc.y += f.y;
+        acc.z += f.z;
+        acc.w += f.w;
+      }
+      y[(size_t)t * nvec + i] = acc;
+    }
+  }
+}
+
+// All threads: thread 0 waits for *c >= need, the CTA learns the outcome.
+__device__ bool cta_wait_count(const int* c, int need, int* abort_g, uint32_t* status,
+                               volatile int* s_ok) {
+  if (threadIdx.x == 0) *s_ok = wait_count(c, need, abort_g, status) ? 1 : 0;
+  __syncthreads();
+  const bool ok = *s_ok != 0;
+  __syncthreads();
+  return ok;
+}
+
+template <bool MX>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fwd_mega_kernel(const __grid_constant__ MegaMaps mm, const MegaParams q) {
+  using C = Cfg<MX>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_ok = abort_flag + 1;
+  volatile int* s_pub = abort_flag + 2;   // epilogue: the tile's outcome, read by all 4 warps
+  // gather SMs: 18 copy barriers after the GEMM barriers (those end before +128)
+  uint64_t* copy_bars = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES + 128);
+  const MegaCnt CN = {0, q.M * q.mt_m_max, 2 * q.M * q.mt_m_max, 2 * q.M * q.mt_m_max + q.M,
+                      2 * q.M * q.mt_m_max + 2 * q.M, 0};
+  int* cnt = q.cnt;
+  int* abort_g = cnt + CN.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool comm = (int)blockIdx.x < q.n_comm;
+  const int G = (int)gridDim.x - q.n_comm;
+
+  if (comm) {
+    // ---------------- gather / combine SM
+    uint8_t* bufs = smem;                                           // 6 warps x 3 x 8 KB
+    uint8_t* zero = smem + kCommWarps * kCopyBufs * kCopyChunk;     // 8 KB of zeros
+    for (int i = threadIdx.x; i < kCopyChunk / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(zero)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kCommWarps * kCopyBufs; ++i) mbar_init(&copy_bars[i], 1);
+      fence_mbar_init();
+    }
+    fence_proxy_async_smem();   // the zero chunk is read by bulk stores
+    __syncthreads();
+    uint32_t phase = 0;
+    const int c = blockIdx.x;
+    bool ok = true;
+    for (int m = 0; m < q.M && ok; ++m) {
+      if (m >= q.S)   // slot m % S drains when every up|gate tile of m - S has read it
+        ok = cta_wait_count(cnt + CN.upg_done + (m - q.S), mega_mtiles(q, m - q.S) * q.up.n_tiles,
+                            abort_g, q.status, s_ok);
+      const int mt = mega_mtiles(q, m);
+      for (int r = c; r < mt && ok; r += q.n_comm) {
+        ok = mega_gather_tile<MX>(q, m, r, bufs, zero, copy_bars, phase, abort_g);
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        if (ok && threadIdx.x == 0) red_release_add(cnt + CN.gathered + m * q.mt_m_max + r, 1);
+      }
+      if (ok && m >= 1) {   // combine the previous macrobatch while the GEMMs run this one
+        ok = cta_wait_count(cnt + CN.down_done + (m - 1),
+                            mega_mtiles(q, m - 1) * q.down.n_tiles, abort_g, q.status, s_ok);
+        if (ok) mega_combine(q, m - 1, c * kCommWarps + warp, q.n_comm * kCommWarps);
+      }
+    }
+    if (!ok) return;
+  } else {
+    // ---------------- GEMM SM
+    const int g = (int)blockIdx.x - q.n_comm;
+    uint8_t* staging = smem + q.up.stages * q.up.stage_bytes;
+    if (threadIdx.x == 0) {
+      for (int s2 = 0; s2 < STAGES; ++s2) {
+        mbar_init(&full[s2], 1);
+        mbar_init(&empty[s2], 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(&acc_full[a], 1);
+        mbar_init(&acc_empty[a], 128);
+      }
+      *abort_flag = 0;
+      fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (warp == 0) {
+      if (lane == 0) {
+        uint32_t it = 0;
+        mega_for_each(q, g, G, [&](int m, int ph, int t) {
+          const Params& p = ph ? q.down : q.up;
+          const int r = t / p.n_tiles;
+          const int* dep = cnt + (ph ? CN.hcnt : CN.gathered) + m * q.mt_m_max + r;
+          if (!wait_count(dep, ph ? q.up.n_tiles : 1, abort_g, q.status)) {
+            *abort_flag = 1;
+            return false;
+          }
+          fence_proxy_async_global();   // the TMA reads below follow the acquire
+          return produce_tile<MX>(p, ph ? mm.down : mm.up, smem, full, empty, abort_flag,
+                                  mega_tile(q, m, ph, t), it);
+        });
+        produce_drain<MX>(q.up, full, empty, it);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        uint32_t it = 0;
+        int local = 0;
+        mega_for_each(q, g, G, [&](int m, int ph, int t) {
+          return mma_tile<MX>(ph ? q.down : q.up, smem, full, empty, acc_full, acc_empty,
+                              tmem_base, abort_flag, mega_tile(q, m, ph, t), it, local++);
+        });
+      }
+    } else {
+      Stager st{staging + (warp - 2) * q.up.nbuf * STAGE_OUT_BYTES, 0u, lane, q.up.nbuf};
+      int local = 0;
+      mega_for_each(q, g, G, [&](int m, int ph, int t) {
+        const Params& p = ph ? q.down : q.up;
+        // a warp that timed out has raised the CTA's abort flag; every warp still meets
+        // the others at the barrier below, and after it all of them see the flag
+        epilogue_tile<MX>(p, ph ? mm.down : mm.up, st, acc_full, acc_empty, tmem_base,
+                          abort_flag, mega_tile(q, m, ph, t), local++);
+        // publish the tile: its TMA stores have landed (and, MXFP8, the plain stores of h)
+        if (lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+        }
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) {   // one reader, so the four warps decide alike
+          const int ok64 = *abort_flag == 0;
+          *s_pub = ok64;
+          if (ok64) {
+            const int r = t / p.n_tiles;
+            if (ph == 0) {
+              red_release_add(cnt + CN.hcnt + m * q.mt_m_max + r, 1);
+              red_release_add(cnt + CN.upg_done + m, 1);
+            } else {
+              red_release_add(cnt + CN.down_done + m, 1);
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+        const bool ok = *s_pub != 0;
+        named_bar_sync(1, 128);   // s_pub is rewritten only after every warp has read it
+        return ok;
+      });
+      st.drain();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+  }
+  // ---------------- last macrobatch: every CTA combines
+  const int mlast = q.M - 1;
+  if (!cta_wait_count(cnt + CN.down_done + mlast, mega_mtiles(q, mlast) * q.down.n_tiles,
+                      abort_g, q.status, s_ok))
+    return;
+  mega_combine(q, mlast, (int)blockIdx.x * kCommWarps + warp, (int)gridDim.x * kCommWarps);
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -840,19 +1339,12 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int 
   return r == CUDA_SUCCESS;
 }
 
+// Kernel parameters and tensor maps of one grouped-GEMM call; max_tiles = tiles of the
+// largest possible problem (the launch's grid bound).
 template <bool MX>
-cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
+cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   using C = Cfg<MX>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   if (MX && c.dense) return cudaErrorNotSupported;  // the shared expert stays BF16
-  Params p;
   memset(&p, 0, sizeof(p));
   p.mode = c.mode;
   p.dense = c.dense ? 1 : 0;
@@ -897,11 +1389,11 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
 
   const int eb = MX ? 1 : 2;                  // element bytes of the GEMM operands
   const uint64_t rows = (uint64_t)c.M_rows;   // rows of the row-space buffers
+  const uint64_t arows = c.a_rows > 0 ? (uint64_t)c.a_rows : rows;  // rows of A's buffer
   const uint64_t G = (uint64_t)p.groups;
-  Maps mp;
   memset(&mp, 0, sizeof(mp));
   bool ok = true;
-  int max_tiles = 0;
+  max_tiles = 0;
   const int mt_rows = (int)((rows + BM - 1) / BM);
   const int BK = C::BK;
   switch (c.mode) {
@@ -912,7 +1404,7 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       p.kcs_a = c.H / 128;
       p.kcs_b = c.H / 128;
       p.ncs_b = c.I / 128;
-      ok = make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
+      ok = make_map(&mp.a[0], c.a[0], c.H, arows, BM, eb) &&
            make_map(&mp.b[0], c.b[0], c.I, G * c.H, BK, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, BK, eb) &&
            (MX || make_out_map(&mp.o[0], c.out[0], c.I, rows, 2)) &&
@@ -979,6 +1471,25 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+template <bool MX>
+cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
+  using C = Cfg<MX>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  Params p;
+  Maps mp;
+  int max_tiles = 0;
+  cudaError_t e = build_call<MX>(c, p, mp, max_tiles);
+  if (e != cudaSuccess) return e;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
   grouped_gemm_kernel<MX><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(mp, p);
@@ -987,7 +1498,76 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
 
 }  // namespace
 
+template <bool MX>
+cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
+  using C = Cfg<MX>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_mega_kernel<MX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  static_assert(kCommWarps * kCopyBufs * kCopyChunk + kCopyChunk <= C::DATA_BYTES,
+                "gather buffers exceed the data area");
+  MegaParams q;
+  MegaMaps mm;
+  memset(&q, 0, sizeof(q));
+  int mt = 0;
+  cudaError_t e = build_call<MX>(c.up, q.up, mm.up, mt);
+  if (e != cudaSuccess) return e;
+  if ((e = build_call<MX>(c.down, q.down, mm.down, mt)) != cudaSuccess) return e;
+  if (q.up.stages != q.down.stages || q.up.stage_bytes != q.down.stage_bytes ||
+      q.up.nbuf != q.down.nbuf)
+    return cudaErrorInvalidValue;
+  q.M = c.M;
+  q.S = c.S;
+  q.P_slot = c.P_slot;
+  q.Tm = c.Tm;
+  q.T = c.T;
+  q.H = c.up.H;
+  q.I = c.up.I;
+  q.E = c.up.groups;
+  q.k = c.up.k;
+  q.mt_m_max = c.mt_m_max;
+  q.has_shared = c.Os != nullptr;
+  q.mstart = c.mstart;
+  q.mcount = c.mcount;
+  q.mpoff = c.mpoff;
+  q.mtile_expert = c.mtile_expert;
+  q.mtiles = c.mtiles;
+  q.mrow0 = c.mrow0;
+  q.table = c.up.table;
+  q.topk_idx = c.topk_idx;
+  q.inv = c.inv;
+  q.gates = c.up.gates;
+  q.x = static_cast<const uint8_t*>(c.x);
+  q.ring = static_cast<uint8_t*>(c.ring);
+  q.ring_sf = static_cast<uint8_t*>(c.ring_sf);
+  q.O = c.O;
+  q.Os = c.Os;
+  q.y = c.y;
+  q.cnt = c.cnt;
+  q.status = c.up.status;
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_mega_kernel<MX>, NUM_THREADS,
+                                                         C::SMEM_BYTES)) != cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int grid = num_sms;   // one CTA per SM, all resident (cooperative launch)
+  q.n_comm = c.n_comm > 0 ? c.n_comm : (grid >= 32 ? 8 : 1);
+  if (grid - q.n_comm < 1) return cudaErrorInvalidConfiguration;
+  void* args[] = {&mm, &q};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fwd_mega_kernel<MX>), grid,
+                                     NUM_THREADS, args, C::SMEM_BYTES, s);
+}
+
 int gemm_dh_parts(int I) { return (I % 256 == 0) ? I / 256 : I / 128; }
+
+cudaError_t launch_fwd_mega(const MegaCall& c, int num_sms, cudaStream_t s) {
+  return c.up.mx ? launch_mega_impl<true>(c, num_sms, s) : launch_mega_impl<false>(c, num_sms, s);
+}
 
 cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s) {
   return c.mx ? launch_impl<true>(c, num_sms, s) : launch_impl<false>(c, num_sms, s);

@@ -24,20 +24,48 @@ struct Dims {
   int P_max;    // upper bound of padded rows: R + E*127, rounded up to 128
   int mt_max;   // P_max / 128
   int nblk;     // ceil(T / 32) histogram blocks
+  // macrobatches: consecutive token ranges of Tm tokens (a multiple of 128), each with its
+  // own 128-row padded expert segments; their padded row spaces are concatenated (P_cat
+  // rows) for h, U, V and O. Dispatched rows pass through a ring of S slots of P_slot rows.
+  int M;        // macrobatches
+  int Tm;       // tokens per macrobatch (the last one may hold fewer)
+  int mt_m_max; // most 128-row tiles of one macrobatch
+  int P_slot;   // rows of one ring slot (mt_m_max * 128)
+  int S;        // ring slots (1 <= S <= M)
+  int P_cat;    // concatenated padded rows of all macrobatches, bound
 };
 
-// aux buffer (persists from mok_plan to mok_moe_fwd / mok_moe_bwd)
+// aux buffer (persists from mok_plan to mok_moe_fwd / mok_moe_bwd). Per macrobatch m and
+// expert e: mstart[m][e] (table row of e's first row in m), mcount[m][e], mpoff[m][e]
+// (padded offset inside m, E+1 entries), mtile_expert[m][tile], mtiles[m], mrow0[m] (first
+// row of m in the concatenated padded space, M+1 entries).
 struct AuxLayout {
-  size_t status, poff, tile_expert, num_mtiles, total;
+  size_t status, poff, tile_expert, num_mtiles;
+  size_t mstart, mcount, mpoff, mtile_expert, mtiles, mrow0, total;
 };
 // scratch for mok_plan
 struct PlanWs {
   size_t logits, hist, lrank, total;
 };
-// scratch for the forward (xq/xsf, hq/hsf: MXFP8 operands and their scale atoms)
+// scratch for the forward (xq/xsf, hq/hsf: MXFP8 operands and their scale atoms; ring:
+// S slots of dispatched rows (bf16, or E4M3 + atoms at ring_sf); cnt: megakernel counters)
 struct FwdWs {
-  size_t xg, h, o, hs, os, xq, xsf, hq, hsf, total;
+  size_t xg, h, o, hs, os, xq, xsf, hq, hsf, ring, ring_sf, cnt, total;
 };
+// device counters of the forward megakernel (ints, zeroed before each launch)
+struct MegaCnt {
+  int gathered, hcnt, upg_done, down_done, abort_flag, total;
+};
+inline MegaCnt mega_cnt(const Dims& d) {
+  MegaCnt c;
+  c.gathered = 0;
+  c.hcnt = c.gathered + d.M * d.mt_m_max;
+  c.upg_done = c.hcnt + d.M * d.mt_m_max;
+  c.down_done = c.upg_done + d.M;
+  c.abort_flag = c.down_done + d.M;
+  c.total = c.abort_flag + 1;
+  return c;
+}
 // MXFP8 copies of the routed weights (mok_quantize_weights_mxfp8): data in the weights'
 // own layouts, atoms [e][K/128][N/128]. *_h: blocks along H; *_i: blocks along I.
 struct MxWeights {
@@ -73,13 +101,20 @@ struct AuxPtrs {
   int32_t* poff;        // [E+1] padded offsets (multiples of 128)
   int32_t* tile_expert; // [mt_max] expert of each 128-row tile of the padded row space
   int32_t* num_mtiles;  // [1]
+  int32_t* mstart;      // [M][E]
+  int32_t* mcount;      // [M][E]
+  int32_t* mpoff;       // [M][E+1]
+  int32_t* mtile_expert;// [M][mt_m_max]
+  int32_t* mtiles;      // [M]
+  int32_t* mrow0;       // [M+1]
 };
 inline AuxPtrs aux_ptrs(const Dims& d, void* aux) {
   AuxLayout L = aux_layout(d);
   char* b = static_cast<char*>(aux);
-  return AuxPtrs{reinterpret_cast<uint32_t*>(b + L.status), reinterpret_cast<int32_t*>(b + L.poff),
-                 reinterpret_cast<int32_t*>(b + L.tile_expert),
-                 reinterpret_cast<int32_t*>(b + L.num_mtiles)};
+  auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(b + off); };
+  return AuxPtrs{reinterpret_cast<uint32_t*>(b + L.status), I32(L.poff), I32(L.tile_expert),
+                 I32(L.num_mtiles), I32(L.mstart), I32(L.mcount), I32(L.mpoff),
+                 I32(L.mtile_expert), I32(L.mtiles), I32(L.mrow0)};
 }
 
 // Read-only views of a context (defined in mok_api.cu).
@@ -142,6 +177,7 @@ struct GemmCall {
   GemmMode mode;
   // problem
   int M_rows;           // rows of the row space (padded rows, or T for the dense case)
+  int a_rows;           // rows of a[0]'s buffer when it differs from M_rows (0: M_rows)
   bool dense;           // one group over M_rows rows (shared expert); else routed groups
   int H, I;             // hidden size and this FFN's intermediate size
   int groups;           // experts (dense: 1)
@@ -164,6 +200,21 @@ struct GemmCall {
   void* out_q[5]; void* out_sf[5];                     // quantised epilogue outputs + atoms
 };
 cudaError_t launch_gemm(const GemmCall& c, int num_sms, cudaStream_t s);
+
+// Forward megakernel (mok_gemm.cu): dispatch into the ring, routed up|gate and down GEMMs
+// and the combine in one cooperative launch over all SMs. up / down describe the two
+// routed GEMMs (up.a[0] = ring, up.a_rows = S * P_slot; rows of h, U, V, O = P_cat).
+struct MegaCall {
+  GemmCall up, down;
+  int M, S, P_slot, Tm, T, mt_m_max, n_comm;   // n_comm 0: default
+  const int32_t* mstart; const int32_t* mcount; const int32_t* mpoff;
+  const int32_t* mtile_expert; const int32_t* mtiles; const int32_t* mrow0;
+  const int32_t* topk_idx; const int32_t* inv;
+  const void* x; void* ring; void* ring_sf;
+  const float* O; const float* Os; float* y;
+  int* cnt;
+};
+cudaError_t launch_fwd_mega(const MegaCall& c, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- MXFP8 quantisers (mok_quant.cu)
 // src [batch][rows][cols] bf16 -> dst e4m3 (same layout) + 512-byte scale atoms; blocks of

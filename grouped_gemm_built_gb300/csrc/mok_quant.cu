@@ -17,25 +17,10 @@
 #include <cuda_runtime.h>
 
 #include "mok_internal.h"
+#include "mok_mx.cuh"
 
 namespace mok {
 
-__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
-  if (amax == 0.f) return 127u;  // all-zero block
-  const int biased = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-  const int b = biased - 8;      // floor(log2 amax) - 8, biased by 127
-  return (uint32_t)(b < 0 ? 0 : b);
-}
-// 2^(127 - byte): the factor that maps the block onto E4M3's range
-__device__ __forceinline__ float mx_inv_scale(uint32_t byte) {
-  return __uint_as_float((254u - byte) << 23);
-}
-__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
-  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-__device__ __forceinline__ size_t atom_byte(int m, int k) {
-  return (size_t)(16 * (m & 31) + 4 * ((m & 127) >> 5) + ((k & 127) >> 5));
-}
 
 // ---------------------------------------------------------------- blocks along columns
 // src [rows][cols] bf16 (batch z at src + z*batch_elems), K = the column axis.

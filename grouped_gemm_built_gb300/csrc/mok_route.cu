@@ -276,11 +276,60 @@ __global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32
   }
 }
 
+// 3b. macrobatches ([C] "Ring token buffers (macrobatch)"): macrobatch m holds tokens
+// [m*Tm, (m+1)*Tm). Inside an expert the table is in ascending token order, so m's rows of
+// expert e are one contiguous run of e's table rows; its start and length follow from the
+// scanned block histograms. Each macrobatch gets its own 128-row padded expert segments
+// and tile map; mrow0 places the macrobatches one after another.
+__global__ void __launch_bounds__(kMaxE) plan_macro_kernel(int E, int nblk, int M, int blk_m,
+                                                           int mt_m_max,
+                                                           const int32_t* __restrict__ hist,
+                                                           const int32_t* __restrict__ counts,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int32_t* mstart, int32_t* mcount,
+                                                           int32_t* mpoff, int32_t* mtile_expert,
+                                                           int32_t* mtiles, int32_t* mrow0) {
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const int e = threadIdx.x;
+  int row0 = 0;
+  for (int m = 0; m < M; ++m) {
+    int st = 0, cnt = 0;
+    if (e < E) {
+      const int b0 = m * blk_m, b1 = (m + 1) * blk_m;
+      const int before = b0 < nblk ? hist[(size_t)b0 * E + e] : counts[e];
+      const int upto = b1 < nblk ? hist[(size_t)b1 * E + e] : counts[e];
+      st = offsets[e] + before;
+      cnt = upto - before;
+    }
+    const int pcnt = (cnt + kRowPad - 1) / kRowPad * kRowPad;
+    const int po = block_exclusive_scan(pcnt, s_warp, &s_total);
+    const int P = s_total;
+    if (e < E) {
+      mstart[(size_t)m * E + e] = st;
+      mcount[(size_t)m * E + e] = cnt;
+      mpoff[(size_t)m * (E + 1) + e] = po;
+      for (int t = po / kRowPad; t < (po + pcnt) / kRowPad && t < mt_m_max; ++t)
+        mtile_expert[(size_t)m * mt_m_max + t] = e;
+    }
+    if (e == 0) {
+      mpoff[(size_t)m * (E + 1) + E] = P;
+      mtiles[m] = P / kRowPad;
+      mrow0[m] = row0;
+    }
+    row0 += P;
+  }
+  if (e == 0) mrow0[M] = row0;
+}
+
 cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int32_t* offsets,
                              const AuxPtrs& a, cudaStream_t s) {
   int threads = (d.E + 31) / 32 * 32;
   plan_scan_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, hist, counts, offsets, a.poff,
                                          a.tile_expert, a.num_mtiles);
+  plan_macro_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, d.M, d.Tm / kTokBlock, d.mt_m_max, hist,
+                                          counts, offsets, a.mstart, a.mcount, a.mpoff,
+                                          a.mtile_expert, a.mtiles, a.mrow0);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,14 @@ class MoELayer:
         except Exception:
             pass
 
+    def set_fwd_path(self, path: str):
+        """"megakernel" (default) or "launches"."""
+        codes = {"megakernel": mok.MOK_FWD_MEGAKERNEL, "launches": mok.MOK_FWD_LAUNCHES}
+        if path not in codes:
+            raise ValueError(f"forward path must be one of {sorted(codes)}, got {path!r}")
+        mok.mok_set_fwd_path(self.ctx, codes[path])
+        self.fwd_path = path
+
     def set_precision(self, precision: str):
         self.precision = precision
         codes = {"bf16": mok.MOK_BF16, "mxfp8": mok.MOK_MXFP8,

@@ -25,6 +25,8 @@ MOK_ERR_DEVICE = -6
 MOK_BF16 = 0
 MOK_MXFP8 = 1
 MOK_BF16_WGRAD_PLAIN = 2
+MOK_FWD_MEGAKERNEL = 0
+MOK_FWD_LAUNCHES = 1
 
 
 class MokDims(ctypes.Structure):
@@ -51,7 +53,7 @@ class MokGrads(ctypes.Structure):
 class MokSizes(ctypes.Structure):
     _fields_ = [("aux_bytes", c_size_t), ("workspace_bytes", c_size_t),
                 ("saved_bytes", c_size_t), ("mx_weight_bytes", c_size_t),
-                ("padded_rows_max", c_int), ("macrobatches", c_int)]
+                ("padded_rows_max", c_int), ("macrobatches", c_int), ("ring_slots", c_int)]
 
 
 class MokError(RuntimeError):
@@ -72,6 +74,7 @@ def _declare(L):
         "mok_minibatch_tokens": (c_int, [c_int, c_int, c_int, c_int]),
         "mok_status_string": (c_char_p, [c_int]),
         "mok_set_precision": (c_int, [c_void_p, c_int]),
+        "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
         "mok_plan": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, _P(MokSched), c_void_p,
                              c_void_p]),
         "mok_moe_fwd": (c_int, [c_void_p, _P(MokSched), c_void_p, _P(MokWeights), c_void_p,
@@ -152,6 +155,10 @@ def mok_get_sizes(ctx) -> MokSizes:
 
 def mok_set_precision(ctx, precision: int) -> None:
     _check(lib().mok_set_precision(ctx, int(precision)), "mok_set_precision")
+
+
+def mok_set_fwd_path(ctx, path: int) -> None:
+    _check(lib().mok_set_fwd_path(ctx, int(path)), "mok_set_fwd_path")
 
 
 def mok_plan(ctx, x, Wr, bias, sched: MokSched, workspace, stream) -> None:

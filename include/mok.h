@@ -65,6 +65,15 @@ typedef enum {
  *   choice. */
 typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1, MOK_BF16_WGRAD_PLAIN = 2 } mok_precision;
 
+/* How mok_moe_fwd runs the routed experts:
+ * MOK_FWD_MEGAKERNEL (default): one persistent cooperative launch over all SMs, split in
+ *   software into gather/combine SMs and GEMM SMs that move macrobatches through the ring
+ *   token buffer and signal each other with device counters ([C] "O que e o MoK",
+ *   "Ring token buffers (macrobatch)"; [S] "Das Scheduling").
+ * MOK_FWD_LAUNCHES: one launch per step (gather, up|gate GEMM, down GEMM, combine) over
+ *   the whole batch; macrobatches are ignored. Same arithmetic, same bits. */
+typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1 } mok_fwd_path;
+
 typedef struct mok_ctx_s* mok_ctx_t;
 
 /* Layer dimensions. T tokens, H hidden, I expert intermediate size, E routed experts,
@@ -141,6 +150,7 @@ typedef struct {
   size_t mx_weight_bytes;  /* mok_weights.mx                                    */
   int padded_rows_max;     /* upper bound of expert rows after 128-row padding  */
   int macrobatches;        /* resolved macrobatch count                         */
+  int ring_slots;          /* macrobatch slots of the ring token buffer         */
 } mok_sizes;
 
 /* ---- helpers (host only; nothing is launched) ---------------------------------- */
@@ -164,6 +174,10 @@ const char* mok_status_string(mok_status s);
  * BF16 and MXFP8 from [S] "Determinismus und MXFP8-Unterstuetzung"; [C] "Outras
  * caracteristicas"). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
+
+/* Select how later mok_moe_fwd calls run (mok_fwd_path above). Host-only state change;
+ * MOK_ERR_INVALID_ARG for other values. */
+mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path);
 
 /* Routing and schedule on the device ([S] "Das Scheduling"; [C] "Escolha da direcao").
  *   x [T][H] bf16; Wr [H][E] fp32; logit_bias [E] fp32 or NULL.

@@ -79,3 +79,45 @@ def test_calls_check_arguments_before_touching_the_device():
 def test_status_strings():
     for st in (0, -1, -2, -3, -4, -5, -6):
         assert mok.mok_status_string(st)
+
+
+def test_macrobatches_and_ring_slots():
+    """Macrobatches are ceil(T / M) tokens rounded up to 128; the ring holds as many
+    macrobatch slots (bf16 rows, whole 128-row tiles) as ring_bytes allows, at most M;
+    a ring smaller than one slot is rejected."""
+    def slot_bytes(T, H, E, k, M):
+        Tm = -(-(-(-T // M)) // 128) * 128
+        rows = min(Tm, T) * k
+        return ((rows + min(E, rows) * 127 + 127) // 128) * 128 * H * 2
+
+    d = dict(T=1000, H=256, I=128, E=6, k=8, router=0)
+    ctx = mok.mok_create(dims(**d, macrobatches=4))
+    s = mok.mok_get_sizes(ctx)
+    assert (s.macrobatches, s.ring_slots) == (4, 4)
+    mok.mok_destroy(ctx)
+    sb = slot_bytes(1000, 256, 6, 8, 4)
+    for ring, slots in ((sb, 1), (2 * sb + sb // 2, 2), (100 * sb, 4)):
+        ctx = mok.mok_create(dims(**d, macrobatches=4, ring_bytes=ring))
+        assert mok.mok_get_sizes(ctx).ring_slots == slots
+        mok.mok_destroy(ctx)
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_create(dims(**d, macrobatches=4, ring_bytes=sb - 1))
+    assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+    # 128-token granularity: 7 macrobatches of 1000 tokens become ceil(1000/7)=143 -> 256
+    # tokens each, so 4 of them
+    ctx = mok.mok_create(dims(**d, macrobatches=7))
+    assert mok.mok_get_sizes(ctx).macrobatches == 4
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(**d))
+    assert mok.mok_get_sizes(ctx).macrobatches == 1
+    mok.mok_destroy(ctx)
+
+
+def test_fwd_path_option():
+    ctx = mok.mok_create(dims())
+    mok.mok_set_fwd_path(ctx, mok.MOK_FWD_LAUNCHES)
+    mok.mok_set_fwd_path(ctx, mok.MOK_FWD_MEGAKERNEL)
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_set_fwd_path(ctx, 7)
+    assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+    mok.mok_destroy(ctx)

@@ -1,0 +1,90 @@
+"""The forward megakernel (one cooperative launch: gather/combine SMs and GEMM SMs that
+pass macrobatches through the ring token buffer) against the one-launch-per-step forward
+and against the oracle. Both paths do the same arithmetic in the same order, so their
+outputs must agree bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from grouped_gemm_built_gb300 import mok
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+ONE_MACROBATCH = {
+    "tiny": mi.CONFIGS["tiny"],
+    "ragged_shared": mi.MoEConfig("ragged_shared", T=300, H=256, I=256, E=12, k=3,
+                                  shared_I=128),
+    "sparse": mi.MoEConfig("sparse", T=64, H=128, I=128, E=64, k=1),
+    "tiny_mx": mi.MoEConfig("tiny_mx", T=256, H=256, I=256, E=8, k=2, precision="mxfp8"),
+    "ragged_shared_mx": mi.MoEConfig("ragged_shared_mx", T=300, H=256, I=256, E=12, k=3,
+                                     shared_I=128, precision="mxfp8"),
+}
+
+
+def _run(cfg, inp, path, backward):
+    L = gu.make_layer(cfg)
+    L.set_fwd_path(path)
+    res, _ = gu.run_gpu(cfg, inp, backward=backward, layer=L)
+    saved = L.saved.cpu().numpy().copy()
+    return res, saved
+
+
+@pytest.mark.parametrize("name", list(ONE_MACROBATCH))
+def test_megakernel_matches_launches_bitwise(name):
+    cfg = ONE_MACROBATCH[name]
+    inp = gu.gpu_inputs(cfg, seed=4)
+    a, sa = _run(cfg, inp, "megakernel", backward=True)
+    b, sb = _run(cfg, inp, "launches", backward=True)
+    assert a["status"] == 0 and b["status"] == 0
+    assert torch.equal(a["y"], b["y"]), "y differs between the two forward paths"
+    assert np.array_equal(sa, sb), "saved U, V differ between the two forward paths"
+    for f in ("dX", "dW_up", "dW_gate", "dW_down", "dgates"):
+        assert torch.equal(a[f], b[f]), f
+
+
+def _ring_case(precision):
+    return mi.MoEConfig(f"ring_{precision}", T=1000, H=256, I=128, E=6, k=8, router=False,
+                        zipf_s=1.2, precision=precision, backward=False, macrobatches=4)
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_ring_wraps_and_reuses_slots_bitwise(precision):
+    """Four macrobatches through a ring of two slots, of four slots, and the whole batch
+    at once: the same bits; and the oracle's forward within the tolerance."""
+    base = _ring_case(precision)
+    inp = gu.gpu_inputs(base, seed=6)
+    two = mi.scaled(base, ring_bytes=2 * _slot_bytes(base) + _slot_bytes(base) // 2)
+    outs = {}
+    for label, cfg, path, slots in (("4 slots", base, "megakernel", 4),
+                                     ("2 slots", two, "megakernel", 2),
+                                     ("launches", base, "launches", 4)):
+        L = gu.make_layer(cfg)
+        assert L.sizes.macrobatches == 4 and L.sizes.ring_slots == slots, label
+        L.set_fwd_path(path)
+        res, _ = gu.run_gpu(cfg, inp, backward=False, layer=L)
+        assert res["status"] == 0, label
+        outs[label] = res["y"]
+    assert torch.equal(outs["4 slots"], outs["2 slots"])
+    assert torch.equal(outs["4 slots"], outs["launches"])
+    idx, gates, _ = gu.oracle_route(base, inp)
+    ref = gu.run_oracle(base, inp, idx, gates, backward=False)
+    assert gu.rel_err(outs["2 slots"], ref["y"]) <= gu.TOL[precision]
+
+
+def _slot_bytes(cfg):
+    """Bytes of one ring slot: a macrobatch's padded rows (whole 128-row tiles), bf16."""
+    M = max(cfg.macrobatches, 1)
+    Tm = -(-(-(-cfg.T // M)) // 128) * 128          # ceil(T / M) rounded up to 128
+    rows = min(Tm, cfg.T) * cfg.k
+    mt = (rows + min(cfg.E, rows) * 127 + 127) // 128
+    return mt * 128 * cfg.H * 2
+
+
+def test_backward_needs_one_macrobatch():
+    cfg = mi.scaled(_ring_case("bf16"), backward=True)
+    inp = gu.gpu_inputs(cfg, seed=1)
+    with pytest.raises(mok.MokError) as ei:
+        gu.run_gpu(cfg, inp, backward=True)
+    assert ei.value.status == mok.MOK_ERR_UNSUPPORTED
