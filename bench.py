@@ -36,6 +36,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="kimi_8192")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--fwd-path", default="auto", choices=["auto", "megakernel", "launches"])
+    ap.add_argument("--comm-sms", type=int, default=0,
+                    help="gather/combine SMs of the forward megakernel (0: automatic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-experts", type=int, default=4)
@@ -189,18 +192,25 @@ def kernel_work(cfg, name, counts=None):
     T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
     R = T * k
     rows = R
-    # (FLOPs, bytes): bf16 operands (2 B), fp32 O / dXg rows and weight gradients (4 B)
+    mx = name.endswith("_mxfp8")
+    name = name[:-len("_mxfp8")] if mx else name
+    b = 1.0 + 1.0 / 32 if mx else 2.0     # bytes per operand element (MXFP8: + scales)
+    # (FLOPs, bytes): operands b bytes, U, V and fp32 O / dXg rows and gradients 4 B
     tbl = {
         "gemm_fwd_upgate_swiglu": (4.0 * H * I * rows,
-                                   2.0 * (2 * H * I * E + rows * H + 3 * rows * I)),
-        "gemm_fwd_down": (2.0 * H * I * rows, 2.0 * (H * I * E + rows * I) + 4.0 * rows * H),
+                                   b * (2 * H * I * E + rows * H + rows * I)
+                                   + 8.0 * rows * I),
+        "gemm_fwd_down": (2.0 * H * I * rows, b * (H * I * E + rows * I) + 4.0 * rows * H),
         "gemm_bwd_dh_swiglu": (2.0 * H * I * rows,
-                               2.0 * (H * I * E + rows * H + 3 * rows * I)
+                               b * (H * I * E + rows * H + 3 * rows * I)
                                + 4.0 * (2 * rows * I + rows)),
-        "gemm_bwd_dx": (4.0 * H * I * rows, 2.0 * (2 * H * I * E + 2 * rows * I) + 4.0 * rows * H),
-        "gemm_bwd_dw_down": (2.0 * H * I * rows, 2.0 * (rows * I + rows * H) + 4.0 * H * I * E),
+        "gemm_bwd_dx": (4.0 * H * I * rows, b * (2 * H * I * E + 2 * rows * I) + 4.0 * rows * H),
+        "gemm_bwd_dw_down": (2.0 * H * I * rows, b * (rows * I + rows * H) + 4.0 * H * I * E),
         "gemm_bwd_dw_upgate": (4.0 * H * I * rows,
-                               2.0 * (rows * H + 2 * rows * I) + 4.0 * 2 * H * I * E),
+                               b * (rows * H + 2 * rows * I) + 4.0 * 2 * H * I * E),
+        # the routed forward in one launch: weights once, x rows, U and V saved, y written
+        "fwd_megakernel": (6.0 * H * I * rows,
+                           b * 3 * H * I * E + 2.0 * rows * H + 8.0 * rows * I + 4.0 * T * H),
     }
     return tbl.get(name)
 
@@ -232,9 +242,15 @@ def run_gpu(args):
     L = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, shared_I=cfg.shared_I, router=cfg.router,
                  macrobatches=cfg.macrobatches, ring_bytes=cfg.ring_bytes,
                  precision=cfg.precision)
+    L.set_fwd_path(args.fwd_path)
+    mok.mok_set_comm_sms(L.ctx, args.comm_sms)
     w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
                   inp["Ws_down"])
-    grads = L.alloc_grads()
+    if cfg.precision == "mxfp8":
+        w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
+                      inp["Ws_down"], mx=L.quantize_weights(inp["W_up"], inp["W_gate"],
+                                                           inp["W_down"]))
+    grads = L.alloc_grads() if cfg.backward else None
     y = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device="cuda")
     Wr = inp["Wr"]
 
@@ -244,7 +260,8 @@ def run_gpu(args):
         else:
             L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
         L.forward(inp["x"], w, y)
-        L.backward(inp["x"], Wr if cfg.router else None, w, inp["dY"], grads)
+        if cfg.backward:
+            L.backward(inp["x"], Wr if cfg.router else None, w, inp["dY"], grads)
 
     def barrier():
         if world > 1:
@@ -272,6 +289,9 @@ def run_gpu(args):
     barrier()
     ms = e0.elapsed_time(e1)
     prof, launches = mok.mok_profile_report(L.ctx)
+    # "fwd_megakernel:<phase>" lines are phases inside the megakernel, not launches
+    phases = {n.split(":", 1)[1]: round(t / c, 4) for n, (c, t) in prof.items() if ":" in n and c}
+    prof = {n: v for n, v in prof.items() if ":" not in n}
     mok.mok_profile_enable(L.ctx, False)
     clocks = clk.stop()
     if L.status() != 0:
@@ -303,9 +323,10 @@ def run_gpu(args):
             else:
                 L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
             L.forward(dx_dev, w, y)
-            L.backward(dx_dev, Wr if cfg.router else None, w, dy_dev, grads)
             hy.copy_(y, non_blocking=True)
-            hdx.copy_(grads["dX"], non_blocking=True)
+            if cfg.backward:
+                L.backward(dx_dev, Wr if cfg.router else None, w, dy_dev, grads)
+                hdx.copy_(grads["dX"], non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -322,13 +343,13 @@ def run_gpu(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ms_e2e = float(t.item())
         e2e = {"value": world * cfg.T * k_e2e / (ms_e2e / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": hx.numel() * 2 + hdy.numel() * 2,
-               "d2h_bytes_per_step": hy.numel() * 4 + hdx.numel() * 4,
+               "h2d_bytes_per_step": hx.numel() * 2 + (hdy.numel() * 2 if cfg.backward else 0),
+               "d2h_bytes_per_step": hy.numel() * 4 + (hdx.numel() * 4 if cfg.backward else 0),
                "steps": k_e2e}
 
     # ------------------------------------------------------------ roofline
     pk = peaks()
-    gemm = {n: v for n, v in prof.items() if n.startswith("gemm_")}
+    gemm = {n: v for n, v in prof.items() if kernel_work(cfg, n) is not None}
     top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
     roofline = None
     per_kernel = {n: {"launches": c, "ms_per_launch": t / c, "share": None}
@@ -341,7 +362,11 @@ def run_gpu(args):
         flops, byts = kernel_work(cfg, name)
         dur = tms / cnt / 1e3
         ai = flops / byts
-        ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+        # an MXFP8 contraction's peak: the measured bf16 one x the nominal fp8/bf16 ratio 2
+        tpk = pk["bf16_tflops_sustained"] * (2.0 if name.endswith("_mxfp8") else 1.0)
+        tsrc = pk["source"] + (" (sustained bf16 x 2, MXFP8)" if name.endswith("_mxfp8")
+                               else " (sustained bf16)")
+        ridge = tpk * 1e12 / (pk["hbm_gbs"] * 1e9)
         if ai < ridge:
             achieved = byts / dur / 1e9
             tr = ncu_traffic(args.workload, name)
@@ -355,16 +380,18 @@ def run_gpu(args):
         else:
             achieved = flops / dur / 1e12
             roofline = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1),
-                        "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
-                        "traffic": None, "peak_source": pk["source"] + " (sustained bf16)"}
+                        "peak": round(tpk, 1), "unit": "TFLOP/s",
+                        "frac": round(achieved / tpk, 4), "traffic": None,
+                        "peak_source": tsrc}
     f_fwd, f_bwd, b_fwd, b_bwd = algorithmic(cfg)
-    t_roof = max((f_fwd + f_bwd) / (pk["bf16_tflops_sustained"] * 1e12),
-                 (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
+    if not cfg.backward:
+        f_bwd = b_bwd = 0.0
+    lpk = pk["bf16_tflops_sustained"] * (2.0 if cfg.precision == "mxfp8" else 1.0)
+    t_roof = max((f_fwd + f_bwd) / (lpk * 1e12), (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
     layer_roofline = {"ms_per_step_bound": round(t_roof * 1e3, 3),
                       "frac": round(t_roof * 1e3 / ms_step, 4),
                       "bound": "hbm" if (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9) >
-                      (f_fwd + f_bwd) / (pk["bf16_tflops_sustained"] * 1e12) else "tensor"}
+                      (f_fwd + f_bwd) / (lpk * 1e12) else "tensor"}
 
     if rank == 0:
         cpu = None
@@ -376,15 +403,18 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
             "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} "
-                                   f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} fwd+bwd",
-                       "step": "plan + forward + backward", "T": cfg.T, "H": cfg.H, "I": cfg.I,
+                                   f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} "
+                                   + ("fwd+bwd" if cfg.backward else "fwd"),
+                       "step": "plan + forward" + (" + backward" if cfg.backward else ""),
+                       "macrobatches": L.sizes.macrobatches, "ring_slots": L.sizes.ring_slots, "T": cfg.T, "H": cfg.H, "I": cfg.I,
                        "E": cfg.E, "k": cfg.k, "shared_I": cfg.shared_I,
-                       "precision": cfg.precision,
+                       "precision": cfg.precision, "fwd_path": args.fwd_path,
                        "l2": "inputs larger than L2 (expert weights 34 GB), no flush",
                        "parallelism": f"replicas x{world}"},
             "clocks": clocks, "gpu_launches": launches,
             "roofline": roofline, "layer_roofline": layer_roofline,
-            "kernels": per_kernel, "e2e": e2e, "cpu_baseline": cpu,
+            "kernels": per_kernel, "megakernel_phases_ms": phases or None,
+            "e2e": e2e, "cpu_baseline": cpu,
         }
         print(json.dumps(line))
     if world > 1:

@@ -24,7 +24,8 @@ struct mok_ctx_s {
   mok_dims dims;
   mok::Dims d;
   mok_precision precision;
-  mok_fwd_path fwd_path = MOK_FWD_MEGAKERNEL;
+  mok_fwd_path fwd_path = MOK_FWD_AUTO;
+  int comm_sms = 0;
   int device;
   int num_sms;
   // optional per-launch timing (mok_profile.h)
@@ -36,6 +37,9 @@ struct mok_ctx_s {
   std::vector<Rec> recs;
   std::vector<cudaEvent_t> pool;
   size_t pool_used = 0;
+  // megakernel phase stamps: kTraceSlots launches x num_sms CTAs x kTraceStamps
+  unsigned long long* trace = nullptr;
+  int trace_launches = 0;
   cudaEvent_t ev() {
     if (pool_used == pool.size()) {
       cudaEvent_t e;
@@ -322,7 +326,10 @@ mok_status mok_create(const mok_dims* dims, mok_ctx_t* out) {
   return MOK_OK;
 }
 
-void mok_destroy(mok_ctx_t ctx) { delete ctx; }
+void mok_destroy(mok_ctx_t ctx) {
+  if (ctx && ctx->trace) cudaFree(ctx->trace);
+  delete ctx;
+}
 
 mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
@@ -333,8 +340,15 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
 
 mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
-  if (path != MOK_FWD_MEGAKERNEL && path != MOK_FWD_LAUNCHES) return MOK_ERR_INVALID_ARG;
+  if (path != MOK_FWD_MEGAKERNEL && path != MOK_FWD_LAUNCHES && path != MOK_FWD_AUTO)
+    return MOK_ERR_INVALID_ARG;
   ctx->fwd_path = path;
+  return MOK_OK;
+}
+
+mok_status mok_set_comm_sms(mok_ctx_t ctx, int n) {
+  if (!ctx || n < 0) return MOK_ERR_INVALID_ARG;
+  ctx->comm_sms = n;
   return MOK_OK;
 }
 
@@ -452,7 +466,8 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
   void* o = W(L.o);
   const bool mx = ctx->precision == MOK_MXFP8;
 
-  if (ctx->fwd_path == MOK_FWD_MEGAKERNEL) {
+  const bool mega = ctx->fwd_path == MOK_FWD_MEGAKERNEL;
+  if (mega) {
     // shared expert first (BF16, dense launches); the megakernel's combine adds its output
     const float* os = nullptr;
     if (d.Is) {
@@ -503,6 +518,8 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       mc.down.b[0] = mxw + M.down_i;
       mc.down.sfb0 = mxw + M.down_i_sf;
     }
+    if (ctx->comm_sms >= ctx->num_sms) return MOK_ERR_INVALID_ARG;
+    mc.n_comm = ctx->comm_sms;
     mc.M = d.M;
     mc.S = d.S;
     mc.P_slot = d.P_slot;
@@ -525,6 +542,12 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     mc.y = static_cast<float*>(y);
     mc.cnt = reinterpret_cast<int*>(W(L.cnt));
     MOK_CHECK_CUDA(cudaMemsetAsync(mc.cnt, 0, sizeof(int) * (size_t)mega_cnt(d).total, s));
+    if (ctx->profile && ctx->trace) {
+      const size_t per = (size_t)ctx->num_sms * kTraceStamps;
+      mc.trace = ctx->trace + (size_t)(ctx->trace_launches % kTraceSlots) * per;
+      MOK_CHECK_CUDA(cudaMemsetAsync(mc.trace, 0, per * sizeof(unsigned long long), s));
+      ++ctx->trace_launches;
+    }
     MOK_LAUNCH(mx ? "fwd_megakernel_mxfp8" : "fwd_megakernel", launch_fwd_mega(mc, ctx->num_sms, s));
     return MOK_OK;
   }
@@ -857,8 +880,61 @@ mok_status mok_profile_enable(mok_ctx_t ctx, int enable) {
   ctx->profile = enable != 0;
   ctx->recs.clear();
   ctx->pool_used = 0;
+  ctx->trace_launches = 0;
+  if (ctx->profile && !ctx->trace && ctx->num_sms > 0) {
+    const size_t bytes = sizeof(unsigned long long) * kTraceSlots * ctx->num_sms * kTraceStamps;
+    if (cudaMalloc(&ctx->trace, bytes) != cudaSuccess) {
+      ctx->trace = nullptr;
+      return MOK_ERR_CUDA;
+    }
+  }
   return MOK_OK;
 }
+
+namespace {
+// Phase times of the recorded megakernel launches (ms, summed over launches), from the
+// per-CTA stamps: gather = last gather SM done - first start; gemm = last GEMM SM done -
+// first start; gemm_spread = last - first GEMM SM done (load imbalance); combine = last
+// end - first final-combine start; total = last end - first start.
+void megakernel_phases(mok_ctx_t ctx, std::string& out) {
+  const int n = std::min(ctx->trace_launches, kTraceSlots);
+  if (n <= 0 || !ctx->trace) return;
+  const size_t per = (size_t)ctx->num_sms * kTraceStamps;
+  std::vector<unsigned long long> h(per * n);
+  if (cudaMemcpy(h.data(), ctx->trace, h.size() * sizeof(unsigned long long),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return;
+  const char* names[5] = {"gather", "gemm", "gemm_spread", "combine", "total"};
+  double sum[5] = {0, 0, 0, 0, 0};
+  for (int l = 0; l < n; ++l) {
+    const unsigned long long* s = h.data() + per * l;
+    unsigned long long t0 = ~0ull, comm_end = 0, gemm_end = 0, gemm_first = ~0ull,
+                       comb0 = ~0ull, end = 0;
+    for (int c = 0; c < ctx->num_sms; ++c) {
+      const unsigned long long* x = s + (size_t)c * kTraceStamps;
+      if (x[kStampStart]) t0 = std::min(t0, x[kStampStart]);
+      comm_end = std::max(comm_end, x[kStampCommDone]);
+      if (x[kStampGemmDone]) {
+        gemm_end = std::max(gemm_end, x[kStampGemmDone]);
+        gemm_first = std::min(gemm_first, x[kStampGemmDone]);
+      }
+      if (x[kStampCombine]) comb0 = std::min(comb0, x[kStampCombine]);
+      end = std::max(end, x[kStampEnd]);
+    }
+    if (t0 == ~0ull || end == 0) continue;
+    sum[0] += comm_end > t0 ? (comm_end - t0) * 1e-6 : 0.0;
+    sum[1] += gemm_end > t0 ? (gemm_end - t0) * 1e-6 : 0.0;
+    sum[2] += (gemm_first != ~0ull && gemm_end > gemm_first) ? (gemm_end - gemm_first) * 1e-6 : 0.0;
+    sum[3] += (comb0 != ~0ull && end > comb0) ? (end - comb0) * 1e-6 : 0.0;
+    sum[4] += (end - t0) * 1e-6;
+  }
+  for (int i = 0; i < 5; ++i) {
+    char line[128];
+    snprintf(line, sizeof(line), "fwd_megakernel:%s %d %.6f\n", names[i], n, sum[i]);
+    out += line;
+  }
+}
+}  // namespace
 
 mok_status mok_profile_report(mok_ctx_t ctx, char* buf, size_t len, int* total_launches) {
   if (!ctx || !buf || len == 0) return MOK_ERR_INVALID_ARG;
@@ -885,6 +961,8 @@ mok_status mok_profile_report(mok_ctx_t ctx, char* buf, size_t len, int* total_l
     snprintf(line, sizeof(line), "%s %d %.6f\n", names[i].c_str(), cnt[i], ms[i]);
     out += line;
   }
+  megakernel_phases(ctx, out);
+  ctx->trace_launches = 0;
   size_t n = out.size() < len - 1 ? out.size() : len - 1;
   memcpy(buf, out.data(), n);
   buf[n] = 0;

@@ -872,6 +872,7 @@ struct MegaParams {
   float* y;             // [T][H]
   int* cnt;             // counters (MegaCnt layout), zero at launch
   uint32_t* status;
+  unsigned long long* trace;   // optional: kTraceStamps %globaltimer stamps per CTA
 };
 struct MegaMaps {
   Maps up, down;
@@ -879,7 +880,13 @@ struct MegaMaps {
 
 constexpr int kCommWarps = NUM_THREADS / 32;
 constexpr int kCopyChunk = 8192;                 // bytes per bulk copy
-constexpr int kCopyBufs = 3;                     // per warp
+// chunk buffers per warp: loads in flight = buffers - 1 (MXFP8 has less shared memory)
+template <bool MX>
+__host__ __device__ constexpr int copy_bufs() { return MX ? 3 : 4; }
+template <bool MX>
+__host__ __device__ constexpr int comm_zero_off() { return kCommWarps * copy_bufs<MX>() * kCopyChunk; }
+template <bool MX>
+__host__ __device__ constexpr int comm_src_off() { return comm_zero_off<MX>() + kCopyChunk; }   // 128 ints
 
 // Bounded wait until *c >= need (acquire). False if the deadline passed or another CTA
 // raised the abort flag.
@@ -935,36 +942,47 @@ __device__ void mega_for_each(const MegaParams& q, int g, int G, F&& f) {
   }
 }
 
-// Gather row tile r of macrobatch m into its ring slot. Each warp moves rows warp, warp+6,
-// ...: lane 0 runs a 3-buffer pipeline of bulk copies global -> shared -> global (two
-// loads ahead); MXFP8 converts each chunk in shared memory (blocks of 32 along H) and
-// writes E4M3 codes and scale bytes with ordinary stores. Padding rows are zeros.
+// Gather row tile r of macrobatch m into its ring slot. The tile's 128 source tokens are
+// looked up once (all threads) into shared memory. Each warp then moves rows warp, warp+6,
+// ...: lane 0 keeps NB - 1 bulk loads (global -> shared) in flight over NB chunk buffers;
+// the lanes copy each landed chunk to the ring (MXFP8: convert it, blocks of 32 along H,
+// to E4M3 codes and scale bytes). Padding rows are
+// zeros. Called by all threads of the CTA.
+//
+// The lanes write the ring with ordinary stores from the shared-memory chunk: bulk stores
+// would queue behind the bulk loads in flight on the SM's copy engine, leaving one load in
+// flight per warp.
 template <bool MX>
 __device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* bufs, const uint8_t* zero,
-                                 uint64_t* bars, uint32_t& phase, int* abort_g) {
+                                 int* s_src, uint64_t* bars, uint32_t& phase, int* abort_g) {
+  constexpr int NB = copy_bufs<MX>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e_raw = q.mtile_expert[(size_t)m * q.mt_m_max + r];
   const int e = (e_raw < 0 || e_raw >= q.E) ? 0 : e_raw;
-  const int po = q.mpoff[(size_t)m * (q.E + 1) + e];
-  const int cnt = q.mcount[(size_t)m * q.E + e];
-  const int st = q.mstart[(size_t)m * q.E + e];
   const int slot_row0 = (m % q.S) * q.P_slot + r * BM;   // ring row of the tile's row 0
   const uint32_t rowbytes = (uint32_t)q.H * 2;          // bf16 source row
+  __syncthreads();   // s_src of the previous tile is no longer read
+  if (threadIdx.x < BM) {
+    const int po = q.mpoff[(size_t)m * (q.E + 1) + e];
+    const int cnt = q.mcount[(size_t)m * q.E + e];
+    const int st = q.mstart[(size_t)m * q.E + e];
+    const int local = r * BM + (int)threadIdx.x - po;   // row of e inside macrobatch m
+    s_src[threadIdx.x] = (local >= 0 && local < cnt) ? q.table[2 * (size_t)(st + local)] : -1;
+  }
+  __syncthreads();
   const int nch = (int)((rowbytes + kCopyChunk - 1) / kCopyChunk);
   const int nrows = (BM - warp + kCommWarps - 1) / kCommWarps;
   const int V = nrows * nch;
-  uint8_t* mybuf = bufs + (size_t)warp * kCopyBufs * kCopyChunk;
-  uint64_t* mybar = bars + warp * kCopyBufs;
+  uint8_t* mybuf = bufs + (size_t)warp * NB * kCopyChunk;
+  uint64_t* mybar = bars + warp * NB;
   // chunk v: row i = warp + (v / nch) * 6 of the tile, bytes [c * chunk, ...) of the row
   auto src_of = [&](int v, uint32_t& off, uint32_t& bytes, int& i) -> const uint8_t* {
     i = warp + (v / nch) * kCommWarps;
     const int c = v - (v / nch) * nch;
     off = (uint32_t)c * kCopyChunk;
     bytes = min((uint32_t)kCopyChunk, rowbytes - off);
-    const int local = r * BM + i - po;                  // row of e inside macrobatch m
-    if (local < 0 || local >= cnt) return nullptr;
-    const int t = q.table[2 * (size_t)(st + local)];
-    return q.x + (size_t)t * rowbytes + off;
+    const int t = s_src[i];
+    return t < 0 ? nullptr : q.x + (size_t)t * rowbytes + off;
   };
   uint32_t pending = 0;   // buffers with a load in flight (every lane tracks the same)
   auto issue_load = [&](int v) {   // lane 0 issues; every lane records it
@@ -973,20 +991,20 @@ __device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* buf
     const uint8_t* src = src_of(v, off, bytes, i);
     if (src) {
       if (lane == 0) {
-        uint64_t* bar = mybar + v % kCopyBufs;
+        uint64_t* bar = mybar + v % NB;
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(mybuf + (v % kCopyBufs) * kCopyChunk, src, bytes, bar);
+        bulk_load(mybuf + (v % NB) * kCopyChunk, src, bytes, bar);
       }
-      pending |= 1u << (v % kCopyBufs);
+      pending |= 1u << (v % NB);
     }
   };
   bool ok = true;
-  for (int v = 0; v < min(2, V); ++v) issue_load(v);
+  for (int v = 0; v < min(NB - 1, V); ++v) issue_load(v);
   for (int v = 0; v < V; ++v) {
     uint32_t off, bytes;
     int i;
     const uint8_t* src = src_of(v, off, bytes, i);
-    const int b = v % kCopyBufs;
+    const int b = v % NB;
     uint8_t* buf = mybuf + b * kCopyChunk;
     const size_t ring_row = (size_t)slot_row0 + i;
     if (src) {   // every lane waits for the load (the MXFP8 path reads it)
@@ -1003,61 +1021,61 @@ __device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* buf
       pending &= ~(1u << b);
     }
     if (!MX) {
-      if (lane == 0) {
-        bulk_store(q.ring + ring_row * rowbytes + off, src ? buf : zero, bytes);
-        bulk_commit();
-      }
+      // the lanes store the chunk with 16-byte stores, so stores never queue behind the
+      // bulk loads in flight
+      uint4* dst = reinterpret_cast<uint4*>(q.ring + ring_row * rowbytes + off);
+      const uint4* from = reinterpret_cast<const uint4*>(src ? buf : zero);
+      for (int u = lane; u < (int)(bytes / 16); u += 32) dst[u] = from[u];
     } else {
-      // 32 lanes x (bytes / 64) blocks: block bk of this chunk covers bf16 elements
-      // [off/2 + 32 bk, +32); codes go to the E4M3 row, scales into the slot's atoms
-      const int nblk = (int)(bytes / 64);
+      // groups of 8 bf16 (16 bytes): 4 neighbouring lanes hold one block of 32 along H
+      // (conflict-free 16-byte reads; the block maximum over two shuffles). Every lane runs
+      // the same number of passes so the shuffles stay converged.
+      const int ngrp = (int)(bytes / 16);
       const size_t hrow = ring_row * (size_t)q.H;          // e4m3 row start
-      for (int bk = lane; bk < nblk; bk += 32) {
-        float f[32];
+      for (int g0 = 0; g0 < ngrp; g0 += 32) {
+        const int gi = g0 + lane;
+        const bool act = gi < ngrp;
+        float f[8];
         float amax = 0.f;
-        if (src) {
-          const uint4* sp4 = reinterpret_cast<const uint4*>(buf + bk * 64);
+        if (src && act) {
+          const uint4 w = *reinterpret_cast<const uint4*>(buf + gi * 16);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 w = sp4[u];
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-              const float2 t2 = __bfloat1622float2(h2[z]);
-              f[8 * u + 2 * z] = t2.x;
-              f[8 * u + 2 * z + 1] = t2.y;
-              amax = fmaxf(amax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
-            }
+          for (int z = 0; z < 4; ++z) {
+            const float2 t2 = __bfloat1622float2(h2[z]);
+            f[2 * z] = t2.x;
+            f[2 * z + 1] = t2.y;
+            amax = fmaxf(amax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
           }
         } else {
 #pragma unroll
-          for (int z = 0; z < 32; ++z) f[z] = 0.f;
+          for (int z = 0; z < 8; ++z) f[z] = 0.f;
         }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (!act) continue;
         const uint32_t sb = mx_scale_byte(amax);
         const float inv = mx_inv_scale(sb);
-        uint32_t wq[8];
-#pragma unroll
-        for (int z = 0; z < 8; ++z)
-          wq[z] = (uint32_t)f32x2_to_e4m3x2(f[4 * z] * inv, f[4 * z + 1] * inv) |
-                  ((uint32_t)f32x2_to_e4m3x2(f[4 * z + 2] * inv, f[4 * z + 3] * inv) << 16);
-        const int hk = (int)(off / 2) + bk * 32;            // first H index of the block
-        uint4* dq = reinterpret_cast<uint4*>(q.ring + hrow + hk);
-        dq[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-        dq[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-        const size_t atom = (ring_row >> 7) * (size_t)(q.H / 128) + (size_t)(hk >> 7);
-        q.ring_sf[atom * 512 + atom_byte((int)(ring_row & 127), hk)] = (uint8_t)sb;
+        uint2 qv;
+        qv.x = (uint32_t)f32x2_to_e4m3x2(f[0] * inv, f[1] * inv) |
+               ((uint32_t)f32x2_to_e4m3x2(f[2] * inv, f[3] * inv) << 16);
+        qv.y = (uint32_t)f32x2_to_e4m3x2(f[4] * inv, f[5] * inv) |
+               ((uint32_t)f32x2_to_e4m3x2(f[6] * inv, f[7] * inv) << 16);
+        const int hk = (int)(off / 2) + gi * 8;              // H index of the group
+        *reinterpret_cast<uint2*>(q.ring + hrow + hk) = qv;
+        if ((lane & 3) == 0) {
+          const size_t atom = (ring_row >> 7) * (size_t)(q.H / 128) + (size_t)(hk >> 7);
+          q.ring_sf[atom * 512 + atom_byte((int)(ring_row & 127), hk)] = (uint8_t)sb;
+        }
       }
-      fence_proxy_async_smem();   // these reads come before the next bulk load into buf
-      __syncwarp();
     }
-    if (v + 2 < V) {
-      if (!MX && lane == 0) bulk_wait_read<1>();   // the store from buffer (v+2) % 3 read it
-      issue_load(v + 2);
-    }
+    // every lane has consumed chunk v - 1's buffer (its values fed stores already issued),
+    // so the next bulk load may refill it
     __syncwarp();
+    if (v + NB - 1 < V) issue_load(v + NB - 1);
   }
   if (!ok) {   // let the loads still in flight land before the CTA can leave
-    for (int b = 0; b < kCopyBufs; ++b)
+    for (int b = 0; b < NB; ++b)
       if (pending & (1u << b))
         mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + kTimeoutNs);
   }
@@ -1096,26 +1114,43 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
       rows[j] = __shfl_sync(0xffffffffu, my_row, j);
       g[j] = __shfl_sync(0xffffffffu, my_g, j);
     }
-    for (int i = lane; i < nvec; i += 32) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // 4 vectors per lane per pass: with 6 warps per SM, loads in flight come from width
+    constexpr int U = 4;
+    for (int i0 = lane; i0 < nvec; i0 += 32 * U) {
+      float4 acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < q.k) {
-          const float4 f = __ldcg(O + (size_t)rows[j] * nvec + i);
-          acc.x = fmaf(g[j], f.x, acc.x);
-          acc.y = fmaf(g[j], f.y, acc.y);
-          acc.z = fmaf(g[j], f.z, acc.z);
-          acc.w = fmaf(g[j], f.w, acc.w);
+          float4 f[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + 32 * u;
+            f[u] = i < nvec ? __ldcg(O + (size_t)rows[j] * nvec + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            acc[u].x = fmaf(g[j], f[u].x, acc[u].x);
+            acc[u].y = fmaf(g[j], f[u].y, acc[u].y);
+            acc[u].z = fmaf(g[j], f[u].z, acc[u].z);
+            acc[u].w = fmaf(g[j], f[u].w, acc[u].w);
+          }
         }
       }
-      if (Os) {
-        const float4 f = __ldcg(Os + (size_t)t * nvec + i);
-        acc.x += f.x;
-        acc.y += f.y;
-        acc.z += f.z;
-        acc.w += f.w;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + 32 * u;
+        if (i >= nvec) continue;
+        if (Os) {
+          const float4 f = __ldcg(Os + (size_t)t * nvec + i);
+          acc[u].x += f.x;
+          acc[u].y += f.y;
+          acc[u].z += f.z;
+          acc[u].w += f.w;
+        }
+        y[(size_t)t * nvec + i] = acc[u];
       }
-      y[(size_t)t * nvec + i] = acc;
     }
   }
 }
@@ -1145,8 +1180,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = abort_flag + 1;
   volatile int* s_pub = abort_flag + 2;   // epilogue: the tile's outcome, read by all 4 warps
-  // gather SMs: 18 copy barriers after the GEMM barriers (those end before +128)
-  uint64_t* copy_bars = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES + 128);
+  // gather SMs: 6 x NB copy barriers in the data area, after the token indices
+  uint64_t* copy_bars = reinterpret_cast<uint64_t*>(smem + comm_src_off<MX>() + BM * 4);
   const MegaCnt CN = {0, q.M * q.mt_m_max, 2 * q.M * q.mt_m_max, 2 * q.M * q.mt_m_max + q.M,
                       2 * q.M * q.mt_m_max + 2 * q.M, 0};
   int* cnt = q.cnt;
@@ -1154,15 +1189,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool comm = (int)blockIdx.x < q.n_comm;
   const int G = (int)gridDim.x - q.n_comm;
+  unsigned long long* stamps = q.trace ? q.trace + (size_t)blockIdx.x * kTraceStamps : nullptr;
+  if (stamps && threadIdx.x == 0) stamps[kStampStart] = globaltimer_ns();
 
   if (comm) {
     // ---------------- gather / combine SM
-    uint8_t* bufs = smem;                                           // 6 warps x 3 x 8 KB
-    uint8_t* zero = smem + kCommWarps * kCopyBufs * kCopyChunk;     // 8 KB of zeros
+    uint8_t* bufs = smem;                                 // 6 warps x NB x 8 KB
+    uint8_t* zero = smem + comm_zero_off<MX>();           // 8 KB of zeros
+    int* s_src = reinterpret_cast<int*>(smem + comm_src_off<MX>());
     for (int i = threadIdx.x; i < kCopyChunk / 16; i += blockDim.x)
       reinterpret_cast<uint4*>(zero)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-      for (int i = 0; i < kCommWarps * kCopyBufs; ++i) mbar_init(&copy_bars[i], 1);
+      for (int i = 0; i < kCommWarps * copy_bufs<MX>(); ++i) mbar_init(&copy_bars[i], 1);
       fence_mbar_init();
     }
     fence_proxy_async_smem();   // the zero chunk is read by bulk stores
@@ -1176,7 +1214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             abort_g, q.status, s_ok);
       const int mt = mega_mtiles(q, m);
       for (int r = c; r < mt && ok; r += q.n_comm) {
-        ok = mega_gather_tile<MX>(q, m, r, bufs, zero, copy_bars, phase, abort_g);
+        ok = mega_gather_tile<MX>(q, m, r, bufs, zero, s_src, copy_bars, phase, abort_g);
         ok = __syncthreads_and(ok ? 1 : 0) != 0;
         if (ok && threadIdx.x == 0) red_release_add(cnt + CN.gathered + m * q.mt_m_max + r, 1);
       }
@@ -1186,6 +1224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ok) mega_combine(q, m - 1, c * kCommWarps + warp, q.n_comm * kCommWarps);
       }
     }
+    if (stamps && threadIdx.x == 0) stamps[kStampCommDone] = globaltimer_ns();
     if (!ok) return;
   } else {
     // ---------------- GEMM SM
@@ -1224,6 +1263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                   mega_tile(q, m, ph, t), it);
         });
         produce_drain<MX>(q.up, full, empty, it);
+        if (stamps) stamps[kStampProducerDone] = globaltimer_ns();
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -1269,6 +1309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return ok;
       });
       st.drain();
+      if (stamps && threadIdx.x == 64) stamps[kStampGemmDone] = globaltimer_ns();
     }
     tc_fence_before();
     __syncthreads();
@@ -1283,7 +1324,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (!cta_wait_count(cnt + CN.down_done + mlast, mega_mtiles(q, mlast) * q.down.n_tiles,
                       abort_g, q.status, s_ok))
     return;
+  if (stamps && threadIdx.x == 0) stamps[kStampCombine] = globaltimer_ns();
   mega_combine(q, mlast, (int)blockIdx.x * kCommWarps + warp, (int)gridDim.x * kCommWarps);
+  if (stamps) {
+    __syncthreads();
+    if (threadIdx.x == 0) stamps[kStampEnd] = globaltimer_ns();
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -1509,7 +1555,7 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  static_assert(kCommWarps * kCopyBufs * kCopyChunk + kCopyChunk <= C::DATA_BYTES,
+  static_assert(comm_src_off<MX>() + BM * 4 + kCommWarps * copy_bufs<MX>() * 8 <= C::DATA_BYTES,
                 "gather buffers exceed the data area");
   MegaParams q;
   MegaMaps mm;
@@ -1550,13 +1596,17 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
   q.y = c.y;
   q.cnt = c.cnt;
   q.status = c.up.status;
+  q.trace = c.trace;
   int per_sm = 0;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_mega_kernel<MX>, NUM_THREADS,
                                                          C::SMEM_BYTES)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int grid = num_sms;   // one CTA per SM, all resident (cooperative launch)
-  q.n_comm = c.n_comm > 0 ? c.n_comm : (grid >= 32 ? 8 : 1);
+  // gather SMs: they move every dispatched row and, with several macrobatches, combine
+  // (their copies are bound by memory latency: with several macrobatches, whose gathers
+  // must keep ahead of the GEMMs, one SM in five gathers and combines)
+  q.n_comm = c.n_comm > 0 ? c.n_comm : (grid < 32 ? 1 : (c.M == 1 ? 8 : grid / 5));
   if (grid - q.n_comm < 1) return cudaErrorInvalidConfiguration;
   void* args[] = {&mm, &q};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fwd_mega_kernel<MX>), grid,

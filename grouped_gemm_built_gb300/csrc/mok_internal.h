@@ -213,7 +213,13 @@ struct MegaCall {
   const void* x; void* ring; void* ring_sf;
   const float* O; const float* Os; float* y;
   int* cnt;
+  unsigned long long* trace;   // profiling: kTraceStamps stamps per CTA, or null
 };
+// megakernel phase stamps (%globaltimer ns), per CTA
+constexpr int kTraceStamps = 8;
+constexpr int kStampStart = 0, kStampCommDone = 1, kStampGemmDone = 2, kStampProducerDone = 3,
+              kStampCombine = 4, kStampEnd = 5;
+constexpr int kTraceSlots = 64;   // megakernel launches kept between two reports
 cudaError_t launch_fwd_mega(const MegaCall& c, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- MXFP8 quantisers (mok_quant.cu)

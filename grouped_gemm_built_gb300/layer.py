@@ -53,8 +53,9 @@ class MoELayer:
             pass
 
     def set_fwd_path(self, path: str):
-        """"megakernel" (default) or "launches"."""
-        codes = {"megakernel": mok.MOK_FWD_MEGAKERNEL, "launches": mok.MOK_FWD_LAUNCHES}
+        """"auto" (default), "megakernel" or "launches"."""
+        codes = {"megakernel": mok.MOK_FWD_MEGAKERNEL, "launches": mok.MOK_FWD_LAUNCHES,
+                 "auto": mok.MOK_FWD_AUTO}
         if path not in codes:
             raise ValueError(f"forward path must be one of {sorted(codes)}, got {path!r}")
         mok.mok_set_fwd_path(self.ctx, codes[path])

@@ -27,6 +27,7 @@ MOK_MXFP8 = 1
 MOK_BF16_WGRAD_PLAIN = 2
 MOK_FWD_MEGAKERNEL = 0
 MOK_FWD_LAUNCHES = 1
+MOK_FWD_AUTO = 2
 
 
 class MokDims(ctypes.Structure):
@@ -75,6 +76,7 @@ def _declare(L):
         "mok_status_string": (c_char_p, [c_int]),
         "mok_set_precision": (c_int, [c_void_p, c_int]),
         "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
+        "mok_set_comm_sms": (c_int, [c_void_p, c_int]),
         "mok_plan": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, _P(MokSched), c_void_p,
                              c_void_p]),
         "mok_moe_fwd": (c_int, [c_void_p, _P(MokSched), c_void_p, _P(MokWeights), c_void_p,
@@ -159,6 +161,10 @@ def mok_set_precision(ctx, precision: int) -> None:
 
 def mok_set_fwd_path(ctx, path: int) -> None:
     _check(lib().mok_set_fwd_path(ctx, int(path)), "mok_set_fwd_path")
+
+
+def mok_set_comm_sms(ctx, n: int) -> None:
+    _check(lib().mok_set_comm_sms(ctx, int(n)), "mok_set_comm_sms")
 
 
 def mok_plan(ctx, x, Wr, bias, sched: MokSched, workspace, stream) -> None:

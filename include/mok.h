@@ -66,13 +66,18 @@ typedef enum {
 typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1, MOK_BF16_WGRAD_PLAIN = 2 } mok_precision;
 
 /* How mok_moe_fwd runs the routed experts:
- * MOK_FWD_MEGAKERNEL (default): one persistent cooperative launch over all SMs, split in
- *   software into gather/combine SMs and GEMM SMs that move macrobatches through the ring
- *   token buffer and signal each other with device counters ([C] "O que e o MoK",
- *   "Ring token buffers (macrobatch)"; [S] "Das Scheduling").
+ * MOK_FWD_MEGAKERNEL: one persistent cooperative launch over all SMs, split in software
+ *   into gather/combine SMs and GEMM SMs that move macrobatches through the ring token
+ *   buffer and signal each other with device counters ([C] "O que e o MoK", "Ring token
+ *   buffers (macrobatch)"; [S] "Das Scheduling").
  * MOK_FWD_LAUNCHES: one launch per step (gather, up|gate GEMM, down GEMM, combine) over
- *   the whole batch; macrobatches are ignored. Same arithmetic, same bits. */
-typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1 } mok_fwd_path;
+ *   the whole batch; macrobatches are ignored. Same arithmetic, same bits.
+ * MOK_FWD_AUTO (default): one launch per step, the faster path on one GPU. There the
+ *   megakernel's gather SMs copy rows between two places of the same HBM while the GEMM
+ *   SMs already keep it busy: their copies wait on memory latency with at most a
+ *   shared-memory's worth of bytes in flight, and the SMs they take are missing from the
+ *   GEMMs. Its overlap pays where the gather side moves rows between GPUs instead. */
+typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1, MOK_FWD_AUTO = 2 } mok_fwd_path;
 
 typedef struct mok_ctx_s* mok_ctx_t;
 
@@ -178,6 +183,11 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
 /* Select how later mok_moe_fwd calls run (mok_fwd_path above). Host-only state change;
  * MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path);
+
+/* Number of the forward megakernel's SMs that gather and combine (the rest run the GEMMs):
+ * 0 = automatic, else 1 .. SMs - 1 (MOK_ERR_INVALID_ARG otherwise, checked at launch
+ * against the device's SM count). Host-only state change. */
+mok_status mok_set_comm_sms(mok_ctx_t ctx, int n);
 
 /* Routing and schedule on the device ([S] "Das Scheduling"; [C] "Escolha da direcao").
  *   x [T][H] bf16; Wr [H][E] fp32; logit_bias [E] fp32 or NULL.
