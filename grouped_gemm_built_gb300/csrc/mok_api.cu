@@ -135,6 +135,7 @@ PlanWs plan_ws(const Dims& d) {
   L.logits = b.take(sizeof(float) * (size_t)d.T * d.E);
   L.hist = b.take(sizeof(int32_t) * (size_t)d.nblk * d.E);
   L.lrank = b.take(sizeof(int32_t) * (size_t)d.R);
+  L.wr3 = d.router ? b.take(2 * 3 * (size_t)d.H * router_ld(d)) : b.off;
   L.total = b.off;
   return L;
 }
@@ -389,7 +390,27 @@ mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* 
   int32_t* hist = reinterpret_cast<int32_t*>(at(workspace, L.hist));
   int32_t* lrank = reinterpret_cast<int32_t*>(at(workspace, L.lrank));
   MOK_CHECK_CUDA(cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s));
-  if (d.router) MOK_LAUNCH("router_logits", launch_router_logits(d, x, Wr, logit_bias, logits, s));
+  if (d.router) {
+    // logits = x Wr (+ bias) on the tensor cores, Wr split exactly into three bf16 parts
+    void* wr3 = at(workspace, L.wr3);
+    MOK_LAUNCH("router_split", launch_split_wr(d, Wr, router_ld(d), wr3, s));
+    GemmCall c;
+    memset(&c, 0, sizeof(c));
+    c.mode = kRouter;
+    c.dense = true;
+    c.M_rows = d.T;
+    c.H = d.H;
+    c.I = d.H;
+    c.groups = 1;
+    c.n_out = d.E;
+    c.ld_b = router_ld(d);
+    c.bias = logit_bias;
+    c.a[0] = x;
+    c.b[0] = wr3;
+    c.out[0] = logits;
+    c.status = a.status;
+    MOK_LAUNCH("router_logits", launch_gemm(c, ctx->num_sms, s));
+  }
   MOK_LAUNCH("topk_rank", launch_topk_rank(d, d.router ? logits : nullptr, sched->topk_idx,
                                             sched->gates, hist, lrank, a.status, s));
   MOK_LAUNCH("plan_scan", launch_plan_scan(d, hist, sched->counts, sched->offsets, a, s));

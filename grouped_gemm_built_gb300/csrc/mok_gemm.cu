@@ -103,6 +103,9 @@ struct Params {
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
   int stage_bytes;  // bytes of one pipeline stage (Cfg::STAGE_BYTES or SPLIT_STAGE_BYTES)
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
+  int n_out;        // kRouter: output columns (E)
+  const float* bias;// kRouter: logit bias or null
+  float* logits;    // kRouter: [M_rows][n_out]
   int stages;       // shared-memory stages of the operand ring
   int nbuf;         // epilogue staging boxes per warp (2 or 4)
   // schedule
@@ -347,6 +350,12 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
           }
           break;
         }
+        case kRouter: {      // A: x rows (K-major, K chunk wraps per part); B: Wr parts (MN-major)
+          tma_load_2d(sa, &mp.a[0], bar, (kb % (p.H / BK)) * BK, ti.arow0);
+          for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
+            tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, k0);
+          break;
+        }
         case kBwdDH: {       // A: dYg rows (K-major); B: W_down rows i (K-major over H)
           tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
           tma_load_2d(sb, &mp.b[0], bar, k0, ti.e * p.I + ti.n0);
@@ -453,6 +462,7 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   switch (p.mode) {
     case kFwdUpGate: b_mn = true; n_mma = 256; break;
     case kFwdDown: b_mn = true; break;
+    case kRouter: b_mn = true; break;
     case kBwdDH: break;
     case kBwdDX: break;
     case kBwdDWDown: a_mn = true; b_mn = true; break;
@@ -595,6 +605,19 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
           const size_t atom = (size_t)(row / BM) * (p.I / 128) + ti.n0 / 128;
           *reinterpret_cast<uint32_t*>(p.out_sf[0] + atom * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
               sbytes;
+        }
+        break;
+      }
+      case kRouter: {  // logits fp32 (+ bias), ordinary stores of the row's valid columns
+        for (int c = 0; c < p.BN / 32; ++c) {
+          tmem_ld32(t_row + c * 32, a);
+          const int col0 = ti.n0 + c * 32;
+          if (valid) {
+            float* dst = p.logits + (size_t)row * p.n_out;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < p.n_out) dst[col0 + i] = a[i] + (p.bias ? p.bias[col0 + i] : 0.f);
+          }
         }
         break;
       }
@@ -1468,6 +1491,19 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       ok = make_map(&mp.a[0], c.a[0], c.I, rows, BM, eb) &&
            make_map(&mp.b[0], c.b[0], c.H, G * c.I, BK, eb) &&
            make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);
+      max_tiles = mt_rows * p.n_tiles;
+      break;
+    case kRouter:
+      if (MX || !c.dense) return cudaErrorNotSupported;
+      p.BN = 128;
+      p.n_out = c.n_out;
+      p.bias = c.bias;
+      p.logits = static_cast<float*>(c.out[0]);
+      p.n_tiles = (c.n_out + 127) / 128;
+      p.kiters = 3 * (c.H / BK);
+      ok = c.ld_b % 64 == 0 && c.ld_b >= c.n_out &&
+           make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
+           make_map(&mp.b[0], c.b[0], c.ld_b, 3 * (uint64_t)c.H, BK, eb);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDH:

@@ -45,8 +45,9 @@ struct AuxLayout {
 };
 // scratch for mok_plan
 struct PlanWs {
-  size_t logits, hist, lrank, total;
+  size_t logits, hist, lrank, wr3, total;
 };
+inline int router_ld(const Dims& d) { return (d.E + 63) / 64 * 64; }
 // scratch for the forward (xq/xsf, hq/hsf: MXFP8 operands and their scale atoms; ring:
 // S slots of dispatched rows (bf16, or E4M3 + atoms at ring_sf); cnt: megakernel counters)
 struct FwdWs {
@@ -122,8 +123,6 @@ const Dims* ctx_dims(mok_ctx_t ctx);
 int ctx_num_sms(mok_ctx_t ctx);
 
 // ---------------------------------------------------------------- launchers (mok_route.cu)
-cudaError_t launch_router_logits(const Dims& d, const void* x, const float* Wr, const float* bias,
-                                 float* logits, cudaStream_t s);
 cudaError_t launch_topk_rank(const Dims& d, const float* logits, int32_t* topk_idx, float* gates,
                              int32_t* hist, int32_t* lrank, uint32_t* status, cudaStream_t s);
 cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int32_t* offsets,
@@ -131,6 +130,10 @@ cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int3
 cudaError_t launch_plan_scatter(const Dims& d, const int32_t* topk_idx, const int32_t* hist,
                                 const int32_t* lrank, const int32_t* offsets, int32_t* table,
                                 int32_t* inv, cudaStream_t s);
+
+// Wr [H][E] fp32 -> three bf16 matrices stacked [3][H][ld] (columns >= E zero) with
+// Wr = hi + mid + lo exactly: hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid).
+cudaError_t launch_split_wr(const Dims& d, const float* Wr, int ld, void* out, cudaStream_t s);
 
 // ---------------------------------------------------------------- launchers (mok_move.cu)
 // Xg[p] = src[table token of padded row p] (zero rows for padding); optional per-row gate.
@@ -161,6 +164,7 @@ enum GemmMode : int {
   kBwdDX = 3,       // dXg = du W_up^T + dv W_gate^T
   kBwdDWDown = 4,   // dW_down = (g h)^T dYg
   kBwdDWUpGate = 5, // dW_up = Xg^T du, dW_gate = Xg^T dv
+  kRouter = 6,      // logits = x [Wr_hi; Wr_mid; Wr_lo] (+ bias): fp32 router on tensor cores
 };
 
 // Operands per mode (BF16; MXFP8 in brackets):
@@ -173,6 +177,8 @@ enum GemmMode : int {
 //   kBwdDWDown   a0, a1 = g*h hi, lo [a0 = g*h_q]; b0 = dYg [dY_q]; out0 = dW_down fp32
 //   kBwdDWUpGate a0 = Xg [x_q]; b0, b1 = du_hi, dv_hi; b2, b3 = du_lo, dv_lo
 //                [b0, b1 = du_q, dv_q]; out0, out1 = dW_up, dW_gate fp32
+//   kRouter      a0 = x; b0 = [Wr_hi; Wr_mid; Wr_lo] [3H][ld_b] bf16; out0 = logits [T][E]
+//                fp32 (dense, BF16 only)
 struct GemmCall {
   GemmMode mode;
   // problem
@@ -181,6 +187,9 @@ struct GemmCall {
   bool dense;           // one group over M_rows rows (shared expert); else routed groups
   int H, I;             // hidden size and this FFN's intermediate size
   int groups;           // experts (dense: 1)
+  int n_out;            // kRouter: E (output columns); the B operand has ld_b columns
+  int ld_b;             // kRouter: columns of the stacked bf16 router weights (E rounded to 64)
+  const float* bias;    // kRouter: logit bias [E] or null
   const void* a[4];     // row-space operands
   const void* b[4];     // weights / second row-space operand
   void* out[6];         // outputs (kBwdDH: du, du lo, dv, dv lo, g*h, g*h lo; lo optional)

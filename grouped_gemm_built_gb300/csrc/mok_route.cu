@@ -14,6 +14,8 @@
 //      into counts, offsets and 128-row padded offsets, and maps each 128-row tile of the
 //      padded row space to its expert;
 //   4. every slot lands at offsets[e] + (rows of e in earlier blocks) + its block rank.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,72 +23,34 @@
 
 namespace mok {
 
-// ---------------------------------------------------------------- 1a. logits (fp32 FMA)
-// CTA: 64 tokens x 128 experts; thread tile 8 tokens x 4 experts; H walked in chunks of
-// 32 in ascending order, so every logit is one fixed-order fp32 sum.
-constexpr int kLgTok = 64, kLgExp = 128, kLgK = 32;
-
-__global__ void __launch_bounds__(256) router_logits_kernel(int T, int H, int E,
-                                                            const __nv_bfloat16* __restrict__ x,
-                                                            const float* __restrict__ Wr,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits) {
-  __shared__ float xs[kLgK][kLgTok + 4];
-  __shared__ float ws[kLgK][kLgExp];
-  const int tid = threadIdx.x;
-  const int tx = tid & 31, ty = tid >> 5;
-  const int t0 = blockIdx.x * kLgTok, e0 = blockIdx.y * kLgExp;
-  float acc[8][4];
-#pragma unroll
-  for (int a = 0; a < 8; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-
-  for (int h0 = 0; h0 < H; h0 += kLgK) {
-    // x tile: 64 tokens x 32 h, stored transposed
-    for (int i = tid; i < kLgTok * kLgK; i += 256) {
-      int tt = i / kLgK, hh = i % kLgK;
-      int t = t0 + tt;
-      xs[hh][tt] = (t < T) ? __bfloat162float(x[(size_t)t * H + h0 + hh]) : 0.f;
-    }
-    for (int i = tid; i < kLgK * kLgExp; i += 256) {
-      int hh = i / kLgExp, ee = i % kLgExp;
-      int e = e0 + ee;
-      ws[hh][ee] = (e < E) ? Wr[(size_t)(h0 + hh) * E + e] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int kk = 0; kk < kLgK; ++kk) {
-      float a[8], b[4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = xs[kk][ty * 8 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx + 32 * j];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    int t = t0 + ty * 8 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int e = e0 + tx + 32 * j;
-      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
-    }
+// ---------------------------------------------------------------- 1a. logits on tensor cores
+// The logits x Wr are fp32 sums of bf16 x fp32 products. Wr splits exactly into three
+// bf16 matrices (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid): 8 + 8 + 8
+// significant bits hold fp32's 24), so x Wr = x hi + x mid + x lo with every product exact
+// in fp32; the grouped-GEMM kernel's router mode sums them on the tensor cores with fp32
+// accumulation and adds the bias in its epilogue.
+__global__ void __launch_bounds__(256) split_wr_kernel(int H, int E, int ld,
+                                                       const float* __restrict__ Wr,
+                                                       __nv_bfloat16* __restrict__ out) {
+  const size_t n = (size_t)H * ld;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int h = (int)(i / ld), e = (int)(i % ld);
+    const float w = e < E ? Wr[(size_t)h * E + e] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    out[i] = hi;
+    out[n + i] = mid;
+    out[2 * n + i] = __float2bfloat16_rn(r2);
   }
 }
 
-cudaError_t launch_router_logits(const Dims& d, const void* x, const float* Wr, const float* bias,
-                                 float* logits, cudaStream_t s) {
-  dim3 grid((d.T + kLgTok - 1) / kLgTok, (d.E + kLgExp - 1) / kLgExp);
-  router_logits_kernel<<<grid, 256, 0, s>>>(d.T, d.H, d.E,
-                                            static_cast<const __nv_bfloat16*>(x), Wr, bias,
-                                            logits);
+cudaError_t launch_split_wr(const Dims& d, const float* Wr, int ld, void* out, cudaStream_t s) {
+  const size_t n = (size_t)d.H * ld;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+  split_wr_kernel<<<blocks, 256, 0, s>>>(d.H, d.E, ld, Wr, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 

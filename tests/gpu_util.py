@@ -104,12 +104,15 @@ def run_oracle(cfg, inp, idx, gates, backward=True, precision=None):
 
 
 def logit_margins(cfg, inp, logits):
-    """Per-token bound on |fp32 logit - exact logit| for the GPU's sequential fp32 FMA
-    sum over H terms (gamma_H * sum|x_h w_h|, plus the bias add)."""
+    """Per-logit bound on |GPU logit - exact logit|. The GPU sums the 3H exact products
+    x_h * (hi, mid, lo parts of w_h) in fp32 on the tensor cores in an order of its own:
+    any order of n rounded additions errs by at most (n-1) u sum|terms|, and an accumulator
+    that truncates instead of rounding to nearest at most twice that; so
+    6 H u sum|x_h w_h|, plus the bias add."""
     x = np.abs(np64(inp["x"]))
     w = np.abs(np64(inp["Wr"]))
     u = 2.0 ** -24
-    gam = cfg.H * u / (1 - cfg.H * u)
+    gam = 6 * cfg.H * u
     return gam * (x @ w) + u * np.abs(logits) + 1e-30
 
 

@@ -36,7 +36,7 @@ def _check_route_and_plan(cfg, inp, res, orc_idx, orc_gates, logits):
         bad = [t for t in diff if t not in amb]
         assert not bad, f"top-k differs outside near-ties: tokens {bad[:10]}"
         assert len(diff) == 0, f"near-tie tokens routed differently: {diff[:10]}"
-        assert np.abs(res["gates"] - orc_gates).max() < 1e-5
+        assert np.abs(res["gates"] - orc_gates).max() < 1e-4   # tensor-core sum order
         assert np.allclose(res["gates"].sum(1), 1.0, atol=1e-5)
     pl = gu.moe.plan(orc_idx, cfg.E)
     assert np.array_equal(res["counts"], pl.counts)
@@ -145,6 +145,13 @@ def test_mxfp8_weight_quantizer_is_bit_exact():
 
 @pytest.mark.parametrize("name", list(MX_CASES))
 def test_mxfp8_layer_matches_oracle(name):
+    """MXFP8 layer against the oracle. With an in-layer router, the GPU's gates come from
+    fp32 logits and the oracle's from exact ones; in MXFP8 a gate scales du and g*h before
+    they are quantised, and E4M3 codes are 2^-3 apart, so a 1e-5 gate difference flips
+    codes near a rounding boundary that the two sides then decide differently. The router
+    run therefore checks routing, y, dX and the router gradients; the weight gradients are
+    compared in a second run that takes the oracle's routing (expert ids and fp32 gates)
+    as its input, so both sides quantise the same values."""
     cfg = MX_CASES[name]
     inp = gu.gpu_inputs(cfg, seed=0)
     idx, gates, logits = gu.oracle_route(cfg, inp)
@@ -153,13 +160,41 @@ def test_mxfp8_layer_matches_oracle(name):
     _check_route_and_plan(cfg, inp, res, idx, gates, logits)
     ref = gu.run_oracle(cfg, inp, idx, gates, backward=cfg.backward)
     fields = ["y"]
+    dw = ["dW_up", "dW_gate", "dW_down"] + (["dWs_up", "dWs_gate", "dWs_down"] if cfg.shared_I
+                                            else [])
     if cfg.backward:
-        fields += ["dX", "dW_up", "dW_gate", "dW_down", "dgates"]
-        if cfg.router:
-            fields.append("dWr")
-        if cfg.shared_I:
-            fields += ["dWs_up", "dWs_gate", "dWs_down"]
+        fields += ["dX", "dgates"] + (["dWr"] if cfg.router else dw)
     errs = {f: gu.rel_err(res[f], ref[f]) for f in fields}
+    if cfg.backward and cfg.router:
+        # weight gradients with the oracle's routing as the input
+        ext = mi.scaled(cfg, router=False)
+        g32 = gates.astype(np.float32)
+        res2, _ = gu.run_gpu(ext, inp, backward=True, routing=(idx, g32))
+        assert res2["status"] == 0
+        ref2 = gu.run_oracle(ext, inp, idx, g32.astype(np.float64), backward=True)
+        for f in ["y", "dX"] + dw:
+            errs[f + " (oracle routing)"] = gu.rel_err(res2[f], ref2[f])
     print(name, errs)
     for f, e in errs.items():
         assert e <= gu.TOL["mxfp8"], (f, e)
+
+
+@pytest.mark.parametrize("name,bias", [("mid", False), ("biased_mx", True)])
+def test_router_logits_within_fp32_bound(name, bias):
+    """The tensor-core router's logits (fp32 accumulation of exact bf16 x bf16-part
+    products) stay inside the worst-case fp32 error bound of the exact logits."""
+    cfg = CASES.get(name) or MX_CASES[name]
+    inp = gu.gpu_inputs(cfg, seed=2)
+    L = gu.make_layer(cfg)
+    d = gu.to_dev(inp)
+    L.plan(x=d["x"], Wr=d["Wr"], bias=d["bias"])
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    got = L.workspace[: cfg.T * cfg.E * 4].view(torch.float32).reshape(cfg.T, cfg.E)
+    got = got.cpu().double().numpy()
+    x, Wr = gu.np64(inp["x"]), gu.np64(inp["Wr"])
+    exact = x @ Wr + (gu.np64(inp["bias"])[None, :] if inp["bias"] is not None else 0.0)
+    bound = gu.logit_margins(cfg, inp, exact)
+    ratio = np.abs(got - exact) / bound
+    print(name, "max |err| / bound", float(ratio.max()))
+    assert float(ratio.max()) <= 1.0
