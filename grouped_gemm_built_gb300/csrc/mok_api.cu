@@ -26,6 +26,8 @@ struct mok_ctx_s {
   mok_precision precision;
   mok_fwd_path fwd_path = MOK_FWD_AUTO;
   int comm_sms = 0;
+  uint64_t wait_timeout_ns = 0;   // 0: the kernels' default (2 s)
+  int withhold = 0;               // test hook of mok_test_withhold_signal
   int device;
   int num_sms;
   // optional per-launch timing (mok_profile.h)
@@ -52,6 +54,11 @@ struct mok_ctx_s {
     for (auto e : pool) cudaEventDestroy(e);
   }
 };
+// the context's bound on device waits, applied to one GEMM call
+static mok::GemmCall timed(mok::GemmCall c, mok_ctx_t ctx) {
+  c.timeout_ns = ctx->wait_timeout_ns;
+  return c;
+}
 
 namespace {
 // Run a launcher; when profiling, bracket it with two events on the launch stream.
@@ -347,6 +354,18 @@ mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path) {
   return MOK_OK;
 }
 
+mok_status mok_set_wait_timeout(mok_ctx_t ctx, uint64_t ns) {
+  if (!ctx || ns > 60000000000ull) return MOK_ERR_INVALID_ARG;
+  ctx->wait_timeout_ns = ns;
+  return MOK_OK;
+}
+
+mok_status mok_test_withhold_signal(mok_ctx_t ctx, int on) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  ctx->withhold = on ? 1 : 0;
+  return MOK_OK;
+}
+
 mok_status mok_set_comm_sms(mok_ctx_t ctx, int n) {
   if (!ctx || n < 0) return MOK_ERR_INVALID_ARG;
   ctx->comm_sms = n;
@@ -409,7 +428,7 @@ mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* 
     c.b[0] = wr3;
     c.out[0] = logits;
     c.status = a.status;
-    MOK_LAUNCH("router_logits", launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH("router_logits", launch_gemm(timed(c, ctx), ctx->num_sms, s));
   }
   MOK_LAUNCH("topk_rank", launch_topk_rank(d, d.router ? logits : nullptr, sched->topk_idx,
                                             sched->gates, hist, lrank, a.status, s));
@@ -499,12 +518,12 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       cs.out[0] = W(L.hs);
       cs.out[1] = at(saved, S.us);
       cs.out[2] = at(saved, S.vs);
-      MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+      MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
       cs = dense_call(d, a, kFwdDown);
       cs.a[0] = W(L.hs);
       cs.b[0] = w->Ws_down;
       cs.out[0] = W(L.os);
-      MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+      MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
       os = reinterpret_cast<const float*>(W(L.os));
     }
     MegaCall mc;
@@ -541,6 +560,8 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     }
     if (ctx->comm_sms >= ctx->num_sms) return MOK_ERR_INVALID_ARG;
     mc.n_comm = ctx->comm_sms;
+    mc.up.timeout_ns = mc.down.timeout_ns = ctx->wait_timeout_ns;
+    mc.withhold = ctx->withhold;
     mc.M = d.M;
     mc.S = d.S;
     mc.P_slot = d.P_slot;
@@ -584,13 +605,13 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.out[0] = W(L.h);
     c.out[1] = at(saved, S.u);
     c.out[2] = at(saved, S.v);
-    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
     // grouped down GEMM
     c = routed_call(d, sched, a, kFwdDown);
     c.a[0] = W(L.h);
     c.b[0] = w->W_down;
     c.out[0] = o;
-    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
   } else {
     MxWeights M = mx_weights_layout(d);
     char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
@@ -609,7 +630,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.out_sf[0] = W(L.hsf);
     c.out[1] = at(saved, S.u);
     c.out[2] = at(saved, S.v);
-    MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
     c = routed_call(d, sched, a, kFwdDown);
     c.mx = true;
     c.a[0] = W(L.hq);
@@ -617,7 +638,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.b[0] = mxw + M.down_i;
     c.sfb0 = mxw + M.down_i_sf;
     c.out[0] = o;
-    MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
   }
   const void* shared_out = nullptr;
   if (d.Is) {
@@ -628,12 +649,12 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     cs.out[0] = W(L.hs);
     cs.out[1] = at(saved, S.us);
     cs.out[2] = at(saved, S.vs);
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
     cs = dense_call(d, a, kFwdDown);
     cs.a[0] = W(L.hs);
     cs.b[0] = w->Ws_down;
     cs.out[0] = W(L.os);
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
     shared_out = W(L.os);
   }
   // weighted combine in slot order
@@ -699,7 +720,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       c.out[5] = W(L.hg_lo);
     }
     c.dgp = dgp;
-    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
     // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
     c = routed_call(d, sched, a, kBwdDX);
     c.a[0] = W(L.du);
@@ -707,7 +728,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[0] = w->W_up;
     c.b[1] = w->W_gate;
     c.out[0] = dxg;
-    MOK_LAUNCH(gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
   } else {
     // reverse dispatch of dY (blocks along H for the dH GEMM, 32-row blocks for dW_down)
     // and replay of x (32-row blocks for dW_up / dW_gate), all through the table
@@ -738,7 +759,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.out_q[4] = W(L.q_hg_r);
     c.out_sf[4] = W(L.sf_hg_r);
     c.dgp = dgp;
-    MOK_LAUNCH("gemm_bwd_dh_swiglu_mxfp8", launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH("gemm_bwd_dh_swiglu_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
     c = routed_call(d, sched, a, kBwdDX);
     c.mx = true;
     c.a[0] = W(L.q_du_i);
@@ -750,7 +771,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[1] = mxw + M.gate_i;
     c.sfb1 = mxw + M.gate_i_sf;
     c.out[0] = dxg;
-    MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(c, ctx->num_sms, s));
+    MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
   }
   // router-weight gradient and the renormalised-softmax backward
   MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I), *sched, a,
@@ -770,14 +791,14 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       cs.out[3] = W(L.dvs_lo);
       cs.out[5] = W(L.hsg_lo);
     }
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDX);
     cs.a[0] = W(L.dus);
     cs.a[1] = W(L.dvs);
     cs.b[0] = w->Ws_up;
     cs.b[1] = w->Ws_gate;
     cs.out[0] = W(L.dxs);
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
     dxs = W(L.dxs);
   }
   // dX: reverse combine in slot order (+ shared expert, + router path)
@@ -807,7 +828,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   }
   c.out[0] = g->dW_up;
   c.out[1] = g->dW_gate;
-  MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
   c = routed_call(d, sched, a, kBwdDWDown);
   c.mx = mx;
   if (mx) {
@@ -824,7 +845,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
   }
   c.out[0] = g->dW_down;
-  MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(c, ctx->num_sms, s));
+  MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDWUpGate);
     cs.a[0] = x;
@@ -837,7 +858,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
     cs.out[0] = g->dWs_up;
     cs.out[1] = g->dWs_gate;
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
     cs = dense_call(d, a, kBwdDWDown);
     cs.a[0] = W(L.hsg);
     cs.b[0] = dY;
@@ -846,7 +867,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       cs.a[1] = W(L.hsg_lo);
     }
     cs.out[0] = g->dWs_down;
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(cs, ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
   }
   if (d.router) MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, dl, g->dWr, s));
   return MOK_OK;

@@ -103,6 +103,7 @@ struct Params {
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
   int stage_bytes;  // bytes of one pipeline stage (Cfg::STAGE_BYTES or SPLIT_STAGE_BYTES)
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
+  uint64_t timeout_ns;  // bound of every wait (MOK_ERR_TIMEOUT when it passes)
   int n_out;        // kRouter: output columns (E)
   const float* bias;// kRouter: logit bias or null
   float* logits;    // kRouter: [M_rows][n_out]
@@ -308,7 +309,7 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
       const uint32_t round = it / STAGES;
-      if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1, globaltimer_ns() + kTimeoutNs)) {
+      if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1, globaltimer_ns() + p.timeout_ns)) {
         set_error(p.status, kErrTimeout);
         *abort_flag = 1;
         return false;
@@ -431,9 +432,9 @@ __device__ void produce_drain(const Params& p, uint64_t* full, uint64_t* empty,
   for (uint32_t s = 0; s < (uint32_t)STAGES && s < n_armed; ++s) {
     const uint32_t last = ((n_armed - 1 - s) / STAGES) * STAGES + s;  // last use of stage s
     const uint32_t round = last / STAGES;
-    if (!mbar_wait(&empty[s], round & 1, globaltimer_ns() + kTimeoutNs)) {
+    if (!mbar_wait(&empty[s], round & 1, globaltimer_ns() + p.timeout_ns)) {
       set_error(p.status, kErrTimeout);
-      mbar_wait(&full[s], round & 1, globaltimer_ns() + kTimeoutNs);
+      mbar_wait(&full[s], round & 1, globaltimer_ns() + p.timeout_ns);
     }
   }
 }
@@ -472,7 +473,7 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   {
     const int acc = local % C::NACC;
     const uint32_t use = local / C::NACC;
-    if (use > 0 && !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + kTimeoutNs)) {
+    if (use > 0 && !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + p.timeout_ns)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
       return false;
@@ -482,7 +483,7 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
       const uint32_t round = it / STAGES;
-      if (!mbar_wait(&full[stage], round & 1, globaltimer_ns() + kTimeoutNs)) {
+      if (!mbar_wait(&full[stage], round & 1, globaltimer_ns() + p.timeout_ns)) {
         set_error(p.status, kErrTimeout);
         *abort_flag = 1;
         return false;
@@ -562,7 +563,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
   {
     const int acc = local % C::NACC;
     const uint32_t use = local / C::NACC;
-    if (!mbar_wait(&acc_full[acc], use & 1, globaltimer_ns() + kTimeoutNs)) {
+    if (!mbar_wait(&acc_full[acc], use & 1, globaltimer_ns() + p.timeout_ns)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
       return false;
@@ -896,6 +897,7 @@ struct MegaParams {
   int* cnt;             // counters (MegaCnt layout), zero at launch
   uint32_t* status;
   unsigned long long* trace;   // optional: kTraceStamps %globaltimer stamps per CTA
+  int withhold;                // test hook: never publish row tile 0 of macrobatch 0
 };
 struct MegaMaps {
   Maps up, down;
@@ -913,8 +915,9 @@ __host__ __device__ constexpr int comm_src_off() { return comm_zero_off<MX>() + 
 
 // Bounded wait until *c >= need (acquire). False if the deadline passed or another CTA
 // raised the abort flag.
-__device__ bool wait_count(const int* c, int need, int* abort_g, uint32_t* status) {
-  const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
+__device__ bool wait_count(const int* c, int need, int* abort_g, uint32_t* status,
+                           uint64_t timeout_ns) {
+  const uint64_t deadline = globaltimer_ns() + timeout_ns;
   uint32_t spins = 0;
   while (ld_acquire(c) < need) {
     if ((++spins & 63u) == 0) {
@@ -1031,7 +1034,7 @@ __device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* buf
     uint8_t* buf = mybuf + b * kCopyChunk;
     const size_t ring_row = (size_t)slot_row0 + i;
     if (src) {   // every lane waits for the load (the MXFP8 path reads it)
-      const bool got = mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + kTimeoutNs);
+      const bool got = mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + q.up.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
           set_error(q.status, kErrTimeout);
@@ -1100,7 +1103,7 @@ __device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* buf
   if (!ok) {   // let the loads still in flight land before the CTA can leave
     for (int b = 0; b < NB; ++b)
       if (pending & (1u << b))
-        mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + kTimeoutNs);
+        mbar_wait(mybar + b, (phase >> b) & 1u, globaltimer_ns() + q.up.timeout_ns);
   }
   if (lane == 0) {
     bulk_wait_all();
@@ -1180,8 +1183,8 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
 
 // All threads: thread 0 waits for *c >= need, the CTA learns the outcome.
 __device__ bool cta_wait_count(const int* c, int need, int* abort_g, uint32_t* status,
-                               volatile int* s_ok) {
-  if (threadIdx.x == 0) *s_ok = wait_count(c, need, abort_g, status) ? 1 : 0;
+                               uint64_t timeout_ns, volatile int* s_ok) {
+  if (threadIdx.x == 0) *s_ok = wait_count(c, need, abort_g, status, timeout_ns) ? 1 : 0;
   __syncthreads();
   const bool ok = *s_ok != 0;
   __syncthreads();
@@ -1234,16 +1237,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int m = 0; m < q.M && ok; ++m) {
       if (m >= q.S)   // slot m % S drains when every up|gate tile of m - S has read it
         ok = cta_wait_count(cnt + CN.upg_done + (m - q.S), mega_mtiles(q, m - q.S) * q.up.n_tiles,
-                            abort_g, q.status, s_ok);
+                            abort_g, q.status, q.up.timeout_ns, s_ok);
       const int mt = mega_mtiles(q, m);
       for (int r = c; r < mt && ok; r += q.n_comm) {
         ok = mega_gather_tile<MX>(q, m, r, bufs, zero, s_src, copy_bars, phase, abort_g);
         ok = __syncthreads_and(ok ? 1 : 0) != 0;
-        if (ok && threadIdx.x == 0) red_release_add(cnt + CN.gathered + m * q.mt_m_max + r, 1);
+        if (ok && threadIdx.x == 0 && !(q.withhold && m == 0 && r == 0))
+          red_release_add(cnt + CN.gathered + m * q.mt_m_max + r, 1);
       }
       if (ok && m >= 1) {   // combine the previous macrobatch while the GEMMs run this one
         ok = cta_wait_count(cnt + CN.down_done + (m - 1),
-                            mega_mtiles(q, m - 1) * q.down.n_tiles, abort_g, q.status, s_ok);
+                            mega_mtiles(q, m - 1) * q.down.n_tiles, abort_g, q.status, q.up.timeout_ns, s_ok);
         if (ok) mega_combine(q, m - 1, c * kCommWarps + warp, q.n_comm * kCommWarps);
       }
     }
@@ -1277,7 +1281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Params& p = ph ? q.down : q.up;
           const int r = t / p.n_tiles;
           const int* dep = cnt + (ph ? CN.hcnt : CN.gathered) + m * q.mt_m_max + r;
-          if (!wait_count(dep, ph ? q.up.n_tiles : 1, abort_g, q.status)) {
+          if (!wait_count(dep, ph ? q.up.n_tiles : 1, abort_g, q.status, q.up.timeout_ns)) {
             *abort_flag = 1;
             return false;
           }
@@ -1345,7 +1349,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // ---------------- last macrobatch: every CTA combines
   const int mlast = q.M - 1;
   if (!cta_wait_count(cnt + CN.down_done + mlast, mega_mtiles(q, mlast) * q.down.n_tiles,
-                      abort_g, q.status, s_ok))
+                      abort_g, q.status, q.up.timeout_ns, s_ok))
     return;
   if (stamps && threadIdx.x == 0) stamps[kStampCombine] = globaltimer_ns();
   mega_combine(q, mlast, (int)blockIdx.x * kCommWarps + warp, (int)gridDim.x * kCommWarps);
@@ -1426,6 +1430,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   static_assert(2 * SPLIT_STAGE_BYTES + 2 * OUT_STAGING <= Cfg<false>::DATA_BYTES,
                 "split stages and staging exceed the data area");
   p.lo_out = (!MX && c.mode == kBwdDH && c.out[1] && c.out[3] && c.out[5]) ? 1 : 0;
+  p.timeout_ns = c.timeout_ns > 0 ? c.timeout_ns : kTimeoutNs;
   // Modes without split keep the full operand ring (trading a stage for deeper output
   // staging made the dW modes slower).
   p.stages = C::STAGES;
@@ -1633,6 +1638,7 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
   q.cnt = c.cnt;
   q.status = c.up.status;
   q.trace = c.trace;
+  q.withhold = c.withhold;
   int per_sm = 0;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_mega_kernel<MX>, NUM_THREADS,
                                                          C::SMEM_BYTES)) != cudaSuccess)

@@ -202,6 +202,7 @@ struct GemmCall {
   const int32_t* tile_expert; const int32_t* num_mtiles;
   const int32_t* table; const float* gates; int k;
   uint32_t* status;
+  uint64_t timeout_ns;  // bound of every device wait (0: 2 s)
   // MXFP8 (E4M3 operands with 512-byte scale atoms; see mok_quant.cu)
   bool mx;
   const void* sfa; const void* sfa1;                   // A scale atoms (second: kBwdDX dv)
@@ -223,6 +224,7 @@ struct MegaCall {
   const float* O; const float* Os; float* y;
   int* cnt;
   unsigned long long* trace;   // profiling: kTraceStamps stamps per CTA, or null
+  int withhold;                // test hook: row tile 0 of macrobatch 0 is never published
 };
 // megakernel phase stamps (%globaltimer ns), per CTA
 constexpr int kTraceStamps = 8;

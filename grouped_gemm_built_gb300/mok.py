@@ -77,6 +77,8 @@ def _declare(L):
         "mok_set_precision": (c_int, [c_void_p, c_int]),
         "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
         "mok_set_comm_sms": (c_int, [c_void_p, c_int]),
+        "mok_set_wait_timeout": (c_int, [c_void_p, ctypes.c_uint64]),
+        "mok_test_withhold_signal": (c_int, [c_void_p, c_int]),
         "mok_plan": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, _P(MokSched), c_void_p,
                              c_void_p]),
         "mok_moe_fwd": (c_int, [c_void_p, _P(MokSched), c_void_p, _P(MokWeights), c_void_p,
@@ -165,6 +167,14 @@ def mok_set_fwd_path(ctx, path: int) -> None:
 
 def mok_set_comm_sms(ctx, n: int) -> None:
     _check(lib().mok_set_comm_sms(ctx, int(n)), "mok_set_comm_sms")
+
+
+def mok_set_wait_timeout(ctx, ns: int) -> None:
+    _check(lib().mok_set_wait_timeout(ctx, int(ns)), "mok_set_wait_timeout")
+
+
+def mok_test_withhold_signal(ctx, on: bool) -> None:
+    _check(lib().mok_test_withhold_signal(ctx, 1 if on else 0), "mok_test_withhold_signal")
 
 
 def mok_plan(ctx, x, Wr, bias, sched: MokSched, workspace, stream) -> None:

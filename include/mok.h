@@ -189,6 +189,18 @@ mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path);
  * against the device's SM count). Host-only state change. */
 mok_status mok_set_comm_sms(mok_ctx_t ctx, int n);
 
+/* Bound, in nanoseconds, of every device-side wait of later calls (pipeline barriers and
+ * the megakernel's counters); 0 = 2 s, at most 60 s. A wait that passes it records
+ * MOK_ERR_TIMEOUT in the status word (mok_get_status), the kernel lets its copies in
+ * flight land, frees its TMEM and returns; nothing traps. Host-only state change. */
+mok_status mok_set_wait_timeout(mok_ctx_t ctx, uint64_t ns);
+
+/* Test hook (no counterpart in the articles): while on, the forward megakernel never
+ * publishes the first gathered row tile, so the GEMM SMs' bounded wait for it passes its
+ * limit and the call's status reads MOK_ERR_TIMEOUT. Failure detection is tested this
+ * way, with no fault. Host-only state change. */
+mok_status mok_test_withhold_signal(mok_ctx_t ctx, int on);
+
 /* Routing and schedule on the device ([S] "Das Scheduling"; [C] "Escolha da direcao").
  *   x [T][H] bf16; Wr [H][E] fp32; logit_bias [E] fp32 or NULL.
  * With dims.router = 1, writes topk_idx and gates (softmax of x Wr + bias, top-k, gates

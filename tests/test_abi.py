@@ -121,3 +121,15 @@ def test_fwd_path_option():
         mok.mok_set_fwd_path(ctx, 7)
     assert ei.value.status == mok.MOK_ERR_INVALID_ARG
     mok.mok_destroy(ctx)
+
+
+def test_wait_timeout_and_test_hook_are_host_settings():
+    ctx = mok.mok_create(dims())
+    mok.mok_set_wait_timeout(ctx, 5_000_000)
+    mok.mok_set_wait_timeout(ctx, 0)
+    with pytest.raises(mok.MokError) as ei:
+        mok.mok_set_wait_timeout(ctx, 61_000_000_000)
+    assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+    mok.mok_test_withhold_signal(ctx, True)
+    mok.mok_test_withhold_signal(ctx, False)
+    mok.mok_destroy(ctx)

@@ -88,3 +88,37 @@ def test_backward_needs_one_macrobatch():
     with pytest.raises(mok.MokError) as ei:
         gu.run_gpu(cfg, inp, backward=True)
     assert ei.value.status == mok.MOK_ERR_UNSUPPORTED
+
+
+def test_withheld_signal_times_out_and_the_context_recovers():
+    """Failure detection without a fault: with the test hook on, the megakernel never
+    publishes one gathered row tile, so the GEMM SM waiting for it passes its bound
+    (20 ms here); the call must end with MOK_ERR_TIMEOUT in the status word, quickly and
+    with no trap, and the same context must then run correctly."""
+    import time
+    cfg = ONE_MACROBATCH["ragged_shared"]
+    inp = gu.gpu_inputs(cfg, seed=8)
+    d = gu.to_dev(inp)
+    L = gu.make_layer(cfg)
+    L.set_fwd_path("megakernel")
+    mok.mok_set_wait_timeout(L.ctx, 20_000_000)
+    L.plan(x=d["x"], Wr=d["Wr"], bias=d["bias"])
+    w = L.weights(d["W_up"], d["W_gate"], d["W_down"], d["Ws_up"], d["Ws_gate"], d["Ws_down"])
+    assert L.status() == 0
+    mok.mok_test_withhold_signal(L.ctx, True)
+    t0 = time.time()
+    L.forward(d["x"], w)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert L.status() == mok.MOK_ERR_TIMEOUT
+    assert elapsed < 5.0, elapsed
+    mok.mok_test_withhold_signal(L.ctx, False)
+    y = L.forward(d["x"], w).clone()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    L2 = gu.make_layer(cfg)
+    L2.set_fwd_path("launches")
+    L2.plan(x=d["x"], Wr=d["Wr"], bias=d["bias"])
+    y2 = L2.forward(d["x"], w)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
