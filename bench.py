@@ -61,8 +61,8 @@ def peaks():
 # A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
 NCU_TRAFFIC = {
     ("kimi_8192", "gemm_bwd_dw_upgate"): {
-        "bytes": 46.43e9, "rev": "ec029a4e93f85a30",
-        "profile": "profiles/grouped_gemm_dw_kimi_e24.md"},
+        "bytes": 46.43e9, "rev": "e8c29ce0ddf402f3",
+        "profile": "profiles/grouped_gemm_kimi_e24.md"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
