@@ -383,6 +383,17 @@ def run_gpu(args):
                         "peak": round(tpk, 1), "unit": "TFLOP/s",
                         "frac": round(achieved / tpk, 4), "traffic": None,
                         "peak_source": tsrc}
+    # every grouped GEMM's tensor throughput against its dtype's peak (the metric's
+    # "grouped-GEMM % of TC peak"; meaningful where the GEMMs are compute-bound)
+    gemm_tc = {}
+    for n, (c, t) in prof.items():
+        wk = kernel_work(cfg, n)
+        if wk is None or c == 0 or t <= 0:
+            continue
+        tf = wk[0] / (t / c / 1e3) / 1e12
+        peak_n = pk["bf16_tflops_sustained"] * (2.0 if n.endswith("_mxfp8") else 1.0)
+        gemm_tc[n] = {"tflops": round(tf, 1), "frac_of_peak": round(tf / peak_n, 4),
+                      "tb_per_s": round(wk[1] / (t / c / 1e3) / 1e12, 3)}
     f_fwd, f_bwd, b_fwd, b_bwd = algorithmic(cfg)
     if not cfg.backward:
         f_bwd = b_bwd = 0.0
@@ -413,7 +424,8 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "clocks": clocks, "gpu_launches": launches,
             "roofline": roofline, "layer_roofline": layer_roofline,
-            "kernels": per_kernel, "megakernel_phases_ms": phases or None,
+            "kernels": per_kernel, "gemm_tc": gemm_tc,
+            "megakernel_phases_ms": phases or None,
             "e2e": e2e, "cpu_baseline": cpu,
         }
         print(json.dumps(line))

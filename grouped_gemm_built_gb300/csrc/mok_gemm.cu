@@ -234,6 +234,36 @@ __device__ __forceinline__ uint32_t quant32_e4m3(const float* v, uint4* q2) {
   return sb;
 }
 
+// MXFP8 blocks of 32 rows (the warp's rows, one per lane) for this lane's 32 columns of
+// one row: per column a warp-wide maximum gives the block's scale; lane i keeps the scale
+// of column i. Writes the row's 32 codes (when valid) and this lane's scale byte.
+__device__ __forceinline__ void quant_rowblock(const float (&x)[32], int lane, bool valid,
+                                               uint8_t* codes, uint8_t* scale) {
+  uint32_t w[8];
+  uint32_t my_sb = 127u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[i])));
+    uint32_t sb = 127u;
+    if (am != 0u) {
+      const int bb = (int)((am >> 23) & 0xFF) - 8;
+      sb = (uint32_t)(bb < 0 ? 0 : bb);
+    }
+    if (i == lane) my_sb = sb;
+    const float inv = __uint_as_float((254u - sb) << 23);
+    const uint32_t code =
+        __nv_cvt_float2_to_fp8x2(make_float2(x[i] * inv, 0.f), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+    if ((i & 3) == 0) w[i >> 2] = 0;
+    w[i >> 2] |= code << (8 * (i & 3));
+  }
+  if (valid) {
+    uint4* dq = reinterpret_cast<uint4*>(codes);
+    dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  *scale = (uint8_t)my_sb;
+}
+
 // Epilogue output path: a warp stages its 32 rows x 128 bytes in shared memory (swizzled
 // like the TMA box, so the 16-byte stores of 32 lanes spread over all banks) and one lane
 // stores the box with TMA. Two buffers per warp: a buffer is refilled only after the TMA
@@ -693,61 +723,14 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
               reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[0] = q[0];
               reinterpret_cast<uint4*>(p.out_q[1] + o + c * 32)[1] = q[1];
             }
-          }
-        }
-        if (MX) {
-          // du, dv, g*h feed the dW GEMMs (K = rows): blocks of the warp's 32 rows. Every
-          // lane takes part (invalid rows are zero), so the warp reductions stay converged.
-          for (int c = 0; c < p.BN / 32; ++c) {
-            const int col = ti.n0 + c * 32;
-            const size_t o2 = (size_t)row * p.I + col;
-            float u[32], v[32];
-            tmem_ld32(t_row + c * 32, a);
-            if (valid) {
-              load_f32x32(p.u + o2, u);
-              load_f32x32(p.v + o2, v);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) u[i] = v[i] = 0.f;
-            }
+            // du, dv, g*h also feed the dW GEMMs (K = rows): blocks of the warp's 32 rows,
+            // one warp-wide maximum per column. Every lane takes part (rows outside the
+            // problem are zero), so the reductions stay converged.
             const size_t atom_r = ((size_t)(row / BM) * (p.I / 128) + col / 128) * 512 +
                                   16 * (lane & 31) + 4 * (((col & 127) + lane) >> 5) + quarter;
-            for (int out = 0; out < 3; ++out) {
-              float x[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float sg = sigmoidf_(v[i]);
-                const float sl = v[i] * sg;
-                const float dh = valid ? g * a[i] : 0.f;
-                x[i] = out == 0 ? dh * sl
-                     : out == 1 ? dh * u[i] * (sg * (1.f + v[i] * (1.f - sg)))
-                                : (valid ? g * sl * u[i] : 0.f);
-              }
-              uint32_t w[8];
-              uint32_t my_sb = 127u;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[i])));
-                uint32_t sb = 127u;
-                if (am != 0u) {
-                  const int bb = (int)((am >> 23) & 0xFF) - 8;
-                  sb = (uint32_t)(bb < 0 ? 0 : bb);
-                }
-                if (i == lane) my_sb = sb;
-                const float inv = __uint_as_float((254u - sb) << 23);
-                const uint32_t code =
-                    __nv_cvt_float2_to_fp8x2(make_float2(x[i] * inv, 0.f), __NV_SATFINITE, __NV_E4M3) &
-                    0xFFu;
-                if ((i & 3) == 0) w[i >> 2] = 0;
-                w[i >> 2] |= code << (8 * (i & 3));
-              }
-              if (valid) {
-                uint4* dq = reinterpret_cast<uint4*>(p.out_q[2 + out] + o2);
-                dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
-              }
-              p.out_sf[2 + out][atom_r] = (uint8_t)my_sb;
-            }
+            quant_rowblock(du, lane, valid, p.out_q[2] + o + c * 32, p.out_sf[2] + atom_r);
+            quant_rowblock(dv, lane, valid, p.out_q[3] + o + c * 32, p.out_sf[3] + atom_r);
+            quant_rowblock(hg, lane, valid, p.out_q[4] + o + c * 32, p.out_sf[4] + atom_r);
           }
         }
         if (valid && p.dgp) p.dgp[(size_t)row * p.n_tiles + ti.n0 / p.BN] = dg;

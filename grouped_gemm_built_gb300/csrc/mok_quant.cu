@@ -213,32 +213,50 @@ __global__ void __launch_bounds__(256) gather_quant_rows_kernel(
       s_tok[threadIdx.x] = (r < counts[e]) ? table[2 * (size_t)(offsets[e] + r)] : -1;
     }
     __syncthreads();
-    const int col = blockIdx.x * 256 + threadIdx.x;
+    // four neighbouring columns per thread: 8-byte loads, 4-byte stores
+    const int col = (blockIdx.x * 256 + threadIdx.x) * 4;
     if (col >= H) continue;
-    float f[32];
-    float amax = 0.f;
+    float f[32][4];
+    float amax[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int t = s_tok[i];
-      f[i] = (t >= 0) ? __bfloat162float(src[(size_t)t * H + col]) : 0.f;
-      amax = fmaxf(amax, fabsf(f[i]));
-    }
-    const uint32_t sb = mx_scale_byte(amax);
-    const float inv = mx_inv_scale(sb);
+      uint2 w = make_uint2(0u, 0u);
+      if (t >= 0) w = __ldg(reinterpret_cast<const uint2*>(src + (size_t)t * H + col));
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+      const float2 a01 = __bfloat1622float2(h2[0]);
+      const float2 a23 = __bfloat1622float2(h2[1]);
+      f[i][0] = a01.x;
+      f[i][1] = a01.y;
+      f[i][2] = a23.x;
+      f[i][3] = a23.y;
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      const uint16_t q = f32x2_to_e4m3x2(f[i] * inv, f[i + 1] * inv);
-      dst[(size_t)(p0 + i) * H + col] = (uint8_t)(q & 0xFF);
-      dst[(size_t)(p0 + i + 1) * H + col] = (uint8_t)(q >> 8);
+      for (int j = 0; j < 4; ++j) amax[j] = fmaxf(amax[j], fabsf(f[i][j]));
     }
-    atoms[((size_t)(p0 >> 7) * kcs + (col >> 7)) * 512 + atom_byte(col, p0)] = (uint8_t)sb;
+    uint32_t sb[4];
+    float inv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      sb[j] = mx_scale_byte(amax[j]);
+      inv[j] = mx_inv_scale(sb[j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t q = (uint32_t)f32x2_to_e4m3x2(f[i][0] * inv[0], f[i][1] * inv[1]) |
+                         ((uint32_t)f32x2_to_e4m3x2(f[i][2] * inv[2], f[i][3] * inv[3]) << 16);
+      *reinterpret_cast<uint32_t*>(dst + (size_t)(p0 + i) * H + col) = q;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      atoms[((size_t)(p0 >> 7) * kcs + ((col + j) >> 7)) * 512 + atom_byte(col + j, p0)] =
+          (uint8_t)sb[j];
   }
 }
 
 cudaError_t launch_gather_quant_rows(const Dims& d, const void* src, const mok_sched& sc,
                                      const AuxPtrs& a, void* dst, void* atoms, int num_sms,
                                      cudaStream_t s) {
-  dim3 grid((d.H + 255) / 256, num_sms * 4);
+  dim3 grid((d.H / 4 + 255) / 256, num_sms * 4);
   gather_quant_rows_kernel<<<grid, 256, 0, s>>>(
       d.H, d.E, static_cast<const __nv_bfloat16*>(src), sc.table, sc.counts, sc.offsets, a.poff,
       a.tile_expert, a.num_mtiles, d.P_max, static_cast<uint8_t*>(dst),
