@@ -26,6 +26,7 @@ struct mok_ctx_s {
   mok_precision precision;
   mok_fwd_path fwd_path = MOK_FWD_AUTO;
   int comm_sms = 0;
+  int sm_limit = 0;               // 0: every SM
   uint64_t wait_timeout_ns = 0;   // 0: the kernels' default (2 s)
   int withhold = 0;               // test hook of mok_test_withhold_signal
   int device;
@@ -54,6 +55,11 @@ struct mok_ctx_s {
     for (auto e : pool) cudaEventDestroy(e);
   }
 };
+// SMs the context's kernels may use (persistent grids are sized to it)
+static int launch_sms(mok_ctx_t ctx) {
+  return ctx->sm_limit > 0 && ctx->sm_limit < ctx->num_sms ? ctx->sm_limit : ctx->num_sms;
+}
+
 // the context's bound on device waits, applied to one GEMM call
 static mok::GemmCall timed(mok::GemmCall c, mok_ctx_t ctx) {
   c.timeout_ns = ctx->wait_timeout_ns;
@@ -366,6 +372,12 @@ mok_status mok_test_withhold_signal(mok_ctx_t ctx, int on) {
   return MOK_OK;
 }
 
+mok_status mok_set_sm_limit(mok_ctx_t ctx, int n) {
+  if (!ctx || n < 0) return MOK_ERR_INVALID_ARG;
+  ctx->sm_limit = n;
+  return MOK_OK;
+}
+
 mok_status mok_set_comm_sms(mok_ctx_t ctx, int n) {
   if (!ctx || n < 0) return MOK_ERR_INVALID_ARG;
   ctx->comm_sms = n;
@@ -428,7 +440,7 @@ mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* 
     c.b[0] = wr3;
     c.out[0] = logits;
     c.status = a.status;
-    MOK_LAUNCH("router_logits", launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH("router_logits", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   MOK_LAUNCH("topk_rank", launch_topk_rank(d, d.router ? logits : nullptr, sched->topk_idx,
                                             sched->gates, hist, lrank, a.status, s));
@@ -518,12 +530,12 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       cs.out[0] = W(L.hs);
       cs.out[1] = at(saved, S.us);
       cs.out[2] = at(saved, S.vs);
-      MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+      MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
       cs = dense_call(d, a, kFwdDown);
       cs.a[0] = W(L.hs);
       cs.b[0] = w->Ws_down;
       cs.out[0] = W(L.os);
-      MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+      MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
       os = reinterpret_cast<const float*>(W(L.os));
     }
     MegaCall mc;
@@ -558,7 +570,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       mc.down.b[0] = mxw + M.down_i;
       mc.down.sfb0 = mxw + M.down_i_sf;
     }
-    if (ctx->comm_sms >= ctx->num_sms) return MOK_ERR_INVALID_ARG;
+    if (ctx->comm_sms >= launch_sms(ctx)) return MOK_ERR_INVALID_ARG;
     mc.n_comm = ctx->comm_sms;
     mc.up.timeout_ns = mc.down.timeout_ns = ctx->wait_timeout_ns;
     mc.withhold = ctx->withhold;
@@ -590,13 +602,13 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       MOK_CHECK_CUDA(cudaMemsetAsync(mc.trace, 0, per * sizeof(unsigned long long), s));
       ++ctx->trace_launches;
     }
-    MOK_LAUNCH(mx ? "fwd_megakernel_mxfp8" : "fwd_megakernel", launch_fwd_mega(mc, ctx->num_sms, s));
+    MOK_LAUNCH(mx ? "fwd_megakernel_mxfp8" : "fwd_megakernel", launch_fwd_mega(mc, launch_sms(ctx), s));
     return MOK_OK;
   }
 
   if (!mx) {
     // dispatch: pull token rows into expert order through the table
-    MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), ctx->num_sms, s));
+    MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), launch_sms(ctx), s));
     // grouped up|gate GEMM + SwiGLU (h bf16; U, V saved in fp32)
     GemmCall c = routed_call(d, sched, a, kFwdUpGate);
     c.a[0] = W(L.xg);
@@ -605,19 +617,19 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.out[0] = W(L.h);
     c.out[1] = at(saved, S.u);
     c.out[2] = at(saved, S.v);
-    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     // grouped down GEMM
     c = routed_call(d, sched, a, kFwdDown);
     c.a[0] = W(L.h);
     c.b[0] = w->W_down;
     c.out[0] = o;
-    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   } else {
     MxWeights M = mx_weights_layout(d);
     char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
     // dispatch with MXFP8 quantisation along H fused in
     MOK_LAUNCH("dispatch_gather_mxfp8",
-               launch_gather_quant(d, x, *sched, a, W(L.xq), W(L.xsf), ctx->num_sms, s));
+               launch_gather_quant(d, x, *sched, a, W(L.xq), W(L.xsf), launch_sms(ctx), s));
     GemmCall c = routed_call(d, sched, a, kFwdUpGate);
     c.mx = true;
     c.a[0] = W(L.xq);
@@ -630,7 +642,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.out_sf[0] = W(L.hsf);
     c.out[1] = at(saved, S.u);
     c.out[2] = at(saved, S.v);
-    MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     c = routed_call(d, sched, a, kFwdDown);
     c.mx = true;
     c.a[0] = W(L.hq);
@@ -638,7 +650,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.b[0] = mxw + M.down_i;
     c.sfb0 = mxw + M.down_i_sf;
     c.out[0] = o;
-    MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   const void* shared_out = nullptr;
   if (d.Is) {
@@ -649,12 +661,12 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     cs.out[0] = W(L.hs);
     cs.out[1] = at(saved, S.us);
     cs.out[2] = at(saved, S.vs);
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kFwdDown);
     cs.a[0] = W(L.hs);
     cs.b[0] = w->Ws_down;
     cs.out[0] = W(L.os);
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     shared_out = W(L.os);
   }
   // weighted combine in slot order
@@ -703,8 +715,8 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   if (!mx) {
     // reverse dispatch of dY and replay of the forward gather, both through the table
     MOK_LAUNCH("reverse_dispatch_gather",
-               launch_gather_rows(d, dY, *sched, a, W(L.dyg), ctx->num_sms, s));
-    MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), ctx->num_sms, s));
+               launch_gather_rows(d, dY, *sched, a, W(L.dyg), launch_sms(ctx), s));
+    MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), launch_sms(ctx), s));
     // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
     GemmCall c = routed_call(d, sched, a, kBwdDH);
     c.a[0] = W(L.dyg);
@@ -720,7 +732,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       c.out[5] = W(L.hg_lo);
     }
     c.dgp = dgp;
-    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
     c = routed_call(d, sched, a, kBwdDX);
     c.a[0] = W(L.du);
@@ -728,17 +740,17 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[0] = w->W_up;
     c.b[1] = w->W_gate;
     c.out[0] = dxg;
-    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   } else {
     // reverse dispatch of dY (blocks along H for the dH GEMM, 32-row blocks for dW_down)
     // and replay of x (32-row blocks for dW_up / dW_gate), all through the table
     MOK_LAUNCH("reverse_dispatch_gather_mxfp8",
-               launch_gather_quant(d, dY, *sched, a, W(L.q_dy_h), W(L.sf_dy_h), ctx->num_sms, s));
+               launch_gather_quant(d, dY, *sched, a, W(L.q_dy_h), W(L.sf_dy_h), launch_sms(ctx), s));
     MOK_LAUNCH("reverse_dispatch_gather_rows_mxfp8",
                launch_gather_quant_rows(d, dY, *sched, a, W(L.q_dy_r), W(L.sf_dy_r),
-                                        ctx->num_sms, s));
+                                        launch_sms(ctx), s));
     MOK_LAUNCH("replay_gather_rows_mxfp8",
-               launch_gather_quant_rows(d, x, *sched, a, W(L.q_x_r), W(L.sf_x_r), ctx->num_sms,
+               launch_gather_quant_rows(d, x, *sched, a, W(L.q_x_r), W(L.sf_x_r), launch_sms(ctx),
                                         s));
     GemmCall c = routed_call(d, sched, a, kBwdDH);
     c.mx = true;
@@ -759,7 +771,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.out_q[4] = W(L.q_hg_r);
     c.out_sf[4] = W(L.sf_hg_r);
     c.dgp = dgp;
-    MOK_LAUNCH("gemm_bwd_dh_swiglu_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH("gemm_bwd_dh_swiglu_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     c = routed_call(d, sched, a, kBwdDX);
     c.mx = true;
     c.a[0] = W(L.q_du_i);
@@ -771,7 +783,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[1] = mxw + M.gate_i;
     c.sfb1 = mxw + M.gate_i_sf;
     c.out[0] = dxg;
-    MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(timed(c, ctx), ctx->num_sms, s));
+    MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   // router-weight gradient and the renormalised-softmax backward
   MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I), *sched, a,
@@ -791,14 +803,14 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       cs.out[3] = W(L.dvs_lo);
       cs.out[5] = W(L.hsg_lo);
     }
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kBwdDX);
     cs.a[0] = W(L.dus);
     cs.a[1] = W(L.dvs);
     cs.b[0] = w->Ws_up;
     cs.b[1] = w->Ws_gate;
     cs.out[0] = W(L.dxs);
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     dxs = W(L.dxs);
   }
   // dX: reverse combine in slot order (+ shared expert, + router path)
@@ -828,7 +840,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   }
   c.out[0] = g->dW_up;
   c.out[1] = g->dW_gate;
-  MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
+  MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   c = routed_call(d, sched, a, kBwdDWDown);
   c.mx = mx;
   if (mx) {
@@ -845,7 +857,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
   }
   c.out[0] = g->dW_down;
-  MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), ctx->num_sms, s));
+  MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDWUpGate);
     cs.a[0] = x;
@@ -858,7 +870,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
     cs.out[0] = g->dWs_up;
     cs.out[1] = g->dWs_gate;
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kBwdDWDown);
     cs.a[0] = W(L.hsg);
     cs.b[0] = dY;
@@ -867,7 +879,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       cs.a[1] = W(L.hsg_lo);
     }
     cs.out[0] = g->dWs_down;
-    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), ctx->num_sms, s));
+    MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
   }
   if (d.router) MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, dl, g->dWr, s));
   return MOK_OK;

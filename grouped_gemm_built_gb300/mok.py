@@ -77,6 +77,7 @@ def _declare(L):
         "mok_set_precision": (c_int, [c_void_p, c_int]),
         "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
         "mok_set_comm_sms": (c_int, [c_void_p, c_int]),
+        "mok_set_sm_limit": (c_int, [c_void_p, c_int]),
         "mok_set_wait_timeout": (c_int, [c_void_p, ctypes.c_uint64]),
         "mok_test_withhold_signal": (c_int, [c_void_p, c_int]),
         "mok_plan": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, _P(MokSched), c_void_p,
@@ -163,6 +164,10 @@ def mok_set_precision(ctx, precision: int) -> None:
 
 def mok_set_fwd_path(ctx, path: int) -> None:
     _check(lib().mok_set_fwd_path(ctx, int(path)), "mok_set_fwd_path")
+
+
+def mok_set_sm_limit(ctx, n: int) -> None:
+    _check(lib().mok_set_sm_limit(ctx, int(n)), "mok_set_sm_limit")
 
 
 def mok_set_comm_sms(ctx, n: int) -> None:

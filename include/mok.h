@@ -184,6 +184,11 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
  * MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_fwd_path(mok_ctx_t ctx, mok_fwd_path path);
 
+/* Most SMs the context's kernels use (0 = all): persistent grids are sized to it. Results
+ * do not depend on it (every sum has a fixed order), which the tests check; it also lets a
+ * caller leave SMs to other work. Host-only state change. */
+mok_status mok_set_sm_limit(mok_ctx_t ctx, int n);
+
 /* Number of the forward megakernel's SMs that gather and combine (the rest run the GEMMs):
  * 0 = automatic, else 1 .. SMs - 1 (MOK_ERR_INVALID_ARG otherwise, checked at launch
  * against the device's SM count). Host-only state change. */

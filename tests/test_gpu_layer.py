@@ -4,6 +4,7 @@ import pytest
 import torch
 
 import moe_inputs as mi
+from grouped_gemm_built_gb300 import mok
 from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
@@ -90,10 +91,15 @@ def test_plan_bit_exact_with_oracle_routing():
         assert np.array_equal(res[f], getattr(pl, f)), f
 
 
-def test_bitwise_deterministic_over_10_runs():
-    cfg = CASES["ragged_shared"]
+@pytest.mark.parametrize("name,path", [("ragged_shared", "launches"),
+                                       ("ragged_shared", "megakernel"),
+                                       ("ragged_shared_mx", "megakernel")])
+def test_bitwise_deterministic_over_10_runs(name, path):
+    cfg = CASES.get(name) or MX_CASES[name]
     inp = gu.gpu_inputs(cfg, seed=1)
-    first, L = gu.run_gpu(cfg, inp)
+    L0 = gu.make_layer(cfg)
+    L0.set_fwd_path(path)
+    first, L = gu.run_gpu(cfg, inp, layer=L0)
     for _ in range(9):
         again, _ = gu.run_gpu(cfg, inp, layer=L)
         for f in ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates", "dWr", "dWs_up"):
@@ -198,3 +204,27 @@ def test_router_logits_within_fp32_bound(name, bias):
     ratio = np.abs(got - exact) / bound
     print(name, "max |err| / bound", float(ratio.max()))
     assert float(ratio.max()) <= 1.0
+
+
+@pytest.mark.parametrize("name", ["ragged_shared", "tiny_mx"])
+def test_split_invariance(name):
+    """Every sum has a fixed order, so the results do not depend on how many SMs the
+    persistent kernels spread their tiles over: 152 (all), 37 and 5 SMs give the same bits,
+    and so does the forward megakernel with 1 or 3 gather SMs on 9 SMs."""
+    cfg = CASES.get(name) or MX_CASES[name]
+    inp = gu.gpu_inputs(cfg, seed=5)
+    fields = ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates")
+    ref = None
+    for limit, path, comm in ((0, "launches", 0), (37, "launches", 0), (5, "launches", 0),
+                              (9, "megakernel", 1), (9, "megakernel", 3)):
+        L = gu.make_layer(cfg)
+        mok.mok_set_sm_limit(L.ctx, limit)
+        L.set_fwd_path(path)
+        mok.mok_set_comm_sms(L.ctx, comm)
+        res, _ = gu.run_gpu(cfg, inp, backward=True, layer=L)
+        assert res["status"] == 0
+        if ref is None:
+            ref = res
+            continue
+        for f in fields:
+            assert torch.equal(res[f], ref[f]), (limit, path, comm, f)
