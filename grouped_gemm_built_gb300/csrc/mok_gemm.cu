@@ -141,21 +141,30 @@ struct TileInfo {
   int n0;       // first output column
   int kiters;   // K iterations
   int krow0;    // dW modes: first row of the contraction range
+  int skip;     // 1: no tile here (the unmatched half of the last row-tile pair)
 };
 
 __device__ __forceinline__ bool is_dw(int mode) { return mode == kBwdDWDown || mode == kBwdDWUpGate; }
 
+__device__ __forceinline__ int routed_mtiles(const Params& p) {
+  return min(max(*p.num_mtiles, 0), (p.M_rows + BM - 1) / BM);
+}
+
+// Routed row-space modes number their tiles in pairs of row tiles: tile 2g + r is row tile
+// 2 (g / n_tiles) + r of column block g mod n_tiles. The two row tiles of a pair usually
+// belong to one expert and read the same weight slice; with this order two neighbouring
+// CTAs take them in the same round, so the second read of the slice is an L2 hit.
 __device__ __forceinline__ int num_tiles_of(const Params& p) {
   if (is_dw(p.mode)) return p.groups * p.m_tiles_dw * p.n_tiles;
-  int mt = (p.M_rows + BM - 1) / BM;            // dense rows, or the padded-row bound
-  if (!p.dense) mt = min(max(*p.num_mtiles, 0), mt);
-  return mt * p.n_tiles;
+  if (p.dense) return ((p.M_rows + BM - 1) / BM) * p.n_tiles;
+  return ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles;
 }
 
 template <bool MX>
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
   constexpr int BK = Cfg<MX>::BK;
   TileInfo ti;
+  ti.skip = 0;
   if (is_dw(p.mode)) {
     const int per_e = p.m_tiles_dw * p.n_tiles;
     ti.e = tile / per_e;
@@ -172,10 +181,20 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
       ti.kiters = min((max(p.counts[ti.e], 0) + BK - 1) / BK, (p.poff[ti.e + 1] - ti.krow0) / BK);
     }
   } else {
-    const int mt = tile / p.n_tiles;
+    int mt, nt;
+    if (p.dense) {
+      mt = tile / p.n_tiles;
+      nt = tile - mt * p.n_tiles;
+    } else {
+      const int g = tile >> 1;
+      mt = (g / p.n_tiles) * 2 + (tile & 1);
+      nt = g % p.n_tiles;
+      ti.skip = mt >= routed_mtiles(p);
+      if (ti.skip) mt = 0;
+    }
     ti.e = p.dense ? 0 : min(max(p.tile_expert[mt], 0), p.groups - 1);
     ti.row0 = mt * BM;
-    ti.n0 = (tile - mt * p.n_tiles) * (p.mode == kFwdUpGate ? 128 : p.BN);
+    ti.n0 = nt * (p.mode == kFwdUpGate ? 128 : p.BN);
     ti.kiters = p.kiters;
     ti.krow0 = 0;
   }
@@ -474,8 +493,11 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
                         uint64_t* empty, volatile int* abort_flag) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
-    if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, tile_info<MX>(p, tile), it)) break;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const TileInfo ti = tile_info<MX>(p, tile);
+    if (ti.skip) continue;
+    if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
+  }
   produce_drain<MX>(p, full, empty, it);
 }
 
@@ -572,10 +594,13 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local)
-    if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag,
-                      tile_info<MX>(p, tile), it, local))
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const TileInfo ti = tile_info<MX>(p, tile);
+    if (ti.skip) continue;
+    if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti, it,
+                      local++))
       return;
+  }
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -777,10 +802,12 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   const int ntiles = num_tiles_of(p);
   Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
   int local = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local)
-    if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag,
-                           tile_info<MX>(p, tile), local))
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const TileInfo ti = tile_info<MX>(p, tile);
+    if (ti.skip) continue;
+    if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti, local++))
       break;
+  }
   st.drain();
 }
 
@@ -931,6 +958,7 @@ __device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph
   ti.n0 = n * (ph ? p.BN : 128);
   ti.kiters = p.kiters;
   ti.krow0 = 0;
+  ti.skip = 0;
   return ti;
 }
 
