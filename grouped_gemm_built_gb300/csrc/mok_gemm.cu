@@ -947,18 +947,24 @@ __device__ __forceinline__ int mega_mtiles(const MegaParams& q, int m) {
   return min(max(q.mtiles[m], 0), q.mt_m_max);
 }
 
+// Task t of a phase: the pair-interleaved order of the standalone routed GEMMs (row tile
+// 2 (g / n_tiles) + (t & 1), column block g mod n_tiles with g = t / 2).
+__device__ __forceinline__ int mega_row_tile(const Params& p, int t) {
+  return ((t >> 1) / p.n_tiles) * 2 + (t & 1);
+}
+
 __device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph, int t) {
   const Params& p = ph ? q.down : q.up;
-  const int r = t / p.n_tiles, n = t - r * p.n_tiles;
+  const int r = mega_row_tile(p, t), n = (t >> 1) % p.n_tiles;
   TileInfo ti;
-  const int e = q.mtile_expert[(size_t)m * q.mt_m_max + r];
+  const int e = r < q.mt_m_max ? q.mtile_expert[(size_t)m * q.mt_m_max + r] : 0;
   ti.e = (e < 0 || e >= q.E) ? 0 : e;
   ti.row0 = q.mrow0[m] + r * BM;                                   // h, U, V, O rows
   ti.arow0 = ph ? ti.row0 : (m % q.S) * q.P_slot + r * BM;        // ring slot rows
   ti.n0 = n * (ph ? p.BN : 128);
   ti.kiters = p.kiters;
   ti.krow0 = 0;
-  ti.skip = 0;
+  ti.skip = r >= mega_mtiles(q, m);
   return ti;
 }
 
@@ -969,7 +975,7 @@ __device__ void mega_for_each(const MegaParams& q, int g, int G, F&& f) {
   for (int m = 0; m < q.M; ++m) {
     const int mt = mega_mtiles(q, m);
     for (int ph = 0; ph < 2; ++ph) {
-      const int n = mt * (ph ? q.down.n_tiles : q.up.n_tiles);
+      const int n = ((mt + 1) / 2) * 2 * (ph ? q.down.n_tiles : q.up.n_tiles);
       int t = (g - base) % G;
       if (t < 0) t += G;
       for (; t < n; t += G)
@@ -1290,15 +1296,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t it = 0;
         mega_for_each(q, g, G, [&](int m, int ph, int t) {
           const Params& p = ph ? q.down : q.up;
-          const int r = t / p.n_tiles;
+          const TileInfo ti = mega_tile(q, m, ph, t);
+          if (ti.skip) return true;
+          const int r = mega_row_tile(p, t);
           const int* dep = cnt + (ph ? CN.hcnt : CN.gathered) + m * q.mt_m_max + r;
           if (!wait_count(dep, ph ? q.up.n_tiles : 1, abort_g, q.status, q.up.timeout_ns)) {
             *abort_flag = 1;
             return false;
           }
           fence_proxy_async_global();   // the TMA reads below follow the acquire
-          return produce_tile<MX>(p, ph ? mm.down : mm.up, smem, full, empty, abort_flag,
-                                  mega_tile(q, m, ph, t), it);
+          return produce_tile<MX>(p, ph ? mm.down : mm.up, smem, full, empty, abort_flag, ti, it);
         });
         produce_drain<MX>(q.up, full, empty, it);
         if (stamps) stamps[kStampProducerDone] = globaltimer_ns();
@@ -1308,8 +1315,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t it = 0;
         int local = 0;
         mega_for_each(q, g, G, [&](int m, int ph, int t) {
+          const TileInfo ti = mega_tile(q, m, ph, t);
+          if (ti.skip) return true;
           return mma_tile<MX>(ph ? q.down : q.up, smem, full, empty, acc_full, acc_empty,
-                              tmem_base, abort_flag, mega_tile(q, m, ph, t), it, local++);
+                              tmem_base, abort_flag, ti, it, local++);
         });
       }
     } else {
@@ -1317,10 +1326,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int local = 0;
       mega_for_each(q, g, G, [&](int m, int ph, int t) {
         const Params& p = ph ? q.down : q.up;
+        const TileInfo ti = mega_tile(q, m, ph, t);
+        if (ti.skip) return true;   // every epilogue warp skips the same tasks
         // a warp that timed out has raised the CTA's abort flag; every warp still meets
         // the others at the barrier below, and after it all of them see the flag
         epilogue_tile<MX>(p, ph ? mm.down : mm.up, st, acc_full, acc_empty, tmem_base,
-                          abort_flag, mega_tile(q, m, ph, t), local++);
+                          abort_flag, ti, local++);
         // publish the tile: its TMA stores have landed (and, MXFP8, the plain stores of h)
         if (lane == 0) {
           bulk_wait_all();
@@ -1332,7 +1343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int ok64 = *abort_flag == 0;
           *s_pub = ok64;
           if (ok64) {
-            const int r = t / p.n_tiles;
+            const int r = mega_row_tile(p, t);
             if (ph == 0) {
               red_release_add(cnt + CN.hcnt + m * q.mt_m_max + r, 1);
               red_release_add(cnt + CN.upg_done + m, 1);

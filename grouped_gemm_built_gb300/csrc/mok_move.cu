@@ -66,6 +66,8 @@ cudaError_t launch_gather_rows(const Dims& d, const void* src, const mok_sched& 
 // One warp per token, fp32 rows. weighted: y = sum_j g_tj O[row(t,j)] (+ add[t]);
 // otherwise the plain sum (the reverse combine of the backward), plus the router path
 // sum_j dl_tj Wr[:, e_j] when dl is given.
+constexpr int kCombineWarps = 4;   // warps per token: more loads in flight per SM
+
 __global__ void __launch_bounds__(256) combine_kernel(
     int T, int H, int E, int k, const float4* __restrict__ O, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ gates, const int32_t* __restrict__ inv,
@@ -73,7 +75,9 @@ __global__ void __launch_bounds__(256) combine_kernel(
     const float4* __restrict__ add, const float* __restrict__ dl, const float* __restrict__ WrT,
     int weighted, float4* __restrict__ y) {
   const int lane = threadIdx.x & 31;
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  // kCombineWarps warps per token, each taking every kCombineWarps-th block of 32 vectors
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int t = gw / kCombineWarps, part = gw % kCombineWarps;
   if (t >= T) return;
   const int nvec = H / 4;
   int my_row = 0, my_e = 0;
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     g[j] = __shfl_sync(0xffffffffu, my_g, j);
     dls[j] = __shfl_sync(0xffffffffu, my_dl, j);
   }
-  for (int i = lane; i < nvec; i += 32) {
+  for (int i = part * 32 + lane; i < nvec; i += 32 * kCombineWarps) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 
 cudaError_t launch_combine(const Dims& d, const void* O, const mok_sched& sc, const AuxPtrs& a,
                            const void* add, bool weighted, void* y, cudaStream_t s) {
-  int blocks = (d.T * 32 + 255) / 256;
+  int blocks = (d.T * kCombineWarps * 32 + 255) / 256;
   combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const float4*>(O),
                                         sc.topk_idx, sc.gates, sc.inv, sc.offsets, a.poff,
                                         static_cast<const float4*>(add), nullptr, nullptr,
@@ -169,7 +173,7 @@ cudaError_t launch_transpose_wr(const Dims& d, const float* Wr, float* WrT, cuda
 cudaError_t launch_reverse_combine(const Dims& d, const void* dXg, const mok_sched& sc,
                                    const AuxPtrs& a, const void* dXs, const float* dl,
                                    const float* WrT, void* dX, cudaStream_t s) {
-  int blocks = (d.T * 32 + 255) / 256;
+  int blocks = (d.T * kCombineWarps * 32 + 255) / 256;
   combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const float4*>(dXg),
                                         sc.topk_idx, sc.gates, sc.inv, sc.offsets, a.poff,
                                         static_cast<const float4*>(dXs), dl, dl ? WrT : nullptr,
