@@ -157,7 +157,6 @@ FwdWs fwd_ws(const Dims& d) {
   Bump b;
   FwdWs L;
   const size_t P = d.P_cat;
-  L.xg = b.take(2 * P * d.H);
   L.h = b.take(2 * P * d.I);
   L.o = b.take(4 * P * d.H);
   L.hs = b.take(2 * (size_t)d.T * d.Is);
@@ -198,7 +197,6 @@ BwdWs bwd_ws(const Dims& d) {
   BwdWs L;
   const size_t P = d.P_max;
   L.dyg = b.take(2 * P * d.H);
-  L.xg = b.take(2 * P * d.H);
   L.du = b.take(2 * P * d.I);   // du, dv, g*h: bf16 hi parts ...
   L.dv = b.take(2 * P * d.I);
   L.hg = b.take(2 * P * d.I);
@@ -243,6 +241,7 @@ SavedLayout saved_layout(const Dims& d) {
   L.v = b.take(4 * P * d.I);
   L.us = b.take(4 * (size_t)d.T * d.Is);
   L.vs = b.take(4 * (size_t)d.T * d.Is);
+  L.xg = b.take(2 * P * d.H);
   L.total = b.off;
   return L;
 }
@@ -545,7 +544,10 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     mc.up.M_rows = mc.down.M_rows = d.P_cat;
     mc.up.a_rows = d.S * d.P_slot;
     mc.up.mx = mc.down.mx = mx;
-    mc.up.a[0] = W(L.ring);
+    // one macrobatch, BF16: the ring's only slot is the saved gathered rows, which the
+    // backward reads again
+    void* ring = (d.M == 1 && !mx) ? at(saved, S.xg) : W(L.ring);
+    mc.up.a[0] = ring;
     mc.up.out[1] = at(saved, S.u);
     mc.up.out[2] = at(saved, S.v);
     mc.down.out[0] = o;
@@ -589,7 +591,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     mc.topk_idx = sched->topk_idx;
     mc.inv = sched->inv;
     mc.x = x;
-    mc.ring = W(L.ring);
+    mc.ring = ring;
     mc.ring_sf = W(L.ring_sf);
     mc.O = reinterpret_cast<const float*>(o);
     mc.Os = os;
@@ -608,10 +610,11 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
 
   if (!mx) {
     // dispatch: pull token rows into expert order through the table
-    MOK_LAUNCH("dispatch_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), launch_sms(ctx), s));
+    MOK_LAUNCH("dispatch_gather",
+               launch_gather_rows(d, x, *sched, a, at(saved, S.xg), launch_sms(ctx), s));
     // grouped up|gate GEMM + SwiGLU (h bf16; U, V saved in fp32)
     GemmCall c = routed_call(d, sched, a, kFwdUpGate);
-    c.a[0] = W(L.xg);
+    c.a[0] = at(saved, S.xg);
     c.b[0] = w->W_up;
     c.b[1] = w->W_gate;
     c.out[0] = W(L.h);
@@ -716,7 +719,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     // reverse dispatch of dY and replay of the forward gather, both through the table
     MOK_LAUNCH("reverse_dispatch_gather",
                launch_gather_rows(d, dY, *sched, a, W(L.dyg), launch_sms(ctx), s));
-    MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, W(L.xg), launch_sms(ctx), s));
+    // x's gathered rows come from the forward (saved), no replay
     // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
     GemmCall c = routed_call(d, sched, a, kBwdDH);
     c.a[0] = W(L.dyg);
@@ -829,7 +832,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.sfb0 = W(L.sf_du_r);
     c.sfb1 = W(L.sf_dv_r);
   } else {
-    c.a[0] = W(L.xg);
+    c.a[0] = at(const_cast<void*>(saved), S.xg);
     c.b[0] = W(L.du);
     c.b[1] = W(L.dv);
     if (hilo) {

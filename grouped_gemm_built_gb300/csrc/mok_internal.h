@@ -51,7 +51,7 @@ inline int router_ld(const Dims& d) { return (d.E + 63) / 64 * 64; }
 // scratch for the forward (xq/xsf, hq/hsf: MXFP8 operands and their scale atoms; ring:
 // S slots of dispatched rows (bf16, or E4M3 + atoms at ring_sf); cnt: megakernel counters)
 struct FwdWs {
-  size_t xg, h, o, hs, os, xq, xsf, hq, hsf, ring, ring_sf, cnt, total;
+  size_t h, o, hs, os, xq, xsf, hq, hsf, ring, ring_sf, cnt, total;
 };
 // device counters of the forward megakernel (ints, zeroed before each launch)
 struct MegaCnt {
@@ -77,15 +77,16 @@ struct MxWeights {
 // scratch for the backward. MXFP8 operands (E4M3 + atoms): dY along H (dH GEMM), dY and
 // x in 32-row blocks (dW GEMMs), du/dv along I (dX GEMM), du/dv/g*h in 32-row blocks.
 struct BwdWs {
-  size_t dyg, xg, du, dv, hg, du_lo, dv_lo, hg_lo, dxg, dgp, dl, dus, dvs, hsg, dus_lo,
+  size_t dyg, du, dv, hg, du_lo, dv_lo, hg_lo, dxg, dgp, dl, dus, dvs, hsg, dus_lo,
       dvs_lo, hsg_lo, dxs;
   size_t q_dy_h, sf_dy_h, q_dy_r, sf_dy_r, q_x_r, sf_x_r;
   size_t q_du_i, sf_du_i, q_dv_i, sf_dv_i, q_du_r, sf_du_r, q_dv_r, sf_dv_r, q_hg_r, sf_hg_r;
   size_t total;
 };
-// saved activations (forward -> backward): U, V fp32
+// saved activations (forward -> backward): U, V fp32; xg: the gathered rows of x in the
+// padded row space (BF16 forward), which the backward's weight gradients read again
 struct SavedLayout {
-  size_t u, v, us, vs, total;
+  size_t u, v, us, vs, xg, total;
 };
 
 Dims make_dims(const mok_dims& d);
