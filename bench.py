@@ -215,13 +215,6 @@ def kernel_work(cfg, name, counts=None):
     return tbl.get(name)
 
 
-def kernels_per_step(cfg):
-    n_plan = 4 if cfg.router else 3
-    n_fwd = 4 + (2 if cfg.shared_I else 0)
-    n_bwd = 9 + (4 if cfg.shared_I else 0) + (2 if cfg.router else 0)
-    return n_plan + n_fwd + n_bwd
-
-
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch

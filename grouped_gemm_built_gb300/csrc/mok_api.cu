@@ -444,6 +444,7 @@ mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* 
   MOK_LAUNCH("topk_rank", launch_topk_rank(d, d.router ? logits : nullptr, sched->topk_idx,
                                             sched->gates, hist, lrank, a.status, s));
   MOK_LAUNCH("plan_scan", launch_plan_scan(d, hist, sched->counts, sched->offsets, a, s));
+  MOK_LAUNCH("plan_macro", launch_plan_macro(d, hist, sched->counts, sched->offsets, a, s));
   MOK_LAUNCH("plan_scatter", launch_plan_scatter(d, sched->topk_idx, hist, lrank,
                                                   sched->offsets, sched->table, sched->inv, s));
   return MOK_OK;
@@ -716,7 +717,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   char* mxw = static_cast<char*>(const_cast<void*>(w->mx));
 
   if (!mx) {
-    // reverse dispatch of dY and replay of the forward gather, both through the table
+    // reverse dispatch of dY through the table
     MOK_LAUNCH("reverse_dispatch_gather",
                launch_gather_rows(d, dY, *sched, a, W(L.dyg), launch_sms(ctx), s));
     // x's gathered rows come from the forward (saved), no replay

@@ -128,6 +128,9 @@ cudaError_t launch_topk_rank(const Dims& d, const float* logits, int32_t* topk_i
                              int32_t* hist, int32_t* lrank, uint32_t* status, cudaStream_t s);
 cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int32_t* offsets,
                              const AuxPtrs& a, cudaStream_t s);
+// per-macrobatch arrays from the scanned histograms (after launch_plan_scan)
+cudaError_t launch_plan_macro(const Dims& d, const int32_t* hist, const int32_t* counts,
+                              const int32_t* offsets, const AuxPtrs& a, cudaStream_t s);
 cudaError_t launch_plan_scatter(const Dims& d, const int32_t* topk_idx, const int32_t* hist,
                                 const int32_t* lrank, const int32_t* offsets, int32_t* table,
                                 int32_t* inv, cudaStream_t s);

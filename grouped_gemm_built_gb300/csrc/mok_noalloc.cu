@@ -76,6 +76,8 @@ extern "C" mok_status mok_plan_noalloc(mok_ctx_t ctx, mok_sched* sched, void* st
     return MOK_ERR_CUDA;
   if (launch_plan_scan(d, hist, sched->counts, sched->offsets, a, s) != cudaSuccess)
     return MOK_ERR_CUDA;
+  if (launch_plan_macro(d, hist, sched->counts, sched->offsets, a, s) != cudaSuccess)
+    return MOK_ERR_CUDA;
   if (launch_plan_scatter(d, sched->topk_idx, hist, lrank, sched->offsets, sched->table,
                           sched->inv, s) != cudaSuccess)
     return MOK_ERR_CUDA;

@@ -291,6 +291,12 @@ cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int3
   int threads = (d.E + 31) / 32 * 32;
   plan_scan_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, hist, counts, offsets, a.poff,
                                          a.tile_expert, a.num_mtiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_macro(const Dims& d, const int32_t* hist, const int32_t* counts,
+                              const int32_t* offsets, const AuxPtrs& a, cudaStream_t s) {
+  int threads = (d.E + 31) / 32 * 32;
   plan_macro_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, d.M, d.Tm / kTokBlock, d.mt_m_max, hist,
                                           counts, offsets, a.mstart, a.mcount, a.mpoff,
                                           a.mtile_expert, a.mtiles, a.mrow0);
