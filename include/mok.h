@@ -85,9 +85,13 @@ typedef struct mok_ctx_s* mok_ctx_t;
  * k experts per token. H and I must be multiples of 128; 1 <= k <= 8 <= ... E <= 512;
  * shared_I (0 = no shared expert) a multiple of 128. router = 1: mok_plan routes from
  * x and Wr; router = 0: the caller supplies topk_idx and gates (an expert slice fed by
- * an external dispatcher). macrobatches (0 = auto) splits the token range into
- * consecutive chunks that pass through the ring token buffer one after another;
- * ring_bytes (0 = auto) bounds that buffer ([C] "Ring token buffers"). */
+ * an external dispatcher). macrobatches splits the token range into consecutive chunks of
+ * ceil(T / macrobatches) tokens rounded up to 128 (0 or 1: one chunk), which the forward
+ * megakernel passes through the ring token buffer one after another; ring_bytes bounds
+ * that buffer: it holds ring_bytes / (one macrobatch's padded rows of bf16) slots, at
+ * most one per macrobatch (0: one per macrobatch); fewer than one slot is
+ * MOK_ERR_INVALID_ARG ([C] "Ring token buffers"). mok_get_sizes reports the resolved
+ * counts. The backward needs one macrobatch. */
 typedef struct {
   int T, H, I, E, k;
   int shared_I;
