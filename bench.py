@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--fwd-path", default="auto", choices=["auto", "megakernel", "launches"])
     ap.add_argument("--comm-sms", type=int, default=0,
                     help="gather/combine SMs of the forward megakernel (0: automatic)")
+    ap.add_argument("--sm-limit", type=int, default=0,
+                    help="most SMs any kernel uses (0: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-experts", type=int, default=4)
@@ -237,6 +239,7 @@ def run_gpu(args):
                  precision=cfg.precision)
     L.set_fwd_path(args.fwd_path)
     mok.mok_set_comm_sms(L.ctx, args.comm_sms)
+    mok.mok_set_sm_limit(L.ctx, args.sm_limit)
     w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
                   inp["Ws_down"])
     if cfg.precision == "mxfp8":
