@@ -63,8 +63,8 @@ def peaks():
 # A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
 NCU_TRAFFIC = {
     ("kimi_8192", "gemm_bwd_dw_upgate"): {
-        "bytes": 46.43e9, "rev": "e8c29ce0ddf402f3",
-        "profile": "profiles/grouped_gemm_kimi_e24.md"},
+        "bytes": 47.355e9, "rev": "c5e644c038dd566a",
+        "profile": "profiles/dram_traffic_kimi8192_bf16.md"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
