@@ -204,7 +204,7 @@ BwdWs bwd_ws(const Dims& d) {
   L.dv_lo = b.take(2 * P * d.I);
   L.hg_lo = b.take(2 * P * d.I);
   L.dxg = b.take(4 * P * d.H);
-  L.dgp = b.take(sizeof(float) * P * gemm_dh_parts(d.I));
+  L.dgp = b.take(sizeof(float) * P * gemm_dh_parts(d.I, true));   // the larger count
   L.dl = b.take(sizeof(float) * (size_t)d.R);
   L.dus = b.take(2 * (size_t)d.T * d.Is);
   L.dvs = b.take(2 * (size_t)d.T * d.Is);
@@ -790,7 +790,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   // router-weight gradient and the renormalised-softmax backward
-  MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I), *sched, a,
+  MOK_LAUNCH("router_grad", launch_router_grad(d, dgp, gemm_dh_parts(d.I, mx), *sched, a,
                                               g->dgates, d.router ? dl : nullptr, s));
   const void* dxs = nullptr;
   if (d.Is) {

@@ -70,7 +70,7 @@ struct Cfg {
   static constexpr int MN_KSTEP = MMA_K * 128;       // bytes per instruction along K, MN-major
   static constexpr int SF_OFF = A_BYTES + B_BYTES;   // scale atoms: A 512 B, B 1024 B
   static constexpr int STAGE_BYTES = MX ? 51200 : 49152;
-  static constexpr int NACC = MX ? 1 : 2;
+  static constexpr int NACC = MX ? 1 : 2;             // accumulators of ACC_COLS columns
   static constexpr int ACC_COLS = 256;
   static constexpr int SF_TMEM = 256;                // MX: scale columns start here
   // data area: the larger of (STAGES stages + 2 staging boxes per warp) and
@@ -109,6 +109,8 @@ struct Params {
   float* logits;    // kRouter: [M_rows][n_out]
   int stages;       // shared-memory stages of the operand ring
   int nbuf;         // epilogue staging boxes per warp (2 or 4)
+  int nacc;         // TMEM accumulators (Cfg::NACC; MXFP8 dH: 2 of 128 columns)
+  int acc_cols;     // columns of one accumulator
   // schedule
   const int32_t* poff;
   const int32_t* counts;
@@ -523,15 +525,15 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   }
   const uint32_t idesc = idesc_bf16(BM, n_mma, a_mn, b_mn);
   {
-    const int acc = local % C::NACC;
-    const uint32_t use = local / C::NACC;
+    const int acc = local % p.nacc;
+    const uint32_t use = local / p.nacc;
     if (use > 0 && !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + p.timeout_ns)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
       return false;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+    const uint32_t d_tmem = tmem_base + acc * p.acc_cols;
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
       const uint32_t round = it / STAGES;
@@ -616,15 +618,15 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
   const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
   const int r = quarter * 32 + lane;        // row inside the tile
   {
-    const int acc = local % C::NACC;
-    const uint32_t use = local / C::NACC;
+    const int acc = local % p.nacc;
+    const uint32_t use = local / p.nacc;
     if (!mbar_wait(&acc_full[acc], use & 1, globaltimer_ns() + p.timeout_ns)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
       return false;
     }
     tc_fence_after();
-    const uint32_t t_row = tmem_base + acc * C::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t t_row = tmem_base + acc * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
     const bool have = ti.kiters > 0;
     float a[32], b[32];
     // tcgen05.ld and the staged stores are warp-collective: every lane takes part, rows
@@ -1458,6 +1460,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.stages = C::STAGES;
   p.nbuf = 2;
   p.stage_bytes = C::STAGE_BYTES;
+  p.nacc = C::NACC;
+  p.acc_cols = C::ACC_COLS;
   if (p.split) {   // two chunk-sized hi/lo stages leave room for 4 staging boxes per warp
     p.stages = 2;
     p.nbuf = 4;
@@ -1534,7 +1538,13 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDH:
-      p.BN = (c.I % 256 == 0) ? 256 : 128;
+      // MXFP8: 128-column tiles, so that two accumulators fit next to the scale columns
+      // and the long epilogue overlaps the next tile's MMAs
+      p.BN = (!MX && c.I % 256 == 0) ? 256 : 128;
+      if (MX) {
+        p.nacc = 2;
+        p.acc_cols = 128;
+      }
       p.n_tiles = c.I / p.BN;
       p.kiters = c.H / BK;
       p.kcs_a = c.H / 128;
@@ -1627,8 +1637,9 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
   cudaError_t e = build_call<MX>(c.up, q.up, mm.up, mt);
   if (e != cudaSuccess) return e;
   if ((e = build_call<MX>(c.down, q.down, mm.down, mt)) != cudaSuccess) return e;
+  // both phases share the CTA's stage ring, staging boxes and accumulator sequence
   if (q.up.stages != q.down.stages || q.up.stage_bytes != q.down.stage_bytes ||
-      q.up.nbuf != q.down.nbuf)
+      q.up.nbuf != q.down.nbuf || q.up.nacc != q.down.nacc || q.up.acc_cols != q.down.acc_cols)
     return cudaErrorInvalidValue;
   q.M = c.M;
   q.S = c.S;
@@ -1677,7 +1688,7 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
                                      NUM_THREADS, args, C::SMEM_BYTES, s);
 }
 
-int gemm_dh_parts(int I) { return (I % 256 == 0) ? I / 256 : I / 128; }
+int gemm_dh_parts(int I, bool mx) { return (!mx && I % 256 == 0) ? I / 256 : I / 128; }
 
 cudaError_t launch_fwd_mega(const MegaCall& c, int num_sms, cudaStream_t s) {
   return c.up.mx ? launch_mega_impl<true>(c, num_sms, s) : launch_mega_impl<false>(c, num_sms, s);

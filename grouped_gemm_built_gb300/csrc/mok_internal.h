@@ -254,6 +254,6 @@ cudaError_t launch_gather_quant(const Dims& d, const void* src, const mok_sched&
 cudaError_t launch_gather_quant_rows(const Dims& d, const void* src, const mok_sched& sc,
                                      const AuxPtrs& a, void* dst, void* atoms, int num_sms,
                                      cudaStream_t s);
-int gemm_dh_parts(int I);  // number of partial dg columns kBwdDH writes per row
+int gemm_dh_parts(int I, bool mx);  // partial dg columns kBwdDH writes per row
 
 }  // namespace mok
