@@ -219,7 +219,9 @@ __device__ __forceinline__ void load_f32x32(const float* src, float* v) {
     v[4 * q + 3] = w.w;
   }
 }
-__device__ __forceinline__ float sigmoidf_(float v) { return 1.f / (1.f + __expf(-v)); }
+// Fast division: the SwiGLU epilogues run one warp per SM sub-partition and are
+// latency-bound; IEEE division made the MXFP8 forward up|gate launch 19% slower.
+__device__ __forceinline__ float sigmoidf_(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
 
 // bf16 pair of an fp32 value: hi = bf16(v), lo = bf16(v - hi) (v - hi is exact in fp32).
 __device__ __forceinline__ void split_bf16(const float* v, float* hi, float* lo) {
