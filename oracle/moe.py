@@ -58,12 +58,11 @@ class Route:
     gates: np.ndarray    # [T, k] float64
 
 
-def route(x, Wr, k: int, bias=None) -> Route:
-    """Softmax top-k router with renormalised gates (reading stated in the module doc)."""
-    x = np.asarray(x, np.float64)
-    logits = x @ np.asarray(Wr, np.float64)
-    if bias is not None:
-        logits = logits + np.asarray(bias, np.float64)[None, :]
+def select(logits, k: int):
+    """Top-k of softmax(logits) per row with renormalised gates: the k largest logits in
+    descending order, equal logits in ascending expert order; gates = the chosen
+    probabilities over their sum. Returns (idx [T, k] int64, gates [T, k] float64)."""
+    logits = np.asarray(logits, np.float64)
     m = logits.max(axis=1, keepdims=True)
     p = np.exp(logits - m)
     p = p / p.sum(axis=1, keepdims=True)
@@ -72,7 +71,17 @@ def route(x, Wr, k: int, bias=None) -> Route:
     idx = order[:, :k]
     pS = np.take_along_axis(p, idx, axis=1)
     gates = pS / pS.sum(axis=1, keepdims=True)
-    return Route(logits=logits, idx=idx.astype(np.int64), gates=gates)
+    return idx.astype(np.int64), gates
+
+
+def route(x, Wr, k: int, bias=None) -> Route:
+    """Softmax top-k router with renormalised gates (reading stated in the module doc)."""
+    x = np.asarray(x, np.float64)
+    logits = x @ np.asarray(Wr, np.float64)
+    if bias is not None:
+        logits = logits + np.asarray(bias, np.float64)[None, :]
+    idx, gates = select(logits, k)
+    return Route(logits=logits, idx=idx, gates=gates)
 
 
 # ----------------------------------------------------------------------------- schedule

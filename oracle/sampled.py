@@ -13,6 +13,10 @@ the weight-gradient functions take ``plain`` to choose "bf16_plain" over "bf16")
 * dW_down[e][i][h] = sum over e's rows of (g silu(V) U)[i] dY[t][h];
 * dW_up[e][h][i] = sum over e's rows of x[t][h] du[i] (dW_gate with dv).
 
+The ``*_mx`` functions follow ``moe``'s precision "mxfp8" instead: every GEMM operand in
+MXFP8 blocks of 32 along that GEMM's contraction axis (x, h and dY along H or I per row;
+du, dv, g*h, x and dY along the expert rows for the weight gradients).
+
 ``W`` arguments are callables returning one expert's float64 matrices on demand, so the
 caller can stream them from wherever they live.
 """
@@ -161,6 +165,74 @@ def token_forward_mx(t, x, idx, gates, weights_q, shared=None):
         v = x_t @ Ws_gate
         y += bf16_round(silu(v) * u) @ Ws_down
     return y
+
+
+# ----------------------------------------------------------------------------- MXFP8 backward
+def mx_expert_weights_bwd(Wu, Wg, Wd, hs):
+    """What the MXFP8 GEMMs of one token's backward see of one expert: W_up, W_gate in
+    blocks of 32 along H (the forward's U, V), W_down in blocks along H (dH GEMM), and rows
+    ``hs`` of W_up, W_gate in blocks along I (dX GEMM; a row's blocks lie in that row)."""
+    hs = np.asarray(hs)
+    return mx_qdq(Wu, 0), mx_qdq(Wg, 0), mx_qdq(Wd, 1), mx_qdq(Wu[hs], 1), mx_qdq(Wg[hs], 1)
+
+
+def token_backward_mx(t, x, idx, gates, weights_q, dY, Wr=None):
+    """MXFP8 mode, token t: the k router-weight gradients dg_t and dX_t at the hidden
+    indices the weights were cut to (``weights_q(e)`` -> mx_expert_weights_bwd(..., hs)).
+    D = dY_t W_down^T with dY_t and W_down in blocks along H; dg = D . (silu(V) U);
+    du = g D silu(V), dv = g D U silu'(V), each in blocks along I before the dX GEMM;
+    with Wr ([H][E], rows hs only) the router path dl Wr^T is added."""
+    x_t = np.asarray(x[t], np.float64)
+    xq = mx_qdq(x_t[None, :], 1)[0]
+    dYq = mx_qdq(np.asarray(dY[t], np.float64)[None, :], 1)[0]
+    k = idx.shape[1]
+    dg = np.zeros(k)
+    dX = None
+    for j in range(k):
+        e = int(idx[t, j])
+        g = float(gates[t, j])
+        Wu, Wg, Wd, Wu_rows, Wg_rows = weights_q(e)
+        U = xq @ Wu
+        V = xq @ Wg
+        D = Wd @ dYq
+        dg[j] = float(D @ (silu(V) * U))
+        du = mx_qdq((g * D * silu(V))[None, :], 1)[0]
+        dv = mx_qdq((g * D * U * dsilu(V))[None, :], 1)[0]
+        part = Wu_rows @ du + Wg_rows @ dv
+        dX = part if dX is None else dX + part
+    if Wr is not None:
+        s = float((gates[t] * dg).sum())
+        dl = gates[t] * (dg - s)
+        for j in range(k):
+            dX = dX + dl[j] * np.asarray(Wr, np.float64)[:, int(idx[t, j])]
+    return {"dX": dX, "dgates": dg}
+
+
+def dw_lines_mx(pairs, x, dY, gates, Wu, Wg, Wd, i_list):
+    """MXFP8 mode, one expert (its table rows ``pairs``), for each i in ``i_list``: the
+    row dW_down[e][i, :] and the columns dW_up[e][:, i], dW_gate[e][:, i]. U, V from x in
+    blocks along H and W_up, W_gate columns in blocks along H; D from dY in blocks along
+    H and the W_down row in blocks along H; then g*h, du, dv, x and dY in blocks of 32
+    expert rows (the last block completed with zero rows)."""
+    t = pairs[:, 0]
+    g = np.asarray(gates[t, pairs[:, 1]], np.float64)
+    X = np.asarray(x[t], np.float64)
+    dYe = np.asarray(dY[t], np.float64)
+    Xq = mx_qdq(X, 1)
+    dYq = mx_qdq(dYe, 1)
+    XR = mx_qdq_rows_padded(X)
+    dYR = mx_qdq_rows_padded(dYe)
+    out = {}
+    for i in i_list:
+        U = Xq @ mx_qdq(Wu[:, i:i + 1], 0)[:, 0]
+        V = Xq @ mx_qdq(Wg[:, i:i + 1], 0)[:, 0]
+        D = dYq @ mx_qdq(Wd[i:i + 1, :], 1)[0]
+        col = lambda v: mx_qdq_rows_padded(v[:, None])[:, 0]
+        hg = col(g * silu(V) * U)
+        du = col(g * D * silu(V))
+        dv = col(g * D * U * dsilu(V))
+        out[i] = {"dW_down": hg @ dYR, "dW_up": XR.T @ du, "dW_gate": XR.T @ dv}
+    return out
 
 
 def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i, plain=False):

@@ -28,6 +28,10 @@ def _run(cfg, seed, backward):
     L = gu.make_layer(cfg)
     if cfg.router:
         L.plan(x=inp["x"], Wr=inp["Wr"], bias=inp["bias"])
+        torch.cuda.synchronize()
+        # the router's fp32 logits (bias included) open the workspace until the forward
+        L.gpu_logits = f64(L.workspace[: cfg.T * cfg.E * 4].view(torch.float32)
+                           .reshape(cfg.T, cfg.E))
     else:
         L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
     mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"]) \
@@ -42,23 +46,30 @@ def _run(cfg, seed, backward):
 
 
 def _check_schedule(cfg, inp, L):
-    """Routing: equal to the oracle's on every token whose top-(k+1) logits are farther
-    apart than the fp32 error bound; on the others the GPU's choice must be one the bound
-    allows. The schedule of the GPU's expert ids is compared bit for bit. Returns the
-    expert ids and the oracle's gates for those ids (fp64), for the sampled checks."""
+    """Routing, in three parts. (1) The GPU's fp32 logits lie inside the worst-case fp32
+    error bound of the exact ones. (2) The integer decision, taken in the GPU's precision:
+    the oracle's top-k of the GPU's own logits equals the GPU's expert ids on every token,
+    and its gates agree to fp32 rounding. (3) Against the exact logits: a token may be
+    routed differently only where the exact logits of its choice are within twice the
+    largest measured logit error of the exact k-th logit. The schedule of the GPU's
+    expert ids is compared bit for bit. Returns the expert ids and the oracle's gates
+    (exact logits) for those ids, for the sampled checks."""
     x = f64(inp["x"])
     gi = L.topk_idx.cpu().numpy().astype(np.int64)
     if cfg.router:
         r = moe.route(x, f64(inp["Wr"]), cfg.k, None if inp["bias"] is None else f64(inp["bias"]))
-        amb = set(gu.ambiguous_tokens(cfg, inp, r.logits).tolist())
-        diff = np.where((gi != r.idx).any(axis=1))[0]
-        assert all(t in amb for t in diff), f"top-k differs outside near-ties: {diff[:10]}"
+        lg = L.gpu_logits
+        lerr = np.abs(lg - r.logits)
+        assert float((lerr / gu.logit_margins(cfg, inp, r.logits)).max()) <= 1.0
+        sel_idx, sel_g = moe.select(lg, cfg.k)
+        assert np.array_equal(gi, sel_idx), "top-k of the GPU's own logits differs"
+        assert np.abs(L.gates.cpu().numpy() - sel_g).max() < 2e-6
+        emax = float(lerr.max())
+        diff = np.where((np.sort(gi, axis=1) != np.sort(r.idx, axis=1)).any(axis=1))[0]
         if len(diff):
-            bound = gu.logit_margins(cfg, inp, r.logits)[diff]
             kth = np.sort(r.logits[diff], axis=1)[:, -cfg.k]
             chosen = np.take_along_axis(r.logits[diff], gi[diff], axis=1)
-            cb = np.take_along_axis(bound, gi[diff], axis=1)
-            assert np.all(chosen + 2 * cb.max(1, keepdims=True) >= kth[:, None])
+            assert np.all(chosen + 2 * emax >= kth[:, None])
         m = r.logits.max(axis=1, keepdims=True)
         p = np.exp(r.logits - m)
         pS = np.take_along_axis(p, gi, axis=1)
@@ -66,7 +77,8 @@ def _check_schedule(cfg, inp, L):
         # the tensor-core router sums 3H products in its own order: observed 2e-5 at the
         # Kimi size; the layer outputs carry their own tolerance
         assert np.abs(L.gates.cpu().numpy() - gates).max() < 1e-4
-        print(f"{cfg.name}: {len(amb)} near-tie tokens, {len(diff)} routed differently")
+        print(f"{cfg.name}: max logit error {emax:.3g}, {len(diff)} tokens routed to another "
+              f"expert set than the exact logits give")
     else:
         assert np.array_equal(gi, inp["topk_idx"].cpu().numpy())
         gates = f64(inp["gates"])
@@ -78,9 +90,12 @@ def _check_schedule(cfg, inp, L):
     return x, gi, gates, pl
 
 
-def test_kimi_8192_bf16_full_size_sampled():
-    cfg = mi.CONFIGS["kimi_8192"]
-    inp, L, y, g = _run(cfg, seed=7, backward=True)
+@pytest.mark.parametrize("name,seed", [("kimi_8192", 7), ("kimi_2368", 5)])
+def test_kimi_bf16_full_size_sampled(name, seed):
+    """Kimi-2.5 expert shape with all 384 experts on one GPU: T=8192 (about 171 rows per
+    expert) and T=2368 (about 49, most experts a single partly filled row tile)."""
+    cfg = mi.CONFIGS[name]
+    inp, L, y, g = _run(cfg, seed=seed, backward=True)
     x, idx, gates, pl = _check_schedule(cfg, inp, L)
     dY = f64(inp["dY"])
     Wr = f64(inp["Wr"])
@@ -93,7 +108,7 @@ def test_kimi_8192_bf16_full_size_sampled():
             cache[e] = tuple(f64(inp[n][e]) for n in ("W_up", "W_gate", "W_down"))
         return cache[e]
 
-    tokens = [0, 2049, 5000, cfg.T - 1]
+    tokens = [0, cfg.T // 4 + 1, (5 * cfg.T) // 8, cfg.T - 1]
     gy, gdx, gdg, ry, rdx, rdg = [], [], [], [], [], []
     for t in tokens:
         o = sampled.token_outputs(t, x, idx, gates, W, dY=dY, shared=shared, Wr=Wr)
@@ -115,7 +130,7 @@ def test_kimi_8192_bf16_full_size_sampled():
         errs[f"dWs_down[{i}]"] = err(f64(g["dWs_down"][i, :]), ref["dWs_down"])
         errs[f"dWs_up[{i}]"] = err(f64(g["dWs_up"][:, i]), ref["dWs_up"])
         errs[f"dWs_gate[{i}]"] = err(f64(g["dWs_gate"][:, i]), ref["dWs_gate"])
-    print("kimi_8192", errs)
+    print(name, errs)
     for k, v in errs.items():
         assert v <= gu.TOL["bf16"], (k, v)
 
@@ -154,6 +169,58 @@ def test_dsv3_imbalanced_mxfp8_forward_sampled():
     inp, L, y, _ = _run(cfg, seed=11, backward=False)
     pl = _mx_forward_sampled(cfg, inp, L, y, [1, cfg.T // 2, cfg.T - 2])
     assert pl.counts[:4].min() > 4 * np.median(pl.counts)
+
+
+def test_dsv3_imbalanced_mxfp8_backward_sampled():
+    """MXFP8 backward at the DeepSeek-V3 shape (T=16384, 256 experts, four hot experts).
+    In the bench's configuration (router in the layer): the schedule, one token's
+    router-weight gradients and its dX at 64 hidden indices (router path included).
+    Weight gradients: whole lines of the busiest expert in a second run that takes the
+    oracle's routing (expert ids and fp32 gates) as its input, so that both sides quantise
+    the same g*du values (see test_mxfp8_layer_matches_oracle)."""
+    cfg = mi.CONFIGS["dsv3_imbalanced"]
+    inp, L, y, g = _run(cfg, seed=11, backward=True)
+    x, idx, gates, pl = _check_schedule(cfg, inp, L)
+    dY = f64(inp["dY"])
+    hs = np.arange(0, cfg.H, cfg.H // 64) + 3
+    Wr_hs = f64(inp["Wr"])[hs]
+
+    def wq(e):
+        return sampled.mx_expert_weights_bwd(*(f64(inp[n][e]) for n in
+                                               ("W_up", "W_gate", "W_down")), hs)
+
+    t = cfg.T // 3
+    o = sampled.token_backward_mx(t, x, idx, gates, wq, dY, Wr=Wr_hs)
+    errs = {"dX": err(f64(g["dX"][t])[hs], o["dX"]),
+            "dgates": err(g["dgates"][t].cpu().numpy(), o["dgates"])}
+    del L, y, g
+    torch.cuda.empty_cache()
+
+    r = moe.route(x, f64(inp["Wr"]), cfg.k, f64(inp["bias"]))
+    g32 = r.gates.astype(np.float32)
+    ext = mi.scaled(cfg, router=False)
+    L2 = gu.make_layer(ext)
+    L2.plan(topk_idx=torch.as_tensor(r.idx, dtype=torch.int32).cuda(),
+            gates=torch.as_tensor(g32).cuda())
+    mx = L2.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"])
+    w = L2.weights(inp["W_up"], inp["W_gate"], inp["W_down"], mx=mx)
+    L2.forward(inp["x"], w)
+    g2 = L2.backward(inp["x"], None, w, inp["dY"])
+    torch.cuda.synchronize()
+    assert L2.status() == 0
+    pl2 = moe.plan(r.idx, cfg.E)
+    e = int(np.argmax(pl2.counts))
+    assert pl2.counts[e] > 4 * np.median(pl2.counts)
+    lines = sampled.dw_lines_mx(sampled.expert_rows(pl2, e), x, dY, g32.astype(np.float64),
+                                *(f64(inp[n][e]) for n in ("W_up", "W_gate", "W_down")),
+                                [5, cfg.I - 3])
+    for i, li in lines.items():
+        errs[f"dW_down[{e}][{i}]"] = err(f64(g2["dW_down"][e, i, :]), li["dW_down"])
+        errs[f"dW_up[{e}][{i}]"] = err(f64(g2["dW_up"][e, :, i]), li["dW_up"])
+        errs[f"dW_gate[{e}][{i}]"] = err(f64(g2["dW_gate"][e, :, i]), li["dW_gate"])
+    print("dsv3_imbalanced backward", int(pl2.counts[e]), "rows", errs)
+    for k, v in errs.items():
+        assert v <= gu.TOL["mxfp8"], (k, v)
 
 
 def test_ep64_slice_megakernel_matches_launches_full_size():

@@ -312,6 +312,34 @@ def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng, mode):
         assert np.allclose(yt, ym[t], rtol=1e-12, atol=1e-12)
 
 
+def test_mx_backward_evaluators_match_the_dense_oracle(rng):
+    """The MXFP8 full-size backward evaluators (one token's dgates and dX at sampled
+    hidden indices with the router path; whole dW lines of one expert) against the dense
+    per-expert oracle in mxfp8 mode."""
+    from oracle import sampled
+    from oracle.numerics import bf16_round
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=64, H=64, I=64, E=3, k=2)
+    x = bf16_round(x)
+    r = moe.route(x, Wr, 2)
+    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="mxfp8")
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, precision="mxfp8", Wr=Wr)
+    hs = np.array([0, 5, 31, 63])
+    wq = lambda e: sampled.mx_expert_weights_bwd(Wu[e], Wg[e], Wd[e], hs)
+    for t in range(40):
+        o = sampled.token_backward_mx(t, x, r.idx, r.gates, wq, dY, Wr=Wr[hs])
+        assert np.allclose(o["dgates"], g.dgates[t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(o["dX"], g.dX[t, hs], rtol=1e-12, atol=1e-12)
+    pl = saved["plan"]
+    assert pl.counts.max() > 32          # an expert with more than one 32-row block
+    for e in range(3):
+        L = sampled.dw_lines_mx(sampled.expert_rows(pl, e), x, dY, r.gates, Wu[e], Wg[e],
+                                Wd[e], [0, 17, 63])
+        for i, li in L.items():
+            assert np.allclose(li["dW_down"], g.dW_down[e, i, :], rtol=1e-12, atol=1e-12)
+            assert np.allclose(li["dW_up"], g.dW_up[e, :, i], rtol=1e-12, atol=1e-12)
+            assert np.allclose(li["dW_gate"], g.dW_gate[e, :, i], rtol=1e-12, atol=1e-12)
+
+
 @pytest.mark.parametrize("mode", ["bf16", "bf16_plain", "mxfp8"])
 def test_shared_dw_lines_match_the_dense_oracle(rng, mode):
     from oracle import sampled
