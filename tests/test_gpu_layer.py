@@ -27,6 +27,14 @@ CASES = {
     "mid_plain": mi.scaled(mi.CONFIGS["mid"], name="mid_plain", precision="bf16_plain"),
     "sparse_plain": mi.MoEConfig("sparse_plain", T=64, H=128, I=128, E=64, k=1,
                                  precision="bf16_plain"),
+    # the largest expert count and top-k the library takes, Zipf(1.2) loads: a few busy
+    # experts, hundreds with one row or none
+    "max_experts": mi.MoEConfig("max_experts", T=200, H=128, I=128, E=512, k=8, router=False,
+                                zipf_s=1.2, macrobatches=0),
+    # degenerate: one expert, top-1 (a dense SwiGLU FFN with gate 1)
+    "single_expert": mi.MoEConfig("single_expert", T=130, H=128, I=128, E=1, k=1),
+    # degenerate: every token routed to every expert (k = E)
+    "all_experts": mi.MoEConfig("all_experts", T=96, H=128, I=256, E=4, k=4, shared_I=128),
 }
 
 
@@ -126,6 +134,8 @@ MX_CASES = {
                                      backward=False),
     "ragged_shared_mx": mi.MoEConfig("ragged_shared_mx", T=300, H=256, I=256, E=12, k=3,
                                      shared_I=128, precision="mxfp8"),
+    "max_experts_mx": mi.MoEConfig("max_experts_mx", T=128, H=256, I=256, E=512, k=8,
+                                   router=False, zipf_s=1.2, macrobatches=0, precision="mxfp8"),
 }
 
 
@@ -204,6 +214,35 @@ def test_router_logits_within_fp32_bound(name, bias):
     ratio = np.abs(got - exact) / bound
     print(name, "max |err| / bound", float(ratio.max()))
     assert float(ratio.max()) <= 1.0
+
+
+@pytest.mark.parametrize("E,k,bias", [(512, 8, True), (4, 4, False), (1, 1, False)])
+def test_topk_of_gpu_logits_is_exact(E, k, bias):
+    """The integer decision in the GPU's own precision: the oracle's top-k (same rule:
+    larger logit first, equal logits in ascending expert order) of the router's fp32
+    logits equals the GPU's expert ids on every token, at the largest expert count and
+    top-k and at k = E and E = 1; gates agree to fp32 rounding; the schedule of those ids
+    is the oracle's, bit for bit."""
+    cfg = mi.MoEConfig(f"topk_{E}_{k}", T=300, H=256, I=128, E=E, k=k,
+                       bias_experts=(0, 1, 2, 3) if bias else (), bias_value=1.0)
+    inp = gu.gpu_inputs(cfg, seed=4)
+    L = gu.make_layer(cfg)
+    d = gu.to_dev(inp)
+    L.plan(x=d["x"], Wr=d["Wr"], bias=d["bias"])
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    lg = L.workspace[: cfg.T * cfg.E * 4].view(torch.float32).reshape(cfg.T, cfg.E)
+    lg = lg.cpu().double().numpy()
+    x, Wr = gu.np64(inp["x"]), gu.np64(inp["Wr"])
+    exact = x @ Wr + (gu.np64(inp["bias"])[None, :] if inp["bias"] is not None else 0.0)
+    assert float((np.abs(lg - exact) / gu.logit_margins(cfg, inp, exact)).max()) <= 1.0
+    idx, gates = gu.moe.select(lg, cfg.k)
+    gi = L.topk_idx.cpu().numpy()
+    assert np.array_equal(gi, idx)
+    assert np.abs(L.gates.cpu().numpy() - gates).max() < 2e-6
+    pl = gu.moe.plan(idx, cfg.E)
+    for f in ("counts", "offsets", "table", "inv"):
+        assert np.array_equal(getattr(L, f).cpu().numpy(), getattr(pl, f)), f
 
 
 @pytest.mark.parametrize("name", ["ragged_shared", "tiny_mx"])
