@@ -188,75 +188,83 @@ cudaError_t launch_gather_quant(const Dims& d, const void* src, const mok_sched&
 namespace mok {
 
 // ---------------------------------------------------------------- dispatch + row blocks
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
 // Pull rows by the table and quantise them in blocks of 32 consecutive padded rows (the
 // contraction axis of the dW GEMMs). Blocks start at each expert segment's first row,
-// since segments start on 128-row boundaries. One CTA per (32-row block, 256 columns):
-// thread per column; atoms [P/128][H/128], m = column, b = block inside the 128-row tile.
-__global__ void __launch_bounds__(256) gather_quant_rows_kernel(
+// since segments start on 128-row boundaries. A CTA takes 512 columns (two per thread) of
+// every gridDim.y-th 32-row block; atoms [P/128][H/128], m = column, b = block inside the
+// 128-row tile.
+__global__ void __launch_bounds__(256, 2) gather_quant_rows_kernel(
     int H, int E, const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ table,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ poff, const int32_t* __restrict__ tile_expert,
     const int32_t* __restrict__ num_mtiles, int P_max, uint8_t* __restrict__ dst,
     uint8_t* __restrict__ atoms) {
-  __shared__ int s_tok[32];
+  // source tokens of the CTA's next 8 blocks (blockIdx.y + q gridDim.y), one lookup per
+  // thread, so the table's dependent loads are paid once per 8 blocks
+  __shared__ int s_tok[8][32];
   const int P = min(*num_mtiles, P_max / kRowPad) * kRowPad;
   const int nblocks = P / 32;
   const int kcs = H / 128;
-  for (int blk = blockIdx.y; blk < nblocks; blk += gridDim.y) {
-    const int p0 = blk * 32;
+  // two neighbouring columns per thread (a warp loads a whole 128-byte line of each row);
+  // the 32 rows stay in registers as the loaded bf16 pairs and are widened twice
+  const int col = (blockIdx.x * 256 + threadIdx.x) * 2;
+  for (int base = blockIdx.y; base < nblocks; base += 8 * gridDim.y) {
     __syncthreads();
-    if (threadIdx.x < 32) {
-      const int p = p0 + threadIdx.x;
-      int e = tile_expert[p / kRowPad];
-      e = (e < 0 || e >= E) ? 0 : e;
-      const int r = p - poff[e];
-      s_tok[threadIdx.x] = (r < counts[e]) ? table[2 * (size_t)(offsets[e] + r)] : -1;
+    {
+      const int b = base + (threadIdx.x >> 5) * gridDim.y;
+      int tok = -1;
+      if (b < nblocks) {
+        const int p = b * 32 + (threadIdx.x & 31);
+        int e = tile_expert[p / kRowPad];
+        e = (e < 0 || e >= E) ? 0 : e;
+        const int r = p - poff[e];
+        if (r < counts[e]) tok = table[2 * (size_t)(offsets[e] + r)];
+      }
+      s_tok[threadIdx.x >> 5][threadIdx.x & 31] = tok;
     }
     __syncthreads();
-    // four neighbouring columns per thread: 8-byte loads, 4-byte stores
-    const int col = (blockIdx.x * 256 + threadIdx.x) * 4;
     if (col >= H) continue;
-    float f[32][4];
-    float amax[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int q = 0; q < 8; ++q) {
+      const int blk = base + q * gridDim.y;
+      if (blk >= nblocks) break;
+      const int p0 = blk * 32;
+      uint32_t raw[32];
+      float amax0 = 0.f, amax1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int t = s_tok[i];
-      uint2 w = make_uint2(0u, 0u);
-      if (t >= 0) w = __ldg(reinterpret_cast<const uint2*>(src + (size_t)t * H + col));
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
-      const float2 a01 = __bfloat1622float2(h2[0]);
-      const float2 a23 = __bfloat1622float2(h2[1]);
-      f[i][0] = a01.x;
-      f[i][1] = a01.y;
-      f[i][2] = a23.x;
-      f[i][3] = a23.y;
+      for (int i = 0; i < 32; ++i) {
+        const int t = s_tok[q][i];
+        raw[i] = 0u;
+        if (t >= 0) raw[i] = __ldg(reinterpret_cast<const uint32_t*>(src + (size_t)t * H + col));
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) amax[j] = fmaxf(amax[j], fabsf(f[i][j]));
+      for (int i = 0; i < 32; ++i) {
+        const float2 f = bf16x2_to_float2(raw[i]);
+        amax0 = fmaxf(amax0, fabsf(f.x));
+        amax1 = fmaxf(amax1, fabsf(f.y));
+      }
+      const uint32_t sb0 = mx_scale_byte(amax0), sb1 = mx_scale_byte(amax1);
+      const float inv0 = mx_inv_scale(sb0), inv1 = mx_inv_scale(sb1);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 f = bf16x2_to_float2(raw[i]);
+        *reinterpret_cast<uint16_t*>(dst + (size_t)(p0 + i) * H + col) =
+            (uint16_t)f32x2_to_e4m3x2(f.x * inv0, f.y * inv1);
+      }
+      atoms[((size_t)(p0 >> 7) * kcs + (col >> 7)) * 512 + atom_byte(col, p0)] = (uint8_t)sb0;
+      atoms[((size_t)(p0 >> 7) * kcs + ((col + 1) >> 7)) * 512 + atom_byte(col + 1, p0)] =
+          (uint8_t)sb1;
     }
-    uint32_t sb[4];
-    float inv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      sb[j] = mx_scale_byte(amax[j]);
-      inv[j] = mx_inv_scale(sb[j]);
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t q = (uint32_t)f32x2_to_e4m3x2(f[i][0] * inv[0], f[i][1] * inv[1]) |
-                         ((uint32_t)f32x2_to_e4m3x2(f[i][2] * inv[2], f[i][3] * inv[3]) << 16);
-      *reinterpret_cast<uint32_t*>(dst + (size_t)(p0 + i) * H + col) = q;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      atoms[((size_t)(p0 >> 7) * kcs + ((col + j) >> 7)) * 512 + atom_byte(col + j, p0)] =
-          (uint8_t)sb[j];
   }
 }
 
 cudaError_t launch_gather_quant_rows(const Dims& d, const void* src, const mok_sched& sc,
                                      const AuxPtrs& a, void* dst, void* atoms, int num_sms,
                                      cudaStream_t s) {
-  dim3 grid((d.H / 4 + 255) / 256, num_sms * 4);
+  dim3 grid((d.H / 2 + 255) / 256, num_sms * 4);
   gather_quant_rows_kernel<<<grid, 256, 0, s>>>(
       d.H, d.E, static_cast<const __nv_bfloat16*>(src), sc.table, sc.counts, sc.offsets, a.poff,
       a.tile_expert, a.num_mtiles, d.P_max, static_cast<uint8_t*>(dst),
