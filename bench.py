@@ -217,6 +217,26 @@ def kernel_work(cfg, name, counts=None):
     return tbl.get(name)
 
 
+# ----------------------------------------------------------------------------- replicas
+def max_over_ranks(x, device):
+    """x's maximum over the ranks of the default process group (x itself on one rank):
+    the slowest replica's time is the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, tokens_per_rank, steps, ms):
+    """Tokens per second of the whole job: each of ``world`` replicas processes
+    ``tokens_per_rank`` tokens per step (weak scaling); ``ms`` is the slowest replica's
+    time for ``steps`` steps."""
+    return world * tokens_per_rank * steps / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -292,12 +312,9 @@ def run_gpu(args):
     clocks = clk.stop()
     if L.status() != 0:
         raise RuntimeError("device status error in the timed region")
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, "cuda")
     ms_step = ms / args.steps
-    value = world * cfg.T * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, cfg.T, args.steps, ms)
 
     # ------------------------------------------------------------ e2e (host buffers)
     e2e = None
@@ -365,12 +382,8 @@ def run_gpu(args):
         run_e2e(k_e2e, e0, e1)
         cs.synchronize()
         barrier()
-        ms_e2e = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms_e2e], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": world * cfg.T * k_e2e / (ms_e2e / 1e3), "unit": "tokens/s",
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), "cuda")
+        e2e = {"value": whole_job_rate(world, cfg.T, k_e2e, ms_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": hx.numel() * 2 + (hdy.numel() * 2 if cfg.backward else 0),
                "d2h_bytes_per_step": hy.numel() * 4 + (hdx.numel() * 4 if cfg.backward else 0),
                "steps": k_e2e,
