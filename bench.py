@@ -63,7 +63,7 @@ def peaks():
 # A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
 NCU_TRAFFIC = {
     ("kimi_8192", "gemm_bwd_dw_upgate"): {
-        "bytes": 47.355e9, "rev": "c5e644c038dd566a",
+        "bytes": 47.35e9, "rev": "2bb504ba8cf845a9",
         "profile": "profiles/dram_traffic_kimi8192_bf16.md"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
