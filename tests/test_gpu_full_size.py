@@ -223,6 +223,55 @@ def test_dsv3_imbalanced_mxfp8_backward_sampled():
         assert v <= gu.TOL["mxfp8"], (k, v)
 
 
+def _bit_checksums(t):
+    """Two 64-bit checksums of a tensor's 32-bit words, in chunks on the device: the plain
+    sum and a sum weighted by position (mod 65521), so that a changed or moved word
+    changes them."""
+    w = t.detach().contiguous().view(torch.int32).reshape(-1)
+    n = w.numel()
+    chunk = 1 << 27
+    pos = (torch.arange(chunk, device=w.device, dtype=torch.int64) % 65521) + 1
+    s1 = torch.zeros((), dtype=torch.int64, device=w.device)
+    s2 = torch.zeros((), dtype=torch.int64, device=w.device)
+    for i in range(0, n, chunk):
+        c = w[i:i + chunk].to(torch.int64)
+        s1 += c.sum()
+        s2 += (c * pos[:c.numel()]).sum()
+    return int(s1), int(s2)
+
+
+@pytest.mark.parametrize("name", ["dsv3_imbalanced", "kimi_8192"])
+def test_full_size_bitwise_deterministic_over_10_runs(name):
+    """Ten plan + forward + backward steps at full size, in the bench's launch sequence,
+    give the same bits for the routing, y, dX and every gradient (checksums of the 32-bit
+    words, compared run by run)."""
+    cfg = mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, seed=13, device="cuda", with_dy=True)
+    L = gu.make_layer(cfg)
+    mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"]) \
+        if cfg.precision == "mxfp8" else None
+    w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
+                  inp["Ws_down"], mx=mx)
+    grads = L.alloc_grads()
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device="cuda")
+    first = None
+    for run in range(10):
+        L.plan(x=inp["x"], Wr=inp["Wr"], bias=inp["bias"])
+        L.forward(inp["x"], w, y)
+        L.backward(inp["x"], inp["Wr"], w, inp["dY"], grads)
+        torch.cuda.synchronize()
+        assert L.status() == 0
+        sums = {"topk_idx": _bit_checksums(L.topk_idx), "gates": _bit_checksums(L.gates),
+                "y": _bit_checksums(y)}
+        for f, v in grads.items():
+            if v is not None:
+                sums[f] = _bit_checksums(v)
+        if first is None:
+            first = sums
+        else:
+            assert sums == first, (run, [f for f in sums if sums[f] != first[f]])
+
+
 def test_ep64_slice_megakernel_matches_launches_full_size():
     """The full EP=64 slice through the forward megakernel (4 macrobatches, a 256 MB ring
     of 3 slots, so slots are reused) gives the same bits as one launch per step."""
