@@ -815,10 +815,14 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   st.drain();
 }
 
-template <bool MX>
+// One instantiation per mode: with the mode a compile-time constant the compiler keeps
+// only that mode's producer, MMA and epilogue code (a smaller instruction footprint).
+template <bool MX, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p) {
+    grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p_in) {
   using C = Cfg<MX>;
+  Params p = p_in;
+  p.mode = MODE;
   constexpr int STAGES = C::STAGES;   // barrier slots; the launch uses p.stages of them
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1595,16 +1599,34 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   return cudaSuccess;
 }
 
+using GemmKernel = void (*)(const Maps, const Params);
+
+template <bool MX>
+GemmKernel gemm_kernel_for(int mode) {
+  switch (mode) {
+    case kFwdUpGate: return grouped_gemm_kernel<MX, kFwdUpGate>;
+    case kFwdDown: return grouped_gemm_kernel<MX, kFwdDown>;
+    case kBwdDH: return grouped_gemm_kernel<MX, kBwdDH>;
+    case kBwdDX: return grouped_gemm_kernel<MX, kBwdDX>;
+    case kBwdDWDown: return grouped_gemm_kernel<MX, kBwdDWDown>;
+    case kBwdDWUpGate: return grouped_gemm_kernel<MX, kBwdDWUpGate>;
+    case kRouter: return grouped_gemm_kernel<MX, kRouter>;
+    default: return nullptr;
+  }
+}
+
 template <bool MX>
 cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   using C = Cfg<MX>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static bool attr_set[8] = {};
+  if (c.mode < 0 || c.mode >= 8) return cudaErrorInvalidValue;
+  const GemmKernel kern = gemm_kernel_for<MX>(c.mode);
+  if (!kern) return cudaErrorInvalidValue;
+  if (!attr_set[c.mode]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[c.mode] = true;
   }
   Params p;
   Maps mp;
@@ -1613,7 +1635,7 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MX><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(mp, p);
+  kern<<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(mp, p);
   return cudaGetLastError();
 }
 
