@@ -143,6 +143,7 @@ struct TileInfo {
   int n0;       // first output column
   int kiters;   // K iterations
   int krow0;    // dW modes: first row of the contraction range
+  int klast;    // dW modes: MMA K steps of the last K iteration that hold rows
   int skip;     // 1: no tile here (the unmatched half of the last row-tile pair)
 };
 
@@ -165,8 +166,10 @@ __device__ __forceinline__ int num_tiles_of(const Params& p) {
 template <bool MX>
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
   constexpr int BK = Cfg<MX>::BK;
+  constexpr int MMA_K = Cfg<MX>::MMA_K;
   TileInfo ti;
   ti.skip = 0;
+  ti.klast = BK / MMA_K;
   if (is_dw(p.mode)) {
     const int per_e = p.m_tiles_dw * p.n_tiles;
     ti.e = tile / per_e;
@@ -174,13 +177,21 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
     const int mt = rem / p.n_tiles;
     ti.row0 = mt * BM;
     ti.n0 = (rem - mt * p.n_tiles) * (p.mode == kBwdDWUpGate ? 128 : p.BN);
+    int krows;
     if (p.dense) {
       ti.krow0 = 0;
+      krows = p.M_rows;
       ti.kiters = (p.M_rows + BK - 1) / BK;
     } else {
       // the expert's rows rounded up to the K step; the segment's padding rows are zero
       ti.krow0 = p.poff[ti.e];
-      ti.kiters = min((max(p.counts[ti.e], 0) + BK - 1) / BK, (p.poff[ti.e + 1] - ti.krow0) / BK);
+      krows = max(p.counts[ti.e], 0);
+      ti.kiters = min((krows + BK - 1) / BK, (p.poff[ti.e + 1] - ti.krow0) / BK);
+    }
+    // the last K iteration's MMAs stop after the last row (the rest would add zeros)
+    if (ti.kiters > 0) {
+      const int rem = krows - (ti.kiters - 1) * BK;
+      if (rem > 0 && rem < BK) ti.klast = (rem + MMA_K - 1) / MMA_K;
     }
   } else {
     int mt, nt;
@@ -547,6 +558,8 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
       const uint32_t sb = sa + A_BYTES;
+      // MMA K steps of this stage: all four, except in a dW tile's last K iteration
+      const int nk = (is_dw(p.mode) && kb == ti.kiters - 1) ? ti.klast : 4;
       uint32_t t_sfa = 0, t_sfb = 0;
       if (MX) {
         // scale atoms -> TMEM: A in 4 columns, B in 4 columns per 128 rows of N
@@ -559,6 +572,7 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
+        if (kk >= nk) break;
         // K-major: the kk-th K slice starts 32 bytes further along each 128-byte row.
         // MN-major: it starts MMA_K rows further; 128-byte MN chunks are MN_LBO apart
         // (leading byte offset), 8-row groups 1 KB apart (stride byte offset).
@@ -579,9 +593,11 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
         const uint32_t a2 = p.mode == kBwdDWDown ? sx : sa;
         const uint32_t b2 = p.mode == kBwdDWDown ? sb : sx;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < 4; ++kk) {
+          if (kk >= nk) break;
           umma_bf16(d_tmem, umma_desc_sw128(a2 + kk * C::MN_KSTEP, C::MN_LBO, 1024),
                     umma_desc_sw128(b2 + kk * C::MN_KSTEP, C::MN_LBO, 1024), idesc, 1u);
+        }
       }
       umma_commit(&empty[stage]);   // frees the stage once these MMAs have read it
     }
@@ -972,6 +988,7 @@ __device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph
   ti.n0 = n * (ph ? p.BN : 128);
   ti.kiters = p.kiters;
   ti.krow0 = 0;
+  ti.klast = 4;
   ti.skip = r >= mega_mtiles(q, m);
   return ti;
 }
