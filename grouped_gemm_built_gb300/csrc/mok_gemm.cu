@@ -232,6 +232,20 @@ __device__ __forceinline__ void load_f32x32(const float* src, float* v) {
 }
 // Fast division: the SwiGLU epilogues run one warp per SM sub-partition and are
 // latency-bound; IEEE division made the MXFP8 forward up|gate launch 19% slower.
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = __ldg(s + q);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * q + 2 * i] = f.x;
+      v[8 * q + 2 * i + 1] = f.y;
+    }
+  }
+}
 __device__ __forceinline__ float sigmoidf_(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
 
 // bf16 pair of an fp32 value: hi = bf16(v), lo = bf16(v - hi) (v - hi is exact in fp32).
@@ -674,8 +688,13 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
           } else {
             st.bf16(&mp.o[0], h, col, wrow);     // h, bf16 operand of the down GEMM
           }
-          st.f32(&mp.o[1], a, col, wrow);        // saved U, fp32
-          st.f32(&mp.o[2], b, col, wrow);        // saved V, fp32
+          if (MX) {   // saved U, V in bf16: the backward quantises du, dv to E4M3 anyway
+            st.bf16(&mp.o[1], a, col, wrow);
+            st.bf16(&mp.o[2], b, col, wrow);
+          } else {    // saved U, V in fp32
+            st.f32(&mp.o[1], a, col, wrow);
+            st.f32(&mp.o[2], b, col, wrow);
+          }
         }
         if (MX && valid) {
           const size_t atom = (size_t)(row / BM) * (p.I / 128) + ti.n0 / 128;
@@ -722,8 +741,13 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
           tmem_ld32(t_row + c * 32, a);          // D = dY W_down^T
           float u[32], v[32];
           if (valid) {
-            load_f32x32(p.u + o + c * 32, u);    // saved U
-            load_f32x32(p.v + o + c * 32, v);    // saved V
+            if (MX) {                            // saved U, V (bf16 in MXFP8)
+              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.u) + o + c * 32, u);
+              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.v) + o + c * 32, v);
+            } else {                             // saved U, V (fp32)
+              load_f32x32(p.u + o + c * 32, u);
+              load_f32x32(p.v + o + c * 32, v);
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = v[i] = a[i] = 0.f;
@@ -1531,8 +1555,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
            make_map(&mp.b[0], c.b[0], c.I, G * c.H, BK, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, BK, eb) &&
            (MX || make_out_map(&mp.o[0], c.out[0], c.I, rows, 2)) &&
-           make_out_map(&mp.o[1], c.out[1], c.I, rows, 4) &&
-           make_out_map(&mp.o[2], c.out[2], c.I, rows, 4);
+           make_out_map(&mp.o[1], c.out[1], c.I, rows, MX ? 2 : 4) &&
+           make_out_map(&mp.o[2], c.out[2], c.I, rows, MX ? 2 : 4);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kFwdDown:

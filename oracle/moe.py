@@ -37,7 +37,8 @@ stay unrounded here; U, V, expert outputs, routed dX rows and all results stay u
 too (the GPU keeps them in fp32). "bf16_plain" is "bf16" with du, dv and g*h rounded to
 bf16 for the weight-gradient GEMMs as well. "mxfp8" quantises every GEMM operand to
 MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, dv, g*h,
-dY). Everything else is float64. The shared expert is always BF16: single bf16
+dY), and keeps U, V for the backward as bf16 values (h is formed from the unrounded ones).
+Everything else is float64. The shared expert is always BF16: single bf16
 weight-gradient operands in "bf16_plain", hi/lo ones in "bf16" and "mxfp8".
 """
 from __future__ import annotations
@@ -163,6 +164,10 @@ class Precision:
         """du, dv feeding the dX GEMM along ``axis`` (I): bf16, or MXFP8 blocks."""
         return self.fwd_act(a, axis)
 
+    def saved_uv(self, a):
+        """U, V as kept for the backward: bf16 in mxfp8 mode, unrounded otherwise."""
+        return bf16_round(a) if self.mx else a
+
     def bwd_act_rows(self, a):
         """du, dv, g*h feeding a weight-gradient GEMM (K = expert rows): MXFP8 blocks of 32
         rows in mxfp8 mode, bf16 in bf16_plain mode; bf16 mode carries them as a bf16
@@ -215,8 +220,8 @@ def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
         V = A @ P.op(W_gate[e], 0)
         h = P.fwd_act(silu(V) * U, 1)
         O_rows[r0:r1] = h @ P.op(W_down[e], 0)
-        U_s[r0:r1] = U
-        V_s[r0:r1] = V
+        U_s[r0:r1] = P.saved_uv(U)
+        V_s[r0:r1] = P.saved_uv(V)
     y = np.zeros((T, H))
     for j in range(k):                                  # combine in slot order
         y += gates[:, j:j + 1] * O_rows[pl.inv[:, j]]

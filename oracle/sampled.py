@@ -15,7 +15,8 @@ the weight-gradient functions take ``plain`` to choose "bf16_plain" over "bf16")
 
 The ``*_mx`` functions follow ``moe``'s precision "mxfp8" instead: every GEMM operand in
 MXFP8 blocks of 32 along that GEMM's contraction axis (x, h and dY along H or I per row;
-du, dv, g*h, x and dY along the expert rows for the weight gradients).
+du, dv, g*h, x and dY along the expert rows for the weight gradients), and the backward
+reads U, V as bf16 values.
 
 ``W`` arguments are callables returning one expert's float64 matrices on demand, so the
 caller can stream them from wherever they live.
@@ -192,8 +193,8 @@ def token_backward_mx(t, x, idx, gates, weights_q, dY, Wr=None):
         e = int(idx[t, j])
         g = float(gates[t, j])
         Wu, Wg, Wd, Wu_rows, Wg_rows = weights_q(e)
-        U = xq @ Wu
-        V = xq @ Wg
+        U = bf16_round(xq @ Wu)          # U, V as saved for the backward
+        V = bf16_round(xq @ Wg)
         D = Wd @ dYq
         dg[j] = float(D @ (silu(V) * U))
         du = mx_qdq((g * D * silu(V))[None, :], 1)[0]
@@ -224,8 +225,8 @@ def dw_lines_mx(pairs, x, dY, gates, Wu, Wg, Wd, i_list):
     dYR = mx_qdq_rows_padded(dYe)
     out = {}
     for i in i_list:
-        U = Xq @ mx_qdq(Wu[:, i:i + 1], 0)[:, 0]
-        V = Xq @ mx_qdq(Wg[:, i:i + 1], 0)[:, 0]
+        U = bf16_round(Xq @ mx_qdq(Wu[:, i:i + 1], 0)[:, 0])   # as saved for the backward
+        V = bf16_round(Xq @ mx_qdq(Wg[:, i:i + 1], 0)[:, 0])
         D = dYq @ mx_qdq(Wd[i:i + 1, :], 1)[0]
         col = lambda v: mx_qdq_rows_padded(v[:, None])[:, 0]
         hg = col(g * silu(V) * U)
