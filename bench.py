@@ -63,10 +63,10 @@ def peaks():
 # A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
 NCU_TRAFFIC = {
     ("kimi_8192", "gemm_bwd_dw_upgate"): {
-        "bytes": 47.35e9, "rev": "21ad7db0dde0eab2",
+        "bytes": 47.35e9, "rev": "c338f66c2126f3f3",
         "profile": "profiles/dram_traffic_kimi8192_bf16.md"},
     ("dsv3_imbalanced", "gemm_bwd_dw_upgate_mxfp8"): {
-        "bytes": 31.91e9, "rev": "21ad7db0dde0eab2",
+        "bytes": 32.32e9, "rev": "c338f66c2126f3f3",
         "profile": "profiles/dram_traffic_dsv3_mxfp8.md"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
@@ -200,22 +200,23 @@ def kernel_work(cfg, name, counts=None):
     mx = name.endswith("_mxfp8")
     name = name[:-len("_mxfp8")] if mx else name
     b = 1.0 + 1.0 / 32 if mx else 2.0     # bytes per operand element (MXFP8: + scales)
-    # (FLOPs, bytes): operands b bytes, U, V and fp32 O / dXg rows and gradients 4 B
+    uv = 2.0 if mx else 4.0               # bytes per saved U, V element (MXFP8 keeps bf16)
+    # (FLOPs, bytes): operands b bytes, U and V uv bytes, fp32 O / dXg rows and gradients
     tbl = {
         "gemm_fwd_upgate_swiglu": (4.0 * H * I * rows,
                                    b * (2 * H * I * E + rows * H + rows * I)
-                                   + 8.0 * rows * I),
+                                   + 2 * uv * rows * I),
         "gemm_fwd_down": (2.0 * H * I * rows, b * (H * I * E + rows * I) + 4.0 * rows * H),
         "gemm_bwd_dh_swiglu": (2.0 * H * I * rows,
                                b * (H * I * E + rows * H + 3 * rows * I)
-                               + 4.0 * (2 * rows * I + rows)),
+                               + 2 * uv * rows * I + 4.0 * rows),
         "gemm_bwd_dx": (4.0 * H * I * rows, b * (2 * H * I * E + 2 * rows * I) + 4.0 * rows * H),
         "gemm_bwd_dw_down": (2.0 * H * I * rows, b * (rows * I + rows * H) + 4.0 * H * I * E),
         "gemm_bwd_dw_upgate": (4.0 * H * I * rows,
                                b * (rows * H + 2 * rows * I) + 4.0 * 2 * H * I * E),
         # the routed forward in one launch: weights once, x rows, U and V saved, y written
         "fwd_megakernel": (6.0 * H * I * rows,
-                           b * 3 * H * I * E + 2.0 * rows * H + 8.0 * rows * I + 4.0 * T * H),
+                           b * 3 * H * I * E + 2.0 * rows * H + 2 * uv * rows * I + 4.0 * T * H),
     }
     return tbl.get(name)
 
