@@ -855,14 +855,16 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   st.drain();
 }
 
-// One instantiation per mode: with the mode a compile-time constant the compiler keeps
-// only that mode's producer, MMA and epilogue code (a smaller instruction footprint).
-template <bool MX, int MODE>
+// One instantiation per mode (and, for the dW modes, per hi/lo split): with both
+// compile-time constants the compiler keeps only that launch's producer, MMA and epilogue
+// code (a smaller instruction footprint, a straight-line MMA issue).
+template <bool MX, int MODE, int SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p_in) {
   using C = Cfg<MX>;
   Params p = p_in;
   p.mode = MODE;
+  p.split = SPLIT;
   constexpr int STAGES = C::STAGES;   // barrier slots; the launch uses p.stages of them
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1643,15 +1645,18 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
 using GemmKernel = void (*)(const Maps, const Params);
 
 template <bool MX>
-GemmKernel gemm_kernel_for(int mode) {
+GemmKernel gemm_kernel_for(int mode, int split) {
   switch (mode) {
-    case kFwdUpGate: return grouped_gemm_kernel<MX, kFwdUpGate>;
-    case kFwdDown: return grouped_gemm_kernel<MX, kFwdDown>;
-    case kBwdDH: return grouped_gemm_kernel<MX, kBwdDH>;
-    case kBwdDX: return grouped_gemm_kernel<MX, kBwdDX>;
-    case kBwdDWDown: return grouped_gemm_kernel<MX, kBwdDWDown>;
-    case kBwdDWUpGate: return grouped_gemm_kernel<MX, kBwdDWUpGate>;
-    case kRouter: return grouped_gemm_kernel<MX, kRouter>;
+    case kFwdUpGate: return grouped_gemm_kernel<MX, kFwdUpGate, 0>;
+    case kFwdDown: return grouped_gemm_kernel<MX, kFwdDown, 0>;
+    case kBwdDH: return grouped_gemm_kernel<MX, kBwdDH, 0>;
+    case kBwdDX: return grouped_gemm_kernel<MX, kBwdDX, 0>;
+    case kBwdDWDown:
+      return split ? grouped_gemm_kernel<MX, kBwdDWDown, !MX> : grouped_gemm_kernel<MX, kBwdDWDown, 0>;
+    case kBwdDWUpGate:
+      return split ? grouped_gemm_kernel<MX, kBwdDWUpGate, !MX>
+                   : grouped_gemm_kernel<MX, kBwdDWUpGate, 0>;
+    case kRouter: return grouped_gemm_kernel<MX, kRouter, 0>;
     default: return nullptr;
   }
 }
@@ -1659,21 +1664,20 @@ GemmKernel gemm_kernel_for(int mode) {
 template <bool MX>
 cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   using C = Cfg<MX>;
-  static bool attr_set[8] = {};
+  static bool attr_set[8][2] = {};
   if (c.mode < 0 || c.mode >= 8) return cudaErrorInvalidValue;
-  const GemmKernel kern = gemm_kernel_for<MX>(c.mode);
-  if (!kern) return cudaErrorInvalidValue;
-  if (!attr_set[c.mode]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[c.mode] = true;
-  }
   Params p;
   Maps mp;
   int max_tiles = 0;
   cudaError_t e = build_call<MX>(c, p, mp, max_tiles);
   if (e != cudaSuccess) return e;
+  const GemmKernel kern = gemm_kernel_for<MX>(c.mode, p.split);
+  if (!kern) return cudaErrorInvalidValue;
+  if (!attr_set[c.mode][p.split ? 1 : 0]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[c.mode][p.split ? 1 : 0] = true;
+  }
   int grid = max_tiles < num_sms ? max_tiles : num_sms;
   if (grid < 1) grid = 1;
   kern<<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(mp, p);
