@@ -354,6 +354,43 @@ def test_shared_dw_lines_match_the_dense_oracle(rng, mode):
         assert np.allclose(L["dWs_gate"], g.dWs_gate[:, i], rtol=1e-12, atol=1e-12)
 
 
+def test_mxfp8_saved_uv_rounding_point(rng):
+    """In mxfp8 mode the forward keeps U, V for the backward as bf16 values, while h (and
+    so y) is formed from the unrounded U, V; bf16 mode keeps U, V unrounded."""
+    from oracle.numerics import bf16_round, mx_qdq, silu
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=24, H=64, I=64, E=3, k=2)
+    r = moe.route(x, Wr, 2)
+    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="mxfp8")
+    U, V = saved["U"], saved["V"]
+    assert np.array_equal(U, bf16_round(U)) and np.array_equal(V, bf16_round(V))
+    pl = saved["plan"]
+    e = int(np.argmax(pl.counts))
+    r0, r1 = pl.offsets[e], pl.offsets[e + 1]
+    A = mx_qdq(x[pl.table[r0:r1, 0]], 1)
+    Ue, Ve = A @ mx_qdq(Wu[e], 0), A @ mx_qdq(Wg[e], 0)
+    assert np.array_equal(U[r0:r1], bf16_round(Ue))          # rounded where they are saved
+    assert not np.array_equal(Ue, bf16_round(Ue))             # (so rounding changes them)
+    _, saved16 = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="bf16")
+    assert not np.array_equal(saved16["U"], bf16_round(saved16["U"]))
+    # h, the down GEMM's operand, comes from the unrounded U, V: y matches that, not the
+    # rounded values
+    h_exact = mx_qdq(silu(Ve) * Ue, 1)
+    h_saved = mx_qdq(silu(V[r0:r1]) * U[r0:r1], 1)
+    assert not np.array_equal(h_exact, h_saved)
+    ytok = np.zeros(x.shape[1])
+    t, j = pl.table[r0]
+    others = [jj for jj in range(2) if jj != j]
+    for jj in others:
+        ee = int(r.idx[t, jj])
+        rr = pl.inv[t, jj] - pl.offsets[ee]
+        s0 = pl.offsets[ee]
+        Ax = mx_qdq(x[pl.table[s0:pl.offsets[ee + 1], 0]], 1)
+        hh = mx_qdq(silu(Ax @ mx_qdq(Wg[ee], 0)) * (Ax @ mx_qdq(Wu[ee], 0)), 1)
+        ytok += r.gates[t, jj] * (hh[rr] @ mx_qdq(Wd[ee], 0))
+    ytok += r.gates[t, j] * (h_exact[0] @ mx_qdq(Wd[e], 0))
+    assert np.allclose(ytok, y[t], rtol=1e-12, atol=1e-12)
+
+
 @pytest.mark.parametrize("mode", ["bf16", "bf16_plain"])
 def test_weight_gradient_operand_rounding_point(rng, mode):
     """One token routed to one expert, x made of powers of two: dW_up[e][h][i] =
