@@ -63,10 +63,10 @@ def peaks():
 # A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
 NCU_TRAFFIC = {
     ("kimi_8192", "gemm_bwd_dw_upgate"): {
-        "bytes": 47.35e9, "rev": "4fbd616d3914860d",
+        "bytes": 47.35e9, "rev": "5748f4b0b1915006",
         "profile": "profiles/dram_traffic_kimi8192_bf16.md"},
     ("dsv3_imbalanced", "gemm_bwd_dw_upgate_mxfp8"): {
-        "bytes": 31.90e9, "rev": "4fbd616d3914860d",
+        "bytes": 31.98e9, "rev": "5748f4b0b1915006",
         "profile": "profiles/dram_traffic_dsv3_mxfp8.md"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",

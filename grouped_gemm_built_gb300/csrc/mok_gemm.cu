@@ -3,15 +3,16 @@
 // Expert FFN (sebask.de MoK article, intro: up, gate and down projection; stamatios.com,
 // "Outras caracteristicas": SwiGLU, router-weight gradient fused into the SwiGLU
 // backward, MXFP8 with a BF16 shared expert). One persistent, warp-specialised kernel
-// serves every GEMM of the layer:
+// template serves every GEMM of the layer, instantiated per mode (and, for the dW modes,
+// per hi/lo split) so that each launch carries only its own code:
 //
 //   warp 0      TMA producer: one lane streams A/B tiles (and, in MXFP8, their scale
 //               atoms) into a ring of shared-memory stages (128-byte swizzle);
 //   warp 1      MMA issuer: allocates 512 TMEM columns and issues tcgen05.mma
 //               (M=128, N=256) from one lane; BF16: kind::f16, K=16 per instruction, two
 //               256-column accumulators; MXFP8: kind::mxf8f6f4.block_scale, K=32 per
-//               instruction, one accumulator plus per-stage scale columns filled by
-//               tcgen05.cp;
+//               instruction, one 256-column accumulator (dH: two of 128 columns) plus
+//               per-stage scale columns filled by tcgen05.cp;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output row), run
 //               the mode's fused math, stage 32-row boxes in shared memory and store them
 //               with TMA; with two accumulators the next tile's MMAs overlap this epilogue.
