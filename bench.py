@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +45,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-experts", type=int, default=4)
+    ap.add_argument("--clocks-csv", default="",
+                    help="keep nvidia-smi's clock samples in this file (default: a temporary "
+                         "file); {gpu} is replaced by the GPU index")
     return ap.parse_args()
 
 
@@ -98,23 +102,26 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, path=""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = (path.replace("{gpu}", str(gpu_index)) if path else
+                     os.path.join(tempfile.gettempdir(), f"mok_bench_clocks_gpu{gpu_index}.csv"))
 
     def start(self):
         """Start sampling and wait for the first sample: nvidia-smi's start-up (NVML
         initialisation) can stall CUDA calls of this process for seconds, so it must be
         over before anything is timed."""
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(self.path) or ".", exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
+            if getattr(self, "f", None) is not None:
+                self.f.close()
             self.proc = None
             return
         t0 = time.time()
@@ -129,6 +136,8 @@ class ClockSampler:
 
     def mark(self):
         """Only samples taken after this point count (the timed region)."""
+        if self.proc is None:
+            return
         self.f.flush()
         try:
             self.skip = sum(1 for _ in open(self.path))
@@ -288,7 +297,7 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    clk = ClockSampler(local)
+    clk = ClockSampler(local, args.clocks_csv)
     clk.start()
     for _ in range(max(args.warmup, 0)):
         step()
