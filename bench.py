@@ -44,7 +44,10 @@ def parse():
                     help="most SMs any kernel uses (0: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-experts", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="routed-expert time of the CPU oracle's one timed sample")
+    ap.add_argument("--ref-rows-per-step", type=int, default=1024,
+                    help="routed rows in each step of the reference arm (the oracle)")
     ap.add_argument("--clocks-csv", default="",
                     help="keep nvidia-smi's clock samples in this file (default: a temporary "
                          "file); {gpu} is replaced by the GPU index")
@@ -179,6 +182,20 @@ class ClockSampler:
 def workload_config(name):
     import moe_inputs as mi
     return mi.CONFIGS[name]
+
+
+def workload_json(cfg):
+    """The workload keys of the JSON line, the same for both arms."""
+    wb = 1.0 if cfg.precision == "mxfp8" else 2.0
+    weights_gb = 3.0 * cfg.H * cfg.I * cfg.E * wb / 1e9
+    return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} "
+                        f"shared_I={cfg.shared_I} {cfg.precision} "
+                        + ("fwd+bwd" if cfg.backward else "fwd"),
+            "step": "plan + forward" + (" + backward" if cfg.backward else ""),
+            "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k,
+            "shared_I": cfg.shared_I, "precision": cfg.precision,
+            "l2": (f"inputs larger than L2 (expert weights {weights_gb:.3g} GB), no flush"
+                   if weights_gb * 1e9 > 129e6 else "inputs smaller than L2, no flush")}
 
 
 def algorithmic(cfg):
@@ -463,21 +480,15 @@ def run_gpu(args):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline(cfg, args.cpu_sample_experts)
+            cpu = cpu_baseline(cfg, args.cpu_seconds)
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} "
-                                   f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} "
-                                   + ("fwd+bwd" if cfg.backward else "fwd"),
-                       "step": "plan + forward" + (" + backward" if cfg.backward else ""),
-                       "macrobatches": L.sizes.macrobatches, "ring_slots": L.sizes.ring_slots, "T": cfg.T, "H": cfg.H, "I": cfg.I,
-                       "E": cfg.E, "k": cfg.k, "shared_I": cfg.shared_I,
-                       "precision": cfg.precision, "fwd_path": args.fwd_path,
-                       "l2": "inputs larger than L2 (expert weights 34 GB), no flush",
-                       "parallelism": f"replicas x{world}"},
+            "config": dict(workload_json(cfg),
+                           macrobatches=L.sizes.macrobatches, ring_slots=L.sizes.ring_slots,
+                           fwd_path=args.fwd_path, parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
             "roofline": roofline, "layer_roofline": layer_roofline,
             "kernels": per_kernel, "gemm_tc": gemm_tc,
@@ -490,84 +501,158 @@ def run_gpu(args):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def cpu_baseline(cfg, n_experts=4, seed=0):
-    """Time the fp64 oracle on a bounded sample of the workload and extrapolate to the
-    whole layer: router over all T tokens, n_experts routed experts (fwd + bwd over the
-    rows the router sends them), the shared expert over T/64 tokens."""
-    import numpy as np
+class OracleStep:
+    """The layer step (router, schedule, routed and shared experts: forward, and backward
+    where the workload has one) run by the fp64 oracle on the host cores, on a bounded
+    sample: the router and the schedule over all T tokens, some routed experts over the
+    rows the router sends them, the shared expert over T/64 tokens. The time is extrapolated to the whole
+    step by rows. Inputs are drawn once; every sampled expert uses the same drawn weights
+    (the oracle's time does not depend on their values)."""
 
-    from oracle import moe
+    def __init__(self, cfg, seed=0):
+        import numpy as np
+        self.np = np
+        self.cfg = cfg
+        rng = np.random.default_rng(seed)
+        T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
+        self.x = rng.standard_normal((T, H), dtype=np.float32).astype(np.float64)
+        self.dY = rng.standard_normal((T, H), dtype=np.float32).astype(np.float64)
+        self.Wr = rng.normal(0, cfg.wr_std, (H, E)) if cfg.router else None
+        self.bias = None
+        if cfg.router and cfg.bias_experts:
+            self.bias = np.zeros(E)
+            self.bias[list(cfg.bias_experts)] = cfg.bias_value
+        if not cfg.router:
+            # caller-supplied routing with the workload's expert loads (Zipf counts)
+            import moe_inputs as mi
+            counts = (mi.zipf_counts(T * k, E, cfg.zipf_s) if cfg.zipf_s > 0
+                      else [T * k // E] * E)
+            labels = np.repeat(np.arange(E), counts)
+            self.idx = rng.permutation(np.resize(labels, T * k)).reshape(T, k)
+            u = rng.uniform(size=(T, k))
+            self.gates = u / u.sum(axis=1, keepdims=True)
+        self.precision = cfg.precision
+        w = lambda *shape: rng.standard_normal(shape, dtype=np.float32).astype(np.float64) \
+            * cfg.w_std
+        self.W = (w(1, H, I), w(1, H, I), w(1, I, H))
+        self.Ts = max(1, T // 64)
+        self.shared = (w(H, Is), w(H, Is), w(Is, H)) if Is else None
 
-    rng = np.random.default_rng(seed)
-    T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
-    cores = os.cpu_count()
-    x = rng.standard_normal((T, H)).astype(np.float32).astype(np.float64)
-    t0 = time.perf_counter()
-    if cfg.router:
-        Wr = rng.normal(0, cfg.wr_std, (H, E))
-        r = moe.route(x, Wr, k)
-        idx, gates = r.idx, r.gates
-    else:
-        idx = rng.integers(0, E, (T, k))
-        gates = np.full((T, k), 1.0 / k)
-    pl = moe.plan(idx, E)
-    t_route = time.perf_counter() - t0
-    t_exp = 0.0
-    rows_done = 0
-    for e in range(min(n_experts, E)):
-        r0, r1 = pl.offsets[e], pl.offsets[e + 1]
-        n = r1 - r0
-        if n == 0:
-            continue
-        sel = pl.table[r0:r1]
-        Wu = rng.normal(0, cfg.w_std, (1, H, I))
-        Wg = rng.normal(0, cfg.w_std, (1, H, I))
-        Wd = rng.normal(0, cfg.w_std, (1, I, H))
-        xs = x[sel[:, 0]]
-        sub_idx = np.zeros((n, 1), np.int64)
-        sub_g = gates[sel[:, 0], sel[:, 1]][:, None]
-        dY = rng.standard_normal((n, H))
-        t1 = time.perf_counter()
-        y, saved = moe.forward(xs, sub_idx, sub_g, Wu, Wg, Wd, precision="bf16")
-        moe.backward(xs, sub_idx, sub_g, Wu, Wg, Wd, saved, dY, precision="bf16")
-        t_exp += time.perf_counter() - t1
-        rows_done += n
-    t_shared = 0.0
-    Ts = max(1, T // 64)
-    if Is:
-        sh = (rng.normal(0, cfg.w_std, (H, Is)), rng.normal(0, cfg.w_std, (H, Is)),
-              rng.normal(0, cfg.w_std, (Is, H)))
-        xs = x[:Ts]
-        dY = rng.standard_normal((Ts, H))
-        t1 = time.perf_counter()
-        O, ss = moe.shared_forward(xs, *sh, "bf16")
-        moe.shared_backward(xs, *sh, ss, dY, "bf16")
-        t_shared = time.perf_counter() - t1
-    total = t_route + (t_exp / max(rows_done, 1)) * T * k + t_shared * (T / Ts)
-    return {"value": round(T / total, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"router+schedule over all {T} tokens; {min(n_experts, E)} of {E} routed "
-                      f"experts fwd+bwd ({rows_done} rows) scaled to {T * k} rows; shared "
-                      f"expert over {Ts} tokens scaled to {T}; fp64 NumPy, bf16 rounding model",
-            "seconds_measured": round(t_route + t_exp + t_shared, 2),
-            "seconds_extrapolated": round(total, 2)}
+    def run(self, first, max_rows=None, max_seconds=None):
+        """Time one sample: routed experts first, first+1, ... (mod E), up to ``max_rows``
+        rows or ``max_seconds`` of expert time, at least one non-empty expert and at most
+        all E. Returns the measured and extrapolated seconds and where the next sample
+        starts."""
+        from oracle import moe
+        np, cfg = self.np, self.cfg
+        T, E, k = cfg.T, cfg.E, cfg.k
+        t0 = time.perf_counter()
+        if cfg.router:
+            r = moe.route(self.x, self.Wr, k, self.bias)
+            idx, gates = r.idx, r.gates
+        else:
+            idx, gates = self.idx, self.gates
+        pl = moe.plan(idx, E)
+        t_route = time.perf_counter() - t0
+        t_exp, rows, n_exp, e = 0.0, 0, 0, first
+        for step in range(E):
+            if n_exp and ((max_rows is not None and rows >= max_rows) or
+                          (max_seconds is not None and t_exp >= max_seconds)):
+                break
+            e = (first + step) % E
+            r0, r1 = pl.offsets[e], pl.offsets[e + 1]
+            n = int(r1 - r0)
+            if n == 0:
+                continue
+            sel = pl.table[r0:r1]
+            xs, dYs = self.x[sel[:, 0]], self.dY[sel[:, 0]]
+            sub_idx = np.zeros((n, 1), np.int64)
+            sub_g = gates[sel[:, 0], sel[:, 1]][:, None]
+            t1 = time.perf_counter()
+            _, saved = moe.forward(xs, sub_idx, sub_g, *self.W, precision=self.precision)
+            if cfg.backward:
+                moe.backward(xs, sub_idx, sub_g, *self.W, saved, dYs,
+                             precision=self.precision)
+            t_exp += time.perf_counter() - t1
+            rows += n
+            n_exp += 1
+        t_shared = 0.0
+        if self.shared is not None:
+            xs, dYs = self.x[:self.Ts], self.dY[:self.Ts]
+            t1 = time.perf_counter()
+            _, ss = moe.shared_forward(xs, *self.shared, self.precision)
+            if cfg.backward:
+                moe.shared_backward(xs, *self.shared, ss, dYs, self.precision)
+            t_shared = time.perf_counter() - t1
+        total = t_route + (t_exp / max(rows, 1)) * T * k + t_shared * (T / self.Ts)
+        return {"measured": t_route + t_exp + t_shared, "extrapolated": total,
+                "experts": n_exp, "rows": rows, "next": (e + 1) % E}
+
+    def describe(self, n_experts, rows):
+        cfg = self.cfg
+        passes = "fwd+bwd" if cfg.backward else "fwd"
+        head = (f"router+schedule over all {cfg.T} tokens" if cfg.router else
+                f"schedule over all {cfg.T} tokens (routing supplied)")
+        shared = (f"; shared expert over {self.Ts} tokens scaled to {cfg.T}"
+                  if self.shared is not None else "")
+        return (f"{head}; {n_experts} of {cfg.E} routed experts {passes} ({rows} rows) "
+                f"scaled to {cfg.T * cfg.k} rows{shared}; fp64 NumPy, "
+                f"{self.precision} rounding model")
+
+
+def cpu_baseline(cfg, seconds=10.0, seed=0):
+    """The oracle on one bounded sample of the workload (routed experts in index order
+    until about ``seconds`` of expert time), extrapolated to the whole step, in tokens per
+    second."""
+    step = OracleStep(cfg, seed)
+    r = step.run(0, max_seconds=seconds)
+    return {"value": round(cfg.T / r["extrapolated"], 3), "unit": "tokens/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": step.describe(r["experts"], r["rows"]),
+            "seconds_measured": round(r["measured"], 2),
+            "seconds_extrapolated": round(r["extrapolated"], 2)}
 
 
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on the host cores. W untimed warm-up
+    steps, then K timed steps; every step is one bounded sample (the router and schedule
+    over all tokens, routed experts taken in turn up to ``--ref-rows-per-step`` rows, the
+    shared-expert slice), extrapolated to the whole step. Rank 0 alone runs it."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     cfg = workload_config(args.workload)
-    cpu = cpu_baseline(cfg, args.cpu_sample_experts)
+    step = OracleStep(cfg)
+    nxt = 0
+
+    def one():
+        nonlocal nxt
+        r = step.run(nxt, max_rows=args.ref_rows_per_step)
+        nxt = r["next"]
+        return r
+
+    for _ in range(max(args.warmup, 0)):
+        one()
+    K = max(args.steps, 1)
+    runs = [one() for _ in range(K)]
+    ext = sum(r["extrapolated"] for r in runs)
+    value = round(cfg.T * K / ext, 3)
+    rows = sum(r["rows"] for r in runs)
+    cpu = {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"each of {K} steps: " +
+                     step.describe(round(sum(r["experts"] for r in runs) / K, 1), rows // K) +
+                     " (experts taken in turn; mean per step)",
+           "seconds_measured": round(sum(r["measured"] for r in runs), 2),
+           "seconds_extrapolated": round(ext, 2)}
     line = {
-        "impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "tokens/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * cfg.T / cpu["value"], 3), "higher_is_better": True,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * ext / K, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} "
-                               f"k={cfg.k} shared_I={cfg.shared_I} {cfg.precision} fwd+bwd",
-                   "step": "plan + forward + backward (CPU oracle, bounded sample)"},
+        "config": dict(workload_json(cfg), parallelism="replicas x1",
+                       oracle="fp64 NumPy on the host cores, a bounded sample per step"),
         "cpu_baseline": cpu,
-        "e2e": {"value": cpu["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

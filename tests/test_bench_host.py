@@ -61,3 +61,40 @@ def test_clock_sampler_without_nvidia_smi_reports_unsampled(tmp_path, monkeypatc
     clk.start()
     clk.mark()
     assert clk.stop() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+
+def test_oracle_step_takes_experts_in_turn_up_to_the_row_bound():
+    import moe_inputs as mi
+    cfg = mi.CONFIGS["tiny"]                       # 8 experts, 512 routed rows
+    step = bench.OracleStep(cfg)
+    r = step.run(6, max_rows=100)
+    assert r["rows"] >= 100 and r["experts"] >= 1
+    assert r["experts"] < cfg.E
+    assert r["next"] == (6 + r["experts"]) % cfg.E   # every tiny expert has rows; wraps at E
+    whole = step.run(0)                            # no bound: every expert once
+    assert whole["rows"] == cfg.T * cfg.k
+    assert whole["experts"] == cfg.E and whole["next"] == 0
+    assert whole["extrapolated"] >= whole["measured"] * 0.999
+
+
+def test_reference_arm_line():
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+                        "--steps", "4", "--warmup", "3"], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 4 and d["warmup"] == 3
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    import moe_inputs as mi
+    want = bench.workload_json(mi.CONFIGS["tiny"])
+    assert {k: d["config"][k] for k in want} == want     # the GPU arm's workload keys
