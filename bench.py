@@ -33,7 +33,7 @@ METRIC = "MoE layer tokens/sec fwd & bwd (BF16, MXFP8) on 1 GB300; grouped-GEMM 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="kimi_8192")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
