@@ -133,3 +133,116 @@ def test_wait_timeout_and_test_hook_are_host_settings():
     mok.mok_test_withhold_signal(ctx, True)
     mok.mok_test_withhold_signal(ctx, False)
     mok.mok_destroy(ctx)
+
+
+# ----------------------------------------------------------------- argument checks of the calls
+# Every case below is rejected before the call touches a device: the checks run first and
+# return a status, so fake (never dereferenced) addresses are enough.
+A = 1 << 20                                   # a fake, 256-byte aligned address
+
+
+def _sched():
+    return mok.MokSched(*([A] * 7))
+
+
+def _weights(shared=False, mx=False):
+    return mok.MokWeights(A, A, A, *((A, A, A) if shared else (None, None, None)),
+                          A if mx else None)
+
+
+def _grads(router=True, shared=False):
+    return mok.MokGrads(A, A, A, A, A if router else None,
+                        *((A, A, A) if shared else (None, None, None)))
+
+
+def _status(fn, *args):
+    with pytest.raises(mok.MokError) as ei:
+        fn(*args)
+    return ei.value.status
+
+
+def test_fwd_rejects_bad_arguments():
+    ctx = mok.mok_create(dims())
+    S, W = _sched(), _weights()
+    fwd = mok.mok_moe_fwd
+    assert _status(fwd, ctx, S, A, mok.MokWeights(None, A, A), A, A, A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # missing W_up
+    assert _status(fwd, ctx, S, A + 8, W, A, A, A, None) == mok.MOK_ERR_INVALID_ARG  # x
+    assert _status(fwd, ctx, S, A, W, None, A, A, None) == mok.MOK_ERR_INVALID_ARG   # y
+    assert _status(fwd, ctx, S, A, W, A, A, None, None) == mok.MOK_ERR_WORKSPACE
+    assert _status(fwd, ctx, S, A, W, A, A + 16, A, None) == mok.MOK_ERR_WORKSPACE  # saved
+    assert _status(fwd, ctx, mok.MokSched(*([A] * 6), None), A, W, A, A, A, None) == \
+        mok.MOK_ERR_WORKSPACE                                          # no aux
+    mok.mok_set_precision(ctx, mok.MOK_MXFP8)
+    assert _status(fwd, ctx, S, A, W, A, A, A, None) == mok.MOK_ERR_INVALID_ARG  # no mx
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(shared_I=128))
+    assert _status(fwd, ctx, S, A, W, A, A, A, None) == mok.MOK_ERR_INVALID_ARG  # no Ws_*
+    mok.mok_destroy(ctx)
+
+
+def test_bwd_rejects_bad_arguments():
+    ctx = mok.mok_create(dims())
+    S, W, G = _sched(), _weights(), _grads()
+    bwd = mok.mok_moe_bwd
+    assert _status(bwd, ctx, S, A, None, W, A, A, A, G, A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # router needs Wr
+    assert _status(bwd, ctx, S, A, A, W, A, A, A, _grads(router=False), A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # and dWr
+    assert _status(bwd, ctx, S, A, A, W, A, None, A, G, A, None) == mok.MOK_ERR_INVALID_ARG
+    assert _status(bwd, ctx, S, A, A, W, A, A, A,
+                   mok.MokGrads(A, A, A, None, A, None, None, None), A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # dgates
+    assert _status(bwd, ctx, S, A, A, W, None, A, A, G, A, None) == mok.MOK_ERR_WORKSPACE
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(router=0))
+    assert _status(bwd, ctx, S, A, A, W, A, A, A, _grads(router=False), A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # Wr without a router
+    assert _status(bwd, ctx, S, A, None, W, A, A, A, G, A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # dWr without a router
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(shared_I=128))
+    assert _status(bwd, ctx, S, A, A, _weights(shared=True), A, A, A, G, A, None) == \
+        mok.MOK_ERR_INVALID_ARG                                        # shared grads
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(router=0, macrobatches=2))
+    assert mok.mok_get_sizes(ctx).macrobatches == 2
+    assert _status(bwd, ctx, S, A, None, W, A, A, A, _grads(router=False), A, None) == \
+        mok.MOK_ERR_UNSUPPORTED                                        # backward is M = 1
+    mok.mok_destroy(ctx)
+
+
+def test_plan_and_quantize_reject_bad_arguments():
+    ctx = mok.mok_create(dims())
+    S = _sched()
+    assert _status(mok.mok_plan, ctx, A, None, None, S, A, None) == mok.MOK_ERR_INVALID_ARG
+    assert _status(mok.mok_plan, ctx, A + 4, A, None, S, A, None) == mok.MOK_ERR_INVALID_ARG
+    assert _status(mok.mok_plan, ctx, A, A, None, S, A + 64, None) == mok.MOK_ERR_WORKSPACE
+    assert _status(mok.mok_quantize_weights_mxfp8, ctx, _weights(), A + 128, None) == \
+        mok.MOK_ERR_INVALID_ARG
+    assert _status(mok.mok_quantize_weights_mxfp8, ctx, mok.MokWeights(A, None, A), A,
+                   None) == mok.MOK_ERR_INVALID_ARG
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(router=0))
+    for x, Wr, b in ((A, None, None), (None, A, None), (None, None, A)):
+        assert _status(mok.mok_plan, ctx, x, Wr, b, S, A, None) == mok.MOK_ERR_INVALID_ARG
+    mok.mok_destroy(ctx)
+
+
+def _no_device():
+    import torch
+    return not torch.cuda.is_available() and not os.path.exists("/dev/nvidia0")
+
+
+@pytest.mark.skipif(not _no_device(), reason="only where no GPU exists: the call would launch")
+def test_valid_calls_without_a_device_return_cuda_error():
+    """With every argument valid, the calls get as far as the device and report that there
+    is none, without launching anything."""
+    ctx = mok.mok_create(dims())
+    S, W = _sched(), _weights()
+    assert _status(mok.mok_plan, ctx, A, A, None, S, A, None) == mok.MOK_ERR_CUDA
+    assert _status(mok.mok_moe_fwd, ctx, S, A, W, A, A, A, None) == mok.MOK_ERR_CUDA
+    assert _status(mok.mok_moe_bwd, ctx, S, A, A, W, A, A, A, _grads(), A, None) == \
+        mok.MOK_ERR_CUDA
+    assert _status(mok.mok_quantize_weights_mxfp8, ctx, W, A, None) == mok.MOK_ERR_CUDA
+    mok.mok_destroy(ctx)
