@@ -16,12 +16,35 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
 
 
+def _dev(t, name: str, dtype: torch.dtype, numel: int, optional: bool = False):
+    """The device address of a tensor handed to the library, after checking that it can
+    be one: a CUDA tensor (a host address would be dereferenced on the GPU), contiguous,
+    of ``dtype`` and ``numel`` elements. ``None`` passes where ``optional``."""
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    return t.data_ptr()
+
+
 class MoELayer:
     """One MoE SwiGLU layer of fixed dims on one CUDA device."""
 
     def __init__(self, T, H, I, E, k, shared_I=0, router=True, macrobatches=0, ring_bytes=0,
                  precision="bf16", device="cuda"):
         self.device = torch.device(device)
+        if self.device.type != "cuda":
+            raise ValueError(f"the layer's buffers live on a CUDA device, got {self.device}")
         self.dims = mok.MokDims(T=T, H=H, I=I, E=E, k=k, shared_I=shared_I,
                                 router=1 if router else 0, macrobatches=macrobatches,
                                 ring_bytes=ring_bytes)
@@ -73,32 +96,61 @@ class MoELayer:
     def _stream():
         return torch.cuda.current_stream().cuda_stream
 
+    def _routed_weights(self, W_up, W_gate, W_down):
+        bf, EHI = torch.bfloat16, self.E * self.H * self.I
+        return (_dev(W_up, "W_up", bf, EHI), _dev(W_gate, "W_gate", bf, EHI),
+                _dev(W_down, "W_down", bf, EHI))
+
     def weights(self, W_up, W_gate, W_down, Ws_up=None, Ws_gate=None, Ws_down=None, mx=None):
+        """The weight pointers for forward and backward: W_up, W_gate [E,H,I] and W_down
+        [E,I,H] bf16; the shared expert's Ws_up, Ws_gate [H,Is], Ws_down [Is,H] bf16 when
+        the layer has one; ``mx`` from ``quantize_weights`` for MXFP8."""
+        up, gate, down = self._routed_weights(W_up, W_gate, W_down)
+        sh = self.H * self.Is
+        opt = self.Is == 0
         self._w_keep = (W_up, W_gate, W_down, Ws_up, Ws_gate, Ws_down, mx)
-        return mok.MokWeights(W_up=_ptr(W_up), W_gate=_ptr(W_gate), W_down=_ptr(W_down),
-                              Ws_up=_ptr(Ws_up), Ws_gate=_ptr(Ws_gate), Ws_down=_ptr(Ws_down),
-                              mx=_ptr(mx))
+        return mok.MokWeights(
+            W_up=up, W_gate=gate, W_down=down,
+            Ws_up=_dev(Ws_up, "Ws_up", torch.bfloat16, sh, opt),
+            Ws_gate=_dev(Ws_gate, "Ws_gate", torch.bfloat16, sh, opt),
+            Ws_down=_dev(Ws_down, "Ws_down", torch.bfloat16, sh, opt),
+            mx=_dev(mx, "mx", torch.uint8, self.sizes.mx_weight_bytes, True))
 
     def quantize_weights(self, W_up, W_gate, W_down):
         """MXFP8 copies of the routed weights (library-private layout), as a uint8 tensor."""
+        up, gate, down = self._routed_weights(W_up, W_gate, W_down)
         mx = torch.empty(self.sizes.mx_weight_bytes, dtype=torch.uint8, device=self.device)
-        w = mok.MokWeights(W_up=W_up.data_ptr(), W_gate=W_gate.data_ptr(),
-                           W_down=W_down.data_ptr())
+        w = mok.MokWeights(W_up=up, W_gate=gate, W_down=down)
         mok.mok_quantize_weights_mxfp8(self.ctx, w, mx.data_ptr(), self._stream())
         return mx
 
     def plan(self, x=None, Wr=None, bias=None, topk_idx=None, gates=None):
+        """Routing and schedule. With the router: x [T,H] bf16, Wr [H,E] fp32, optional
+        bias [E] fp32. Without: the caller's topk_idx [T,k] and gates [T,k], copied into
+        the schedule's buffers."""
         if not self.router:
+            if x is not None or Wr is not None or bias is not None:
+                raise ValueError("a layer without a router takes topk_idx and gates only")
+            if topk_idx is None or gates is None:
+                raise ValueError("a layer without a router needs topk_idx and gates")
             self.topk_idx.copy_(topk_idx)
             self.gates.copy_(gates)
-        mok.mok_plan(self.ctx, _ptr(x), _ptr(Wr), _ptr(bias), self.sched,
-                     self.workspace.data_ptr(), self._stream())
+            px = pw = pb = None
+        else:
+            px = _dev(x, "x", torch.bfloat16, self.T * self.H)
+            pw = _dev(Wr, "Wr", torch.float32, self.H * self.E)
+            pb = _dev(bias, "bias", torch.float32, self.E, optional=True)
+        mok.mok_plan(self.ctx, px, pw, pb, self.sched, self.workspace.data_ptr(),
+                     self._stream())
 
     def forward(self, x, w: "mok.MokWeights", y=None):
+        """y [T,H] fp32 (allocated when not given) from x [T,H] bf16."""
+        px = _dev(x, "x", torch.bfloat16, self.T * self.H)
         if y is None:
             y = torch.empty((self.T, self.H), dtype=torch.float32, device=self.device)
-        mok.mok_moe_fwd(self.ctx, self.sched, x.data_ptr(), w, y.data_ptr(),
-                        self.saved.data_ptr(), self.workspace.data_ptr(), self._stream())
+        py = _dev(y, "y", torch.float32, self.T * self.H)
+        mok.mok_moe_fwd(self.ctx, self.sched, px, w, py, self.saved.data_ptr(),
+                        self.workspace.data_ptr(), self._stream())
         return y
 
     def alloc_grads(self):
@@ -122,14 +174,27 @@ class MoELayer:
         return g
 
     def backward(self, x, Wr, w: "mok.MokWeights", dY, grads=None):
+        """Gradients (fp32, the shapes of ``alloc_grads``, allocated when not given) from
+        x and dY [T,H] bf16; Wr [H,E] fp32 when the layer runs its router, else None."""
         g = grads if grads is not None else self.alloc_grads()
-        mg = mok.MokGrads(dW_up=_ptr(g["dW_up"]), dW_gate=_ptr(g["dW_gate"]),
-                          dW_down=_ptr(g["dW_down"]), dgates=_ptr(g["dgates"]),
-                          dWr=_ptr(g["dWr"]), dWs_up=_ptr(g["dWs_up"]),
-                          dWs_gate=_ptr(g["dWs_gate"]), dWs_down=_ptr(g["dWs_down"]))
-        mok.mok_moe_bwd(self.ctx, self.sched, x.data_ptr(), _ptr(Wr), w, self.saved.data_ptr(),
-                        dY.data_ptr(), g["dX"].data_ptr(), mg, self.workspace.data_ptr(),
-                        self._stream())
+        f32 = torch.float32
+        EHI, TH, sh = self.E * self.H * self.I, self.T * self.H, self.H * self.Is
+        no_sh = self.Is == 0
+        mg = mok.MokGrads(
+            dW_up=_dev(g["dW_up"], "dW_up", f32, EHI),
+            dW_gate=_dev(g["dW_gate"], "dW_gate", f32, EHI),
+            dW_down=_dev(g["dW_down"], "dW_down", f32, EHI),
+            dgates=_dev(g["dgates"], "dgates", f32, self.T * self.k),
+            dWr=_dev(g.get("dWr"), "dWr", f32, self.H * self.E, optional=True),
+            dWs_up=_dev(g.get("dWs_up"), "dWs_up", f32, sh, no_sh),
+            dWs_gate=_dev(g.get("dWs_gate"), "dWs_gate", f32, sh, no_sh),
+            dWs_down=_dev(g.get("dWs_down"), "dWs_down", f32, sh, no_sh))
+        px = _dev(x, "x", torch.bfloat16, TH)
+        pwr = _dev(Wr, "Wr", f32, self.H * self.E, optional=True)
+        pdy = _dev(dY, "dY", torch.bfloat16, TH)
+        pdx = _dev(g["dX"], "dX", f32, TH)
+        mok.mok_moe_bwd(self.ctx, self.sched, px, pwr, w, self.saved.data_ptr(), pdy, pdx, mg,
+                        self.workspace.data_ptr(), self._stream())
         return g
 
     def status(self) -> int:
