@@ -45,8 +45,9 @@ def _needs_build(objs_src, target):
     if not os.path.exists(target):
         return True
     t = os.path.getmtime(target)
+    inc = os.path.join(ROOT, "include")
     deps = list(objs_src) + [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    deps.append(os.path.join(ROOT, "include", "mok.h"))
+    deps += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
