@@ -415,3 +415,60 @@ def test_weight_gradient_operand_rounding_point(rng, mode):
         assert n_bf16 == I
     else:
         assert n_bf16 < I // 4
+
+
+def _one_token_one_expert(rng, H, c=0.5):
+    """x, dY bf16 values; W_up and W_down the identity, W_gate c times it (H = I): then
+    U = x, V = c x and D = dY exactly in every precision mode (MXFP8 blocks of an identity
+    row or column hold a single power of two)."""
+    from oracle.numerics import bf16_round
+    x = bf16_round(rng.normal(0, 1, (1, H)))
+    dY = bf16_round(rng.normal(0, 1, (1, H)))
+    eye = np.eye(H)[None]
+    return x, dY, eye, c * eye, eye
+
+
+@pytest.mark.parametrize("mode", ["fp64", "bf16", "mxfp8"])
+def test_down_gemm_operand_rounding_point(rng, mode):
+    """With W_down the identity, gate 1 and one slot, y is h itself, so it shows where h
+    is rounded: to bf16 in the bf16 mode (h is stored as bf16 for the down GEMM), to MXFP8
+    blocks of 32 along I in the mxfp8 mode, not at all in fp64."""
+    from oracle.numerics import bf16_round, mx_qdq, silu
+    H = 64
+    x, _, _, _, Wd = _one_token_one_expert(rng, H)
+    Wu = bf16_round(rng.normal(0, 0.2, (1, H, H)))
+    Wg = bf16_round(rng.normal(0, 0.2, (1, H, H)))
+    y, _ = moe.forward(x, np.zeros((1, 1), np.int64), np.ones((1, 1)), Wu, Wg, Wd,
+                       precision=mode)
+    if mode == "mxfp8":
+        A = mx_qdq(x, 1)
+        h = silu(A @ mx_qdq(Wg[0], 0)) * (A @ mx_qdq(Wu[0], 0))
+        want = mx_qdq(h, 1)
+    else:
+        h = silu(x @ Wg[0]) * (x @ Wu[0])
+        want = bf16_round(h) if mode == "bf16" else h
+    assert np.array_equal(y, want)
+    if mode != "fp64":
+        assert not np.array_equal(want, h)
+
+
+@pytest.mark.parametrize("mode", ["fp64", "bf16", "mxfp8"])
+def test_dx_gemm_operand_rounding_point(rng, mode):
+    """With W_up, W_down the identity and W_gate = identity / 2, gate 1 and one slot,
+    dX = du' + dv' / 2, where du', dv' are du = D silu(V) and dv = D U silu'(V) as the dX
+    GEMM reads them: bf16 in the bf16 mode, MXFP8 blocks of 32 along I in the mxfp8 mode,
+    unrounded in fp64."""
+    from oracle.numerics import bf16_round, dsilu, mx_qdq, silu
+    H, c = 64, 0.5
+    x, dY, Wu, Wg, Wd = _one_token_one_expert(rng, H, c)
+    idx, gates = np.zeros((1, 1), np.int64), np.ones((1, 1))
+    _, saved = moe.forward(x, idx, gates, Wu, Wg, Wd, precision=mode)
+    g = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY, precision=mode)
+    mx = mode == "mxfp8"
+    A, D = (mx_qdq(x, 1), mx_qdq(dY, 1)) if mx else (x, dY)
+    U, V = A, c * A
+    du, dv = D * silu(V), D * U * dsilu(V)
+    rd = {"fp64": lambda a: a, "bf16": bf16_round, "mxfp8": lambda a: mx_qdq(a, 1)}[mode]
+    assert np.array_equal(g.dX, rd(du) + c * rd(dv))
+    if mode != "fp64":
+        assert not np.array_equal(rd(du), du) and not np.array_equal(rd(dv), dv)
