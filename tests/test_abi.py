@@ -246,3 +246,33 @@ def test_valid_calls_without_a_device_return_cuda_error():
         mok.MOK_ERR_CUDA
     assert _status(mok.mok_quantize_weights_mxfp8, ctx, W, A, None) == mok.MOK_ERR_CUDA
     mok.mok_destroy(ctx)
+
+
+def test_a_plain_c_program_uses_the_abi(tmp_path):
+    """tests/abi_consumer.c includes the headers as C99 (-pedantic, warnings as errors),
+    links libmok.so and runs the host-side calls; its view of the sizes equals the
+    binding's."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(build.lib_path())
+    exe = str(tmp_path / "abi_consumer")
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+           "-I", os.path.join(root, "include"), os.path.join(root, "tests", "abi_consumer.c"),
+           "-L", libdir, "-lmok", f"-Wl,-rpath,{libdir}", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    out = dict(line.split(" ", 1) for line in r.stdout.splitlines())
+    assert out["failures"] == "0"
+    assert int(out["minibatch_148"]) == 2368
+    ctx = mok.mok_create(dims(T=300, H=256, I=256, E=12, k=3, shared_I=128))
+    s = mok.mok_get_sizes(ctx)
+    mok.mok_destroy(ctx)
+    want = [s.aux_bytes, s.workspace_bytes, s.saved_bytes, s.mx_weight_bytes,
+            s.padded_rows_max, s.macrobatches, s.ring_slots]
+    assert [int(v) for v in out["sizes"].split()] == want
