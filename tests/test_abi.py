@@ -276,3 +276,32 @@ def test_a_plain_c_program_uses_the_abi(tmp_path):
     want = [s.aux_bytes, s.workspace_bytes, s.saved_bytes, s.mx_weight_bytes,
             s.padded_rows_max, s.macrobatches, s.ring_slots]
     assert [int(v) for v in out["sizes"].split()] == want
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the built library every call raises at once."""
+    monkeypatch.setattr(mok, "_LIB", None)
+    monkeypatch.setattr(mok, "lib_path", lambda: str(tmp_path / "libmok.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        mok.mok_status_string(0)
+    with pytest.raises(RuntimeError, match="not built"):
+        mok.mok_create(dims())
+
+
+def test_product_path_never_imports_the_oracle():
+    """The library package and its binding import nothing from oracle/ (the oracle is
+    test infrastructure); checked on the source text of every module in the package."""
+    import ast
+    pkg = os.path.dirname(os.path.abspath(mok.__file__))
+    for name in sorted(os.listdir(pkg)):
+        if not name.endswith(".py"):
+            continue
+        tree = ast.parse(open(os.path.join(pkg, name)).read())
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Import):
+                mods = [a.name for a in node.names]
+            elif isinstance(node, ast.ImportFrom):
+                mods = [node.module or ""]
+            else:
+                continue
+            assert not any(m == "oracle" or m.startswith("oracle.") for m in mods), name
