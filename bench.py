@@ -247,6 +247,55 @@ def kernel_work(cfg, name, counts=None):
     return tbl.get(name)
 
 
+def method_work(cfg):
+    """(FLOPs, bytes) of every launch of one step of the per-step path, keyed by the
+    bench's kernel names: the grouped GEMMs as in ``kernel_work``; the shared expert's
+    GEMMs with the same formulas (one expert, every token, BF16); the router's logits;
+    dispatch and reverse dispatch (rows read as bf16, written in the GEMM operand format);
+    combine and reverse combine (fp32 rows read, fp32 token rows written); the router's
+    weight gradient. The launches with a few KB of traffic (top-k, scans, small
+    transposes) are left out."""
+    import dataclasses
+    T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
+    R = T * k
+    mx = cfg.precision == "mxfp8"
+    sfx = "_mxfp8" if mx else ""
+    b_op = 1.0 + 1.0 / 32 if mx else 2.0
+    fwd = ["gemm_fwd_upgate_swiglu", "gemm_fwd_down"]
+    bwd = ["gemm_bwd_dh_swiglu", "gemm_bwd_dx", "gemm_bwd_dw_upgate", "gemm_bwd_dw_down"]
+    names = fwd + (bwd if cfg.backward else [])
+    out = {n + sfx: kernel_work(cfg, n + sfx) for n in names}
+    if Is:
+        sh = dataclasses.replace(cfg, k=1, E=1, I=Is, precision="bf16")
+        for n in names:
+            out["shared_" + n[len("gemm_"):]] = kernel_work(sh, n)
+    if cfg.router:
+        out["router_logits"] = (2.0 * T * H * E * 3, 2.0 * T * H + 3 * 2.0 * H * E + 4.0 * T * E)
+    out["dispatch_gather"] = (0.0, 2.0 * R * H + b_op * R * H)
+    out["combine"] = (0.0, 4.0 * R * H + 4.0 * T * H + (4.0 * T * H if Is else 0.0))
+    if cfg.backward:
+        out["reverse_dispatch_gather"] = (0.0, 2.0 * R * H + b_op * R * H)
+        out["reverse_combine"] = (0.0, 4.0 * R * H + 4.0 * T * H + (4.0 * T * H if Is else 0.0))
+        if cfg.router:
+            out["router_dwr"] = (2.0 * T * H * k, 2.0 * T * H + 4.0 * H * E + 4.0 * T * k)
+    return out
+
+
+def method_roofline(cfg, pk, ms_step):
+    """The per-step path's own bound: every launch at its own roofline (its bytes at the
+    measured copy bandwidth or its FLOPs at the measured tensor peak of its dtype,
+    whichever is longer), launches one after another."""
+    t = 0.0
+    byts = flops = 0.0
+    for name, (f, b) in method_work(cfg).items():
+        tc = pk["bf16_tflops_sustained"] * (2.0 if name.endswith("_mxfp8") else 1.0)
+        t += max(f / (tc * 1e12), b / (pk["hbm_gbs"] * 1e9))
+        byts += b
+        flops += f
+    return {"ms_per_step_bound": round(t * 1e3, 3), "frac": round(t * 1e3 / ms_step, 4),
+            "bytes_gb": round(byts / 1e9, 2), "tflop": round(flops / 1e12, 2)}
+
+
 # ----------------------------------------------------------------------------- replicas
 def max_over_ranks(x, device):
     """x's maximum over the ranks of the default process group (x itself on one rank):
@@ -476,6 +525,10 @@ def run_gpu(args):
                       "frac": round(t_roof * 1e3 / ms_step, 4),
                       "bound": "hbm" if (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9) >
                       (f_fwd + f_bwd) / (lpk * 1e12) else "tensor"}
+    try:
+        method = method_roofline(cfg, pk, ms_step)
+    except Exception as exc:          # reporting only: never lose the line over it
+        method = {"error": repr(exc)}
 
     if rank == 0:
         cpu = None
@@ -491,6 +544,7 @@ def run_gpu(args):
                            fwd_path=args.fwd_path, parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
             "roofline": roofline, "layer_roofline": layer_roofline,
+            "method_roofline": method,
             "kernels": per_kernel, "gemm_tc": gemm_tc,
             "megakernel_phases_ms": phases or None,
             "e2e": e2e, "cpu_baseline": cpu,

@@ -98,3 +98,28 @@ def test_reference_arm_line():
     import moe_inputs as mi
     want = bench.workload_json(mi.CONFIGS["tiny"])
     assert {k: d["config"][k] for k in want} == want     # the GPU arm's workload keys
+
+
+def test_method_roofline_bounds_the_layer_roofline():
+    """The per-step path's own bound (every launch at its own roofline, one after another)
+    is at least the layer's compulsory bound, and its grouped-GEMM part is the per-kernel
+    algorithmic bytes (at the Kimi shape 147.4 GB, the sum of the DRAM-traffic profile's
+    algorithmic column)."""
+    import moe_inputs as mi
+    pk = {"hbm_gbs": 6789.6, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1720.0}
+    for name in ("kimi_8192", "kimi_2368", "dsv3_imbalanced", "ep64_slice", "mid", "tiny"):
+        cfg = mi.CONFIGS[name]
+        work = bench.method_work(cfg)
+        f_fwd, f_bwd, b_fwd, b_bwd = bench.algorithmic(cfg)
+        if not cfg.backward:
+            f_bwd = b_bwd = 0.0
+        m = bench.method_roofline(cfg, pk, 1.0)
+        tc = pk["bf16_tflops_sustained"] * (2.0 if cfg.precision == "mxfp8" else 1.0)
+        layer = max((f_fwd + f_bwd) / (tc * 1e12), (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
+        assert m["ms_per_step_bound"] >= layer * 1e3 * 0.999, name
+        assert m["bytes_gb"] * 1e9 >= (b_fwd + b_bwd) * 0.999, name
+        n_gemm = 6 if cfg.backward else 2
+        assert sum(1 for n in work if n.startswith("gemm_")) == n_gemm, name
+    kimi = bench.method_work(mi.CONFIGS["kimi_8192"])
+    gemm_gb = sum(b for n, (f, b) in kimi.items() if n.startswith("gemm_")) / 1e9
+    assert abs(gemm_gb - 147.4) < 0.35            # six entries rounded to 0.1 GB
