@@ -251,7 +251,8 @@ def method_work(cfg):
     """(FLOPs, bytes) of every launch of one step of the per-step path, keyed by the
     bench's kernel names: the grouped GEMMs as in ``kernel_work``; the shared expert's
     GEMMs with the same formulas (one expert, every token, BF16); the router's logits;
-    dispatch and reverse dispatch (rows read as bf16, written in the GEMM operand format);
+    dispatch and reverse dispatch (rows read as bf16, written in the GEMM operand format;
+    MXFP8 gathers x and dY once more, quantised along the rows, for the dW GEMMs);
     combine and reverse combine (fp32 rows read, fp32 token rows written); the router's
     weight gradient. The launches with a few KB of traffic (top-k, scans, small
     transposes) are left out."""
@@ -271,10 +272,14 @@ def method_work(cfg):
             out["shared_" + n[len("gemm_"):]] = kernel_work(sh, n)
     if cfg.router:
         out["router_logits"] = (2.0 * T * H * E * 3, 2.0 * T * H + 3 * 2.0 * H * E + 4.0 * T * E)
-    out["dispatch_gather"] = (0.0, 2.0 * R * H + b_op * R * H)
+    move = (0.0, 2.0 * R * H + b_op * R * H)          # bf16 rows in, operand rows out
+    out["dispatch_gather" + sfx] = move
     out["combine"] = (0.0, 4.0 * R * H + 4.0 * T * H + (4.0 * T * H if Is else 0.0))
     if cfg.backward:
-        out["reverse_dispatch_gather"] = (0.0, 2.0 * R * H + b_op * R * H)
+        out["reverse_dispatch_gather" + sfx] = move
+        if mx:   # the dW GEMMs' operands, quantised along the expert rows: x and dY again
+            out["replay_gather_rows_mxfp8"] = move
+            out["reverse_dispatch_gather_rows_mxfp8"] = move
         out["reverse_combine"] = (0.0, 4.0 * R * H + 4.0 * T * H + (4.0 * T * H if Is else 0.0))
         if cfg.router:
             out["router_dwr"] = (2.0 * T * H * k, 2.0 * T * H + 4.0 * H * E + 4.0 * T * k)
@@ -294,6 +299,23 @@ def method_roofline(cfg, pk, ms_step):
         flops += f
     return {"ms_per_step_bound": round(t * 1e3, 3), "frac": round(t * 1e3 / ms_step, 4),
             "bytes_gb": round(byts / 1e9, 2), "tflop": round(flops / 1e12, 2)}
+
+
+def data_movement(cfg, prof, pk):
+    """Achieved bandwidth of the launches that move rows rather than multiply (router
+    logits included): bytes from ``method_work`` over the launch's measured time, and its
+    fraction of the measured copy bandwidth."""
+    out = {}
+    for name, (f, b) in method_work(cfg).items():
+        if name.startswith(("gemm_", "shared_")) or name not in prof:
+            continue
+        c, t = prof[name]
+        if c == 0 or t <= 0:
+            continue
+        gbs = b / (t / c / 1e3) / 1e9
+        out[name] = {"gb": round(b / 1e9, 3), "ms": round(t / c, 4), "gb_per_s": round(gbs, 1),
+                     "frac_of_copy": round(gbs / pk["hbm_gbs"], 4)}
+    return out
 
 
 # ----------------------------------------------------------------------------- replicas
@@ -527,8 +549,9 @@ def run_gpu(args):
                       (f_fwd + f_bwd) / (lpk * 1e12) else "tensor"}
     try:
         method = method_roofline(cfg, pk, ms_step)
+        moves = data_movement(cfg, prof, pk)
     except Exception as exc:          # reporting only: never lose the line over it
-        method = {"error": repr(exc)}
+        method = moves = {"error": repr(exc)}
 
     if rank == 0:
         cpu = None
@@ -544,7 +567,7 @@ def run_gpu(args):
                            fwd_path=args.fwd_path, parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
             "roofline": roofline, "layer_roofline": layer_roofline,
-            "method_roofline": method,
+            "method_roofline": method, "data_movement": moves,
             "kernels": per_kernel, "gemm_tc": gemm_tc,
             "megakernel_phases_ms": phases or None,
             "e2e": e2e, "cpu_baseline": cpu,
