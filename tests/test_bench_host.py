@@ -123,3 +123,24 @@ def test_method_roofline_bounds_the_layer_roofline():
     kimi = bench.method_work(mi.CONFIGS["kimi_8192"])
     gemm_gb = sum(b for n, (f, b) in kimi.items() if n.startswith("gemm_")) / 1e9
     assert abs(gemm_gb - 147.4) < 0.35            # six entries rounded to 0.1 GB
+
+
+def test_data_movement_reads_the_profile_names():
+    """The row-moving launches are found under the names the library's profile records
+    use (BF16 and MXFP8), and their bandwidth is bytes over time per launch."""
+    import moe_inputs as mi
+    pk = {"hbm_gbs": 6789.6}
+    cfg = mi.CONFIGS["kimi_8192"]
+    prof = {"dispatch_gather": (10, 3.4), "combine": (10, 4.84), "gemm_fwd_down": (10, 24.3),
+            "topk_rank": (10, 0.4)}
+    got = bench.data_movement(cfg, prof, pk)
+    assert set(got) == {"dispatch_gather", "combine"}
+    R, H = cfg.T * cfg.k, cfg.H
+    assert got["dispatch_gather"]["gb"] == round(4.0 * R * H / 1e9, 3)
+    assert abs(got["dispatch_gather"]["gb_per_s"] - 4.0 * R * H / 0.34e-3 / 1e9) < 0.1
+    mx = bench.data_movement(mi.CONFIGS["dsv3_imbalanced"],
+                             {"dispatch_gather_mxfp8": (1, 0.45),
+                              "replay_gather_rows_mxfp8": (1, 0.6),
+                              "reverse_dispatch_gather_rows_mxfp8": (1, 0.6)}, pk)
+    assert set(mx) == {"dispatch_gather_mxfp8", "replay_gather_rows_mxfp8",
+                       "reverse_dispatch_gather_rows_mxfp8"}
