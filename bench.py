@@ -556,7 +556,10 @@ def run_gpu(args):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline(cfg, args.cpu_seconds)
+            try:
+                cpu = cpu_baseline(cfg, args.cpu_seconds)
+            except Exception as exc:   # a reported baseline only: keep the GPU line
+                cpu = {"error": repr(exc), "kind": "oracle"}
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
