@@ -99,3 +99,73 @@ def test_router_less_layer_takes_routing_only():
         L.plan(x=dev(16, 128))
     with pytest.raises(ValueError, match="needs topk_idx and gates"):
         L.plan(topk_idx=dev(16, 2, dtype=torch.int32))
+
+
+class _TorchOnDevice:
+    """torch, except that the tensors the layer allocates come back as device stand-ins."""
+
+    def __getattr__(self, name):
+        return getattr(torch, name)
+
+    @staticmethod
+    def empty(*shape, **kw):
+        kw.pop("device", None)
+        return torch.empty(*shape, **kw).as_subclass(_OnDevice)
+
+
+def _on_device(inp):
+    return {k: (v.as_subclass(_OnDevice) if isinstance(v, torch.Tensor) else v)
+            for k, v in inp.items()}
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_shared", "tiny_mx", "sparse", "router_less",
+                                  "single_expert"])
+def test_the_gpu_tests_call_pattern_passes_the_checks(monkeypatch, name):
+    """The call sequence of the GPU tests and the bench (plan, quantize_weights for MXFP8,
+    weights, forward, alloc_grads, backward), on the inputs ``moe_inputs`` makes for them,
+    passes every tensor check; the library calls are stubbed out."""
+    import moe_inputs as mi
+    cases = {
+        "tiny": mi.CONFIGS["tiny"],
+        "ragged_shared": mi.MoEConfig("ragged_shared", T=300, H=256, I=256, E=12, k=3,
+                                      shared_I=128),
+        "tiny_mx": mi.scaled(mi.CONFIGS["tiny"], name="tiny_mx", precision="mxfp8"),
+        "sparse": mi.MoEConfig("sparse", T=40, H=128, I=128, E=64, k=2),
+        "router_less": mi.MoEConfig("rl", T=200, H=256, I=128, E=6, k=8, router=False,
+                                    zipf_s=1.2),
+        "single_expert": mi.MoEConfig("one", T=64, H=128, I=128, E=1, k=1, shared_I=128),
+    }
+    cfg = cases[name]
+    calls = []
+    for fn in ("mok_plan", "mok_moe_fwd", "mok_moe_bwd", "mok_quantize_weights_mxfp8"):
+        monkeypatch.setattr(lay.mok, fn, lambda *a, fn=fn: calls.append(fn))
+    monkeypatch.setattr(lay, "torch", _TorchOnDevice())
+    L = lay.MoELayer.__new__(lay.MoELayer)
+    L.T, L.H, L.I, L.E, L.k, L.Is, L.router = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, \
+        cfg.shared_I, cfg.router
+    L.device, L.ctx = torch.device("cpu"), None
+
+    class _S:
+        mx_weight_bytes = 4096
+
+    L.sizes = _S()
+    L.topk_idx = torch.zeros((cfg.T, cfg.k), dtype=torch.int32)
+    L.gates = torch.zeros((cfg.T, cfg.k))
+    L.workspace = L.saved = torch.zeros(256, dtype=torch.uint8)
+    L.sched = None
+    L._stream = lambda: 0
+    d = _on_device(mi.make_inputs(cfg, seed=0, device="cpu", with_dy=True))
+    if cfg.router:
+        L.plan(x=d["x"], Wr=d["Wr"], bias=d["bias"])
+    else:
+        L.plan(topk_idx=d["topk_idx"], gates=d["gates"])
+    mx = L.quantize_weights(d["W_up"], d["W_gate"], d["W_down"]) \
+        if cfg.precision == "mxfp8" else None
+    w = L.weights(d["W_up"], d["W_gate"], d["W_down"], d["Ws_up"], d["Ws_gate"], d["Ws_down"],
+                  mx=mx)
+    y = L.forward(d["x"], w)
+    L.forward(d["x"], w, torch.empty((cfg.T, cfg.H)).as_subclass(_OnDevice))
+    g = L.backward(d["x"], d["Wr"] if cfg.router else None, w, d["dY"])
+    L.backward(d["x"], d["Wr"] if cfg.router else None, w, d["dY"], g)
+    assert y.shape == (cfg.T, cfg.H)
+    assert calls.count("mok_moe_bwd") == 2 and calls.count("mok_moe_fwd") == 2
