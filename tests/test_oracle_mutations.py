@@ -86,6 +86,13 @@ P = {
     "mx_axis": lambda: tn.test_mx_axis_and_error_bound(_rng()),
     "mx_rows": lambda: tn.test_mx_rows_padded_equals_explicit_zero_rows(_rng()),
     "silu": lambda: tn.test_silu_and_derivative(),
+    "dw_lines_bf16": lambda: tl.test_dw_lines_and_mx_token_forward_match_the_dense_oracle(
+        _rng(), "bf16"),
+    "dw_lines_plain": lambda: tl.test_dw_lines_and_mx_token_forward_match_the_dense_oracle(
+        _rng(), "bf16_plain"),
+    "shared_lines_plain": lambda: tl.test_shared_dw_lines_match_the_dense_oracle(
+        _rng(), "bf16_plain"),
+    "shared_lines_mx": lambda: tl.test_shared_dw_lines_match_the_dense_oracle(_rng(), "mxfp8"),
 }
 
 # (owner, function, original text, planted text, pins expected to catch it)
@@ -218,6 +225,43 @@ MISTAKES = {
         "dv = g * D * U * dsilu(V)", ["mx_bwd_eval"]),
     "MXFP8 dW lines quantise x along H, not the rows": (
         sampled, "dw_lines_mx", "XR = mx_qdq_rows_padded(X)", "XR = Xq", ["mx_bwd_eval"]),
+    # the rest of the oracle's functions
+    "router ignores the logit bias": (
+        moe, "route", "logits = logits + np.asarray(bias, np.float64)[None, :]",
+        "logits = logits", ["route_brute"]),
+    "MXFP8 operands left unquantised": (
+        moe.Precision, "op", "return mx_qdq(a, axis) if self.mx else a", "return a",
+        ["saved_uv", "down_mx"]),
+    "MXFP8 row operands left unquantised": (
+        moe.Precision, "op_rows", "return mx_qdq_rows_padded(a) if self.mx else a",
+        "return a", ["mx_bwd_eval"]),
+    "shared expert's h not rounded": (
+        moe, "shared_forward", "h = P.fwd_act(silu(V) * U, 1)", "h = silu(V) * U",
+        ["sampled"]),
+    "shared expert always in the routed experts' precision": (
+        moe, "shared_forward", 'P = Precision("fp64" if mode == "fp64" else "bf16")',
+        "P = Precision(mode)", ["shared_lines_mx"]),
+    "MX dequantisation with the wrong exponent bias": (
+        numerics, "mx_dequantize", "s.astype(np.int64) - 127", "s.astype(np.int64) - 126",
+        ["mx_axis"]),
+    "sampled router path with the wrong sign": (
+        sampled, "token_outputs", "dl = gates[t] * (dg - s)", "dl = gates[t] * (s - dg)",
+        ["sampled"]),
+    "sampled dW elements: dv without U": (
+        sampled, "dw_elements", "d = rnd(g * D * U * dsilu(V))", "d = rnd(g * D * dsilu(V))",
+        ["sampled"]),
+    "sampled dW lines: plain mode not rounded": (
+        sampled, "dw_lines", "rnd = bf16_round if plain else (lambda v: v)",
+        "rnd = (lambda v: v)", ["dw_lines_plain"]),
+    "sampled dW lines: dW_down without the gate": (
+        sampled, "dw_lines", "hg = rnd(g * silu(V) * U)", "hg = rnd(silu(V) * U)",
+        ["dw_lines_bf16"]),
+    "MXFP8 token forward: h unquantised": (
+        sampled, "token_forward_mx", "hq = mx_qdq((silu(V) * U)[None, :], 1)[0]",
+        "hq = silu(V) * U", ["dw_lines_bf16"]),
+    "shared dW lines: plain mode not rounded": (
+        sampled, "shared_dw_lines", "rnd = bf16_round if plain else (lambda v: v)",
+        "rnd = (lambda v: v)", ["shared_lines_plain"]),
 }
 
 
