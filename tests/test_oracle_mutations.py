@@ -262,7 +262,55 @@ MISTAKES = {
     "shared dW lines: plain mode not rounded": (
         sampled, "shared_dw_lines", "rnd = bf16_round if plain else (lambda v: v)",
         "rnd = (lambda v: v)", ["shared_lines_plain"]),
+    "dX GEMM operands left unrounded": (
+        moe.Precision, "dx_act", "return self.fwd_act(a, axis)", "return a", ["dx_bf16"]),
+    "floor(log2) one too high": (
+        numerics, "_floor_log2", "return e - 1", "return e", ["mx_448", "mx_pow2"]),
+    "sigmoid of -v": (
+        numerics, "sigmoid", "1.0 / (1.0 + np.exp(-v))", "1.0 / (1.0 + np.exp(v))",
+        ["silu"]),
+    "qdq dequantises along the last axis": (
+        numerics, "mx_qdq", "return mx_dequantize(c, s, axis)",
+        "return mx_dequantize(c, s, -1)", ["mx_axis"]),
+    "E4M3 decode off by one code": (
+        numerics, "e4m3_decode", "_E4M3[np.asarray(codes, dtype=np.uint8)]",
+        "_E4M3[np.asarray(codes, dtype=np.uint8) ^ 1]", ["mx_axis"]),
+    "expert rows lose their last row": (
+        sampled, "expert_rows", "plan.table[plan.offsets[e]:plan.offsets[e + 1]]",
+        "plan.table[plan.offsets[e]:plan.offsets[e + 1] - 1]", ["sampled", "dw_lines_bf16"]),
+    "MXFP8 forward weights: W_down along H": (
+        sampled, "mx_expert_weights", "mx_qdq(Wd, 0)", "mx_qdq(Wd, 1)", ["dw_lines_bf16"]),
+    "MXFP8 backward weights: W_down along I": (
+        sampled, "mx_expert_weights_bwd", "mx_qdq(Wd, 1)", "mx_qdq(Wd, 0)", ["mx_bwd_eval"]),
+    # the pins' own references
+    "brute-force token forward drops the gate": (
+        moe, "token_forward_bruteforce", "y += g * ((silu(v) * u) @ W_down[e])",
+        "y += (silu(v) * u) @ W_down[e]", ["fwd_brute"]),
+    "finite-difference loss without renormalised gates": (
+        moe, "layer_loss", "gates = pS / pS.sum(axis=1, keepdims=True)", "gates = pS",
+        ["fd"]),
+    "loop-built schedule in descending token order": (
+        moe, "plan_loops", "rows[idx[t][j]].append((t, j))",
+        "rows[idx[t][j]].insert(0, (t, j))", ["plan_loops"]),
 }
+
+
+def test_every_oracle_function_has_a_planted_mistake():
+    """No function of the oracle is left out of the planted mistakes (the E4M3 table is
+    computed once at import and pinned by its known values and round trip)."""
+    planted = {(getattr(owner, "__name__", ""), fn) for owner, fn, *_ in MISTAKES.values()}
+    missing = []
+    for mod in (moe, numerics, sampled):
+        for name, obj in vars(mod).items():
+            if inspect.isfunction(obj) and obj.__module__ == mod.__name__:
+                if (mod.__name__, name) not in planted and name != "e4m3_decode_table":
+                    missing.append(f"{mod.__name__}.{name}")
+            if inspect.isclass(obj) and obj.__module__ == mod.__name__:
+                for mname, m in vars(obj).items():
+                    if inspect.isfunction(m) and not mname.startswith("__") and \
+                            (obj.__name__, mname) not in planted:
+                        missing.append(f"{obj.__name__}.{mname}")
+    assert not missing, missing
 
 
 def test_pins_pass_on_the_oracle_as_it_is():
