@@ -42,6 +42,13 @@ def parse():
                     help="gather/combine SMs of the forward megakernel (0: automatic)")
     ap.add_argument("--sm-limit", type=int, default=0,
                     help="most SMs any kernel uses (0: all)")
+    ap.add_argument("--out", default="", choices=["", "bf16", "fp32"],
+                    help="result type of y, dX and the weight gradients (default: the "
+                         "workload's, bf16)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the sub-records (fp32 results, forward megakernel, MXFP8)")
+    ap.add_argument("--sub-steps", type=int, default=10,
+                    help="timed steps of each sub-record")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -66,16 +73,10 @@ def peaks():
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a kernel, from
-# one ncu capture, scaled to the workload's launch as the named profile summary states.
-# A figure is valid only for the GEMM source revision it was taken on (gemm_source_rev).
-NCU_TRAFFIC = {
-    ("kimi_8192", "gemm_bwd_dw_upgate"): {
-        "bytes": 47.35e9, "rev": "5748f4b0b1915006",
-        "profile": "profiles/dram_traffic_kimi8192_bf16.md"},
-    ("dsv3_imbalanced", "gemm_bwd_dw_upgate_mxfp8"): {
-        "bytes": 31.98e9, "rev": "5748f4b0b1915006",
-        "profile": "profiles/dram_traffic_dsv3_mxfp8.md"},
-}
+# one ncu capture, scaled to the workload's launch as the profile summary of that kernel
+# and workload states. A figure is valid only for the GEMM source revision it was taken on
+# (gemm_source_rev) and the result type it was taken with.
+NCU_TRAFFIC = {}
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
                 "grouped_gemm_built_gb300/csrc/mok_internal.h")
@@ -92,8 +93,8 @@ def gemm_source_rev():
     return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
-def ncu_traffic(workload, kernel):
-    rec = NCU_TRAFFIC.get((workload, kernel))
+def ncu_traffic(workload, kernel, out="bf16"):
+    rec = NCU_TRAFFIC.get((workload, kernel, out))
     if rec is None or rec["rev"] != gemm_source_rev():
         return None
     return rec["bytes"]
@@ -198,23 +199,33 @@ def workload_json(cfg):
                    if weights_gb * 1e9 > 129e6 else "inputs smaller than L2, no flush")}
 
 
+def result_bytes(cfg):
+    """Bytes of one result element: y, dX, the weight gradients, and the expert output rows
+    and routed dX rows the combines read (bf16 or fp32, as the layer was asked)."""
+    return 2.0 if cfg.out == "bf16" else 4.0
+
+
 def algorithmic(cfg):
-    """Algorithmic FLOPs and bytes of one step (plan + forward + backward).
+    """Algorithmic FLOPs and compulsory HBM bytes of one step (plan + forward + backward).
 
     FLOPs: per routed row 6*H*I forward (up, gate, down), 12*H*I backward (dX, dW);
     shared expert the same per token; router 2*H*E per token forward, backward dWr and
-    dX router path 4*H*k per token. Bytes: compulsory HBM traffic (inputs, weights read
-    once per pass, outputs, weight gradients written once)."""
+    dX router path 4*H*k per token. Bytes, forward: the weights once (MXFP8: 1 + 1/32
+    bytes per routed weight; the shared expert stays bf16), x in, y out, the router
+    weights; backward: the weights once more, the weight gradients written once, x and dY
+    in, dX out, the saved U, V read once as bf16 values, Wr in and dWr out. y, dX and the
+    weight gradients count at the result type's size (bf16 by default)."""
     T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
     R = T * k
     f_fwd = 6.0 * H * I * R + 6.0 * H * Is * T + 2.0 * H * E * T
     f_bwd = 12.0 * H * I * R + 12.0 * H * Is * T + 4.0 * H * k * T
-    wb = 1.0 if cfg.precision == "mxfp8" else 2.0      # weight element bytes read
+    wb = 1.0 + 1.0 / 32 if cfg.precision == "mxfp8" else 2.0   # routed weight bytes read
+    ob = result_bytes(cfg)
+    w_read = wb * 3.0 * H * I * E + 2.0 * 3.0 * H * Is
     n_w = 3.0 * H * I * E + 3.0 * H * Is
-    # forward: weights, x (bf16) in, y (fp32) out, router weights
-    b_fwd = wb * n_w + 2.0 * T * H + 4.0 * T * H + 4.0 * H * E
-    # backward: weights in, fp32 weight gradients out, x and dY in, dX (fp32) out, Wr, dWr
-    b_bwd = wb * n_w + 4.0 * n_w + 2.0 * 2 * T * H + 4.0 * T * H + 4.0 * H * E * 2
+    b_fwd = w_read + 2.0 * T * H + ob * T * H + 4.0 * H * E
+    b_bwd = w_read + ob * n_w + 2.0 * 2 * T * H + ob * T * H + 2.0 * 2 * R * I \
+        + 4.0 * H * E * 2
     return f_fwd, f_bwd, b_fwd, b_bwd
 
 
@@ -227,22 +238,23 @@ def kernel_work(cfg, name, counts=None):
     name = name[:-len("_mxfp8")] if mx else name
     b = 1.0 + 1.0 / 32 if mx else 2.0     # bytes per operand element (MXFP8: + scales)
     uv = 2.0 if mx else 4.0               # bytes per saved U, V element (MXFP8 keeps bf16)
-    # (FLOPs, bytes): operands b bytes, U and V uv bytes, fp32 O / dXg rows and gradients
+    ob = result_bytes(cfg)                # O / dXg rows and weight gradients written
+    # (FLOPs, bytes): operands b bytes, U and V uv bytes, O / dXg rows and gradients ob
     tbl = {
         "gemm_fwd_upgate_swiglu": (4.0 * H * I * rows,
                                    b * (2 * H * I * E + rows * H + rows * I)
                                    + 2 * uv * rows * I),
-        "gemm_fwd_down": (2.0 * H * I * rows, b * (H * I * E + rows * I) + 4.0 * rows * H),
+        "gemm_fwd_down": (2.0 * H * I * rows, b * (H * I * E + rows * I) + ob * rows * H),
         "gemm_bwd_dh_swiglu": (2.0 * H * I * rows,
                                b * (H * I * E + rows * H + 3 * rows * I)
                                + 2 * uv * rows * I + 4.0 * rows),
-        "gemm_bwd_dx": (4.0 * H * I * rows, b * (2 * H * I * E + 2 * rows * I) + 4.0 * rows * H),
-        "gemm_bwd_dw_down": (2.0 * H * I * rows, b * (rows * I + rows * H) + 4.0 * H * I * E),
+        "gemm_bwd_dx": (4.0 * H * I * rows, b * (2 * H * I * E + 2 * rows * I) + ob * rows * H),
+        "gemm_bwd_dw_down": (2.0 * H * I * rows, b * (rows * I + rows * H) + ob * H * I * E),
         "gemm_bwd_dw_upgate": (4.0 * H * I * rows,
-                               b * (rows * H + 2 * rows * I) + 4.0 * 2 * H * I * E),
+                               b * (rows * H + 2 * rows * I) + ob * 2 * H * I * E),
         # the routed forward in one launch: weights once, x rows, U and V saved, y written
         "fwd_megakernel": (6.0 * H * I * rows,
-                           b * 3 * H * I * E + 2.0 * rows * H + 2 * uv * rows * I + 4.0 * T * H),
+                           b * 3 * H * I * E + 2.0 * rows * H + 2 * uv * rows * I + ob * T * H),
     }
     return tbl.get(name)
 
@@ -253,15 +265,16 @@ def method_work(cfg):
     GEMMs with the same formulas (one expert, every token, BF16); the router's logits;
     dispatch and reverse dispatch (rows read as bf16, written in the GEMM operand format;
     MXFP8 gathers x and dY once more, quantised along the rows, for the dW GEMMs);
-    combine and reverse combine (fp32 rows read, fp32 token rows written); the router's
-    weight gradient. The launches with a few KB of traffic (top-k, scans, small
-    transposes) are left out."""
+    combine and reverse combine (result-type rows read, result-type token rows written);
+    the router's weight gradient. The launches with a few KB of traffic (top-k, scans,
+    small transposes) are left out."""
     import dataclasses
     T, H, I, E, k, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.shared_I
     R = T * k
     mx = cfg.precision == "mxfp8"
     sfx = "_mxfp8" if mx else ""
     b_op = 1.0 + 1.0 / 32 if mx else 2.0
+    ob = result_bytes(cfg)
     fwd = ["gemm_fwd_upgate_swiglu", "gemm_fwd_down"]
     bwd = ["gemm_bwd_dh_swiglu", "gemm_bwd_dx", "gemm_bwd_dw_upgate", "gemm_bwd_dw_down"]
     names = fwd + (bwd if cfg.backward else [])
@@ -274,13 +287,14 @@ def method_work(cfg):
         out["router_logits"] = (2.0 * T * H * E * 3, 2.0 * T * H + 3 * 2.0 * H * E + 4.0 * T * E)
     move = (0.0, 2.0 * R * H + b_op * R * H)          # bf16 rows in, operand rows out
     out["dispatch_gather" + sfx] = move
-    out["combine"] = (0.0, 4.0 * R * H + 4.0 * T * H + (4.0 * T * H if Is else 0.0))
+    comb = (0.0, ob * R * H + ob * T * H + (ob * T * H if Is else 0.0))
+    out["combine"] = comb
     if cfg.backward:
         out["reverse_dispatch_gather" + sfx] = move
         if mx:   # the dW GEMMs' operands, quantised along the expert rows: x and dY again
             out["replay_gather_rows_mxfp8"] = move
             out["reverse_dispatch_gather_rows_mxfp8"] = move
-        out["reverse_combine"] = (0.0, 4.0 * R * H + 4.0 * T * H + (4.0 * T * H if Is else 0.0))
+        out["reverse_combine"] = comb
         if cfg.router:
             out["router_dwr"] = (2.0 * T * H * k, 2.0 * T * H + 4.0 * H * E + 4.0 * T * k)
     return out
@@ -293,7 +307,7 @@ def method_roofline(cfg, pk, ms_step):
     t = 0.0
     byts = flops = 0.0
     for name, (f, b) in method_work(cfg).items():
-        tc = pk["bf16_tflops_sustained"] * (2.0 if name.endswith("_mxfp8") else 1.0)
+        tc = pk["bf16_tflops"] * (2.0 if name.endswith("_mxfp8") else 1.0)
         t += max(f / (tc * 1e12), b / (pk["hbm_gbs"] * 1e9))
         byts += b
         flops += f
@@ -339,60 +353,64 @@ def whole_job_rate(world, tokens_per_rank, steps, ms):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_gpu(args):
+def make_layer_for(cfg, args, device="cuda", fwd_path=None):
+    """The layer of one workload with its device inputs, weights, gradients and y."""
     import torch
-    import torch.distributed as dist
 
     import moe_inputs as mi
     from grouped_gemm_built_gb300 import mok
     from grouped_gemm_built_gb300.layer import MoELayer
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    cfg = workload_config(args.workload)
-    inp = mi.make_inputs(cfg, seed=1000 + rank, device="cuda", with_dy=True)
+    inp = mi.make_inputs(cfg, seed=1000 + rank, device=device, with_dy=True)
     L = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, shared_I=cfg.shared_I, router=cfg.router,
                  macrobatches=cfg.macrobatches, ring_bytes=cfg.ring_bytes,
-                 precision=cfg.precision)
-    L.set_fwd_path(args.fwd_path)
+                 precision=cfg.precision, out=cfg.out)
+    L.set_fwd_path(fwd_path or args.fwd_path)
     mok.mok_set_comm_sms(L.ctx, args.comm_sms)
     mok.mok_set_sm_limit(L.ctx, args.sm_limit)
-    w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
-                  inp["Ws_down"])
+    mx = None
     if cfg.precision == "mxfp8":
-        w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
-                      inp["Ws_down"], mx=L.quantize_weights(inp["W_up"], inp["W_gate"],
-                                                           inp["W_down"]))
+        mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"])
+    w = L.weights(inp["W_up"], inp["W_gate"], inp["W_down"], inp["Ws_up"], inp["Ws_gate"],
+                  inp["Ws_down"], mx=mx)
     grads = L.alloc_grads() if cfg.backward else None
-    y = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device="cuda")
-    Wr = inp["Wr"]
+    y = torch.empty((cfg.T, cfg.H), dtype=L.out_dtype, device=device)
+    return L, inp, w, grads, y
 
-    def step():
-        if cfg.router:
-            L.plan(x=inp["x"], Wr=Wr, bias=inp["bias"])
-        else:
-            L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
-        L.forward(inp["x"], w, y)
-        if cfg.backward:
-            L.backward(inp["x"], Wr if cfg.router else None, w, inp["dY"], grads)
+
+def layer_step(cfg, L, inp, w, grads, y, x=None, dY=None, y_out=None, g_out=None):
+    """One step: plan, forward and (where the workload has one) backward."""
+    x = inp["x"] if x is None else x
+    if cfg.router:
+        L.plan(x=x, Wr=inp["Wr"], bias=inp["bias"])
+    else:
+        L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
+    L.forward(x, w, y if y_out is None else y_out)
+    if cfg.backward:
+        L.backward(x, inp["Wr"] if cfg.router else None, w, inp["dY"] if dY is None else dY,
+                   grads if g_out is None else g_out)
+
+
+def time_steps(cfg, L, step, steps, warmup, clk, world):
+    """W untimed warm-up steps, then ``steps`` timed ones between barriers and device
+    synchronisations, CUDA events on the launch stream, with the library's per-launch
+    event records and the clock sampler's timed-region samples. Returns (ms of all timed
+    steps, {kernel: (launches, ms)}, launches, megakernel phases, clocks)."""
+    import torch
+    import torch.distributed as dist
+
+    from grouped_gemm_built_gb300 import mok
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    clk = ClockSampler(local, args.clocks_csv)
-    clk.start()
-    for _ in range(max(args.warmup, 0)):
+    for _ in range(max(warmup, 0)):
         step()
     barrier()
     if L.status() != 0:
-        raise RuntimeError("device status error during warm-up")
-
+        raise RuntimeError(f"device status error during warm-up ({cfg.name})")
     stream = torch.cuda.current_stream()
     clk.mark()
     mok.mok_profile_enable(L.ctx, True)
@@ -400,7 +418,7 @@ def run_gpu(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     e1.record(stream)
     barrier()
@@ -412,10 +430,138 @@ def run_gpu(args):
     mok.mok_profile_enable(L.ctx, False)
     clocks = clk.stop()
     if L.status() != 0:
-        raise RuntimeError("device status error in the timed region")
+        raise RuntimeError(f"device status error in the timed region ({cfg.name})")
+    return ms, prof, launches, phases, clocks
+
+
+def analyse(cfg, prof, ms_step, pk, workload):
+    """Roofline of the dominant grouped GEMM, every GEMM's tensor throughput, the layer's
+    compulsory bound, the per-step path's own bound and the row moves' bandwidth. Tensor
+    fractions use the measured burst bf16 peak (x 2 for MXFP8, the nominal fp8/bf16 ratio):
+    each GEMM launch runs for milliseconds inside a step, and the burst figure is the
+    conservative denominator (the sustained one is lower)."""
+    gemm = {n: v for n, v in prof.items() if kernel_work(cfg, n) is not None}
+    top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
+    roofline = None
+    per_kernel = {n: {"launches": c, "ms_per_launch": round(t / c, 5), "share": None}
+                  for n, (c, t) in prof.items()}
+    tot = sum(t for _, t in prof.values()) or 1.0
+    for n, (c, t) in prof.items():
+        per_kernel[n]["share"] = round(t / tot, 4)
+    if top is not None:
+        name, (cnt, tms) = top
+        flops, byts = kernel_work(cfg, name)
+        dur = tms / cnt / 1e3
+        ai = flops / byts
+        tpk = pk["bf16_tflops"] * (2.0 if name.endswith("_mxfp8") else 1.0)
+        tsrc = pk["source"] + (" (burst bf16 x 2, MXFP8)" if name.endswith("_mxfp8")
+                               else " (burst bf16)")
+        ridge = tpk * 1e12 / (pk["hbm_gbs"] * 1e9)
+        if ai < ridge:
+            achieved = byts / dur / 1e9
+            tr = ncu_traffic(workload, name, cfg.out)
+            roofline = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
+                        "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / pk["hbm_gbs"], 4),
+                        "traffic": None if tr is None else round(tr / 1e9, 3),
+                        "traffic_unit": "GB per launch",
+                        "algorithmic": round(byts / 1e9, 3),
+                        "peak_source": pk["source"] + " (copy bandwidth)"}
+        else:
+            achieved = flops / dur / 1e12
+            roofline = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1),
+                        "peak": round(tpk, 1), "unit": "TFLOP/s",
+                        "frac": round(achieved / tpk, 4), "traffic": None,
+                        "peak_source": tsrc}
+    # every grouped GEMM's tensor throughput against its dtype's peak (the metric's
+    # "grouped-GEMM % of TC peak"; meaningful where the GEMMs are compute-bound)
+    gemm_tc = {}
+    for n, (c, t) in prof.items():
+        wk = kernel_work(cfg, n)
+        if wk is None or c == 0 or t <= 0:
+            continue
+        tf = wk[0] / (t / c / 1e3) / 1e12
+        peak_n = pk["bf16_tflops"] * (2.0 if n.endswith("_mxfp8") else 1.0)
+        gemm_tc[n] = {"tflops": round(tf, 1), "frac_of_peak": round(tf / peak_n, 4),
+                      "tb_per_s": round(wk[1] / (t / c / 1e3) / 1e12, 3)}
+    f_fwd, f_bwd, b_fwd, b_bwd = algorithmic(cfg)
+    if not cfg.backward:
+        f_bwd = b_bwd = 0.0
+    lpk = pk["bf16_tflops"] * (2.0 if cfg.precision == "mxfp8" else 1.0)
+    t_roof = max((f_fwd + f_bwd) / (lpk * 1e12), (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
+    layer_roofline = {"ms_per_step_bound": round(t_roof * 1e3, 3),
+                      "frac": round(t_roof * 1e3 / ms_step, 4),
+                      "bytes_gb": round((b_fwd + b_bwd) / 1e9, 2),
+                      "tflop": round((f_fwd + f_bwd) / 1e12, 2),
+                      "bound": "hbm" if (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9) >
+                      (f_fwd + f_bwd) / (lpk * 1e12) else "tensor"}
+    try:
+        method = method_roofline(cfg, pk, ms_step)
+        moves = data_movement(cfg, prof, pk)
+    except Exception as exc:          # reporting only: never lose the line over it
+        method = moves = {"error": repr(exc)}
+    return {"roofline": roofline, "layer_roofline": layer_roofline, "method_roofline": method,
+            "data_movement": moves, "kernels": per_kernel, "gemm_tc": gemm_tc}
+
+
+def sub_record(name, cfg, args, pk, local, fwd_path=None):
+    """One more workload measured the same way in this process (one GPU): its own layer,
+    warm-up, timed steps, clock samples and analysis; the buffers are freed afterwards."""
+    import torch
+    L, inp, w, grads, y = make_layer_for(cfg, args, fwd_path=fwd_path)
+    clk = ClockSampler(local, args.clocks_csv.replace("{gpu}", f"{local}_{name}")
+                       if args.clocks_csv else "")
+    clk.start()
+    steps = max(3, args.sub_steps)
+    ms, prof, launches, phases, clocks = time_steps(
+        cfg, L, lambda: layer_step(cfg, L, inp, w, grads, y), steps, args.warmup, clk, 1)
+    ms_step = ms / steps
+    rec = {"workload": workload_json(cfg)["workload"], "out": cfg.out,
+           "fwd_path": fwd_path or args.fwd_path,
+           "value": round(cfg.T * steps / (ms / 1e3), 1), "unit": "tokens/s",
+           "ms_per_step": round(ms_step, 4), "steps": steps, "warmup": args.warmup,
+           "clocks": clocks, "gpu_launches": launches,
+           "megakernel_phases_ms": phases or None}
+    a = analyse(cfg, prof, ms_step, pk, cfg.name)
+    a.pop("kernels")
+    rec.update(a)
+    del L, inp, w, grads, y
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_gpu(args):
+    import dataclasses
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = workload_config(args.workload)
+    if args.out:
+        cfg = dataclasses.replace(cfg, out=args.out)
+    L, inp, w, grads, y = make_layer_for(cfg, args)
+    stream = torch.cuda.current_stream()
+
+    clk = ClockSampler(local, args.clocks_csv)
+    clk.start()
+    ms, prof, launches, phases, clocks = time_steps(
+        cfg, L, lambda: layer_step(cfg, L, inp, w, grads, y), args.steps, args.warmup, clk,
+        world)
     ms = max_over_ranks(ms, "cuda")
     ms_step = ms / args.steps
     value = whole_job_rate(world, cfg.T, args.steps, ms)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
 
     # ------------------------------------------------------------ e2e (host buffers)
     e2e = None
@@ -424,8 +570,8 @@ def run_gpu(args):
         hdy = torch.empty_like(inp["dY"], device="cpu").pin_memory()
         hx.copy_(inp["x"])
         hdy.copy_(inp["dY"])
-        hy = torch.empty((cfg.T, cfg.H), dtype=torch.float32).pin_memory()
-        hdx = torch.empty((cfg.T, cfg.H), dtype=torch.float32).pin_memory()
+        hy = torch.empty((cfg.T, cfg.H), dtype=L.out_dtype).pin_memory()
+        hdx = torch.empty((cfg.T, cfg.H), dtype=L.out_dtype).pin_memory()
         # double-buffered device inputs and outputs: step i+1's host->device copies and
         # step i-1's device->host copies run on a copy stream while step i computes
         cs = torch.cuda.Stream()
@@ -436,6 +582,8 @@ def run_gpu(args):
         ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b on the device
         ev_done = [torch.cuda.Event() for _ in range(2)]  # step using buffer b computed
         ev_out = [torch.cuda.Event() for _ in range(2)]   # outputs of buffer b copied out
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
 
         def h2d(j):
             b = j % 2
@@ -459,13 +607,8 @@ def run_gpu(args):
                 stream.wait_event(ev_in[b])
                 if i >= 2:
                     stream.wait_event(ev_out[b])
-                if cfg.router:
-                    L.plan(x=xin[b], Wr=Wr, bias=inp["bias"])
-                else:
-                    L.plan(topk_idx=inp["topk_idx"], gates=inp["gates"])
-                L.forward(xin[b], w, yb[b])
-                if cfg.backward:
-                    L.backward(xin[b], Wr if cfg.router else None, w, dyin[b], gb[b])
+                layer_step(cfg, L, inp, w, grads, y, x=xin[b], dY=dyin[b], y_out=yb[b],
+                           g_out=gb[b])
                 ev_done[b].record(stream)
                 with torch.cuda.stream(cs):
                     cs.wait_event(ev_done[b])
@@ -486,72 +629,35 @@ def run_gpu(args):
         ms_e2e = max_over_ranks(e0.elapsed_time(e1), "cuda")
         e2e = {"value": whole_job_rate(world, cfg.T, k_e2e, ms_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": hx.numel() * 2 + (hdy.numel() * 2 if cfg.backward else 0),
-               "d2h_bytes_per_step": hy.numel() * 4 + (hdx.numel() * 4 if cfg.backward else 0),
+               "d2h_bytes_per_step": hy.numel() * hy.element_size()
+               + (hdx.numel() * hdx.element_size() if cfg.backward else 0),
                "steps": k_e2e,
                "pipeline": "inputs and results double-buffered; copies on a second stream "
                            "overlap the neighbouring steps' compute"}
 
-    # ------------------------------------------------------------ roofline
     pk = peaks()
-    gemm = {n: v for n, v in prof.items() if kernel_work(cfg, n) is not None}
-    top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
-    roofline = None
-    per_kernel = {n: {"launches": c, "ms_per_launch": t / c, "share": None}
-                  for n, (c, t) in prof.items()}
-    tot = sum(t for _, t in prof.values()) or 1.0
-    for n, (c, t) in prof.items():
-        per_kernel[n]["share"] = round(t / tot, 4)
-    if top is not None:
-        name, (cnt, tms) = top
-        flops, byts = kernel_work(cfg, name)
-        dur = tms / cnt / 1e3
-        ai = flops / byts
-        # an MXFP8 contraction's peak: the measured bf16 one x the nominal fp8/bf16 ratio 2
-        tpk = pk["bf16_tflops_sustained"] * (2.0 if name.endswith("_mxfp8") else 1.0)
-        tsrc = pk["source"] + (" (sustained bf16 x 2, MXFP8)" if name.endswith("_mxfp8")
-                               else " (sustained bf16)")
-        ridge = tpk * 1e12 / (pk["hbm_gbs"] * 1e9)
-        if ai < ridge:
-            achieved = byts / dur / 1e9
-            tr = ncu_traffic(args.workload, name)
-            roofline = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
-                        "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(achieved / pk["hbm_gbs"], 4),
-                        "traffic": None if tr is None else round(tr / 1e9, 3),
-                        "traffic_unit": "GB per launch",
-                        "algorithmic": round(byts / 1e9, 3),
-                        "peak_source": pk["source"] + " (copy bandwidth)"}
-        else:
-            achieved = flops / dur / 1e12
-            roofline = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1),
-                        "peak": round(tpk, 1), "unit": "TFLOP/s",
-                        "frac": round(achieved / tpk, 4), "traffic": None,
-                        "peak_source": tsrc}
-    # every grouped GEMM's tensor throughput against its dtype's peak (the metric's
-    # "grouped-GEMM % of TC peak"; meaningful where the GEMMs are compute-bound)
-    gemm_tc = {}
-    for n, (c, t) in prof.items():
-        wk = kernel_work(cfg, n)
-        if wk is None or c == 0 or t <= 0:
-            continue
-        tf = wk[0] / (t / c / 1e3) / 1e12
-        peak_n = pk["bf16_tflops_sustained"] * (2.0 if n.endswith("_mxfp8") else 1.0)
-        gemm_tc[n] = {"tflops": round(tf, 1), "frac_of_peak": round(tf / peak_n, 4),
-                      "tb_per_s": round(wk[1] / (t / c / 1e3) / 1e12, 3)}
-    f_fwd, f_bwd, b_fwd, b_bwd = algorithmic(cfg)
-    if not cfg.backward:
-        f_bwd = b_bwd = 0.0
-    lpk = pk["bf16_tflops_sustained"] * (2.0 if cfg.precision == "mxfp8" else 1.0)
-    t_roof = max((f_fwd + f_bwd) / (lpk * 1e12), (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
-    layer_roofline = {"ms_per_step_bound": round(t_roof * 1e3, 3),
-                      "frac": round(t_roof * 1e3 / ms_step, 4),
-                      "bound": "hbm" if (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9) >
-                      (f_fwd + f_bwd) / (lpk * 1e12) else "tensor"}
-    try:
-        method = method_roofline(cfg, pk, ms_step)
-        moves = data_movement(cfg, prof, pk)
-    except Exception as exc:          # reporting only: never lose the line over it
-        method = moves = {"error": repr(exc)}
+    a = analyse(cfg, prof, ms_step, pk, args.workload)
+    mb = {"macrobatches": L.sizes.macrobatches, "ring_slots": L.sizes.ring_slots}
+    del L, inp, w, grads, y
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ sub-records (one GPU)
+    subs = None
+    if world == 1 and not args.no_sub:
+        subs = {}
+        plans = []
+        if cfg.out == "bf16":
+            plans.append(("fp32_results", dataclasses.replace(cfg, out="fp32"), None))
+        if args.workload == "kimi_8192":
+            plans.append(("megakernel_fwd", cfg, "megakernel"))
+            plans.append(("mxfp8_dsv3_imbalanced", workload_config("dsv3_imbalanced"), None))
+        for name, c2, path in plans:
+            try:
+                subs[name] = sub_record(name, c2, args, pk, local, fwd_path=path)
+            except Exception as exc:   # a sub-record never costs the headline line
+                subs[name] = {"error": repr(exc)}
+                torch.cuda.empty_cache()
 
     if rank == 0:
         cpu = None
@@ -565,15 +671,12 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
-            "config": dict(workload_json(cfg),
-                           macrobatches=L.sizes.macrobatches, ring_slots=L.sizes.ring_slots,
+            "config": dict(workload_json(cfg), out=cfg.out, **mb,
                            fwd_path=args.fwd_path, parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
-            "roofline": roofline, "layer_roofline": layer_roofline,
-            "method_roofline": method, "data_movement": moves,
-            "kernels": per_kernel, "gemm_tc": gemm_tc,
             "megakernel_phases_ms": phases or None,
-            "e2e": e2e, "cpu_baseline": cpu,
+            **a,
+            "e2e": e2e, "cpu_baseline": cpu, "sub": subs,
         }
         print(json.dumps(line))
     if world > 1:

@@ -24,11 +24,18 @@ struct mok_ctx_s {
   mok_dims dims;
   mok::Dims d;
   mok_precision precision;
+  mok_out_dtype out_dtype = MOK_OUT_BF16;
   mok_fwd_path fwd_path = MOK_FWD_AUTO;
   int comm_sms = 0;
   int sm_limit = 0;               // 0: every SM
   uint64_t wait_timeout_ns = 0;   // 0: the kernels' default (2 s)
   int withhold = 0;               // test hook of mok_test_withhold_signal
+  mok_tile_order tile_order = MOK_TILES_STATIC;
+  int* tcnt = nullptr;            // tile counters of the current call (dynamic order)
+  int tcnt_used = 0;
+  // the latest forward kept U, V (and the gathered rows) in the per-macrobatch padded
+  // layout: the megakernel with more than one macrobatch
+  bool fwd_cat = false;
   int device;
   int num_sms;
   // optional per-launch timing (mok_profile.h)
@@ -60,10 +67,20 @@ static int launch_sms(mok_ctx_t ctx) {
   return ctx->sm_limit > 0 && ctx->sm_limit < ctx->num_sms ? ctx->sm_limit : ctx->num_sms;
 }
 
-// the context's bound on device waits, applied to one GEMM call
+// the context's bound on device waits and its tile order, applied to one GEMM call
 static mok::GemmCall timed(mok::GemmCall c, mok_ctx_t ctx) {
   c.timeout_ns = ctx->wait_timeout_ns;
+  c.tile_counter = nullptr;
+  if (ctx->tcnt && ctx->tcnt_used < mok::kTileCounters) c.tile_counter = ctx->tcnt + ctx->tcnt_used++;
   return c;
+}
+// start of a call's launches: its tile counters (zeroed here, one per GEMM launch)
+static cudaError_t begin_counters(mok_ctx_t ctx, void* base, cudaStream_t s) {
+  ctx->tcnt_used = 0;
+  ctx->tcnt = nullptr;
+  if (ctx->tile_order != MOK_TILES_DYNAMIC) return cudaSuccess;
+  ctx->tcnt = static_cast<int*>(base);
+  return cudaMemsetAsync(base, 0, sizeof(int) * mok::kTileCounters, s);
 }
 
 namespace {
@@ -83,7 +100,7 @@ cudaError_t prof_launch(mok_ctx_s* c, const char* name, cudaStream_t s, F&& f) {
 
 namespace mok {
 
-Dims make_dims(const mok_dims& x) {
+Dims make_dims(const mok_dims& x, int num_sms) {
   Dims d;
   d.T = x.T;
   d.H = x.H;
@@ -97,9 +114,16 @@ Dims make_dims(const mok_dims& x) {
   d.mt_max = d.P_max / kRowPad;
   d.nblk = (x.T + kTokBlock - 1) / kTokBlock;
   // macrobatches: Tm tokens each, a multiple of 128 (so a macrobatch is whole histogram
-  // blocks and whole 128-token tiles); 0 means one
-  const int want = x.macrobatches > 0 ? x.macrobatches : 1;
-  d.Tm = (int)align_up((size_t)((x.T + want - 1) / want), kRowPad);
+  // blocks and whole 128-token tiles); 0 means one. By tokens: minibatch_tokens, or the
+  // two-wave rule at the device's SM count.
+  if (x.minibatch_tokens != 0) {
+    int tok = x.minibatch_tokens;
+    if (tok < 0) tok = num_sms > 0 ? mok_minibatch_tokens(x.H, x.I, x.k, num_sms) : x.T;
+    d.Tm = (int)align_up((size_t)std::max(tok, 1), kRowPad);
+  } else {
+    const int want = x.macrobatches > 0 ? x.macrobatches : 1;
+    d.Tm = (int)align_up((size_t)((x.T + want - 1) / want), kRowPad);
+  }
   d.M = (x.T + d.Tm - 1) / d.Tm;
   const long long rows_m = (long long)std::min(d.Tm, x.T) * x.k;
   d.mt_m_max = (int)((rows_m + (long long)std::min<long long>(x.E, rows_m) * (kRowPad - 1) +
@@ -168,6 +192,7 @@ FwdWs fwd_ws(const Dims& d) {
   L.ring = b.take((size_t)d.S * d.P_slot * d.H * 2);
   L.ring_sf = b.take((size_t)d.S * d.P_slot * d.H / 32);
   L.cnt = b.take(sizeof(int) * (size_t)mega_cnt(d).total);
+  L.tcnt = b.take(sizeof(int) * kTileCounters);
   L.total = b.off;
   return L;
 }
@@ -229,6 +254,10 @@ BwdWs bwd_ws(const Dims& d) {
   L.sf_dv_r = b.take(P * d.I / 32);
   L.q_hg_r = b.take(P * d.I);
   L.sf_hg_r = b.take(P * d.I / 32);
+  // only after a multi-macrobatch megakernel forward
+  L.uvmap = d.M > 1 ? b.take(sizeof(int32_t) * P) : b.off;
+  L.xr = d.M > 1 ? b.take(2 * P * d.H) : b.off;
+  L.tcnt = b.take(sizeof(int) * kTileCounters);
   L.total = b.off;
   return L;
 }
@@ -314,14 +343,14 @@ mok_status mok_create(const mok_dims* dims, mok_ctx_t* out) {
   if (x.shared_I < 0 || (x.shared_I % 128) != 0) return MOK_ERR_INVALID_ARG;
   if (x.router != 0 && x.router != 1) return MOK_ERR_INVALID_ARG;
   if (x.macrobatches < 0) return MOK_ERR_INVALID_ARG;
-  if (make_dims(x).S < 1) return MOK_ERR_INVALID_ARG;  // ring_bytes below one slot
+  if (x.minibatch_tokens < -1 || (x.minibatch_tokens != 0 && x.macrobatches > 0))
+    return MOK_ERR_INVALID_ARG;
   if ((long long)x.T * x.k + (long long)x.E * 127 > (1LL << 30)) return MOK_ERR_INVALID_ARG;
   if ((long long)x.E * x.H > (1LL << 31) || (long long)x.E * x.I > (1LL << 31))
     return MOK_ERR_INVALID_ARG;
   mok_ctx_s* c = new (std::nothrow) mok_ctx_s;
   if (!c) return MOK_ERR_INVALID_ARG;
   c->dims = x;
-  c->d = make_dims(x);
   c->precision = MOK_BF16;
   // Without a usable device the context still answers the host-only queries
   // (mok_get_sizes); every call that launches work then returns MOK_ERR_CUDA.
@@ -334,6 +363,11 @@ mok_status mok_create(const mok_dims* dims, mok_ctx_t* out) {
     c->num_sms = sms;
   } else {
     cudaGetLastError();
+  }
+  c->d = make_dims(x, c->num_sms);
+  if (c->d.S < 1) {   // ring_bytes below one slot
+    delete c;
+    return MOK_ERR_INVALID_ARG;
   }
   *out = c;
   return MOK_OK;
@@ -348,6 +382,20 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
   if (p != MOK_BF16 && p != MOK_MXFP8 && p != MOK_BF16_WGRAD_PLAIN) return MOK_ERR_INVALID_ARG;
   ctx->precision = p;
+  return MOK_OK;
+}
+
+mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  if (order != MOK_TILES_STATIC && order != MOK_TILES_DYNAMIC) return MOK_ERR_INVALID_ARG;
+  ctx->tile_order = order;
+  return MOK_OK;
+}
+
+mok_status mok_set_output_dtype(mok_ctx_t ctx, mok_out_dtype t) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  if (t != MOK_OUT_BF16 && t != MOK_OUT_F32) return MOK_ERR_INVALID_ARG;
+  ctx->out_dtype = t;
   return MOK_OK;
 }
 
@@ -397,6 +445,7 @@ mok_status mok_get_sizes(mok_ctx_t ctx, mok_sizes* out) {
   out->padded_rows_max = d.P_max;
   out->macrobatches = d.M;
   out->ring_slots = d.S;
+  out->macrobatch_tokens = d.Tm;
   return MOK_OK;
 }
 
@@ -414,6 +463,8 @@ mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* 
   }
   if (ctx->num_sms <= 0) return MOK_ERR_CUDA;  // no usable device
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ctx->tcnt = nullptr;   // the router GEMM takes the static tile order
+  ctx->tcnt_used = 0;
   AuxPtrs a = aux_ptrs(d, sched->aux);
   PlanWs L = plan_ws(d);
   float* logits = reinterpret_cast<float*>(at(workspace, L.logits));
@@ -517,11 +568,13 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
   auto W = [&](size_t off) -> void* { return at(workspace, off); };
   void* o = W(L.o);
   const bool mx = ctx->precision == MOK_MXFP8;
+  const bool ob = ctx->out_dtype == MOK_OUT_BF16;   // O, Os, y in bf16
+  MOK_CHECK_CUDA(begin_counters(ctx, W(L.tcnt), s));
 
   const bool mega = ctx->fwd_path == MOK_FWD_MEGAKERNEL;
   if (mega) {
     // shared expert first (BF16, dense launches); the megakernel's combine adds its output
-    const float* os = nullptr;
+    const void* os = nullptr;
     if (d.Is) {
       GemmCall cs = dense_call(d, a, kFwdUpGate);
       cs.a[0] = x;
@@ -535,14 +588,16 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       cs.a[0] = W(L.hs);
       cs.b[0] = w->Ws_down;
       cs.out[0] = W(L.os);
+      cs.out_bf16 = ob;
       MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
-      os = reinterpret_cast<const float*>(W(L.os));
+      os = W(L.os);
     }
     MegaCall mc;
     memset(&mc, 0, sizeof(mc));
     mc.up = routed_call(d, sched, a, kFwdUpGate);
     mc.down = routed_call(d, sched, a, kFwdDown);
     mc.up.M_rows = mc.down.M_rows = d.P_cat;
+    mc.down.out_bf16 = ob;
     mc.up.a_rows = d.S * d.P_slot;
     mc.up.mx = mc.down.mx = mx;
     // one macrobatch, BF16: the ring's only slot is the saved gathered rows, which the
@@ -594,9 +649,9 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     mc.x = x;
     mc.ring = ring;
     mc.ring_sf = W(L.ring_sf);
-    mc.O = reinterpret_cast<const float*>(o);
+    mc.O = o;
     mc.Os = os;
-    mc.y = static_cast<float*>(y);
+    mc.y = y;
     mc.cnt = reinterpret_cast<int*>(W(L.cnt));
     MOK_CHECK_CUDA(cudaMemsetAsync(mc.cnt, 0, sizeof(int) * (size_t)mega_cnt(d).total, s));
     if (ctx->profile && ctx->trace) {
@@ -606,6 +661,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
       ++ctx->trace_launches;
     }
     MOK_LAUNCH(mx ? "fwd_megakernel_mxfp8" : "fwd_megakernel", launch_fwd_mega(mc, launch_sms(ctx), s));
+    ctx->fwd_cat = d.M > 1;
     return MOK_OK;
   }
 
@@ -627,6 +683,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.a[0] = W(L.h);
     c.b[0] = w->W_down;
     c.out[0] = o;
+    c.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   } else {
     MxWeights M = mx_weights_layout(d);
@@ -654,6 +711,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.b[0] = mxw + M.down_i;
     c.sfb0 = mxw + M.down_i_sf;
     c.out[0] = o;
+    c.out_bf16 = ob;
     MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   const void* shared_out = nullptr;
@@ -670,11 +728,13 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     cs.a[0] = W(L.hs);
     cs.b[0] = w->Ws_down;
     cs.out[0] = W(L.os);
+    cs.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     shared_out = W(L.os);
   }
   // weighted combine in slot order
-  MOK_LAUNCH("combine", launch_combine(d, o, *sched, a, shared_out, true, y, s));
+  MOK_LAUNCH("combine", launch_combine(d, o, *sched, a, shared_out, true, ob, y, s));
+  ctx->fwd_cat = false;
   return MOK_OK;
 }
 
@@ -691,7 +751,6 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   if (!g || !g->dW_up || !g->dW_gate || !g->dW_down || !g->dgates) return MOK_ERR_INVALID_ARG;
   if (!aligned(g->dW_up, 16) || !aligned(g->dW_gate, 16) || !aligned(g->dW_down, 16))
     return MOK_ERR_INVALID_ARG;
-  if (d.M > 1) return MOK_ERR_UNSUPPORTED;   // saved U, V are per macrobatch then
   if (ctx->precision == MOK_MXFP8 && (!w->mx || !aligned(w->mx, 256))) return MOK_ERR_INVALID_ARG;
   if (d.router && (!Wr || !g->dWr)) return MOK_ERR_INVALID_ARG;
   if (!d.router && (Wr || g->dWr)) return MOK_ERR_INVALID_ARG;
@@ -704,13 +763,31 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   BwdWs L = bwd_ws(d);
   SavedLayout S = saved_layout(d);
   auto W = [&](size_t off) -> void* { return at(workspace, off); };
+  MOK_CHECK_CUDA(begin_counters(ctx, W(L.tcnt), s));
   const float* su = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.u));
   const float* sv = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.v));
   void* dxg = W(L.dxg);
   float* dgp = reinterpret_cast<float*>(W(L.dgp));
   float* dl = reinterpret_cast<float*>(W(L.dl));
   const bool mx = ctx->precision == MOK_MXFP8;
+  const bool ob = ctx->out_dtype == MOK_OUT_BF16;   // dXg, dXs, dX and every dW in bf16
   const bool hilo = ctx->precision == MOK_BF16;  // dW operands as bf16 hi + lo pairs
+  // After a megakernel forward over several macrobatches, U, V sit in the per-macrobatch
+  // padded rows where the megakernel wrote them: the dH GEMM reads them there through a
+  // row map (no copy). The gathered x rows of the weight gradients passed through the
+  // ring, whose slots later macrobatches reuse: they are gathered again from x (the same
+  // HBM bytes that reading resident ring slots would cost on one GPU).
+  const int32_t* uvmap = nullptr;
+  void* xrows = at(const_cast<void*>(saved), S.xg);
+  if (ctx->fwd_cat) {
+    int32_t* map = reinterpret_cast<int32_t*>(W(L.uvmap));
+    MOK_LAUNCH("uv_rowmap", launch_uv_rowmap(d, *sched, a, map, s));
+    uvmap = map;
+    if (!mx) {
+      xrows = W(L.xr);
+      MOK_LAUNCH("replay_gather", launch_gather_rows(d, x, *sched, a, xrows, launch_sms(ctx), s));
+    }
+  }
   // the shared expert is BF16 in the MXFP8 mode too, with that mode's dW operands
   const bool hilo_s = ctx->precision != MOK_BF16_WGRAD_PLAIN;
   MxWeights M = mx_weights_layout(d);
@@ -727,6 +804,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[0] = w->W_down;
     c.u = su;
     c.v = sv;
+    c.uv_row = uvmap;
     c.out[0] = W(L.du);
     c.out[2] = W(L.dv);
     c.out[4] = W(L.hg);
@@ -744,6 +822,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[0] = w->W_up;
     c.b[1] = w->W_gate;
     c.out[0] = dxg;
+    c.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   } else {
     // reverse dispatch of dY (blocks along H for the dH GEMM, 32-row blocks for dW_down)
@@ -764,6 +843,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.sfb0 = mxw + M.down_h_sf;
     c.u = su;
     c.v = sv;
+    c.uv_row = uvmap;
     c.out_q[0] = W(L.q_du_i);
     c.out_sf[0] = W(L.sf_du_i);
     c.out_q[1] = W(L.q_dv_i);
@@ -787,6 +867,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.b[1] = mxw + M.gate_i;
     c.sfb1 = mxw + M.gate_i_sf;
     c.out[0] = dxg;
+    c.out_bf16 = ob;
     MOK_LAUNCH("gemm_bwd_dx_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   // router-weight gradient and the renormalised-softmax backward
@@ -814,6 +895,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     cs.b[0] = w->Ws_up;
     cs.b[1] = w->Ws_gate;
     cs.out[0] = W(L.dxs);
+    cs.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     dxs = W(L.dxs);
   }
@@ -821,7 +903,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   float* wrt = reinterpret_cast<float*>(at(workspace, L.dxs + 4 * (size_t)d.T * d.H));
   if (d.router) MOK_LAUNCH("transpose_wr", launch_transpose_wr(d, Wr, wrt, s));
   MOK_LAUNCH("reverse_combine", launch_reverse_combine(d, dxg, *sched, a, dxs,
-                                                       d.router ? dl : nullptr, wrt, dX, s));
+                                                       d.router ? dl : nullptr, wrt, ob, dX, s));
   // weight gradients, each a fixed-order sum over the expert's rows
   GemmCall c = routed_call(d, sched, a, kBwdDWUpGate);
   c.mx = mx;
@@ -833,7 +915,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.sfb0 = W(L.sf_du_r);
     c.sfb1 = W(L.sf_dv_r);
   } else {
-    c.a[0] = at(const_cast<void*>(saved), S.xg);
+    c.a[0] = xrows;
     c.b[0] = W(L.du);
     c.b[1] = W(L.dv);
     if (hilo) {
@@ -844,6 +926,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   }
   c.out[0] = g->dW_up;
   c.out[1] = g->dW_gate;
+  c.out_bf16 = ob;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   c = routed_call(d, sched, a, kBwdDWDown);
   c.mx = mx;
@@ -861,6 +944,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
   }
   c.out[0] = g->dW_down;
+  c.out_bf16 = ob;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDWUpGate);
@@ -874,6 +958,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
     cs.out[0] = g->dWs_up;
     cs.out[1] = g->dWs_gate;
+    cs.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kBwdDWDown);
     cs.a[0] = W(L.hsg);
@@ -883,6 +968,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       cs.a[1] = W(L.hsg_lo);
     }
     cs.out[0] = g->dWs_down;
+    cs.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
   }
   if (d.router) MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, dl, g->dWr, s));

@@ -55,6 +55,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int STAGE_OUT_BYTES = 4096;               // one 32-row epilogue staging box
+constexpr int TQ = 4;                               // slots of the dynamic tile queue
 constexpr int OUT_STAGING = 4 * 2 * STAGE_OUT_BYTES;  // 4 epilogue warps x 2 buffers
 // split (hi/lo) dW stage: [A 16 KB][B 32 KB][second half: B lo 32 KB, or A lo 16 KB]
 constexpr int SPLIT_STAGE_BYTES = A_BYTES + 2 * B_BYTES;
@@ -104,6 +105,9 @@ struct Params {
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
   int stage_bytes;  // bytes of one pipeline stage (Cfg::STAGE_BYTES or SPLIT_STAGE_BYTES)
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
+  int out_bf16;     // kFwdDown, kBwdDX, dW modes: round the outputs to bf16 (64-column boxes)
+  int* tile_counter;// dynamic tile order: the next tile is atomicAdd(tile_counter, 1) (zero at
+                    // launch); null: the static order (tile blockIdx.x, + gridDim.x, ...)
   uint64_t timeout_ns;  // bound of every wait (MOK_ERR_TIMEOUT when it passes)
   int n_out;        // kRouter: output columns (E)
   const float* bias;// kRouter: logit bias or null
@@ -123,6 +127,7 @@ struct Params {
   // epilogue inputs
   const float* u;   // kBwdDH: saved U, V [rows][I] fp32
   const float* v;
+  const int32_t* uv_row;   // kBwdDH: row of U, V per row of the row space (null: the same)
   float* dgp;
   uint32_t* status;
   // MXFP8 scale atoms (512 B each): A side [row tile][kcs_a], B side [e][kcs_b][ncs_b]
@@ -364,11 +369,65 @@ struct Stager {
     }
     issue(m, b, col, row);
   }
+  // 64 values of this lane's row (v0: columns 0..31, v1: 32..63), rounded to bf16 ->
+  // box (64 cols, 32 rows), 128-byte rows with the 128-byte swizzle of the fp32 boxes: half
+  // the bytes of two fp32 boxes in one store
+  __device__ __forceinline__ void bf16x64(const CUtensorMap* m, const float* v0, const float* v1,
+                                          int col, int row) {
+    uint8_t* b = next();
+    uint8_t* r = b + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float* v = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+      uint4 w;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      *reinterpret_cast<uint4*>(r + ((j ^ (lane & 7)) << 4)) = w;
+    }
+    issue(m, b, col, row);
+  }
   __device__ __forceinline__ void drain() {
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
 };
+
+// ------------------------------------------------------------------ tile order
+// Static order: CTA b takes tiles b, b + G, b + 2G, ... Dynamic order (a tile counter in
+// global memory): the producer lane of each CTA takes the next tile with an atomic add when
+// it is ready for one, and passes it to the CTA's MMA lane and epilogue warps through a
+// queue of TQ slots in shared memory (slot q: tile id, "full" barrier of 1 arrival, "empty"
+// barrier of 5: the MMA lane and one lane per epilogue warp). A CTA whose tiles run long
+// then simply takes fewer of them. The queue ends with tile -1. Which CTA runs a tile
+// changes nothing in it: each output tile is one CTA's fixed-order sum either way.
+struct TileQueue {
+  volatile int* tile;
+  uint64_t* full;
+  uint64_t* empty;
+};
+
+// Producer: publish entry n (tile id or -1). False after a timed-out wait.
+__device__ __forceinline__ bool tq_publish(const Params& p, const TileQueue& tq, uint32_t n,
+                                           int tile) {
+  const int q = n % TQ;
+  const uint32_t round = n / TQ;
+  if (round > 0 && !mbar_wait(&tq.empty[q], (round - 1) & 1, globaltimer_ns() + p.timeout_ns))
+    return false;
+  tq.tile[q] = tile;
+  mbar_arrive(&tq.full[q]);   // release: the id is visible to the waiters' acquire
+  return true;
+}
+
+// Consumer (one lane): read entry n and free its slot. False after a timed-out wait.
+__device__ __forceinline__ bool tq_take(const Params& p, const TileQueue& tq, uint32_t n,
+                                        int& tile) {
+  const int q = n % TQ;
+  if (!mbar_wait(&tq.full[q], (n / TQ) & 1, globaltimer_ns() + p.timeout_ns)) return false;
+  tile = tq.tile[q];
+  mbar_arrive(&tq.empty[q]);
+  return true;
+}
 
 // ------------------------------------------------------------------ producer
 // One tile's K loop: fills stages it, it+1, ... (it counts stage uses over the CTA's
@@ -520,13 +579,35 @@ __device__ void produce_drain(const Params& p, uint64_t* full, uint64_t* empty,
 
 template <bool MX>
 __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
-                        uint64_t* empty, volatile int* abort_flag) {
+                        uint64_t* empty, volatile int* abort_flag, const TileQueue& tq) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const TileInfo ti = tile_info<MX>(p, tile);
-    if (ti.skip) continue;
-    if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
+  if (!p.tile_counter) {
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = tile_info<MX>(p, tile);
+      if (ti.skip) continue;
+      if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
+    }
+  } else {
+    for (uint32_t n = 0;; ++n) {
+      int tile;
+      TileInfo ti;
+      do {   // the next tile that is not the unmatched half of a row-tile pair
+        tile = atomicAdd(p.tile_counter, 1);
+        if (tile >= ntiles) {
+          tile = -1;
+          break;
+        }
+        ti = tile_info<MX>(p, tile);
+      } while (ti.skip);
+      if (!tq_publish(p, tq, n, tile)) {
+        set_error(p.status, kErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      if (tile < 0) break;
+      if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
+    }
   }
   produce_drain<MX>(p, full, empty, it);
 }
@@ -625,13 +706,29 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
 template <bool MX>
 __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                           uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
-                          volatile int* abort_flag) {
+                          volatile int* abort_flag, const TileQueue& tq) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+  if (!p.tile_counter) {
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = tile_info<MX>(p, tile);
+      if (ti.skip) continue;
+      if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                        it, local++))
+        return;
+    }
+    return;
+  }
+  for (uint32_t n = 0;; ++n) {
+    int tile;
+    if (!tq_take(p, tq, n, tile)) {
+      set_error(p.status, kErrTimeout);
+      *abort_flag = 1;
+      return;
+    }
+    if (tile < 0) return;
     const TileInfo ti = tile_info<MX>(p, tile);
-    if (ti.skip) continue;
     if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti, it,
                       local++))
       return;
@@ -718,10 +815,18 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         break;
       }
       case kFwdDown:
-      case kBwdDX: {   // expert outputs / routed dX rows, fp32
-        for (int c = 0; c < p.BN / 32; ++c) {
-          tmem_ld32(t_row + c * 32, a);
-          st.f32(&mp.o[0], a, ti.n0 + c * 32, wrow);
+      case kBwdDX: {   // expert outputs / routed dX rows, fp32 or bf16
+        if (p.out_bf16) {
+          for (int c = 0; c < p.BN / 32; c += 2) {
+            tmem_ld32(t_row + c * 32, a);
+            tmem_ld32(t_row + (c + 1) * 32, b);
+            st.bf16x64(&mp.o[0], a, b, ti.n0 + c * 32, wrow);
+          }
+        } else {
+          for (int c = 0; c < p.BN / 32; ++c) {
+            tmem_ld32(t_row + c * 32, a);
+            st.f32(&mp.o[0], a, ti.n0 + c * 32, wrow);
+          }
         }
         break;
       }
@@ -736,18 +841,22 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
           }
         }
         const size_t o = (size_t)row * p.I + ti.n0;
+        // U, V of this row: the same row, or its row in the layout the forward kept them in
+        const int urow = p.uv_row ? p.uv_row[row] : row;
+        const bool have_uv = valid && urow >= 0;
+        const size_t ouv = (size_t)(urow < 0 ? 0 : urow) * p.I + ti.n0;
         float dg = 0.f;
         for (int c = 0; c < p.BN / 32; ++c) {
           const int col = ti.n0 + c * 32;
           tmem_ld32(t_row + c * 32, a);          // D = dY W_down^T
           float u[32], v[32];
-          if (valid) {
+          if (have_uv) {
             if (MX) {                            // saved U, V (bf16 in MXFP8)
-              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.u) + o + c * 32, u);
-              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.v) + o + c * 32, v);
+              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.u) + ouv + c * 32, u);
+              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.v) + ouv + c * 32, v);
             } else {                             // saved U, V (fp32)
-              load_f32x32(p.u + o + c * 32, u);
-              load_f32x32(p.v + o + c * 32, v);
+              load_f32x32(p.u + ouv + c * 32, u);
+              load_f32x32(p.v + ouv + c * 32, v);
             }
           } else {
 #pragma unroll
@@ -806,8 +915,21 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         if (valid && p.dgp) p.dgp[(size_t)row * p.n_tiles + ti.n0 / p.BN] = dg;
         break;
       }
-      case kBwdDWDown: {                         // rows = i of dW_down[e], fp32
+      case kBwdDWDown: {                         // rows = i of dW_down[e], fp32 or bf16
         const int orow = ti.e * p.I + wrow;
+        if (p.out_bf16) {
+          for (int c = 0; c < p.BN / 32; c += 2) {
+            if (have) {
+              tmem_ld32(t_row + c * 32, a);
+              tmem_ld32(t_row + (c + 1) * 32, b);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.f;
+            }
+            st.bf16x64(&mp.o[0], a, b, ti.n0 + c * 32, orow);
+          }
+          break;
+        }
         for (int c = 0; c < p.BN / 32; ++c) {
           if (have) tmem_ld32(t_row + c * 32, a);
           else {
@@ -818,8 +940,32 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         }
         break;
       }
-      default: {                                 // kBwdDWUpGate; rows = h, fp32
+      default: {                                 // kBwdDWUpGate; rows = h, fp32 or bf16
         const int orow = ti.e * p.H + wrow;
+        if (p.out_bf16) {
+          // columns c*32 .. c*32+63 of dW_up (accumulator columns 0..127) and of dW_gate
+          // (columns 128..255), one 64-column box each
+          for (int c = 0; c < 4; c += 2) {
+            float a1[32];
+            if (have) {
+              tmem_ld32(t_row + c * 32, a);
+              tmem_ld32(t_row + (c + 1) * 32, a1);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) a[i] = a1[i] = 0.f;
+            }
+            st.bf16x64(&mp.o[0], a, a1, ti.n0 + c * 32, orow);
+            if (have) {
+              tmem_ld32(t_row + 128 + c * 32, b);
+              tmem_ld32(t_row + 128 + (c + 1) * 32, a1);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) b[i] = a1[i] = 0.f;
+            }
+            st.bf16x64(&mp.o[1], b, a1, ti.n0 + c * 32, orow);
+          }
+          break;
+        }
         for (int c = 0; c < 4; ++c) {
           if (have) {
             tmem_ld32(t_row + c * 32, a);
@@ -842,16 +988,41 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
 
 template <bool MX>
 __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint64_t* acc_full,
-                         uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag) {
+                         uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag,
+                         const TileQueue& tq) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = num_tiles_of(p);
   Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
   int local = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const TileInfo ti = tile_info<MX>(p, tile);
-    if (ti.skip) continue;
-    if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti, local++))
-      break;
+  if (!p.tile_counter) {
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = tile_info<MX>(p, tile);
+      if (ti.skip) continue;
+      if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                             local++))
+        break;
+    }
+  } else {
+    for (uint32_t n = 0;; ++n) {
+      // lane 0 takes the warp's queue entry, the warp learns it by a shuffle
+      int tile = -1;
+      int ok = 1;
+      if (lane == 0) ok = tq_take(p, tq, n, tile) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (!ok) {
+        if (lane == 0) {
+          set_error(p.status, kErrTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      if (tile < 0) break;
+      const TileInfo ti = tile_info<MX>(p, tile);
+      if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                             local++))
+        break;
+    }
   }
   st.drain();
 }
@@ -874,8 +1045,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  TileQueue tq;
+  tq.full = acc_empty + 2;
+  tq.empty = tq.full + TQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq.empty + TQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  tq.tile = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -886,6 +1061,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 128);
+    }
+    for (int q = 0; q < TQ; ++q) {
+      mbar_init(&tq.full[q], 1);
+      mbar_init(&tq.empty[q], 5);   // the MMA lane and lane 0 of each epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -899,12 +1078,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (threadIdx.x == 0) produce<MX>(p, mp, smem, full, empty, abort_flag);
+    if (threadIdx.x == 0) produce<MX>(p, mp, smem, full, empty, abort_flag, tq);
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0)
-      mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag);
+      mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, tq);
   } else {
-    epilogue<MX>(p, mp, staging, acc_full, acc_empty, tmem_base, abort_flag);
+    epilogue<MX>(p, mp, staging, acc_full, acc_empty, tmem_base, abort_flag, tq);
   }
   tc_fence_before();
   __syncthreads();
@@ -952,9 +1131,10 @@ struct MegaParams {
   const uint8_t* x;     // [T][H] bf16
   uint8_t* ring;        // [S][P_slot][H] bf16 (MXFP8: e4m3)
   uint8_t* ring_sf;     // MXFP8: atoms [S][P_slot/128][H/128]
-  const float* O;       // expert outputs [P_cat][H]
-  const float* Os;      // shared expert output [T][H] or null
-  float* y;             // [T][H]
+  const void* O;        // expert outputs [P_cat][H]: fp32, or bf16 with out_bf16
+  const void* Os;       // shared expert output [T][H] or null (O's type)
+  void* y;              // [T][H] (O's type)
+  int out_bf16;
   int* cnt;             // counters (MegaCnt layout), zero at launch
   uint32_t* status;
   unsigned long long* trace;   // optional: kTraceStamps %globaltimer stamps per CTA
@@ -1183,14 +1363,28 @@ __device__ bool mega_gather_tile(const MegaParams& q, int m, int r, uint8_t* buf
 }
 
 // y[t] = sum_j g_tj O[row(t, j)] (+ Os[t]) for the tokens of macrobatch m, one warp per
-// token, warps wi, wi + nw, ... (same arithmetic and order as the standalone combine).
+// token, warps wi, wi + nw, ... (same arithmetic and order as the standalone combine:
+// fp32 sums in slot order, then the shared expert; bf16 mode rounds y once at the end).
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& w, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+  for (int z = 0; z < 4; ++z) {
+    const float2 t2 = __bfloat1622float2(h[z]);
+    f[2 * z] = t2.x;
+    f[2 * z + 1] = t2.y;
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+  uint4 w;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+  for (int z = 0; z < 4; ++z) h[z] = __floats2bfloat162_rn(f[2 * z], f[2 * z + 1]);
+  return w;
+}
+
 __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
   const int lane = threadIdx.x & 31;
   const int t0 = m * q.Tm, t1 = min(q.T, t0 + q.Tm);
-  const int nvec = q.H / 4;
-  const float4* O = reinterpret_cast<const float4*>(q.O);
-  const float4* Os = reinterpret_cast<const float4*>(q.Os);
-  float4* y = reinterpret_cast<float4*>(q.y);
   for (int t = t0 + wi; t < t1; t += nw) {
     int my_row = 0;
     float my_g = 0.f;
@@ -1209,6 +1403,56 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
       rows[j] = __shfl_sync(0xffffffffu, my_row, j);
       g[j] = __shfl_sync(0xffffffffu, my_g, j);
     }
+    if (q.out_bf16) {
+      // 8 bf16 (16 bytes) per vector; 2 vectors per lane per pass
+      const int nvec = q.H / 8;
+      const uint4* O = reinterpret_cast<const uint4*>(q.O);
+      const uint4* Os = reinterpret_cast<const uint4*>(q.Os);
+      uint4* y = reinterpret_cast<uint4*>(q.y);
+      constexpr int U = 2;
+      for (int i0 = lane; i0 < nvec; i0 += 32 * U) {
+        float acc[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int z = 0; z < 8; ++z) acc[u][z] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          if (j < q.k) {
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int i = i0 + 32 * u;
+              w[u] = i < nvec ? __ldcg(O + (size_t)rows[j] * nvec + i) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              float f[8];
+              bf16x8_to_f32(w[u], f);
+#pragma unroll
+              for (int z = 0; z < 8; ++z) acc[u][z] = fmaf(g[j], f[z], acc[u][z]);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + 32 * u;
+          if (i >= nvec) continue;
+          if (Os) {
+            float f[8];
+            bf16x8_to_f32(__ldcg(Os + (size_t)t * nvec + i), f);
+#pragma unroll
+            for (int z = 0; z < 8; ++z) acc[u][z] += f[z];
+          }
+          y[(size_t)t * nvec + i] = f32_to_bf16x8(acc[u]);
+        }
+      }
+      continue;
+    }
+    const int nvec = q.H / 4;
+    const float4* O = reinterpret_cast<const float4*>(q.O);
+    const float4* Os = reinterpret_cast<const float4*>(q.Os);
+    float4* y = reinterpret_cast<float4*>(q.y);
     // 4 vectors per lane per pass: with 6 warps per SM, loads in flight come from width
     constexpr int U = 4;
     for (int i0 = lane; i0 < nvec; i0 += 32 * U) {
@@ -1470,20 +1714,27 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, in
   return r == CUDA_SUCCESS;
 }
 
-// Output map for the epilogue's 32 x 32 boxes: fp32 (128-byte rows, 128-byte swizzle) or
-// bf16 (64-byte rows, 64-byte swizzle); stores outside the matrix are dropped.
-bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int elem_bytes) {
+// Output map for the epilogue's boxes of 32 rows: fp32 32 columns (128-byte rows,
+// 128-byte swizzle), bf16 32 columns (64-byte rows, 64-byte swizzle) or, with wide, bf16 64
+// columns (128-byte rows, 128-byte swizzle); stores outside the matrix are dropped.
+bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, int elem_bytes,
+                  bool wide = false) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc || base == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * elem_bytes};
-  cuuint32_t box[2] = {32, 32};
+  const bool sw128 = elem_bytes == 4 || wide;
+  cuuint32_t box[2] = {(cuuint32_t)(elem_bytes == 2 && wide ? 64 : 32), 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   elem_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+// the map of an fp32 or (out_bf16) bf16 64-column-box output
+bool make_res_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool out_bf16) {
+  return out_bf16 ? make_out_map(m, base, cols, rows, 2, true) : make_out_map(m, base, cols, rows, 4);
 }
 
 // Kernel parameters and tensor maps of one grouped-GEMM call; max_tiles = tiles of the
@@ -1504,6 +1755,9 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   static_assert(2 * SPLIT_STAGE_BYTES + 2 * OUT_STAGING <= Cfg<false>::DATA_BYTES,
                 "split stages and staging exceed the data area");
   p.lo_out = (!MX && c.mode == kBwdDH && c.out[1] && c.out[3] && c.out[5]) ? 1 : 0;
+  p.out_bf16 = (c.out_bf16 && (c.mode == kFwdDown || c.mode == kBwdDX || c.mode == kBwdDWDown ||
+                               c.mode == kBwdDWUpGate)) ? 1 : 0;
+  const bool ob = p.out_bf16 != 0;
   p.timeout_ns = c.timeout_ns > 0 ? c.timeout_ns : kTimeoutNs;
   // Modes without split keep the full operand ring (trading a stage for deeper output
   // staging made the dW modes slower).
@@ -1526,6 +1780,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.gates = c.gates;
   p.u = c.u;
   p.v = c.v;
+  p.uv_row = c.uv_row;
+  p.tile_counter = c.tile_counter;
   p.dgp = c.dgp;
   p.status = c.status;
   p.sfa = static_cast<const uint8_t*>(c.sfa);
@@ -1571,7 +1827,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       p.ncs_b = c.H / 128;
       ok = make_map(&mp.a[0], c.a[0], c.I, rows, BM, eb) &&
            make_map(&mp.b[0], c.b[0], c.H, G * c.I, BK, eb) &&
-           make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);
+           make_res_map(&mp.o[0], c.out[0], c.H, rows, ob);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kRouter:
@@ -1616,7 +1872,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       for (int i = 0; i < 2 && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BM, eb);
       ok = ok && make_map(&mp.b[0], c.b[0], c.I, G * c.H, p.BN, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, p.BN, eb) &&
-           make_out_map(&mp.o[0], c.out[0], c.H, rows, 4);
+           make_res_map(&mp.o[0], c.out[0], c.H, rows, ob);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kBwdDWDown:
@@ -1625,7 +1881,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       p.m_tiles_dw = c.I / BM;
       for (int i = 0; i < (p.split ? 2 : 1) && ok; ++i) ok = make_map(&mp.a[i], c.a[i], c.I, rows, BK, eb);
       ok = ok && make_map(&mp.b[0], c.b[0], c.H, rows, BK, eb) &&
-           make_out_map(&mp.o[0], c.out[0], c.H, G * c.I, 4);
+           make_res_map(&mp.o[0], c.out[0], c.H, G * c.I, ob);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
     case kBwdDWUpGate:
@@ -1634,8 +1890,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       p.m_tiles_dw = c.H / BM;
       ok = make_map(&mp.a[0], c.a[0], c.H, rows, BK, eb);
       for (int i = 0; i < (p.split ? 4 : 2) && ok; ++i) ok = make_map(&mp.b[i], c.b[i], c.I, rows, BK, eb);
-      ok = ok && make_out_map(&mp.o[0], c.out[0], c.I, G * c.H, 4) &&
-           make_out_map(&mp.o[1], c.out[1], c.I, G * c.H, 4);
+      ok = ok && make_res_map(&mp.o[0], c.out[0], c.I, G * c.H, ob) &&
+           make_res_map(&mp.o[1], c.out[1], c.I, G * c.H, ob);
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
   }
@@ -1738,6 +1994,7 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
   q.O = c.O;
   q.Os = c.Os;
   q.y = c.y;
+  q.out_bf16 = c.down.out_bf16 ? 1 : 0;
   q.cnt = c.cnt;
   q.status = c.up.status;
   q.trace = c.trace;

@@ -14,6 +14,7 @@ constexpr int kMaxE = 512;
 constexpr int kMaxK = 8;
 constexpr uint32_t kErrTimeout = 1u;  // device status bits
 constexpr uint32_t kErrBadExpert = 2u;
+constexpr int kTileCounters = 16;     // GEMM launches of one call with a dynamic tile order
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -51,7 +52,7 @@ inline int router_ld(const Dims& d) { return (d.E + 63) / 64 * 64; }
 // scratch for the forward (xq/xsf, hq/hsf: MXFP8 operands and their scale atoms; ring:
 // S slots of dispatched rows (bf16, or E4M3 + atoms at ring_sf); cnt: megakernel counters)
 struct FwdWs {
-  size_t h, o, hs, os, xq, xsf, hq, hsf, ring, ring_sf, cnt, total;
+  size_t h, o, hs, os, xq, xsf, hq, hsf, ring, ring_sf, cnt, tcnt, total;
 };
 // device counters of the forward megakernel (ints, zeroed before each launch)
 struct MegaCnt {
@@ -79,6 +80,8 @@ struct MxWeights {
 struct BwdWs {
   size_t dyg, du, dv, hg, du_lo, dv_lo, hg_lo, dxg, dgp, dl, dus, dvs, hsg, dus_lo,
       dvs_lo, hsg_lo, dxs;
+  size_t uvmap, xr;   // after a multi-macrobatch megakernel forward: U, V row map; x rows
+  size_t tcnt;        // tile counters (dynamic tile order)
   size_t q_dy_h, sf_dy_h, q_dy_r, sf_dy_r, q_x_r, sf_x_r;
   size_t q_du_i, sf_du_i, q_dv_i, sf_dv_i, q_du_r, sf_du_r, q_dv_r, sf_dv_r, q_hg_r, sf_hg_r;
   size_t total;
@@ -89,7 +92,8 @@ struct SavedLayout {
   size_t u, v, us, vs, xg, total;
 };
 
-Dims make_dims(const mok_dims& d);
+// num_sms: the device's SM count (0 without a device), for the two-wave minibatch rule
+Dims make_dims(const mok_dims& d, int num_sms);
 AuxLayout aux_layout(const Dims& d);
 PlanWs plan_ws(const Dims& d);
 FwdWs fwd_ws(const Dims& d);
@@ -143,19 +147,25 @@ cudaError_t launch_split_wr(const Dims& d, const float* Wr, int ld, void* out, c
 // Xg[p] = src[table token of padded row p] (zero rows for padding); optional per-row gate.
 cudaError_t launch_gather_rows(const Dims& d, const void* src, const mok_sched& sc,
                                const AuxPtrs& a, void* dst, int num_sms, cudaStream_t s);
-// y[t] = sum_j gates[t][j] * O[row(t,j)] (+ add[t]), all fp32, in slot order.
+// y[t] = sum_j gates[t][j] * O[row(t,j)] (+ add[t]) in slot order, summed in fp32. O, add
+// and y are fp32, or (bf16) all three bf16 with y rounded once from the fp32 sum.
 cudaError_t launch_combine(const Dims& d, const void* O, const mok_sched& sc, const AuxPtrs& a,
-                           const void* add, bool weighted, void* y, cudaStream_t s);
+                           const void* add, bool weighted, bool bf16, void* y, cudaStream_t s);
 // WrT [E][H] = Wr [H][E]^T (router rows made contiguous for the reverse combine)
 cudaError_t launch_transpose_wr(const Dims& d, const float* Wr, float* WrT, cudaStream_t s);
-// dX[t] = sum_j dXg[row(t,j)] + dXs[t] + sum_j dl[t][j] * WrT[e_j][:], all fp32
-// (dl may be null)
+// dX[t] = sum_j dXg[row(t,j)] + dXs[t] + sum_j dl[t][j] * WrT[e_j][:], summed in fp32
+// (dl may be null); dXg, dXs and dX fp32, or (bf16) all three bf16
 cudaError_t launch_reverse_combine(const Dims& d, const void* dXg, const mok_sched& sc,
                                    const AuxPtrs& a, const void* dXs, const float* dl,
-                                   const float* WrT, void* dX, cudaStream_t s);
+                                   const float* WrT, bool bf16, void* dX, cudaStream_t s);
 // dg[t][j] = sum of the per-tile partial dot products; dl = softmax-renorm backward.
 cudaError_t launch_router_grad(const Dims& d, const float* dgp, int n_parts, const mok_sched& sc,
                                const AuxPtrs& a, float* dgates, float* dl, cudaStream_t s);
+// After a forward that kept U, V in the per-macrobatch padded layout: for every row p of the
+// whole-batch padded row space, the row of the same (token, slot) in that layout (mrow0[m] +
+// mpoff[m][e] + its place in m's run of e's rows), -1 for padding rows.
+cudaError_t launch_uv_rowmap(const Dims& d, const mok_sched& sc, const AuxPtrs& a, int32_t* map,
+                             cudaStream_t s);
 // dWr[:, e] = sum over expert e's table rows of x[t] * dl[t][j]   (fixed row order)
 cudaError_t launch_router_dwr(const Dims& d, const void* x, const mok_sched& sc, const AuxPtrs& a,
                               const float* dl, float* dWr, cudaStream_t s);
@@ -174,13 +184,15 @@ enum GemmMode : int {
 // Operands per mode (BF16; MXFP8 in brackets):
 //   kFwdUpGate   a0 = Xg [x_q]; b0, b1 = W_up, W_gate; out0 = h bf16 [out_q0 + atoms],
 //                out1, out2 = U, V fp32 (saved)
-//   kFwdDown     a0 = h [h_q]; b0 = W_down; out0 = O fp32
+//   kFwdDown     a0 = h [h_q]; b0 = W_down; out0 = O fp32 (out_bf16: bf16)
 //   kBwdDH       a0 = dYg [dY_q]; b0 = W_down; u, v = saved U, V; out0..5 = du, dv, g*h as
 //                bf16 hi/lo pairs [out_q0..4 + atoms]; dgp
 //   kBwdDX       a0, a1 = du_hi, dv_hi [du_q, dv_q]; b0, b1 = W_up, W_gate; out0 = dXg fp32
+//                (out_bf16: bf16)
 //   kBwdDWDown   a0, a1 = g*h hi, lo [a0 = g*h_q]; b0 = dYg [dY_q]; out0 = dW_down fp32
+//                (out_bf16: bf16)
 //   kBwdDWUpGate a0 = Xg [x_q]; b0, b1 = du_hi, dv_hi; b2, b3 = du_lo, dv_lo
-//                [b0, b1 = du_q, dv_q]; out0, out1 = dW_up, dW_gate fp32
+//                [b0, b1 = du_q, dv_q]; out0, out1 = dW_up, dW_gate fp32 (out_bf16: bf16)
 //   kRouter      a0 = x; b0 = [Wr_hi; Wr_mid; Wr_lo] [3H][ld_b] bf16; out0 = logits [T][E]
 //                fp32 (dense, BF16 only)
 struct GemmCall {
@@ -198,8 +210,11 @@ struct GemmCall {
   const void* b[4];     // weights / second row-space operand
   void* out[6];         // outputs (kBwdDH: du, du lo, dv, dv lo, g*h, g*h lo; lo optional)
   bool split;           // dW modes (bf16): operands a[1] / b[2..3] hold the lo halves
+  bool out_bf16;        // kFwdDown, kBwdDX, dW modes: outputs rounded to bf16 (else fp32)
   const float* u;       // kBwdDH: saved U, V (fp32)
   const float* v;
+  const int32_t* uv_row;// kBwdDH: row of U, V for each row of the row space (null: the same
+                        // row; -1: a padding row, read as zeros)
   float* dgp;           // kBwdDH: per-tile partial router-weight gradients
   // schedule (routed case)
   const int32_t* poff; const int32_t* counts; const int32_t* offsets;
@@ -207,6 +222,7 @@ struct GemmCall {
   const int32_t* table; const float* gates; int k;
   uint32_t* status;
   uint64_t timeout_ns;  // bound of every device wait (0: 2 s)
+  int* tile_counter;    // dynamic tile order: a zeroed int of device memory (null: static)
   // MXFP8 (E4M3 operands with 512-byte scale atoms; see mok_quant.cu)
   bool mx;
   const void* sfa; const void* sfa1;                   // A scale atoms (second: kBwdDX dv)
@@ -225,7 +241,7 @@ struct MegaCall {
   const int32_t* mtile_expert; const int32_t* mtiles; const int32_t* mrow0;
   const int32_t* topk_idx; const int32_t* inv;
   const void* x; void* ring; void* ring_sf;
-  const float* O; const float* Os; float* y;
+  const void* O; const void* Os; void* y;   // fp32, or bf16 when down.out_bf16
   int* cnt;
   unsigned long long* trace;   // profiling: kTraceStamps stamps per CTA, or null
   int withhold;                // test hook: row tile 0 of macrobatch 0 is never published

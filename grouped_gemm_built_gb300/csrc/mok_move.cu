@@ -63,23 +63,62 @@ cudaError_t launch_gather_rows(const Dims& d, const void* src, const mok_sched& 
 }
 
 // ---------------------------------------------------------------- combine
-// One warp per token, fp32 rows. weighted: y = sum_j g_tj O[row(t,j)] (+ add[t]);
-// otherwise the plain sum (the reverse combine of the backward), plus the router path
-// sum_j dl_tj Wr[:, e_j] when dl is given.
+// kCombineWarps warps per token. weighted: y = sum_j g_tj O[row(t,j)] (+ add[t]); otherwise
+// the plain sum (the reverse combine of the backward), plus the router path
+// sum_j dl_tj Wr[:, e_j] when dl is given. Sums in fp32, slot order, then add, then the
+// router path. Rows are fp32 (4 per 16-byte vector) or, with BF16, bf16 (8 per vector) with
+// the result rounded to bf16 once.
 constexpr int kCombineWarps = 4;   // warps per token: more loads in flight per SM
 
+template <bool BF16>
+struct RowVec {
+  static constexpr int N = BF16 ? 8 : 4;   // values per 16-byte vector
+  __device__ static void load(const uint4* p, float* f) {
+    const uint4 w = __ldg(p);
+    if (BF16) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const float2 t2 = __bfloat1622float2(h[z]);
+        f[2 * z] = t2.x;
+        f[2 * z + 1] = t2.y;
+      }
+    } else {
+      f[0] = __uint_as_float(w.x);
+      f[1] = __uint_as_float(w.y);
+      f[2] = __uint_as_float(w.z);
+      f[3] = __uint_as_float(w.w);
+    }
+  }
+  __device__ static void store(uint4* p, const float* f) {
+    uint4 w;
+    if (BF16) {
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+      for (int z = 0; z < 4; ++z) h[z] = __floats2bfloat162_rn(f[2 * z], f[2 * z + 1]);
+    } else {
+      w = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                     __float_as_uint(f[3]));
+    }
+    *p = w;
+  }
+};
+
+template <bool BF16>
 __global__ void __launch_bounds__(256) combine_kernel(
-    int T, int H, int E, int k, const float4* __restrict__ O, const int32_t* __restrict__ topk_idx,
+    int T, int H, int E, int k, const uint4* __restrict__ O, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ gates, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ poff,
-    const float4* __restrict__ add, const float* __restrict__ dl, const float* __restrict__ WrT,
-    int weighted, float4* __restrict__ y) {
+    const uint4* __restrict__ add, const float* __restrict__ dl, const float* __restrict__ WrT,
+    int weighted, uint4* __restrict__ y) {
+  using V = RowVec<BF16>;
+  constexpr int N = V::N;
   const int lane = threadIdx.x & 31;
   // kCombineWarps warps per token, each taking every kCombineWarps-th block of 32 vectors
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int t = gw / kCombineWarps, part = gw % kCombineWarps;
   if (t >= T) return;
-  const int nvec = H / 4;
+  const int nvec = H / N;
   int my_row = 0, my_e = 0;
   float my_g = 0.f, my_dl = 0.f;
   if (lane < k) {
@@ -99,55 +138,67 @@ __global__ void __launch_bounds__(256) combine_kernel(
     dls[j] = __shfl_sync(0xffffffffu, my_dl, j);
   }
   for (int i = part * 32 + lane; i < nvec; i += 32 * kCombineWarps) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[N];
+#pragma unroll
+    for (int z = 0; z < N; ++z) acc[z] = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j < k) {
-        const float4 f = __ldg(O + (size_t)rows[j] * nvec + i);
+        float f[N];
+        V::load(O + (size_t)rows[j] * nvec + i, f);
         if (weighted) {
-          acc.x = fmaf(g[j], f.x, acc.x);
-          acc.y = fmaf(g[j], f.y, acc.y);
-          acc.z = fmaf(g[j], f.z, acc.z);
-          acc.w = fmaf(g[j], f.w, acc.w);
+#pragma unroll
+          for (int z = 0; z < N; ++z) acc[z] = fmaf(g[j], f[z], acc[z]);
         } else {
-          acc.x += f.x;
-          acc.y += f.y;
-          acc.z += f.z;
-          acc.w += f.w;
+#pragma unroll
+          for (int z = 0; z < N; ++z) acc[z] += f[z];
         }
       }
     }
     if (add) {
-      const float4 f = __ldg(add + (size_t)t * nvec + i);
-      acc.x += f.x;
-      acc.y += f.y;
-      acc.z += f.z;
-      acc.w += f.w;
+      float f[N];
+      V::load(add + (size_t)t * nvec + i, f);
+#pragma unroll
+      for (int z = 0; z < N; ++z) acc[z] += f[z];
     }
     if (dl) {
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
-          const float4 w = __ldg(reinterpret_cast<const float4*>(WrT + (size_t)ex[j] * H) + i);
-          acc.x = fmaf(dls[j], w.x, acc.x);
-          acc.y = fmaf(dls[j], w.y, acc.y);
-          acc.z = fmaf(dls[j], w.z, acc.z);
-          acc.w = fmaf(dls[j], w.w, acc.w);
+          const float4* w = reinterpret_cast<const float4*>(WrT + (size_t)ex[j] * H + (size_t)i * N);
+#pragma unroll
+          for (int q = 0; q < N / 4; ++q) {
+            const float4 wv = __ldg(w + q);
+            acc[4 * q] = fmaf(dls[j], wv.x, acc[4 * q]);
+            acc[4 * q + 1] = fmaf(dls[j], wv.y, acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(dls[j], wv.z, acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(dls[j], wv.w, acc[4 * q + 3]);
+          }
         }
       }
     }
-    y[(size_t)t * nvec + i] = acc;
+    V::store(y + (size_t)t * nvec + i, acc);
   }
 }
 
-cudaError_t launch_combine(const Dims& d, const void* O, const mok_sched& sc, const AuxPtrs& a,
-                           const void* add, bool weighted, void* y, cudaStream_t s) {
+namespace {
+cudaError_t launch_combine_impl(const Dims& d, const void* rows, const mok_sched& sc,
+                                const AuxPtrs& a, const void* add, const float* dl,
+                                const float* WrT, bool weighted, bool bf16, void* out,
+                                cudaStream_t s) {
   int blocks = (d.T * kCombineWarps * 32 + 255) / 256;
-  combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const float4*>(O),
-                                        sc.topk_idx, sc.gates, sc.inv, sc.offsets, a.poff,
-                                        static_cast<const float4*>(add), nullptr, nullptr,
-                                        weighted ? 1 : 0, static_cast<float4*>(y));
+  auto kern = bf16 ? combine_kernel<true> : combine_kernel<false>;
+  kern<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const uint4*>(rows), sc.topk_idx,
+                              sc.gates, sc.inv, sc.offsets, a.poff,
+                              static_cast<const uint4*>(add), dl, dl ? WrT : nullptr,
+                              weighted ? 1 : 0, static_cast<uint4*>(out));
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_combine(const Dims& d, const void* O, const mok_sched& sc, const AuxPtrs& a,
+                           const void* add, bool weighted, bool bf16, void* y, cudaStream_t s) {
+  return launch_combine_impl(d, O, sc, a, add, nullptr, nullptr, weighted, bf16, y, s);
 }
 
 // ---------------------------------------------------------------- reverse combine
@@ -172,12 +223,42 @@ cudaError_t launch_transpose_wr(const Dims& d, const float* Wr, float* WrT, cuda
 
 cudaError_t launch_reverse_combine(const Dims& d, const void* dXg, const mok_sched& sc,
                                    const AuxPtrs& a, const void* dXs, const float* dl,
-                                   const float* WrT, void* dX, cudaStream_t s) {
-  int blocks = (d.T * kCombineWarps * 32 + 255) / 256;
-  combine_kernel<<<blocks, 256, 0, s>>>(d.T, d.H, d.E, d.k, static_cast<const float4*>(dXg),
-                                        sc.topk_idx, sc.gates, sc.inv, sc.offsets, a.poff,
-                                        static_cast<const float4*>(dXs), dl, dl ? WrT : nullptr,
-                                        0, static_cast<float4*>(dX));
+                                   const float* WrT, bool bf16, void* dX, cudaStream_t s) {
+  return launch_combine_impl(d, dXg, sc, a, dXs, dl, WrT, false, bf16, dX, s);
+}
+
+// ---------------------------------------------------------------- U, V row map
+__global__ void uv_rowmap_kernel(int E, int Tm, int P_max, const int32_t* __restrict__ table,
+                                 const int32_t* __restrict__ counts,
+                                 const int32_t* __restrict__ offsets,
+                                 const int32_t* __restrict__ poff,
+                                 const int32_t* __restrict__ tile_expert,
+                                 const int32_t* __restrict__ num_mtiles,
+                                 const int32_t* __restrict__ mstart,
+                                 const int32_t* __restrict__ mpoff,
+                                 const int32_t* __restrict__ mrow0, int32_t* __restrict__ map) {
+  const int P = min(*num_mtiles, P_max / kRowPad) * kRowPad;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P_max; p += gridDim.x * blockDim.x) {
+    int out = -1;
+    if (p < P) {
+      const int e = clamp_expert(tile_expert[p / kRowPad], E);
+      const int rl = p - poff[e];
+      if (rl >= 0 && rl < counts[e]) {
+        const int tr = offsets[e] + rl;
+        const int m = table[2 * (size_t)tr] / Tm;
+        out = mrow0[m] + mpoff[(size_t)m * (E + 1) + e] + (tr - mstart[(size_t)m * E + e]);
+      }
+    }
+    map[p] = out;
+  }
+}
+
+cudaError_t launch_uv_rowmap(const Dims& d, const mok_sched& sc, const AuxPtrs& a, int32_t* map,
+                             cudaStream_t s) {
+  const int blocks = (d.P_max + 255) / 256;
+  uv_rowmap_kernel<<<blocks, 256, 0, s>>>(d.E, d.Tm, d.P_max, sc.table, sc.counts, sc.offsets,
+                                          a.poff, a.tile_expert, a.num_mtiles, a.mstart, a.mpoff,
+                                          a.mrow0, map);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 // entry point keeps the per-block expert histograms and slot ranks of the schedule builder
 // in a file-scope __device__ array of kNoAllocScratchBytes, which every GPU that loads the
 // library holds until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,24 +24,54 @@ static __device__ __align__(256) int32_t g_plan_scratch[kNoAllocScratchBytes / s
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  CUcontext ctx;   // the context the address belongs to
+  void* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry points (the library does not link
+// the driver library itself).
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 // Device address of g_plan_scratch on the current device. In host code the symbol's name
-// is only a host-side stand-in, so the address is looked up once per device, with that
-// device current, and cached.
+// is only a host-side stand-in, so the address is looked up with the device current and
+// cached per device, together with the context it was looked up in: a device reset (or any
+// new primary context) loads the module again, possibly elsewhere, and the next call then
+// finds another current context and looks the address up again.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  if (!get) return cudaErrorDeviceUninitialized;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!ctx || !g_scratch[dev].ptr || g_scratch[dev].ctx != ctx) {
+    // the lookup also makes the device's primary context current when none is yet
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_plan_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+    g_scratch[dev] = ScratchAddr{ctx, p};
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

@@ -41,17 +41,18 @@ class MoELayer:
     """One MoE SwiGLU layer of fixed dims on one CUDA device."""
 
     def __init__(self, T, H, I, E, k, shared_I=0, router=True, macrobatches=0, ring_bytes=0,
-                 precision="bf16", device="cuda"):
+                 precision="bf16", device="cuda", out="bf16", minibatch_tokens=0):
         self.device = torch.device(device)
         if self.device.type != "cuda":
             raise ValueError(f"the layer's buffers live on a CUDA device, got {self.device}")
         self.dims = mok.MokDims(T=T, H=H, I=I, E=E, k=k, shared_I=shared_I,
                                 router=1 if router else 0, macrobatches=macrobatches,
-                                ring_bytes=ring_bytes)
+                                ring_bytes=ring_bytes, minibatch_tokens=minibatch_tokens)
         self.T, self.H, self.I, self.E, self.k, self.Is = T, H, I, E, k, shared_I
         self.router = router
         self.ctx = mok.mok_create(self.dims)
         self.set_precision(precision)
+        self.set_output_dtype(out)
         self.sizes = mok.mok_get_sizes(self.ctx)
         dev = self.device
         u8 = dict(dtype=torch.uint8, device=dev)
@@ -91,6 +92,15 @@ class MoELayer:
         if precision not in codes:
             raise ValueError(f"precision must be one of {sorted(codes)}, got {precision!r}")
         mok.mok_set_precision(self.ctx, codes[precision])
+
+    def set_output_dtype(self, out: str):
+        """"bf16" (default) or "fp32": the type of y, dX and the weight gradients."""
+        codes = {"bf16": mok.MOK_OUT_BF16, "fp32": mok.MOK_OUT_F32}
+        if out not in codes:
+            raise ValueError(f"output type must be one of {sorted(codes)}, got {out!r}")
+        mok.mok_set_output_dtype(self.ctx, codes[out])
+        self.out = out
+        self.out_dtype = torch.bfloat16 if out == "bf16" else torch.float32
 
     @staticmethod
     def _stream():
@@ -144,18 +154,19 @@ class MoELayer:
                      self._stream())
 
     def forward(self, x, w: "mok.MokWeights", y=None):
-        """y [T,H] fp32 (allocated when not given) from x [T,H] bf16."""
+        """y [T,H] in the output type (allocated when not given) from x [T,H] bf16."""
         px = _dev(x, "x", torch.bfloat16, self.T * self.H)
         if y is None:
-            y = torch.empty((self.T, self.H), dtype=torch.float32, device=self.device)
-        py = _dev(y, "y", torch.float32, self.T * self.H)
+            y = torch.empty((self.T, self.H), dtype=self.out_dtype, device=self.device)
+        py = _dev(y, "y", self.out_dtype, self.T * self.H)
         mok.mok_moe_fwd(self.ctx, self.sched, px, w, py, self.saved.data_ptr(),
                         self.workspace.data_ptr(), self._stream())
         return y
 
     def alloc_grads(self):
+        """dX and the weight gradients in the output type; dgates and dWr fp32."""
         dev = self.device
-        bf = dict(dtype=torch.float32, device=dev)   # all gradients are fp32
+        bf = dict(dtype=self.out_dtype, device=dev)
         g = {
             "dX": torch.empty((self.T, self.H), **bf),
             "dW_up": torch.empty((self.E, self.H, self.I), **bf),
@@ -174,25 +185,25 @@ class MoELayer:
         return g
 
     def backward(self, x, Wr, w: "mok.MokWeights", dY, grads=None):
-        """Gradients (fp32, the shapes of ``alloc_grads``, allocated when not given) from
-        x and dY [T,H] bf16; Wr [H,E] fp32 when the layer runs its router, else None."""
+        """Gradients (the shapes and types of ``alloc_grads``, allocated when not given)
+        from x and dY [T,H] bf16; Wr [H,E] fp32 when the layer runs its router, else None."""
         g = grads if grads is not None else self.alloc_grads()
-        f32 = torch.float32
+        f32, od = torch.float32, self.out_dtype
         EHI, TH, sh = self.E * self.H * self.I, self.T * self.H, self.H * self.Is
         no_sh = self.Is == 0
         mg = mok.MokGrads(
-            dW_up=_dev(g["dW_up"], "dW_up", f32, EHI),
-            dW_gate=_dev(g["dW_gate"], "dW_gate", f32, EHI),
-            dW_down=_dev(g["dW_down"], "dW_down", f32, EHI),
+            dW_up=_dev(g["dW_up"], "dW_up", od, EHI),
+            dW_gate=_dev(g["dW_gate"], "dW_gate", od, EHI),
+            dW_down=_dev(g["dW_down"], "dW_down", od, EHI),
             dgates=_dev(g["dgates"], "dgates", f32, self.T * self.k),
             dWr=_dev(g.get("dWr"), "dWr", f32, self.H * self.E, optional=True),
-            dWs_up=_dev(g.get("dWs_up"), "dWs_up", f32, sh, no_sh),
-            dWs_gate=_dev(g.get("dWs_gate"), "dWs_gate", f32, sh, no_sh),
-            dWs_down=_dev(g.get("dWs_down"), "dWs_down", f32, sh, no_sh))
+            dWs_up=_dev(g.get("dWs_up"), "dWs_up", od, sh, no_sh),
+            dWs_gate=_dev(g.get("dWs_gate"), "dWs_gate", od, sh, no_sh),
+            dWs_down=_dev(g.get("dWs_down"), "dWs_down", od, sh, no_sh))
         px = _dev(x, "x", torch.bfloat16, TH)
         pwr = _dev(Wr, "Wr", f32, self.H * self.E, optional=True)
         pdy = _dev(dY, "dY", torch.bfloat16, TH)
-        pdx = _dev(g["dX"], "dX", f32, TH)
+        pdx = _dev(g["dX"], "dX", od, TH)
         mok.mok_moe_bwd(self.ctx, self.sched, px, pwr, w, self.saved.data_ptr(), pdy, pdx, mg,
                         self.workspace.data_ptr(), self._stream())
         return g

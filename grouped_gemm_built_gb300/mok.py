@@ -25,6 +25,10 @@ MOK_ERR_DEVICE = -6
 MOK_BF16 = 0
 MOK_MXFP8 = 1
 MOK_BF16_WGRAD_PLAIN = 2
+MOK_OUT_BF16 = 0
+MOK_OUT_F32 = 1
+MOK_TILES_STATIC = 0
+MOK_TILES_DYNAMIC = 1
 MOK_FWD_MEGAKERNEL = 0
 MOK_FWD_LAUNCHES = 1
 MOK_FWD_AUTO = 2
@@ -33,7 +37,7 @@ MOK_FWD_AUTO = 2
 class MokDims(ctypes.Structure):
     _fields_ = [("T", c_int), ("H", c_int), ("I", c_int), ("E", c_int), ("k", c_int),
                 ("shared_I", c_int), ("router", c_int), ("macrobatches", c_int),
-                ("ring_bytes", c_size_t)]
+                ("ring_bytes", c_size_t), ("minibatch_tokens", c_int)]
 
 
 class MokSched(ctypes.Structure):
@@ -54,7 +58,8 @@ class MokGrads(ctypes.Structure):
 class MokSizes(ctypes.Structure):
     _fields_ = [("aux_bytes", c_size_t), ("workspace_bytes", c_size_t),
                 ("saved_bytes", c_size_t), ("mx_weight_bytes", c_size_t),
-                ("padded_rows_max", c_int), ("macrobatches", c_int), ("ring_slots", c_int)]
+                ("padded_rows_max", c_int), ("macrobatches", c_int), ("ring_slots", c_int),
+                ("macrobatch_tokens", c_int)]
 
 
 class MokError(RuntimeError):
@@ -75,6 +80,8 @@ def _declare(L):
         "mok_minibatch_tokens": (c_int, [c_int, c_int, c_int, c_int]),
         "mok_status_string": (c_char_p, [c_int]),
         "mok_set_precision": (c_int, [c_void_p, c_int]),
+        "mok_set_output_dtype": (c_int, [c_void_p, c_int]),
+        "mok_set_tile_order": (c_int, [c_void_p, c_int]),
         "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
         "mok_set_comm_sms": (c_int, [c_void_p, c_int]),
         "mok_set_sm_limit": (c_int, [c_void_p, c_int]),
@@ -160,6 +167,14 @@ def mok_get_sizes(ctx) -> MokSizes:
 
 def mok_set_precision(ctx, precision: int) -> None:
     _check(lib().mok_set_precision(ctx, int(precision)), "mok_set_precision")
+
+
+def mok_set_tile_order(ctx, order: int) -> None:
+    _check(lib().mok_set_tile_order(ctx, int(order)), "mok_set_tile_order")
+
+
+def mok_set_output_dtype(ctx, out_dtype: int) -> None:
+    _check(lib().mok_set_output_dtype(ctx, int(out_dtype)), "mok_set_output_dtype")
 
 
 def mok_set_fwd_path(ctx, path: int) -> None:

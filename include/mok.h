@@ -54,7 +54,8 @@ typedef enum {
   MOK_ERR_DEVICE = -6       /* the device flagged bad data (e.g. expert id >= E)    */
 } mok_status;
 
-/* MOK_BF16: bf16 tensor-core operands with fp32 accumulation and fp32 outputs. Inputs,
+/* MOK_BF16: bf16 tensor-core operands with fp32 accumulation (results in the type that
+ *   mok_set_output_dtype selects). Inputs,
  *   weights, h and the dX GEMM's du, dv are bf16; the weight-gradient GEMMs take du, dv
  *   and g*h as bf16 hi + lo pairs (two MMAs per K step), close to fp32 operands.
  * MOK_MXFP8: E4M3 elements with one UE8M0 scale per 32 along each GEMM's contraction axis;
@@ -65,6 +66,16 @@ typedef enum {
  *   name BF16 and MXFP8 only; how BF16 feeds the weight gradients is this library's
  *   choice. */
 typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1, MOK_BF16_WGRAD_PLAIN = 2 } mok_precision;
+
+/* Type of the layer's results, in every precision:
+ * MOK_OUT_BF16 (default): y, dX and the weight gradients dW_up, dW_gate, dW_down, dWs_* are
+ *   bf16, each rounded once (to nearest even) from its fp32 accumulator; the expert output
+ *   rows and routed dX rows that the combines add up are bf16 too, and the combines sum in
+ *   fp32 before their one rounding.
+ * MOK_OUT_F32: all of these in fp32, and the expert output rows and routed dX rows too.
+ * dgates and dWr are fp32 in both. The pages fix no output type; BF16 training reads as
+ * bf16 results accumulated in fp32, with fp32 results as the option. */
+typedef enum { MOK_OUT_BF16 = 0, MOK_OUT_F32 = 1 } mok_out_dtype;
 
 /* How mok_moe_fwd runs the routed experts:
  * MOK_FWD_MEGAKERNEL: one persistent cooperative launch over all SMs, split in software
@@ -80,6 +91,15 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1, MOK_BF16_WGRAD_PLAIN = 2 } mok_preci
  *   GEMMs. Its overlap pays where the gather side moves rows between GPUs instead. */
 typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1, MOK_FWD_AUTO = 2 } mok_fwd_path;
 
+/* Order in which the persistent grouped-GEMM launches take their tiles ([C] "Outras
+ * caracteristicas" and the ihal.it article: tiles scheduled on the GPU at run time rather
+ * than fixed ahead):
+ * MOK_TILES_STATIC (default): CTA b takes tiles b, b + G, b + 2G, ... (G CTAs);
+ * MOK_TILES_DYNAMIC: each CTA takes the next tile from a device counter when it is ready
+ *   for one, so CTAs whose tiles run long (the weight gradients of busy experts) take
+ *   fewer. Every output tile is one CTA's fixed-order sum either way: same bits. */
+typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1 } mok_tile_order;
+
 typedef struct mok_ctx_s* mok_ctx_t;
 
 /* Layer dimensions. T tokens, H hidden, I expert intermediate size, E routed experts,
@@ -91,14 +111,20 @@ typedef struct mok_ctx_s* mok_ctx_t;
  * megakernel passes through the ring token buffer one after another; ring_bytes bounds
  * that buffer: it holds ring_bytes / (one macrobatch's padded rows of bf16) slots, at
  * most one per macrobatch (0: one per macrobatch); fewer than one slot is
- * MOK_ERR_INVALID_ARG ([C] "Ring token buffers"). mok_get_sizes reports the resolved
- * counts. The backward needs one macrobatch. */
+ * MOK_ERR_INVALID_ARG ([C] "Ring token buffers"). minibatch_tokens sizes the macrobatches
+ * by tokens instead: 0 = not used (macrobatches decides); > 0 = that many tokens per
+ * macrobatch (rounded up to 128); -1 = the two-wave rule of [C] "Granularidade do
+ * overlap": mok_minibatch_tokens(H, I, k, SMs of the current device) tokens, rounded up
+ * to 128, so that every macrobatch's grouped GEMMs have at least two full waves of row
+ * tiles (one macrobatch when there is no device); setting both it and macrobatches is
+ * MOK_ERR_INVALID_ARG. mok_get_sizes reports the resolved counts. */
 typedef struct {
   int T, H, I, E, k;
   int shared_I;
   int router;
   int macrobatches;
   size_t ring_bytes;
+  int minibatch_tokens;
 } mok_dims;
 
 /* Schedule produced by mok_plan and passed unchanged to mok_moe_fwd and mok_moe_bwd
@@ -138,10 +164,10 @@ typedef struct {
   const void* mx;
 } mok_weights;
 
-/* Gradients written by mok_moe_bwd (device, all fp32): dW_* with the weights' shapes
- * (fp32 sums of bf16/MXFP8 products); dgates [T][k] (dL/dgate, the router-weight
- * gradient); dWr [H][E] (NULL when there is no router); dWs_* (NULL when there is no
- * shared expert). */
+/* Gradients written by mok_moe_bwd (device): dW_* with the weights' shapes (fp32 sums of
+ * bf16/MXFP8 products, stored as bf16 or fp32 per mok_set_output_dtype); dgates [T][k] fp32
+ * (dL/dgate, the router-weight gradient); dWr [H][E] fp32 (NULL when there is no router);
+ * dWs_* (output type; NULL when there is no shared expert). */
 typedef struct {
   void* dW_up;
   void* dW_gate;
@@ -161,6 +187,7 @@ typedef struct {
   int padded_rows_max;     /* upper bound of expert rows after 128-row padding  */
   int macrobatches;        /* resolved macrobatch count                         */
   int ring_slots;          /* macrobatch slots of the ring token buffer         */
+  int macrobatch_tokens;   /* resolved tokens per macrobatch (the last may hold fewer) */
 } mok_sizes;
 
 /* ---- helpers (host only; nothing is launched) ---------------------------------- */
@@ -184,6 +211,14 @@ const char* mok_status_string(mok_status s);
  * BF16 and MXFP8 from [S] "Determinismus und MXFP8-Unterstuetzung"; [C] "Outras
  * caracteristicas"). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
+
+/* Select the tile order of later mok_moe_fwd / mok_moe_bwd grouped GEMMs (mok_tile_order
+ * above). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
+mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order);
+
+/* Select the type of later mok_moe_fwd / mok_moe_bwd results (mok_out_dtype above).
+ * Host-only state change; MOK_ERR_INVALID_ARG for other values. */
+mok_status mok_set_output_dtype(mok_ctx_t ctx, mok_out_dtype t);
 
 /* Select how later mok_moe_fwd calls run (mok_fwd_path above). Host-only state change;
  * MOK_ERR_INVALID_ARG for other values. */
@@ -221,17 +256,19 @@ mok_status mok_test_withhold_signal(mok_ctx_t ctx, int on);
 mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* logit_bias,
                     mok_sched* sched, void* workspace, void* stream);
 
-/* Forward: y [T][H] fp32 = sum_j gates[t][j] * FFN_{topk_idx[t][j]}(x[t]) (+ shared
- * expert), FFN_e(v) = (silu(v W_gate[e]) * (v W_up[e])) W_down[e]; the GEMMs take bf16
- * (or MXFP8) operands with fp32 accumulation, h is rounded to the operand format, and the
+/* Forward: y [T][H] (bf16, or fp32 per mok_set_output_dtype) = sum_j gates[t][j] *
+ * FFN_{topk_idx[t][j]}(x[t]) (+ shared expert), FFN_e(v) = (silu(v W_gate[e]) *
+ * (v W_up[e])) W_down[e]; the GEMMs take bf16 (or MXFP8) operands with fp32 accumulation,
+ * h is rounded to the operand format, each expert output row to the output type, and the
  * k terms are added in slot order in fp32. `saved` (mok_sizes.saved_bytes) receives what
  * mok_moe_bwd needs; it must stay untouched until then. */
 mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
                        const mok_weights* w, void* y, void* saved, void* workspace,
                        void* stream);
 
-/* Backward for upstream gradient dY [T][H] bf16. Writes dX [T][H] fp32 (routed experts,
- * shared expert and, when routing ran on the device, the router path) and `grads`.
+/* Backward for upstream gradient dY [T][H] bf16. Writes dX [T][H] (output type: routed
+ * experts, shared expert and, when routing ran on the device, the router path, summed in
+ * fp32 in slot order and rounded once) and `grads`.
  * Wr must be the router weight given to mok_plan (NULL when dims.router = 0). */
 mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, const float* Wr,
                        const mok_weights* w, const void* saved, const void* dY, void* dX,
@@ -259,7 +296,9 @@ mok_status mok_get_status(mok_ctx_t ctx, const mok_sched* sched, void* stream);
  * MOK_ERR_UNSUPPORTED; contexts with router = 1 return MOK_ERR_INVALID_ARG.
  *
  * The first call on a device looks up that array's device address (with the device
- * current) and caches it; make that first call before any stream capture. Every call
+ * current) and caches it with the CUDA context it belongs to; make that first call before
+ * any stream capture. After a device reset the next call finds another context and looks
+ * the address up again (make that call before any capture too). Every call
  * shares the one array: calls whose work overlaps on the GPU (other streams, other host
  * threads) race and must be serialised by the caller. No state carries over from one
  * call to the next: the scratch is fully rewritten before it is read. Does not call

@@ -42,6 +42,8 @@ class MoEConfig:
     backward: bool = True
     macrobatches: int = 1
     ring_bytes: int = 0          # 0 = ring sized to hold every routed row
+    out: str = "bf16"            # type of y, dX and the weight gradients: "bf16" or "fp32"
+    minibatch_tokens: int = 0    # tokens per macrobatch (-1: the two-wave rule; 0: unused)
 
     @property
     def R(self) -> int:

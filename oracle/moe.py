@@ -40,6 +40,15 @@ MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, d
 dY), and keeps U, V for the backward as bf16 values (h is formed from the unrounded ones).
 Everything else is float64. The shared expert is always BF16: single bf16
 weight-gradient operands in "bf16_plain", hi/lo ones in "bf16" and "mxfp8".
+
+Result type (``out``): "fp32" keeps every result unrounded (the GPU writes fp32, whose
+rounding the comparison's tolerance covers). "bf16" models bf16 results: each expert output
+row O and the shared expert's output, each routed dX row and the shared expert's dX, and
+then y, dX and every weight gradient are rounded to bf16 once (nearest, ties to even); the
+combines add the rounded rows up exactly and round their sum. dgates and dWr stay
+unrounded. The values just before the last rounding are kept (``y_unrounded`` in the
+forward's saved dict, ``Grads.unrounded``), since a result that lies close to a bf16
+rounding midpoint may round either way on a GPU that sums in fp32.
 """
 from __future__ import annotations
 
@@ -180,23 +189,33 @@ class Precision:
         return a
 
 
+# ----------------------------------------------------------------------------- results
+def out_round(out: str):
+    """The rounding of a result of type ``out``: bf16 for "bf16", none for "fp32"."""
+    if out not in ("fp32", "bf16"):
+        raise ValueError(out)
+    return bf16_round if out == "bf16" else (lambda v: v)
+
+
 # ----------------------------------------------------------------------------- forward
-def shared_forward(x, Ws_up, Ws_gate, Ws_down, mode: str):
-    """Always-on shared expert (BF16 in the bf16 and mxfp8 modes), gate 1."""
+def shared_forward(x, Ws_up, Ws_gate, Ws_down, mode: str, out: str = "fp32"):
+    """Always-on shared expert (BF16 in the bf16 and mxfp8 modes), gate 1; its output
+    is a result row, rounded to the result type."""
     P = Precision("fp64" if mode == "fp64" else "bf16")
     U = x @ Ws_up
     V = x @ Ws_gate
     h = P.fwd_act(silu(V) * U, 1)
-    O = h @ Ws_down
+    O = out_round(out)(h @ Ws_down)
     return O, {"Us": U, "Vs": V}
 
 
 def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
-            expert_fn=None):
+            expert_fn=None, out="fp32"):
     """Layer forward. ``shared`` = (Ws_up, Ws_gate, Ws_down) or None.
     ``expert_fn(e, Xe)`` (test hook) replaces expert e's FFN with any row-wise map.
-    Returns (y [T,H] float64, saved dict)."""
+    ``out``: the result type (module docstring). Returns (y [T,H] float64, saved dict)."""
     P = Precision(precision)
+    rnd = out_round(out)
     x = np.asarray(x, np.float64)
     T, H = x.shape
     E = W_up.shape[0]
@@ -219,7 +238,7 @@ def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
         U = A @ P.op(W_up[e], 0)
         V = A @ P.op(W_gate[e], 0)
         h = P.fwd_act(silu(V) * U, 1)
-        O_rows[r0:r1] = h @ P.op(W_down[e], 0)
+        O_rows[r0:r1] = rnd(h @ P.op(W_down[e], 0))
         U_s[r0:r1] = P.saved_uv(U)
         V_s[r0:r1] = P.saved_uv(V)
     y = np.zeros((T, H))
@@ -227,10 +246,11 @@ def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",
         y += gates[:, j:j + 1] * O_rows[pl.inv[:, j]]
     saved = {"plan": pl, "U": U_s, "V": V_s}
     if shared is not None:
-        Os, ss = shared_forward(x, *shared, precision)
+        Os, ss = shared_forward(x, *shared, precision, out)
         y = y + Os
         saved.update(ss)
-    return y, saved
+    saved["y_unrounded"] = y
+    return rnd(y), saved
 
 
 # ----------------------------------------------------------------------------- backward
@@ -246,18 +266,21 @@ class Grads:
     dWs_up: Optional[np.ndarray] = None
     dWs_gate: Optional[np.ndarray] = None
     dWs_down: Optional[np.ndarray] = None
+    # the results before their last rounding (the same values when out is "fp32")
+    unrounded: Optional[dict] = None
 
 
-def shared_backward(x, Ws_up, Ws_gate, Ws_down, saved, dY, mode: str):
+def shared_backward(x, Ws_up, Ws_gate, Ws_down, saved, dY, mode: str, out: str = "fp32"):
     """Shared expert backward: BF16 (single bf16 weight-gradient operands in bf16_plain,
-    hi/lo ones in the bf16 and mxfp8 modes)."""
+    hi/lo ones in the bf16 and mxfp8 modes). dXs is a result row, rounded to the result
+    type; the weight gradients are returned unrounded."""
     P = Precision(mode if mode in ("fp64", "bf16_plain") else "bf16")
     Us, Vs = saved["Us"], saved["Vs"]
     D = dY @ Ws_down.T
     hv = silu(Vs) * Us
     du = D * silu(Vs)
     dv = D * Us * dsilu(Vs)
-    dXs = P.dx_act(du, 1) @ Ws_up.T + P.dx_act(dv, 1) @ Ws_gate.T
+    dXs = out_round(out)(P.dx_act(du, 1) @ Ws_up.T + P.dx_act(dv, 1) @ Ws_gate.T)
     dWs_down = P.bwd_act_rows(hv).T @ dY
     dWs_up = x.T @ P.bwd_act_rows(du)
     dWs_gate = x.T @ P.bwd_act_rows(dv)
@@ -279,9 +302,11 @@ def router_backward(x, Wr, idx, gates, dgates):
 
 
 def backward(x, idx, gates, W_up, W_gate, W_down, saved, dY, shared=None,
-             precision="fp64", Wr=None):
-    """Layer backward for upstream gradient dY. Returns Grads (float64)."""
+             precision="fp64", Wr=None, out="fp32"):
+    """Layer backward for upstream gradient dY; ``out``: the result type (module
+    docstring). Returns Grads (float64)."""
     P = Precision(precision)
+    rnd = out_round(out)
     x = np.asarray(x, np.float64)
     dY = np.asarray(dY, np.float64)
     T, H = x.shape
@@ -310,8 +335,8 @@ def backward(x, idx, gates, W_up, W_gate, W_down, saved, dY, shared=None,
         dh = g * D
         du = dh * silu(Vs)
         dv = dh * Us * dsilu(Vs)
-        dXg[r0:r1] = (P.dx_act(du, 1) @ P.op(W_up[e], 1).T
-                      + P.dx_act(dv, 1) @ P.op(W_gate[e], 1).T)
+        dXg[r0:r1] = rnd(P.dx_act(du, 1) @ P.op(W_up[e], 1).T
+                          + P.dx_act(dv, 1) @ P.op(W_gate[e], 1).T)
         dW_down[e] = P.bwd_act_rows(g * hv).T @ P.op_rows(dYe)
         XR = P.op_rows(Xe)
         dW_up[e] = XR.T @ P.bwd_act_rows(du)
@@ -319,15 +344,20 @@ def backward(x, idx, gates, W_up, W_gate, W_down, saved, dY, shared=None,
     dX = np.zeros((T, H))
     for j in range(k):                                   # reverse combine in slot order
         dX += dXg[pl.inv[:, j]]
-    out = Grads(dX=dX, dW_up=dW_up, dW_gate=dW_gate, dW_down=dW_down, dgates=dgates)
+    res = Grads(dX=dX, dW_up=dW_up, dW_gate=dW_gate, dW_down=dW_down, dgates=dgates)
     if shared is not None:
-        dXs, out.dWs_up, out.dWs_gate, out.dWs_down = shared_backward(
-            x, *shared, saved, dY, precision)
-        out.dX = out.dX + dXs
+        dXs, res.dWs_up, res.dWs_gate, res.dWs_down = shared_backward(
+            x, *shared, saved, dY, precision, out)
+        res.dX = res.dX + dXs
     if Wr is not None:
-        out.dlogits, out.dWr, dxr = router_backward(x, Wr, idx, gates, dgates)
-        out.dX = out.dX + dxr
-    return out
+        res.dlogits, res.dWr, dxr = router_backward(x, Wr, idx, gates, dgates)
+        res.dX = res.dX + dxr
+    names = ["dX", "dW_up", "dW_gate", "dW_down"] + \
+        (["dWs_up", "dWs_gate", "dWs_down"] if shared is not None else [])
+    res.unrounded = {n: getattr(res, n) for n in names}
+    for n in names:
+        setattr(res, n, rnd(getattr(res, n)))
+    return res
 
 
 # ----------------------------------------------------------------------------- per token

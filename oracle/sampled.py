@@ -18,6 +18,12 @@ MXFP8 blocks of 32 along that GEMM's contraction axis (x, h and dY along H or I 
 du, dv, g*h, x and dY along the expert rows for the weight gradients), and the backward
 reads U, V as bf16 values.
 
+``out`` ("fp32" or "bf16", as in ``moe``) models the result type: with "bf16" the expert
+output rows, the shared expert's output, the routed dX rows and the shared expert's dX are
+rounded to bf16, and so is each returned y, dX and weight-gradient line (once, after the
+exact sum); dgates stay unrounded. The values before that last rounding come back too
+(keys ending in ``_unrounded``).
+
 ``W`` arguments are callables returning one expert's float64 matrices on demand, so the
 caller can stream them from wherever they live.
 """
@@ -25,29 +31,32 @@ from __future__ import annotations
 
 import numpy as np
 
+from .moe import out_round
 from .numerics import bf16_round, dsilu, mx_qdq, mx_qdq_rows_padded, silu
 
 
-def _row_terms(x_t, dY_t, g, Wu, Wg, Wd):
+def _row_terms(x_t, dY_t, g, Wu, Wg, Wd, out="fp32"):
+    rnd = out_round(out)
     U = x_t @ Wu
     V = x_t @ Wg
     h = bf16_round(silu(V) * U)
-    O = h @ Wd
-    out = {"O": O}
+    O = rnd(h @ Wd)
+    res = {"O": O}
     if dY_t is not None:
         D = Wd @ dY_t                      # = dY_t W_down^T
         hv = silu(V) * U
-        out["dg"] = float(D @ hv)
+        res["dg"] = float(D @ hv)
         du = g * D * silu(V)
         dv = g * D * U * dsilu(V)
-        out["dXg"] = Wu @ bf16_round(du) + Wg @ bf16_round(dv)
-    return out
+        res["dXg"] = rnd(Wu @ bf16_round(du) + Wg @ bf16_round(dv))
+    return res
 
 
-def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
+def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None, out="fp32"):
     """y_t, and with dY: dX_t and dg_t (the k router-weight gradients) for token t.
     weights(e) -> (W_up[e], W_gate[e], W_down[e]) float64; shared = (Ws_up, Ws_gate,
     Ws_down) float64 or None; Wr [H][E] float64 or None (router path of dX)."""
+    rnd = out_round(out)
     x_t = np.asarray(x[t], np.float64)
     dY_t = None if dY is None else np.asarray(dY[t], np.float64)
     k = idx.shape[1]
@@ -57,7 +66,7 @@ def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
     for j in range(k):
         e = int(idx[t, j])
         g = float(gates[t, j])
-        r = _row_terms(x_t, dY_t, g, *weights(e))
+        r = _row_terms(x_t, dY_t, g, *weights(e), out=out)
         y += g * r["O"]
         if dY_t is not None:
             dg[j] = r["dg"]
@@ -66,22 +75,23 @@ def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None):
         Ws_up, Ws_gate, Ws_down = shared
         u = x_t @ Ws_up
         v = x_t @ Ws_gate
-        y += bf16_round(silu(v) * u) @ Ws_down
+        y += rnd(bf16_round(silu(v) * u) @ Ws_down)
         if dY_t is not None:
             D = Ws_down @ dY_t
             du = D * silu(v)
             dv = D * u * dsilu(v)
-            dX += Ws_up @ bf16_round(du) + Ws_gate @ bf16_round(dv)
-    out = {"y": y}
+            dX += rnd(Ws_up @ bf16_round(du) + Ws_gate @ bf16_round(dv))
+    res = {"y": rnd(y), "y_unrounded": y}
     if dY_t is not None:
         if Wr is not None:
             s = float((gates[t] * dg).sum())
             dl = gates[t] * (dg - s)
             for j in range(k):
                 dX += dl[j] * Wr[:, int(idx[t, j])]
-        out["dX"] = dX
-        out["dgates"] = dg
-    return out
+        res["dX"] = rnd(dX)
+        res["dX_unrounded"] = dX
+        res["dgates"] = dg
+    return res
 
 
 def expert_rows(plan, e):
@@ -123,10 +133,11 @@ def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks, plain=False):
 
 
 # ----------------------------------------------------------------------------- whole dW lines
-def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i, plain=False):
+def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i, plain=False, out="fp32"):
     """For one expert (its table rows ``pairs``) and one intermediate index i: the row
     dW_down[e][i, :] (length H) and the columns dW_up[e][:, i], dW_gate[e][:, i]
-    (length H); du, dv, g*h unrounded (rounded to bf16 with ``plain``)."""
+    (length H); du, dv, g*h unrounded (rounded to bf16 with ``plain``); each line rounded
+    to the result type."""
     rnd = bf16_round if plain else (lambda v: v)
     t = pairs[:, 0]
     g = np.asarray(gates[t, pairs[:, 1]], np.float64)
@@ -138,7 +149,8 @@ def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i, plain=False):
     hg = rnd(g * silu(V) * U)
     du = rnd(g * D * silu(V))
     dv = rnd(g * D * U * dsilu(V))
-    return {"dW_down": hg @ dYe, "dW_up": X.T @ du, "dW_gate": X.T @ dv}
+    ro = out_round(out)
+    return {"dW_down": ro(hg @ dYe), "dW_up": ro(X.T @ du), "dW_gate": ro(X.T @ dv)}
 
 
 # ----------------------------------------------------------------------------- MXFP8 forward
@@ -148,9 +160,10 @@ def mx_expert_weights(Wu, Wg, Wd):
     return mx_qdq(Wu, 0), mx_qdq(Wg, 0), mx_qdq(Wd, 0)
 
 
-def token_forward_mx(t, x, idx, gates, weights_q, shared=None):
+def token_forward_mx(t, x, idx, gates, weights_q, shared=None, out="fp32"):
     """y_t in MXFP8 mode: x_t in blocks of 32 along H, h in blocks of 32 along I; the
     shared expert BF16 (h rounded to bf16). weights_q(e) -> mx_expert_weights(...)."""
+    rnd = out_round(out)
     x_t = np.asarray(x[t], np.float64)
     xq = mx_qdq(x_t[None, :], 1)[0]
     y = np.zeros(x_t.shape[0])
@@ -159,13 +172,13 @@ def token_forward_mx(t, x, idx, gates, weights_q, shared=None):
         U = xq @ Wu
         V = xq @ Wg
         hq = mx_qdq((silu(V) * U)[None, :], 1)[0]
-        y += float(gates[t, j]) * (hq @ Wd)
+        y += float(gates[t, j]) * rnd(hq @ Wd)
     if shared is not None:
         Ws_up, Ws_gate, Ws_down = shared
         u = x_t @ Ws_up
         v = x_t @ Ws_gate
-        y += bf16_round(silu(v) * u) @ Ws_down
-    return y
+        y += rnd(bf16_round(silu(v) * u) @ Ws_down)
+    return rnd(y)
 
 
 # ----------------------------------------------------------------------------- MXFP8 backward
@@ -177,12 +190,15 @@ def mx_expert_weights_bwd(Wu, Wg, Wd, hs):
     return mx_qdq(Wu, 0), mx_qdq(Wg, 0), mx_qdq(Wd, 1), mx_qdq(Wu[hs], 1), mx_qdq(Wg[hs], 1)
 
 
-def token_backward_mx(t, x, idx, gates, weights_q, dY, Wr=None):
+def token_backward_mx(t, x, idx, gates, weights_q, dY, Wr=None, out="fp32"):
     """MXFP8 mode, token t: the k router-weight gradients dg_t and dX_t at the hidden
     indices the weights were cut to (``weights_q(e)`` -> mx_expert_weights_bwd(..., hs)).
     D = dY_t W_down^T with dY_t and W_down in blocks along H; dg = D . (silu(V) U);
     du = g D silu(V), dv = g D U silu'(V), each in blocks along I before the dX GEMM;
-    with Wr ([H][E], rows hs only) the router path dl Wr^T is added."""
+    with Wr ([H][E], rows hs only) the router path dl Wr^T is added. With bf16 results
+    the routed dX rows and the sum are rounded (the rows are rounded over the hidden
+    indices given, which is what the full rows' rounding gives there)."""
+    rnd = out_round(out)
     x_t = np.asarray(x[t], np.float64)
     xq = mx_qdq(x_t[None, :], 1)[0]
     dYq = mx_qdq(np.asarray(dY[t], np.float64)[None, :], 1)[0]
@@ -199,22 +215,24 @@ def token_backward_mx(t, x, idx, gates, weights_q, dY, Wr=None):
         dg[j] = float(D @ (silu(V) * U))
         du = mx_qdq((g * D * silu(V))[None, :], 1)[0]
         dv = mx_qdq((g * D * U * dsilu(V))[None, :], 1)[0]
-        part = Wu_rows @ du + Wg_rows @ dv
+        part = rnd(Wu_rows @ du + Wg_rows @ dv)
         dX = part if dX is None else dX + part
     if Wr is not None:
         s = float((gates[t] * dg).sum())
         dl = gates[t] * (dg - s)
         for j in range(k):
             dX = dX + dl[j] * np.asarray(Wr, np.float64)[:, int(idx[t, j])]
-    return {"dX": dX, "dgates": dg}
+    return {"dX": rnd(dX), "dX_unrounded": dX, "dgates": dg}
 
 
-def dw_lines_mx(pairs, x, dY, gates, Wu, Wg, Wd, i_list):
+def dw_lines_mx(pairs, x, dY, gates, Wu, Wg, Wd, i_list, out="fp32"):
     """MXFP8 mode, one expert (its table rows ``pairs``), for each i in ``i_list``: the
     row dW_down[e][i, :] and the columns dW_up[e][:, i], dW_gate[e][:, i]. U, V from x in
     blocks along H and W_up, W_gate columns in blocks along H; D from dY in blocks along
     H and the W_down row in blocks along H; then g*h, du, dv, x and dY in blocks of 32
-    expert rows (the last block completed with zero rows)."""
+    expert rows (the last block completed with zero rows); each line rounded to the
+    result type."""
+    ro = out_round(out)
     t = pairs[:, 0]
     g = np.asarray(gates[t, pairs[:, 1]], np.float64)
     X = np.asarray(x[t], np.float64)
@@ -223,7 +241,7 @@ def dw_lines_mx(pairs, x, dY, gates, Wu, Wg, Wd, i_list):
     dYq = mx_qdq(dYe, 1)
     XR = mx_qdq_rows_padded(X)
     dYR = mx_qdq_rows_padded(dYe)
-    out = {}
+    res = {}
     for i in i_list:
         U = bf16_round(Xq @ mx_qdq(Wu[:, i:i + 1], 0)[:, 0])   # as saved for the backward
         V = bf16_round(Xq @ mx_qdq(Wg[:, i:i + 1], 0)[:, 0])
@@ -232,17 +250,19 @@ def dw_lines_mx(pairs, x, dY, gates, Wu, Wg, Wd, i_list):
         hg = col(g * silu(V) * U)
         du = col(g * D * silu(V))
         dv = col(g * D * U * dsilu(V))
-        out[i] = {"dW_down": hg @ dYR, "dW_up": XR.T @ du, "dW_gate": XR.T @ dv}
-    return out
+        res[i] = {"dW_down": ro(hg @ dYR), "dW_up": ro(XR.T @ du), "dW_gate": ro(XR.T @ dv)}
+    return res
 
 
-def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i, plain=False):
-    """Shared expert (gate 1, every token): dWs_down[i, :], dWs_up[:, i], dWs_gate[:, i]."""
+def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i, plain=False, out="fp32"):
+    """Shared expert (gate 1, every token): dWs_down[i, :], dWs_up[:, i], dWs_gate[:, i],
+    each rounded to the result type."""
     rnd = bf16_round if plain else (lambda v: v)
+    ro = out_round(out)
     x = np.asarray(x, np.float64)
     dY = np.asarray(dY, np.float64)
     U = x @ Ws_up[:, i]
     V = x @ Ws_gate[:, i]
     D = dY @ Ws_down[i, :]
-    return {"dWs_down": rnd(silu(V) * U) @ dY, "dWs_up": x.T @ rnd(D * silu(V)),
-            "dWs_gate": x.T @ rnd(D * U * dsilu(V))}
+    return {"dWs_down": ro(rnd(silu(V) * U) @ dY), "dWs_up": ro(x.T @ rnd(D * silu(V))),
+            "dWs_gate": ro(x.T @ rnd(D * U * dsilu(V)))}

@@ -32,7 +32,8 @@ def make_layer(cfg, device="cuda"):
     from grouped_gemm_built_gb300.layer import MoELayer
     return MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, shared_I=cfg.shared_I,
                     router=cfg.router, macrobatches=cfg.macrobatches,
-                    ring_bytes=cfg.ring_bytes, precision=cfg.precision, device=device)
+                    ring_bytes=cfg.ring_bytes, precision=cfg.precision, device=device,
+                    out=cfg.out, minibatch_tokens=cfg.minibatch_tokens)
 
 
 def gpu_inputs(cfg, seed=0):
@@ -85,22 +86,27 @@ def oracle_route(cfg, inp):
     return inp["topk_idx"].numpy().astype(np.int64), np64(inp["gates"]), None
 
 
-def run_oracle(cfg, inp, idx, gates, backward=True, precision=None):
+def run_oracle(cfg, inp, idx, gates, backward=True, precision=None, out=None):
+    """The oracle on the same inputs; ``out`` (default: the config's) models the result
+    type. ``unrounded`` holds the results before their last rounding."""
     precision = precision or cfg.precision
+    out = out or cfg.out
     x = np64(inp["x"])
     W = [np64(inp[n]) for n in ("W_up", "W_gate", "W_down")]
     shared = None
     if cfg.shared_I:
         shared = tuple(np64(inp[n]) for n in ("Ws_up", "Ws_gate", "Ws_down"))
-    y, saved = moe.forward(x, idx, gates, *W, shared=shared, precision=precision)
-    out = {"y": y, "plan": saved["plan"]}
+    y, saved = moe.forward(x, idx, gates, *W, shared=shared, precision=precision, out=out)
+    res = {"y": y, "plan": saved["plan"], "unrounded": {"y": saved["y_unrounded"]}}
     if backward:
         g = moe.backward(x, idx, gates, *W, saved, np64(inp["dY"]), shared=shared,
-                         precision=precision, Wr=np64(inp["Wr"]) if cfg.router else None)
-        out.update({"dX": g.dX, "dW_up": g.dW_up, "dW_gate": g.dW_gate, "dW_down": g.dW_down,
+                         precision=precision, Wr=np64(inp["Wr"]) if cfg.router else None,
+                         out=out)
+        res.update({"dX": g.dX, "dW_up": g.dW_up, "dW_gate": g.dW_gate, "dW_down": g.dW_down,
                     "dgates": g.dgates, "dWr": g.dWr, "dWs_up": g.dWs_up,
                     "dWs_gate": g.dWs_gate, "dWs_down": g.dWs_down})
-    return out
+        res["unrounded"].update(g.unrounded)
+    return res
 
 
 def logit_margins(cfg, inp, logits):

@@ -123,6 +123,21 @@ def test_fwd_path_option():
     mok.mok_destroy(ctx)
 
 
+def test_tile_order_and_output_type_options():
+    ctx = mok.mok_create(dims())
+    for order in (mok.MOK_TILES_DYNAMIC, mok.MOK_TILES_STATIC):
+        mok.mok_set_tile_order(ctx, order)
+    for out in (mok.MOK_OUT_F32, mok.MOK_OUT_BF16):
+        mok.mok_set_output_dtype(ctx, out)
+    for setter in (mok.mok_set_tile_order, mok.mok_set_output_dtype):
+        with pytest.raises(mok.MokError) as ei:
+            setter(ctx, 2)
+        assert ei.value.status == mok.MOK_ERR_INVALID_ARG
+    mok.mok_destroy(ctx)
+    assert mok.lib().mok_set_tile_order(None, 0) == mok.MOK_ERR_INVALID_ARG
+    assert mok.lib().mok_set_output_dtype(None, 0) == mok.MOK_ERR_INVALID_ARG
+
+
 def test_wait_timeout_and_test_hook_are_host_settings():
     ctx = mok.mok_create(dims())
     mok.mok_set_wait_timeout(ctx, 5_000_000)
@@ -207,9 +222,32 @@ def test_bwd_rejects_bad_arguments():
     mok.mok_destroy(ctx)
     ctx = mok.mok_create(dims(router=0, macrobatches=2))
     assert mok.mok_get_sizes(ctx).macrobatches == 2
+    # several macrobatches are accepted: past the argument checks, a machine without a
+    # GPU then fails at the launch
     assert _status(bwd, ctx, S, A, None, W, A, A, A, _grads(router=False), A, None) == \
-        mok.MOK_ERR_UNSUPPORTED                                        # backward is M = 1
+        mok.MOK_ERR_CUDA
     mok.mok_destroy(ctx)
+
+
+def test_minibatch_tokens_resolve_macrobatches():
+    """minibatch_tokens > 0 sizes macrobatches by tokens (rounded up to 128); -1 takes the
+    two-wave rule at the device's SM count, which without a device is one macrobatch;
+    setting it together with macrobatches, or below -1, is rejected."""
+    d = dict(T=1000, H=256, I=128, E=6, k=8, router=0)
+    ctx = mok.mok_create(dims(**d, minibatch_tokens=300))
+    s = mok.mok_get_sizes(ctx)
+    assert (s.macrobatch_tokens, s.macrobatches) == (384, 3)
+    mok.mok_destroy(ctx)
+    ctx = mok.mok_create(dims(**d, minibatch_tokens=-1))
+    s = mok.mok_get_sizes(ctx)
+    import torch
+    if not torch.cuda.is_available():
+        assert s.macrobatches == 1 and s.macrobatch_tokens >= 1000
+    mok.mok_destroy(ctx)
+    for bad in (dict(minibatch_tokens=256, macrobatches=2), dict(minibatch_tokens=-2)):
+        with pytest.raises(mok.MokError) as ei:
+            mok.mok_create(dims(**d, **bad))
+        assert ei.value.status == mok.MOK_ERR_INVALID_ARG
 
 
 def test_plan_and_quantize_reject_bad_arguments():

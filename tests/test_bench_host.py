@@ -114,15 +114,36 @@ def test_method_roofline_bounds_the_layer_roofline():
         if not cfg.backward:
             f_bwd = b_bwd = 0.0
         m = bench.method_roofline(cfg, pk, 1.0)
-        tc = pk["bf16_tflops_sustained"] * (2.0 if cfg.precision == "mxfp8" else 1.0)
+        tc = pk["bf16_tflops"] * (2.0 if cfg.precision == "mxfp8" else 1.0)
         layer = max((f_fwd + f_bwd) / (tc * 1e12), (b_fwd + b_bwd) / (pk["hbm_gbs"] * 1e9))
         assert m["ms_per_step_bound"] >= layer * 1e3 * 0.999, name
         assert m["bytes_gb"] * 1e9 >= (b_fwd + b_bwd) * 0.999, name
         n_gemm = 6 if cfg.backward else 2
         assert sum(1 for n in work if n.startswith("gemm_")) == n_gemm, name
-    kimi = bench.method_work(mi.CONFIGS["kimi_8192"])
-    gemm_gb = sum(b for n, (f, b) in kimi.items() if n.startswith("gemm_")) / 1e9
+    kimi32 = mi.scaled(mi.CONFIGS["kimi_8192"], out="fp32")
+    gemm_gb = sum(b for n, (f, b) in bench.method_work(kimi32).items()
+                  if n.startswith("gemm_")) / 1e9
     assert abs(gemm_gb - 147.4) < 0.35            # six entries rounded to 0.1 GB
+    # bf16 results: the weight gradients and O, dXg rows take half the bytes
+    kimi = bench.method_work(mi.CONFIGS["kimi_8192"])
+    gemm16 = sum(b for n, (f, b) in kimi.items() if n.startswith("gemm_")) / 1e9
+    cfg = mi.CONFIGS["kimi_8192"]
+    R, H, I, E = cfg.T * cfg.k, cfg.H, cfg.I, cfg.E
+    assert abs((gemm_gb - gemm16) * 1e9 - 2.0 * (3 * H * I * E + 2 * R * H)) < 1e6
+
+
+def test_compulsory_bytes_of_the_workloads():
+    """The layer's compulsory bytes per step with bf16 results: the weights read in each
+    pass, x, y, dY, dX, the bf16 weight gradients and the saved U, V read once as bf16:
+    34.15 + 68.7 GB for the Kimi shape at T=8192 and 12.1 + 36.0 GB for the DeepSeek-V3
+    shape in MXFP8 (weights 1 + 1/32 bytes, gradients bf16)."""
+    import moe_inputs as mi
+    f, b, bf, bb = bench.algorithmic(mi.CONFIGS["kimi_8192"])
+    assert abs(bf / 1e9 - 34.15) < 0.05 and abs(bb / 1e9 - 68.7) < 0.1
+    f, b, bf, bb = bench.algorithmic(mi.CONFIGS["dsv3_imbalanced"])
+    assert abs(bf / 1e9 - 12.1) < 0.1 and abs(bb / 1e9 - 36.0) < 0.15
+    f, b, bf32, bb32 = bench.algorithmic(mi.scaled(mi.CONFIGS["kimi_8192"], out="fp32"))
+    assert bb32 - bb > 30e9            # fp32 weight gradients double their bytes
 
 
 def test_data_movement_reads_the_profile_names():

@@ -82,12 +82,59 @@ def _slot_bytes(cfg):
     return mt * 128 * cfg.H * 2
 
 
-def test_backward_needs_one_macrobatch():
-    cfg = mi.scaled(_ring_case("bf16"), backward=True)
-    inp = gu.gpu_inputs(cfg, seed=1)
-    with pytest.raises(mok.MokError) as ei:
-        gu.run_gpu(cfg, inp, backward=True)
-    assert ei.value.status == mok.MOK_ERR_UNSUPPORTED
+@pytest.mark.parametrize("precision,slots", [("bf16", 4), ("bf16", 2), ("bf16", 1),
+                                             ("mxfp8", 2)])
+def test_backward_after_macrobatches_matches_one_launch_per_step(precision, slots):
+    """Forward through the megakernel over four macrobatches (ring of 4, 2 or 1 slots) and
+    the backward after it: U, V are read where the megakernel left them (per-macrobatch
+    padded rows) and the x rows are gathered again. y and every gradient equal, bit for
+    bit, those of the one-launch-per-step path; and they match the oracle."""
+    base = mi.scaled(_ring_case(precision), backward=True, router=True, zipf_s=0.0,
+                     shared_I=128)
+    sb = _slot_bytes(base)
+    cfg = mi.scaled(base, ring_bytes=0 if slots == 4 else slots * sb + sb // 2)
+    inp = gu.gpu_inputs(cfg, seed=9)
+    res = {}
+    for path in ("megakernel", "launches"):
+        L = gu.make_layer(cfg)
+        assert (L.sizes.macrobatches, L.sizes.ring_slots) == (4, slots)
+        L.set_fwd_path(path)
+        res[path], _ = gu.run_gpu(cfg, inp, backward=True, layer=L)
+        assert res[path]["status"] == 0, path
+    for f in ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates", "dWr", "dWs_up",
+              "dWs_gate", "dWs_down"):
+        assert torch.equal(res["megakernel"][f], res["launches"][f]), f
+    if slots == 2:
+        idx, gates, logits = gu.oracle_route(cfg, inp)
+        ref = gu.run_oracle(cfg, inp, idx, gates, backward=True)
+        from tests import out_slack as osl
+        r = res["megakernel"]
+        for f in ("y", "dX", "dgates"):
+            sl = (osl.bf16_spacing(ref["unrounded"][f]) if f != "dgates" and precision == "mxfp8"
+                  else osl.layer_slack(cfg, inp, idx, gates, logits)[f] if f != "dgates"
+                  else 0.0)
+            assert gu.rel_err_slack(r[f], ref[f], sl) <= gu.TOL[precision], f
+
+
+def test_two_wave_macrobatches_resolve_and_keep_the_bits():
+    """minibatch_tokens = -1 sizes macrobatches by the two-wave rule at the device's SM
+    count (ceil(2 * SMs * 64 / k) tokens, rounded up to 128). Through the megakernel, with
+    the backward, the results equal the one-launch-per-step path's bit for bit."""
+    props = torch.cuda.get_device_properties(0)
+    cfg = mi.MoEConfig("two_wave", T=5000, H=256, I=128, E=16, k=8, shared_I=0,
+                       minibatch_tokens=-1, macrobatches=0)
+    want = -(-mok.mok_minibatch_tokens(256, 128, 8, props.multi_processor_count) // 128) * 128
+    inp = gu.gpu_inputs(cfg, seed=10)
+    res = {}
+    for path in ("megakernel", "launches"):
+        L = gu.make_layer(cfg)
+        assert L.sizes.macrobatch_tokens == want
+        assert L.sizes.macrobatches == -(-5000 // want) and L.sizes.macrobatches > 1
+        L.set_fwd_path(path)
+        res[path], _ = gu.run_gpu(cfg, inp, backward=True, layer=L)
+        assert res[path]["status"] == 0
+    for f in ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates", "dWr"):
+        assert torch.equal(res["megakernel"][f], res["launches"][f]), f
 
 
 def test_withheld_signal_times_out_and_the_context_recovers():

@@ -44,11 +44,12 @@ def test_layer_refuses_host_buffers():
         lay.MoELayer(256, 256, 128, 8, 2, device="cpu")
 
 
-def _bare_layer(router=True, shared_I=0):
+def _bare_layer(router=True, shared_I=0, out_dtype=torch.float32):
     """The layer's dims without its device buffers or library context: enough for the
     argument checks, which all run before the library is called."""
     L = lay.MoELayer.__new__(lay.MoELayer)
     L.T, L.H, L.I, L.E, L.k, L.Is, L.router = 16, 128, 128, 4, 2, shared_I, router
+    L.out_dtype = out_dtype
     L.ctx = None
 
     class _S:
@@ -93,6 +94,25 @@ def test_layer_calls_check_their_tensors_before_the_library():
         _bare_layer(shared_I=128).weights(*W)               # the shared expert's weights
 
 
+def test_bf16_results_take_bf16_buffers():
+    """With bf16 results, y, dX and the weight gradients must be bf16 tensors; dgates and
+    dWr stay fp32."""
+    L = _bare_layer(out_dtype=torch.bfloat16)
+    x, Wr = dev(16, 128), dev(128, 4, dtype=torch.float32)
+    with pytest.raises(ValueError, match="y must be torch.bfloat16"):
+        L.forward(x, None, y=dev(16, 128, dtype=torch.float32))
+    g = {"dX": dev(16, 128), "dW_up": dev(4, 128, 128), "dW_gate": dev(4, 128, 128),
+         "dW_down": dev(4, 128, 128), "dgates": dev(16, 2, dtype=torch.float32),
+         "dWr": dev(128, 4, dtype=torch.float32)}
+    with pytest.raises(ValueError, match="dW_down must be torch.bfloat16"):
+        L.backward(x, Wr, None, dev(16, 128),
+                   dict(g, dW_down=dev(4, 128, 128, dtype=torch.float32)))
+    with pytest.raises(ValueError, match="dgates must be torch.float32"):
+        L.backward(x, Wr, None, dev(16, 128), dict(g, dgates=dev(16, 2)))
+    with pytest.raises(ValueError, match="dX must be torch.bfloat16"):
+        L.backward(x, Wr, None, dev(16, 128), dict(g, dX=dev(16, 128, dtype=torch.float32)))
+
+
 def test_router_less_layer_takes_routing_only():
     L = _bare_layer(router=False)
     with pytest.raises(ValueError, match="topk_idx and gates only"):
@@ -118,9 +138,10 @@ def _on_device(inp):
             for k, v in inp.items()}
 
 
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
 @pytest.mark.parametrize("name", ["tiny", "ragged_shared", "tiny_mx", "sparse", "router_less",
                                   "single_expert"])
-def test_the_gpu_tests_call_pattern_passes_the_checks(monkeypatch, name):
+def test_the_gpu_tests_call_pattern_passes_the_checks(monkeypatch, name, out):
     """The call sequence of the GPU tests and the bench (plan, quantize_weights for MXFP8,
     weights, forward, alloc_grads, backward), on the inputs ``moe_inputs`` makes for them,
     passes every tensor check; the library calls are stubbed out."""
@@ -144,6 +165,7 @@ def test_the_gpu_tests_call_pattern_passes_the_checks(monkeypatch, name):
     L.T, L.H, L.I, L.E, L.k, L.Is, L.router = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, \
         cfg.shared_I, cfg.router
     L.device, L.ctx = torch.device("cpu"), None
+    L.out_dtype = torch.bfloat16 if out == "bf16" else torch.float32
 
     class _S:
         mx_weight_bytes = 4096
@@ -164,8 +186,9 @@ def test_the_gpu_tests_call_pattern_passes_the_checks(monkeypatch, name):
     w = L.weights(d["W_up"], d["W_gate"], d["W_down"], d["Ws_up"], d["Ws_gate"], d["Ws_down"],
                   mx=mx)
     y = L.forward(d["x"], w)
-    L.forward(d["x"], w, torch.empty((cfg.T, cfg.H)).as_subclass(_OnDevice))
+    L.forward(d["x"], w, torch.empty((cfg.T, cfg.H), dtype=L.out_dtype).as_subclass(_OnDevice))
     g = L.backward(d["x"], d["Wr"] if cfg.router else None, w, d["dY"])
     L.backward(d["x"], d["Wr"] if cfg.router else None, w, d["dY"], g)
-    assert y.shape == (cfg.T, cfg.H)
+    assert y.shape == (cfg.T, cfg.H) and y.dtype == L.out_dtype
+    assert g["dW_up"].dtype == L.out_dtype and g["dgates"].dtype == torch.float32
     assert calls.count("mok_moe_bwd") == 2 and calls.count("mok_moe_fwd") == 2

@@ -256,50 +256,58 @@ def test_empty_experts_get_zero_gradients(rng):
     assert np.abs(g.dW_up[0]).max() > 0
 
 
-def test_sampled_evaluators_match_the_dense_oracle(rng):
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_sampled_evaluators_match_the_dense_oracle(rng, out):
     """Per-token and per-element evaluators (no table, no streaming) against the dense
-    per-expert oracle, bf16 rounding model, shared expert and router path included."""
+    per-expert oracle, bf16 rounding model, shared expert and router path included; both
+    result types (with bf16 results the values before the last rounding too)."""
     from oracle import sampled
     x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=14, H=16, I=8, E=5, k=2, shared=True)
     r = moe.route(x, Wr, 2)
-    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16")
+    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="bf16", out=out)
     g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16",
-                     Wr=Wr)
+                     Wr=Wr, out=out)
     W = lambda e: (Wu[e], Wg[e], Wd[e])
     for t in range(14):
-        o = sampled.token_outputs(t, x, r.idx, r.gates, W, dY=dY, shared=sh, Wr=Wr)
+        o = sampled.token_outputs(t, x, r.idx, r.gates, W, dY=dY, shared=sh, Wr=Wr, out=out)
         assert np.allclose(o["y"], y[t], rtol=1e-12, atol=1e-12)
         assert np.allclose(o["dX"], g.dX[t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(o["y_unrounded"], saved["y_unrounded"][t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(o["dX_unrounded"], g.unrounded["dX"][t], rtol=1e-12, atol=1e-12)
         assert np.allclose(o["dgates"], g.dgates[t], rtol=1e-12, atol=1e-12)
     pl = saved["plan"]
     for e in range(5):
         pairs = sampled.expert_rows(pl, e)
         picks = [("dW_up", 3, 5), ("dW_gate", 15, 0), ("dW_down", 7, 11), ("dW_down", 0, 0)]
         got = sampled.dw_elements(e, pairs, x, dY, r.gates, Wu[e], Wg[e], Wd[e], picks)
-        ref = [g.dW_up[e, 3, 5], g.dW_gate[e, 15, 0], g.dW_down[e, 7, 11], g.dW_down[e, 0, 0]]
+        G = g.unrounded
+        ref = [G["dW_up"][e, 3, 5], G["dW_gate"][e, 15, 0], G["dW_down"][e, 7, 11],
+               G["dW_down"][e, 0, 0]]
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_plain"])
-def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng, mode):
+@pytest.mark.parametrize("mode,out", [("bf16", "fp32"), ("bf16_plain", "fp32"),
+                                      ("bf16", "bf16")])
+def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng, mode, out):
     """The full-size evaluators (whole dW lines; MXFP8 per-token forward) against the
-    dense per-expert oracle."""
+    dense per-expert oracle, in both result types."""
     from oracle import sampled
     from oracle.numerics import bf16_round
     x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=20, H=64, I=32, E=4, k=2, shared=True)
     x = bf16_round(x)
     r = moe.route(x, Wr, 2)
-    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision=mode)
-    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision=mode)
+    y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision=mode, out=out)
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision=mode,
+                     out=out)
     pl = saved["plan"]
     for e in range(4):
         for i in (0, 17, 31):
             L = sampled.dw_lines(sampled.expert_rows(pl, e), x, dY, r.gates, Wu[e], Wg[e], Wd[e], i,
-                                 plain=mode != "bf16")
+                                 plain=mode != "bf16", out=out)
             assert np.allclose(L["dW_down"], g.dW_down[e, i, :], rtol=1e-12, atol=1e-12)
             assert np.allclose(L["dW_up"], g.dW_up[e, :, i], rtol=1e-12, atol=1e-12)
             assert np.allclose(L["dW_gate"], g.dW_gate[e, :, i], rtol=1e-12, atol=1e-12)
-    ym, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="mxfp8")
+    ym, _ = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision="mxfp8", out=out)
     cache = {}
 
     def wq(e):
@@ -308,47 +316,51 @@ def test_dw_lines_and_mx_token_forward_match_the_dense_oracle(rng, mode):
         return cache[e]
 
     for t in range(20):
-        yt = sampled.token_forward_mx(t, x, r.idx, r.gates, wq, shared=sh)
+        yt = sampled.token_forward_mx(t, x, r.idx, r.gates, wq, shared=sh, out=out)
         assert np.allclose(yt, ym[t], rtol=1e-12, atol=1e-12)
 
 
-def test_mx_backward_evaluators_match_the_dense_oracle(rng):
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_mx_backward_evaluators_match_the_dense_oracle(rng, out):
     """The MXFP8 full-size backward evaluators (one token's dgates and dX at sampled
     hidden indices with the router path; whole dW lines of one expert) against the dense
-    per-expert oracle in mxfp8 mode."""
+    per-expert oracle in mxfp8 mode, in both result types."""
     from oracle import sampled
     from oracle.numerics import bf16_round
     x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=64, H=64, I=64, E=3, k=2)
     x = bf16_round(x)
     r = moe.route(x, Wr, 2)
-    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="mxfp8")
-    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, precision="mxfp8", Wr=Wr)
+    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="mxfp8", out=out)
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, precision="mxfp8", Wr=Wr,
+                     out=out)
     hs = np.array([0, 5, 31, 63])
     wq = lambda e: sampled.mx_expert_weights_bwd(Wu[e], Wg[e], Wd[e], hs)
     for t in range(40):
-        o = sampled.token_backward_mx(t, x, r.idx, r.gates, wq, dY, Wr=Wr[hs])
+        o = sampled.token_backward_mx(t, x, r.idx, r.gates, wq, dY, Wr=Wr[hs], out=out)
         assert np.allclose(o["dgates"], g.dgates[t], rtol=1e-12, atol=1e-12)
         assert np.allclose(o["dX"], g.dX[t, hs], rtol=1e-12, atol=1e-12)
     pl = saved["plan"]
     assert pl.counts.max() > 32          # an expert with more than one 32-row block
     for e in range(3):
         L = sampled.dw_lines_mx(sampled.expert_rows(pl, e), x, dY, r.gates, Wu[e], Wg[e],
-                                Wd[e], [0, 17, 63])
+                                Wd[e], [0, 17, 63], out=out)
         for i, li in L.items():
             assert np.allclose(li["dW_down"], g.dW_down[e, i, :], rtol=1e-12, atol=1e-12)
             assert np.allclose(li["dW_up"], g.dW_up[e, :, i], rtol=1e-12, atol=1e-12)
             assert np.allclose(li["dW_gate"], g.dW_gate[e, :, i], rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_plain", "mxfp8"])
-def test_shared_dw_lines_match_the_dense_oracle(rng, mode):
+@pytest.mark.parametrize("mode,out", [("bf16", "fp32"), ("bf16_plain", "fp32"),
+                                      ("mxfp8", "fp32"), ("bf16", "bf16")])
+def test_shared_dw_lines_match_the_dense_oracle(rng, mode, out):
     from oracle import sampled
     x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=12, H=32, I=32, E=3, k=1, shared=True)
     r = moe.route(x, Wr, 1)
-    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision=mode)
-    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision=mode)
+    _, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, shared=sh, precision=mode, out=out)
+    g = moe.backward(x, r.idx, r.gates, Wu, Wg, Wd, saved, dY, shared=sh, precision=mode,
+                     out=out)
     for i in range(6):
-        L = sampled.shared_dw_lines(x, dY, *sh, i, plain=mode == "bf16_plain")
+        L = sampled.shared_dw_lines(x, dY, *sh, i, plain=mode == "bf16_plain", out=out)
         assert np.allclose(L["dWs_down"], g.dWs_down[i], rtol=1e-12, atol=1e-12)
         assert np.allclose(L["dWs_up"], g.dWs_up[:, i], rtol=1e-12, atol=1e-12)
         assert np.allclose(L["dWs_gate"], g.dWs_gate[:, i], rtol=1e-12, atol=1e-12)
@@ -472,3 +484,79 @@ def test_dx_gemm_operand_rounding_point(rng, mode):
     assert np.array_equal(g.dX, rd(du) + c * rd(dv))
     if mode != "fp64":
         assert not np.array_equal(rd(du), du) and not np.array_equal(rd(dv), dv)
+
+
+# ----------------------------------------------------------------------------- result type
+def test_result_rounding_points_forward(rng):
+    """bf16 results: with W_down = c * identity (c = 1 + 2^-10, so c h is not a bf16 value
+    while bf16(c h) is h's neighbourhood), two slots to two experts with gates 1/3, 2/3 and
+    a shared expert of the same form, the value before y's rounding is
+    g1 bf16(c h1) + g2 bf16(c h2) + bf16(c hs) exactly: each expert output row and the
+    shared output rounded on its own, then summed; y is that sum rounded once. With fp32
+    results nothing is rounded: g1 c h1 + g2 c h2 + c hs."""
+    from oracle.numerics import bf16_round, silu
+    H, c = 64, 1.0 + 2.0 ** -10
+    x = bf16_round(rng.normal(0, 1, (1, H)))
+    Wu = bf16_round(rng.normal(0, 0.2, (2, H, H)))
+    Wg = bf16_round(rng.normal(0, 0.2, (2, H, H)))
+    Wd = c * np.stack([np.eye(H), np.eye(H)])
+    sh = (bf16_round(rng.normal(0, 0.2, (H, H))), bf16_round(rng.normal(0, 0.2, (H, H))),
+          c * np.eye(H))
+    idx, gates = np.array([[1, 0]]), np.array([[1 / 3, 2 / 3]])
+    h = [bf16_round(silu(x @ Wg[e]) * (x @ Wu[e])) for e in (0, 1)]
+    hs = bf16_round(silu(x @ sh[1]) * (x @ sh[0]))
+    y, saved = moe.forward(x, idx, gates, Wu, Wg, Wd, shared=sh, precision="bf16", out="bf16")
+    pre = gates[0, 0] * bf16_round(c * h[1]) + gates[0, 1] * bf16_round(c * h[0]) \
+        + bf16_round(c * hs)
+    assert np.array_equal(saved["y_unrounded"], pre)
+    assert np.array_equal(y, bf16_round(pre))
+    assert not np.array_equal(bf16_round(pre), pre)
+    y32, s32 = moe.forward(x, idx, gates, Wu, Wg, Wd, shared=sh, precision="bf16", out="fp32")
+    want = gates[0, 0] * (c * h[1]) + gates[0, 1] * (c * h[0]) + c * hs
+    assert np.array_equal(y32, want) and np.array_equal(s32["y_unrounded"], want)
+    assert not np.array_equal(pre, want)
+
+
+def test_result_rounding_points_backward(rng):
+    """bf16 results: one token, both slots to one expert (gates 1/4, 3/4), a shared expert,
+    W_down the identity, W_up = c I and W_gate = (c/2) I (c = 1 + 2^-10). Each routed dX
+    row is bf16(c du' + (c/2) dv') with du', dv' the dX GEMM's bf16 operands, the shared
+    expert's dX row likewise with gate 1; dX is their sum rounded once; every weight
+    gradient is its exact sum over the rows rounded once (dW_up = x^T du per slot)."""
+    from oracle.numerics import bf16_round, dsilu, silu
+    H, c = 64, 1.0 + 2.0 ** -10
+    x = bf16_round(rng.normal(0, 1, (1, H)))
+    dY = bf16_round(rng.normal(0, 1, (1, H)))
+    eye = np.eye(H)
+    Wu, Wg, Wd = (c * eye)[None], (c / 2 * eye)[None], eye[None]
+    sh = (c * eye, c / 2 * eye, eye)
+    idx, gates = np.array([[0, 0]]), np.array([[0.25, 0.75]])
+    _, saved = moe.forward(x, idx, gates, Wu, Wg, Wd, shared=sh, precision="bf16", out="bf16")
+    g = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16",
+                     out="bf16")
+    U, V = c * x, c / 2 * x
+
+    def rows(gt):
+        du, dv = gt * dY * silu(V), gt * dY * U * dsilu(V)
+        return bf16_round(c * bf16_round(du) + c / 2 * bf16_round(dv)), du
+    r1, du1 = rows(0.25)
+    r2, du2 = rows(0.75)
+    rs, _ = rows(1.0)
+    pre = r1 + r2 + rs
+    assert np.array_equal(g.unrounded["dX"], pre)
+    assert np.array_equal(g.dX, bf16_round(pre))
+    assert not np.array_equal(bf16_round(pre), pre)
+    dwu = x.T @ du1 + x.T @ du2
+    assert np.allclose(g.unrounded["dW_up"][0], dwu, rtol=1e-14, atol=0)
+    assert np.array_equal(g.dW_up, bf16_round(g.unrounded["dW_up"]))
+    assert not np.array_equal(g.dW_up, g.unrounded["dW_up"])
+    for n in ("dW_gate", "dW_down", "dWs_up", "dWs_gate", "dWs_down"):
+        assert np.array_equal(getattr(g, n), bf16_round(g.unrounded[n])), n
+    g32 = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16",
+                       out="fp32")
+    pre32 = (c * bf16_round(rows(0.25)[1]) + c / 2 * bf16_round(0.25 * dY * U * dsilu(V))) \
+        + (c * bf16_round(rows(0.75)[1]) + c / 2 * bf16_round(0.75 * dY * U * dsilu(V)))
+    assert np.allclose(g32.dX - (c * bf16_round(dY * silu(V))
+                                 + c / 2 * bf16_round(dY * U * dsilu(V))), pre32,
+                       rtol=1e-14, atol=1e-15)
+    assert np.allclose(g32.dW_up[0], dwu, rtol=1e-14, atol=0)

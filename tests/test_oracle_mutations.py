@@ -68,8 +68,13 @@ P = {
     "fd_dgates": lambda: tl.test_dgates_match_finite_differences(_rng()),
     "router_inv": lambda: tl.test_router_backward_invariants(_rng()),
     "empty": lambda: tl.test_empty_experts_get_zero_gradients(_rng()),
-    "sampled": lambda: tl.test_sampled_evaluators_match_the_dense_oracle(_rng()),
-    "mx_bwd_eval": lambda: tl.test_mx_backward_evaluators_match_the_dense_oracle(_rng()),
+    "sampled": lambda: tl.test_sampled_evaluators_match_the_dense_oracle(_rng(), "fp32"),
+    "sampled_bf16": lambda: tl.test_sampled_evaluators_match_the_dense_oracle(_rng(), "bf16"),
+    "mx_bwd_eval": lambda: tl.test_mx_backward_evaluators_match_the_dense_oracle(_rng(), "fp32"),
+    "mx_bwd_eval_bf16": lambda: tl.test_mx_backward_evaluators_match_the_dense_oracle(
+        _rng(), "bf16"),
+    "out_fwd": lambda: tl.test_result_rounding_points_forward(_rng()),
+    "out_bwd": lambda: tl.test_result_rounding_points_backward(_rng()),
     "saved_uv": lambda: tl.test_mxfp8_saved_uv_rounding_point(_rng()),
     "wgrad_plain": lambda: tl.test_weight_gradient_operand_rounding_point(_rng(), "bf16_plain"),
     "wgrad_hilo": lambda: tl.test_weight_gradient_operand_rounding_point(_rng(), "bf16"),
@@ -87,12 +92,17 @@ P = {
     "mx_rows": lambda: tn.test_mx_rows_padded_equals_explicit_zero_rows(_rng()),
     "silu": lambda: tn.test_silu_and_derivative(),
     "dw_lines_bf16": lambda: tl.test_dw_lines_and_mx_token_forward_match_the_dense_oracle(
-        _rng(), "bf16"),
+        _rng(), "bf16", "fp32"),
     "dw_lines_plain": lambda: tl.test_dw_lines_and_mx_token_forward_match_the_dense_oracle(
-        _rng(), "bf16_plain"),
+        _rng(), "bf16_plain", "fp32"),
+    "dw_lines_out": lambda: tl.test_dw_lines_and_mx_token_forward_match_the_dense_oracle(
+        _rng(), "bf16", "bf16"),
     "shared_lines_plain": lambda: tl.test_shared_dw_lines_match_the_dense_oracle(
-        _rng(), "bf16_plain"),
-    "shared_lines_mx": lambda: tl.test_shared_dw_lines_match_the_dense_oracle(_rng(), "mxfp8"),
+        _rng(), "bf16_plain", "fp32"),
+    "shared_lines_mx": lambda: tl.test_shared_dw_lines_match_the_dense_oracle(
+        _rng(), "mxfp8", "fp32"),
+    "shared_lines_out": lambda: tl.test_shared_dw_lines_match_the_dense_oracle(
+        _rng(), "bf16", "bf16"),
 }
 
 # (owner, function, original text, planted text, pins expected to catch it)
@@ -157,7 +167,7 @@ MISTAKES = {
         moe, "backward", "dX += dXg[pl.inv[:, j]]",
         "dX += gates[:, j:j + 1] * dXg[pl.inv[:, j]]", ["fd"]),
     "router path of dX with the wrong sign": (
-        moe, "backward", "out.dX = out.dX + dxr", "out.dX = out.dX - dxr", ["fd"]),
+        moe, "backward", "res.dX = res.dX + dxr", "res.dX = res.dX - dxr", ["fd"]),
     "router backward with the wrong sign": (
         moe, "router_backward", "dlS = gates * (dgates - s)", "dlS = gates * (s - dgates)",
         ["fd", "router_inv"]),
@@ -213,7 +223,7 @@ MISTAKES = {
         "return sigmoid(v)", ["silu"]),
     # full-size evaluators
     "sampled router-weight gradient against U": (
-        sampled, "_row_terms", 'out["dg"] = float(D @ hv)', 'out["dg"] = float(D @ U)',
+        sampled, "_row_terms", 'res["dg"] = float(D @ hv)', 'res["dg"] = float(D @ U)',
         ["sampled"]),
     "sampled forward leaves h unrounded": (
         sampled, "_row_terms", "h = bf16_round(silu(V) * U)", "h = silu(V) * U", ["sampled"]),
@@ -282,6 +292,46 @@ MISTAKES = {
         sampled, "mx_expert_weights", "mx_qdq(Wd, 0)", "mx_qdq(Wd, 1)", ["dw_lines_bf16"]),
     "MXFP8 backward weights: W_down along I": (
         sampled, "mx_expert_weights_bwd", "mx_qdq(Wd, 1)", "mx_qdq(Wd, 0)", ["mx_bwd_eval"]),
+    # bf16 results
+    "bf16 results left unrounded": (
+        moe, "out_round", 'return bf16_round if out == "bf16" else (lambda v: v)',
+        "return (lambda v: v)", ["out_fwd", "out_bwd"]),
+    "expert output rows not rounded before the combine": (
+        moe, "forward", "O_rows[r0:r1] = rnd(h @ P.op(W_down[e], 0))",
+        "O_rows[r0:r1] = h @ P.op(W_down[e], 0)", ["out_fwd"]),
+    "y not rounded after the combine": (
+        moe, "forward", "return rnd(y), saved", "return y, saved", ["out_fwd"]),
+    "shared expert output not rounded": (
+        moe, "shared_forward", "O = out_round(out)(h @ Ws_down)", "O = h @ Ws_down",
+        ["out_fwd"]),
+    "routed dX rows not rounded before the reverse combine": (
+        moe, "backward", "dXg[r0:r1] = rnd(P.dx_act(du, 1)",
+        "dXg[r0:r1] = (P.dx_act(du, 1)", ["out_bwd"]),
+    "gradients not rounded after their sums": (
+        moe, "backward", "setattr(res, n, rnd(getattr(res, n)))",
+        "setattr(res, n, getattr(res, n))", ["out_bwd"]),
+    "shared expert dX row not rounded": (
+        moe, "shared_backward", "dXs = out_round(out)(", "dXs = (", ["out_bwd"]),
+    "sampled y not rounded": (
+        sampled, "token_outputs", 'res = {"y": rnd(y), "y_unrounded": y}',
+        'res = {"y": y, "y_unrounded": y}', ["sampled_bf16"]),
+    "sampled expert output rows not rounded": (
+        sampled, "_row_terms", "O = rnd(h @ Wd)", "O = h @ Wd", ["sampled_bf16"]),
+    "sampled dW lines not rounded": (
+        sampled, "dw_lines", 'return {"dW_down": ro(hg @ dYe)', 'return {"dW_down": (hg @ dYe)',
+        ["dw_lines_out"]),
+    "sampled MXFP8 y: expert rows not rounded": (
+        sampled, "token_forward_mx", "y += float(gates[t, j]) * rnd(hq @ Wd)",
+        "y += float(gates[t, j]) * (hq @ Wd)", ["dw_lines_out"]),
+    "sampled MXFP8 dX rows not rounded": (
+        sampled, "token_backward_mx", "part = rnd(Wu_rows @ du + Wg_rows @ dv)",
+        "part = (Wu_rows @ du + Wg_rows @ dv)", ["mx_bwd_eval_bf16"]),
+    "sampled MXFP8 dW lines not rounded": (
+        sampled, "dw_lines_mx", 'res[i] = {"dW_down": ro(hg @ dYR)',
+        'res[i] = {"dW_down": (hg @ dYR)', ["mx_bwd_eval_bf16"]),
+    "sampled shared dW lines not rounded": (
+        sampled, "shared_dw_lines", '"dWs_up": ro(x.T @ rnd(D * silu(V)))',
+        '"dWs_up": (x.T @ rnd(D * silu(V)))', ["shared_lines_out"]),
     # the pins' own references
     "brute-force token forward drops the gate": (
         moe, "token_forward_bruteforce", "y += g * ((silu(v) * u) @ W_down[e])",
