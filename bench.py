@@ -4,7 +4,8 @@ forward and backward of one batch), as one JSON line.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Default workload: the Kimi-2.5-shaped layer (T=8192, H=7168, I=2048, E=384, top-8, one
-BF16 shared expert with I=2048), BF16. Inputs are seeded synthetic tensors resident in HBM;
+BF16 shared expert with I=2048), BF16: bf16 operands in every GEMM (the weight gradients'
+too), fp32 accumulation, bf16 results. Inputs are seeded synthetic tensors resident in HBM;
 the expert weights alone are 34 GB, far larger than the 129 MB L2, so no flush is needed
 between steps. Under torchrun each rank runs an independent replica on its own batch
 (weak scaling, no collective on the data path).
@@ -35,7 +36,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="kimi_8192")
+    ap.add_argument("--workload", default="kimi_8192_plain")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--fwd-path", default="auto", choices=["auto", "megakernel", "launches"])
     ap.add_argument("--comm-sms", type=int, default=0,
@@ -45,6 +46,8 @@ def parse():
     ap.add_argument("--out", default="", choices=["", "bf16", "fp32"],
                     help="result type of y, dX and the weight gradients (default: the "
                          "workload's, bf16)")
+    ap.add_argument("--tile-order", default="static", choices=["static", "dynamic"],
+                    help="tile order of the persistent grouped GEMMs")
     ap.add_argument("--no-sub", action="store_true",
                     help="skip the sub-records (fp32 results, forward megakernel, MXFP8)")
     ap.add_argument("--sub-steps", type=int, default=10,
@@ -195,6 +198,11 @@ def workload_json(cfg):
             "step": "plan + forward" + (" + backward" if cfg.backward else ""),
             "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k,
             "shared_I": cfg.shared_I, "precision": cfg.precision,
+            "operands": {"bf16_plain": "bf16 in every GEMM, fp32 accumulation",
+                         "bf16": "bf16, the weight-gradient GEMMs on bf16 hi + lo pairs",
+                         "mxfp8": "E4M3 + UE8M0 per 32 (routed experts), bf16 shared expert",
+                         }.get(cfg.precision, cfg.precision),
+            "results": f"{cfg.out} (y, dX, weight gradients); dgates, dWr fp32",
             "l2": (f"inputs larger than L2 (expert weights {weights_gb:.3g} GB), no flush"
                    if weights_gb * 1e9 > 129e6 else "inputs smaller than L2, no flush")}
 
@@ -368,6 +376,8 @@ def make_layer_for(cfg, args, device="cuda", fwd_path=None):
     L.set_fwd_path(fwd_path or args.fwd_path)
     mok.mok_set_comm_sms(L.ctx, args.comm_sms)
     mok.mok_set_sm_limit(L.ctx, args.sm_limit)
+    mok.mok_set_tile_order(L.ctx, mok.MOK_TILES_DYNAMIC if args.tile_order == "dynamic"
+                           else mok.MOK_TILES_STATIC)
     mx = None
     if cfg.precision == "mxfp8":
         mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"])
@@ -649,7 +659,10 @@ def run_gpu(args):
         plans = []
         if cfg.out == "bf16":
             plans.append(("fp32_results", dataclasses.replace(cfg, out="fp32"), None))
-        if args.workload == "kimi_8192":
+        if args.workload.startswith("kimi_8192"):
+            if cfg.precision == "bf16_plain":
+                # the weight-gradient GEMMs on bf16 hi + lo operand pairs (MOK_BF16)
+                plans.append(("bf16_hilo_wgrad", workload_config("kimi_8192"), None))
             plans.append(("megakernel_fwd", cfg, "megakernel"))
             plans.append(("mxfp8_dsv3_imbalanced", workload_config("dsv3_imbalanced"), None))
         for name, c2, path in plans:
@@ -672,7 +685,8 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
             "config": dict(workload_json(cfg), out=cfg.out, **mb,
-                           fwd_path=args.fwd_path, parallelism=f"replicas x{world}"),
+                           fwd_path=args.fwd_path, tile_order=args.tile_order,
+                           parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
             "megakernel_phases_ms": phases or None,
             **a,

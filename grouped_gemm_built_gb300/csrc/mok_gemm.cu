@@ -759,6 +759,17 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
     const uint32_t t_row = tmem_base + acc * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
     const bool have = ti.kiters > 0;
     float a[32], b[32];
+    // The accumulator is handed back to the MMA lane right after this thread's last TMEM
+    // load (before that chunk's math and stores), so the next tile's MMAs can start while
+    // the stores drain; with one accumulator (MXFP8) this is the overlap there is.
+    bool released = false;
+    auto release = [&]() {
+      if (!released) {
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+        released = true;
+      }
+    };
     // tcgen05.ld and the staged stores are warp-collective: every lane takes part, rows
     // outside the problem only skip their global loads (TMA drops their stores).
     const int row = ti.row0 + r;
@@ -771,6 +782,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         for (int c = 0; c < 4; ++c) {
           tmem_ld32(t_row + c * 32, a);          // U
           tmem_ld32(t_row + 128 + c * 32, b);    // V
+          if (c == 3) release();
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
@@ -804,6 +816,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
       case kRouter: {  // logits fp32 (+ bias), ordinary stores of the row's valid columns
         for (int c = 0; c < p.BN / 32; ++c) {
           tmem_ld32(t_row + c * 32, a);
+          if (c == p.BN / 32 - 1) release();
           const int col0 = ti.n0 + c * 32;
           if (valid) {
             float* dst = p.logits + (size_t)row * p.n_out;
@@ -820,11 +833,13 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
           for (int c = 0; c < p.BN / 32; c += 2) {
             tmem_ld32(t_row + c * 32, a);
             tmem_ld32(t_row + (c + 1) * 32, b);
+            if (c + 2 >= p.BN / 32) release();
             st.bf16x64(&mp.o[0], a, b, ti.n0 + c * 32, wrow);
           }
         } else {
           for (int c = 0; c < p.BN / 32; ++c) {
             tmem_ld32(t_row + c * 32, a);
+            if (c == p.BN / 32 - 1) release();
             st.f32(&mp.o[0], a, ti.n0 + c * 32, wrow);
           }
         }
@@ -849,6 +864,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         for (int c = 0; c < p.BN / 32; ++c) {
           const int col = ti.n0 + c * 32;
           tmem_ld32(t_row + c * 32, a);          // D = dY W_down^T
+          if (c == p.BN / 32 - 1) release();
           float u[32], v[32];
           if (have_uv) {
             if (MX) {                            // saved U, V (bf16 in MXFP8)
@@ -926,6 +942,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
 #pragma unroll
               for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.f;
             }
+            if (c + 2 >= p.BN / 32) release();
             st.bf16x64(&mp.o[0], a, b, ti.n0 + c * 32, orow);
           }
           break;
@@ -936,6 +953,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = 0.f;
           }
+          if (c == p.BN / 32 - 1) release();
           st.f32(&mp.o[0], a, ti.n0 + c * 32, orow);
         }
         break;
@@ -962,6 +980,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
 #pragma unroll
               for (int i = 0; i < 32; ++i) b[i] = a1[i] = 0.f;
             }
+            if (c == 2) release();
             st.bf16x64(&mp.o[1], b, a1, ti.n0 + c * 32, orow);
           }
           break;
@@ -974,14 +993,14 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = b[i] = 0.f;
           }
+          if (c == 3) release();
           st.f32(&mp.o[0], a, ti.n0 + c * 32, orow);
           st.f32(&mp.o[1], b, ti.n0 + c * 32, orow);
         }
         break;
       }
     }
-    tc_fence_before();
-    mbar_arrive(&acc_empty[acc]);
+    release();
   }
   return true;
 }

@@ -90,7 +90,7 @@ def test_backward_after_macrobatches_matches_one_launch_per_step(precision, slot
     padded rows) and the x rows are gathered again. y and every gradient equal, bit for
     bit, those of the one-launch-per-step path; and they match the oracle."""
     base = mi.scaled(_ring_case(precision), backward=True, router=True, zipf_s=0.0,
-                     shared_I=128)
+                     shared_I=128, E=12, k=4)
     sb = _slot_bytes(base)
     cfg = mi.scaled(base, ring_bytes=0 if slots == 4 else slots * sb + sb // 2)
     inp = gu.gpu_inputs(cfg, seed=9)
