@@ -63,8 +63,9 @@ constexpr int SPLIT_EXTRA_OFF = A_BYTES + B_BYTES;
 
 template <bool MX>
 struct Cfg {
-  static constexpr int STAGES = MX ? 3 : 4;          // most stages a launch uses (an MXFP8
-                                                     // stage holds twice the K)
+  // barrier slots: the most stages a launch uses (MXFP8: 3 or 4 full stages, or 6 of the
+  // dH launch's 128-column tiles, which need a third less)
+  static constexpr int STAGES = MX ? 6 : 4;
   static constexpr int BK = MX ? 128 : 64;           // K elements per stage (128 bytes/row)
   static constexpr int MMA_K = MX ? 32 : 16;         // K elements per instruction
   static constexpr int MN_CHUNK = MX ? 128 : 64;     // elements per 128-byte MN-major chunk
@@ -72,15 +73,25 @@ struct Cfg {
   static constexpr int MN_KSTEP = MMA_K * 128;       // bytes per instruction along K, MN-major
   static constexpr int SF_OFF = A_BYTES + B_BYTES;   // scale atoms: A 512 B, B 1024 B
   static constexpr int STAGE_BYTES = MX ? 51200 : 49152;
+  static constexpr int MX_STAGES = 3;                // MXFP8 stages of STAGE_BYTES (up|gate: 4)
+  static constexpr int MX_DH_STAGE_BYTES = 33792;    // A 16 KB, B 16 KB, atoms 1 KB
+  static constexpr int MX_DH_STAGES = 6;
   static constexpr int NACC = MX ? 1 : 2;             // accumulators of ACC_COLS columns
   static constexpr int ACC_COLS = 256;
   static constexpr int SF_TMEM = 256;                // MX: scale columns start here
-  // data area: the larger of (STAGES stages + 2 staging boxes per warp) and
-  // (STAGES - 1 stages + 4 staging boxes per warp), then barriers
+  // data area, then barriers. BF16: the larger of (STAGES stages + 2 staging boxes per
+  // warp) and (STAGES - 1 stages + 4 staging boxes per warp). MXFP8 (one accumulator per
+  // tile), per mode: the up|gate launch takes 4 stages and 1 staging box per warp (its
+  // tiles' K is long, the operands in flight bound it); the launches that store 256
+  // columns of results per tile take 3 stages and 4 boxes per warp, which hold a whole
+  // 128 x 256 tile of bf16 results, so the tile leaves its accumulator at once and the
+  // stores drain during the next tile's MMAs; dH (plain stores) takes 6 of its smaller
+  // stages. The largest of the three.
   static constexpr int DATA_BYTES =
-      (STAGES * STAGE_BYTES + OUT_STAGING > (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING)
-          ? STAGES * STAGE_BYTES + OUT_STAGING
-          : (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING;
+      MX ? (4 * STAGE_BYTES + OUT_STAGING / 2)
+         : ((STAGES * STAGE_BYTES + OUT_STAGING > (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING)
+                ? STAGES * STAGE_BYTES + OUT_STAGING
+                : (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING);
   static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 256;
 };
 
@@ -104,6 +115,7 @@ struct Params {
   int kiters;       // row-space modes: K iterations per tile
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
   int stage_bytes;  // bytes of one pipeline stage (Cfg::STAGE_BYTES or SPLIT_STAGE_BYTES)
+  int sf_off;       // MXFP8: offset of the stage's scale atoms
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
   int out_bf16;     // kFwdDown, kBwdDX, dW modes: round the outputs to bf16 (64-column boxes)
   int* tile_counter;// dynamic tile order: the next tile is atomicAdd(tile_counter, 1) (zero at
@@ -296,19 +308,24 @@ __device__ __forceinline__ void quant_rowblock(const float (&x)[32], int lane, b
   uint32_t w[8];
   uint32_t my_sb = 127u;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[i])));
-    uint32_t sb = 127u;
-    if (am != 0u) {
-      const int bb = (int)((am >> 23) & 0xFF) - 8;
-      sb = (uint32_t)(bb < 0 ? 0 : bb);
+  for (int i = 0; i < 32; i += 2) {
+    // two columns per step: each its own warp-wide maximum and scale, one conversion
+    float inv[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x[i + c])));
+      uint32_t sb = 127u;
+      if (am != 0u) {
+        const int bb = (int)((am >> 23) & 0xFF) - 8;
+        sb = (uint32_t)(bb < 0 ? 0 : bb);
+      }
+      if (i + c == lane) my_sb = sb;
+      inv[c] = __uint_as_float((254u - sb) << 23);
     }
-    if (i == lane) my_sb = sb;
-    const float inv = __uint_as_float((254u - sb) << 23);
-    const uint32_t code =
-        __nv_cvt_float2_to_fp8x2(make_float2(x[i] * inv, 0.f), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+    const uint32_t code2 = __nv_cvt_float2_to_fp8x2(make_float2(x[i] * inv[0], x[i + 1] * inv[1]),
+                                                    __NV_SATFINITE, __NV_E4M3) & 0xFFFFu;
     if ((i & 3) == 0) w[i >> 2] = 0;
-    w[i >> 2] |= code << (8 * (i & 3));
+    w[i >> 2] |= code2 << (8 * (i & 3));
   }
   if (valid) {
     uint4* dq = reinterpret_cast<uint4*>(codes);
@@ -331,7 +348,8 @@ struct Stager {
     uint8_t* b = buf + (n & (nbuf - 1)) * STAGE_OUT_BYTES;
     if (n >= (uint32_t)nbuf && lane == 0) {
       if (nbuf == 4) bulk_wait_read<3>();
-      else bulk_wait_read<1>();
+      else if (nbuf == 2) bulk_wait_read<1>();
+      else bulk_wait_read<0>();
     }
     __syncwarp();
     return b;
@@ -454,7 +472,7 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
       }
       uint8_t* sa = smem + stage * p.stage_bytes;
       uint8_t* sb = sa + A_BYTES;
-      uint8_t* sf = sa + C::SF_OFF;
+      uint8_t* sf = sa + p.sf_off;
       uint64_t* bar = &full[stage];
       uint32_t extra = 0;   // split dW stages also carry the lo half of the split operand
       if (sp) extra = p.mode == kBwdDWUpGate ? 2 * 128 * 128 : BM * 128;
@@ -662,9 +680,9 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
         const uint32_t col = C::SF_TMEM + stage * 16;
         t_sfa = tmem_base + col;
         t_sfb = tmem_base + col + 4;
-        tmem_cp_32x128b_x4(t_sfa, smem_desc_rows16(sa + C::SF_OFF));
+        tmem_cp_32x128b_x4(t_sfa, smem_desc_rows16(sa + p.sf_off));
         for (int j = 0; j < n_mma / 128; ++j)
-          tmem_cp_32x128b_x4(t_sfb + 4 * j, smem_desc_rows16(sa + C::SF_OFF + 512 + 512 * j));
+          tmem_cp_32x128b_x4(t_sfb + 4 * j, smem_desc_rows16(sa + p.sf_off + 512 + 512 * j));
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -778,38 +796,53 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
     switch (p.mode) {
       case kFwdUpGate: {
         const size_t o = (size_t)row * p.I + ti.n0;
-        uint32_t sbytes = 0;
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(t_row + c * 32, a);          // U
-          tmem_ld32(t_row + 128 + c * 32, b);    // V
-          if (c == 3) release();
-          float h[32];
+        if constexpr (MX) {
+          uint32_t sbytes = 0;
+          // two 32-column chunks at a time: U, V leave as bf16 in 64-column boxes, h as
+          // MXFP8 blocks of 32 along I (plain stores of the codes, the scale word below)
+          for (int c = 0; c < 4; c += 2) {
+            float a1[32], b1[32];
+            tmem_ld32(t_row + c * 32, a);               // U
+            tmem_ld32(t_row + 128 + c * 32, b);         // V
+            tmem_ld32(t_row + (c + 1) * 32, a1);
+            tmem_ld32(t_row + 128 + (c + 1) * 32, b1);
+            if (c == 2) release();
+            for (int half = 0; half < 2; ++half) {
+              const float* uu = half ? a1 : a;
+              const float* vv = half ? b1 : b;
+              float h[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
-          const int col = ti.n0 + c * 32;
-          if (MX) {   // h feeds the down GEMM as MXFP8 blocks of 32 along I
-            uint4 q[2];
-            sbytes |= quant32_e4m3(h, q) << (8 * c);
-            if (valid) {
-              uint4* dq = reinterpret_cast<uint4*>(p.out_q[0] + o + c * 32);
-              dq[0] = q[0];
-              dq[1] = q[1];
+              for (int i = 0; i < 32; ++i) h[i] = vv[i] * sigmoidf_(vv[i]) * uu[i];
+              uint4 q[2];
+              sbytes |= quant32_e4m3(h, q) << (8 * (c + half));
+              if (valid) {
+                uint4* dq = reinterpret_cast<uint4*>(p.out_q[0] + o + (c + half) * 32);
+                dq[0] = q[0];
+                dq[1] = q[1];
+              }
             }
-          } else {
-            st.bf16(&mp.o[0], h, col, wrow);     // h, bf16 operand of the down GEMM
+            st.bf16x64(&mp.o[1], a, a1, ti.n0 + c * 32, wrow);
+            st.bf16x64(&mp.o[2], b, b1, ti.n0 + c * 32, wrow);
           }
-          if (MX) {   // saved U, V in bf16: the backward quantises du, dv to E4M3 anyway
-            st.bf16(&mp.o[1], a, col, wrow);
-            st.bf16(&mp.o[2], b, col, wrow);
-          } else {    // saved U, V in fp32
+          if (valid) {
+            const size_t atom = (size_t)(row / BM) * (p.I / 128) + ti.n0 / 128;
+            *reinterpret_cast<uint32_t*>(p.out_sf[0] + atom * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
+                sbytes;
+          }
+        } else {
+          // BF16: h as the down GEMM's bf16 operand, U, V saved in fp32
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(t_row + c * 32, a);          // U
+            tmem_ld32(t_row + 128 + c * 32, b);    // V
+            if (c == 3) release();
+            float h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
+            const int col = ti.n0 + c * 32;
+            st.bf16(&mp.o[0], h, col, wrow);
             st.f32(&mp.o[1], a, col, wrow);
             st.f32(&mp.o[2], b, col, wrow);
           }
-        }
-        if (MX && valid) {
-          const size_t atom = (size_t)(row / BM) * (p.I / 128) + ti.n0 / 128;
-          *reinterpret_cast<uint32_t*>(p.out_sf[0] + atom * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
-              sbytes;
         }
         break;
       }
@@ -1780,9 +1813,10 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.timeout_ns = c.timeout_ns > 0 ? c.timeout_ns : kTimeoutNs;
   // Modes without split keep the full operand ring (trading a stage for deeper output
   // staging made the dW modes slower).
-  p.stages = C::STAGES;
+  p.stages = MX ? C::MX_STAGES : C::STAGES;
   p.nbuf = 2;
   p.stage_bytes = C::STAGE_BYTES;
+  p.sf_off = C::SF_OFF;
   p.nacc = C::NACC;
   p.acc_cols = C::ACC_COLS;
   if (p.split) {   // two chunk-sized hi/lo stages leave room for 4 staging boxes per warp
@@ -1790,6 +1824,24 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
     p.nbuf = 4;
     p.stage_bytes = SPLIT_STAGE_BYTES;
   }
+  // MXFP8 stages and staging per mode (see Cfg::DATA_BYTES)
+  if (MX) {
+    p.nbuf = 4;
+    if (c.mode == kFwdUpGate) {
+      p.stages = 4;
+      p.nbuf = 1;
+    } else if (c.mode == kBwdDH) {
+      p.stages = C::MX_DH_STAGES;
+      p.stage_bytes = C::MX_DH_STAGE_BYTES;
+      p.sf_off = A_BYTES + A_BYTES;
+    }
+  }
+  static_assert(4 * Cfg<true>::STAGE_BYTES + OUT_STAGING / 2 <= Cfg<true>::DATA_BYTES &&
+                    3 * Cfg<true>::STAGE_BYTES + 2 * OUT_STAGING <= Cfg<true>::DATA_BYTES &&
+                    Cfg<true>::MX_DH_STAGES * Cfg<true>::MX_DH_STAGE_BYTES <= Cfg<true>::DATA_BYTES,
+                "MXFP8 stages and staging exceed the data area");
+  static_assert(Cfg<true>::MX_DH_STAGE_BYTES % 1024 == 0 && Cfg<true>::STAGE_BYTES % 1024 == 0,
+                "stages must keep the 1024-byte alignment of the swizzled tiles");
   p.poff = c.poff;
   p.counts = c.counts;
   p.offsets = c.offsets;
@@ -1833,8 +1885,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
            make_map(&mp.b[0], c.b[0], c.I, G * c.H, BK, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, BK, eb) &&
            (MX || make_out_map(&mp.o[0], c.out[0], c.I, rows, 2)) &&
-           make_out_map(&mp.o[1], c.out[1], c.I, rows, MX ? 2 : 4) &&
-           make_out_map(&mp.o[2], c.out[2], c.I, rows, MX ? 2 : 4);
+           make_out_map(&mp.o[1], c.out[1], c.I, rows, MX ? 2 : 4, MX) &&
+           make_out_map(&mp.o[2], c.out[2], c.I, rows, MX ? 2 : 4, MX);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kFwdDown:
@@ -1982,7 +2034,12 @@ cudaError_t launch_mega_impl(const MegaCall& c, int num_sms, cudaStream_t s) {
   cudaError_t e = build_call<MX>(c.up, q.up, mm.up, mt);
   if (e != cudaSuccess) return e;
   if ((e = build_call<MX>(c.down, q.down, mm.down, mt)) != cudaSuccess) return e;
-  // both phases share the CTA's stage ring, staging boxes and accumulator sequence
+  // both phases share the CTA's stage ring, staging boxes and accumulator sequence: MXFP8
+  // takes the down GEMM's setting for both
+  if (MX) {
+    q.up.stages = q.down.stages;
+    q.up.nbuf = q.down.nbuf;
+  }
   if (q.up.stages != q.down.stages || q.up.stage_bytes != q.down.stage_bytes ||
       q.up.nbuf != q.down.nbuf || q.up.nacc != q.down.nacc || q.up.acc_cols != q.down.acc_cols)
     return cudaErrorInvalidValue;

@@ -66,6 +66,8 @@ CONFIGS = {
     # Kimi-2.5 expert shape with 24 experts and the same ~171 rows per expert as T=8192:
     # a few GB on the device, for detailed kernel profiles.
     "kimi_e24_profile": MoEConfig("kimi_e24_profile", T=512, H=7168, I=2048, E=24, k=8),
+    "kimi_e24_profile_plain": MoEConfig("kimi_e24_profile_plain", T=512, H=7168, I=2048,
+                                        E=24, k=8, precision="bf16_plain"),
     # DeepSeek-V3 expert shape in MXFP8 with 16 experts and the same ~512 rows per expert
     # as T=16384 with 256 experts: a few GB on the device, for detailed kernel profiles.
     "dsv3_e16_profile": MoEConfig("dsv3_e16_profile", T=1024, H=7168, I=2048, E=16, k=8,
