@@ -74,8 +74,8 @@ struct Cfg {
   static constexpr int SF_OFF = A_BYTES + B_BYTES;   // scale atoms: A 512 B, B 1024 B
   static constexpr int STAGE_BYTES = MX ? 51200 : 49152;
   static constexpr int MX_STAGES = 3;                // MXFP8 stages of STAGE_BYTES (up|gate: 4)
-  static constexpr int MX_DH_STAGE_BYTES = 33792;    // A 16 KB, B 16 KB, atoms 1 KB
-  static constexpr int MX_DH_STAGES = 6;
+  static constexpr int MX_DH_STAGE_BYTES = 67584;    // 2 x (A 16 KB, B 16 KB, atoms 1 KB)
+  static constexpr int MX_DH_STAGES = 3;
   static constexpr int NACC = MX ? 1 : 2;             // accumulators of ACC_COLS columns
   static constexpr int ACC_COLS = 256;
   static constexpr int SF_TMEM = 256;                // MX: scale columns start here
@@ -116,6 +116,9 @@ struct Params {
   int split;        // 1: the dW GEMMs run hi and lo halves of their computed operand
   int stage_bytes;  // bytes of one pipeline stage (Cfg::STAGE_BYTES or SPLIT_STAGE_BYTES)
   int sf_off;       // MXFP8: offset of the stage's scale atoms
+  int kdouble;      // MXFP8 dH: a stage holds two 128-element K chunks of each operand (A0,
+                    // A1, B0, B1 of 16 KB, then the atoms A0, A1, B0, B1): half the barrier,
+                    // scale-copy and commit work per MMA of these short 128-column tiles
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
   int out_bf16;     // kFwdDown, kBwdDX, dW modes: round the outputs to bf16 (64-column boxes)
   int* tile_counter;// dynamic tile order: the next tile is atomicAdd(tile_counter, 1) (zero at
@@ -476,6 +479,7 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
       uint64_t* bar = &full[stage];
       uint32_t extra = 0;   // split dW stages also carry the lo half of the split operand
       if (sp) extra = p.mode == kBwdDWUpGate ? 2 * 128 * 128 : BM * 128;
+      if (MX && p.kdouble) extra = A_BYTES + b_bytes;   // the second K chunk
       mbar_arrive_expect_tx(bar, A_BYTES + b_bytes + extra);
       const int k0 = kb * BK;
       switch (p.mode) {
@@ -514,6 +518,18 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
           break;
         }
         case kBwdDH: {       // A: dYg rows (K-major); B: W_down rows i (K-major over H)
+          if (MX && p.kdouble) {   // two K chunks: A0 A1 B0 B1, then atoms A0 A1 B0 B1
+            for (int h = 0; h < 2; ++h) {
+              const int kc = 2 * kb + h;
+              tma_load_2d(sa + h * A_BYTES, &mp.a[0], bar, kc * BK, ti.arow0);
+              tma_load_2d(sa + (2 + h) * A_BYTES, &mp.b[0], bar, kc * BK, ti.e * p.I + ti.n0);
+              bulk_load(sf + h * 512, p.sfa + ((size_t)(ti.arow0 / BM) * p.kcs_a + kc) * 512, 512,
+                        bar);
+              const size_t bi = (((size_t)ti.e * p.kcs_b + kc) * p.ncs_b + ti.n0 / 128) * 512;
+              bulk_load(sf + 1024 + h * 512, p.sfb0 + bi, 512, bar);
+            }
+            break;
+          }
           tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
           tma_load_2d(sb, &mp.b[0], bar, k0, ti.e * p.I + ti.n0);
           if (MX) {
@@ -675,6 +691,25 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
       // MMA K steps of this stage: all four, except in a dW tile's last K iteration
       const int nk = (is_dw(p.mode) && kb == ti.kiters - 1) ? ti.klast : 4;
       uint32_t t_sfa = 0, t_sfb = 0;
+      if (MX && p.kdouble) {
+        // two K chunks of 128: atoms A0, A1 -> columns 0-3, 4-7; B0, B1 -> 8-11, 12-15
+        const uint32_t t_sf = tmem_base + C::SF_TMEM + stage * 16;
+        for (int j = 0; j < 4; ++j)
+          tmem_cp_32x128b_x4(t_sf + 4 * j, smem_desc_rows16(sa + p.sf_off + 512 * j));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = umma_desc_sw128(sa + h * A_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(sa + (2 + h) * A_BYTES + kk * 32, 16, 1024);
+            const uint32_t accum = (kb > 0 || h > 0 || kk > 0) ? 1u : 0u;
+            umma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, n_mma, false, false, kk), t_sf + 4 * h,
+                      t_sf + 8 + 4 * h, accum);
+          }
+        }
+        umma_commit(&empty[stage]);
+        continue;
+      }
       if (MX) {
         // scale atoms -> TMEM: A in 4 columns, B in 4 columns per 128 rows of N
         const uint32_t col = C::SF_TMEM + stage * 16;
@@ -1830,10 +1865,11 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
     if (c.mode == kFwdUpGate) {
       p.stages = 4;
       p.nbuf = 1;
-    } else if (c.mode == kBwdDH) {
+    } else if (c.mode == kBwdDH && c.H % 256 == 0) {
       p.stages = C::MX_DH_STAGES;
       p.stage_bytes = C::MX_DH_STAGE_BYTES;
-      p.sf_off = A_BYTES + A_BYTES;
+      p.sf_off = 4 * A_BYTES;
+      p.kdouble = 1;
     }
   }
   static_assert(4 * Cfg<true>::STAGE_BYTES + OUT_STAGING / 2 <= Cfg<true>::DATA_BYTES &&
@@ -1923,7 +1959,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
         p.acc_cols = 128;
       }
       p.n_tiles = c.I / p.BN;
-      p.kiters = c.H / BK;
+      p.kiters = c.H / BK / (p.kdouble ? 2 : 1);
       p.kcs_a = c.H / 128;
       p.kcs_b = c.H / 128;
       p.ncs_b = c.I / 128;
