@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--out", default="", choices=["", "bf16", "fp32"],
                     help="result type of y, dX and the weight gradients (default: the "
                          "workload's, bf16)")
-    ap.add_argument("--tile-order", default="static", choices=["static", "dynamic"],
+    ap.add_argument("--tile-order", default="static", choices=["static", "dynamic", "clc"],
                     help="tile order of the persistent grouped GEMMs")
     ap.add_argument("--no-sub", action="store_true",
                     help="skip the sub-records (fp32 results, forward megakernel, MXFP8)")
@@ -380,8 +380,9 @@ def make_layer_for(cfg, args, device="cuda", fwd_path=None):
     L.set_fwd_path(fwd_path or args.fwd_path)
     mok.mok_set_comm_sms(L.ctx, args.comm_sms)
     mok.mok_set_sm_limit(L.ctx, args.sm_limit)
-    mok.mok_set_tile_order(L.ctx, mok.MOK_TILES_DYNAMIC if args.tile_order == "dynamic"
-                           else mok.MOK_TILES_STATIC)
+    mok.mok_set_tile_order(L.ctx, {"static": mok.MOK_TILES_STATIC,
+                                   "dynamic": mok.MOK_TILES_DYNAMIC,
+                                   "clc": mok.MOK_TILES_CLC}[args.tile_order])
     mx = None
     if cfg.precision == "mxfp8":
         mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"])

@@ -68,10 +68,13 @@ static int launch_sms(mok_ctx_t ctx) {
 }
 
 // the context's bound on device waits and its tile order, applied to one GEMM call
-static mok::GemmCall timed(mok::GemmCall c, mok_ctx_t ctx) {
+// (ordered = false: the static order, for the router GEMM of mok_plan)
+static mok::GemmCall timed(mok::GemmCall c, mok_ctx_t ctx, bool ordered = true) {
   c.timeout_ns = ctx->wait_timeout_ns;
   c.tile_counter = nullptr;
-  if (ctx->tcnt && ctx->tcnt_used < mok::kTileCounters) c.tile_counter = ctx->tcnt + ctx->tcnt_used++;
+  if (ordered && ctx->tcnt && ctx->tcnt_used < mok::kTileCounters)
+    c.tile_counter = ctx->tcnt + ctx->tcnt_used++;
+  c.clc = ordered && ctx->tile_order == MOK_TILES_CLC;
   return c;
 }
 // start of a call's launches: its tile counters (zeroed here, one per GEMM launch)
@@ -387,7 +390,8 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p) {
 
 mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
-  if (order != MOK_TILES_STATIC && order != MOK_TILES_DYNAMIC) return MOK_ERR_INVALID_ARG;
+  if (order != MOK_TILES_STATIC && order != MOK_TILES_DYNAMIC && order != MOK_TILES_CLC)
+    return MOK_ERR_INVALID_ARG;
   ctx->tile_order = order;
   return MOK_OK;
 }
@@ -490,7 +494,7 @@ mok_status mok_plan(mok_ctx_t ctx, const void* x, const float* Wr, const float* 
     c.b[0] = wr3;
     c.out[0] = logits;
     c.status = a.status;
-    MOK_LAUNCH("router_logits", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
+    MOK_LAUNCH("router_logits", launch_gemm(timed(c, ctx, false), launch_sms(ctx), s));
   }
   MOK_LAUNCH("topk_rank", launch_topk_rank(d, d.router ? logits : nullptr, sched->topk_idx,
                                             sched->gates, hist, lrank, a.status, s));

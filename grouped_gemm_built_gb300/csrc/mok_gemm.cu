@@ -92,7 +92,10 @@ struct Cfg {
          : ((STAGES * STAGE_BYTES + OUT_STAGING > (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING)
                 ? STAGES * STAGE_BYTES + OUT_STAGING
                 : (STAGES - 1) * STAGE_BYTES + 2 * OUT_STAGING);
-  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + 256;
+  // + 1024 alignment slack, + barriers and flags (256), + the cluster-launch-control
+  // barrier and answer (at BAR_BYTES / 2 of the barrier area)
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = DATA_BYTES + 1024 + BAR_BYTES;
 };
 
 // Tensor maps of one launch: operands a[], b[] (loads) and outputs o[] (stores).
@@ -123,6 +126,8 @@ struct Params {
   int out_bf16;     // kFwdDown, kBwdDX, dW modes: round the outputs to bf16 (64-column boxes)
   int* tile_counter;// dynamic tile order: the next tile is atomicAdd(tile_counter, 1) (zero at
                     // launch); null: the static order (tile blockIdx.x, + gridDim.x, ...)
+  int clc;          // cluster launch control: one CTA per tile; a CTA runs tile blockIdx.x,
+                    // then the tiles of the not yet launched CTAs it cancels
   uint64_t timeout_ns;  // bound of every wait (MOK_ERR_TIMEOUT when it passes)
   int n_out;        // kRouter: output columns (E)
   const float* bias;// kRouter: logit bias or null
@@ -168,7 +173,7 @@ struct TileInfo {
   int skip;     // 1: no tile here (the unmatched half of the last row-tile pair)
 };
 
-__device__ __forceinline__ bool is_dw(int mode) { return mode == kBwdDWDown || mode == kBwdDWUpGate; }
+__host__ __device__ __forceinline__ bool is_dw(int mode) { return mode == kBwdDWDown || mode == kBwdDWUpGate; }
 
 __device__ __forceinline__ int routed_mtiles(const Params& p) {
   return min(max(*p.num_mtiles, 0), (p.M_rows + BM - 1) / BM);
@@ -420,8 +425,12 @@ struct Stager {
 // it is ready for one, and passes it to the CTA's MMA lane and epilogue warps through a
 // queue of TQ slots in shared memory (slot q: tile id, "full" barrier of 1 arrival, "empty"
 // barrier of 5: the MMA lane and one lane per epilogue warp). A CTA whose tiles run long
-// then simply takes fewer of them. The queue ends with tile -1. Which CTA runs a tile
-// changes nothing in it: each output tile is one CTA's fixed-order sum either way.
+// then simply takes fewer of them. The queue ends with tile -1. Cluster launch control
+// ([I], the paragraph on CLC) feeds the same queue: the grid has a CTA per tile, a CTA
+// starts with tile blockIdx.x, and the producer lane asks the hardware to cancel a CTA that
+// has not been launched yet and takes over its tile; it asks for the next one as soon as it
+// starts a tile, so the answer is there when the tile's loads are issued. Which CTA runs a
+// tile changes nothing in it: each output tile is one CTA's fixed-order sum in every order.
 struct TileQueue {
   volatile int* tile;
   uint64_t* full;
@@ -611,29 +620,82 @@ __device__ void produce_drain(const Params& p, uint64_t* full, uint64_t* empty,
   }
 }
 
+// Cluster-launch-control requests of one producer lane: at most one in flight.
+struct ClcState {
+  uint64_t* bar;
+  uint8_t* answer;     // 16 bytes, 16-byte aligned
+  uint32_t made = 0;   // answered requests (the phase of bar)
+  bool in_flight = false;
+  bool ended = false;  // an answer said no CTA was left: no further request may be made
+};
+__device__ __forceinline__ void clc_ask(ClcState& c) {
+  if (c.ended || c.in_flight) return;
+  if (c.made) fence_proxy_async_smem();   // the last answer's reads before the next write
+  mbar_arrive_expect_tx(c.bar, 16);
+  clc_try_cancel(c.answer, c.bar);
+  c.in_flight = true;
+}
+// The answer of the request in flight: the cancelled CTA's index, or -1 (none left). False
+// after a timed-out wait.
+__device__ __forceinline__ bool clc_answer(const Params& p, ClcState& c, int& x) {
+  if (!mbar_wait(c.bar, c.made & 1, globaltimer_ns() + p.timeout_ns)) return false;
+  ++c.made;
+  c.in_flight = false;
+  x = clc_cancelled_x(c.answer);
+  if (x < 0) c.ended = true;
+  return true;
+}
+
 template <bool MX>
 __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
-                        uint64_t* empty, volatile int* abort_flag, const TileQueue& tq) {
+                        uint64_t* empty, volatile int* abort_flag, const TileQueue& tq,
+                        ClcState& clc) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
-  if (!p.tile_counter) {
+  if (!p.tile_counter && !p.clc) {
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
       if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
     }
   } else {
+    int own = p.clc ? (int)blockIdx.x : -1;   // CLC: the CTA's own tile comes first
     for (uint32_t n = 0;; ++n) {
       int tile;
       TileInfo ti;
-      do {   // the next tile that is not the unmatched half of a row-tile pair
-        tile = atomicAdd(p.tile_counter, 1);
+      bool ok = true;
+      for (;;) {   // the next tile that is not the unmatched half of a row-tile pair
+        if (!p.clc) {
+          tile = atomicAdd(p.tile_counter, 1);
+        } else if (own >= 0) {
+          tile = own;
+          own = -1;
+        } else {
+          clc_ask(clc);                 // (already in flight after the previous tile)
+          if (clc.ended) {
+            tile = -1;
+            break;
+          }
+          if (!clc_answer(p, clc, tile)) {
+            ok = false;
+            break;
+          }
+          if (tile < 0) break;
+        }
         if (tile >= ntiles) {
           tile = -1;
           break;
         }
         ti = tile_info<MX>(p, tile);
-      } while (ti.skip);
+        if (!ti.skip) break;
+      }
+      if (!ok) {   // no answer in time: end the queue so the consumers stop too
+        set_error(p.status, kErrTimeout);
+        *abort_flag = 1;
+        tile = -1;
+      } else if (p.clc && tile >= 0) {
+        clc_ask(clc);   // the answer arrives while this tile's loads run
+      }
       if (!tq_publish(p, tq, n, tile)) {
         set_error(p.status, kErrTimeout);
         *abort_flag = 1;
@@ -763,7 +825,7 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
-  if (!p.tile_counter) {
+  if (!p.tile_counter && !p.clc) {
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
@@ -1081,7 +1143,7 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   const int ntiles = num_tiles_of(p);
   Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
   int local = 0;
-  if (!p.tile_counter) {
+  if (!p.tile_counter && !p.clc) {
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
@@ -1124,6 +1186,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   Params p = p_in;
   p.mode = MODE;
   p.split = SPLIT;
+  // CLC: the grid is sized to the largest tile count; a CTA past the actual count (which
+  // the plan wrote to device memory) has no tile and leaves before taking any resource
+  if (p.clc && (int)blockIdx.x >= num_tiles_of(p)) return;
   constexpr int STAGES = C::STAGES;   // barrier slots; the launch uses p.stages of them
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1138,6 +1203,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq.empty + TQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   tq.tile = abort_flag + 1;
+  ClcState clc;
+  clc.bar = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES + C::BAR_BYTES / 2);
+  clc.answer = smem + C::DATA_BYTES + C::BAR_BYTES / 2 + 16;
+  static_assert(C::DATA_BYTES % 16 == 0 && 2 * TQ * 8 + 2 * C::STAGES * 8 + 32 + 8 + 4 * TQ <=
+                    C::BAR_BYTES / 2, "barrier area overlaps the CLC answer");
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -1153,6 +1223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&tq.full[q], 1);
       mbar_init(&tq.empty[q], 5);   // the MMA lane and lane 0 of each epilogue warp
     }
+    mbar_init(clc.bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mp.a[0]);
@@ -1165,7 +1236,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (threadIdx.x == 0) produce<MX>(p, mp, smem, full, empty, abort_flag, tq);
+    if (threadIdx.x == 0) {
+      produce<MX>(p, mp, smem, full, empty, abort_flag, tq, clc);
+      // leave no request in flight: its answer is written to this CTA's shared memory
+      int unused;
+      if (clc.in_flight && !clc_answer(p, clc, unused)) set_error(p.status, kErrTimeout);
+    }
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0)
       mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, tq);
@@ -1889,6 +1965,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.v = c.v;
   p.uv_row = c.uv_row;
   p.tile_counter = c.tile_counter;
+  p.clc = c.clc ? 1 : 0;
   p.dgp = c.dgp;
   p.status = c.status;
   p.sfa = static_cast<const uint8_t*>(c.sfa);
@@ -2002,6 +2079,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       max_tiles = p.groups * p.m_tiles_dw * p.n_tiles;
       break;
   }
+  // routed row-space launches number their tiles in row-tile pairs (num_tiles_of)
+  if (!p.dense && !is_dw(c.mode)) max_tiles = (mt_rows + 1) / 2 * 2 * p.n_tiles;
   if (!ok) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
@@ -2042,7 +2121,9 @@ cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set[c.mode][p.split ? 1 : 0] = true;
   }
-  int grid = max_tiles < num_sms ? max_tiles : num_sms;
+  // persistent: one CTA per SM; CLC: one CTA per tile (the hardware keeps one per SM
+  // running and the running CTAs cancel the rest)
+  int grid = p.clc ? max_tiles : (max_tiles < num_sms ? max_tiles : num_sms);
   if (grid < 1) grid = 1;
   kern<<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(mp, p);
   return cudaGetLastError();

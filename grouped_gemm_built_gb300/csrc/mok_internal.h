@@ -223,6 +223,7 @@ struct GemmCall {
   uint32_t* status;
   uint64_t timeout_ns;  // bound of every device wait (0: 2 s)
   int* tile_counter;    // dynamic tile order: a zeroed int of device memory (null: static)
+  bool clc = false;     // tiles handed out by cluster launch control (one CTA per tile)
   // MXFP8 (E4M3 operands with 512-byte scale atoms; see mok_quant.cu)
   bool mx;
   const void* sfa; const void* sfa1;                   // A scale atoms (second: kBwdDX dv)

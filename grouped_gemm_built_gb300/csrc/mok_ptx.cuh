@@ -65,6 +65,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// ------------------------------------------------------------------ cluster launch control
+// A running CTA asks the hardware to cancel one CTA of the same grid that has not been
+// launched yet and to hand over its index ([I], the paragraph on CLC). The 16-byte answer
+// is written to shared memory (16-byte aligned) by the async proxy and completes `bar` with
+// 16 transaction bytes; the caller arms `bar` with mbar_arrive_expect_tx(bar, 16) first.
+// Once an answer has said "nothing left", no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(void* answer, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(smem_u32(answer)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// Decodes an answer: the cancelled CTA's x index, or -1 when no CTA was cancelled.
+__device__ __forceinline__ int clc_cancelled_x(const void* answer) {
+  uint32_t x = 0xffffffffu;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b128 R;\n\t"
+      "ld.shared.b128 R, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 P, R;\n\t"
+      "@P clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, R;\n\t}"
+      : "+r"(x)
+      : "r"(smem_u32(answer))
+      : "memory");
+  return (int)x;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -29,6 +29,7 @@ MOK_OUT_BF16 = 0
 MOK_OUT_F32 = 1
 MOK_TILES_STATIC = 0
 MOK_TILES_DYNAMIC = 1
+MOK_TILES_CLC = 2
 MOK_FWD_MEGAKERNEL = 0
 MOK_FWD_LAUNCHES = 1
 MOK_FWD_AUTO = 2

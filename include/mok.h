@@ -97,8 +97,15 @@ typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1, MOK_FWD_AUTO = 2 } 
  * MOK_TILES_STATIC (default): CTA b takes tiles b, b + G, b + 2G, ... (G CTAs);
  * MOK_TILES_DYNAMIC: each CTA takes the next tile from a device counter when it is ready
  *   for one, so CTAs whose tiles run long (the weight gradients of busy experts) take
- *   fewer. Every output tile is one CTA's fixed-order sum either way: same bits. */
-typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1 } mok_tile_order;
+ *   fewer;
+ * MOK_TILES_CLC: cluster launch control, the hardware scheduler of the ihal.it article's
+ *   paragraph on CLC: the launch has one CTA per tile; a running CTA, when it is ready
+ *   for another tile, cancels a CTA that has not been launched yet and runs that CTA's
+ *   tile, so about one CTA per SM runs while the hardware hands out the rest. A launch
+ *   whose tile count lives on the device (routed experts) is sized to the largest count
+ *   the context's dimensions allow; CTAs beyond the actual count return at once.
+ * Every output tile is one CTA's fixed-order sum in each order: same bits. */
+typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1, MOK_TILES_CLC = 2 } mok_tile_order;
 
 typedef struct mok_ctx_s* mok_ctx_t;
 

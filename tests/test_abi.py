@@ -125,13 +125,13 @@ def test_fwd_path_option():
 
 def test_tile_order_and_output_type_options():
     ctx = mok.mok_create(dims())
-    for order in (mok.MOK_TILES_DYNAMIC, mok.MOK_TILES_STATIC):
+    for order in (mok.MOK_TILES_DYNAMIC, mok.MOK_TILES_CLC, mok.MOK_TILES_STATIC):
         mok.mok_set_tile_order(ctx, order)
     for out in (mok.MOK_OUT_F32, mok.MOK_OUT_BF16):
         mok.mok_set_output_dtype(ctx, out)
-    for setter in (mok.mok_set_tile_order, mok.mok_set_output_dtype):
+    for setter, bad in ((mok.mok_set_tile_order, 3), (mok.mok_set_output_dtype, 2)):
         with pytest.raises(mok.MokError) as ei:
-            setter(ctx, 2)
+            setter(ctx, bad)
         assert ei.value.status == mok.MOK_ERR_INVALID_ARG
     mok.mok_destroy(ctx)
     assert mok.lib().mok_set_tile_order(None, 0) == mok.MOK_ERR_INVALID_ARG

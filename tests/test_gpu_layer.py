@@ -281,7 +281,8 @@ def test_split_invariance(name):
     """Every sum has a fixed order, so the results do not depend on how many SMs the
     persistent kernels spread their tiles over: 152 (all), 37 and 5 SMs give the same bits,
     and so does the forward megakernel with 1 or 3 gather SMs on 9 SMs, and so do tiles
-    taken in a dynamic order (from a device counter) on all SMs and on 7."""
+    taken in a dynamic order (from a device counter) on all SMs and on 7, and tiles handed
+    out by cluster launch control (which always spreads over every SM)."""
     cfg = CASES.get(name) or MX_CASES[name]
     inp = gu.gpu_inputs(cfg, seed=5)
     fields = ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates")
@@ -289,7 +290,7 @@ def test_split_invariance(name):
     for limit, path, comm, order in ((0, "launches", 0, 0), (37, "launches", 0, 0),
                                      (5, "launches", 0, 0), (9, "megakernel", 1, 0),
                                      (9, "megakernel", 3, 0), (0, "launches", 0, 1),
-                                     (7, "launches", 0, 1)):
+                                     (7, "launches", 0, 1), (0, "launches", 0, 2)):
         L = gu.make_layer(cfg)
         mok.mok_set_sm_limit(L.ctx, limit)
         L.set_fwd_path(path)
