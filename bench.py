@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--out", default="", choices=["", "bf16", "fp32"],
                     help="result type of y, dX and the weight gradients (default: the "
                          "workload's, bf16)")
+    ap.add_argument("--row-pairs", default="auto", choices=["auto", "on", "off"],
+                    help="row-tile pairs in the BF16 routed GEMMs")
     ap.add_argument("--tile-order", default="static", choices=["static", "dynamic", "clc"],
                     help="tile order of the persistent grouped GEMMs")
     ap.add_argument("--no-sub", action="store_true",
@@ -164,7 +166,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for n_line, line in enumerate(open(self.path)):
             if n_line < getattr(self, "skip", 0):
@@ -177,13 +179,18 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": round(statistics.median(power), 1) if power else None}
 
 
 # ----------------------------------------------------------------------------- workload
@@ -383,6 +390,8 @@ def make_layer_for(cfg, args, device="cuda", fwd_path=None):
     mok.mok_set_tile_order(L.ctx, {"static": mok.MOK_TILES_STATIC,
                                    "dynamic": mok.MOK_TILES_DYNAMIC,
                                    "clc": mok.MOK_TILES_CLC}[args.tile_order])
+    mok.mok_set_row_pairs(L.ctx, {"auto": mok.MOK_PAIRS_AUTO, "on": mok.MOK_PAIRS_ON,
+                                  "off": mok.MOK_PAIRS_OFF}[args.row_pairs])
     mx = None
     if cfg.precision == "mxfp8":
         mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"])
@@ -691,6 +700,7 @@ def run_gpu(args):
             "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
             "config": dict(workload_json(cfg), out=cfg.out, **mb,
                            fwd_path=args.fwd_path, tile_order=args.tile_order,
+                           row_pairs=args.row_pairs,
                            parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
             "megakernel_phases_ms": phases or None,

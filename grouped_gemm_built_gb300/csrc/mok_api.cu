@@ -31,6 +31,7 @@ struct mok_ctx_s {
   uint64_t wait_timeout_ns = 0;   // 0: the kernels' default (2 s)
   int withhold = 0;               // test hook of mok_test_withhold_signal
   mok_tile_order tile_order = MOK_TILES_STATIC;
+  mok_row_pairs row_pairs = MOK_PAIRS_AUTO;
   int* tcnt = nullptr;            // tile counters of the current call (dynamic order)
   int tcnt_used = 0;
   // the latest forward kept U, V (and the gathered rows) in the per-macrobatch padded
@@ -65,6 +66,22 @@ struct mok_ctx_s {
 // SMs the context's kernels may use (persistent grids are sized to it)
 static int launch_sms(mok_ctx_t ctx) {
   return ctx->sm_limit > 0 && ctx->sm_limit < ctx->num_sms ? ctx->sm_limit : ctx->num_sms;
+}
+
+// Row-tile pairs for the BF16 routed forward and dX GEMMs. Automatic: when the experts average
+// more than one and at most two 128-row tiles of rows. There the launches stream weights
+// (a weight tile meets 129..256 rows, below the tensor cores' ridge) and are bound by the
+// bytes each SM keeps in flight; a pair tile streams its weight tile once into three stages
+// of [A0 | B | A1] instead of two CTAs each keeping four [A | B] stages, half of whose
+// weight bytes the other CTA also requests. With more rows per expert the GEMMs are
+// compute-bound and keep their two accumulators for overlapping the epilogue. The dH launch
+// keeps single row tiles: a pair holds both accumulators through its long SwiGLU'
+// epilogue, which measured 10% slower at the Kimi shape.
+static bool use_pairs(mok_ctx_t ctx) {
+  if (ctx->row_pairs == MOK_PAIRS_ON) return true;
+  if (ctx->row_pairs == MOK_PAIRS_OFF) return false;
+  const long long R = (long long)ctx->d.R, E = ctx->d.E;
+  return R > 128 * E && R <= 256 * E;
 }
 
 // the context's bound on device waits and its tile order, applied to one GEMM call
@@ -165,6 +182,8 @@ AuxLayout aux_layout(const Dims& d) {
   L.mtile_expert = b.take(sizeof(int32_t) * (size_t)d.M * d.mt_m_max);
   L.mtiles = b.take(sizeof(int32_t) * (size_t)d.M);
   L.mrow0 = b.take(sizeof(int32_t) * (size_t)(d.M + 1));
+  L.ptile = b.take(sizeof(int32_t) * (size_t)max_ptiles(d));
+  L.num_ptiles = b.take(sizeof(int32_t));
   L.total = b.off;
   return L;
 }
@@ -396,6 +415,14 @@ mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order) {
   return MOK_OK;
 }
 
+mok_status mok_set_row_pairs(mok_ctx_t ctx, mok_row_pairs mode) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  if (mode != MOK_PAIRS_AUTO && mode != MOK_PAIRS_ON && mode != MOK_PAIRS_OFF)
+    return MOK_ERR_INVALID_ARG;
+  ctx->row_pairs = mode;
+  return MOK_OK;
+}
+
 mok_status mok_set_output_dtype(mok_ctx_t ctx, mok_out_dtype t) {
   if (!ctx) return MOK_ERR_INVALID_ARG;
   if (t != MOK_OUT_BF16 && t != MOK_OUT_F32) return MOK_ERR_INVALID_ARG;
@@ -517,9 +544,15 @@ static mok_status check_weights(const Dims& d, const mok_weights* w) {
   return MOK_OK;
 }
 
-static GemmCall routed_call(const Dims& d, const mok_sched* sc, const AuxPtrs& a, GemmMode m) {
+// pair: the launch may run row-tile pairs (BF16 row-space modes; see use_pairs)
+static GemmCall routed_call(const Dims& d, const mok_sched* sc, const AuxPtrs& a, GemmMode m,
+                            bool pair = false) {
   GemmCall c;
   memset(&c, 0, sizeof(c));
+  c.pair = pair;
+  c.ptile = a.ptile;
+  c.num_ptiles = a.num_ptiles;
+  c.max_ptiles = max_ptiles(d);
   c.mode = m;
   c.M_rows = d.P_max;
   c.dense = false;
@@ -674,7 +707,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     MOK_LAUNCH("dispatch_gather",
                launch_gather_rows(d, x, *sched, a, at(saved, S.xg), launch_sms(ctx), s));
     // grouped up|gate GEMM + SwiGLU (h bf16; U, V saved in fp32)
-    GemmCall c = routed_call(d, sched, a, kFwdUpGate);
+    GemmCall c = routed_call(d, sched, a, kFwdUpGate, use_pairs(ctx));
     c.a[0] = at(saved, S.xg);
     c.b[0] = w->W_up;
     c.b[1] = w->W_gate;
@@ -683,7 +716,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.out[2] = at(saved, S.v);
     MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     // grouped down GEMM
-    c = routed_call(d, sched, a, kFwdDown);
+    c = routed_call(d, sched, a, kFwdDown, use_pairs(ctx));
     c.a[0] = W(L.h);
     c.b[0] = w->W_down;
     c.out[0] = o;
@@ -803,6 +836,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
                launch_gather_rows(d, dY, *sched, a, W(L.dyg), launch_sms(ctx), s));
     // x's gathered rows come from the forward (saved), no replay
     // D = dYg W_down^T with SwiGLU' and the router-weight gradient fused in
+    // (single row tiles: its long epilogue needs the second accumulator to overlap)
     GemmCall c = routed_call(d, sched, a, kBwdDH);
     c.a[0] = W(L.dyg);
     c.b[0] = w->W_down;
@@ -820,7 +854,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     c.dgp = dgp;
     MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
-    c = routed_call(d, sched, a, kBwdDX);
+    c = routed_call(d, sched, a, kBwdDX, use_pairs(ctx));
     c.a[0] = W(L.du);
     c.a[1] = W(L.dv);
     c.b[0] = w->W_up;

@@ -60,6 +60,9 @@ constexpr int OUT_STAGING = 4 * 2 * STAGE_OUT_BYTES;  // 4 epilogue warps x 2 bu
 // split (hi/lo) dW stage: [A 16 KB][B 32 KB][second half: B lo 32 KB, or A lo 16 KB]
 constexpr int SPLIT_STAGE_BYTES = A_BYTES + 2 * B_BYTES;
 constexpr int SPLIT_EXTRA_OFF = A_BYTES + B_BYTES;
+// row-tile pair stage (BF16): [A0 16 KB][B 32 KB][A1 16 KB]
+constexpr int PAIR_STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+constexpr int PAIR_A1_OFF = A_BYTES + B_BYTES;
 
 template <bool MX>
 struct Cfg {
@@ -128,6 +131,12 @@ struct Params {
                     // launch); null: the static order (tile blockIdx.x, + gridDim.x, ...)
   int clc;          // cluster launch control: one CTA per tile; a CTA runs tile blockIdx.x,
                     // then the tiles of the not yet launched CTAs it cancels
+  int pair;         // BF16 routed up|gate, down and dX: a tile is a pair of row tiles of one
+                    // expert (ptile), two M=128 accumulators side by side against one
+                    // weight tile; stages [A0 | B | A1]
+  const int32_t* ptile;
+  const int32_t* num_ptiles;
+  int max_ptiles;
   uint64_t timeout_ns;  // bound of every wait (MOK_ERR_TIMEOUT when it passes)
   int n_out;        // kRouter: output columns (E)
   const float* bias;// kRouter: logit bias or null
@@ -171,6 +180,7 @@ struct TileInfo {
   int krow0;    // dW modes: first row of the contraction range
   int klast;    // dW modes: MMA K steps of the last K iteration that hold rows
   int skip;     // 1: no tile here (the unmatched half of the last row-tile pair)
+  int nrt;      // row tiles in this tile: 1, or 2 (a row-tile pair: rows row0 .. row0+255)
 };
 
 __host__ __device__ __forceinline__ bool is_dw(int mode) { return mode == kBwdDWDown || mode == kBwdDWUpGate; }
@@ -185,6 +195,7 @@ __device__ __forceinline__ int routed_mtiles(const Params& p) {
 // CTAs take them in the same round, so the second read of the slice is an L2 hit.
 __device__ __forceinline__ int num_tiles_of(const Params& p) {
   if (is_dw(p.mode)) return p.groups * p.m_tiles_dw * p.n_tiles;
+  if (p.pair) return min(max(*p.num_ptiles, 0), p.max_ptiles) * p.n_tiles;
   if (p.dense) return ((p.M_rows + BM - 1) / BM) * p.n_tiles;
   return ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles;
 }
@@ -195,7 +206,23 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
   constexpr int MMA_K = Cfg<MX>::MMA_K;
   TileInfo ti;
   ti.skip = 0;
+  ti.nrt = 1;
   ti.klast = BK / MMA_K;
+  if (p.pair) {   // tile = pair q of column block nt; the pair's tiles share the expert
+    const int q = tile / p.n_tiles;
+    const int nt = tile - q * p.n_tiles;
+    const int pt = p.ptile[q];
+    const int mt = pt >> 1;
+    ti.skip = mt >= routed_mtiles(p);
+    ti.nrt = (pt & 1) && mt + 1 < routed_mtiles(p) ? 2 : 1;
+    ti.e = ti.skip ? 0 : min(max(p.tile_expert[mt], 0), p.groups - 1);
+    ti.row0 = ti.skip ? 0 : mt * BM;
+    ti.n0 = nt * (p.mode == kFwdUpGate ? 128 : p.BN);
+    ti.kiters = p.kiters;
+    ti.krow0 = 0;
+    ti.arow0 = ti.row0;
+    return ti;
+  }
   if (is_dw(p.mode)) {
     const int per_e = p.m_tiles_dw * p.n_tiles;
     ti.e = tile / per_e;
@@ -489,11 +516,14 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
       uint32_t extra = 0;   // split dW stages also carry the lo half of the split operand
       if (sp) extra = p.mode == kBwdDWUpGate ? 2 * 128 * 128 : BM * 128;
       if (MX && p.kdouble) extra = A_BYTES + b_bytes;   // the second K chunk
+      const bool a1 = !MX && ti.nrt == 2;              // the pair's second row tile
+      if (a1) extra += A_BYTES;
       mbar_arrive_expect_tx(bar, A_BYTES + b_bytes + extra);
       const int k0 = kb * BK;
       switch (p.mode) {
         case kFwdUpGate: {   // A: Xg rows (K-major); B: W_up|W_gate cols n0..n0+127 (MN-major)
           tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
+          if (a1) tma_load_2d(sa + PAIR_A1_OFF, &mp.a[0], bar, k0, ti.arow0 + BM);
           const int brow = ti.e * p.H + k0;
           for (int c = 0; c < 128 / C::MN_CHUNK; ++c) {
             tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, brow);
@@ -510,6 +540,7 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
         }
         case kFwdDown: {     // A: h rows (K-major); B: W_down cols (MN-major)
           tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
+          if (a1) tma_load_2d(sa + PAIR_A1_OFF, &mp.a[0], bar, k0, ti.arow0 + BM);
           const int brow = ti.e * p.I + k0;
           for (int c = 0; c < p.BN / C::MN_CHUNK; ++c)
             tma_load_2d(sb + c * CH, &mp.b[0], bar, ti.n0 + c * C::MN_CHUNK, brow);
@@ -540,6 +571,7 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
             break;
           }
           tma_load_2d(sa, &mp.a[0], bar, k0, ti.arow0);
+          if (a1) tma_load_2d(sa + PAIR_A1_OFF, &mp.a[0], bar, k0, ti.arow0 + BM);
           tma_load_2d(sb, &mp.b[0], bar, k0, ti.e * p.I + ti.n0);
           if (MX) {
             bulk_load(sf, p.sfa + ((size_t)(ti.arow0 / BM) * p.kcs_a + kb) * 512, 512, bar);
@@ -553,6 +585,7 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
           const int second = kb >= per_half ? 1 : 0;
           const int kq = kb - second * per_half;   // K chunk inside the half
           tma_load_2d(sa, &mp.a[second], bar, kq * BK, ti.arow0);
+          if (a1) tma_load_2d(sa + PAIR_A1_OFF, &mp.a[second], bar, kq * BK, ti.arow0 + BM);
           tma_load_2d(sb, &mp.b[second], bar, kq * BK, ti.e * p.H + ti.n0);
           if (MX) {
             bulk_load(sf, (second ? p.sfa1 : p.sfa) + ((size_t)(ti.arow0 / BM) * p.kcs_a + kq) * 512,
@@ -792,10 +825,14 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
         const uint64_t bd = b_mn ? umma_desc_sw128(sb + kk * C::MN_KSTEP, C::MN_LBO, 1024)
                                  : umma_desc_sw128(sb + kk * 32, 16, 1024);
         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-        if (MX)
+        if (MX) {
           umma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, n_mma, a_mn, b_mn, kk), t_sfa, t_sfb, accum);
-        else
+        } else {
           umma_bf16(d_tmem, ad, bd, idesc, accum);
+          if (ti.nrt == 2)   // the pair's second row tile (K-major A), same B, columns +256
+            umma_bf16(d_tmem + 256, umma_desc_sw128(sa + PAIR_A1_OFF + kk * 32, 16, 1024), bd,
+                      idesc, accum);
+        }
       }
       if (!MX && p.split) {
         // the lo half of the K chunk, after the hi half, into the same accumulator:
@@ -857,7 +894,7 @@ __device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64
 template <bool MX>
 __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint64_t* acc_full,
                               uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag,
-                              const TileInfo& ti, int local) {
+                              const TileInfo& tile_in, int local) {
   using C = Cfg<MX>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
@@ -871,20 +908,27 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
       return false;
     }
     tc_fence_after();
-    const uint32_t t_row = tmem_base + acc * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
-    const bool have = ti.kiters > 0;
+    const bool have = tile_in.kiters > 0;
     float a[32], b[32];
     // The accumulator is handed back to the MMA lane right after this thread's last TMEM
     // load (before that chunk's math and stores), so the next tile's MMAs can start while
-    // the stores drain; with one accumulator (MXFP8) this is the overlap there is.
+    // the stores drain; with one accumulator (MXFP8) this is the overlap there is. A
+    // row-tile pair hands both back after its second row tile's last load.
     bool released = false;
+    int half = 0;
     auto release = [&]() {
-      if (!released) {
+      if (!released && half >= tile_in.nrt - 1) {
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
         released = true;
       }
     };
+    for (; half < tile_in.nrt; ++half) {
+    TileInfo ti = tile_in;   // row tile `half` of a pair: rows +128, accumulator columns +256
+    ti.row0 += half * BM;
+    ti.arow0 += half * BM;
+    const uint32_t t_row =
+        tmem_base + acc * p.acc_cols + half * 256 + ((uint32_t)(quarter * 32) << 16);
     // tcgen05.ld and the staged stores are warp-collective: every lane takes part, rows
     // outside the problem only skip their global loads (TMA drops their stores).
     const int row = ti.row0 + r;
@@ -1130,6 +1174,8 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         break;
       }
     }
+    }
+    half = tile_in.nrt - 1;
     release();
   }
   return true;
@@ -1179,13 +1225,16 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
 // One instantiation per mode (and, for the dW modes, per hi/lo split): with both
 // compile-time constants the compiler keeps only that launch's producer, MMA and epilogue
 // code (a smaller instruction footprint, a straight-line MMA issue).
-template <bool MX, int MODE, int SPLIT>
+// VAR: 0 plain, 1 split (hi/lo dW operands), 2 row-tile pairs. Fixing the variant at
+// compile time keeps the pair and split paths out of the other kernels' code.
+template <bool MX, int MODE, int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p_in) {
   using C = Cfg<MX>;
   Params p = p_in;
   p.mode = MODE;
-  p.split = SPLIT;
+  p.split = VAR == 1;
+  p.pair = VAR == 2;
   // CLC: the grid is sized to the largest tile count; a CTA past the actual count (which
   // the plan wrote to device memory) has no tile and leaves before taking any resource
   if (p.clc && (int)blockIdx.x >= num_tiles_of(p)) return;
@@ -1360,6 +1409,7 @@ __device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph
   ti.krow0 = 0;
   ti.klast = 4;
   ti.skip = r >= mega_mtiles(q, m);
+  ti.nrt = 1;
   return ti;
 }
 
@@ -1966,6 +2016,12 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.uv_row = c.uv_row;
   p.tile_counter = c.tile_counter;
   p.clc = c.clc ? 1 : 0;
+  p.pair = (!MX && c.pair && !c.dense && !p.split && c.ptile && c.num_ptiles &&
+            (c.mode == kFwdUpGate || c.mode == kFwdDown || c.mode == kBwdDX))
+               ? 1 : 0;
+  p.ptile = c.ptile;
+  p.num_ptiles = c.num_ptiles;
+  p.max_ptiles = c.max_ptiles;
   p.dgp = c.dgp;
   p.status = c.status;
   p.sfa = static_cast<const uint8_t*>(c.sfa);
@@ -2081,6 +2137,17 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   }
   // routed row-space launches number their tiles in row-tile pairs (num_tiles_of)
   if (!p.dense && !is_dw(c.mode)) max_tiles = (mt_rows + 1) / 2 * 2 * p.n_tiles;
+  if (p.pair) {   // three [A0 | B | A1] stages, both accumulators for one tile
+    static_assert(3 * PAIR_STAGE_BYTES + OUT_STAGING <= Cfg<false>::DATA_BYTES &&
+                      PAIR_STAGE_BYTES % 1024 == 0 && PAIR_A1_OFF % 1024 == 0,
+                  "row-tile pair stages exceed the data area");
+    p.stages = 3;
+    p.stage_bytes = PAIR_STAGE_BYTES;
+    p.nbuf = 2;
+    p.nacc = 1;
+    p.acc_cols = 512;
+    max_tiles = (p.max_ptiles > 0 ? p.max_ptiles : 0) * p.n_tiles;
+  }
   if (!ok) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
@@ -2088,12 +2155,18 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
 using GemmKernel = void (*)(const Maps, const Params);
 
 template <bool MX>
-GemmKernel gemm_kernel_for(int mode, int split) {
+GemmKernel gemm_kernel_for(int mode, int split, int pair) {
   switch (mode) {
-    case kFwdUpGate: return grouped_gemm_kernel<MX, kFwdUpGate, 0>;
-    case kFwdDown: return grouped_gemm_kernel<MX, kFwdDown, 0>;
+    case kFwdUpGate:
+      return pair ? grouped_gemm_kernel<MX, kFwdUpGate, MX ? 0 : 2>
+                  : grouped_gemm_kernel<MX, kFwdUpGate, 0>;
+    case kFwdDown:
+      return pair ? grouped_gemm_kernel<MX, kFwdDown, MX ? 0 : 2>
+                  : grouped_gemm_kernel<MX, kFwdDown, 0>;
     case kBwdDH: return grouped_gemm_kernel<MX, kBwdDH, 0>;
-    case kBwdDX: return grouped_gemm_kernel<MX, kBwdDX, 0>;
+    case kBwdDX:
+      return pair ? grouped_gemm_kernel<MX, kBwdDX, MX ? 0 : 2>
+                  : grouped_gemm_kernel<MX, kBwdDX, 0>;
     case kBwdDWDown:
       return split ? grouped_gemm_kernel<MX, kBwdDWDown, !MX> : grouped_gemm_kernel<MX, kBwdDWDown, 0>;
     case kBwdDWUpGate:
@@ -2107,19 +2180,20 @@ GemmKernel gemm_kernel_for(int mode, int split) {
 template <bool MX>
 cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   using C = Cfg<MX>;
-  static bool attr_set[8][2] = {};
+  static bool attr_set[8][3] = {};
   if (c.mode < 0 || c.mode >= 8) return cudaErrorInvalidValue;
   Params p;
   Maps mp;
   int max_tiles = 0;
   cudaError_t e = build_call<MX>(c, p, mp, max_tiles);
   if (e != cudaSuccess) return e;
-  const GemmKernel kern = gemm_kernel_for<MX>(c.mode, p.split);
+  const GemmKernel kern = gemm_kernel_for<MX>(c.mode, p.split, p.pair);
   if (!kern) return cudaErrorInvalidValue;
-  if (!attr_set[c.mode][p.split ? 1 : 0]) {
+  const int var = p.split ? 1 : p.pair ? 2 : 0;
+  if (!attr_set[c.mode][var]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[c.mode][p.split ? 1 : 0] = true;
+    attr_set[c.mode][var] = true;
   }
   // persistent: one CTA per SM; CLC: one CTA per tile (the hardware keeps one per SM
   // running and the running CTAs cancel the rest)

@@ -40,10 +40,14 @@ struct Dims {
 // expert e: mstart[m][e] (table row of e's first row in m), mcount[m][e], mpoff[m][e]
 // (padded offset inside m, E+1 entries), mtile_expert[m][tile], mtiles[m], mrow0[m] (first
 // row of m in the concatenated padded space, M+1 entries).
+// ptile[q] = (first row tile << 1) | (1 if the pair has a second row tile): the row-tile
+// pairs of each expert's segment (tiles 0-1, 2-3, ...; an odd last tile alone), expert
+// by expert; num_ptiles[0] = their count (at most max_ptiles(d)).
 struct AuxLayout {
   size_t status, poff, tile_expert, num_mtiles;
-  size_t mstart, mcount, mpoff, mtile_expert, mtiles, mrow0, total;
+  size_t mstart, mcount, mpoff, mtile_expert, mtiles, mrow0, ptile, num_ptiles, total;
 };
+inline int max_ptiles(const Dims& d) { return (d.mt_max + d.E + 1) / 2; }
 // scratch for mok_plan
 struct PlanWs {
   size_t logits, hist, lrank, wr3, total;
@@ -113,6 +117,8 @@ struct AuxPtrs {
   int32_t* mtile_expert;// [M][mt_m_max]
   int32_t* mtiles;      // [M]
   int32_t* mrow0;       // [M+1]
+  int32_t* ptile;       // [max_ptiles] row-tile pairs of the padded row space
+  int32_t* num_ptiles;  // [1]
 };
 inline AuxPtrs aux_ptrs(const Dims& d, void* aux) {
   AuxLayout L = aux_layout(d);
@@ -120,7 +126,8 @@ inline AuxPtrs aux_ptrs(const Dims& d, void* aux) {
   auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(b + off); };
   return AuxPtrs{reinterpret_cast<uint32_t*>(b + L.status), I32(L.poff), I32(L.tile_expert),
                  I32(L.num_mtiles), I32(L.mstart), I32(L.mcount), I32(L.mpoff),
-                 I32(L.mtile_expert), I32(L.mtiles), I32(L.mrow0)};
+                 I32(L.mtile_expert), I32(L.mtiles), I32(L.mrow0), I32(L.ptile),
+                 I32(L.num_ptiles)};
 }
 
 // Read-only views of a context (defined in mok_api.cu).
@@ -220,6 +227,10 @@ struct GemmCall {
   const int32_t* poff; const int32_t* counts; const int32_t* offsets;
   const int32_t* tile_expert; const int32_t* num_mtiles;
   const int32_t* table; const float* gates; int k;
+  // row-tile pairs (BF16 routed row-space modes): one CTA runs both row tiles of a pair
+  // against one weight tile, two accumulators side by side (AuxLayout::ptile)
+  bool pair = false;
+  const int32_t* ptile; const int32_t* num_ptiles; int max_ptiles;
   uint32_t* status;
   uint64_t timeout_ns;  // bound of every device wait (0: 2 s)
   int* tile_counter;    // dynamic tile order: a zeroed int of device memory (null: static)

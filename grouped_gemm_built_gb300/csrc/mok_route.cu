@@ -203,7 +203,8 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 __global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32_t* hist,
                                                           int32_t* counts, int32_t* offsets,
                                                           int32_t* poff, int32_t* tile_expert,
-                                                          int32_t* num_mtiles) {
+                                                          int32_t* num_mtiles, int32_t* ptile,
+                                                          int32_t* num_ptiles) {
   __shared__ int s_warp[32];
   __shared__ int s_total;
   const int e = threadIdx.x;
@@ -227,16 +228,24 @@ __global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32
   const int R = s_total;
   int poff_e = block_exclusive_scan(pcnt, s_warp, &s_total);
   const int P = s_total;
+  // row-tile pairs of the expert's segment: tiles 0-1, 2-3, ...; an odd last one alone
+  const int mt_e = pcnt / kRowPad;
+  const int np_e = (mt_e + 1) / 2;
+  const int pq0 = block_exclusive_scan(np_e, s_warp, &s_total);
+  const int NP = s_total;
   if (e < E) {
     counts[e] = cnt;
     offsets[e] = off;
     poff[e] = poff_e;
     for (int m = poff_e / kRowPad; m < (poff_e + pcnt) / kRowPad; ++m) tile_expert[m] = e;
+    for (int q = 0; q < np_e; ++q)
+      ptile[pq0 + q] = ((poff_e / kRowPad + 2 * q) << 1) | (2 * q + 1 < mt_e ? 1 : 0);
   }
   if (e == 0) {
     offsets[E] = R;
     poff[E] = P;
     *num_mtiles = P / kRowPad;
+    *num_ptiles = NP;
   }
 }
 
@@ -290,7 +299,7 @@ cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int3
                              const AuxPtrs& a, cudaStream_t s) {
   int threads = (d.E + 31) / 32 * 32;
   plan_scan_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, hist, counts, offsets, a.poff,
-                                         a.tile_expert, a.num_mtiles);
+                                         a.tile_expert, a.num_mtiles, a.ptile, a.num_ptiles);
   return cudaGetLastError();
 }
 

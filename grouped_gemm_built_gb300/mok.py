@@ -30,6 +30,9 @@ MOK_OUT_F32 = 1
 MOK_TILES_STATIC = 0
 MOK_TILES_DYNAMIC = 1
 MOK_TILES_CLC = 2
+MOK_PAIRS_AUTO = 0
+MOK_PAIRS_ON = 1
+MOK_PAIRS_OFF = 2
 MOK_FWD_MEGAKERNEL = 0
 MOK_FWD_LAUNCHES = 1
 MOK_FWD_AUTO = 2
@@ -83,6 +86,7 @@ def _declare(L):
         "mok_set_precision": (c_int, [c_void_p, c_int]),
         "mok_set_output_dtype": (c_int, [c_void_p, c_int]),
         "mok_set_tile_order": (c_int, [c_void_p, c_int]),
+        "mok_set_row_pairs": (c_int, [c_void_p, c_int]),
         "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
         "mok_set_comm_sms": (c_int, [c_void_p, c_int]),
         "mok_set_sm_limit": (c_int, [c_void_p, c_int]),
@@ -172,6 +176,10 @@ def mok_set_precision(ctx, precision: int) -> None:
 
 def mok_set_tile_order(ctx, order: int) -> None:
     _check(lib().mok_set_tile_order(ctx, int(order)), "mok_set_tile_order")
+
+
+def mok_set_row_pairs(ctx, mode: int) -> None:
+    _check(lib().mok_set_row_pairs(ctx, int(mode)), "mok_set_row_pairs")
 
 
 def mok_set_output_dtype(ctx, out_dtype: int) -> None:

@@ -107,6 +107,15 @@ typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1, MOK_FWD_AUTO = 2 } 
  * Every output tile is one CTA's fixed-order sum in each order: same bits. */
 typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1, MOK_TILES_CLC = 2 } mok_tile_order;
 
+/* Row-tile pairs in the BF16 routed GEMMs of the forward and of dX: one CTA runs two
+ * 128-row tiles of one expert against one weight tile (two accumulators side by side,
+ * pipeline stages [rows 0-127 | weight tile | rows 128-255]), so each SM keeps more weight
+ * bytes in flight. MOK_PAIRS_AUTO (default): on when the experts average more than 128 and
+ * at most 256 rows (weight-streaming launches); MOK_PAIRS_ON / MOK_PAIRS_OFF force it.
+ * Same bits either way. MXFP8 launches, the shared expert and the forward megakernel run
+ * single row tiles. */
+typedef enum { MOK_PAIRS_AUTO = 0, MOK_PAIRS_ON = 1, MOK_PAIRS_OFF = 2 } mok_row_pairs;
+
 typedef struct mok_ctx_s* mok_ctx_t;
 
 /* Layer dimensions. T tokens, H hidden, I expert intermediate size, E routed experts,
@@ -222,6 +231,10 @@ mok_status mok_set_precision(mok_ctx_t ctx, mok_precision p);
 /* Select the tile order of later mok_moe_fwd / mok_moe_bwd grouped GEMMs (mok_tile_order
  * above). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order);
+
+/* Select the row-tile pairing of later mok_moe_fwd / mok_moe_bwd BF16 routed GEMMs
+ * (mok_row_pairs above). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
+mok_status mok_set_row_pairs(mok_ctx_t ctx, mok_row_pairs mode);
 
 /* Select the type of later mok_moe_fwd / mok_moe_bwd results (mok_out_dtype above).
  * Host-only state change; MOK_ERR_INVALID_ARG for other values. */

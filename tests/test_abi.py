@@ -123,19 +123,23 @@ def test_fwd_path_option():
     mok.mok_destroy(ctx)
 
 
-def test_tile_order_and_output_type_options():
+def test_tile_order_row_pairs_and_output_type_options():
     ctx = mok.mok_create(dims())
     for order in (mok.MOK_TILES_DYNAMIC, mok.MOK_TILES_CLC, mok.MOK_TILES_STATIC):
         mok.mok_set_tile_order(ctx, order)
     for out in (mok.MOK_OUT_F32, mok.MOK_OUT_BF16):
         mok.mok_set_output_dtype(ctx, out)
-    for setter, bad in ((mok.mok_set_tile_order, 3), (mok.mok_set_output_dtype, 2)):
+    for mode in (mok.MOK_PAIRS_ON, mok.MOK_PAIRS_OFF, mok.MOK_PAIRS_AUTO):
+        mok.mok_set_row_pairs(ctx, mode)
+    for setter, bad in ((mok.mok_set_tile_order, 3), (mok.mok_set_output_dtype, 2),
+                        (mok.mok_set_row_pairs, 3)):
         with pytest.raises(mok.MokError) as ei:
             setter(ctx, bad)
         assert ei.value.status == mok.MOK_ERR_INVALID_ARG
     mok.mok_destroy(ctx)
     assert mok.lib().mok_set_tile_order(None, 0) == mok.MOK_ERR_INVALID_ARG
     assert mok.lib().mok_set_output_dtype(None, 0) == mok.MOK_ERR_INVALID_ARG
+    assert mok.lib().mok_set_row_pairs(None, 0) == mok.MOK_ERR_INVALID_ARG
 
 
 def test_wait_timeout_and_test_hook_are_host_settings():

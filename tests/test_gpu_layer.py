@@ -305,6 +305,30 @@ def test_split_invariance(name):
             assert torch.equal(res[f], ref[f]), (limit, path, comm, order, f)
 
 
+@pytest.mark.parametrize("name", ["mid", "mid_plain", "external_routing", "max_experts"])
+def test_row_tile_pairs_keep_the_bits(name):
+    """Row-tile pairs (one CTA runs two 128-row tiles of an expert against one weight tile,
+    or the odd last tile alone) give the single-tile launches' bits in every tile order:
+    each output row is the same fixed-order K sum. The cases have experts of one, two,
+    three and more row tiles."""
+    cfg = CASES[name]
+    inp = gu.gpu_inputs(cfg, seed=8)
+    fields = ("y", "dX", "dW_up", "dW_gate", "dW_down", "dgates")
+    ref = None
+    for pairs, order in ((mok.MOK_PAIRS_OFF, 0), (mok.MOK_PAIRS_ON, 0), (mok.MOK_PAIRS_ON, 1),
+                         (mok.MOK_PAIRS_ON, 2)):
+        L = gu.make_layer(cfg)
+        mok.mok_set_row_pairs(L.ctx, pairs)
+        mok.mok_set_tile_order(L.ctx, order)
+        res, _ = gu.run_gpu(cfg, inp, backward=True, layer=L)
+        assert res["status"] == 0
+        if ref is None:
+            ref = res
+            continue
+        for f in fields:
+            assert torch.equal(res[f], ref[f]), (pairs, order, f)
+
+
 @pytest.mark.parametrize("name", ["ragged_shared", "ragged_shared_plain", "ragged_shared_mx"])
 def test_bf16_results_are_the_fp32_sums_rounded(name):
     """The weight gradients come out of the same fp32 accumulators in both result types:
