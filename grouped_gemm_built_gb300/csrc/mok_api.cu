@@ -184,6 +184,8 @@ AuxLayout aux_layout(const Dims& d) {
   L.mrow0 = b.take(sizeof(int32_t) * (size_t)(d.M + 1));
   L.ptile = b.take(sizeof(int32_t) * (size_t)max_ptiles(d));
   L.num_ptiles = b.take(sizeof(int32_t));
+  L.dwr_q0 = b.take(sizeof(int32_t) * (size_t)(d.E + 1));
+  L.dwr_item_e = b.take(sizeof(int32_t) * (size_t)dwr_items_max(d));
   L.total = b.off;
   return L;
 }
@@ -280,6 +282,7 @@ BwdWs bwd_ws(const Dims& d) {
   L.uvmap = d.M > 1 ? b.take(sizeof(int32_t) * P) : b.off;
   L.xr = d.M > 1 ? b.take(2 * P * d.H) : b.off;
   L.tcnt = b.take(sizeof(int) * kTileCounters);
+  L.dwr_part = d.router ? b.take(sizeof(float) * (size_t)dwr_items_max(d) * d.H) : b.off;
   L.total = b.off;
   return L;
 }
@@ -1009,7 +1012,9 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     cs.out_bf16 = ob;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
   }
-  if (d.router) MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, dl, g->dWr, s));
+  if (d.router)
+    MOK_LAUNCH("router_dwr", launch_router_dwr(d, x, *sched, a, reinterpret_cast<float*>(W(L.dwr_part)),
+                                               dl, g->dWr, s));
   return MOK_OK;
 }
 

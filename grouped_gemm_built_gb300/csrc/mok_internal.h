@@ -45,9 +45,15 @@ struct Dims {
 // by expert; num_ptiles[0] = their count (at most max_ptiles(d)).
 struct AuxLayout {
   size_t status, poff, tile_expert, num_mtiles;
-  size_t mstart, mcount, mpoff, mtile_expert, mtiles, mrow0, ptile, num_ptiles, total;
+  size_t mstart, mcount, mpoff, mtile_expert, mtiles, mrow0, ptile, num_ptiles;
+  size_t dwr_q0, dwr_item_e, total;
 };
 inline int max_ptiles(const Dims& d) { return (d.mt_max + d.E + 1) / 2; }
+// The router weight gradient sums each expert's table rows in chunks of kDwrChunk rows
+// (a busy expert spreads over many CTAs): dwr_q0[e] = the expert's first chunk (E+1
+// entries, exclusive scan of ceil(count / kDwrChunk)), dwr_item_e[q] = the expert of chunk q.
+constexpr int kDwrChunk = 1024;
+inline int dwr_items_max(const Dims& d) { return (d.R + kDwrChunk - 1) / kDwrChunk + d.E; }
 // scratch for mok_plan
 struct PlanWs {
   size_t logits, hist, lrank, wr3, total;
@@ -86,6 +92,7 @@ struct BwdWs {
       dvs_lo, hsg_lo, dxs;
   size_t uvmap, xr;   // after a multi-macrobatch megakernel forward: U, V row map; x rows
   size_t tcnt;        // tile counters (dynamic tile order)
+  size_t dwr_part;    // router weight gradient: per-chunk partial sums [dwr_items_max][H]
   size_t q_dy_h, sf_dy_h, q_dy_r, sf_dy_r, q_x_r, sf_x_r;
   size_t q_du_i, sf_du_i, q_dv_i, sf_dv_i, q_du_r, sf_du_r, q_dv_r, sf_dv_r, q_hg_r, sf_hg_r;
   size_t total;
@@ -119,6 +126,8 @@ struct AuxPtrs {
   int32_t* mrow0;       // [M+1]
   int32_t* ptile;       // [max_ptiles] row-tile pairs of the padded row space
   int32_t* num_ptiles;  // [1]
+  int32_t* dwr_q0;      // [E+1]
+  int32_t* dwr_item_e;  // [dwr_items_max]
 };
 inline AuxPtrs aux_ptrs(const Dims& d, void* aux) {
   AuxLayout L = aux_layout(d);
@@ -127,7 +136,7 @@ inline AuxPtrs aux_ptrs(const Dims& d, void* aux) {
   return AuxPtrs{reinterpret_cast<uint32_t*>(b + L.status), I32(L.poff), I32(L.tile_expert),
                  I32(L.num_mtiles), I32(L.mstart), I32(L.mcount), I32(L.mpoff),
                  I32(L.mtile_expert), I32(L.mtiles), I32(L.mrow0), I32(L.ptile),
-                 I32(L.num_ptiles)};
+                 I32(L.num_ptiles), I32(L.dwr_q0), I32(L.dwr_item_e)};
 }
 
 // Read-only views of a context (defined in mok_api.cu).
@@ -175,6 +184,7 @@ cudaError_t launch_uv_rowmap(const Dims& d, const mok_sched& sc, const AuxPtrs& 
                              cudaStream_t s);
 // dWr[:, e] = sum over expert e's table rows of x[t] * dl[t][j]   (fixed row order)
 cudaError_t launch_router_dwr(const Dims& d, const void* x, const mok_sched& sc, const AuxPtrs& a,
+                              float* part,
                               const float* dl, float* dWr, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped GEMMs (mok_gemm.cu)

@@ -297,46 +297,90 @@ cudaError_t launch_router_grad(const Dims& d, const float* dgp, int n_parts, con
   return cudaGetLastError();
 }
 
-// dWr[h][e] = sum over expert e's table rows r (ascending) of x[t_r][h] * dl[t_r][j_r].
-// Grid (E, H/256); each thread owns one h, so the row loop is one fixed-order fp32 sum.
-__global__ void __launch_bounds__(256) router_dwr_kernel(int H, int E, int k,
-                                                         const __nv_bfloat16* __restrict__ x,
-                                                         const int32_t* __restrict__ table,
-                                                         const int32_t* __restrict__ counts,
-                                                         const int32_t* __restrict__ offsets,
-                                                         const float* __restrict__ dl,
-                                                         float* __restrict__ dWr) {
-  const int e = blockIdx.x;
-  const int h = blockIdx.y * 256 + threadIdx.x;
-  __shared__ int s_tok[256];
-  __shared__ float s_w[256];
-  const int n = counts[e], r0 = offsets[e];
-  float acc = 0.f;
-  for (int c = 0; c < n; c += 256) {
-    __syncthreads();
-    if (c + (int)threadIdx.x < n) {
-      const int r = r0 + c + threadIdx.x;
-      const int t = table[2 * (size_t)r], j = table[2 * (size_t)r + 1];
-      s_tok[threadIdx.x] = t;
-      s_w[threadIdx.x] = dl[(size_t)t * k + j];
-    }
-    __syncthreads();
-    const int m = min(256, n - c);
-    if (h < H) {
-#pragma unroll 8
-      for (int i = 0; i < m; ++i)
-        acc = fmaf(__bfloat162float(x[(size_t)s_tok[i] * H + h]), s_w[i], acc);
+// dWr[h][e] = sum over expert e's table rows r of x[t_r][h] * dl[t_r][j_r], in two fixed-order
+// passes. Pass 1, grid (chunk items, H/256): a CTA takes one chunk of kDwrChunk rows of one
+// expert and 256 columns h; warp w sums the chunk's rows w, w+8, w+16, ... (ascending), each
+// lane 8 consecutive h from one 16-byte load per row; the eight warp sums are added in warp
+// order into part[q][h]. Pass 2, grid (E, H/256): dWr[h][e] = the expert's chunk sums in
+// chunk order. A busy expert (the biased experts take most tokens) spreads over many CTAs.
+constexpr int kDwrWarps = 8;
+__global__ void __launch_bounds__(kDwrWarps * 32) router_dwr_part_kernel(
+    int H, int k, const uint4* __restrict__ x, const int32_t* __restrict__ table,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ dwr_q0, const int32_t* __restrict__ dwr_item_e, int E,
+    const float* __restrict__ dl, float* __restrict__ part) {
+  __shared__ int s_tok[kDwrChunk];
+  __shared__ float s_w[kDwrChunk];
+  __shared__ float s_red[kDwrWarps][256];
+  const int q = blockIdx.x;
+  if (q >= dwr_q0[E]) return;
+  const int e = dwr_item_e[q];
+  const int c0 = (q - dwr_q0[e]) * kDwrChunk;
+  const int m = min(kDwrChunk, counts[e] - c0);
+  const int r0 = offsets[e] + c0;
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const int t = table[2 * (size_t)(r0 + i)], j = table[2 * (size_t)(r0 + i) + 1];
+    s_tok[i] = t;
+    s_w[i] = dl[(size_t)t * k + j];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h0 = blockIdx.y * 256 + lane * 8;   // this lane's 8 columns
+  const bool on = h0 < H;
+  const int hv = H / 8;                         // 16-byte vectors per row of x
+  float acc[8];
+#pragma unroll
+  for (int z = 0; z < 8; ++z) acc[z] = 0.f;
+  if (on) {
+#pragma unroll 4
+    for (int i = warp; i < m; i += kDwrWarps) {
+      const uint4 w = __ldg(x + (size_t)s_tok[i] * hv + h0 / 8);
+      const float wt = s_w[i];
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const float2 f = __bfloat1622float2(b[z]);
+        acc[2 * z] = fmaf(f.x, wt, acc[2 * z]);
+        acc[2 * z + 1] = fmaf(f.y, wt, acc[2 * z + 1]);
+      }
     }
   }
-  if (h < H) dWr[(size_t)h * E + e] = acc;
+#pragma unroll
+  for (int z = 0; z < 8; ++z) s_red[warp][lane * 8 + z] = acc[z];
+  __syncthreads();
+  const int h = blockIdx.y * 256 + threadIdx.x;
+  if (h < H) {
+    float v = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kDwrWarps; ++w2) v += s_red[w2][threadIdx.x];
+    part[(size_t)q * H + h] = v;
+  }
+}
+
+__global__ void __launch_bounds__(256) router_dwr_sum_kernel(int H, int E,
+                                                             const int32_t* __restrict__ dwr_q0,
+                                                             const float* __restrict__ part,
+                                                             float* __restrict__ dWr) {
+  const int e = blockIdx.x;
+  const int h = blockIdx.y * 256 + threadIdx.x;
+  if (h >= H) return;
+  const int q0 = dwr_q0[e], q1 = dwr_q0[e + 1];
+  float v = 0.f;
+  for (int q = q0; q < q1; ++q) v += part[(size_t)q * H + h];
+  dWr[(size_t)h * E + e] = v;
 }
 
 cudaError_t launch_router_dwr(const Dims& d, const void* x, const mok_sched& sc, const AuxPtrs& a,
-                              const float* dl, float* dWr, cudaStream_t s) {
-  (void)a;
-  dim3 grid(d.E, (d.H + 255) / 256);
-  router_dwr_kernel<<<grid, 256, 0, s>>>(d.H, d.E, d.k, static_cast<const __nv_bfloat16*>(x),
-                                         sc.table, sc.counts, sc.offsets, dl, dWr);
+                              float* part, const float* dl, float* dWr, cudaStream_t s) {
+  if (d.H % 8 != 0) return cudaErrorInvalidValue;
+  dim3 g1(dwr_items_max(d), (d.H + 255) / 256);
+  router_dwr_part_kernel<<<g1, kDwrWarps * 32, 0, s>>>(
+      d.H, d.k, static_cast<const uint4*>(x), sc.table, sc.counts, sc.offsets, a.dwr_q0,
+      a.dwr_item_e, d.E, dl, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2(d.E, (d.H + 255) / 256);
+  router_dwr_sum_kernel<<<g2, 256, 0, s>>>(d.H, d.E, a.dwr_q0, part, dWr);
   return cudaGetLastError();
 }
 

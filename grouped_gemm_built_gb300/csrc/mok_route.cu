@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32
                                                           int32_t* counts, int32_t* offsets,
                                                           int32_t* poff, int32_t* tile_expert,
                                                           int32_t* num_mtiles, int32_t* ptile,
-                                                          int32_t* num_ptiles) {
+                                                          int32_t* num_ptiles, int32_t* dwr_q0,
+                                                          int32_t* dwr_item_e) {
   __shared__ int s_warp[32];
   __shared__ int s_total;
   const int e = threadIdx.x;
@@ -233,6 +234,10 @@ __global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32
   const int np_e = (mt_e + 1) / 2;
   const int pq0 = block_exclusive_scan(np_e, s_warp, &s_total);
   const int NP = s_total;
+  // chunks of the router weight gradient's row sums
+  const int nq_e = (cnt + kDwrChunk - 1) / kDwrChunk;
+  const int q0 = block_exclusive_scan(nq_e, s_warp, &s_total);
+  const int NQ = s_total;
   if (e < E) {
     counts[e] = cnt;
     offsets[e] = off;
@@ -240,12 +245,15 @@ __global__ void __launch_bounds__(kMaxE) plan_scan_kernel(int E, int nblk, int32
     for (int m = poff_e / kRowPad; m < (poff_e + pcnt) / kRowPad; ++m) tile_expert[m] = e;
     for (int q = 0; q < np_e; ++q)
       ptile[pq0 + q] = ((poff_e / kRowPad + 2 * q) << 1) | (2 * q + 1 < mt_e ? 1 : 0);
+    dwr_q0[e] = q0;
+    for (int q = 0; q < nq_e; ++q) dwr_item_e[q0 + q] = e;
   }
   if (e == 0) {
     offsets[E] = R;
     poff[E] = P;
     *num_mtiles = P / kRowPad;
     *num_ptiles = NP;
+    dwr_q0[E] = NQ;
   }
 }
 
@@ -299,7 +307,8 @@ cudaError_t launch_plan_scan(const Dims& d, int32_t* hist, int32_t* counts, int3
                              const AuxPtrs& a, cudaStream_t s) {
   int threads = (d.E + 31) / 32 * 32;
   plan_scan_kernel<<<1, threads, 0, s>>>(d.E, d.nblk, hist, counts, offsets, a.poff,
-                                         a.tile_expert, a.num_mtiles, a.ptile, a.num_ptiles);
+                                         a.tile_expert, a.num_mtiles, a.ptile, a.num_ptiles,
+                                         a.dwr_q0, a.dwr_item_e);
   return cudaGetLastError();
 }
 
