@@ -256,7 +256,7 @@ def kernel_work(cfg, name, counts=None):
     mx = name.endswith("_mxfp8")
     name = name[:-len("_mxfp8")] if mx else name
     b = 1.0 + 1.0 / 32 if mx else 2.0     # bytes per operand element (MXFP8: + scales)
-    uv = 2.0 if mx else 4.0               # bytes per saved U, V element (MXFP8 keeps bf16)
+    uv = 2.0                              # bytes per saved U, V element (kept as bf16)
     ob = result_bytes(cfg)                # O / dXg rows and weight gradients written
     # (FLOPs, bytes): operands b bytes, U and V uv bytes, O / dXg rows and gradients ob
     tbl = {

@@ -291,10 +291,10 @@ SavedLayout saved_layout(const Dims& d) {
   Bump b;
   SavedLayout L;
   const size_t P = d.P_cat;
-  L.u = b.take(4 * P * d.I);
-  L.v = b.take(4 * P * d.I);
-  L.us = b.take(4 * (size_t)d.T * d.Is);
-  L.vs = b.take(4 * (size_t)d.T * d.Is);
+  L.u = b.take(2 * P * d.I);   // U, V kept for the backward as bf16
+  L.v = b.take(2 * P * d.I);
+  L.us = b.take(2 * (size_t)d.T * d.Is);
+  L.vs = b.take(2 * (size_t)d.T * d.Is);
   L.xg = b.take(2 * P * d.H);
   L.total = b.off;
   return L;
@@ -804,8 +804,8 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   SavedLayout S = saved_layout(d);
   auto W = [&](size_t off) -> void* { return at(workspace, off); };
   MOK_CHECK_CUDA(begin_counters(ctx, W(L.tcnt), s));
-  const float* su = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.u));
-  const float* sv = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.v));
+  const void* su = at(const_cast<void*>(saved), S.u);   // U, V kept as bf16
+  const void* sv = at(const_cast<void*>(saved), S.v);
   void* dxg = W(L.dxg);
   float* dgp = reinterpret_cast<float*>(W(L.dgp));
   float* dl = reinterpret_cast<float*>(W(L.dl));
@@ -919,8 +919,8 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     GemmCall cs = dense_call(d, a, kBwdDH);
     cs.a[0] = dY;
     cs.b[0] = w->Ws_down;
-    cs.u = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.us));
-    cs.v = reinterpret_cast<const float*>(at(const_cast<void*>(saved), S.vs));
+    cs.u = at(const_cast<void*>(saved), S.us);
+    cs.v = at(const_cast<void*>(saved), S.vs);
     cs.out[0] = W(L.dus);
     cs.out[2] = W(L.dvs);
     cs.out[4] = W(L.hsg);

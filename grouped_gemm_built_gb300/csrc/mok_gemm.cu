@@ -154,8 +154,8 @@ struct Params {
   const int32_t* table;
   const float* gates;
   // epilogue inputs
-  const float* u;   // kBwdDH: saved U, V [rows][I] fp32
-  const float* v;
+  const void* u;    // kBwdDH: saved U, V [rows][I] bf16
+  const void* v;
   const int32_t* uv_row;   // kBwdDH: row of U, V per row of the row space (null: the same)
   float* dgp;
   uint32_t* status;
@@ -272,17 +272,6 @@ __device__ __forceinline__ void set_error(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);
 }
 
-__device__ __forceinline__ void load_f32x32(const float* src, float* v) {
-  const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 w = __ldg(s + q);
-    v[4 * q] = w.x;
-    v[4 * q + 1] = w.y;
-    v[4 * q + 2] = w.z;
-    v[4 * q + 3] = w.w;
-  }
-}
 // Fast division: the SwiGLU epilogues run one warp per SM sub-partition and are
 // latency-bound; IEEE division made the MXFP8 forward up|gate launch 19% slower.
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
@@ -971,18 +960,25 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
                 sbytes;
           }
         } else {
-          // BF16: h as the down GEMM's bf16 operand, U, V saved in fp32
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(t_row + c * 32, a);          // U
-            tmem_ld32(t_row + 128 + c * 32, b);    // V
-            if (c == 3) release();
+          // BF16: h as the down GEMM's bf16 operand; U, V kept as bf16 for the backward, two
+          // 32-column chunks at a time in 64-column boxes
+          for (int c = 0; c < 4; c += 2) {
+            float a1[32], b1[32];
+            tmem_ld32(t_row + c * 32, a);                // U
+            tmem_ld32(t_row + 128 + c * 32, b);          // V
+            tmem_ld32(t_row + (c + 1) * 32, a1);
+            tmem_ld32(t_row + 128 + (c + 1) * 32, b1);
+            if (c == 2) release();
+            const int col = ti.n0 + c * 32;
             float h[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
-            const int col = ti.n0 + c * 32;
             st.bf16(&mp.o[0], h, col, wrow);
-            st.f32(&mp.o[1], a, col, wrow);
-            st.f32(&mp.o[2], b, col, wrow);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = b1[i] * sigmoidf_(b1[i]) * a1[i];
+            st.bf16(&mp.o[0], h, col + 32, wrow);
+            st.bf16x64(&mp.o[1], a, a1, col, wrow);
+            st.bf16x64(&mp.o[2], b, b1, col, wrow);
           }
         }
         break;
@@ -1040,14 +1036,9 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
           tmem_ld32(t_row + c * 32, a);          // D = dY W_down^T
           if (c == p.BN / 32 - 1) release();
           float u[32], v[32];
-          if (have_uv) {
-            if (MX) {                            // saved U, V (bf16 in MXFP8)
-              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.u) + ouv + c * 32, u);
-              load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.v) + ouv + c * 32, v);
-            } else {                             // saved U, V (fp32)
-              load_f32x32(p.u + ouv + c * 32, u);
-              load_f32x32(p.v + ouv + c * 32, v);
-            }
+          if (have_uv) {                         // U, V as the forward kept them (bf16)
+            load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.u) + ouv + c * 32, u);
+            load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(p.v) + ouv + c * 32, v);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = v[i] = a[i] = 0.f;
@@ -2054,8 +2045,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
            make_map(&mp.b[0], c.b[0], c.I, G * c.H, BK, eb) &&
            make_map(&mp.b[1], c.b[1], c.I, G * c.H, BK, eb) &&
            (MX || make_out_map(&mp.o[0], c.out[0], c.I, rows, 2)) &&
-           make_out_map(&mp.o[1], c.out[1], c.I, rows, MX ? 2 : 4, MX) &&
-           make_out_map(&mp.o[2], c.out[2], c.I, rows, MX ? 2 : 4, MX);
+           make_out_map(&mp.o[1], c.out[1], c.I, rows, 2, true) &&
+           make_out_map(&mp.o[2], c.out[2], c.I, rows, 2, true);
       max_tiles = mt_rows * p.n_tiles;
       break;
     case kFwdDown:

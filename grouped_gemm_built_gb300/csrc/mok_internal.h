@@ -228,8 +228,8 @@ struct GemmCall {
   void* out[6];         // outputs (kBwdDH: du, du lo, dv, dv lo, g*h, g*h lo; lo optional)
   bool split;           // dW modes (bf16): operands a[1] / b[2..3] hold the lo halves
   bool out_bf16;        // kFwdDown, kBwdDX, dW modes: outputs rounded to bf16 (else fp32)
-  const float* u;       // kBwdDH: saved U, V (fp32)
-  const float* v;
+  const void* u;        // kBwdDH: saved U, V (bf16)
+  const void* v;
   const int32_t* uv_row;// kBwdDH: row of U, V for each row of the row space (null: the same
                         // row; -1: a padding row, read as zeros)
   float* dgp;           // kBwdDH: per-tile partial router-weight gradients

@@ -59,8 +59,9 @@ typedef enum {
  *   weights, h and the dX GEMM's du, dv are bf16; the weight-gradient GEMMs take du, dv
  *   and g*h as bf16 hi + lo pairs (two MMAs per K step), close to fp32 operands.
  * MOK_MXFP8: E4M3 elements with one UE8M0 scale per 32 along each GEMM's contraction axis;
- *   the forward keeps U, V for the backward in bf16 (du, dv are quantised to E4M3
- *   anyway); the shared expert stays BF16 (as in MOK_BF16).
+ *   the shared expert stays BF16 (as in MOK_BF16).
+ * In every precision the forward keeps U = x W_up and V = x W_gate for the backward as bf16
+ *   values (h itself is formed from the fp32 accumulators).
  * MOK_BF16_WGRAD_PLAIN: as MOK_BF16 with single bf16 du, dv, g*h in the weight-gradient
  *   GEMMs: half their MMAs, at the cost of one bf16 rounding of each operand. The pages
  *   name BF16 and MXFP8 only; how BF16 feeds the weight gradients is this library's

@@ -33,11 +33,13 @@ Precision model (``precision``): "fp64" applies no rounding at all. "bf16" (the 
 BF16 mode: bf16 tensor-core operands, fp32 accumulation) rounds h, the down GEMM's
 operand, and du, dv as operands of the dX GEMM to bf16; the GPU feeds du, dv and g*h to
 the weight-gradient GEMMs as bf16 hi + lo pairs (a 16-bit significand), so there they
-stay unrounded here; U, V, expert outputs, routed dX rows and all results stay unrounded
-too (the GPU keeps them in fp32). "bf16_plain" is "bf16" with du, dv and g*h rounded to
-bf16 for the weight-gradient GEMMs as well. "mxfp8" quantises every GEMM operand to
-MXFP8 blocks of 32 along that GEMM's contraction axis (inputs, weights, h, du, dv, g*h,
-dY), and keeps U, V for the backward as bf16 values (h is formed from the unrounded ones).
+stay unrounded here; expert outputs, routed dX rows and all results stay unrounded too
+(the GPU keeps them in fp32 until the result's own rounding). "bf16_plain" is "bf16" with
+du, dv and g*h rounded to bf16 for the weight-gradient GEMMs as well. "mxfp8" quantises
+every GEMM operand to MXFP8 blocks of 32 along that GEMM's contraction axis (inputs,
+weights, h, du, dv, g*h, dY). Every mode but "fp64" keeps U, V for the backward as bf16
+values, the routed experts' and the shared expert's (h is formed from the unrounded
+ones in the forward; the backward's SwiGLU', du, dv and g*h read the kept values).
 Everything else is float64. The shared expert is always BF16: single bf16
 weight-gradient operands in "bf16_plain", hi/lo ones in "bf16" and "mxfp8".
 
@@ -174,8 +176,8 @@ class Precision:
         return self.fwd_act(a, axis)
 
     def saved_uv(self, a):
-        """U, V as kept for the backward: bf16 in mxfp8 mode, unrounded otherwise."""
-        return bf16_round(a) if self.mx else a
+        """U, V as kept for the backward: bf16 values (unrounded in fp64 mode)."""
+        return a if self.mode == "fp64" else bf16_round(a)
 
     def bwd_act_rows(self, a):
         """du, dv, g*h feeding a weight-gradient GEMM (K = expert rows): MXFP8 blocks of 32
@@ -206,7 +208,7 @@ def shared_forward(x, Ws_up, Ws_gate, Ws_down, mode: str, out: str = "fp32"):
     V = x @ Ws_gate
     h = P.fwd_act(silu(V) * U, 1)
     O = out_round(out)(h @ Ws_down)
-    return O, {"Us": U, "Vs": V}
+    return O, {"Us": P.saved_uv(U), "Vs": P.saved_uv(V)}
 
 
 def forward(x, idx, gates, W_up, W_gate, W_down, shared=None, precision="fp64",

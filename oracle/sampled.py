@@ -4,12 +4,13 @@ TEST INFRASTRUCTURE ONLY (see oracle/__init__.py). The dense oracle in ``moe`` h
 routed row of every expert; at the Kimi/DeepSeek sizes that is too much, so these
 functions compute one token's y or dX row, or one element or line of a weight gradient,
 straight from the definition (with the same rounding model as ``moe``, precision "bf16":
-h, the down GEMM's operand, and du, dv as operands of the dX GEMM are rounded to bf16;
-the weight-gradient functions take ``plain`` to choose "bf16_plain" over "bf16"):
+h, the down GEMM's operand, and du, dv as operands of the dX GEMM are rounded to bf16,
+and the backward reads U, V as bf16 values, as the forward keeps them; the
+weight-gradient functions take ``plain`` to choose "bf16_plain" over "bf16"):
 
 * y_t = sum_j g_tj O_(t,j) + shared(x_t), O = bf16(silu(x W_gate) * (x W_up)) W_down;
 * dX_t = sum_j (bf16(du) W_up^T + bf16(dv) W_gate^T) + dXs_t + sum_j dl_tj Wr[:, e_j],
-  with D = dY_t W_down^T, du = g D silu(V), dv = g D U silu'(V);
+  with D = dY_t W_down^T, du = g D silu(V), dv = g D U silu'(V) (U, V the kept bf16 values);
 * dW_down[e][i][h] = sum over e's rows of (g silu(V) U)[i] dY[t][h];
 * dW_up[e][h][i] = sum over e's rows of x[t][h] du[i] (dW_gate with dv).
 
@@ -43,6 +44,7 @@ def _row_terms(x_t, dY_t, g, Wu, Wg, Wd, out="fp32"):
     O = rnd(h @ Wd)
     res = {"O": O}
     if dY_t is not None:
+        U, V = bf16_round(U), bf16_round(V)   # as kept for the backward
         D = Wd @ dY_t                      # = dY_t W_down^T
         hv = silu(V) * U
         res["dg"] = float(D @ hv)
@@ -77,6 +79,7 @@ def token_outputs(t, x, idx, gates, weights, dY=None, shared=None, Wr=None, out=
         v = x_t @ Ws_gate
         y += rnd(bf16_round(silu(v) * u) @ Ws_down)
         if dY_t is not None:
+            u, v = bf16_round(u), bf16_round(v)   # as kept for the backward
             D = Ws_down @ dY_t
             du = D * silu(v)
             dv = D * u * dsilu(v)
@@ -115,14 +118,14 @@ def dw_elements(e, pairs, x, dY, gates, Wu, Wg, Wd, picks, plain=False):
             continue
         if name == "dW_down":
             i, h = a, b
-            U = X @ Wu[:, i]
-            V = X @ Wg[:, i]
+            U = bf16_round(X @ Wu[:, i])   # U, V as kept for the backward
+            V = bf16_round(X @ Wg[:, i])
             hg = rnd(g * silu(V) * U)
             out.append(float(hg @ dYe[:, h]))
         else:
             h, i = a, b
-            U = X @ Wu[:, i]
-            V = X @ Wg[:, i]
+            U = bf16_round(X @ Wu[:, i])
+            V = bf16_round(X @ Wg[:, i])
             D = dYe @ Wd[i, :]
             if name == "dW_up":
                 d = rnd(g * D * silu(V))
@@ -143,8 +146,8 @@ def dw_lines(pairs, x, dY, gates, Wu, Wg, Wd, i, plain=False, out="fp32"):
     g = np.asarray(gates[t, pairs[:, 1]], np.float64)
     X = np.asarray(x[t], np.float64)
     dYe = np.asarray(dY[t], np.float64)
-    U = X @ Wu[:, i]
-    V = X @ Wg[:, i]
+    U = bf16_round(X @ Wu[:, i])   # U, V as kept for the backward
+    V = bf16_round(X @ Wg[:, i])
     D = dYe @ Wd[i, :]
     hg = rnd(g * silu(V) * U)
     du = rnd(g * D * silu(V))
@@ -261,8 +264,8 @@ def shared_dw_lines(x, dY, Ws_up, Ws_gate, Ws_down, i, plain=False, out="fp32"):
     ro = out_round(out)
     x = np.asarray(x, np.float64)
     dY = np.asarray(dY, np.float64)
-    U = x @ Ws_up[:, i]
-    V = x @ Ws_gate[:, i]
+    U = bf16_round(x @ Ws_up[:, i])   # U, V as kept for the backward
+    V = bf16_round(x @ Ws_gate[:, i])
     D = dY @ Ws_down[i, :]
     return {"dWs_down": ro(rnd(silu(V) * U) @ dY), "dWs_up": ro(x.T @ rnd(D * silu(V))),
             "dWs_gate": ro(x.T @ rnd(D * U * dsilu(V)))}

@@ -180,32 +180,40 @@ def _flip_dev(a, delta):
 
 
 def bf16_flip_slack(cfg, inp, idx, gates):
-    """Elementwise allowance for the weight gradients in the bf16_plain mode, where du, dv and
-    g*h are rounded to bf16 before the weight-gradient GEMMs. The GPU rounds fp32 values
-    that come out of GEMMs over H; the oracle rounds exact ones. The fp32 sums U, V, D
-    are taken to be within 6 sqrt(H) u sum|a b| of the exact ones (u = 2^-24): the
-    probabilistic bound of Higham and Mary ("A New Approach to Probabilistic Rounding
-    Error Analysis", 2019) with lambda = 6, which fails for a given sum with probability
-    below 2 exp(-18); the worst-case bound H u sum|a b| flags about half of all operands
-    at these sizes and would say little. Propagated to first order through SwiGLU', an
-    operand within that bound of a rounding midpoint may round to another bf16 value: the
-    slack of a dW element is the sum, over its contraction, of |other operand| * (largest
-    such move) for its operands.
-    Returns (dict of slack arrays shaped like the gradients, fraction of operands near a
-    midpoint)."""
+    """Elementwise allowance for the weight gradients in the BF16 modes with fp32 results.
+    The backward reads U, V as the forward kept them, bf16 on both sides: the GPU rounds
+    its fp32 sums, the oracle exact values. In bf16_plain, du, dv and g*h are rounded to
+    bf16 again before the weight-gradient GEMMs; in bf16 they go in as hi + lo pairs
+    (a 16-bit significand). The fp32 sums U, V, D are taken to be within
+    6 sqrt(H) u sum|a b| of the exact ones (u = 2^-24): the probabilistic bound of Higham
+    and Mary ("A New Approach to Probabilistic Rounding Error Analysis", 2019) with
+    lambda = 6, which fails for a given sum with probability below 2 exp(-18); the
+    worst-case bound H u sum|a b| flags about half of all operands at these sizes and
+    would say little. A U or V within that bound of a rounding midpoint may keep another
+    bf16 value; propagated to first order through SwiGLU', that moves du, dv, g*h, and in
+    bf16_plain one of those within its moved bound of a midpoint may round to another bf16
+    value. The slack of a dW element is the sum, over its contraction, of |other operand|
+    * (largest such move) for its operands.
+    Returns (dict of slack arrays shaped like the gradients, fraction of operands whose
+    value may differ by a rounding flip: du, dv, g*h in bf16_plain, U, V in bf16)."""
     from oracle import moe
-    from oracle.numerics import sigmoid
+    from oracle.numerics import bf16_round, sigmoid
     x = np64(inp["x"])
     dY = np64(inp["dY"])
     Wu, Wg, Wd = (np64(inp[n]) for n in ("W_up", "W_gate", "W_down"))
     H = cfg.H
     u = 2.0 ** -24
     gam = 6.0 * np.sqrt(H) * u   # see the docstring
+    plain = cfg.precision == "bf16_plain"
 
     def operand_flips(X, dYr, g, A, B, C):
         U, V, D = X @ A, X @ B, dYr @ C.T
         aX, adY = np.abs(X), np.abs(dYr)
         bU, bV, bD = gam * (aX @ np.abs(A)), gam * (aX @ np.abs(B)), gam * (adY @ np.abs(C).T)
+        # the backward reads U, V kept as bf16 on both sides: they differ by the rounding
+        # flip of the GPU's fp32 sums
+        (bU, nU), (bV, nV) = _flip_dev(U, bU), _flip_dev(V, bV)
+        U, V = bf16_round(U), bf16_round(V)
         sg = sigmoid(V)
         s0 = V * sg
         s1 = sg * (1 + V * (1 - sg))
@@ -216,10 +224,17 @@ def bf16_flip_slack(cfg, inp, idx, gates):
         d_dv = ag * (bD * np.abs(U * s1) + np.abs(D * s1) * bU + np.abs(D * U * s2) * bV) \
             + 8 * u * np.abs(dv)
         d_hg = ag * (np.abs(s1 * U) * bV + np.abs(s0) * bU) + 8 * u * np.abs(hg)
-        f_du, n1 = _flip_dev(du, d_du)
-        f_dv, n2 = _flip_dev(dv, d_dv)
-        f_hg, n3 = _flip_dev(hg, d_hg)
-        return (aX.T @ f_du, aX.T @ f_dv, f_hg.T @ adY), (n1 + n2 + n3) / 3
+        if plain:
+            f_du, n1 = _flip_dev(du, d_du)
+            f_dv, n2 = _flip_dev(dv, d_dv)
+            f_hg, n3 = _flip_dev(hg, d_hg)
+            n = (n1 + n2 + n3) / 3
+        else:   # hi + lo operands: their bound, plus the pair's 2^-17
+            hl = 2.0 ** -17
+            f_du, f_dv, f_hg = (d + hl * np.abs(v) for d, v in
+                                ((d_du, du), (d_dv, dv), (d_hg, hg)))
+            n = (nU + nV) / 2
+        return (aX.T @ f_du, aX.T @ f_dv, f_hg.T @ adY), n
 
     pl = moe.plan(idx, cfg.E)
     out = {"dW_up": np.zeros(Wu.shape), "dW_gate": np.zeros(Wg.shape),

@@ -20,9 +20,10 @@ delta is a first-order bound propagated through the GPU's arithmetic, step by st
   contraction as near a midpoint and say little;
 * elementwise fp32 arithmetic (SwiGLU, its derivative, the gate products) errs by a few
   units, taken as 8 u relative;
-* an intermediate rounded on both sides (h, and du, dv for the dX GEMM, in bf16; the
-  expert output rows and routed dX rows with bf16 results; du, dv, g*h with single bf16
-  weight-gradient operands) moves by its own rounding flip, found the same way;
+* an intermediate rounded on both sides (h, U and V as kept for the backward, and du, dv
+  for the dX GEMM, in bf16; the expert output rows and routed dX rows with bf16 results;
+  du, dv, g*h with single bf16 weight-gradient operands) moves by its own rounding flip,
+  found the same way;
 * the weight-gradient GEMMs' bf16 hi + lo operand pairs carry a 16-bit significand:
   2^-17 relative;
 * the router's gates: the GPU's fp32 logits lie within the worst-case bound of
@@ -119,7 +120,13 @@ def bwd_rows(f, dYr, g, dgb, Wu, Wg, Wd, plain=False, out_bf16=True):
     the routed dX rows (dXg, with bound f_dXg), the router-weight gradient dg and its
     bound d_dg."""
     H, I = Wu.shape
-    U, V, bU, bV, s, s0, s1 = (f[n] for n in ("U", "V", "bU", "bV", "s", "s0", "s1"))
+    # the backward reads U, V as the forward kept them, bf16 on both sides: they differ
+    # by the rounding flip of the GPU's fp32 sums
+    U, V = bf16_round(f["U"]), bf16_round(f["V"])
+    bU, bV = flip_dev(f["U"], f["bU"]), flip_dev(f["V"], f["bV"])
+    s = sigmoid(V)
+    s0 = V * s
+    s1 = s * (1 + V * (1 - s))
     s2 = s * (1 - s) * (2 + V * (1 - 2 * s))
     D = dYr @ Wd.T
     bD = gam(H) * (np.abs(dYr) @ np.abs(Wd).T)

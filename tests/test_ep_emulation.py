@@ -54,8 +54,11 @@ def test_ep_slices_match_the_single_layer(P):
     for f in ("y", "dX", "dWr"):
         err = gu.rel_err(res[f].cpu(), gu.np64(full[f]))
         assert err < 1e-5, (f, err)
-    # and the oracle, at the layer's tolerance
+    # and the oracle, at the layer's tolerance (weight gradients with the allowance for
+    # U, V rounding flips)
     idx, gates, _ = gu.oracle_route(cfg, inp)
     ref = gu.run_oracle(cfg, inp, idx, gates, backward=True)
+    slack, _ = gu.bf16_flip_slack(cfg, inp, idx, gates)
     for f in ("y", "dX", "dW_up", "dW_down", "dWr"):
-        assert gu.rel_err(res[f].cpu(), ref[f]) <= gu.TOL["bf16"], f
+        err = gu.rel_err_slack(res[f].cpu(), ref[f], slack.get(f, 0.0))
+        assert err <= gu.TOL["bf16"], (f, err)

@@ -366,11 +366,12 @@ def test_shared_dw_lines_match_the_dense_oracle(rng, mode, out):
         assert np.allclose(L["dWs_gate"], g.dWs_gate[:, i], rtol=1e-12, atol=1e-12)
 
 
-def test_mxfp8_saved_uv_rounding_point(rng):
-    """In mxfp8 mode the forward keeps U, V for the backward as bf16 values, while h (and
-    so y) is formed from the unrounded U, V; bf16 mode keeps U, V unrounded."""
+def test_saved_uv_rounding_point(rng):
+    """The forward keeps U, V for the backward as bf16 values in mxfp8 and in bf16 mode
+    (the shared expert's too), while h (and so y) is formed from the unrounded U, V; fp64
+    mode keeps them exact."""
     from oracle.numerics import bf16_round, mx_qdq, silu
-    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=24, H=64, I=64, E=3, k=2)
+    x, Wr, b, Wu, Wg, Wd, sh, dY = small_problem(rng, T=24, H=64, I=64, E=3, k=2, shared=True)
     r = moe.route(x, Wr, 2)
     y, saved = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="mxfp8")
     U, V = saved["U"], saved["V"]
@@ -382,8 +383,18 @@ def test_mxfp8_saved_uv_rounding_point(rng):
     Ue, Ve = A @ mx_qdq(Wu[e], 0), A @ mx_qdq(Wg[e], 0)
     assert np.array_equal(U[r0:r1], bf16_round(Ue))          # rounded where they are saved
     assert not np.array_equal(Ue, bf16_round(Ue))             # (so rounding changes them)
+    Xe = x[pl.table[r0:r1, 0]]
     _, saved16 = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="bf16")
-    assert not np.array_equal(saved16["U"], bf16_round(saved16["U"]))
+    assert np.array_equal(saved16["U"][r0:r1], bf16_round(Xe @ Wu[e]))
+    assert np.array_equal(saved16["V"][r0:r1], bf16_round(Xe @ Wg[e]))
+    _, saved64 = moe.forward(x, r.idx, r.gates, Wu, Wg, Wd, precision="fp64")
+    assert np.allclose(saved64["U"][r0:r1], Xe @ Wu[e], rtol=0, atol=1e-12)
+    assert not np.array_equal(saved64["U"], bf16_round(saved64["U"]))
+    _, ssh = moe.shared_forward(x, *sh, "bf16")
+    assert np.array_equal(ssh["Us"], bf16_round(x @ sh[0]))
+    assert np.array_equal(ssh["Vs"], bf16_round(x @ sh[1]))
+    _, ssh64 = moe.shared_forward(x, *sh, "fp64")
+    assert np.allclose(ssh64["Us"], x @ sh[0], rtol=0, atol=1e-12)
     # h, the down GEMM's operand, comes from the unrounded U, V: y matches that, not the
     # rounded values
     h_exact = mx_qdq(silu(Ve) * Ue, 1)
@@ -520,9 +531,10 @@ def test_result_rounding_points_forward(rng):
 def test_result_rounding_points_backward(rng):
     """bf16 results: one token, both slots to one expert (gates 1/4, 3/4), a shared expert,
     W_down the identity, W_up = c I and W_gate = (c/2) I (c = 1 + 2^-10). Each routed dX
-    row is bf16(c du' + (c/2) dv') with du', dv' the dX GEMM's bf16 operands, the shared
-    expert's dX row likewise with gate 1; dX is their sum rounded once; every weight
-    gradient is its exact sum over the rows rounded once (dW_up = x^T du per slot)."""
+    row is bf16(c du' + (c/2) dv') with du', dv' the dX GEMM's bf16 operands (formed from
+    U = bf16(c x), V = bf16(c x / 2), as the forward keeps them), the shared expert's dX
+    row likewise with gate 1; dX is their sum rounded once; every weight gradient is its
+    exact sum over the rows rounded once (dW_up = x^T du per slot)."""
     from oracle.numerics import bf16_round, dsilu, silu
     H, c = 64, 1.0 + 2.0 ** -10
     x = bf16_round(rng.normal(0, 1, (1, H)))
@@ -534,7 +546,8 @@ def test_result_rounding_points_backward(rng):
     _, saved = moe.forward(x, idx, gates, Wu, Wg, Wd, shared=sh, precision="bf16", out="bf16")
     g = moe.backward(x, idx, gates, Wu, Wg, Wd, saved, dY, shared=sh, precision="bf16",
                      out="bf16")
-    U, V = c * x, c / 2 * x
+    U, V = bf16_round(c * x), bf16_round(c / 2 * x)
+    assert not np.array_equal(U, c * x)   # (the kept values differ from the exact ones)
 
     def rows(gt):
         du, dv = gt * dY * silu(V), gt * dY * U * dsilu(V)

@@ -75,7 +75,7 @@ P = {
         _rng(), "bf16"),
     "out_fwd": lambda: tl.test_result_rounding_points_forward(_rng()),
     "out_bwd": lambda: tl.test_result_rounding_points_backward(_rng()),
-    "saved_uv": lambda: tl.test_mxfp8_saved_uv_rounding_point(_rng()),
+    "saved_uv": lambda: tl.test_saved_uv_rounding_point(_rng()),
     "wgrad_plain": lambda: tl.test_weight_gradient_operand_rounding_point(_rng(), "bf16_plain"),
     "wgrad_hilo": lambda: tl.test_weight_gradient_operand_rounding_point(_rng(), "bf16"),
     "down_bf16": lambda: tl.test_down_gemm_operand_rounding_point(_rng(), "bf16"),
@@ -184,9 +184,18 @@ MISTAKES = {
         moe, "backward", "dW_up = np.zeros(W_up.shape)", "dW_up = np.ones(W_up.shape)",
         ["empty"]),
     # rounding points
-    "MXFP8 mode keeps U, V unrounded": (
-        moe.Precision, "saved_uv", "return bf16_round(a) if self.mx else a", "return a",
-        ["saved_uv"]),
+    "U, V kept unrounded for the backward": (
+        moe.Precision, "saved_uv", 'return a if self.mode == "fp64" else bf16_round(a)',
+        "return a", ["saved_uv"]),
+    "U, V rounded in fp64 mode too": (
+        moe.Precision, "saved_uv", 'return a if self.mode == "fp64" else bf16_round(a)',
+        "return bf16_round(a)", ["saved_uv"]),
+    "the shared expert keeps U, V unrounded": (
+        moe, "shared_forward", 'return O, {"Us": P.saved_uv(U), "Vs": P.saved_uv(V)}',
+        'return O, {"Us": U, "Vs": V}', ["saved_uv"]),
+    "the sampled evaluator's backward reads unrounded U, V": (
+        sampled, "_row_terms", "U, V = bf16_round(U), bf16_round(V)   # as kept for the backward",
+        "U, V = U, V", ["sampled"]),
     "bf16_plain weight-gradient operands unrounded": (
         moe.Precision, "bwd_act_rows", "return bf16_round(a)", "return a", ["wgrad_plain"]),
     "hi/lo weight-gradient operands rounded to bf16": (

@@ -1,8 +1,9 @@
 """The allowance for bf16 results (tests/out_slack.py): it admits a GPU-like result and
 still rejects planted mistakes. Everything here runs on the CPU. The "GPU-like" side is an
 fp32 emulation of the library's arithmetic with the library's rounding points (fp32 GEMM
-sums, bf16 h, bf16 du, dv for the dX GEMM, hi + lo weight-gradient operands, bf16 expert
-output rows, routed dX rows and results, fp32 combines in slot order); the oracle side is
+sums, bf16 h, U and V kept as bf16 for the backward, bf16 du, dv for the dX GEMM, hi + lo
+weight-gradient operands, bf16 expert output rows, routed dX rows and results, fp32
+combines in slot order); the oracle side is
 the fp64 oracle with bf16 results modelled (``out="bf16"``)."""
 import numpy as np
 import pytest
@@ -59,6 +60,8 @@ def emulate(cfg, inp, idx, mistake=None):
         s, s0 = _silu32(V)
         h = _bf(s0 * U)
         Orow = _bf(h @ C)
+        U, V = _bf(U), _bf(V)             # kept as bf16 for the backward
+        s, s0 = _silu32(V)
         D = dYr @ C.T
         s1 = (s * (1 + V * (1 - s))).astype(F)
         hv = (s0 * U).astype(F)

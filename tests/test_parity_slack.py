@@ -1,7 +1,8 @@
-"""The bf16 rounding-flip allowance used by the weight-gradient parity checks: it admits
-a GPU-like result (fp32 GEMM errors within the bound, then bf16 rounding) and still
-rejects planted mistakes. Everything here runs on the CPU; the "GPU-like" side is the
-oracle's own arithmetic with perturbed intermediates."""
+"""The bf16 rounding-flip allowance used by the weight-gradient parity checks with fp32
+results: it admits a GPU-like result (fp32 GEMM errors within the bound, then bf16
+rounding of U, V and, in bf16_plain, of du, dv, g*h) and still rejects planted mistakes,
+in both BF16 modes. Everything here runs on the CPU; the "GPU-like" side is the oracle's
+own arithmetic with perturbed intermediates."""
 import numpy as np
 import pytest
 
@@ -11,8 +12,8 @@ from oracle.numerics import bf16_round, dsilu, silu
 from tests import gpu_util as gu
 
 
-def _case(seed=0):
-    cfg = mi.MoEConfig("slack", T=64, H=128, I=128, E=32, k=2)
+def _case(seed=0, precision="bf16_plain"):
+    cfg = mi.MoEConfig("slack", T=64, H=128, I=128, E=32, k=2, precision=precision)
     inp = mi.make_inputs(cfg, seed=seed, with_dy=True)
     idx, gates, _ = gu.oracle_route(cfg, inp)
     return cfg, inp, idx, gates
@@ -20,11 +21,14 @@ def _case(seed=0):
 
 def _dw_with(cfg, inp, idx, gates, perturb, rng, sign_dv=1.0):
     """dW_up, dW_gate, dW_down with U, V, D perturbed by up to ``perturb`` times their
-    fp32-sum bound, then du, dv, g*h rounded to bf16 (the GPU's operand points)."""
+    fp32-sum bound, U, V then kept as bf16 (as the forward keeps them), du, dv, g*h rounded
+    to bf16 in bf16_plain (the GPU's operand points; bf16 takes them as hi + lo pairs,
+    close to exact)."""
     x, dY = gu.np64(inp["x"]), gu.np64(inp["dY"])
     Wu, Wg, Wd = (gu.np64(inp[n]) for n in ("W_up", "W_gate", "W_down"))
     gam = 6.0 * np.sqrt(cfg.H) * 2.0 ** -24      # the bound the allowance assumes
     pl = moe.plan(idx, cfg.E)
+    rnd = bf16_round if cfg.precision == "bf16_plain" else (lambda v: v)
     out = [np.zeros(Wu.shape), np.zeros(Wg.shape), np.zeros(Wd.shape)]
     for e in range(cfg.E):
         r0, r1 = pl.offsets[e], pl.offsets[e + 1]
@@ -39,15 +43,17 @@ def _dw_with(cfg, inp, idx, gates, perturb, rng, sign_dv=1.0):
         U = U + perturb * bU * rng.uniform(-1, 1, U.shape)
         V = V + perturb * bV * rng.uniform(-1, 1, V.shape)
         D = D + perturb * bD * rng.uniform(-1, 1, D.shape)
-        du = bf16_round(g * D * silu(V))
-        dv = bf16_round(sign_dv * g * D * U * dsilu(V))
-        hg = bf16_round(g * silu(V) * U)
+        U, V = bf16_round(U), bf16_round(V)
+        du = rnd(g * D * silu(V))
+        dv = rnd(sign_dv * g * D * U * dsilu(V))
+        hg = rnd(g * silu(V) * U)
         out[0][e], out[1][e], out[2][e] = X.T @ du, X.T @ dv, hg.T @ dYe
     return dict(zip(("dW_up", "dW_gate", "dW_down"), out))
 
 
-def test_slack_admits_perturbations_within_the_bound():
-    cfg, inp, idx, gates = _case()
+@pytest.mark.parametrize("precision", ["bf16_plain", "bf16"])
+def test_slack_admits_perturbations_within_the_bound(precision):
+    cfg, inp, idx, gates = _case(precision=precision)
     rng = np.random.default_rng(1)
     ref = _dw_with(cfg, inp, idx, gates, 0.0, rng)
     slack, frac = gu.bf16_flip_slack(cfg, inp, idx, gates)
@@ -75,9 +81,10 @@ def test_slack_is_zero_away_from_midpoints():
     assert dev[0] == 3 * 2.0 ** -7
 
 
+@pytest.mark.parametrize("precision", ["bf16_plain", "bf16"])
 @pytest.mark.parametrize("mistake", ["dv_sign", "dropped_gate", "scaled_row"])
-def test_slack_still_rejects_planted_mistakes(mistake):
-    cfg, inp, idx, gates = _case()
+def test_slack_still_rejects_planted_mistakes(mistake, precision):
+    cfg, inp, idx, gates = _case(precision=precision)
     rng = np.random.default_rng(2)
     ref = _dw_with(cfg, inp, idx, gates, 0.0, rng)
     slack, _ = gu.bf16_flip_slack(cfg, inp, idx, gates)
