@@ -1017,18 +1017,21 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
       }
       case kBwdDH: {
         float g = 1.f;
+        bool real = true;   // a row of the expert, not segment padding
         if (!p.dense) {
           const int rl = row - p.poff[ti.e];
           g = 0.f;
-          if (rl < p.counts[ti.e]) {
+          real = rl < p.counts[ti.e];
+          if (real) {
             const int tr = p.offsets[ti.e] + rl;
             g = p.gates[(size_t)p.table[2 * tr] * p.k + p.table[2 * tr + 1]];
           }
         }
         const size_t o = (size_t)row * p.I + ti.n0;
-        // U, V of this row: the same row, or its row in the layout the forward kept them in
+        // U, V of this row: the same row, or its row in the layout the forward kept them in.
+        // A padding row reads neither and gives exact zeros (its D, U, V may be anything)
         const int urow = p.uv_row ? p.uv_row[row] : row;
-        const bool have_uv = valid && urow >= 0;
+        const bool have_uv = valid && real && urow >= 0;
         const size_t ouv = (size_t)(urow < 0 ? 0 : urow) * p.I + ti.n0;
         float dg = 0.f;
         for (int c = 0; c < p.BN / 32; ++c) {

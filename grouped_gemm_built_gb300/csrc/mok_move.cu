@@ -28,6 +28,10 @@ __device__ __forceinline__ int padded_row(int sl, int E, const int32_t* topk_idx
 }  // namespace
 
 // ---------------------------------------------------------------- dispatch (pull gather)
+// Rows of the padded row space: an expert's rows from the table; after them, zeros up to the
+// next multiple of 16 rows (the weight-gradient GEMMs' last MMA K step reads that far and
+// multiplies these rows by zero operands, which must not meet a NaN); the rest of the
+// segment is left as it is (no GEMM result that is read depends on it).
 __global__ void __launch_bounds__(256) gather_rows_kernel(
     int H, int E, const uint4* __restrict__ src, const int32_t* __restrict__ table,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
@@ -46,7 +50,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
       const uint4* s = src + (size_t)t * nvec;
 #pragma unroll 4
       for (int i = lane; i < nvec; i += 32) d[i] = __ldg(s + i);
-    } else {
+    } else if (r < (counts[e] + 15) / 16 * 16) {
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int i = lane; i < nvec; i += 32) d[i] = z;
     }
