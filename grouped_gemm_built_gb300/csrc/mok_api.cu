@@ -743,7 +743,20 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.out_sf[0] = W(L.hsf);
     c.out[1] = at(saved, S.u);
     c.out[2] = at(saved, S.v);
-    MOK_LAUNCH("gemm_fwd_upgate_swiglu_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
+    // the BF16 shared expert's tiles run in the same launches ([C] "Outras
+    // caracteristicas": MXFP8 training with the shared expert in BF16)
+    if (d.Is) {
+      c.s_a = x;
+      c.s_b[0] = w->Ws_up;
+      c.s_b[1] = w->Ws_gate;
+      c.s_out[0] = W(L.hs);
+      c.s_out[1] = at(saved, S.us);
+      c.s_out[2] = at(saved, S.vs);
+      c.s_rows = d.T;
+      c.s_I = d.Is;
+    }
+    MOK_LAUNCH(d.Is ? "gemm_fwd_upgate_swiglu_mxfp8_shared" : "gemm_fwd_upgate_swiglu_mxfp8",
+               launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     c = routed_call(d, sched, a, kFwdDown);
     c.mx = true;
     c.a[0] = W(L.hq);
@@ -752,10 +765,20 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     c.sfb0 = mxw + M.down_i_sf;
     c.out[0] = o;
     c.out_bf16 = ob;
-    MOK_LAUNCH("gemm_fwd_down_mxfp8", launch_gemm(timed(c, ctx), launch_sms(ctx), s));
+    if (d.Is) {
+      c.s_a = W(L.hs);
+      c.s_b[0] = w->Ws_down;
+      c.s_out[0] = W(L.os);
+      c.s_rows = d.T;
+      c.s_I = d.Is;
+    }
+    MOK_LAUNCH(d.Is ? "gemm_fwd_down_mxfp8_shared" : "gemm_fwd_down_mxfp8",
+               launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   }
   const void* shared_out = nullptr;
-  if (d.Is) {
+  if (d.Is && mx) {
+    shared_out = W(L.os);   // written by the MXFP8 launches above
+  } else if (d.Is) {
     GemmCall cs = dense_call(d, a, kFwdUpGate);
     cs.a[0] = x;
     cs.b[0] = w->Ws_up;

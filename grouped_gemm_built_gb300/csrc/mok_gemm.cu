@@ -137,6 +137,12 @@ struct Params {
   const int32_t* ptile;
   const int32_t* num_ptiles;
   int max_ptiles;
+  // MXFP8 forward launches that also run the BF16 shared expert ([C] "Outras
+  // caracteristicas": MXFP8 training with the shared expert in BF16): shared_tiles BF16
+  // tiles follow the routed ones (kernel variant 3), with their own maps a[2], b[2..3],
+  // o[3..5]: s_rows = T rows, s_n_tiles column tiles of s_BN, s_kiters K blocks of 64
+  int shared_tiles;
+  int s_rows, s_n_tiles, s_kiters, s_BN, s_I;
   uint64_t timeout_ns;  // bound of every wait (MOK_ERR_TIMEOUT when it passes)
   int n_out;        // kRouter: output columns (E)
   const float* bias;// kRouter: logit bias or null
@@ -181,6 +187,7 @@ struct TileInfo {
   int klast;    // dW modes: MMA K steps of the last K iteration that hold rows
   int skip;     // 1: no tile here (the unmatched half of the last row-tile pair)
   int nrt;      // row tiles in this tile: 1, or 2 (a row-tile pair: rows row0 .. row0+255)
+  int bf;       // 1: a BF16 shared-expert tile of an MXFP8 forward launch (rows of x / hs)
 };
 
 __host__ __device__ __forceinline__ bool is_dw(int mode) { return mode == kBwdDWDown || mode == kBwdDWUpGate; }
@@ -197,7 +204,7 @@ __device__ __forceinline__ int num_tiles_of(const Params& p) {
   if (is_dw(p.mode)) return p.groups * p.m_tiles_dw * p.n_tiles;
   if (p.pair) return min(max(*p.num_ptiles, 0), p.max_ptiles) * p.n_tiles;
   if (p.dense) return ((p.M_rows + BM - 1) / BM) * p.n_tiles;
-  return ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles;
+  return ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles + p.shared_tiles;
 }
 
 template <bool MX>
@@ -207,6 +214,7 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
   TileInfo ti;
   ti.skip = 0;
   ti.nrt = 1;
+  ti.bf = 0;
   ti.klast = BK / MMA_K;
   if (p.pair) {   // tile = pair q of column block nt; the pair's tiles share the expert
     const int q = tile / p.n_tiles;
@@ -248,6 +256,19 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
     }
   } else {
     int mt, nt;
+    const int nr = p.shared_tiles ? ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles : 0;
+    if (p.shared_tiles && tile >= nr) {   // a BF16 shared-expert tile after the routed ones
+      const int l = tile - nr;
+      mt = l / p.s_n_tiles;
+      ti.bf = 1;
+      ti.e = 0;
+      ti.row0 = mt * BM;
+      ti.arow0 = ti.row0;
+      ti.n0 = (l - mt * p.s_n_tiles) * (p.mode == kFwdUpGate ? 128 : p.s_BN);
+      ti.kiters = p.s_kiters;
+      ti.krow0 = 0;
+      return ti;
+    }
     if (p.dense) {
       mt = tile / p.n_tiles;
       nt = tile - mt * p.n_tiles;
@@ -489,6 +510,38 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
   const int sp = p.split;
   uint32_t b_bytes = (p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 256 * 128 : p.BN * 128;
   if (MX) b_bytes += 512 + ((p.mode == kFwdUpGate || p.mode == kBwdDWUpGate) ? 1024 : p.BN * 4);
+  if (MX && ti.bf) {
+    // BF16 shared-expert tile in an MXFP8 launch: the BF16 stage layout (K blocks of 64
+    // elements, 64-element MN chunks Cfg<false>::MN_LBO apart), no scale atoms
+    using CB = Cfg<false>;
+    const uint32_t bb = p.mode == kFwdUpGate ? 256 * 128 : p.s_BN * 128;
+    for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
+      const int stage = it % STAGES;
+      const uint32_t round = it / STAGES;
+      if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1, globaltimer_ns() + p.timeout_ns)) {
+        set_error(p.status, kErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+      uint8_t* sa = smem + stage * p.stage_bytes;
+      uint8_t* sb = sa + A_BYTES;
+      uint64_t* bar = &full[stage];
+      mbar_arrive_expect_tx(bar, A_BYTES + bb);
+      const int k0 = kb * CB::BK;
+      tma_load_2d(sa, &mp.a[2], bar, k0, ti.arow0);
+      if (p.mode == kFwdUpGate) {
+        for (int c = 0; c < 128 / CB::MN_CHUNK; ++c) {
+          tma_load_2d(sb + c * CB::MN_LBO, &mp.b[2], bar, ti.n0 + c * CB::MN_CHUNK, k0);
+          tma_load_2d(sb + (128 / CB::MN_CHUNK + c) * CB::MN_LBO, &mp.b[3], bar,
+                      ti.n0 + c * CB::MN_CHUNK, k0);
+        }
+      } else {
+        for (int c = 0; c < p.s_BN / CB::MN_CHUNK; ++c)
+          tma_load_2d(sb + c * CB::MN_LBO, &mp.b[2], bar, ti.n0 + c * CB::MN_CHUNK, k0);
+      }
+    }
+    return true;
+  }
   {
     for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
       const int stage = it % STAGES;
@@ -751,6 +804,39 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
     default: a_mn = true; b_mn = true; n_mma = 256; break;
   }
   const uint32_t idesc = idesc_bf16(BM, n_mma, a_mn, b_mn);
+  if (MX && ti.bf) {   // BF16 shared-expert tile: kind::f16 MMAs on the BF16 stage layout
+    using CB = Cfg<false>;
+    const uint32_t idb = idesc_bf16(BM, p.mode == kFwdUpGate ? 256 : p.s_BN, false, true);
+    const int acc = local % p.nacc;
+    const uint32_t use = local / p.nacc;
+    if (use > 0 && !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + p.timeout_ns)) {
+      set_error(p.status, kErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + acc * p.acc_cols;
+    for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
+      const int stage = it % STAGES;
+      if (!mbar_wait(&full[stage], (it / STAGES) & 1, globaltimer_ns() + p.timeout_ns)) {
+        set_error(p.status, kErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
+      const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(d_tmem, umma_desc_sw128(sa + kk * 32, 16, 1024),
+                  umma_desc_sw128(sb + kk * CB::MN_KSTEP, CB::MN_LBO, 1024), idb,
+                  (kb > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&empty[stage]);
+    }
+    if (ti.kiters > 0) umma_commit(&acc_full[acc]);
+    else mbar_arrive(&acc_full[acc]);
+    return true;
+  }
   {
     const int acc = local % p.nacc;
     const uint32_t use = local / p.nacc;
@@ -926,7 +1012,33 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
     switch (p.mode) {
       case kFwdUpGate: {
         const size_t o = (size_t)row * p.I + ti.n0;
+        // BF16: h as the down GEMM's bf16 operand; U, V kept as bf16 for the backward, two
+        // 32-column chunks at a time in 64-column boxes (maps o[m0..m0+2])
+        auto bf16_upgate = [&](int m0) {
+          for (int c = 0; c < 4; c += 2) {
+            float a1[32], b1[32];
+            tmem_ld32(t_row + c * 32, a);                // U
+            tmem_ld32(t_row + 128 + c * 32, b);          // V
+            tmem_ld32(t_row + (c + 1) * 32, a1);
+            tmem_ld32(t_row + 128 + (c + 1) * 32, b1);
+            if (c == 2) release();
+            const int col = ti.n0 + c * 32;
+            float h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
+            st.bf16(&mp.o[m0], h, col, wrow);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = b1[i] * sigmoidf_(b1[i]) * a1[i];
+            st.bf16(&mp.o[m0], h, col + 32, wrow);
+            st.bf16x64(&mp.o[m0 + 1], a, a1, col, wrow);
+            st.bf16x64(&mp.o[m0 + 2], b, b1, col, wrow);
+          }
+        };
         if constexpr (MX) {
+          if (ti.bf) {   // the shared expert's tile of a mixed launch
+            bf16_upgate(3);
+            break;
+          }
           uint32_t sbytes = 0;
           // two 32-column chunks at a time: U, V leave as bf16 in 64-column boxes, h as
           // MXFP8 blocks of 32 along I (plain stores of the codes, the scale word below)
@@ -960,26 +1072,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
                 sbytes;
           }
         } else {
-          // BF16: h as the down GEMM's bf16 operand; U, V kept as bf16 for the backward, two
-          // 32-column chunks at a time in 64-column boxes
-          for (int c = 0; c < 4; c += 2) {
-            float a1[32], b1[32];
-            tmem_ld32(t_row + c * 32, a);                // U
-            tmem_ld32(t_row + 128 + c * 32, b);          // V
-            tmem_ld32(t_row + (c + 1) * 32, a1);
-            tmem_ld32(t_row + 128 + (c + 1) * 32, b1);
-            if (c == 2) release();
-            const int col = ti.n0 + c * 32;
-            float h[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = b[i] * sigmoidf_(b[i]) * a[i];
-            st.bf16(&mp.o[0], h, col, wrow);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = b1[i] * sigmoidf_(b1[i]) * a1[i];
-            st.bf16(&mp.o[0], h, col + 32, wrow);
-            st.bf16x64(&mp.o[1], a, a1, col, wrow);
-            st.bf16x64(&mp.o[2], b, b1, col, wrow);
-          }
+          bf16_upgate(0);
         }
         break;
       }
@@ -998,19 +1091,21 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         break;
       }
       case kFwdDown:
-      case kBwdDX: {   // expert outputs / routed dX rows, fp32 or bf16
+      case kBwdDX: {   // expert outputs / routed dX rows (shared expert output: o[3]), fp32 or bf16
+        const int bn = ti.bf ? p.s_BN : p.BN;
+        const CUtensorMap* om = &mp.o[ti.bf ? 3 : 0];
         if (p.out_bf16) {
-          for (int c = 0; c < p.BN / 32; c += 2) {
+          for (int c = 0; c < bn / 32; c += 2) {
             tmem_ld32(t_row + c * 32, a);
             tmem_ld32(t_row + (c + 1) * 32, b);
-            if (c + 2 >= p.BN / 32) release();
-            st.bf16x64(&mp.o[0], a, b, ti.n0 + c * 32, wrow);
+            if (c + 2 >= bn / 32) release();
+            st.bf16x64(om, a, b, ti.n0 + c * 32, wrow);
           }
         } else {
-          for (int c = 0; c < p.BN / 32; ++c) {
+          for (int c = 0; c < bn / 32; ++c) {
             tmem_ld32(t_row + c * 32, a);
-            if (c == p.BN / 32 - 1) release();
-            st.f32(&mp.o[0], a, ti.n0 + c * 32, wrow);
+            if (c == bn / 32 - 1) release();
+            st.f32(om, a, ti.n0 + c * 32, wrow);
           }
         }
         break;
@@ -1219,8 +1314,9 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
 // One instantiation per mode (and, for the dW modes, per hi/lo split): with both
 // compile-time constants the compiler keeps only that launch's producer, MMA and epilogue
 // code (a smaller instruction footprint, a straight-line MMA issue).
-// VAR: 0 plain, 1 split (hi/lo dW operands), 2 row-tile pairs. Fixing the variant at
-// compile time keeps the pair and split paths out of the other kernels' code.
+// VAR: 0 plain, 1 split (hi/lo dW operands), 2 row-tile pairs, 3 MXFP8 forward with the
+// BF16 shared expert's tiles. Fixing the variant at compile time keeps those paths out of
+// the other kernels' code.
 template <bool MX, int MODE, int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p_in) {
@@ -1229,6 +1325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   p.mode = MODE;
   p.split = VAR == 1;
   p.pair = VAR == 2;
+  if (VAR != 3) p.shared_tiles = 0;   // variant 3: MXFP8 forward with BF16 shared tiles
   // CLC: the grid is sized to the largest tile count; a CTA past the actual count (which
   // the plan wrote to device memory) has no tile and leaves before taking any resource
   if (p.clc && (int)blockIdx.x >= num_tiles_of(p)) return;
@@ -1404,6 +1501,7 @@ __device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph
   ti.klast = 4;
   ti.skip = r >= mega_mtiles(q, m);
   ti.nrt = 1;
+  ti.bf = 0;
   return ti;
 }
 
@@ -2016,6 +2114,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.ptile = c.ptile;
   p.num_ptiles = c.num_ptiles;
   p.max_ptiles = c.max_ptiles;
+  const bool mixed = MX && c.s_a && (c.mode == kFwdUpGate || c.mode == kFwdDown);
   p.dgp = c.dgp;
   p.status = c.status;
   p.sfa = static_cast<const uint8_t*>(c.sfa);
@@ -2133,6 +2232,32 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   }
   // routed row-space launches number their tiles in row-tile pairs (num_tiles_of)
   if (!p.dense && !is_dw(c.mode)) max_tiles = (mt_rows + 1) / 2 * 2 * p.n_tiles;
+  if (mixed && ok) {   // the BF16 shared expert's tiles after the routed ones
+    const uint64_t T = (uint64_t)c.s_rows;
+    if (c.s_rows <= 0 || c.s_I <= 0 || c.s_I % 128) return cudaErrorInvalidValue;
+    p.s_rows = c.s_rows;
+    p.s_I = c.s_I;
+    if (c.mode == kFwdUpGate) {
+      p.s_n_tiles = c.s_I / 128;
+      p.s_kiters = c.H / Cfg<false>::BK;
+      p.s_BN = 256;
+      ok = make_map(&mp.a[2], c.s_a, c.H, T, BM, 2) &&
+           make_map(&mp.b[2], c.s_b[0], c.s_I, c.H, Cfg<false>::BK, 2) &&
+           make_map(&mp.b[3], c.s_b[1], c.s_I, c.H, Cfg<false>::BK, 2) &&
+           make_out_map(&mp.o[3], c.s_out[0], c.s_I, T, 2) &&
+           make_out_map(&mp.o[4], c.s_out[1], c.s_I, T, 2, true) &&
+           make_out_map(&mp.o[5], c.s_out[2], c.s_I, T, 2, true);
+    } else {
+      p.s_BN = (c.H % 256 == 0) ? 256 : 128;
+      p.s_n_tiles = c.H / p.s_BN;
+      p.s_kiters = c.s_I / Cfg<false>::BK;
+      ok = make_map(&mp.a[2], c.s_a, c.s_I, T, BM, 2) &&
+           make_map(&mp.b[2], c.s_b[0], c.H, c.s_I, Cfg<false>::BK, 2) &&
+           make_res_map(&mp.o[3], c.s_out[0], c.H, T, ob);
+    }
+    p.shared_tiles = (int)((T + BM - 1) / BM) * p.s_n_tiles;
+    max_tiles += p.shared_tiles;
+  }
   if (p.pair) {   // three [A0 | B | A1] stages, both accumulators for one tile
     static_assert(3 * PAIR_STAGE_BYTES + OUT_STAGING <= Cfg<false>::DATA_BYTES &&
                       PAIR_STAGE_BYTES % 1024 == 0 && PAIR_A1_OFF % 1024 == 0,
@@ -2151,12 +2276,14 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
 using GemmKernel = void (*)(const Maps, const Params);
 
 template <bool MX>
-GemmKernel gemm_kernel_for(int mode, int split, int pair) {
+GemmKernel gemm_kernel_for(int mode, int split, int pair, int mixed) {
   switch (mode) {
     case kFwdUpGate:
+      if (MX && mixed) return grouped_gemm_kernel<MX, kFwdUpGate, MX ? 3 : 0>;
       return pair ? grouped_gemm_kernel<MX, kFwdUpGate, MX ? 0 : 2>
                   : grouped_gemm_kernel<MX, kFwdUpGate, 0>;
     case kFwdDown:
+      if (MX && mixed) return grouped_gemm_kernel<MX, kFwdDown, MX ? 3 : 0>;
       return pair ? grouped_gemm_kernel<MX, kFwdDown, MX ? 0 : 2>
                   : grouped_gemm_kernel<MX, kFwdDown, 0>;
     case kBwdDH: return grouped_gemm_kernel<MX, kBwdDH, 0>;
@@ -2176,16 +2303,16 @@ GemmKernel gemm_kernel_for(int mode, int split, int pair) {
 template <bool MX>
 cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   using C = Cfg<MX>;
-  static bool attr_set[8][3] = {};
+  static bool attr_set[8][4] = {};
   if (c.mode < 0 || c.mode >= 8) return cudaErrorInvalidValue;
   Params p;
   Maps mp;
   int max_tiles = 0;
   cudaError_t e = build_call<MX>(c, p, mp, max_tiles);
   if (e != cudaSuccess) return e;
-  const GemmKernel kern = gemm_kernel_for<MX>(c.mode, p.split, p.pair);
+  const GemmKernel kern = gemm_kernel_for<MX>(c.mode, p.split, p.pair, p.shared_tiles > 0);
   if (!kern) return cudaErrorInvalidValue;
-  const int var = p.split ? 1 : p.pair ? 2 : 0;
+  const int var = p.split ? 1 : p.pair ? 2 : p.shared_tiles > 0 ? 3 : 0;
   if (!attr_set[c.mode][var]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

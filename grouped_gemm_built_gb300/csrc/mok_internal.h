@@ -241,6 +241,10 @@ struct GemmCall {
   // against one weight tile, two accumulators side by side (AuxLayout::ptile)
   bool pair = false;
   const int32_t* ptile; const int32_t* num_ptiles; int max_ptiles;
+  // MXFP8 kFwdUpGate / kFwdDown: the BF16 shared expert's tiles in the same launch
+  // (s_a: x, or the shared h; s_b: Ws_up, Ws_gate, or Ws_down; s_out: hs, Us, Vs, or the
+  // shared output rows; s_rows = T; s_I the shared expert's intermediate size); null: none
+  const void* s_a; const void* s_b[2]; void* s_out[3]; int s_rows, s_I;
   uint32_t* status;
   uint64_t timeout_ns;  // bound of every device wait (0: 2 s)
   int* tile_counter;    // dynamic tile order: a zeroed int of device memory (null: static)

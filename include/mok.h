@@ -59,7 +59,8 @@ typedef enum {
  *   weights, h and the dX GEMM's du, dv are bf16; the weight-gradient GEMMs take du, dv
  *   and g*h as bf16 hi + lo pairs (two MMAs per K step), close to fp32 operands.
  * MOK_MXFP8: E4M3 elements with one UE8M0 scale per 32 along each GEMM's contraction axis;
- *   the shared expert stays BF16 (as in MOK_BF16).
+ *   the shared expert stays BF16 (as in MOK_BF16); in the forward its BF16 tiles run in
+ *   the same launches as the routed MXFP8 tiles (up|gate, then down), after them.
  * In every precision the forward keeps U = x W_up and V = x W_gate for the backward as bf16
  *   values (h itself is formed from the fp32 accumulators).
  * MOK_BF16_WGRAD_PLAIN: as MOK_BF16 with single bf16 du, dv, g*h in the weight-gradient

@@ -330,6 +330,29 @@ def test_row_tile_pairs_keep_the_bits(name):
             assert torch.equal(res[f], ref[f]), (pairs, order, f)
 
 
+@pytest.mark.parametrize("shared_I", [128, 384])
+def test_mxfp8_launches_carry_the_bf16_shared_expert(shared_I):
+    """In MXFP8 the routed forward launches also run the BF16 shared expert's tiles
+    (after the routed ones, with their own operands and stage layout). The shared expert's
+    weight gradients, which read the U, V those tiles kept, equal bit for bit the BF16
+    layer's, whose shared expert runs in launches of its own (both take hi/lo shared
+    operands); the layer against the oracle is covered by ragged_shared_mx."""
+    base = mi.scaled(MX_CASES["ragged_shared_mx"], shared_I=shared_I)
+    inp = gu.gpu_inputs(base, seed=3)
+    rm, _ = gu.run_gpu(base, inp)
+    rb, _ = gu.run_gpu(mi.scaled(base, precision="bf16"), inp)
+    assert rm["status"] == 0 and rb["status"] == 0
+    for f in ("dWs_up", "dWs_gate", "dWs_down"):
+        assert torch.equal(rm[f], rb[f]), f
+    for order in (1, 2):   # the shared tiles in the dynamic and CLC tile orders
+        L = gu.make_layer(base)
+        mok.mok_set_tile_order(L.ctx, order)
+        ro, _ = gu.run_gpu(base, inp, layer=L)
+        assert ro["status"] == 0
+        for f in ("y", "dX", "dWs_up", "dWs_gate", "dWs_down"):
+            assert torch.equal(ro[f], rm[f]), (order, f)
+
+
 @pytest.mark.parametrize("name", ["ragged_shared", "ragged_shared_plain", "ragged_shared_mx"])
 def test_bf16_results_are_the_fp32_sums_rounded(name):
     """The weight gradients come out of the same fp32 accumulators in both result types:
