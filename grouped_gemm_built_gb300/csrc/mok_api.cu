@@ -709,7 +709,7 @@ mok_status mok_moe_fwd(mok_ctx_t ctx, const mok_sched* sched, const void* x,
     // dispatch: pull token rows into expert order through the table
     MOK_LAUNCH("dispatch_gather",
                launch_gather_rows(d, x, *sched, a, at(saved, S.xg), launch_sms(ctx), s));
-    // grouped up|gate GEMM + SwiGLU (h bf16; U, V saved in fp32)
+    // grouped up|gate GEMM + SwiGLU (h bf16; U, V saved as bf16)
     GemmCall c = routed_call(d, sched, a, kFwdUpGate, use_pairs(ctx));
     c.a[0] = at(saved, S.xg);
     c.b[0] = w->W_up;

@@ -97,7 +97,7 @@ struct BwdWs {
   size_t q_du_i, sf_du_i, q_dv_i, sf_dv_i, q_du_r, sf_du_r, q_dv_r, sf_dv_r, q_hg_r, sf_hg_r;
   size_t total;
 };
-// saved activations (forward -> backward): U, V fp32; xg: the gathered rows of x in the
+// saved activations (forward -> backward): U, V bf16; xg: the gathered rows of x in the
 // padded row space (BF16 forward), which the backward's weight gradients read again
 struct SavedLayout {
   size_t u, v, us, vs, xg, total;
@@ -200,7 +200,7 @@ enum GemmMode : int {
 
 // Operands per mode (BF16; MXFP8 in brackets):
 //   kFwdUpGate   a0 = Xg [x_q]; b0, b1 = W_up, W_gate; out0 = h bf16 [out_q0 + atoms],
-//                out1, out2 = U, V fp32 (saved)
+//                out1, out2 = U, V bf16 (saved)
 //   kFwdDown     a0 = h [h_q]; b0 = W_down; out0 = O fp32 (out_bf16: bf16)
 //   kBwdDH       a0 = dYg [dY_q]; b0 = W_down; u, v = saved U, V; out0..5 = du, dv, g*h as
 //                bf16 hi/lo pairs [out_q0..4 + atoms]; dgp
