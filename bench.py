@@ -528,15 +528,16 @@ def analyse(cfg, prof, ms_step, pk, workload):
             "data_movement": moves, "kernels": per_kernel, "gemm_tc": gemm_tc}
 
 
-def sub_record(name, cfg, args, pk, local, fwd_path=None):
+def sub_record(name, cfg, args, pk, local, fwd_path=None, min_steps=3):
     """One more workload measured the same way in this process (one GPU): its own layer,
-    warm-up, timed steps, clock samples and analysis; the buffers are freed afterwards."""
+    warm-up, timed steps (at least ``min_steps``: short steps need more of them for the
+    clock samples), clock samples and analysis; the buffers are freed afterwards."""
     import torch
     L, inp, w, grads, y = make_layer_for(cfg, args, fwd_path=fwd_path)
     clk = ClockSampler(local, args.clocks_csv.replace("{gpu}", f"{local}_{name}")
                        if args.clocks_csv else "")
     clk.start()
-    steps = max(3, args.sub_steps)
+    steps = max(min_steps, args.sub_steps)
     ms, prof, launches, phases, clocks = time_steps(
         cfg, L, lambda: layer_step(cfg, L, inp, w, grads, y), steps, args.warmup, clk, 1)
     ms_step = ms / steps
@@ -679,9 +680,15 @@ def run_gpu(args):
                 plans.append(("bf16_hilo_wgrad", workload_config("kimi_8192"), None))
             plans.append(("megakernel_fwd", cfg, "megakernel"))
             plans.append(("mxfp8_dsv3_imbalanced", workload_config("dsv3_imbalanced"), None))
+            # the pages' own megakernel setting: one EP=64 slice (6 experts, 2048 tokens of
+            # 8 slots, MXFP8 forward), one launch per step and the megakernel
+            ep = workload_config("ep64_slice")
+            plans.append(("ep64_slice_launches", ep, "launches"))
+            plans.append(("ep64_slice_megakernel", ep, "megakernel"))
         for name, c2, path in plans:
             try:
-                subs[name] = sub_record(name, c2, args, pk, local, fwd_path=path)
+                subs[name] = sub_record(name, c2, args, pk, local, fwd_path=path,
+                                        min_steps=200 if name.startswith("ep64") else 3)
             except Exception as exc:   # a sub-record never costs the headline line
                 subs[name] = {"error": repr(exc)}
                 torch.cuda.empty_cache()
