@@ -68,6 +68,11 @@ CONFIGS = {
     "kimi_e24_profile": MoEConfig("kimi_e24_profile", T=512, H=7168, I=2048, E=24, k=8),
     "kimi_e24_profile_plain": MoEConfig("kimi_e24_profile_plain", T=512, H=7168, I=2048,
                                         E=24, k=8, precision="bf16_plain"),
+    # Kimi-2.5 hidden size, every token to all 8 experts (32768 routed rows, 0.47 GB of
+    # gathered bf16 rows, more than L2): a few GB on the device, for the DRAM counters of
+    # the row-moving kernels (dispatch, combine and their reverses) and the router's.
+    "kimi_movement_profile": MoEConfig("kimi_movement_profile", T=4096, H=7168, I=2048, E=8,
+                                       k=8, precision="bf16_plain"),
     # DeepSeek-V3 expert shape in MXFP8 with 16 experts and the same ~512 rows per expert
     # as T=16384 with 256 experts: a few GB on the device, for detailed kernel profiles.
     "dsv3_e16_profile": MoEConfig("dsv3_e16_profile", T=1024, H=7168, I=2048, E=16, k=8,
