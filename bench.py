@@ -84,7 +84,7 @@ def peaks():
 NCU_TRAFFIC = {
     # profiles/grouped_gemm_kimi_e24.md: 16 x (0.105 + 1.347) GB at E=24, T=512
     ("kimi_8192_plain", "gemm_bwd_dw_upgate", "bf16"): {"bytes": 23.23e9,
-                                                       "rev": "5001f0384ce2255a"},
+                                                       "rev": "4e474ea25490adf7"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",

@@ -239,7 +239,7 @@ struct GemmCall {
   const int32_t* table; const float* gates; int k;
   // row-tile pairs (BF16 routed row-space modes): one CTA runs both row tiles of a pair
   // against one weight tile, two accumulators side by side (AuxLayout::ptile)
-  bool pair = false;
+  bool pair;
   const int32_t* ptile; const int32_t* num_ptiles; int max_ptiles;
   // MXFP8 kFwdUpGate / kFwdDown: the BF16 shared expert's tiles in the same launch
   // (s_a: x, or the shared h; s_b: Ws_up, Ws_gate, or Ws_down; s_out: hs, Us, Vs, or the
@@ -248,7 +248,7 @@ struct GemmCall {
   uint32_t* status;
   uint64_t timeout_ns;  // bound of every device wait (0: 2 s)
   int* tile_counter;    // dynamic tile order: a zeroed int of device memory (null: static)
-  bool clc = false;     // tiles handed out by cluster launch control (one CTA per tile)
+  bool clc;             // tiles handed out by cluster launch control (one CTA per tile)
   // MXFP8 (E4M3 operands with 512-byte scale atoms; see mok_quant.cu)
   bool mx;
   const void* sfa; const void* sfa1;                   // A scale atoms (second: kBwdDX dv)
