@@ -105,7 +105,8 @@ typedef enum { MOK_FWD_MEGAKERNEL = 0, MOK_FWD_LAUNCHES = 1, MOK_FWD_AUTO = 2 } 
  *   for another tile, cancels a CTA that has not been launched yet and runs that CTA's
  *   tile, so about one CTA per SM runs while the hardware hands out the rest. A launch
  *   whose tile count lives on the device (routed experts) is sized to the largest count
- *   the context's dimensions allow; CTAs beyond the actual count return at once.
+ *   the context's dimensions allow; CTAs beyond the actual count return at once. The
+ *   hardware places these CTAs on every SM: mok_set_sm_limit does not apply to them.
  * Every output tile is one CTA's fixed-order sum in each order: same bits. */
 typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1, MOK_TILES_CLC = 2 } mok_tile_order;
 
