@@ -48,6 +48,8 @@ def parse():
                          "workload's, bf16)")
     ap.add_argument("--row-pairs", default="auto", choices=["auto", "on", "off"],
                     help="row-tile pairs in the BF16 routed GEMMs")
+    ap.add_argument("--sm-pairs", default="auto", choices=["auto", "on", "off"],
+                    help="SM pairs (2-CTA clusters) in the BF16 weight-gradient GEMMs")
     ap.add_argument("--tile-order", default="static", choices=["static", "dynamic", "clc"],
                     help="tile order of the persistent grouped GEMMs")
     ap.add_argument("--no-sub", action="store_true",
@@ -82,9 +84,9 @@ def peaks():
 # and workload states. A figure is valid only for the GEMM source revision it was taken on
 # (gemm_source_rev) and the result type it was taken with.
 NCU_TRAFFIC = {
-    # profiles/grouped_gemm_kimi_e24.md: 16 x (0.105 + 1.347) GB at E=24, T=512
-    ("kimi_8192_plain", "gemm_bwd_dw_upgate", "bf16"): {"bytes": 23.23e9,
-                                                       "rev": "4e474ea25490adf7"},
+    # the 24-expert profiling case (E=24, T=512) scaled by 16: 16 x (0.105 + 1.348) GB
+    ("kimi_8192_plain", "gemm_bwd_dw_upgate", "bf16"): {"bytes": 23.25e9,
+                                                       "rev": "2db7fccf277e6c44"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
@@ -392,6 +394,8 @@ def make_layer_for(cfg, args, device="cuda", fwd_path=None):
                                    "clc": mok.MOK_TILES_CLC}[args.tile_order])
     mok.mok_set_row_pairs(L.ctx, {"auto": mok.MOK_PAIRS_AUTO, "on": mok.MOK_PAIRS_ON,
                                   "off": mok.MOK_PAIRS_OFF}[args.row_pairs])
+    mok.mok_set_sm_pairs(L.ctx, {"auto": mok.MOK_SMPAIRS_AUTO, "on": mok.MOK_SMPAIRS_ON,
+                                 "off": mok.MOK_SMPAIRS_OFF}[args.sm_pairs])
     mx = None
     if cfg.precision == "mxfp8":
         mx = L.quantize_weights(inp["W_up"], inp["W_gate"], inp["W_down"])
@@ -707,7 +711,7 @@ def run_gpu(args):
             "dtype": "mxfp8" if cfg.precision == "mxfp8" else "bf16", "data": "synthetic",
             "config": dict(workload_json(cfg), out=cfg.out, **mb,
                            fwd_path=args.fwd_path, tile_order=args.tile_order,
-                           row_pairs=args.row_pairs,
+                           row_pairs=args.row_pairs, sm_pairs=args.sm_pairs,
                            parallelism=f"replicas x{world}"),
             "clocks": clocks, "gpu_launches": launches,
             "megakernel_phases_ms": phases or None,

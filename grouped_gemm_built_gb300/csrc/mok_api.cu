@@ -32,6 +32,7 @@ struct mok_ctx_s {
   int withhold = 0;               // test hook of mok_test_withhold_signal
   mok_tile_order tile_order = MOK_TILES_STATIC;
   mok_row_pairs row_pairs = MOK_PAIRS_AUTO;
+  mok_sm_pairs sm_pairs = MOK_SMPAIRS_AUTO;
   int* tcnt = nullptr;            // tile counters of the current call (dynamic order)
   int tcnt_used = 0;
   // the latest forward kept U, V (and the gathered rows) in the per-macrobatch padded
@@ -415,6 +416,14 @@ mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order) {
   if (order != MOK_TILES_STATIC && order != MOK_TILES_DYNAMIC && order != MOK_TILES_CLC)
     return MOK_ERR_INVALID_ARG;
   ctx->tile_order = order;
+  return MOK_OK;
+}
+
+mok_status mok_set_sm_pairs(mok_ctx_t ctx, mok_sm_pairs mode) {
+  if (!ctx) return MOK_ERR_INVALID_ARG;
+  if (mode != MOK_SMPAIRS_AUTO && mode != MOK_SMPAIRS_ON && mode != MOK_SMPAIRS_OFF)
+    return MOK_ERR_INVALID_ARG;
+  ctx->sm_pairs = mode;
   return MOK_OK;
 }
 
@@ -991,6 +1000,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   c.out[0] = g->dW_up;
   c.out[1] = g->dW_gate;
   c.out_bf16 = ob;
+  c.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_upgate_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   c = routed_call(d, sched, a, kBwdDWDown);
   c.mx = mx;
@@ -1009,6 +1019,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
   }
   c.out[0] = g->dW_down;
   c.out_bf16 = ob;
+  c.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
   MOK_LAUNCH(mx ? "gemm_bwd_dw_down_mxfp8" : gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
   if (d.Is) {
     GemmCall cs = dense_call(d, a, kBwdDWUpGate);
@@ -1023,6 +1034,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     cs.out[0] = g->dWs_up;
     cs.out[1] = g->dWs_gate;
     cs.out_bf16 = ob;
+    cs.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kBwdDWDown);
     cs.a[0] = W(L.hsg);
@@ -1033,6 +1045,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
     cs.out[0] = g->dWs_down;
     cs.out_bf16 = ob;
+    cs.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
   }
   if (d.router)

@@ -63,6 +63,10 @@ constexpr int SPLIT_EXTRA_OFF = A_BYTES + B_BYTES;
 // row-tile pair stage (BF16): [A0 16 KB][B 32 KB][A1 16 KB]
 constexpr int PAIR_STAGE_BYTES = 2 * A_BYTES + B_BYTES;
 constexpr int PAIR_A1_OFF = A_BYTES + B_BYTES;
+// SM-pair dW stage (BF16, clusters of two CTAs): [A: this CTA's 128 rows][B: its half of the
+// tile's columns, at most 128], 16 KB each; six stages and two staging boxes per warp
+constexpr int SMP_STAGE_BYTES = 2 * A_BYTES;
+constexpr int SMP_STAGES = 6;
 
 template <bool MX>
 struct Cfg {
@@ -128,7 +132,7 @@ struct Params {
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
   int out_bf16;     // kFwdDown, kBwdDX, dW modes: round the outputs to bf16 (64-column boxes)
   int* tile_counter;// dynamic tile order: the next tile is atomicAdd(tile_counter, 1) (zero at
-                    // launch); null: the static order (tile blockIdx.x, + gridDim.x, ...)
+                    // launch); null: the static order (tiles t0, t0 + tstep, ...)
   int clc;          // cluster launch control: one CTA per tile; a CTA runs tile blockIdx.x,
                     // then the tiles of the not yet launched CTAs it cancels
   int pair;         // BF16 routed up|gate, down and dX: a tile is a pair of row tiles of one
@@ -137,6 +141,12 @@ struct Params {
   const int32_t* ptile;
   const int32_t* num_ptiles;
   int max_ptiles;
+  int smpair;       // BF16 dW modes on SM pairs: the two CTAs of a cluster share M = 256
+                    // MMAs (rank 0 issues them); a tile is 256 rows of dW, 128 per CTA, and
+                    // each CTA loads its A rows and half of the B columns
+  int crank;        // SM pairs: this CTA's rank in its cluster (set at kernel entry)
+  int t0, tstep;    // static order: first tile and stride (the CTA's, or its cluster's,
+                    // index and count; set at kernel entry)
   // MXFP8 forward launches that also run the BF16 shared expert ([C] "Outras
   // caracteristicas": MXFP8 training with the shared expert in BF16): shared_tiles BF16
   // tiles follow the routed ones (kernel variant 3), with their own maps a[2], b[2..3],
@@ -201,7 +211,7 @@ __device__ __forceinline__ int routed_mtiles(const Params& p) {
 // belong to one expert and read the same weight slice; with this order two neighbouring
 // CTAs take them in the same round, so the second read of the slice is an L2 hit.
 __device__ __forceinline__ int num_tiles_of(const Params& p) {
-  if (is_dw(p.mode)) return p.groups * p.m_tiles_dw * p.n_tiles;
+  if (is_dw(p.mode)) return p.groups * (p.smpair ? p.m_tiles_dw / 2 : p.m_tiles_dw) * p.n_tiles;
   if (p.pair) return min(max(*p.num_ptiles, 0), p.max_ptiles) * p.n_tiles;
   if (p.dense) return ((p.M_rows + BM - 1) / BM) * p.n_tiles;
   return ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles + p.shared_tiles;
@@ -232,11 +242,11 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
     return ti;
   }
   if (is_dw(p.mode)) {
-    const int per_e = p.m_tiles_dw * p.n_tiles;
+    const int per_e = (p.smpair ? p.m_tiles_dw / 2 : p.m_tiles_dw) * p.n_tiles;
     ti.e = tile / per_e;
     const int rem = tile - ti.e * per_e;
     const int mt = rem / p.n_tiles;
-    ti.row0 = mt * BM;
+    ti.row0 = (p.smpair ? 2 * mt + p.crank : mt) * BM;   // SM pair: this CTA's 128 rows
     ti.n0 = (rem - mt * p.n_tiles) * (p.mode == kBwdDWUpGate ? 128 : p.BN);
     int krows;
     if (p.dense) {
@@ -457,7 +467,8 @@ struct Stager {
 };
 
 // ------------------------------------------------------------------ tile order
-// Static order: CTA b takes tiles b, b + G, b + 2G, ... Dynamic order (a tile counter in
+// Static order: CTA b takes tiles b, b + G, b + 2G, ... (SM pairs: cluster b of G, both of
+// its CTAs the same tiles, each its half of the rows). Dynamic order (a tile counter in
 // global memory): the producer lane of each CTA takes the next tile with an atomic add when
 // it is ready for one, and passes it to the CTA's MMA lane and epilogue warps through a
 // queue of TQ slots in shared memory (slot q: tile id, "full" barrier of 1 arrival, "empty"
@@ -499,7 +510,9 @@ __device__ __forceinline__ bool tq_take(const Params& p, const TileQueue& tq, ui
 // ------------------------------------------------------------------ producer
 // One tile's K loop: fills stages it, it+1, ... (it counts stage uses over the CTA's
 // whole task sequence). Returns false after a timed-out wait.
-template <bool MX>
+// SMP: the SM-pair kernel (its tcgen05 and TMA instructions of the CTA pair may not share a
+// kernel with single-CTA ones, so the pair paths exist only in that instantiation).
+template <bool MX, bool SMP = false>
 __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
                              uint64_t* empty, volatile int* abort_flag, const TileInfo& ti,
                              uint32_t& it) {
@@ -555,6 +568,23 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
       uint8_t* sb = sa + A_BYTES;
       uint8_t* sf = sa + p.sf_off;
       uint64_t* bar = &full[stage];
+      if constexpr (!MX && SMP) {
+        // SM pair: this CTA's 128 rows of A and its half of B's columns (dW up|gate: rank
+        // 0 du, rank 1 dv, columns n0..n0+127; dW down: columns n0 + rank * BN/2 ..), the
+        // copies of both CTAs counted on rank 0's barrier, which rank 0 arms for both
+        const uint32_t lbar = mapa_rank(bar, 0);
+        const int nb = p.BN / 2;
+        if (p.crank == 0) mbar_arrive_expect_tx(bar, 2 * (A_BYTES + nb * 128));
+        const int kr = ti.krow0 + kb * BK;
+        for (int c = 0; c < BM / C::MN_CHUNK; ++c)
+          tma_load_2d_pair(sa + c * CH, &mp.a[0], lbar, ti.row0 + c * C::MN_CHUNK, kr);
+        const bool ug = p.mode == kBwdDWUpGate;
+        const CUtensorMap* bmap = ug ? &mp.b[p.crank] : &mp.b[0];
+        const int bc = ug ? ti.n0 : ti.n0 + p.crank * nb;
+        for (int c = 0; c < nb / C::MN_CHUNK; ++c)
+          tma_load_2d_pair(sb + c * CH, bmap, lbar, bc + c * C::MN_CHUNK, kr);
+        continue;
+      }
       uint32_t extra = 0;   // split dW stages also carry the lo half of the split operand
       if (sp) extra = p.mode == kBwdDWUpGate ? 2 * 128 * 128 : BM * 128;
       if (MX && p.kdouble) extra = A_BYTES + b_bytes;   // the second K chunk
@@ -721,17 +751,17 @@ __device__ __forceinline__ bool clc_answer(const Params& p, ClcState& c, int& x)
   return true;
 }
 
-template <bool MX>
+template <bool MX, bool SMP = false>
 __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t* full,
                         uint64_t* empty, volatile int* abort_flag, const TileQueue& tq,
                         ClcState& clc) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   if (!p.tile_counter && !p.clc) {
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
-      if (!produce_tile<MX>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
+      if (!produce_tile<MX, SMP>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
     }
   } else {
     int own = p.clc ? (int)blockIdx.x : -1;   // CLC: the CTA's own tile comes first
@@ -784,6 +814,56 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// SM pair, rank 0: one tile's M = 256 MMAs over both CTAs' stages (both operands MN-major);
+// each commit arrives on the barrier at the same offset in both CTAs. Returns false after a
+// timed-out wait.
+template <bool MX>
+__device__ bool mma_tile_pair(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                              uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                              volatile int* abort_flag, const TileInfo& ti, uint32_t& it,
+                              int local) {
+  using C = Cfg<MX>;
+  const int STAGES = p.stages;
+  const uint32_t idp = idesc_bf16(2 * BM, p.BN, true, true);
+  const int acc = local % p.nacc;
+  const uint32_t use = local / p.nacc;
+  if (use > 0 &&
+      !mbar_wait(&acc_empty[acc], (use - 1) & 1, globaltimer_ns() + p.timeout_ns)) {
+    set_error(p.status, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+  }
+  tc_fence_after();
+  const uint32_t d_tmem = tmem_base + acc * p.acc_cols;
+  for (int kb = 0; kb < ti.kiters; ++kb, ++it) {
+    const int stage = it % STAGES;
+    if (!mbar_wait(&full[stage], (it / STAGES) & 1, globaltimer_ns() + p.timeout_ns)) {
+      set_error(p.status, kErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+    tc_fence_after();
+    const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
+    const uint32_t sb = sa + A_BYTES;
+    const int nk = kb == ti.kiters - 1 ? ti.klast : 4;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      if (kk >= nk) break;
+      umma_bf16_pair(d_tmem, umma_desc_sw128(sa + kk * C::MN_KSTEP, C::MN_LBO, 1024),
+                     umma_desc_sw128(sb + kk * C::MN_KSTEP, C::MN_LBO, 1024), idp,
+                     (kb > 0 || kk > 0) ? 1u : 0u);
+    }
+    umma_commit_pair(&empty[stage]);
+  }
+  if (ti.kiters > 0) {
+    umma_commit_pair(&acc_full[acc]);
+  } else {   // nothing to accumulate: both epilogues write zeros
+    mbar_arrive(&acc_full[acc]);
+    mbar_arrive_cluster(mapa_rank(&acc_full[acc], 1));
+  }
+  return true;
+}
+
 // One tile: waits for a free accumulator (local = the CTA's tile count so far), issues the
 // K loop's MMAs and commits the accumulator. Returns false after a timed-out wait.
 template <bool MX>
@@ -930,35 +1010,54 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   return true;
 }
 
-template <bool MX>
-__device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                          uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
-                          volatile int* abort_flag, const TileQueue& tq) {
+// Returns the number of tiles whose MMAs were issued.
+template <bool MX, bool SMP = false>
+__device__ int mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                         uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                         volatile int* abort_flag, const TileQueue& tq) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
   if (!p.tile_counter && !p.clc) {
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
-      if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
-                        it, local++))
-        return;
+      bool ok;
+      if constexpr (SMP)
+        ok = mma_tile_pair<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag,
+                               ti, it, local);
+      else
+        ok = mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                          it, local);
+      if (!ok) return local;
+      ++local;
     }
-    return;
+    return local;
   }
   for (uint32_t n = 0;; ++n) {
     int tile;
     if (!tq_take(p, tq, n, tile)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
-      return;
+      return local;
     }
-    if (tile < 0) return;
+    if (tile < 0) return local;
+    if constexpr (SMP) return local;   // SM pairs take the static order only
     const TileInfo ti = tile_info<MX>(p, tile);
     if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti, it,
-                      local++))
-      return;
+                      local))
+      return local;
+    ++local;
+  }
+}
+
+// SM pair, rank 0 after its last tile: every epilogue release of both CTAs has arrived
+// (the other CTA's arrivals target this CTA's shared memory), n = tiles issued.
+__device__ void mma_drain_pair(const Params& p, uint64_t* acc_empty, int n) {
+  for (int a = 0; a < p.nacc && a < n; ++a) {
+    const uint32_t uses = (uint32_t)((n - 1 - a) / p.nacc + 1);
+    if (!mbar_wait(&acc_empty[a], (uses - 1) & 1, globaltimer_ns() + p.timeout_ns))
+      set_error(p.status, kErrTimeout);
   }
 }
 
@@ -994,7 +1093,12 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
     auto release = [&]() {
       if (!released && half >= tile_in.nrt - 1) {
         tc_fence_before();
-        mbar_arrive(&acc_empty[acc]);
+        if (p.smpair) {   // one arrival per warp on rank 0's barrier (8 in all)
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_rank(&acc_empty[acc], 0));
+        } else {
+          mbar_arrive(&acc_empty[acc]);
+        }
         released = true;
       }
     };
@@ -1279,7 +1383,7 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
   int local = 0;
   if (!p.tile_counter && !p.clc) {
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
       if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti,
@@ -1315,8 +1419,8 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
 // compile-time constants the compiler keeps only that launch's producer, MMA and epilogue
 // code (a smaller instruction footprint, a straight-line MMA issue).
 // VAR: 0 plain, 1 split (hi/lo dW operands), 2 row-tile pairs, 3 MXFP8 forward with the
-// BF16 shared expert's tiles. Fixing the variant at compile time keeps those paths out of
-// the other kernels' code.
+// BF16 shared expert's tiles, 4 BF16 dW on SM pairs (clusters of two CTAs, M = 256 MMAs).
+// Fixing the variant at compile time keeps those paths out of the other kernels' code.
 template <bool MX, int MODE, int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps mp, const Params p_in) {
@@ -1326,10 +1430,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   p.split = VAR == 1;
   p.pair = VAR == 2;
   if (VAR != 3) p.shared_tiles = 0;   // variant 3: MXFP8 forward with BF16 shared tiles
+  p.smpair = VAR == 4;
+  p.crank = VAR == 4 ? (int)cluster_ctarank() : 0;
+  p.t0 = VAR == 4 ? (int)cluster_id_x() : (int)blockIdx.x;
+  p.tstep = VAR == 4 ? (int)cluster_count_x() : (int)gridDim.x;
   // CLC: the grid is sized to the largest tile count; a CTA past the actual count (which
   // the plan wrote to device memory) has no tile and leaves before taking any resource
   if (p.clc && (int)blockIdx.x >= num_tiles_of(p)) return;
-  constexpr int STAGES = C::STAGES;   // barrier slots; the launch uses p.stages of them
+  // barrier slots; the launch uses p.stages of them
+  constexpr int STAGES = VAR == 4 ? SMP_STAGES : C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + p.stages * p.stage_bytes;
@@ -1346,7 +1455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ClcState clc;
   clc.bar = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES + C::BAR_BYTES / 2);
   clc.answer = smem + C::DATA_BYTES + C::BAR_BYTES / 2 + 16;
-  static_assert(C::DATA_BYTES % 16 == 0 && 2 * TQ * 8 + 2 * C::STAGES * 8 + 32 + 8 + 4 * TQ <=
+  static_assert(C::DATA_BYTES % 16 == 0 && 2 * TQ * 8 + 2 * STAGES * 8 + 32 + 8 + 4 * TQ <=
                     C::BAR_BYTES / 2, "barrier area overlaps the CLC answer");
 
   const int warp = threadIdx.x >> 5;
@@ -1357,7 +1466,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 128);
+      // SM pair: one arrival per epilogue warp of both CTAs, on rank 0's barrier
+      mbar_init(&acc_empty[a], VAR == 4 ? 8 : 128);
     }
     for (int q = 0; q < TQ; ++q) {
       mbar_init(&tq.full[q], 1);
@@ -1369,31 +1479,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&mp.a[0]);
     tma_prefetch_desc(&mp.b[0]);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (VAR == 4) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    else tmem_alloc(tmem_slot, TMEM_COLS);
+  }
   tc_fence_before();
-  __syncthreads();
+  if (VAR == 4) cluster_sync_all();   // both CTAs' barriers initialised, TMEM allocated
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (threadIdx.x == 0) {
-      produce<MX>(p, mp, smem, full, empty, abort_flag, tq, clc);
+      produce<MX, VAR == 4>(p, mp, smem, full, empty, abort_flag, tq, clc);
       // leave no request in flight: its answer is written to this CTA's shared memory
       int unused;
       if (clc.in_flight && !clc_answer(p, clc, unused)) set_error(p.status, kErrTimeout);
     }
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0)
-      mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, tq);
+    if ((threadIdx.x & 31) == 0 && (VAR != 4 || p.crank == 0)) {
+      const int n = mma_issue<MX, VAR == 4>(p, smem, full, empty, acc_full, acc_empty, tmem_base,
+                                            abort_flag, tq);
+      if (VAR == 4) mma_drain_pair(p, acc_empty, n);
+    }
   } else {
     epilogue<MX>(p, mp, staging, acc_full, acc_empty, tmem_base, abort_flag, tq);
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (VAR == 4) cluster_sync_all();   // no traffic of either CTA into the other is left
+  else __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (VAR == 4) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -2114,6 +2234,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.ptile = c.ptile;
   p.num_ptiles = c.num_ptiles;
   p.max_ptiles = c.max_ptiles;
+  p.smpair = (!MX && c.smpair && !p.split && !c.tile_counter && !c.clc &&
+              (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
   const bool mixed = MX && c.s_a && (c.mode == kFwdUpGate || c.mode == kFwdDown);
   p.dgp = c.dgp;
   p.status = c.status;
@@ -2258,6 +2380,16 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
     p.shared_tiles = (int)((T + BM - 1) / BM) * p.s_n_tiles;
     max_tiles += p.shared_tiles;
   }
+  if (p.smpair && p.m_tiles_dw % 2) p.smpair = 0;   // 256-row tiles only
+  if (p.smpair) {   // six [A | half of B] stages; max_tiles counts 256-row tiles
+    static_assert(SMP_STAGES * SMP_STAGE_BYTES + OUT_STAGING <= Cfg<false>::DATA_BYTES &&
+                      SMP_STAGE_BYTES % 1024 == 0,
+                  "SM-pair stages exceed the data area");
+    p.stages = SMP_STAGES;
+    p.stage_bytes = SMP_STAGE_BYTES;
+    p.nbuf = 2;
+    max_tiles = p.groups * (p.m_tiles_dw / 2) * p.n_tiles;
+  }
   if (p.pair) {   // three [A0 | B | A1] stages, both accumulators for one tile
     static_assert(3 * PAIR_STAGE_BYTES + OUT_STAGING <= Cfg<false>::DATA_BYTES &&
                       PAIR_STAGE_BYTES % 1024 == 0 && PAIR_A1_OFF % 1024 == 0,
@@ -2276,7 +2408,7 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
 using GemmKernel = void (*)(const Maps, const Params);
 
 template <bool MX>
-GemmKernel gemm_kernel_for(int mode, int split, int pair, int mixed) {
+GemmKernel gemm_kernel_for(int mode, int split, int pair, int mixed, int smpair) {
   switch (mode) {
     case kFwdUpGate:
       if (MX && mixed) return grouped_gemm_kernel<MX, kFwdUpGate, MX ? 3 : 0>;
@@ -2291,8 +2423,10 @@ GemmKernel gemm_kernel_for(int mode, int split, int pair, int mixed) {
       return pair ? grouped_gemm_kernel<MX, kBwdDX, MX ? 0 : 2>
                   : grouped_gemm_kernel<MX, kBwdDX, 0>;
     case kBwdDWDown:
+      if (!MX && smpair) return grouped_gemm_kernel<MX, kBwdDWDown, MX ? 0 : 4>;
       return split ? grouped_gemm_kernel<MX, kBwdDWDown, !MX> : grouped_gemm_kernel<MX, kBwdDWDown, 0>;
     case kBwdDWUpGate:
+      if (!MX && smpair) return grouped_gemm_kernel<MX, kBwdDWUpGate, MX ? 0 : 4>;
       return split ? grouped_gemm_kernel<MX, kBwdDWUpGate, !MX>
                    : grouped_gemm_kernel<MX, kBwdDWUpGate, 0>;
     case kRouter: return grouped_gemm_kernel<MX, kRouter, 0>;
@@ -2303,20 +2437,57 @@ GemmKernel gemm_kernel_for(int mode, int split, int pair, int mixed) {
 template <bool MX>
 cudaError_t launch_impl(const GemmCall& c, int num_sms, cudaStream_t s) {
   using C = Cfg<MX>;
-  static bool attr_set[8][4] = {};
+  static bool attr_set[8][5] = {};
+  static int pair_clusters[8] = {};   // SM pairs: clusters of two that fit at once (0: not asked)
   if (c.mode < 0 || c.mode >= 8) return cudaErrorInvalidValue;
   Params p;
   Maps mp;
   int max_tiles = 0;
   cudaError_t e = build_call<MX>(c, p, mp, max_tiles);
   if (e != cudaSuccess) return e;
-  const GemmKernel kern = gemm_kernel_for<MX>(c.mode, p.split, p.pair, p.shared_tiles > 0);
+  const GemmKernel kern =
+      gemm_kernel_for<MX>(c.mode, p.split, p.pair, p.shared_tiles > 0, p.smpair);
   if (!kern) return cudaErrorInvalidValue;
-  const int var = p.split ? 1 : p.pair ? 2 : p.shared_tiles > 0 ? 3 : 0;
+  const int var = p.split ? 1 : p.pair ? 2 : p.shared_tiles > 0 ? 3 : p.smpair ? 4 : 0;
   if (!attr_set[c.mode][var]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[c.mode][var] = true;
+  }
+  if (p.smpair) {
+    // persistent clusters of two: as many as fit on the device at once (a GPC with an odd
+    // number of free SMs leaves one out), at most one per two SMs of the limit
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (pair_clusters[c.mode] == 0) {
+      cfg.gridDim = dim3(2, 1, 1);
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg);
+      if (e != cudaSuccess) return e;
+      pair_clusters[c.mode] = n > 0 ? n : -1;
+    }
+    if (pair_clusters[c.mode] < 0 || num_sms < 2) {   // no cluster of two: one CTA per tile
+      GemmCall c1 = c;
+      c1.smpair = false;
+      return launch_impl<MX>(c1, num_sms, s);
+    }
+    int clusters = pair_clusters[c.mode] < num_sms / 2 ? pair_clusters[c.mode] : num_sms / 2;
+    if (clusters > max_tiles) clusters = max_tiles;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, mp, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
   }
   // persistent: one CTA per SM; CLC: one CTA per tile (the hardware keeps one per SM
   // running and the running CTAs cancel the rest)

@@ -33,6 +33,9 @@ MOK_TILES_CLC = 2
 MOK_PAIRS_AUTO = 0
 MOK_PAIRS_ON = 1
 MOK_PAIRS_OFF = 2
+MOK_SMPAIRS_AUTO = 0
+MOK_SMPAIRS_ON = 1
+MOK_SMPAIRS_OFF = 2
 MOK_FWD_MEGAKERNEL = 0
 MOK_FWD_LAUNCHES = 1
 MOK_FWD_AUTO = 2
@@ -87,6 +90,7 @@ def _declare(L):
         "mok_set_output_dtype": (c_int, [c_void_p, c_int]),
         "mok_set_tile_order": (c_int, [c_void_p, c_int]),
         "mok_set_row_pairs": (c_int, [c_void_p, c_int]),
+        "mok_set_sm_pairs": (c_int, [c_void_p, c_int]),
         "mok_set_fwd_path": (c_int, [c_void_p, c_int]),
         "mok_set_comm_sms": (c_int, [c_void_p, c_int]),
         "mok_set_sm_limit": (c_int, [c_void_p, c_int]),
@@ -180,6 +184,10 @@ def mok_set_tile_order(ctx, order: int) -> None:
 
 def mok_set_row_pairs(ctx, mode: int) -> None:
     _check(lib().mok_set_row_pairs(ctx, int(mode)), "mok_set_row_pairs")
+
+
+def mok_set_sm_pairs(ctx, mode: int) -> None:
+    _check(lib().mok_set_sm_pairs(ctx, int(mode)), "mok_set_sm_pairs")
 
 
 def mok_set_output_dtype(ctx, out_dtype: int) -> None:

@@ -119,6 +119,16 @@ typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1, MOK_TILES_CLC = 2 } 
  * single row tiles. */
 typedef enum { MOK_PAIRS_AUTO = 0, MOK_PAIRS_ON = 1, MOK_PAIRS_OFF = 2 } mok_row_pairs;
 
+/* SM pairs in the BF16 weight-gradient GEMMs (dW_up|dW_gate, dW_down, routed and shared,
+ * without the hi/lo split): the two CTAs of a cluster of two share each tensor-core MMA of
+ * 256 rows (tcgen05 cta_group::2); each CTA loads its 128 rows of the transposed operand
+ * and half of the other operand's columns, so a 128 x 256 tile moves a third less through
+ * its SM's shared memory. Needs the static tile order and dW rows per expert (H, I) in whole
+ * 256-row tiles; otherwise, and when no cluster of two fits, the launch runs one CTA per
+ * tile. MOK_SMPAIRS_AUTO (default): on; MOK_SMPAIRS_ON / MOK_SMPAIRS_OFF force it.
+ * Every output tile is the same fixed-order sum either way. */
+typedef enum { MOK_SMPAIRS_AUTO = 0, MOK_SMPAIRS_ON = 1, MOK_SMPAIRS_OFF = 2 } mok_sm_pairs;
+
 typedef struct mok_ctx_s* mok_ctx_t;
 
 /* Layer dimensions. T tokens, H hidden, I expert intermediate size, E routed experts,
@@ -238,6 +248,10 @@ mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order);
 /* Select the row-tile pairing of later mok_moe_fwd / mok_moe_bwd BF16 routed GEMMs
  * (mok_row_pairs above). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_row_pairs(mok_ctx_t ctx, mok_row_pairs mode);
+
+/* Select SM pairs for later mok_moe_bwd BF16 weight-gradient GEMMs (mok_sm_pairs above).
+ * Host-only state change; MOK_ERR_INVALID_ARG for other values. */
+mok_status mok_set_sm_pairs(mok_ctx_t ctx, mok_sm_pairs mode);
 
 /* Select the type of later mok_moe_fwd / mok_moe_bwd results (mok_out_dtype above).
  * Host-only state change; MOK_ERR_INVALID_ARG for other values. */

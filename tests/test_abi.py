@@ -123,7 +123,7 @@ def test_fwd_path_option():
     mok.mok_destroy(ctx)
 
 
-def test_tile_order_row_pairs_and_output_type_options():
+def test_tile_order_row_pairs_sm_pairs_and_output_type_options():
     ctx = mok.mok_create(dims())
     for order in (mok.MOK_TILES_DYNAMIC, mok.MOK_TILES_CLC, mok.MOK_TILES_STATIC):
         mok.mok_set_tile_order(ctx, order)
@@ -131,8 +131,11 @@ def test_tile_order_row_pairs_and_output_type_options():
         mok.mok_set_output_dtype(ctx, out)
     for mode in (mok.MOK_PAIRS_ON, mok.MOK_PAIRS_OFF, mok.MOK_PAIRS_AUTO):
         mok.mok_set_row_pairs(ctx, mode)
+    for mode in (mok.MOK_SMPAIRS_ON, mok.MOK_SMPAIRS_OFF, mok.MOK_SMPAIRS_AUTO):
+        mok.mok_set_sm_pairs(ctx, mode)
     for setter, bad in ((mok.mok_set_tile_order, 3), (mok.mok_set_output_dtype, 2),
-                        (mok.mok_set_row_pairs, 3)):
+                        (mok.mok_set_row_pairs, 3), (mok.mok_set_sm_pairs, 3),
+                        (mok.mok_set_sm_pairs, -1)):
         with pytest.raises(mok.MokError) as ei:
             setter(ctx, bad)
         assert ei.value.status == mok.MOK_ERR_INVALID_ARG
@@ -140,6 +143,7 @@ def test_tile_order_row_pairs_and_output_type_options():
     assert mok.lib().mok_set_tile_order(None, 0) == mok.MOK_ERR_INVALID_ARG
     assert mok.lib().mok_set_output_dtype(None, 0) == mok.MOK_ERR_INVALID_ARG
     assert mok.lib().mok_set_row_pairs(None, 0) == mok.MOK_ERR_INVALID_ARG
+    assert mok.lib().mok_set_sm_pairs(None, 0) == mok.MOK_ERR_INVALID_ARG
 
 
 def test_wait_timeout_and_test_hook_are_host_settings():

@@ -330,6 +330,46 @@ def test_row_tile_pairs_keep_the_bits(name):
             assert torch.equal(res[f], ref[f]), (pairs, order, f)
 
 
+SM_PAIR_CASES = {
+    # dW rows in whole 256-row tiles in every weight-gradient launch (routed and shared)
+    "even": mi.MoEConfig("smp_even", T=512, H=512, I=256, E=8, k=2, shared_I=256,
+                         precision="bf16_plain"),
+    # I = 384: the routed and shared dW_down launches (rows = I) fall back to single CTAs,
+    # dW up/gate (rows = H) runs on pairs; ragged experts, some with no rows
+    "odd_I": mi.MoEConfig("smp_odd", T=300, H=512, I=384, E=16, k=2, shared_I=384,
+                          precision="bf16_plain"),
+    # fp32 results, no shared expert
+    "fp32": mi.MoEConfig("smp_f32", T=700, H=256, I=256, E=8, k=4, precision="bf16_plain",
+                         out="fp32"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SM_PAIR_CASES))
+def test_sm_pairs_keep_the_bits(name):
+    """SM pairs (clusters of two CTAs sharing the weight-gradient GEMMs' M = 256 MMAs) give
+    the single-CTA launches' weight gradients bit for bit: each output element is the same
+    fixed-order K sum. Also with an SM limit that leaves room for one pair, and with one SM
+    (no pair fits: single CTAs). The layer against the oracle is covered by the cases of
+    test_layer_matches_oracle, whose BF16-plain cases run on pairs by default."""
+    cfg = SM_PAIR_CASES[name]
+    inp = gu.gpu_inputs(cfg, seed=14)
+    fields = ("dW_up", "dW_gate", "dW_down", "dX", "dgates", "dWr") + (
+        ("dWs_up", "dWs_gate", "dWs_down") if cfg.shared_I else ())
+    ref = None
+    for pairs, limit in ((mok.MOK_SMPAIRS_OFF, 0), (mok.MOK_SMPAIRS_ON, 0),
+                         (mok.MOK_SMPAIRS_ON, 2), (mok.MOK_SMPAIRS_ON, 1)):
+        L = gu.make_layer(cfg)
+        mok.mok_set_sm_pairs(L.ctx, pairs)
+        mok.mok_set_sm_limit(L.ctx, limit)
+        res, _ = gu.run_gpu(cfg, inp, backward=True, layer=L)
+        assert res["status"] == 0, (pairs, limit)
+        if ref is None:
+            ref = res
+            continue
+        for f in fields:
+            assert torch.equal(res[f], ref[f]), (pairs, limit, f)
+
+
 @pytest.mark.parametrize("shared_I", [128, 384])
 def test_mxfp8_launches_carry_the_bf16_shared_expert(shared_I):
     """In MXFP8 the routed forward launches also run the BF16 shared expert's tiles
