@@ -132,7 +132,7 @@ struct Params {
   int lo_out;       // kBwdDH (bf16): also write the lo halves of du, dv, g*h
   int out_bf16;     // kFwdDown, kBwdDX, dW modes: round the outputs to bf16 (64-column boxes)
   int* tile_counter;// dynamic tile order: the next tile is atomicAdd(tile_counter, 1) (zero at
-                    // launch); null: the static order (tiles t0, t0 + tstep, ...)
+                    // launch); null: the static order (tile blockIdx.x, + gridDim.x, ...)
   int clc;          // cluster launch control: one CTA per tile; a CTA runs tile blockIdx.x,
                     // then the tiles of the not yet launched CTAs it cancels
   int pair;         // BF16 routed up|gate, down and dX: a tile is a pair of row tiles of one
@@ -141,12 +141,6 @@ struct Params {
   const int32_t* ptile;
   const int32_t* num_ptiles;
   int max_ptiles;
-  int smpair;       // BF16 dW modes on SM pairs: the two CTAs of a cluster share M = 256
-                    // MMAs (rank 0 issues them); a tile is 256 rows of dW, 128 per CTA, and
-                    // each CTA loads its A rows and half of the B columns
-  int crank;        // SM pairs: this CTA's rank in its cluster (set at kernel entry)
-  int t0, tstep;    // static order: first tile and stride (the CTA's, or its cluster's,
-                    // index and count; set at kernel entry)
   // MXFP8 forward launches that also run the BF16 shared expert ([C] "Outras
   // caracteristicas": MXFP8 training with the shared expert in BF16): shared_tiles BF16
   // tiles follow the routed ones (kernel variant 3), with their own maps a[2], b[2..3],
@@ -185,6 +179,11 @@ struct Params {
   // q[2], q[3], q[4] = du, dv, g*h in 32-row blocks. E4M3 [rows][I], atoms [row tile][I/128].
   uint8_t* out_q[5];
   uint8_t* out_sf[5];
+  int smpair;       // BF16 dW modes on SM pairs: the two CTAs of a cluster share M = 256
+                    // MMAs (rank 0 issues them); a tile is 256 rows of dW, 128 per CTA, and
+                    // each CTA loads its A rows and half of the B columns
+  int crank;        // SM pairs: this CTA's rank in its cluster (set at kernel entry)
+  int t0, tstep;    // SM pairs, static order: the cluster's index and the cluster count
 };
 
 struct TileInfo {
@@ -758,7 +757,8 @@ __device__ void produce(const Params& p, const Maps& mp, uint8_t* smem, uint64_t
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   if (!p.tile_counter && !p.clc) {
-    for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
+    const int t0 = SMP ? p.t0 : (int)blockIdx.x, step = SMP ? p.tstep : (int)gridDim.x;
+    for (int tile = t0; tile < ntiles; tile += step) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
       if (!produce_tile<MX, SMP>(p, mp, smem, full, empty, abort_flag, ti, it)) break;
@@ -1010,45 +1010,55 @@ __device__ bool mma_tile(const Params& p, uint8_t* smem, uint64_t* full, uint64_
   return true;
 }
 
-// Returns the number of tiles whose MMAs were issued.
-template <bool MX, bool SMP = false>
-__device__ int mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                         uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
-                         volatile int* abort_flag, const TileQueue& tq) {
+template <bool MX>
+__device__ void mma_issue(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                          uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                          volatile int* abort_flag, const TileQueue& tq) {
   const int ntiles = num_tiles_of(p);
   uint32_t it = 0;
   int local = 0;
   if (!p.tile_counter && !p.clc) {
-    for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
-      bool ok;
-      if constexpr (SMP)
-        ok = mma_tile_pair<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag,
-                               ti, it, local);
-      else
-        ok = mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
-                          it, local);
-      if (!ok) return local;
-      ++local;
+      if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                        it, local++))
+        return;
     }
-    return local;
+    return;
   }
   for (uint32_t n = 0;; ++n) {
     int tile;
     if (!tq_take(p, tq, n, tile)) {
       set_error(p.status, kErrTimeout);
       *abort_flag = 1;
-      return local;
+      return;
     }
-    if (tile < 0) return local;
-    if constexpr (SMP) return local;   // SM pairs take the static order only
+    if (tile < 0) return;
     const TileInfo ti = tile_info<MX>(p, tile);
     if (!mma_tile<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti, it,
-                      local))
+                      local++))
+      return;
+  }
+}
+
+// SM pair, rank 0: the cluster's tiles in the static order. Returns the number of tiles
+// whose MMAs were issued.
+template <bool MX>
+__device__ int mma_issue_pair(const Params& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                              uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base,
+                              volatile int* abort_flag) {
+  const int ntiles = num_tiles_of(p);
+  uint32_t it = 0;
+  int local = 0;
+  for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
+    const TileInfo ti = tile_info<MX>(p, tile);
+    if (!mma_tile_pair<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                           it, local))
       return local;
     ++local;
   }
+  return local;
 }
 
 // SM pair, rank 0 after its last tile: every epilogue release of both CTAs has arrived
@@ -1065,7 +1075,7 @@ __device__ void mma_drain_pair(const Params& p, uint64_t* acc_empty, int n) {
 // One tile (local = the CTA's tile count so far): waits for its accumulator, runs the
 // mode's epilogue and frees the accumulator. Warp-collective over the 4 epilogue warps.
 // Returns false after a timed-out wait.
-template <bool MX>
+template <bool MX, bool SMP = false>
 __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint64_t* acc_full,
                               uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag,
                               const TileInfo& tile_in, int local) {
@@ -1093,7 +1103,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
     auto release = [&]() {
       if (!released && half >= tile_in.nrt - 1) {
         tc_fence_before();
-        if (p.smpair) {   // one arrival per warp on rank 0's barrier (8 in all)
+        if constexpr (SMP) {   // one arrival per warp on rank 0's barrier (8 in all)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_rank(&acc_empty[acc], 0));
         } else {
@@ -1374,7 +1384,7 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
   return true;
 }
 
-template <bool MX>
+template <bool MX, bool SMP = false>
 __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint64_t* acc_full,
                          uint64_t* acc_empty, uint32_t tmem_base, volatile int* abort_flag,
                          const TileQueue& tq) {
@@ -1383,11 +1393,12 @@ __device__ void epilogue(const Params& p, const Maps& mp, uint8_t* staging, uint
   Stager st{staging + (warp - 2) * p.nbuf * STAGE_OUT_BYTES, 0u, lane, p.nbuf};
   int local = 0;
   if (!p.tile_counter && !p.clc) {
-    for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
+    const int t0 = SMP ? p.t0 : (int)blockIdx.x, step = SMP ? p.tstep : (int)gridDim.x;
+    for (int tile = t0; tile < ntiles; tile += step) {
       const TileInfo ti = tile_info<MX>(p, tile);
       if (ti.skip) continue;
-      if (!epilogue_tile<MX>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti,
-                             local++))
+      if (!epilogue_tile<MX, SMP>(p, mp, st, acc_full, acc_empty, tmem_base, abort_flag, ti,
+                                  local++))
         break;
     }
   } else {
@@ -1432,8 +1443,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (VAR != 3) p.shared_tiles = 0;   // variant 3: MXFP8 forward with BF16 shared tiles
   p.smpair = VAR == 4;
   p.crank = VAR == 4 ? (int)cluster_ctarank() : 0;
-  p.t0 = VAR == 4 ? (int)cluster_id_x() : (int)blockIdx.x;
-  p.tstep = VAR == 4 ? (int)cluster_count_x() : (int)gridDim.x;
+  p.t0 = VAR == 4 ? (int)cluster_id_x() : 0;
+  p.tstep = VAR == 4 ? (int)cluster_count_x() : 1;
   // CLC: the grid is sized to the largest tile count; a CTA past the actual count (which
   // the plan wrote to device memory) has no tile and leaves before taking any resource
   if (p.clc && (int)blockIdx.x >= num_tiles_of(p)) return;
@@ -1497,18 +1508,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (clc.in_flight && !clc_answer(p, clc, unused)) set_error(p.status, kErrTimeout);
     }
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0 && (VAR != 4 || p.crank == 0)) {
-      const int n = mma_issue<MX, VAR == 4>(p, smem, full, empty, acc_full, acc_empty, tmem_base,
-                                            abort_flag, tq);
-      if (VAR == 4) mma_drain_pair(p, acc_empty, n);
+    if constexpr (VAR == 4) {
+      if ((threadIdx.x & 31) == 0 && p.crank == 0) {
+        const int n = mma_issue_pair<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base,
+                                         abort_flag);
+        mma_drain_pair(p, acc_empty, n);
+      }
+    } else if ((threadIdx.x & 31) == 0) {
+      mma_issue<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, tq);
     }
   } else {
-    epilogue<MX>(p, mp, staging, acc_full, acc_empty, tmem_base, abort_flag, tq);
+    epilogue<MX, VAR == 4>(p, mp, staging, acc_full, acc_empty, tmem_base, abort_flag, tq);
   }
   tc_fence_before();
-  __syncwarp();
-  if (VAR == 4) cluster_sync_all();   // no traffic of either CTA into the other is left
-  else __syncthreads();
+  if constexpr (VAR == 4) {
+    __syncwarp();
+    cluster_sync_all();   // no traffic of either CTA into the other is left
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
