@@ -77,8 +77,8 @@ constexpr int kCombineWarps = 4;   // warps per token: more loads in flight per 
 template <bool BF16>
 struct RowVec {
   static constexpr int N = BF16 ? 8 : 4;   // values per 16-byte vector
-  __device__ static void load(const uint4* p, float* f) {
-    const uint4 w = __ldg(p);
+  __device__ static void load(const uint4* p, float* f) { unpack(__ldg(p), f); }
+  __device__ static void unpack(const uint4 w, float* f) {
     if (BF16) {
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
@@ -142,6 +142,13 @@ __global__ void __launch_bounds__(256) combine_kernel(
     dls[j] = __shfl_sync(0xffffffffu, my_dl, j);
   }
   for (int i = part * 32 + lane; i < nvec; i += 32 * kCombineWarps) {
+    // every load of this vector first (the k rows and the added row are independent),
+    // then the sums in slot order
+    uint4 w[kMaxK], wa = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) w[j] = __ldg(O + (size_t)rows[j] * nvec + i);
+    if (add) wa = __ldg(add + (size_t)t * nvec + i);
     float acc[N];
 #pragma unroll
     for (int z = 0; z < N; ++z) acc[z] = 0.f;
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     for (int j = 0; j < kMaxK; ++j) {
       if (j < k) {
         float f[N];
-        V::load(O + (size_t)rows[j] * nvec + i, f);
+        V::unpack(w[j], f);
         if (weighted) {
 #pragma unroll
           for (int z = 0; z < N; ++z) acc[z] = fmaf(g[j], f[z], acc[z]);
@@ -161,22 +168,34 @@ __global__ void __launch_bounds__(256) combine_kernel(
     }
     if (add) {
       float f[N];
-      V::load(add + (size_t)t * nvec + i, f);
+      V::unpack(wa, f);
 #pragma unroll
       for (int z = 0; z < N; ++z) acc[z] += f[z];
     }
-    if (dl) {
+    if (dl) {   // the router weights' columns, four slots' loads at a time, in slot order
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          const float4* w = reinterpret_cast<const float4*>(WrT + (size_t)ex[j] * H + (size_t)i * N);
+      for (int j0 = 0; j0 < kMaxK; j0 += 4) {
+        float4 wv[4][N / 4];
 #pragma unroll
-          for (int q = 0; q < N / 4; ++q) {
-            const float4 wv = __ldg(w + q);
-            acc[4 * q] = fmaf(dls[j], wv.x, acc[4 * q]);
-            acc[4 * q + 1] = fmaf(dls[j], wv.y, acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(dls[j], wv.z, acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(dls[j], wv.w, acc[4 * q + 3]);
+        for (int jj = 0; jj < 4; ++jj) {
+          if (j0 + jj < k) {
+            const float4* w =
+                reinterpret_cast<const float4*>(WrT + (size_t)ex[j0 + jj] * H + (size_t)i * N);
+#pragma unroll
+            for (int q = 0; q < N / 4; ++q) wv[jj][q] = __ldg(w + q);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = j0 + jj;
+          if (j < k) {
+#pragma unroll
+            for (int q = 0; q < N / 4; ++q) {
+              acc[4 * q] = fmaf(dls[j], wv[jj][q].x, acc[4 * q]);
+              acc[4 * q + 1] = fmaf(dls[j], wv[jj][q].y, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(dls[j], wv[jj][q].z, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(dls[j], wv[jj][q].w, acc[4 * q + 3]);
+            }
           }
         }
       }
