@@ -2305,13 +2305,15 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       break;
     case kRouter:
       if (MX || !c.dense) return cudaErrorNotSupported;
-      // 256 columns per tile above 128 experts: one launch round of long-K tiles (K = 3H)
-      // instead of two, and half the x re-reads; the columns past E load as zeros
-      p.BN = c.n_out > 128 ? 256 : 128;
+      // the fewest column tiles of at most 256 columns (one launch round of long-K tiles,
+      // K = 3H, and the fewest x re-reads), each as narrow as they allow in steps of 64
+      // (E = 384: two of 192, not 256 + 128 of which half past E); columns past E load as
+      // zeros
+      p.n_tiles = (c.n_out + 255) / 256;
+      p.BN = ((c.n_out + p.n_tiles - 1) / p.n_tiles + 63) / 64 * 64;
       p.n_out = c.n_out;
       p.bias = c.bias;
       p.logits = static_cast<float*>(c.out[0]);
-      p.n_tiles = (c.n_out + p.BN - 1) / p.BN;
       p.kiters = 3 * (c.H / BK);
       ok = c.ld_b % 64 == 0 && c.ld_b >= c.n_out &&
            make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
