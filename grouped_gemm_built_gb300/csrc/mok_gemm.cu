@@ -1852,8 +1852,26 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
       const uint4* O = reinterpret_cast<const uint4*>(q.O);
       const uint4* Os = reinterpret_cast<const uint4*>(q.Os);
       uint4* y = reinterpret_cast<uint4*>(q.y);
+      // every load of a pass first (k rows x U vectors, and the shared rows), then the
+      // sums in slot order: with 6 warps per SM the loads in flight come from each lane
       constexpr int U = 2;
       for (int i0 = lane; i0 < nvec; i0 += 32 * U) {
+        uint4 w[kMaxK][U], ws[U];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          if (j < q.k) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int i = i0 + 32 * u;
+              w[j][u] = i < nvec ? __ldcg(O + (size_t)rows[j] * nvec + i) : make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + 32 * u;
+          ws[u] = (Os && i < nvec) ? __ldcg(Os + (size_t)t * nvec + i) : make_uint4(0, 0, 0, 0);
+        }
         float acc[U][8];
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -1862,16 +1880,10 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
           if (j < q.k) {
-            uint4 w[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int i = i0 + 32 * u;
-              w[u] = i < nvec ? __ldcg(O + (size_t)rows[j] * nvec + i) : make_uint4(0, 0, 0, 0);
-            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
               float f[8];
-              bf16x8_to_f32(w[u], f);
+              bf16x8_to_f32(w[j][u], f);
 #pragma unroll
               for (int z = 0; z < 8; ++z) acc[u][z] = fmaf(g[j], f[z], acc[u][z]);
             }
@@ -1883,7 +1895,7 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
           if (i >= nvec) continue;
           if (Os) {
             float f[8];
-            bf16x8_to_f32(__ldcg(Os + (size_t)t * nvec + i), f);
+            bf16x8_to_f32(ws[u], f);
 #pragma unroll
             for (int z = 0; z < 8; ++z) acc[u][z] += f[z];
           }
@@ -1899,24 +1911,30 @@ __device__ void mega_combine(const MegaParams& q, int m, int wi, int nw) {
     // 4 vectors per lane per pass: with 6 warps per SM, loads in flight come from width
     constexpr int U = 4;
     for (int i0 = lane; i0 < nvec; i0 += 32 * U) {
+      float4 f[kMaxK][U];   // every load of the pass first, then the sums in slot order
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < q.k) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + 32 * u;
+            f[j][u] = i < nvec ? __ldcg(O + (size_t)rows[j] * nvec + i)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
       float4 acc[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < q.k) {
-          float4 f[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const int i = i0 + 32 * u;
-            f[u] = i < nvec ? __ldcg(O + (size_t)rows[j] * nvec + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            acc[u].x = fmaf(g[j], f[u].x, acc[u].x);
-            acc[u].y = fmaf(g[j], f[u].y, acc[u].y);
-            acc[u].z = fmaf(g[j], f[u].z, acc[u].z);
-            acc[u].w = fmaf(g[j], f[u].w, acc[u].w);
+            acc[u].x = fmaf(g[j], f[j][u].x, acc[u].x);
+            acc[u].y = fmaf(g[j], f[j][u].y, acc[u].y);
+            acc[u].z = fmaf(g[j], f[j][u].z, acc[u].z);
+            acc[u].w = fmaf(g[j], f[j][u].w, acc[u].w);
           }
         }
       }
