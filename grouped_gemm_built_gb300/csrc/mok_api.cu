@@ -887,6 +887,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       c.out[5] = W(L.hg_lo);
     }
     c.dgp = dgp;
+    c.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
     MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
     c = routed_call(d, sched, a, kBwdDX, use_pairs(ctx));
@@ -961,6 +962,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       cs.out[3] = W(L.dvs_lo);
       cs.out[5] = W(L.hsg_lo);
     }
+    cs.smpair = ctx->sm_pairs == MOK_SMPAIRS_ON;   // shared expert: on request only
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kBwdDX);
     cs.a[0] = W(L.dus);
@@ -1034,7 +1036,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     cs.out[0] = g->dWs_up;
     cs.out[1] = g->dWs_gate;
     cs.out_bf16 = ob;
-    cs.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
+    cs.smpair = ctx->sm_pairs == MOK_SMPAIRS_ON;   // shared expert: on request only
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
     cs = dense_call(d, a, kBwdDWDown);
     cs.a[0] = W(L.hsg);
@@ -1045,7 +1047,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
     }
     cs.out[0] = g->dWs_down;
     cs.out_bf16 = ob;
-    cs.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
+    cs.smpair = ctx->sm_pairs == MOK_SMPAIRS_ON;   // shared expert: on request only
     MOK_LAUNCH(gemm_name(cs), launch_gemm(timed(cs, ctx), launch_sms(ctx), s));
   }
   if (d.router)

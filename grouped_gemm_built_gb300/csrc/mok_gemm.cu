@@ -197,6 +197,8 @@ struct TileInfo {
   int skip;     // 1: no tile here (the unmatched half of the last row-tile pair)
   int nrt;      // row tiles in this tile: 1, or 2 (a row-tile pair: rows row0 .. row0+255)
   int bf;       // 1: a BF16 shared-expert tile of an MXFP8 forward launch (rows of x / hs)
+  int norows;   // SM pairs, row-space modes: this CTA's half of the pair tile has no rows
+                // (the pair's odd last row tile): it loads and takes part, writes nothing
 };
 
 __host__ __device__ __forceinline__ bool is_dw(int mode) { return mode == kBwdDWDown || mode == kBwdDWUpGate; }
@@ -211,6 +213,10 @@ __device__ __forceinline__ int routed_mtiles(const Params& p) {
 // CTAs take them in the same round, so the second read of the slice is an L2 hit.
 __device__ __forceinline__ int num_tiles_of(const Params& p) {
   if (is_dw(p.mode)) return p.groups * (p.smpair ? p.m_tiles_dw / 2 : p.m_tiles_dw) * p.n_tiles;
+  if (p.smpair) {   // row-space modes on SM pairs: pairs of row tiles
+    if (p.dense) return (((p.M_rows + BM - 1) / BM + 1) / 2) * p.n_tiles;
+    return min(max(*p.num_ptiles, 0), p.max_ptiles) * p.n_tiles;
+  }
   if (p.pair) return min(max(*p.num_ptiles, 0), p.max_ptiles) * p.n_tiles;
   if (p.dense) return ((p.M_rows + BM - 1) / BM) * p.n_tiles;
   return ((routed_mtiles(p) + 1) / 2) * 2 * p.n_tiles + p.shared_tiles;
@@ -224,7 +230,34 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tile) {
   ti.skip = 0;
   ti.nrt = 1;
   ti.bf = 0;
+  ti.norows = 0;
   ti.klast = BK / MMA_K;
+  if (p.smpair && !is_dw(p.mode)) {
+    // SM pair over a pair of row tiles of one expert (routed: the plan's list; dense:
+    // consecutive): rank 0 takes the first, rank 1 the second, or no rows when there is none
+    const int q = tile / p.n_tiles;
+    const int nt = tile - q * p.n_tiles;
+    int mt, two;
+    if (p.dense) {
+      mt = 2 * q;
+      two = mt + 1 < (p.M_rows + BM - 1) / BM;
+      ti.e = 0;
+    } else {
+      const int pt = p.ptile[q];
+      mt = pt >> 1;
+      ti.skip = mt >= routed_mtiles(p);   // both CTAs see the same list entry
+      two = (pt & 1) && mt + 1 < routed_mtiles(p);
+      ti.e = ti.skip ? 0 : min(max(p.tile_expert[mt], 0), p.groups - 1);
+      if (ti.skip) mt = 0;
+    }
+    ti.norows = p.crank == 1 && !two;
+    ti.row0 = (mt + p.crank) * BM;
+    ti.arow0 = ti.row0;
+    ti.n0 = nt * p.BN;
+    ti.kiters = p.kiters;
+    ti.krow0 = 0;
+    return ti;
+  }
   if (p.pair) {   // tile = pair q of column block nt; the pair's tiles share the expert
     const int q = tile / p.n_tiles;
     const int nt = tile - q * p.n_tiles;
@@ -569,11 +602,17 @@ __device__ bool produce_tile(const Params& p, const Maps& mp, uint8_t* smem, uin
       uint64_t* bar = &full[stage];
       if constexpr (!MX && SMP) {
         // SM pair: this CTA's 128 rows of A and its half of B's columns (dW up|gate: rank
-        // 0 du, rank 1 dv, columns n0..n0+127; dW down: columns n0 + rank * BN/2 ..), the
-        // copies of both CTAs counted on rank 0's barrier, which rank 0 arms for both
+        // 0 du, rank 1 dv, columns n0..n0+127; dW down: columns n0 + rank * BN/2 ..; dH:
+        // rows n0 + rank * BN/2 .. of W_down), the copies of both CTAs counted on rank 0's
+        // barrier, which rank 0 arms for both
         const uint32_t lbar = mapa_rank(bar, 0);
         const int nb = p.BN / 2;
         if (p.crank == 0) mbar_arrive_expect_tx(bar, 2 * (A_BYTES + nb * 128));
+        if (p.mode == kBwdDH) {   // A: dYg rows (K-major); B: nb rows of W_down (K-major)
+          tma_load_2d_pair(sa, &mp.a[0], lbar, kb * BK, ti.arow0);
+          tma_load_2d_pair(sb, &mp.b[0], lbar, kb * BK, ti.e * p.I + ti.n0 + p.crank * nb);
+          continue;
+        }
         const int kr = ti.krow0 + kb * BK;
         for (int c = 0; c < BM / C::MN_CHUNK; ++c)
           tma_load_2d_pair(sa + c * CH, &mp.a[0], lbar, ti.row0 + c * C::MN_CHUNK, kr);
@@ -824,7 +863,9 @@ __device__ bool mma_tile_pair(const Params& p, uint8_t* smem, uint64_t* full, ui
                               int local) {
   using C = Cfg<MX>;
   const int STAGES = p.stages;
-  const uint32_t idp = idesc_bf16(2 * BM, p.BN, true, true);
+  // the weight gradients' operands are MN-major, dH's K-major
+  const bool mn = is_dw(p.mode);
+  const uint32_t idp = idesc_bf16(2 * BM, p.BN, mn, mn);
   const int acc = local % p.nacc;
   const uint32_t use = local / p.nacc;
   if (use > 0 &&
@@ -849,9 +890,11 @@ __device__ bool mma_tile_pair(const Params& p, uint8_t* smem, uint64_t* full, ui
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       if (kk >= nk) break;
-      umma_bf16_pair(d_tmem, umma_desc_sw128(sa + kk * C::MN_KSTEP, C::MN_LBO, 1024),
-                     umma_desc_sw128(sb + kk * C::MN_KSTEP, C::MN_LBO, 1024), idp,
-                     (kb > 0 || kk > 0) ? 1u : 0u);
+      const uint64_t ad = mn ? umma_desc_sw128(sa + kk * C::MN_KSTEP, C::MN_LBO, 1024)
+                             : umma_desc_sw128(sa + kk * 32, 16, 1024);
+      const uint64_t bd = mn ? umma_desc_sw128(sb + kk * C::MN_KSTEP, C::MN_LBO, 1024)
+                             : umma_desc_sw128(sb + kk * 32, 16, 1024);
+      umma_bf16_pair(d_tmem, ad, bd, idp, (kb > 0 || kk > 0) ? 1u : 0u);
     }
     umma_commit_pair(&empty[stage]);
   }
@@ -1225,6 +1268,10 @@ __device__ bool epilogue_tile(const Params& p, const Maps& mp, Stager& st, uint6
         break;
       }
       case kBwdDH: {
+        if (ti.norows) {   // SM pair without a second row tile: nothing to read or write
+          release();
+          break;
+        }
         float g = 1.f;
         bool real = true;   // a row of the expert, not segment padding
         if (!p.dense) {
@@ -1640,6 +1687,7 @@ __device__ __forceinline__ TileInfo mega_tile(const MegaParams& q, int m, int ph
   ti.skip = r >= mega_mtiles(q, m);
   ti.nrt = 1;
   ti.bf = 0;
+  ti.norows = 0;
   return ti;
 }
 
@@ -2271,7 +2319,8 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
   p.num_ptiles = c.num_ptiles;
   p.max_ptiles = c.max_ptiles;
   p.smpair = (!MX && c.smpair && !p.split && !c.tile_counter && !c.clc &&
-              (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate)) ? 1 : 0;
+              (c.mode == kBwdDWDown || c.mode == kBwdDWUpGate ||
+               (c.mode == kBwdDH && (c.dense || (c.ptile && c.num_ptiles))))) ? 1 : 0;
   const bool mixed = MX && c.s_a && (c.mode == kFwdUpGate || c.mode == kFwdDown);
   p.dgp = c.dgp;
   p.status = c.status;
@@ -2351,8 +2400,9 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
       p.kcs_a = c.H / 128;
       p.kcs_b = c.H / 128;
       p.ncs_b = c.I / 128;
+      // SM pairs: each CTA copies half of the weight tile's rows
       ok = make_map(&mp.a[0], c.a[0], c.H, rows, BM, eb) &&
-           make_map(&mp.b[0], c.b[0], c.H, G * c.I, p.BN, eb);
+           make_map(&mp.b[0], c.b[0], c.H, G * c.I, p.smpair ? p.BN / 2 : p.BN, eb);
       for (int i = 0; i < 6 && ok && !MX; ++i)
         if (i % 2 == 0 || p.lo_out) ok = make_out_map(&mp.o[i], c.out[i], c.I, rows, 2);
       max_tiles = mt_rows * p.n_tiles;
@@ -2418,15 +2468,18 @@ cudaError_t build_call(const GemmCall& c, Params& p, Maps& mp, int& max_tiles) {
     p.shared_tiles = (int)((T + BM - 1) / BM) * p.s_n_tiles;
     max_tiles += p.shared_tiles;
   }
-  if (p.smpair && p.m_tiles_dw % 2) p.smpair = 0;   // 256-row tiles only
-  if (p.smpair) {   // six [A | half of B] stages; max_tiles counts 256-row tiles
+  if (p.smpair && is_dw(c.mode) && p.m_tiles_dw % 2) p.smpair = 0;   // 256-row tiles only
+  if (p.smpair) {   // six [A | half of B] stages; max_tiles counts pair tiles
     static_assert(SMP_STAGES * SMP_STAGE_BYTES + OUT_STAGING <= Cfg<false>::DATA_BYTES &&
                       SMP_STAGE_BYTES % 1024 == 0,
                   "SM-pair stages exceed the data area");
     p.stages = SMP_STAGES;
     p.stage_bytes = SMP_STAGE_BYTES;
     p.nbuf = 2;
-    max_tiles = p.groups * (p.m_tiles_dw / 2) * p.n_tiles;
+    if (is_dw(c.mode))
+      max_tiles = p.groups * (p.m_tiles_dw / 2) * p.n_tiles;
+    else
+      max_tiles = (p.dense ? (mt_rows + 1) / 2 : (p.max_ptiles > 0 ? p.max_ptiles : 0)) * p.n_tiles;
   }
   if (p.pair) {   // three [A0 | B | A1] stages, both accumulators for one tile
     static_assert(3 * PAIR_STAGE_BYTES + OUT_STAGING <= Cfg<false>::DATA_BYTES &&
@@ -2456,7 +2509,9 @@ GemmKernel gemm_kernel_for(int mode, int split, int pair, int mixed, int smpair)
       if (MX && mixed) return grouped_gemm_kernel<MX, kFwdDown, MX ? 3 : 0>;
       return pair ? grouped_gemm_kernel<MX, kFwdDown, MX ? 0 : 2>
                   : grouped_gemm_kernel<MX, kFwdDown, 0>;
-    case kBwdDH: return grouped_gemm_kernel<MX, kBwdDH, 0>;
+    case kBwdDH:
+      if (!MX && smpair) return grouped_gemm_kernel<MX, kBwdDH, MX ? 0 : 4>;
+      return grouped_gemm_kernel<MX, kBwdDH, 0>;
     case kBwdDX:
       return pair ? grouped_gemm_kernel<MX, kBwdDX, MX ? 0 : 2>
                   : grouped_gemm_kernel<MX, kBwdDX, 0>;

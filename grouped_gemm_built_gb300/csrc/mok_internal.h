@@ -241,9 +241,10 @@ struct GemmCall {
   // against one weight tile, two accumulators side by side (AuxLayout::ptile)
   bool pair;
   const int32_t* ptile; const int32_t* num_ptiles; int max_ptiles;
-  // BF16 dW modes without hi/lo split, static tile order: run on SM pairs (clusters of two
-  // CTAs sharing M = 256 MMAs) when the dW rows per expert are a whole number of 256-row
-  // tiles; otherwise the launch runs one CTA per tile as usual
+  // BF16 dW modes without hi/lo split and dH, static tile order: run on SM pairs
+  // (clusters of two CTAs sharing M = 256 MMAs; dW when the dW rows per expert are a whole
+  // number of 256-row tiles, dH over the plan's pairs of row tiles); otherwise the launch
+  // runs one CTA per tile as usual
   bool smpair;
   // MXFP8 kFwdUpGate / kFwdDown: the BF16 shared expert's tiles in the same launch
   // (s_a: x, or the shared h; s_b: Ws_up, Ws_gate, or Ws_down; s_out: hs, Us, Vs, or the

@@ -119,14 +119,16 @@ typedef enum { MOK_TILES_STATIC = 0, MOK_TILES_DYNAMIC = 1, MOK_TILES_CLC = 2 } 
  * single row tiles. */
 typedef enum { MOK_PAIRS_AUTO = 0, MOK_PAIRS_ON = 1, MOK_PAIRS_OFF = 2 } mok_row_pairs;
 
-/* SM pairs in the BF16 weight-gradient GEMMs (dW_up|dW_gate, dW_down, routed and shared,
- * without the hi/lo split): the two CTAs of a cluster of two share each tensor-core MMA of
- * 256 rows (tcgen05 cta_group::2); each CTA loads its 128 rows of the transposed operand
- * and half of the other operand's columns, so a 128 x 256 tile moves a third less through
- * its SM's shared memory. Needs the static tile order and dW rows per expert (H, I) in whole
- * 256-row tiles; otherwise, and when no cluster of two fits, the launch runs one CTA per
- * tile. MOK_SMPAIRS_AUTO (default): on; MOK_SMPAIRS_ON / MOK_SMPAIRS_OFF force it.
- * Every output tile is the same fixed-order sum either way. */
+/* SM pairs in the BF16 weight-gradient GEMMs (dW_up|dW_gate, dW_down, without the hi/lo
+ * split) and the BF16 dH GEMM: the two CTAs of a cluster of two share each tensor-core MMA
+ * of 256 rows (tcgen05 cta_group::2). Each CTA loads its 128 rows of A (a row tile of dY for
+ * dH; 128 rows of the transposed operand for dW) and half of the other operand's 256
+ * columns, so a tile moves a third less through its SM's shared memory; dH's two row tiles
+ * of an expert share one weight tile. Needs the static tile order; the dW launches need dW
+ * rows per expert (H, I) in whole 256-row tiles. Otherwise, and when no cluster of two
+ * fits, the launch runs one CTA per tile. MOK_SMPAIRS_AUTO (default): the routed experts'
+ * launches; MOK_SMPAIRS_ON: the shared expert's as well; MOK_SMPAIRS_OFF: none.
+ * Every output element is the same fixed-order sum either way. */
 typedef enum { MOK_SMPAIRS_AUTO = 0, MOK_SMPAIRS_ON = 1, MOK_SMPAIRS_OFF = 2 } mok_sm_pairs;
 
 typedef struct mok_ctx_s* mok_ctx_t;
@@ -249,7 +251,7 @@ mok_status mok_set_tile_order(mok_ctx_t ctx, mok_tile_order order);
  * (mok_row_pairs above). Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_row_pairs(mok_ctx_t ctx, mok_row_pairs mode);
 
-/* Select SM pairs for later mok_moe_bwd BF16 weight-gradient GEMMs (mok_sm_pairs above).
+/* Select SM pairs for later mok_moe_bwd BF16 dH and weight-gradient GEMMs (mok_sm_pairs above).
  * Host-only state change; MOK_ERR_INVALID_ARG for other values. */
 mok_status mok_set_sm_pairs(mok_ctx_t ctx, mok_sm_pairs mode);
 

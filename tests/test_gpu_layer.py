@@ -346,18 +346,20 @@ SM_PAIR_CASES = {
 
 @pytest.mark.parametrize("name", sorted(SM_PAIR_CASES))
 def test_sm_pairs_keep_the_bits(name):
-    """SM pairs (clusters of two CTAs sharing the weight-gradient GEMMs' M = 256 MMAs) give
-    the single-CTA launches' weight gradients bit for bit: each output element is the same
-    fixed-order K sum. Also with an SM limit that leaves room for one pair, and with one SM
-    (no pair fits: single CTAs). The layer against the oracle is covered by the cases of
-    test_layer_matches_oracle, whose BF16-plain cases run on pairs by default."""
+    """SM pairs (clusters of two CTAs sharing the M = 256 MMAs of the dH and weight-gradient
+    GEMMs) give the single-CTA launches' results bit for bit: each output element is the
+    same fixed-order K sum. Every eligible launch on pairs (ON), the routed ones only
+    (AUTO), with an SM limit that leaves room for one pair, and with one SM (no pair fits:
+    single CTAs). The layer against the oracle is covered by the cases of
+    test_layer_matches_oracle, whose BF16 cases run on pairs by default."""
     cfg = SM_PAIR_CASES[name]
     inp = gu.gpu_inputs(cfg, seed=14)
     fields = ("dW_up", "dW_gate", "dW_down", "dX", "dgates", "dWr") + (
         ("dWs_up", "dWs_gate", "dWs_down") if cfg.shared_I else ())
     ref = None
     for pairs, limit in ((mok.MOK_SMPAIRS_OFF, 0), (mok.MOK_SMPAIRS_ON, 0),
-                         (mok.MOK_SMPAIRS_ON, 2), (mok.MOK_SMPAIRS_ON, 1)):
+                         (mok.MOK_SMPAIRS_AUTO, 0), (mok.MOK_SMPAIRS_ON, 2),
+                         (mok.MOK_SMPAIRS_ON, 1)):
         L = gu.make_layer(cfg)
         mok.mok_set_sm_pairs(L.ctx, pairs)
         mok.mok_set_sm_limit(L.ctx, limit)
