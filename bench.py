@@ -86,7 +86,7 @@ def peaks():
 NCU_TRAFFIC = {
     # the 24-expert profiling case (E=24, T=512) scaled by 16: 16 x (0.105 + 1.348) GB
     ("kimi_8192_plain", "gemm_bwd_dw_upgate", "bf16"): {"bytes": 23.25e9,
-                                                       "rev": "c2a06a03bcec2651"},
+                                                       "rev": "a1da9bf55d025dcb"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
