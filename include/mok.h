@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
   MOK_OK = 0,
   MOK_ERR_INVALID_ARG = -1, /* bad pointer, size or combination of arguments        */
-  MOK_ERR_UNSUPPORTED = -2, /* valid request this build does not support            */
+  MOK_ERR_UNSUPPORTED = -2, /* valid request the library does not support           */
   MOK_ERR_WORKSPACE = -3,   /* workspace/aux/saved buffer missing or misaligned     */
   MOK_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed                    */
   MOK_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired                   */
