@@ -78,11 +78,26 @@ static int launch_sms(mok_ctx_t ctx) {
 // compute-bound and keep their two accumulators for overlapping the epilogue. The dH launch
 // keeps single row tiles: a pair holds both accumulators through its long SwiGLU'
 // epilogue, which measured 10% slower at the Kimi shape.
+// experts that average more than one and at most two 128-row tiles of rows
+static bool two_row_tiles(const mok::Dims& d) {
+  const long long R = (long long)d.R, E = d.E;
+  return R > 128 * E && R <= 256 * E;
+}
 static bool use_pairs(mok_ctx_t ctx) {
   if (ctx->row_pairs == MOK_PAIRS_ON) return true;
   if (ctx->row_pairs == MOK_PAIRS_OFF) return false;
-  const long long R = (long long)ctx->d.R, E = ctx->d.E;
-  return R > 128 * E && R <= 256 * E;
+  return two_row_tiles(ctx->d);
+}
+
+// SM pairs for the routed dH launch: a cluster takes a pair of an expert's row tiles, and
+// an expert's odd last row tile leaves one of its two CTAs without rows. Automatic, like
+// the row-tile pairs, where that is rare: at 384 rows per expert (three row tiles) the
+// idle halves made dH 16% slower than single CTAs (0.199 to 0.231 ms), at about 171 rows
+// it is 6% faster.
+static bool use_dh_sm_pairs(mok_ctx_t ctx) {
+  if (ctx->sm_pairs == MOK_SMPAIRS_ON) return true;
+  if (ctx->sm_pairs == MOK_SMPAIRS_OFF) return false;
+  return two_row_tiles(ctx->d);
 }
 
 // the context's bound on device waits and its tile order, applied to one GEMM call
@@ -887,7 +902,7 @@ mok_status mok_moe_bwd(mok_ctx_t ctx, const mok_sched* sched, const void* x, con
       c.out[5] = W(L.hg_lo);
     }
     c.dgp = dgp;
-    c.smpair = ctx->sm_pairs != MOK_SMPAIRS_OFF;
+    c.smpair = use_dh_sm_pairs(ctx);
     MOK_LAUNCH(gemm_name(c), launch_gemm(timed(c, ctx), launch_sms(ctx), s));
     // dXg = du W_up^T + dv W_gate^T (bf16 du, dv)
     c = routed_call(d, sched, a, kBwdDX, use_pairs(ctx));

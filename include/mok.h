@@ -127,7 +127,9 @@ typedef enum { MOK_PAIRS_AUTO = 0, MOK_PAIRS_ON = 1, MOK_PAIRS_OFF = 2 } mok_row
  * of an expert share one weight tile. Needs the static tile order; the dW launches need dW
  * rows per expert (H, I) in whole 256-row tiles. Otherwise, and when no cluster of two
  * fits, the launch runs one CTA per tile. MOK_SMPAIRS_AUTO (default): the routed experts'
- * launches; MOK_SMPAIRS_ON: the shared expert's as well; MOK_SMPAIRS_OFF: none.
+ * weight-gradient launches, and their dH launch when the experts average more than 128
+ * and at most 256 rows (an expert's odd last row tile leaves half a cluster idle);
+ * MOK_SMPAIRS_ON: every eligible launch, the shared expert's as well; MOK_SMPAIRS_OFF: none.
  * Every output element is the same fixed-order sum either way. */
 typedef enum { MOK_SMPAIRS_AUTO = 0, MOK_SMPAIRS_ON = 1, MOK_SMPAIRS_OFF = 2 } mok_sm_pairs;
 
