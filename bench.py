@@ -84,9 +84,9 @@ def peaks():
 # and workload states. A figure is valid only for the GEMM source revision it was taken on
 # (gemm_source_rev) and the result type it was taken with.
 NCU_TRAFFIC = {
-    # the 24-expert profiling case (E=24, T=512) scaled by 16: 16 x (0.105 + 1.348) GB
+    # the 24-expert profiling case (E=24, T=512) scaled by 16: 16 x (0.106 + 1.347) GB
     ("kimi_8192_plain", "gemm_bwd_dw_upgate", "bf16"): {"bytes": 23.25e9,
-                                                       "rev": "a1da9bf55d025dcb"},
+                                                       "rev": "8bd3d8902a958a87"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",

@@ -1096,6 +1096,7 @@ __device__ int mma_issue_pair(const Params& p, uint8_t* smem, uint64_t* full, ui
   int local = 0;
   for (int tile = p.t0; tile < ntiles; tile += p.tstep) {
     const TileInfo ti = tile_info<MX>(p, tile);
+    if (ti.skip) continue;   // as the producer and the epilogue
     if (!mma_tile_pair<MX>(p, smem, full, empty, acc_full, acc_empty, tmem_base, abort_flag, ti,
                            it, local))
       return local;
