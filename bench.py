@@ -86,7 +86,7 @@ def peaks():
 NCU_TRAFFIC = {
     # the 24-expert profiling case (E=24, T=512) scaled by 16: 16 x (0.106 + 1.347) GB
     ("kimi_8192_plain", "gemm_bwd_dw_upgate", "bf16"): {"bytes": 23.25e9,
-                                                       "rev": "8bd3d8902a958a87"},
+                                                       "rev": "3a358dec299f5f3f"},
 }
 GEMM_SOURCES = ("grouped_gemm_built_gb300/csrc/mok_gemm.cu",
                 "grouped_gemm_built_gb300/csrc/mok_ptx.cuh",
